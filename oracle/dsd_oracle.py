@@ -1,0 +1,443 @@
+"""Plain fp64 CPU oracle for the DSpark draft/verify hot path.
+
+TEST INFRASTRUCTURE ONLY.  This module is imported by the test-suite, by
+``__graft_entry__.smoke()`` and by ``bench.py``'s CPU-baseline / reference leg.
+The product path (the CUDA library under ``semi_autoregressive_draft_gb300``
+and its binding) never imports, calls or links it, and there is no CPU
+fallback anywhere in the product.
+
+Everything here is written for a reader checking it against the pages by eye:
+numpy in float64, loops over requests and positions, one library primitive per
+step at most (a matrix-vector product, a sort).  Sources, by page title and
+section:
+
+  [TRAIN]  "Qwen3.8-Flash-Next DSpark 训练实验"
+           -- 评估口径 / 离线指标 (overlap a_i, tau_prob, accept_rate@i)
+           -- Baseline 架构 / Markov 顺序修正 (m_i, b_i, l_i = l_i^0 + b_i, greedy)
+  [NOTES]  "DSpark notes" (h.sjds.net/a/571373)
+           -- 2.2 Sequential Stage; 2.3 串行头的两种形态 (Markov head = low-rank
+              factorisation of a V x V transition matrix)
+  [READ]   "DSpark 论文精读：置信度调度推测解码、半自回归生成与大模型推理加速"
+           -- 2.2 (biased logits, sampling), 2.3 (VanillaMarkov), 3.1 (prefix
+              survival, overlap identity), 3.2 (hardware-aware prefix scheduler)
+  [WALK]   "DeepSpec 训练全流程详解（以 Qwen3 + DSpark 为例）"
+           -- 4.3 Propose, 4.4 Verify (rejection test, residual, bonus token)
+
+Readings where the pages are silent or disagree (each one is listed with its
+reason in the repository's design notes):
+  * position 0 is biased by the Markov head using ``prev_tok`` ([TRAIN], m_1 =
+    W_1[D]); ``bias_at_first=False`` gives the [READ] 2.3 behaviour instead;
+  * no activation between the two Markov tables ([TRAIN]); ``act="silu"`` gives
+    the [READ] 2.3 variant;
+  * argmax ties go to the lowest token index;
+  * temperature T divides the logits of both draft and target; T = 0 is greedy
+    (argmax) for draft, accept test, correction and bonus;
+  * random numbers: Philox4x32-10 (Salmon et al., SC'11) keyed by the 64-bit
+    seed, counter (element group, position, request id, stream); streams
+    0 draft Gumbel, 1 accept uniform, 2 residual Gumbel, 3 bonus Gumbel;
+    u = ((w >> 9) + 0.5) * 2^-23, exactly representable in fp32 and in (0,1);
+  * accept iff u < min(1, p/q) (strict);
+  * an empty residual (sum <= 1e-12 * sum p) falls back to sampling p;
+  * scheduler sort key (a desc, r asc, j asc); Theta must strictly improve;
+    SPS table is 1-based (sps[B-1] = SPS(B)); B beyond the table is infeasible;
+  * conf is clamped to [0, 1];
+  * overlap: a_i is reported as sum(min(p,q)) unclamped; positions i >=
+    valid_len have a_i = 0; a block is valid when valid_len >= 1.
+
+Parity pins (what checks this oracle against something other than itself)
+live in tests/test_oracle_pins.py; nothing in this file is "parity unpinned".
+"""
+
+from __future__ import annotations
+
+import numpy as np
+
+# ---------------------------------------------------------------------------
+# Philox4x32-10, from its published definition (Salmon, Moraes, Dror, Shaw,
+# "Parallel Random Numbers: As Easy as 1, 2, 3", SC'11): a 4-word counter is
+# scrambled by 10 rounds; each round multiplies words 0 and 2 by fixed odd
+# constants, swaps the high/low halves across the words and xors in the key;
+# the 2-word key advances by a Weyl sequence between rounds.
+# ---------------------------------------------------------------------------
+
+PHILOX_M0 = 0xD2511F53
+PHILOX_M1 = 0xCD9E8D57
+PHILOX_W0 = 0x9E3779B9
+PHILOX_W1 = 0xBB67AE85
+_MASK32 = np.uint64(0xFFFFFFFF)
+
+STREAM_DRAFT = 0
+STREAM_ACCEPT = 1
+STREAM_RESIDUAL = 2
+STREAM_BONUS = 3
+
+
+def philox4x32_10(c0, c1, c2, c3, k0, k1):
+    """Philox4x32 with 10 rounds.  Arguments are integers or integer arrays
+    holding 32-bit values; returns the four output words as uint64 arrays."""
+    c = [np.asarray(x, dtype=np.uint64) & _MASK32 for x in (c0, c1, c2, c3)]
+    k0 = np.uint64(int(k0) & 0xFFFFFFFF)
+    k1 = np.uint64(int(k1) & 0xFFFFFFFF)
+    m0 = np.uint64(PHILOX_M0)
+    m1 = np.uint64(PHILOX_M1)
+    for _ in range(10):
+        p0 = m0 * c[0]                  # 32 x 32 -> 64 bits, exact in uint64
+        p1 = m1 * c[2]
+        hi0, lo0 = p0 >> np.uint64(32), p0 & _MASK32
+        hi1, lo1 = p1 >> np.uint64(32), p1 & _MASK32
+        c = [hi1 ^ c[1] ^ k0, lo1, hi0 ^ c[3] ^ k1, lo0]
+        k0 = np.uint64((int(k0) + PHILOX_W0) & 0xFFFFFFFF)
+        k1 = np.uint64((int(k1) + PHILOX_W1) & 0xFFFFFFFF)
+    return tuple(x & _MASK32 for x in c)
+
+
+def seed_key(seed: int):
+    seed = int(seed) & 0xFFFFFFFFFFFFFFFF
+    return seed & 0xFFFFFFFF, seed >> 32
+
+
+def uniform_from_word(w):
+    """u = ((w >> 9) + 0.5) * 2^-23, in (0, 1)."""
+    w = np.asarray(w, dtype=np.uint64)
+    return ((w >> np.uint64(9)).astype(np.float64) + 0.5) * 2.0 ** -23
+
+
+def vocab_uniforms(seed: int, position: int, req: int, stream: int, V: int):
+    """One uniform per vocabulary entry v: word (v mod 4) of
+    Philox(counter = (v div 4, position, req, stream), key = seed)."""
+    v = np.arange(V, dtype=np.uint64)
+    k0, k1 = seed_key(seed)
+    words = philox4x32_10(v >> np.uint64(2), position, req, stream, k0, k1)
+    w = np.choose((v & np.uint64(3)).astype(np.int64), words)
+    return uniform_from_word(w)
+
+
+def vocab_gumbel(seed: int, position: int, req: int, stream: int, V: int):
+    """Standard Gumbel noise g_v = -ln(-ln u_v)."""
+    u = vocab_uniforms(seed, position, req, stream, V)
+    return -np.log(-np.log(u))
+
+
+def accept_uniform(seed: int, position: int, req: int) -> float:
+    """The uniform of the accept test at one position ([WALK] 4.4: random())."""
+    k0, k1 = seed_key(seed)
+    w = philox4x32_10(0, position, req, STREAM_ACCEPT, k0, k1)[0]
+    return float(uniform_from_word(w))
+
+
+# ---------------------------------------------------------------------------
+# Small numerical helpers, written out.
+# ---------------------------------------------------------------------------
+
+def logsumexp(x):
+    x = np.asarray(x, dtype=np.float64)
+    m = np.max(x)
+    return float(m + np.log(np.sum(np.exp(x - m))))
+
+
+def softmax(x):
+    x = np.asarray(x, dtype=np.float64)
+    return np.exp(x - logsumexp(x))
+
+
+def top2_margin(z):
+    """Gap between the largest and the second-largest entry (inf if V == 1)."""
+    z = np.asarray(z, dtype=np.float64)
+    if z.size < 2:
+        return float("inf")
+    i = int(np.argmax(z))
+    rest = np.delete(z, i)
+    return float(z[i] - np.max(rest))
+
+
+def _f64(a):
+    return np.asarray(a).astype(np.float64)
+
+
+# ---------------------------------------------------------------------------
+# a1: prefix survival  ([READ] 3.1: a_{r,j} = prod_{i<=j} c_{r,i})
+# ---------------------------------------------------------------------------
+
+def survival(conf):
+    """a[r, j] = prod_{i <= j} clamp(c[r, i], 0, 1), in fp64.
+
+    ``conf`` is [R, gamma].  Non-finite confidences are an error."""
+    c = _f64(conf)
+    if not np.all(np.isfinite(c)):
+        raise ValueError("non-finite confidence")
+    c = np.clip(c, 0.0, 1.0)
+    R, G = c.shape
+    a = np.empty((R, G), dtype=np.float64)
+    for r in range(R):
+        acc = 1.0
+        for j in range(G):
+            acc = acc * c[r, j]
+            a[r, j] = acc
+    return a
+
+
+# ---------------------------------------------------------------------------
+# a2/a3: Markov bias  ([TRAIN] Markov 顺序修正: m_i = W_1[t_{i-1}], b_i = W_2 m_i;
+# [NOTES] 2.3: one table lookup plus one low-rank projection)
+#
+# Storage: E is the down table [V, r] (row t is the embedding of token t);
+# W is the up projection stored [V, r] (row v is the weight vector producing
+# logit bias v), i.e. b[v] = sum_k W[v, k] * m[k].
+# ---------------------------------------------------------------------------
+
+def markov_bias(E, W, prev: int, act: str = "none"):
+    m = _f64(E[prev])
+    if act == "silu":
+        m = m / (1.0 + np.exp(-m))
+    elif act != "none":
+        raise ValueError(act)
+    return _f64(W) @ m
+
+
+# ---------------------------------------------------------------------------
+# a2-a4: sequential propose  ([TRAIN] Markov 顺序修正; [READ] 2.2, 2.3)
+# ---------------------------------------------------------------------------
+
+def propose(U, E, W, conf, prev_tok, req_id=None, temperature=0.0, seed=0,
+            bias_at_first=True, act="none"):
+    """Sequential Markov-head proposal for a batch of R requests.
+
+    For each request r and position j = 0..gamma-1:
+        prev  = prev_tok[r] if j == 0 else x[r, j-1]
+        l     = U[r, j] + b(prev)        (b omitted at j = 0 if not bias_at_first)
+        T = 0: x = argmax l,              lse = logsumexp(l),   l(x)
+        T > 0: x = argmax l/T + g,        lse = logsumexp(l/T), l(x)/T
+    where g is the stream-0 Gumbel noise of (seed, j, req_id[r]).
+
+    Returns a dict with tokens [R,G] int, lse_q [R,G], logit_at_tok [R,G],
+    survival [R,G] (fp64) and margin [R,G] (top-2 gap of the decision
+    variable, for the near-tie exemption rule)."""
+    U = np.asarray(U)
+    R, G, V = U.shape
+    if req_id is None:
+        req_id = np.arange(R)
+    T = float(temperature)
+    tokens = np.zeros((R, G), dtype=np.int64)
+    lse_q = np.zeros((R, G))
+    logit_at_tok = np.zeros((R, G))
+    margin = np.zeros((R, G))
+    for r in range(R):
+        prev = int(prev_tok[r])
+        for j in range(G):
+            ell = _f64(U[r, j])
+            if j > 0 or bias_at_first:
+                ell = ell + markov_bias(E, W, prev, act)
+            if T == 0.0:
+                z = ell
+                lse_q[r, j] = logsumexp(ell)
+            else:
+                s = ell / T
+                z = s + vocab_gumbel(seed, j, int(req_id[r]), STREAM_DRAFT, V)
+                lse_q[r, j] = logsumexp(s)
+            x = int(np.argmax(z))              # first maximum: lowest index
+            tokens[r, j] = x
+            margin[r, j] = top2_margin(z)
+            logit_at_tok[r, j] = ell[x] if T == 0.0 else ell[x] / T
+            prev = x
+    return dict(tokens=tokens, lse_q=lse_q, logit_at_tok=logit_at_tok,
+                survival=survival(conf), margin=margin)
+
+
+# ---------------------------------------------------------------------------
+# a5: hardware-aware batch-global prefix scheduler  ([READ] 3.2)
+# ---------------------------------------------------------------------------
+
+def schedule(a, sps):
+    """Greedy global allocation maximising Theta = tau * SPS(B).
+
+    a is [R, gamma] (prefix survival, non-increasing in j); sps[B-1] = SPS(B).
+    Start from l_r = 0: B = R, tau = R, Theta* = R * SPS(R).  Visit the
+    (r, j) items in order of a descending (ties: r, then j ascending); each
+    visit adds one verify slot (B += 1) and its expected token (tau += a).
+    Keep the cut with the largest Theta (strictly larger wins, so the
+    smallest B attaining the maximum is kept).  Items beyond the SPS table
+    are infeasible.  keep_len[r] = number of kept items of request r.
+
+    Returns dict(keep_len [R] int, theta, B, theta_gap) where theta_gap is the
+    relative gap between Theta* and the best Theta at any other cut (used to
+    count near-ties)."""
+    a = _f64(a)
+    sps = _f64(sps)
+    R, G = a.shape
+    n_sps = sps.shape[0]
+    if R < 1 or R > n_sps:
+        raise ValueError("R outside the SPS table")
+    items = sorted(((a[r, j], r, j) for r in range(R) for j in range(G)),
+                   key=lambda it: (-it[0], it[1], it[2]))
+    tau = float(R)
+    best_theta = R * sps[R - 1]
+    best_k = 0
+    thetas = [best_theta]
+    for k, (av, r, j) in enumerate(items, start=1):
+        B = R + k
+        if B > n_sps:
+            break
+        tau = tau + av
+        theta = tau * sps[B - 1]
+        thetas.append(theta)
+        if theta > best_theta:
+            best_theta = theta
+            best_k = k
+    keep_len = np.zeros(R, dtype=np.int64)
+    for (av, r, j) in items[:best_k]:
+        keep_len[r] += 1
+    others = [t for k, t in enumerate(thetas) if k != best_k]
+    gap = (best_theta - max(others)) / abs(best_theta) if others and best_theta != 0 else float("inf")
+    return dict(keep_len=keep_len, theta=float(best_theta), B=R + best_k,
+                theta_gap=float(gap), sorted_items=items)
+
+
+# ---------------------------------------------------------------------------
+# a6/a7: target verification  ([WALK] 4.4; [READ] 2.1, 3.1)
+# ---------------------------------------------------------------------------
+
+def _draft_logits(U, E, W, prev_tok, tokens, r, t, bias_at_first, act):
+    ell = _f64(U[r, t])
+    prev = int(prev_tok[r]) if t == 0 else int(tokens[r, t - 1])
+    if t > 0 or bias_at_first:
+        ell = ell + markov_bias(E, W, prev, act)
+    return ell
+
+
+def verify(P, U, E, W, prev_tok, tokens, keep_len, req_id=None,
+           temperature=0.0, seed=0, bias_at_first=True, act="none"):
+    """Rejection verification of the kept prefix of every request.
+
+    P is [R, gamma+1, V]: row t scores draft token x_t, row keep_len[r] gives
+    the bonus distribution.  The draft distribution q_t = softmax(l_t / T) is
+    recomputed here from U, E, W and the draft tokens (its definition).
+
+    T > 0, for t = 0..keep_len-1: accept x_t iff u_t < min(1, p_t(x_t)/q_t(x_t))
+    (u_t: stream-1 uniform of (seed, t, req)); stop at the first rejection k.
+    If k < keep_len the next token is drawn from norm(max(0, p_k - q_k)) by
+    Gumbel-max on stream 2; otherwise the bonus token is drawn from p at row
+    keep_len by Gumbel-max on stream 3.
+    T = 0: accept iff x_t == argmax P[r, t]; the correction / bonus is argmax P.
+
+    Returns dict(accept_len [R], next_token [R]) plus diagnostics:
+    accept_gap [R] (smallest |u - min(1,p/q)| over the tests taken, or the
+    smallest argmax margin in greedy mode) and next_margin [R]."""
+    P = np.asarray(P)
+    R = P.shape[0]
+    V = P.shape[2]
+    if req_id is None:
+        req_id = np.arange(R)
+    T = float(temperature)
+    accept_len = np.zeros(R, dtype=np.int64)
+    next_token = np.zeros(R, dtype=np.int64)
+    accept_gap = np.full(R, np.inf)
+    next_margin = np.zeros(R)
+    for r in range(R):
+        L = int(keep_len[r])
+        req = int(req_id[r])
+        k = L
+        p_k = q_k = None
+        for t in range(L):
+            x = int(tokens[r, t])
+            if T == 0.0:
+                row = _f64(P[r, t])
+                accept_gap[r] = min(accept_gap[r], top2_margin(row))
+                ok = int(np.argmax(row)) == x
+            else:
+                p = softmax(_f64(P[r, t]) / T)
+                q = softmax(_draft_logits(U, E, W, prev_tok, tokens, r, t,
+                                          bias_at_first, act) / T)
+                accept_prob = min(1.0, p[x] / q[x])
+                u = accept_uniform(seed, t, req)
+                accept_gap[r] = min(accept_gap[r], abs(u - accept_prob))
+                ok = u < accept_prob
+                if not ok:
+                    p_k, q_k = p, q
+            if not ok:
+                k = t
+                break
+        if k < L:
+            if T == 0.0:
+                z = _f64(P[r, k])
+            else:
+                res = np.maximum(0.0, p_k - q_k)
+                g = vocab_gumbel(seed, k, req, STREAM_RESIDUAL, V)
+                if np.sum(res) <= 1e-12 * np.sum(p_k):
+                    z = np.log(p_k) + g
+                else:
+                    with np.errstate(divide="ignore"):
+                        z = np.where(res > 0.0, np.log(res), -np.inf) + g
+        else:
+            if T == 0.0:
+                z = _f64(P[r, L])
+            else:
+                z = _f64(P[r, L]) / T + vocab_gumbel(seed, L, req, STREAM_BONUS, V)
+        accept_len[r] = k
+        next_token[r] = int(np.argmax(z))
+        finite = z[np.isfinite(z)]
+        next_margin[r] = top2_margin(finite) if finite.size > 1 else float("inf")
+    return dict(accept_len=accept_len, next_token=next_token,
+                accept_gap=accept_gap, next_margin=next_margin)
+
+
+# ---------------------------------------------------------------------------
+# a8: offline overlap metrics  ([TRAIN] 评估口径 / 离线指标; [READ] 3.1)
+# ---------------------------------------------------------------------------
+
+def overlap(P_logits, Q_logits, valid_len):
+    """Teacher-forced overlap metrics of N blocks of gamma positions.
+
+    For each block n and valid position i < valid_len[n]:
+        p = softmax(P[n, i]), q = softmax(Q[n, i])
+        a[n, i]  = sum_v min(p, q)
+        l1[n, i] = sum_v |p - q|        (so a = 1 - l1/2 by the identity)
+    invalid positions have a = 0 (and l1 = 0).
+        tau[n] = 1 + sum_i prod_{j <= i} a[n, j]
+        accept_rate[i] = mean of a[n, i] over blocks with position i valid
+        mean_tau = mean of tau over valid blocks (valid_len >= 1)
+    Empty averages are reported as 0."""
+    P = np.asarray(P_logits)
+    Q = np.asarray(Q_logits)
+    N, G, V = P.shape
+    vl = np.asarray(valid_len).astype(np.int64)
+    a = np.zeros((N, G))
+    l1 = np.zeros((N, G))
+    tau = np.zeros(N)
+    for n in range(N):
+        L = int(vl[n])
+        for i in range(min(max(L, 0), G)):
+            p = softmax(_f64(P[n, i]))
+            q = softmax(_f64(Q[n, i]))
+            a[n, i] = np.sum(np.minimum(p, q))
+            l1[n, i] = np.sum(np.abs(p - q))
+        acc = 1.0
+        t = 1.0
+        for i in range(G):
+            acc = acc * a[n, i]
+            t = t + acc
+        tau[n] = t
+    accept_rate = np.zeros(G)
+    for i in range(G):
+        sel = vl > i
+        accept_rate[i] = float(np.mean(a[sel, i])) if np.any(sel) else 0.0
+    valid = vl >= 1
+    mean_tau = float(np.mean(tau[valid])) if np.any(valid) else 0.0
+    return dict(a=a, l1=l1, tau=tau, accept_rate=accept_rate, mean_tau=mean_tau)
+
+
+# ---------------------------------------------------------------------------
+# One whole draft-verify cycle (propose -> schedule -> verify), as the pages'
+# serving loop runs it ([WALK] 4.2), used by the cycle parity tests and the
+# CPU baseline.
+# ---------------------------------------------------------------------------
+
+def cycle(U, E, W, conf, prev_tok, P, sps, req_id=None, temperature=0.0,
+          seed=0, bias_at_first=True, act="none", keep_len=None):
+    prop = propose(U, E, W, conf, prev_tok, req_id, temperature, seed,
+                   bias_at_first, act)
+    a32 = prop["survival"].astype(np.float32)       # the schedule's input type
+    sch = schedule(a32, sps)
+    kl = sch["keep_len"] if keep_len is None else np.asarray(keep_len)
+    ver = verify(P, U, E, W, prev_tok, prop["tokens"], kl, req_id,
+                 temperature, seed, bias_at_first, act)
+    return dict(propose=prop, schedule=sch, verify=ver, keep_len=kl)

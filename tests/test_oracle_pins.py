@@ -1,0 +1,431 @@
+"""Pins of the fp64 oracle against facts fixed outside the oracle itself:
+published known-answer vectors, the pages' worked numbers, closed forms,
+invariants, brute force on tiny inputs and distributional identities checked
+by simulation.  No GPU needed."""
+
+import itertools
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+from scipy import special, stats
+
+from oracle import dsd_oracle as O
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _golden(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return json.load(f)
+
+
+# --------------------------------------------------------------------- Philox
+
+def test_philox_known_answers():
+    kat = _golden("philox4x32_10_kat.json")
+    for vec in kat["vectors"]:
+        ctr = [int(x, 16) for x in vec["ctr"]]
+        key = [int(x, 16) for x in vec["key"]]
+        out = [int(x) for x in O.philox4x32_10(*ctr, *key)]
+        assert out == [int(x, 16) for x in vec["out"]]
+
+
+def test_uniform_endpoints_exact_in_fp32():
+    u = O.uniform_from_word(np.array([0, 0xFFFFFFFF, 1 << 9, 0x80000000], dtype=np.uint64))
+    assert u[0] == 2.0 ** -24
+    assert u[1] == 1.0 - 2.0 ** -24
+    assert u[2] == 1.5 * 2.0 ** -23
+    assert u[3] == 0.5 + 2.0 ** -24
+    assert np.all(u.astype(np.float32).astype(np.float64) == u)
+    assert np.all((u > 0) & (u < 1))
+
+
+def test_vocab_uniforms_select_word_by_index():
+    seed = 0x1234_5678_9ABC_DEF0
+    u = O.vocab_uniforms(seed, position=3, req=77, stream=2, V=10)
+    for v in range(10):
+        words = O.philox4x32_10(v // 4, 3, 77, 2, seed & 0xFFFFFFFF, seed >> 32)
+        assert u[v] == O.uniform_from_word(words[v % 4])
+
+
+def test_gumbel_moments():
+    # Standard Gumbel: mean = Euler-Mascheroni constant, variance = pi^2/6.
+    g = O.vocab_gumbel(seed=99, position=0, req=0, stream=0, V=400_000)
+    assert abs(g.mean() - np.euler_gamma) < 0.01
+    assert abs(g.var() - math.pi ** 2 / 6) < 0.02
+
+
+# ------------------------------------------------------------------- survival
+
+def test_survival_worked_example_from_the_page():
+    ex = _golden("survival_worked_example.json")
+    for case in ex["cases"]:
+        conf = np.full((1, case["positions"]), case["c"])
+        a = O.survival(conf)
+        assert a[0, -1] == pytest.approx(case["a_last"], rel=1e-14)
+        assert round(a[0, -1], 3) == case["page_rounded"]
+    # the page's point: the optimistic product overstates survival by ~44%
+    ratio = 0.377149515625 / 0.262144
+    assert 1.43 < ratio < 1.45
+
+
+def test_survival_clamps_and_is_monotone():
+    conf = np.array([[1.5, 0.5, -0.2, 0.9], [0.9, 0.9, 0.9, 1.0]])
+    a = O.survival(conf)
+    assert a[0].tolist() == [1.0, 0.5, 0.0, 0.0]
+    assert np.allclose(a[1], [0.9, 0.81, 0.729, 0.729])
+    rng = np.random.default_rng(0)
+    a = O.survival(rng.random((50, 7)))
+    assert np.all(np.diff(a, axis=1) <= 0)
+    with pytest.raises(ValueError):
+        O.survival(np.array([[0.5, np.nan]]))
+
+
+# ---------------------------------------------------------------- Markov bias
+
+def test_markov_bias_one_hot_selects_a_column_of_w():
+    # V != r so a transposed table cannot pass silently.
+    V, r = 11, 3
+    rng = np.random.default_rng(1)
+    W = rng.standard_normal((V, r))
+    E = np.zeros((V, r))
+    E[5, 2] = 1.0
+    assert np.array_equal(O.markov_bias(E, W, 5), W[:, 2])
+    E[5, 0] = 2.0
+    assert np.allclose(O.markov_bias(E, W, 5), W[:, 2] + 2 * W[:, 0])
+
+
+def test_markov_bias_by_hand_rows():
+    g = _golden("markov_propose_by_hand.json")
+    E, W = np.array(g["E"], float), np.array(g["W"], float)
+    expected = {0: [2, 0, -1, 1], 1: [0, 3, 1, -2], 2: [2, 3, 0, -1], 3: [0, 0, 0, 0]}
+    for prev, b in expected.items():
+        assert O.markov_bias(E, W, prev).tolist() == b
+
+
+def test_markov_bias_silu_variant():
+    E = np.array([[0.0, 1.0, -30.0]])
+    W = np.eye(3)
+    b = O.markov_bias(E, W, 0, act="silu")
+    assert b[0] == 0.0
+    assert b[1] == pytest.approx(1.0 / (1.0 + math.exp(-1.0)), rel=1e-15)  # silu(1)
+    assert abs(b[2]) < 1e-11
+
+
+# -------------------------------------------------------------------- propose
+
+@pytest.mark.parametrize("variant,baf", [("bias_at_first", True), ("no_bias_at_first", False)])
+def test_propose_by_hand(variant, baf):
+    g = _golden("markov_propose_by_hand.json")
+    out = O.propose(np.array(g["U"], float), np.array(g["E"], float), np.array(g["W"], float),
+                    np.full((1, 3), 0.9), np.array(g["prev_tok"]), bias_at_first=baf)
+    exp = g[variant]
+    assert out["tokens"][0].tolist() == exp["tokens"]
+    assert out["logit_at_tok"][0].tolist() == exp["logit_at_tok"]
+    for j, row in enumerate(exp["logits"]):
+        lse = math.log(sum(math.exp(x) for x in row))
+        assert out["lse_q"][0, j] == pytest.approx(lse, rel=1e-14)
+
+
+def test_propose_zero_tables_is_positionwise_argmax():
+    rng = np.random.default_rng(2)
+    R, G, V, r = 3, 5, 50, 4
+    U = rng.standard_normal((R, G, V)) * 2
+    out = O.propose(U, np.zeros((V, r)), rng.standard_normal((V, r)), rng.random((R, G)),
+                    rng.integers(0, V, R))
+    assert np.array_equal(out["tokens"], U.argmax(axis=2))
+    assert np.allclose(out["lse_q"], special.logsumexp(U, axis=2), rtol=1e-14)
+    assert np.allclose(out["logit_at_tok"], U.max(axis=2))
+
+
+def test_propose_single_position_matches_dense_transition_matrix():
+    # gamma = 1: x = argmax(U_0 + T[prev]) with the V x V transition matrix
+    # T = E W^T built explicitly (the low-rank factorisation of the pages).
+    rng = np.random.default_rng(3)
+    V, r = 40, 6
+    E, W = rng.standard_normal((V, r)), rng.standard_normal((V, r))
+    T = np.zeros((V, V))
+    for i in range(V):
+        for v in range(V):
+            T[i, v] = sum(E[i, k] * W[v, k] for k in range(r))
+    U = rng.standard_normal((8, 1, V))
+    prev = rng.integers(0, V, 8)
+    out = O.propose(U, E, W, np.ones((8, 1)), prev)
+    for rr in range(8):
+        assert out["tokens"][rr, 0] == int(np.argmax(U[rr, 0] + T[prev[rr]]))
+
+
+def test_propose_greedy_brute_force_chain():
+    # gamma = 3 chain, tiny V: at every step the chosen token beats every
+    # other token under the bias of the previously chosen one.
+    rng = np.random.default_rng(4)
+    V, r, G = 9, 3, 3
+    E, W = rng.standard_normal((V, r)), rng.standard_normal((V, r))
+    U = rng.standard_normal((5, G, V))
+    prev = rng.integers(0, V, 5)
+    out = O.propose(U, E, W, np.ones((5, G)), prev)
+    for rr in range(5):
+        p = int(prev[rr])
+        for j in range(G):
+            scores = [U[rr, j, v] + float(np.dot(E[p], W[v])) for v in range(V)]
+            assert out["tokens"][rr, j] == max(range(V), key=lambda v: (scores[v], -v))
+            p = int(out["tokens"][rr, j])
+
+
+def test_propose_ties_take_the_lowest_index():
+    U = np.zeros((1, 2, 6))
+    U[0, 0, [2, 4]] = 1.0
+    U[0, 1, [5, 1]] = 3.0
+    out = O.propose(U, np.zeros((6, 2)), np.zeros((6, 2)), np.ones((1, 2)), np.array([0]))
+    assert out["tokens"][0].tolist() == [2, 1]
+    assert out["margin"][0].tolist() == [0.0, 0.0]
+
+
+def test_propose_sampling_follows_softmax_of_scaled_logits():
+    # Gumbel-max sampling: over many seeds, x ~ softmax(l / T).
+    V, T = 5, 0.7
+    U = np.array([[[0.3, -1.0, 1.2, 0.0, 0.8]]])
+    E, W = np.zeros((V, 2)), np.zeros((V, 2))
+    n = 8000
+    counts = np.zeros(V)
+    for s in range(n):
+        out = O.propose(U, E, W, np.ones((1, 1)), np.array([0]), temperature=T, seed=1000 + s)
+        counts[out["tokens"][0, 0]] += 1
+    p = special.softmax(U[0, 0] / T)
+    chi2 = stats.chisquare(counts, p * n)
+    assert chi2.pvalue > 1e-3
+    out = O.propose(U, E, W, np.ones((1, 1)), np.array([0]), temperature=T, seed=5)
+    x = out["tokens"][0, 0]
+    assert out["lse_q"][0, 0] == pytest.approx(special.logsumexp(U[0, 0] / T), rel=1e-14)
+    assert out["logit_at_tok"][0, 0] == pytest.approx(U[0, 0, x] / T, rel=1e-14)
+
+
+def test_propose_sampling_depends_on_request_id_not_slot():
+    rng = np.random.default_rng(6)
+    V = 30
+    U = rng.standard_normal((2, 3, V))
+    E, W = rng.standard_normal((V, 2)), rng.standard_normal((V, 2))
+    prev = np.array([3, 9])
+    a = O.propose(U, E, W, np.ones((2, 3)), prev, req_id=np.array([10, 20]), temperature=1.0, seed=7)
+    b = O.propose(U[::-1], E, W, np.ones((2, 3)), prev[::-1], req_id=np.array([20, 10]),
+                  temperature=1.0, seed=7)
+    assert np.array_equal(a["tokens"], b["tokens"][::-1])
+
+
+# ------------------------------------------------------------------- schedule
+
+def test_schedule_by_hand():
+    g = _golden("schedule_by_hand.json")
+    a = O.survival(np.array(g["conf"]))
+    assert np.allclose(a, g["survival"], rtol=1e-15)
+    for case in g["cases"]:
+        out = O.schedule(np.array(g["survival"]), np.array(case["sps"], float))
+        assert out["keep_len"].tolist() == case["keep_len"]
+        assert out["theta"] == pytest.approx(case["theta"], rel=1e-14)
+        assert out["B"] == case["B"]
+
+
+def _theta(a, sps, ls):
+    R = a.shape[0]
+    B = sum(1 + l for l in ls)
+    if B > len(sps):
+        return -np.inf
+    tau = sum(1 + a[r, :ls[r]].sum() for r in range(R))
+    return tau * sps[B - 1]
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_schedule_matches_brute_force(seed):
+    rng = np.random.default_rng(100 + seed)
+    R = int(rng.integers(1, 5))
+    G = int(rng.integers(1, 4))
+    a = O.survival(rng.random((R, G)) ** 0.5)
+    n = R * (G + 1) - int(rng.integers(0, 2))       # sometimes one slot short
+    n = max(n, R)
+    knee = rng.uniform(0, n)
+    sps = 1.0 / (1.0 + rng.uniform(0.01, 0.5) * np.maximum(0.0, np.arange(1, n + 1) - knee))
+    best = max(_theta(a, sps, ls) for ls in itertools.product(range(G + 1), repeat=R))
+    out = O.schedule(a, sps)
+    assert out["theta"] == pytest.approx(best, rel=1e-12)
+    assert _theta(a, sps, out["keep_len"]) == pytest.approx(best, rel=1e-12)
+
+
+def test_schedule_constant_sps_keeps_everything():
+    rng = np.random.default_rng(7)
+    a = O.survival(0.05 + 0.95 * rng.random((6, 7)))
+    out = O.schedule(a, np.full(6 * 8, 1e3))
+    assert out["keep_len"].tolist() == [7] * 6
+
+
+def test_schedule_flat_then_inverse_table_keeps_nothing():
+    # SPS = 1e3 up to B = R, then proportional to 1/B: Theta is proportional
+    # to tau/B, which starts at 1 and drops with every slot of survival < 1.
+    rng = np.random.default_rng(8)
+    R = 12
+    a = O.survival(rng.beta(5, 2, size=(R, 7)))
+    B = np.arange(1, 129, dtype=float)
+    sps = np.where(B <= R, 1e3, 1e3 * R / B)
+    out = O.schedule(a, sps)
+    assert out["keep_len"].tolist() == [0] * R
+    assert out["theta"] == pytest.approx(R * 1e3)
+
+
+def test_schedule_result_is_a_prefix_per_request_even_with_ties():
+    a = np.array([[1.0, 1.0, 0.5], [1.0, 0.5, 0.5]])
+    sps = np.array([100, 100, 100, 100, 99, 98, 70, 10], float)
+    out = O.schedule(a, sps)
+    items = out["sorted_items"]
+    assert [(r, j) for _, r, j in items[:5]] == [(0, 0), (0, 1), (1, 0), (0, 2), (1, 1)]
+    # Theta by cut k = 0..6: 200, 300, 400, 495, 539, 420, 65  ->  k* = 4
+    assert out["keep_len"].tolist() == [3, 1]
+    assert out["theta"] == pytest.approx(539.0)
+
+
+# --------------------------------------------------------------------- verify
+
+def test_verify_greedy_by_hand():
+    P = np.zeros((1, 4, 4))
+    P[0, 0] = [5, 1, 0, 0]     # argmax 0
+    P[0, 1] = [0, 0, 1, 4]     # argmax 3
+    P[0, 2] = [0, 6, 2, 0]     # argmax 1
+    P[0, 3] = [0, 0, 0, 9]     # argmax 3
+    tokens = np.array([[0, 3, 2]])
+    U = np.zeros((1, 3, 4))
+    E = W = np.zeros((4, 2))
+    for kl, acc, nxt in [(3, 2, 1), (2, 2, 1), (1, 1, 3), (0, 0, 0)]:
+        out = O.verify(P, U, E, W, np.array([0]), tokens, np.array([kl]))
+        assert (out["accept_len"][0], out["next_token"][0]) == (acc, nxt)
+    tokens2 = np.array([[0, 3, 1]])
+    out = O.verify(P, U, E, W, np.array([0]), tokens2, np.array([3]))
+    assert (out["accept_len"][0], out["next_token"][0]) == (3, 3)   # bonus row 3
+
+
+def test_verify_identical_distributions_accept_everything():
+    rng = np.random.default_rng(9)
+    V, G = 20, 4
+    U = rng.standard_normal((2, G, V))
+    E, W = rng.standard_normal((V, 3)) * 0.5, rng.standard_normal((V, 3)) * 0.5
+    prev = np.array([1, 2])
+    prop = O.propose(U, E, W, np.ones((2, G)), prev, temperature=0.9, seed=3)
+    P = np.zeros((2, G + 1, V))
+    for r in range(2):
+        for t in range(G):
+            P[r, t] = O._draft_logits(U, E, W, prev, prop["tokens"], r, t, True, "none")
+        P[r, G] = rng.standard_normal(V)
+    out = O.verify(P, U, E, W, prev, prop["tokens"], np.array([G, 2]), temperature=0.9, seed=3)
+    assert out["accept_len"].tolist() == [G, 2]
+
+
+def _committed(out, tokens, r=0):
+    k = int(out["accept_len"][r])
+    return list(tokens[r, :k]) + [int(out["next_token"][r])]
+
+
+def test_verify_rejection_sampling_reproduces_the_target_distribution():
+    # The pages' losslessness claim: the first committed token is distributed
+    # as p_0, and given that position 0 was accepted the second one is
+    # distributed as p_1, whatever q is.  Checked by simulation over seeds.
+    V, T = 4, 0.8
+    U = np.array([[[1.5, 0.0, -0.5, 0.3], [0.0, 1.0, 0.2, -1.0]]])
+    E = np.array([[0.5, 0.0], [0.0, 0.7], [0.3, 0.3], [-0.4, 0.2]])
+    W = np.array([[1.0, -0.5], [0.2, 0.8], [-0.6, 0.1], [0.4, 0.4]])
+    P = np.array([[[0.0, 1.0, 0.5, -0.5], [1.2, -0.3, 0.0, 0.6], [0.0, 0.0, 2.0, 0.0]]])
+    prev = np.array([2])
+    p0 = special.softmax(P[0, 0] / T)
+    p1 = special.softmax(P[0, 1] / T)
+    n = 6000
+    first = np.zeros(V)
+    second = np.zeros(V)
+    for s in range(n):
+        prop = O.propose(U, E, W, np.ones((1, 2)), prev, temperature=T, seed=50_000 + s)
+        out = O.verify(P, U, E, W, prev, prop["tokens"], np.array([2]), temperature=T,
+                       seed=50_000 + s)
+        seq = _committed(out, prop["tokens"])
+        first[seq[0]] += 1
+        if len(seq) >= 2:
+            second[seq[1]] += 1
+    assert stats.chisquare(first, p0 * n).pvalue > 1e-3
+    m = second.sum()
+    assert m > 1000
+    assert stats.chisquare(second, p1 * m).pvalue > 1e-3
+    # q differs from p, so the test is not vacuous
+    q0 = special.softmax((U[0, 0] + W @ E[2]) / T)
+    assert 0.5 * np.abs(q0 - p0).sum() > 0.1
+
+
+# -------------------------------------------------------------------- overlap
+
+def test_overlap_identity_and_bounds():
+    rng = np.random.default_rng(10)
+    P = rng.standard_normal((6, 7, 300)) * 2
+    Q = P + rng.standard_normal((6, 7, 300)) * rng.uniform(0.1, 3, size=(6, 1, 1))
+    out = O.overlap(P, Q, np.full(6, 7))
+    assert np.allclose(out["a"], 1.0 - 0.5 * out["l1"], atol=1e-12)
+    assert np.all((out["a"] > 0) & (out["a"] < 1))
+
+
+def test_overlap_equal_and_disjoint():
+    rng = np.random.default_rng(11)
+    V = 64
+    P = rng.standard_normal((2, 7, V))
+    out = O.overlap(P, P.copy(), np.array([7, 7]))
+    assert np.allclose(out["a"], 1.0, atol=1e-14)
+    assert np.allclose(out["tau"], 8.0)
+    Pd = np.full((1, 7, V), -1e4)
+    Qd = np.full((1, 7, V), -1e4)
+    Pd[0, :, : V // 2] = 0.0
+    Qd[0, :, V // 2:] = 0.0
+    out = O.overlap(Pd, Qd, np.array([7]))
+    assert np.allclose(out["a"], 0.0, atol=1e-300)
+    assert np.allclose(out["l1"], 2.0)
+    assert out["tau"][0] == 1.0
+
+
+def _two_point_logits(alphas):
+    # p = (1, 0), q = (alpha, 1 - alpha)  =>  sum min(p, q) = alpha.
+    G = len(alphas)
+    P = np.zeros((1, G, 2))
+    Q = np.zeros((1, G, 2))
+    P[0, :, 1] = -1e9
+    for i, al in enumerate(alphas):
+        Q[0, i] = [math.log(al), math.log1p(-al)] if 0 < al < 1 else (
+            [0.0, -1e9] if al == 1 else [-1e9, 0.0])
+    return P, Q
+
+
+@pytest.mark.parametrize("alpha", [1.0, 0.0, 0.5, 0.8, 0.37])
+def test_tau_closed_forms(alpha):
+    P, Q = _two_point_logits([alpha] * 7)
+    out = O.overlap(P, Q, np.array([7]))
+    assert np.allclose(out["a"], alpha, atol=1e-12)
+    closed = 1.0 + sum(alpha ** k for k in range(1, 8))
+    assert out["tau"][0] == pytest.approx(closed, rel=1e-12, abs=1e-12)
+    if alpha == 1.0:
+        assert out["tau"][0] == pytest.approx(8.0)
+    if alpha == 0.0:
+        assert out["tau"][0] == 1.0
+
+
+def test_tau_first_position_zero_is_one():
+    P, Q = _two_point_logits([0.0, 0.9, 0.9, 0.9, 0.9, 0.9, 0.9])
+    assert O.overlap(P, Q, np.array([7]))["tau"][0] == pytest.approx(1.0)
+
+
+def test_overlap_valid_len_aggregation_by_hand():
+    al = [[0.9, 0.8, 0.7, 0.6, 0.5, 0.4, 0.3], [0.5, 0.5, 0.5, 0.2, 0.2, 0.2, 0.2],
+          [0.1] * 7]
+    P = np.concatenate([_two_point_logits(x)[0] for x in al])
+    Q = np.concatenate([_two_point_logits(x)[1] for x in al])
+    vl = np.array([7, 3, 0])
+    out = O.overlap(P, Q, vl)
+    assert np.allclose(out["a"][1], [0.5, 0.5, 0.5, 0, 0, 0, 0], atol=1e-12)
+    assert np.allclose(out["a"][2], 0.0)
+    tau0 = 1 + 0.9 + 0.72 + 0.504 + 0.3024 + 0.1512 + 0.06048 + 0.018144
+    tau1 = 1 + 0.5 + 0.25 + 0.125
+    assert out["tau"][:2] == pytest.approx([tau0, tau1], rel=1e-12)
+    assert out["tau"][2] == 1.0
+    assert out["mean_tau"] == pytest.approx((tau0 + tau1) / 2, rel=1e-12)
+    assert out["accept_rate"] == pytest.approx([0.7, 0.65, 0.6, 0.6, 0.5, 0.4, 0.3], rel=1e-12)
