@@ -1,0 +1,247 @@
+/*
+ * dsd.h -- C ABI of the DSpark draft/verify hot path on one GB300 (sm_103a).
+ *
+ * One serving cycle for a whole batch of R requests is
+ *     dsd_propose  -> dsd_schedule -> dsd_verify
+ * and dsd_overlap is the separate offline-metric call.  Sources, by page title
+ * and section:
+ *   [TRAIN] "Qwen3.8-Flash-Next DSpark 训练实验": 评估口径/离线指标;
+ *           Baseline 架构/Markov 顺序修正
+ *   [NOTES] "DSpark notes" (h.sjds.net/a/571373): 2.2 Sequential Stage;
+ *           2.3 串行头的两种形态
+ *   [READ]  "DSpark 论文精读：置信度调度推测解码、半自回归生成与大模型推理加速":
+ *           2.2, 2.3, 3.1, 3.2
+ *   [WALK]  "DeepSpec 训练全流程详解（以 Qwen3 + DSpark 为例）": 4.3 Propose,
+ *           4.4 Verify
+ *
+ * Conventions for every call below.
+ *   - Tensor arguments are DEVICE pointers owned by the caller, row-major and
+ *     contiguous with the vocabulary (V) or rank (r) innermost.  The library
+ *     never frees or keeps them.
+ *   - Logit tables (U, P, Q) and Markov tables (E, W) use the context's dtype
+ *     (DSD_BF16 or DSD_F32); all arithmetic is fp32 (fp64 for the survival
+ *     products and the scheduler's running sums).
+ *   - Vectorised loads need 16-byte aligned base pointers and V % 8 == 0;
+ *     the Markov rank must be a multiple of 64 (or r <= 64 and a multiple of
+ *     8).  Violations return DSD_ERR_ALIGN / DSD_ERR_SHAPE before any launch.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t, NULL = legacy
+ *     default stream).  Host-detectable errors return a negative status
+ *     before anything is launched; dsd_last_error() then has the message.
+ *     Errors found on the device (non-finite logits or confidences, a bounded
+ *     wait that ran out) are recorded in the context and returned by
+ *     dsd_sync_status().  Nothing traps, asserts or aborts on the device.
+ *   - No call allocates memory except dsd_create (the workspace) and the
+ *     first dsd_cycle_host call (its device staging buffers).  There is no
+ *     CPU fallback: without a usable sm_103a device dsd_create fails.
+ *   - Calls on one context must not overlap on the GPU (the workspace is
+ *     shared); use one context per concurrent stream.
+ *   - temperature == 0 means greedy everywhere (draft argmax, accept iff the
+ *     draft token is the target argmax, correction/bonus = target argmax).
+ *   - Randomness is Philox4x32-10 (Salmon et al., SC'11) keyed by the 64-bit
+ *     seed with counter (element group v/4, position, request id, stream):
+ *     stream 0 draft Gumbel, 1 accept uniform, 2 residual Gumbel, 3 bonus
+ *     Gumbel; u = ((w >> 9) + 0.5) * 2^-23.  Results therefore depend on the
+ *     request id, never on the batch slot or the grid size.
+ */
+#ifndef DSD_H
+#define DSD_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct dsd_ctx dsd_ctx;
+
+enum dsd_status {
+  DSD_OK = 0,
+  DSD_ERR_ARG = -1,        /* null pointer, negative size, bad enum, NaN temperature */
+  DSD_ERR_ALIGN = -2,      /* pointer not 16-byte aligned, V % 8 != 0 */
+  DSD_ERR_DTYPE = -3,      /* dtype not supported by the requested path */
+  DSD_ERR_SHAPE = -4,      /* size outside what the context was created for */
+  DSD_ERR_CUDA = -5,       /* a CUDA runtime call failed (message in dsd_last_error) */
+  DSD_ERR_NONFINITE = -6,  /* device saw a non-finite logit / confidence / sum */
+  DSD_ERR_TIMEOUT = -7,    /* a bounded device-side wait ran out */
+  DSD_ERR_CAPACITY = -8,   /* R larger than the SPS table */
+  DSD_ERR_UNSUPPORTED = -9 /* no sm_100-family device */
+};
+
+enum dsd_dtype { DSD_F32 = 0, DSD_BF16 = 1 };
+enum dsd_act { DSD_ACT_NONE = 0, DSD_ACT_SILU = 1 };
+/* Propose engine: AUTO picks tcgen05 tensor cores for bf16 batches of at
+ * least 16 requests and the CUDA-core path otherwise. */
+enum dsd_engine { DSD_ENGINE_AUTO = 0, DSD_ENGINE_SIMT = 1, DSD_ENGINE_TCGEN05 = 2 };
+
+typedef struct dsd_config {
+  int V;             /* vocabulary size, multiple of 8 */
+  int rank;          /* Markov rank r (256 on the pages) */
+  int gamma;         /* draft positions per request (7 on the pages), 1..16 */
+  int R_max;         /* largest batch a call may pass; R_max * gamma <= 4096 */
+  int dtype;         /* enum dsd_dtype of U, E, W, P, Q */
+  int act;           /* enum dsd_act between the two Markov tables: NONE per
+                        [TRAIN] Markov 顺序修正; SILU per [READ] 2.3 */
+  int bias_at_first; /* 1: position 0 is biased by E[prev_tok] ([TRAIN],
+                        m_1 = W_1[D]); 0: position 0 uses U only ([READ] 2.3) */
+  int engine;        /* enum dsd_engine */
+  int device;        /* CUDA device ordinal the context is bound to */
+} dsd_config;
+
+/* Create a context bound to cfg->device and allocate its workspace
+ * (one cudaMalloc, sized by R_max, gamma, V and the SM count).
+ * Returns DSD_OK and *out, or a negative status (out untouched). */
+int dsd_create(const dsd_config* cfg, dsd_ctx** out);
+
+/* Free the workspace and the context.  NULL is accepted. */
+int dsd_destroy(dsd_ctx* ctx);
+
+/* Message of the last host-side error on this context ("" if none).  The
+ * string is owned by the context and valid until the next call on it. */
+const char* dsd_last_error(const dsd_ctx* ctx);
+
+/* Wait for `stream`, then return (and clear) the device-side status of the
+ * calls made so far: DSD_OK, DSD_ERR_NONFINITE or DSD_ERR_TIMEOUT. */
+int dsd_sync_status(dsd_ctx* ctx, void* stream);
+
+/* Bytes of device workspace held by the context. */
+size_t dsd_workspace_bytes(const dsd_ctx* ctx);
+
+/* Number of kernels this context has launched so far (host-side count of
+ * every <<<>>> launch made by the calls below; memsets are not counted). */
+uint64_t dsd_launch_count(const dsd_ctx* ctx);
+
+/*
+ * dsd_propose -- sequential Markov-head proposal plus prefix survival.
+ * [TRAIN] Markov 顺序修正; [NOTES] 2.2-2.3; [READ] 2.2, 2.3, 3.1.
+ *
+ * For every request r and position j = 0..gamma-1, with prev = prev_tok[r]
+ * at j = 0 and the token chosen at j-1 afterwards:
+ *   m      = act(E[prev, :])                  (E: [V, r] down table)
+ *   b[v]   = sum_k W[v, k] * m[k]             (W: [V, r] up projection, the
+ *                                              nn.Linear(r, V).weight layout)
+ *   l      = U[r, j, :] + b                   (b skipped at j = 0 when
+ *                                              bias_at_first == 0)
+ *   T == 0: x = argmax_v l,  lse_q = logsumexp(l),   logit_at_tok = l[x]
+ *   T  > 0: x = argmax_v l/T + Gumbel_v(seed, j, req, stream 0),
+ *           lse_q = logsumexp(l/T),  logit_at_tok = l[x]/T
+ * Argmax ties go to the lowest index.  The biased logits never reach HBM.
+ *   survival[r, j] = prod_{i <= j} clamp(conf[r, i], 0, 1)   ([READ] 3.1)
+ *
+ * U        [R, gamma, V]  dtype        base logits of the parallel backbone
+ * E, W     [V, rank]      dtype        Markov tables
+ * conf     [R, gamma]     f32          per-position confidence
+ * prev_tok [R]            i32          token before position 0 (anchor)
+ * req_id   [R]            u32 or NULL  Philox request key (NULL: 0..R-1)
+ * tokens   [R, gamma]     i32  out     draft tokens
+ * lse_q    [R, gamma]     f32  out     log-normaliser of the draft softmax
+ * logit_at_tok [R,gamma]  f32  out     (scaled) draft logit of each token
+ * survival [R, gamma]     f32  out     prefix survival (fp64 product, rounded)
+ * R == 0 is a no-op.  prev_tok outside [0, V) is DSD_ERR_ARG on the device
+ * side (recorded, token 0 used) -- see dsd_sync_status.
+ */
+int dsd_propose(dsd_ctx* ctx, int R, const void* U, const void* E, const void* W,
+                const float* conf, const int32_t* prev_tok, const uint32_t* req_id,
+                float temperature, uint64_t seed, int32_t* tokens, float* lse_q,
+                float* logit_at_tok, float* survival, void* stream);
+
+/*
+ * dsd_schedule -- hardware-aware batch-global prefix scheduler ([READ] 3.2).
+ *
+ * Maximises Theta = tau * SPS(B) with B = sum_r (1 + l_r) and
+ * tau = sum_r (1 + sum_{j < l_r} survival[r, j]).  Starting from l = 0
+ * (Theta = R * SPS(R)) it visits the (r, j) slots by survival descending
+ * (ties: r, then j ascending), adds one slot at a time and keeps the cut with
+ * the strictly largest Theta.  Because survival is non-increasing in j the
+ * kept slots form a prefix of every request.
+ *
+ * survival [R, gamma] f32        (dsd_propose's output, values in [0, 1])
+ * sps      [n_sps]    f32        sps[B-1] = SPS(B), steps/s at verify batch B
+ * keep_len [R]        i32  out   l_r in 0..gamma
+ * theta_B  [2]        f32  out   {Theta*, B*}
+ * R > n_sps returns DSD_ERR_CAPACITY; slots that would push B past n_sps are
+ * never taken.  Also records B* and the verify row list in the workspace for
+ * a following dsd_verify on the same stream.
+ */
+int dsd_schedule(dsd_ctx* ctx, int R, const float* survival, const float* sps, int n_sps,
+                 int32_t* keep_len, float* theta_B, void* stream);
+
+/*
+ * dsd_verify -- rejection verification of the kept prefixes ([WALK] 4.4;
+ * [READ] 2.1, 3.1).
+ *
+ * P [R, gamma+1, V] holds the target logits: row t scores draft token t and
+ * row keep_len[r] gives the bonus distribution.  Only rows 0..keep_len[r]
+ * of each request are read.  With p_t = softmax(P[r,t]/T) and the draft
+ * probability q_t(x_t) = exp(logit_at_tok - lse_q):
+ *   accept x_t iff u(seed, t, req, stream 1) < min(1, p_t(x_t) / q_t(x_t)),
+ *   stop at the first rejection k;
+ *   k < keep_len: next_token ~ norm(max(0, p_k - q_k)) by Gumbel-max
+ *                 (stream 2), where q_k is recomputed in full from U, E, W,
+ *                 prev_tok and tokens; an empty residual falls back to p_k;
+ *   k == keep_len: next_token ~ p_{keep_len} by Gumbel-max (stream 3).
+ * T == 0: accept iff x_t == argmax P[r,t]; next_token = argmax P[r,k].
+ * accept_len [R] i32 out (k), next_token [R] i32 out.  The committed tokens
+ * of request r are tokens[r, :k] followed by next_token[r].
+ * keep_len must come from dsd_schedule (or any values in 0..gamma); U, E, W,
+ * prev_tok, lse_q, logit_at_tok may be NULL when T == 0.
+ */
+int dsd_verify(dsd_ctx* ctx, int R, const void* P, const void* U, const void* E,
+               const void* W, const int32_t* prev_tok, const int32_t* tokens,
+               const float* lse_q, const float* logit_at_tok, const int32_t* keep_len,
+               const uint32_t* req_id, float temperature, uint64_t seed,
+               int32_t* accept_len, int32_t* next_token, void* stream);
+
+/*
+ * dsd_cycle -- dsd_propose, dsd_schedule and dsd_verify back to back on one
+ * stream ([WALK] 4.2 serving loop, one iteration, whole batch).  Outputs as
+ * the three calls; theta_B may be NULL.
+ */
+int dsd_cycle(dsd_ctx* ctx, int R, const void* U, const void* E, const void* W,
+              const float* conf, const int32_t* prev_tok, const uint32_t* req_id,
+              const void* P, const float* sps, int n_sps, float temperature, uint64_t seed,
+              int32_t* tokens, float* lse_q, float* logit_at_tok, float* survival,
+              int32_t* keep_len, float* theta_B, int32_t* accept_len, int32_t* next_token,
+              void* stream);
+
+/*
+ * dsd_cycle_host -- one cycle from HOST buffers.  The per-cycle inputs
+ * (U, P, conf, prev_tok, req_id) are copied host->device into staging
+ * buffers owned by the context (allocated on the first call, sized for
+ * R_max), the cycle runs, and tokens, keep_len, accept_len and next_token
+ * are copied back to the host.  E, W and sps are device pointers (model
+ * constants resident on the GPU).  Pinned host memory makes the copies
+ * asynchronous; the call returns after the results are on the host.
+ */
+int dsd_cycle_host(dsd_ctx* ctx, int R, const void* U_host, const void* E, const void* W,
+                   const float* conf_host, const int32_t* prev_tok_host,
+                   const uint32_t* req_id_host, const void* P_host, const float* sps,
+                   int n_sps, float temperature, uint64_t seed, int32_t* tokens_host,
+                   int32_t* keep_len_host, int32_t* accept_len_host,
+                   int32_t* next_token_host, void* stream);
+
+/*
+ * dsd_overlap -- teacher-forced offline metrics ([TRAIN] 评估口径/离线指标;
+ * [READ] 3.1 overlap identity).
+ *
+ * For block n and valid position i < valid_len[n], with p = softmax(P[n,i]),
+ * q = softmax(Q[n,i]):
+ *   a[n,i]  = sum_v min(p, q),   l1[n,i] = sum_v |p - q|   (a = 1 - l1/2)
+ * Invalid positions get a = l1 = 0.
+ *   tau[n] = 1 + sum_i prod_{j <= i} a[n,j]
+ *   accept_rate[i] = mean of a[n,i] over blocks whose position i is valid
+ *   mean_tau = mean of tau over blocks with valid_len >= 1
+ * (empty means are 0).
+ * P_logits, Q_logits [N, gamma, V] dtype; valid_len [N] i32 in 0..gamma;
+ * a, l1 [N, gamma] f32 out; tau [N] f32 out; accept_rate [gamma] f32 out;
+ * mean_tau [1] f32 out.  N == 0 writes zeros to accept_rate and mean_tau.
+ */
+int dsd_overlap(dsd_ctx* ctx, int N, const void* P_logits, const void* Q_logits,
+                const int32_t* valid_len, float* a, float* l1, float* tau,
+                float* accept_rate, float* mean_tau, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DSD_H */

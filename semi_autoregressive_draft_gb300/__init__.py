@@ -1,0 +1,331 @@
+"""GB300-native DSpark draft/verify hot path.
+
+Python binding of the C ABI declared in ``include/dsd.h``.  This module only
+marshals arguments (device pointers of torch tensors, the current CUDA
+stream) into ``libdsd.so``; every step of the path runs in the library's
+CUDA kernels.  If the library is not built, or no sm_100-family GPU is
+present, the calls fail loudly: there is no CPU fallback.
+
+Low-level functions carry the C names (``dsd_propose`` ...).  ``Context``
+wraps them with output allocation for convenience.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_lib", "libdsd.so")
+
+DSD_OK = 0
+STATUS_NAMES = {
+    0: "DSD_OK", -1: "DSD_ERR_ARG", -2: "DSD_ERR_ALIGN", -3: "DSD_ERR_DTYPE",
+    -4: "DSD_ERR_SHAPE", -5: "DSD_ERR_CUDA", -6: "DSD_ERR_NONFINITE",
+    -7: "DSD_ERR_TIMEOUT", -8: "DSD_ERR_CAPACITY", -9: "DSD_ERR_UNSUPPORTED",
+}
+DTYPES = {"f32": 0, "bf16": 1}
+TORCH_DTYPES = {"f32": torch.float32, "bf16": torch.bfloat16}
+ACTS = {"none": 0, "silu": 1}
+ENGINES = {"auto": 0, "simt": 1, "tcgen05": 2}
+
+EXPORTED = [
+    "dsd_create", "dsd_destroy", "dsd_last_error", "dsd_sync_status", "dsd_workspace_bytes",
+    "dsd_launch_count",
+    "dsd_propose", "dsd_schedule", "dsd_verify", "dsd_cycle", "dsd_cycle_host", "dsd_overlap",
+]
+
+
+class DsdError(RuntimeError):
+    def __init__(self, code, msg=""):
+        self.code = code
+        super().__init__(f"{STATUS_NAMES.get(code, code)}: {msg}")
+
+
+class dsd_config(ctypes.Structure):
+    _fields_ = [("V", ctypes.c_int), ("rank", ctypes.c_int), ("gamma", ctypes.c_int),
+                ("R_max", ctypes.c_int), ("dtype", ctypes.c_int), ("act", ctypes.c_int),
+                ("bias_at_first", ctypes.c_int), ("engine", ctypes.c_int),
+                ("device", ctypes.c_int)]
+
+
+_lib = None
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_F = ctypes.c_float
+_U64 = ctypes.c_uint64
+
+
+def load_library(path: str | None = None):
+    """Load libdsd.so (once) and declare the C signatures."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = path or LIB_PATH
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: build the CUDA library first "
+                           "(python -c 'import __graft_entry__ as g; g.build()')")
+    lib = ctypes.CDLL(path)
+    sig = {
+        "dsd_create": (_I, [ctypes.POINTER(dsd_config), ctypes.POINTER(_P)]),
+        "dsd_destroy": (_I, [_P]),
+        "dsd_last_error": (ctypes.c_char_p, [_P]),
+        "dsd_sync_status": (_I, [_P, _P]),
+        "dsd_workspace_bytes": (ctypes.c_size_t, [_P]),
+        "dsd_launch_count": (_U64, [_P]),
+        "dsd_propose": (_I, [_P, _I, _P, _P, _P, _P, _P, _P, _F, _U64, _P, _P, _P, _P, _P]),
+        "dsd_schedule": (_I, [_P, _I, _P, _P, _I, _P, _P, _P]),
+        "dsd_verify": (_I, [_P, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _F, _U64, _P, _P, _P]),
+        "dsd_cycle": (_I, [_P, _I, _P, _P, _P, _P, _P, _P, _P, _P, _I, _F, _U64,
+                           _P, _P, _P, _P, _P, _P, _P, _P, _P]),
+        "dsd_cycle_host": (_I, [_P, _I, _P, _P, _P, _P, _P, _P, _P, _P, _I, _F, _U64,
+                                _P, _P, _P, _P, _P]),
+        "dsd_overlap": (_I, [_P, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = lib
+    return lib
+
+
+def _ptr(x):
+    """Device/host pointer of a tensor, an int address, or None (NULL)."""
+    if x is None:
+        return None
+    if isinstance(x, torch.Tensor):
+        if not x.is_contiguous():
+            raise ValueError("tensor arguments must be contiguous")
+        return x.data_ptr()
+    return int(x)
+
+
+def _stream(stream, device):
+    if stream is None:
+        return torch.cuda.current_stream(device).cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _check(ctx, rc):
+    if rc != DSD_OK:
+        msg = load_library().dsd_last_error(ctx).decode(errors="replace") if ctx else ""
+        raise DsdError(rc, msg)
+
+
+# ------------------------------------------------------------ C-named calls
+
+def dsd_create(V, rank, gamma, R_max, dtype="bf16", act="none", bias_at_first=True,
+               engine="auto", device=0):
+    lib = load_library()
+    cfg = dsd_config(V, rank, gamma, R_max, DTYPES[dtype], ACTS[act], int(bool(bias_at_first)),
+                     ENGINES[engine], device)
+    out = _P()
+    rc = lib.dsd_create(ctypes.byref(cfg), ctypes.byref(out))
+    if rc != DSD_OK:
+        raise DsdError(rc, "dsd_create")
+    return out
+
+
+def dsd_destroy(ctx):
+    return load_library().dsd_destroy(ctx)
+
+
+def dsd_sync_status(ctx, stream=None, device=0):
+    return load_library().dsd_sync_status(ctx, _stream(stream, device))
+
+
+def dsd_propose(ctx, R, U, E, W, conf, prev_tok, req_id, temperature, seed, tokens, lse_q,
+                logit_at_tok, survival, stream=None, device=0):
+    _check(ctx, load_library().dsd_propose(
+        ctx, R, _ptr(U), _ptr(E), _ptr(W), _ptr(conf), _ptr(prev_tok), _ptr(req_id),
+        float(temperature), int(seed) & (2 ** 64 - 1), _ptr(tokens), _ptr(lse_q),
+        _ptr(logit_at_tok), _ptr(survival), _stream(stream, device)))
+
+
+def dsd_schedule(ctx, R, survival, sps, n_sps, keep_len, theta_B, stream=None, device=0):
+    _check(ctx, load_library().dsd_schedule(
+        ctx, R, _ptr(survival), _ptr(sps), int(n_sps), _ptr(keep_len), _ptr(theta_B),
+        _stream(stream, device)))
+
+
+def dsd_verify(ctx, R, P, U, E, W, prev_tok, tokens, lse_q, logit_at_tok, keep_len, req_id,
+               temperature, seed, accept_len, next_token, stream=None, device=0):
+    _check(ctx, load_library().dsd_verify(
+        ctx, R, _ptr(P), _ptr(U), _ptr(E), _ptr(W), _ptr(prev_tok), _ptr(tokens), _ptr(lse_q),
+        _ptr(logit_at_tok), _ptr(keep_len), _ptr(req_id), float(temperature),
+        int(seed) & (2 ** 64 - 1), _ptr(accept_len), _ptr(next_token), _stream(stream, device)))
+
+
+def dsd_cycle(ctx, R, U, E, W, conf, prev_tok, req_id, P, sps, n_sps, temperature, seed, tokens,
+              lse_q, logit_at_tok, survival, keep_len, theta_B, accept_len, next_token,
+              stream=None, device=0):
+    _check(ctx, load_library().dsd_cycle(
+        ctx, R, _ptr(U), _ptr(E), _ptr(W), _ptr(conf), _ptr(prev_tok), _ptr(req_id), _ptr(P),
+        _ptr(sps), int(n_sps), float(temperature), int(seed) & (2 ** 64 - 1), _ptr(tokens),
+        _ptr(lse_q), _ptr(logit_at_tok), _ptr(survival), _ptr(keep_len), _ptr(theta_B),
+        _ptr(accept_len), _ptr(next_token), _stream(stream, device)))
+
+
+def dsd_cycle_host(ctx, R, U_host, E, W, conf_host, prev_tok_host, req_id_host, P_host, sps,
+                   n_sps, temperature, seed, tokens_host, keep_len_host, accept_len_host,
+                   next_token_host, stream=None, device=0):
+    _check(ctx, load_library().dsd_cycle_host(
+        ctx, R, _ptr(U_host), _ptr(E), _ptr(W), _ptr(conf_host), _ptr(prev_tok_host),
+        _ptr(req_id_host), _ptr(P_host), _ptr(sps), int(n_sps), float(temperature),
+        int(seed) & (2 ** 64 - 1), _ptr(tokens_host), _ptr(keep_len_host),
+        _ptr(accept_len_host), _ptr(next_token_host), _stream(stream, device)))
+
+
+def dsd_overlap(ctx, N, P_logits, Q_logits, valid_len, a, l1, tau, accept_rate, mean_tau,
+                stream=None, device=0):
+    _check(ctx, load_library().dsd_overlap(
+        ctx, N, _ptr(P_logits), _ptr(Q_logits), _ptr(valid_len), _ptr(a), _ptr(l1), _ptr(tau),
+        _ptr(accept_rate), _ptr(mean_tau), _stream(stream, device)))
+
+
+# ------------------------------------------------------------ convenience
+
+class Context:
+    """One library context bound to one GPU.  Allocates outputs with torch;
+    all computation happens in libdsd.so."""
+
+    def __init__(self, V, rank, gamma, R_max, dtype="bf16", act="none", bias_at_first=True,
+                 engine="auto", device=0):
+        if not torch.cuda.is_available():
+            raise RuntimeError("no CUDA device: the DSpark hot path has no CPU fallback")
+        self.V, self.rank, self.gamma, self.R_max = V, rank, gamma, R_max
+        self.dtype, self.device = dtype, device
+        self.torch_dtype = TORCH_DTYPES[dtype]
+        self._dev = torch.device("cuda", device)
+        self.handle = dsd_create(V, rank, gamma, R_max, dtype, act, bias_at_first, engine, device)
+
+    def close(self):
+        if self.handle:
+            dsd_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+    def workspace_bytes(self):
+        return load_library().dsd_workspace_bytes(self.handle)
+
+    def launch_count(self):
+        return int(load_library().dsd_launch_count(self.handle))
+
+    def sync_status(self, stream=None):
+        return dsd_sync_status(self.handle, stream, self.device)
+
+    def _empty(self, shape, dtype):
+        return torch.empty(shape, dtype=dtype, device=self._dev)
+
+    def _check_in(self, name, t, dtype=None):
+        if t is None:
+            return
+        if not isinstance(t, torch.Tensor) or t.device != self._dev:
+            raise ValueError(f"{name} must be a tensor on {self._dev}")
+        if dtype is not None and t.dtype != dtype:
+            raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+
+    def propose(self, U, E, W, conf, prev_tok, req_id=None, temperature=0.0, seed=0,
+                out=None, stream=None):
+        R = U.shape[0]
+        for n, t in (("U", U), ("E", E), ("W", W)):
+            self._check_in(n, t, self.torch_dtype)
+        self._check_in("conf", conf, torch.float32)
+        self._check_in("prev_tok", prev_tok, torch.int32)
+        self._check_in("req_id", req_id, torch.int32)
+        G = self.gamma
+        o = out or dict(tokens=self._empty((R, G), torch.int32),
+                        lse_q=self._empty((R, G), torch.float32),
+                        logit_at_tok=self._empty((R, G), torch.float32),
+                        survival=self._empty((R, G), torch.float32))
+        dsd_propose(self.handle, R, U, E, W, conf, prev_tok, req_id, temperature, seed,
+                    o["tokens"], o["lse_q"], o["logit_at_tok"], o["survival"], stream, self.device)
+        return o
+
+    def schedule(self, survival, sps, out=None, stream=None):
+        R = survival.shape[0]
+        self._check_in("survival", survival, torch.float32)
+        self._check_in("sps", sps, torch.float32)
+        o = out or dict(keep_len=self._empty((R,), torch.int32),
+                        theta_B=self._empty((2,), torch.float32))
+        dsd_schedule(self.handle, R, survival, sps, sps.numel(), o["keep_len"], o["theta_B"],
+                     stream, self.device)
+        return o
+
+    def verify(self, P, tokens, keep_len, U=None, E=None, W=None, prev_tok=None, lse_q=None,
+               logit_at_tok=None, req_id=None, temperature=0.0, seed=0, out=None, stream=None):
+        R = P.shape[0]
+        self._check_in("P", P, self.torch_dtype)
+        self._check_in("tokens", tokens, torch.int32)
+        self._check_in("keep_len", keep_len, torch.int32)
+        o = out or dict(accept_len=self._empty((R,), torch.int32),
+                        next_token=self._empty((R,), torch.int32))
+        dsd_verify(self.handle, R, P, U, E, W, prev_tok, tokens, lse_q, logit_at_tok, keep_len,
+                   req_id, temperature, seed, o["accept_len"], o["next_token"], stream,
+                   self.device)
+        return o
+
+    def cycle_outputs(self, R):
+        G = self.gamma
+        return dict(tokens=self._empty((R, G), torch.int32),
+                    lse_q=self._empty((R, G), torch.float32),
+                    logit_at_tok=self._empty((R, G), torch.float32),
+                    survival=self._empty((R, G), torch.float32),
+                    keep_len=self._empty((R,), torch.int32),
+                    theta_B=self._empty((2,), torch.float32),
+                    accept_len=self._empty((R,), torch.int32),
+                    next_token=self._empty((R,), torch.int32))
+
+    def cycle(self, U, E, W, conf, prev_tok, P, sps, req_id=None, temperature=0.0, seed=0,
+              out=None, stream=None):
+        R = U.shape[0]
+        o = out or self.cycle_outputs(R)
+        dsd_cycle(self.handle, R, U, E, W, conf, prev_tok, req_id, P, sps, sps.numel(),
+                  temperature, seed, o["tokens"], o["lse_q"], o["logit_at_tok"], o["survival"],
+                  o["keep_len"], o["theta_B"], o["accept_len"], o["next_token"], stream,
+                  self.device)
+        return o
+
+    def cycle_host(self, U_host, E, W, conf_host, prev_tok_host, P_host, sps, req_id_host=None,
+                   temperature=0.0, seed=0, out=None, stream=None):
+        """One cycle from host tensors (pinned for asynchronous copies)."""
+        R = U_host.shape[0]
+        G = self.gamma
+        o = out or dict(tokens=torch.empty((R, G), dtype=torch.int32, pin_memory=True),
+                        keep_len=torch.empty((R,), dtype=torch.int32, pin_memory=True),
+                        accept_len=torch.empty((R,), dtype=torch.int32, pin_memory=True),
+                        next_token=torch.empty((R,), dtype=torch.int32, pin_memory=True))
+        dsd_cycle_host(self.handle, R, U_host, E, W, conf_host, prev_tok_host, req_id_host,
+                       P_host, sps, sps.numel(), temperature, seed, o["tokens"], o["keep_len"],
+                       o["accept_len"], o["next_token"], stream, self.device)
+        return o
+
+    def overlap(self, P_logits, Q_logits, valid_len, out=None, stream=None):
+        N = P_logits.shape[0]
+        self._check_in("P_logits", P_logits, self.torch_dtype)
+        self._check_in("Q_logits", Q_logits, self.torch_dtype)
+        self._check_in("valid_len", valid_len, torch.int32)
+        G = self.gamma
+        o = out or dict(a=self._empty((N, G), torch.float32), l1=self._empty((N, G), torch.float32),
+                        tau=self._empty((N,), torch.float32),
+                        accept_rate=self._empty((G,), torch.float32),
+                        mean_tau=self._empty((1,), torch.float32))
+        dsd_overlap(self.handle, N, P_logits, Q_logits, valid_len, o["a"], o["l1"], o["tau"],
+                    o["accept_rate"], o["mean_tau"], stream, self.device)
+        return o

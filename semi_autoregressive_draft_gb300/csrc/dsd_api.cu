@@ -1,0 +1,419 @@
+// C-ABI entry points (include/dsd.h): context and workspace management,
+// host-side argument validation, engine dispatch.  No compute happens here;
+// every step of the path runs in the kernels of this directory.
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <new>
+
+#include "../../include/dsd.h"
+#include "dsd_internal.h"
+
+using namespace dsd;
+
+struct dsd_ctx : public dsd::Ctx {};
+
+namespace {
+
+int fail(dsd_ctx* ctx, int code, const char* fmt, ...) {
+  if (ctx) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(ctx->err, sizeof(ctx->err), fmt, ap);
+    va_end(ap);
+  }
+  return code;
+}
+
+int cuda_fail(dsd_ctx* ctx, cudaError_t e, const char* where) {
+  return fail(ctx, DSD_ERR_CUDA, "%s: %s", where, cudaGetErrorString(e));
+}
+
+bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Carve the workspace; with base == nullptr only computes the size.
+size_t carve(dsd_ctx* c, unsigned char* base) {
+  const int Rm = c->cfg.R_max, G = c->cfg.gamma;
+  size_t off = 0;
+  auto take = [&](size_t bytes) -> unsigned char* {
+    unsigned char* p = base ? base + off : nullptr;
+    off = align_up(off + bytes, 256);
+    return p;
+  };
+  Workspace w{};
+  w.status = reinterpret_cast<int*>(take(sizeof(int) * 4));
+  w.counters = reinterpret_cast<unsigned int*>(take(sizeof(unsigned int) * 16));
+  w.keys = reinterpret_cast<unsigned long long*>(take(sizeof(unsigned long long) * (size_t)G * Rm));
+  w.lse_parts = reinterpret_cast<float2*>(take(sizeof(float2) * (size_t)G * c->n_part * Rm));
+  w.sched_B = reinterpret_cast<int*>(take(sizeof(int) * 4));
+  w.rows = reinterpret_cast<int2*>(take(sizeof(int2) * (size_t)Rm * (G + 1)));
+  w.vparts = reinterpret_cast<RowPart*>(take(sizeof(RowPart) * (size_t)Rm * (G + 1) * kVerifySplits));
+  w.rej_list = reinterpret_cast<int*>(take(sizeof(int) * (size_t)Rm));
+  w.rej_k = reinterpret_cast<int*>(take(sizeof(int) * 2 * (size_t)Rm));  // + row offsets
+  w.rej_lseP = reinterpret_cast<float*>(take(sizeof(float) * (size_t)Rm));
+  w.res_keys = reinterpret_cast<unsigned long long*>(take(sizeof(unsigned long long) * 2 * (size_t)Rm));
+  w.res_sums = reinterpret_cast<float*>(take(sizeof(float) * 2 * (size_t)Rm));
+  w.ov_parts = reinterpret_cast<float*>(take(sizeof(float) * 64));
+  if (base) c->ws = w;
+  return off;
+}
+
+int check_ctx(dsd_ctx* ctx) {
+  if (!ctx) return DSD_ERR_ARG;
+  ctx->err[0] = 0;
+  cudaError_t e = cudaSetDevice(ctx->cfg.device);
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "cudaSetDevice");
+  return DSD_OK;
+}
+
+int check_table(dsd_ctx* ctx, const void* p, const char* name) {
+  if (!p) return fail(ctx, DSD_ERR_ARG, "%s is NULL", name);
+  if (!aligned16(p)) return fail(ctx, DSD_ERR_ALIGN, "%s is not 16-byte aligned", name);
+  return DSD_OK;
+}
+
+int check_R(dsd_ctx* ctx, int R) {
+  if (R < 0) return fail(ctx, DSD_ERR_ARG, "R = %d < 0", R);
+  if (R > ctx->cfg.R_max) return fail(ctx, DSD_ERR_SHAPE, "R = %d > R_max = %d", R, ctx->cfg.R_max);
+  return DSD_OK;
+}
+
+int check_temperature(dsd_ctx* ctx, float T) {
+  if (!(T >= 0.f) || T != T || T > 3.0e38f)
+    return fail(ctx, DSD_ERR_ARG, "temperature must be finite and >= 0");
+  return DSD_OK;
+}
+
+bool use_tc(const dsd_ctx* ctx, int R) {
+  if (ctx->cfg.dtype != DSD_BF16) return false;
+  if (ctx->cfg.engine == DSD_ENGINE_SIMT) return false;
+  if (ctx->cfg.engine == DSD_ENGINE_TCGEN05) return true;
+  return R >= 16 && ctx->cfg.rank % 64 == 0;
+}
+
+}  // namespace
+
+namespace dsd {
+int simt_grid(const Ctx& ctx, int V);
+cudaError_t launch_propose_finalize_n(const Ctx& ctx, const ProposeArgs& a, int n_used,
+                                      cudaStream_t s);
+int tc_supported(const Ctx& ctx, char* why, size_t why_len);
+int tc_grid(const Ctx& ctx);
+}  // namespace dsd
+
+extern "C" {
+
+int dsd_create(const dsd_config* cfg, dsd_ctx** out) {
+  if (!cfg || !out) return DSD_ERR_ARG;
+  if (cfg->V < 8 || cfg->V % 8 != 0) return DSD_ERR_ALIGN;
+  const bool rank_ok = (cfg->rank % 64 == 0 && cfg->rank <= 256) ||
+                       (cfg->rank > 0 && cfg->rank <= 64 && cfg->rank % 8 == 0);
+  if (!rank_ok) return DSD_ERR_SHAPE;
+  if (cfg->gamma < 1 || cfg->gamma > kMaxGamma) return DSD_ERR_SHAPE;
+  if (cfg->R_max < 1 || (long long)cfg->R_max * cfg->gamma > kMaxSchedItems) return DSD_ERR_SHAPE;
+  if (cfg->dtype != DSD_F32 && cfg->dtype != DSD_BF16) return DSD_ERR_DTYPE;
+  if (cfg->act != DSD_ACT_NONE && cfg->act != DSD_ACT_SILU) return DSD_ERR_ARG;
+  if (cfg->engine < DSD_ENGINE_AUTO || cfg->engine > DSD_ENGINE_TCGEN05) return DSD_ERR_ARG;
+  if (cfg->engine == DSD_ENGINE_TCGEN05 && cfg->dtype != DSD_BF16) return DSD_ERR_DTYPE;
+
+  int ndev = 0;
+  if (cudaGetDeviceCount(&ndev) != cudaSuccess || cfg->device < 0 || cfg->device >= ndev)
+    return DSD_ERR_UNSUPPORTED;
+  if (cudaSetDevice(cfg->device) != cudaSuccess) return DSD_ERR_CUDA;
+  cudaDeviceProp prop;
+  if (cudaGetDeviceProperties(&prop, cfg->device) != cudaSuccess) return DSD_ERR_CUDA;
+  if (prop.major != 10) return DSD_ERR_UNSUPPORTED;
+
+  dsd_ctx* c = new (std::nothrow) dsd_ctx();
+  if (!c) return DSD_ERR_ARG;
+  memset(static_cast<dsd::Ctx*>(c), 0, sizeof(dsd::Ctx));
+  c->cfg = Config{cfg->V, cfg->rank, cfg->gamma, cfg->R_max, cfg->dtype,
+                  cfg->act, cfg->bias_at_first ? 1 : 0, cfg->engine, cfg->device};
+  c->num_sms = prop.multiProcessorCount;
+  c->n_part = 2 * c->num_sms;
+  const size_t bytes = carve(c, nullptr);
+  void* base = nullptr;
+  if (cudaMalloc(&base, bytes) != cudaSuccess) {
+    delete c;
+    return DSD_ERR_CUDA;
+  }
+  if (cudaMemset(base, 0, bytes) != cudaSuccess) {
+    cudaFree(base);
+    delete c;
+    return DSD_ERR_CUDA;
+  }
+  c->ws_base = base;
+  c->ws_bytes = bytes;
+  carve(c, static_cast<unsigned char*>(base));
+  *out = c;
+  return DSD_OK;
+}
+
+int dsd_destroy(dsd_ctx* ctx) {
+  if (!ctx) return DSD_OK;
+  cudaSetDevice(ctx->cfg.device);
+  if (ctx->ws_base) cudaFree(ctx->ws_base);
+  if (ctx->stage_base) cudaFree(ctx->stage_base);
+  delete ctx;
+  return DSD_OK;
+}
+
+const char* dsd_last_error(const dsd_ctx* ctx) { return ctx ? ctx->err : "null context"; }
+
+size_t dsd_workspace_bytes(const dsd_ctx* ctx) { return ctx ? ctx->ws_bytes : 0; }
+
+uint64_t dsd_launch_count(const dsd_ctx* ctx) { return ctx ? ctx->launches : 0; }
+
+int dsd_sync_status(dsd_ctx* ctx, void* stream) {
+  int rc = check_ctx(ctx);
+  if (rc) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "cudaStreamSynchronize");
+  int st = 0;
+  e = cudaMemcpy(&st, ctx->ws.status, sizeof(int), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "read status");
+  if (st != 0) {
+    e = cudaMemset(ctx->ws.status, 0, sizeof(int));
+    if (e != cudaSuccess) return cuda_fail(ctx, e, "clear status");
+    fail(ctx, st, "device reported status %d", st);
+  }
+  return st;
+}
+
+int dsd_propose(dsd_ctx* ctx, int R, const void* U, const void* E, const void* W,
+                const float* conf, const int32_t* prev_tok, const uint32_t* req_id,
+                float temperature, uint64_t seed, int32_t* tokens, float* lse_q,
+                float* logit_at_tok, float* survival, void* stream) {
+  int rc = check_ctx(ctx);
+  if (rc) return rc;
+  if ((rc = check_R(ctx, R))) return rc;
+  if ((rc = check_temperature(ctx, temperature))) return rc;
+  if (R == 0) return DSD_OK;
+  if ((rc = check_table(ctx, U, "U")) || (rc = check_table(ctx, E, "E")) ||
+      (rc = check_table(ctx, W, "W")))
+    return rc;
+  if (!conf || !prev_tok || !tokens || !lse_q || !logit_at_tok || !survival)
+    return fail(ctx, DSD_ERR_ARG, "dsd_propose: NULL argument");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  ProposeArgs a{};
+  a.R = R;
+  a.V = ctx->cfg.V;
+  a.rank = ctx->cfg.rank;
+  a.gamma = ctx->cfg.gamma;
+  a.dtype = ctx->cfg.dtype;
+  a.act = ctx->cfg.act;
+  a.bias_at_first = ctx->cfg.bias_at_first;
+  a.U = U;
+  a.E = E;
+  a.W = W;
+  a.conf = conf;
+  a.prev_tok = prev_tok;
+  a.req_id = req_id;
+  a.temperature = temperature;
+  a.seed = seed;
+  a.tokens = tokens;
+  a.lse_q = lse_q;
+  a.logit_at_tok = logit_at_tok;
+  a.survival = survival;
+  cudaError_t e;
+  int n_used;
+  char why[256];
+  const bool tc_ok = tc_supported(*ctx, why, sizeof(why)) != 0;
+  if (ctx->cfg.engine == DSD_ENGINE_TCGEN05 && !tc_ok)
+    return fail(ctx, DSD_ERR_UNSUPPORTED, "%s", why);
+  if (use_tc(ctx, R) && tc_ok) {
+    e = launch_propose_tc(*ctx, a, s);
+    n_used = tc_grid(*ctx);
+  } else {
+    e = launch_propose_simt(*ctx, a, s);
+    n_used = simt_grid(*ctx, a.V);
+  }
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "propose launch");
+  e = launch_propose_finalize_n(*ctx, a, n_used, s);
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "propose finalize launch");
+  return DSD_OK;
+}
+
+int dsd_schedule(dsd_ctx* ctx, int R, const float* survival, const float* sps, int n_sps,
+                 int32_t* keep_len, float* theta_B, void* stream) {
+  int rc = check_ctx(ctx);
+  if (rc) return rc;
+  if ((rc = check_R(ctx, R))) return rc;
+  if (R == 0) return DSD_OK;
+  if (!survival || !sps || !keep_len) return fail(ctx, DSD_ERR_ARG, "dsd_schedule: NULL argument");
+  if (n_sps < 1) return fail(ctx, DSD_ERR_ARG, "n_sps = %d", n_sps);
+  if (R > n_sps) return fail(ctx, DSD_ERR_CAPACITY, "R = %d exceeds the SPS table (%d)", R, n_sps);
+  cudaError_t e = launch_schedule(*ctx, R, survival, sps, n_sps, keep_len, theta_B,
+                                  static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "schedule launch");
+  return DSD_OK;
+}
+
+int dsd_verify(dsd_ctx* ctx, int R, const void* P, const void* U, const void* E, const void* W,
+               const int32_t* prev_tok, const int32_t* tokens, const float* lse_q,
+               const float* logit_at_tok, const int32_t* keep_len, const uint32_t* req_id,
+               float temperature, uint64_t seed, int32_t* accept_len, int32_t* next_token,
+               void* stream) {
+  int rc = check_ctx(ctx);
+  if (rc) return rc;
+  if ((rc = check_R(ctx, R))) return rc;
+  if ((rc = check_temperature(ctx, temperature))) return rc;
+  if (R == 0) return DSD_OK;
+  if ((rc = check_table(ctx, P, "P"))) return rc;
+  if (!tokens || !keep_len || !accept_len || !next_token)
+    return fail(ctx, DSD_ERR_ARG, "dsd_verify: NULL argument");
+  if (temperature > 0.f) {
+    if ((rc = check_table(ctx, U, "U")) || (rc = check_table(ctx, E, "E")) ||
+        (rc = check_table(ctx, W, "W")))
+      return rc;
+    if (!prev_tok || !lse_q || !logit_at_tok)
+      return fail(ctx, DSD_ERR_ARG, "dsd_verify: sampled mode needs prev_tok, lse_q, logit_at_tok");
+  }
+  VerifyArgs a{};
+  a.R = R;
+  a.V = ctx->cfg.V;
+  a.rank = ctx->cfg.rank;
+  a.gamma = ctx->cfg.gamma;
+  a.dtype = ctx->cfg.dtype;
+  a.act = ctx->cfg.act;
+  a.bias_at_first = ctx->cfg.bias_at_first;
+  a.P = P;
+  a.U = U;
+  a.E = E;
+  a.W = W;
+  a.prev_tok = prev_tok;
+  a.tokens = tokens;
+  a.lse_q = lse_q;
+  a.logit_at_tok = logit_at_tok;
+  a.keep_len = keep_len;
+  a.req_id = req_id;
+  a.temperature = temperature;
+  a.seed = seed;
+  a.accept_len = accept_len;
+  a.next_token = next_token;
+  cudaError_t e = launch_verify(*ctx, a, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "verify launch");
+  return DSD_OK;
+}
+
+int dsd_cycle(dsd_ctx* ctx, int R, const void* U, const void* E, const void* W, const float* conf,
+              const int32_t* prev_tok, const uint32_t* req_id, const void* P, const float* sps,
+              int n_sps, float temperature, uint64_t seed, int32_t* tokens, float* lse_q,
+              float* logit_at_tok, float* survival, int32_t* keep_len, float* theta_B,
+              int32_t* accept_len, int32_t* next_token, void* stream) {
+  int rc = dsd_propose(ctx, R, U, E, W, conf, prev_tok, req_id, temperature, seed, tokens, lse_q,
+                       logit_at_tok, survival, stream);
+  if (rc) return rc;
+  rc = dsd_schedule(ctx, R, survival, sps, n_sps, keep_len, theta_B, stream);
+  if (rc) return rc;
+  return dsd_verify(ctx, R, P, U, E, W, prev_tok, tokens, lse_q, logit_at_tok, keep_len, req_id,
+                    temperature, seed, accept_len, next_token, stream);
+}
+
+int dsd_cycle_host(dsd_ctx* ctx, int R, const void* U_host, const void* E, const void* W,
+                   const float* conf_host, const int32_t* prev_tok_host,
+                   const uint32_t* req_id_host, const void* P_host, const float* sps, int n_sps,
+                   float temperature, uint64_t seed, int32_t* tokens_host, int32_t* keep_len_host,
+                   int32_t* accept_len_host, int32_t* next_token_host, void* stream) {
+  int rc = check_ctx(ctx);
+  if (rc) return rc;
+  if ((rc = check_R(ctx, R))) return rc;
+  if (R == 0) return DSD_OK;
+  if (!U_host || !conf_host || !prev_tok_host || !P_host || !tokens_host || !keep_len_host ||
+      !accept_len_host || !next_token_host)
+    return fail(ctx, DSD_ERR_ARG, "dsd_cycle_host: NULL argument");
+  const int Rm = ctx->cfg.R_max, G = ctx->cfg.gamma;
+  const size_t V = (size_t)ctx->cfg.V;
+  const size_t esz = ctx->cfg.dtype == DSD_BF16 ? 2 : 4;
+  // staging layout: U, P, conf, prev, req, tokens, lse, logit, surv, keep, theta, acc, next
+  size_t off = 0;
+  size_t o_U = off; off = align_up(off + (size_t)Rm * G * V * esz, 256);
+  size_t o_P = off; off = align_up(off + (size_t)Rm * (G + 1) * V * esz, 256);
+  size_t o_conf = off; off = align_up(off + sizeof(float) * Rm * G, 256);
+  size_t o_prev = off; off = align_up(off + sizeof(int32_t) * Rm, 256);
+  size_t o_req = off; off = align_up(off + sizeof(uint32_t) * Rm, 256);
+  size_t o_tok = off; off = align_up(off + sizeof(int32_t) * Rm * G, 256);
+  size_t o_lse = off; off = align_up(off + sizeof(float) * Rm * G, 256);
+  size_t o_lg = off; off = align_up(off + sizeof(float) * Rm * G, 256);
+  size_t o_sv = off; off = align_up(off + sizeof(float) * Rm * G, 256);
+  size_t o_keep = off; off = align_up(off + sizeof(int32_t) * Rm, 256);
+  size_t o_th = off; off = align_up(off + sizeof(float) * 2, 256);
+  size_t o_acc = off; off = align_up(off + sizeof(int32_t) * Rm, 256);
+  size_t o_nx = off; off = align_up(off + sizeof(int32_t) * Rm, 256);
+  if (!ctx->stage_base) {
+    cudaError_t e = cudaMalloc(&ctx->stage_base, off);
+    if (e != cudaSuccess) {
+      ctx->stage_base = nullptr;
+      return cuda_fail(ctx, e, "staging cudaMalloc");
+    }
+    ctx->stage_bytes = off;
+  }
+  unsigned char* b = static_cast<unsigned char*>(ctx->stage_base);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  const size_t G1 = (size_t)G + 1;
+#define DSD_CPY(dst, src, bytes, kind)                                   \
+  do {                                                                   \
+    e = cudaMemcpyAsync((dst), (src), (bytes), (kind), s);               \
+    if (e != cudaSuccess) return cuda_fail(ctx, e, "cudaMemcpyAsync");   \
+  } while (0)
+  DSD_CPY(b + o_U, U_host, (size_t)R * G * V * esz, cudaMemcpyHostToDevice);
+  DSD_CPY(b + o_P, P_host, (size_t)R * G1 * V * esz, cudaMemcpyHostToDevice);
+  DSD_CPY(b + o_conf, conf_host, sizeof(float) * R * G, cudaMemcpyHostToDevice);
+  DSD_CPY(b + o_prev, prev_tok_host, sizeof(int32_t) * R, cudaMemcpyHostToDevice);
+  if (req_id_host) DSD_CPY(b + o_req, req_id_host, sizeof(uint32_t) * R, cudaMemcpyHostToDevice);
+  rc = dsd_cycle(ctx, R, b + o_U, E, W, reinterpret_cast<float*>(b + o_conf),
+                 reinterpret_cast<int32_t*>(b + o_prev),
+                 req_id_host ? reinterpret_cast<uint32_t*>(b + o_req) : nullptr, b + o_P, sps,
+                 n_sps, temperature, seed, reinterpret_cast<int32_t*>(b + o_tok),
+                 reinterpret_cast<float*>(b + o_lse), reinterpret_cast<float*>(b + o_lg),
+                 reinterpret_cast<float*>(b + o_sv), reinterpret_cast<int32_t*>(b + o_keep),
+                 reinterpret_cast<float*>(b + o_th), reinterpret_cast<int32_t*>(b + o_acc),
+                 reinterpret_cast<int32_t*>(b + o_nx), stream);
+  if (rc) return rc;
+  DSD_CPY(tokens_host, b + o_tok, sizeof(int32_t) * R * G, cudaMemcpyDeviceToHost);
+  DSD_CPY(keep_len_host, b + o_keep, sizeof(int32_t) * R, cudaMemcpyDeviceToHost);
+  DSD_CPY(accept_len_host, b + o_acc, sizeof(int32_t) * R, cudaMemcpyDeviceToHost);
+  DSD_CPY(next_token_host, b + o_nx, sizeof(int32_t) * R, cudaMemcpyDeviceToHost);
+#undef DSD_CPY
+  e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "cudaStreamSynchronize");
+  return DSD_OK;
+}
+
+int dsd_overlap(dsd_ctx* ctx, int N, const void* P_logits, const void* Q_logits,
+                const int32_t* valid_len, float* a, float* l1, float* tau, float* accept_rate,
+                float* mean_tau, void* stream) {
+  int rc = check_ctx(ctx);
+  if (rc) return rc;
+  if (N < 0) return fail(ctx, DSD_ERR_ARG, "N = %d < 0", N);
+  if (!accept_rate || !mean_tau) return fail(ctx, DSD_ERR_ARG, "dsd_overlap: NULL argument");
+  if (N > 0) {
+    if ((rc = check_table(ctx, P_logits, "P_logits")) || (rc = check_table(ctx, Q_logits, "Q_logits")))
+      return rc;
+    if (!valid_len || !a || !l1 || !tau) return fail(ctx, DSD_ERR_ARG, "dsd_overlap: NULL argument");
+    if ((long long)N * ctx->cfg.gamma > 0x7fffffffLL) return fail(ctx, DSD_ERR_SHAPE, "N too large");
+  }
+  OverlapArgs o{};
+  o.N = N;
+  o.V = ctx->cfg.V;
+  o.gamma = ctx->cfg.gamma;
+  o.dtype = ctx->cfg.dtype;
+  o.P = P_logits;
+  o.Q = Q_logits;
+  o.valid_len = valid_len;
+  o.a = a;
+  o.l1 = l1;
+  o.tau = tau;
+  o.accept_rate = accept_rate;
+  o.mean_tau = mean_tau;
+  cudaError_t e = launch_overlap(*ctx, o, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "overlap launch");
+  return DSD_OK;
+}
+
+}  // extern "C"

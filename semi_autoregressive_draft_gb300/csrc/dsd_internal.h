@@ -1,0 +1,133 @@
+// Internal declarations shared by the C-ABI layer and the kernel files.
+#pragma once
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime.h>
+
+namespace dsd {
+
+constexpr int kActNone = 0;
+constexpr int kActSilu = 1;
+
+constexpr int kMaxGamma = 16;
+constexpr int kMaxSchedItems = 4096;  // R_max * gamma
+constexpr int kVerifySplits = 8;      // V chunks per verified row
+
+// Status codes (mirror enum dsd_status in include/dsd.h).
+constexpr int kOk = 0;
+constexpr int kErrArg = -1;
+constexpr int kErrNonfinite = -6;
+constexpr int kErrTimeout = -7;
+
+// Partial result of one CTA over a slice of the vocabulary for one row:
+// the online log-sum-exp state (base 2) and a packed argmax key.
+struct RowPart {
+  float m, s;
+  unsigned long long key;
+};
+
+// Device workspace, carved out of one allocation at context creation.
+struct Workspace {
+  int* status;                  // first device-side error of the calls so far
+  unsigned int* counters;       // [16] tickets / barrier counters (zeroed per call)
+  unsigned long long* keys;     // [gamma][R_max] argmax keys of the propose steps
+  float2* lse_parts;            // [gamma][n_part][R_max] (m, s) partials
+  int* sched_B;                 // [1] verify batch B* of the last schedule
+  int2* rows;                   // [R_max*(gamma+1)] verify rows (r, t)
+  RowPart* vparts;              // [R_max*(gamma+1)][kVerifySplits]
+  int* rej_list;                // [R_max] requests with a rejection (sampled verify)
+  int* rej_k;                   // [R_max] rejection position per request
+  float* rej_lseP;              // [R_max] target log-normaliser at the rejected row
+  unsigned long long* res_keys; // [2][R_max] residual key, fallback key
+  float* res_sums;              // [2][R_max] sum of the residual, sum of p
+  float* ov_parts;              // scratch of the overlap kernels
+};
+
+struct Config {
+  int V, rank, gamma, R_max, dtype, act, bias_at_first, engine, device;
+};
+
+struct Ctx {
+  Config cfg;
+  int num_sms;
+  int n_part;                  // CTAs of a propose step (lse partial slots)
+  void* ws_base;
+  size_t ws_bytes;
+  Workspace ws;
+  // host-buffer staging for dsd_cycle_host (allocated on first use)
+  void* stage_base;
+  size_t stage_bytes;
+  char err[512];
+  mutable unsigned long long launches;  // kernels launched by this context
+};
+
+inline void count_launch(const Ctx& c, int n = 1) { c.launches += (unsigned long long)n; }
+
+// ----------------------------------------------------------------- launchers
+struct ProposeArgs {
+  int R, V, rank, gamma, dtype, act, bias_at_first;
+  const void* U;
+  const void* E;
+  const void* W;
+  const float* conf;
+  const int32_t* prev_tok;
+  const uint32_t* req_id;
+  float temperature;
+  uint64_t seed;
+  int32_t* tokens;
+  float* lse_q;
+  float* logit_at_tok;
+  float* survival;
+};
+
+cudaError_t launch_propose_simt(const Ctx& ctx, const ProposeArgs& a, cudaStream_t s);
+cudaError_t launch_propose_tc(const Ctx& ctx, const ProposeArgs& a, cudaStream_t s);
+cudaError_t launch_propose_finalize(const Ctx& ctx, const ProposeArgs& a, cudaStream_t s);
+
+cudaError_t launch_schedule(const Ctx& ctx, int R, const float* survival, const float* sps,
+                            int n_sps, int32_t* keep_len, float* theta_B, cudaStream_t s);
+
+struct VerifyArgs {
+  int R, V, rank, gamma, dtype, act, bias_at_first;
+  const void* P;
+  const void* U;
+  const void* E;
+  const void* W;
+  const int32_t* prev_tok;
+  const int32_t* tokens;
+  const float* lse_q;
+  const float* logit_at_tok;
+  const int32_t* keep_len;
+  const uint32_t* req_id;
+  float temperature;
+  uint64_t seed;
+  int32_t* accept_len;
+  int32_t* next_token;
+};
+
+cudaError_t launch_verify(const Ctx& ctx, const VerifyArgs& a, cudaStream_t s);
+
+struct OverlapArgs {
+  int N, V, gamma, dtype;
+  const void* P;
+  const void* Q;
+  const int32_t* valid_len;
+  float* a;
+  float* l1;
+  float* tau;
+  float* accept_rate;
+  float* mean_tau;
+};
+
+cudaError_t launch_overlap(const Ctx& ctx, const OverlapArgs& a, cudaStream_t s);
+
+// Swizzle mask for 16-byte chunks of a staged table row (see propose_simt.cu).
+inline int chunk_swizzle_mask(int chunks_per_row) {
+  if (chunks_per_row % 8 == 0) return 7;
+  if ((chunks_per_row & (chunks_per_row - 1)) == 0) return chunks_per_row - 1;
+  return 0;
+}
+
+}  // namespace dsd

@@ -1,0 +1,483 @@
+// CUDA-core path of the Markov-head bias projection (the GEMV path for small
+// batches and fp32 tables), used by dsd_propose (one launch per draft
+// position) and by dsd_verify's residual pass.
+//
+// Pages: "Qwen3.8-Flash-Next DSpark 训练实验", Baseline 架构 / Markov 顺序修正
+// (m_i = W_1[t_{i-1}], b_i = W_2 m_i, l_i = l_i^0 + b_i, argmax over the full
+// vocabulary); "DSpark 论文精读" 2.2 (x_j ~ Softmax(U_j + b)); "DeepSpec 训练全
+// 流程详解" 4.4 (residual resampling).
+//
+// Work split: the vocabulary is cut into 128-row tiles of W ([V, r] layout,
+// so a tile is one contiguous block of memory); CTAs stride over tiles.  A CTA
+// stages the W tile in shared memory (16-byte chunks XOR-swizzled by row so
+// that eight consecutive rows read by a quarter-warp hit distinct banks) and
+// the gathered rows m = act(E[prev]) of up to 16 requests in fp32.  Thread
+// (vg, half) owns vocabulary entry v0 + vg and 8 requests; it computes the 8
+// bias values from shared memory, adds U and folds the biased logit into a
+// running base-2 log-sum-exp and a packed argmax key.  The biased logits
+// never leave registers.  At the end the CTA reduces per request and
+// publishes one atomicMax key and one (m, s) partial per request.
+#include "dsd_common.cuh"
+
+namespace dsd {
+
+constexpr int kSimtThreads = 256;
+constexpr int kSimtTileV = 128;
+constexpr int kSimtRC = 16;   // requests per pass
+constexpr int kSimtRPT = 8;   // requests per thread
+
+enum SimtMode { kModeStep = 0, kModeResidual = 1 };
+
+struct SimtParams {
+  const void* U;
+  const void* E;
+  const void* W;
+  const void* P;                 // residual mode: target logits [R, gamma+1, V]
+  const int32_t* prev_tok;
+  const int32_t* tokens;         // residual mode: draft tokens [R, gamma]
+  const uint32_t* req_id;
+  const float* lse_q;            // residual mode
+  unsigned long long* keys;      // step: [gamma][R_max]; residual: [2][R_max]
+  float2* parts;                 // step: [gamma][n_part][R_max]
+  float* res_sums;               // residual: [2][R_max]
+  const int* rej_list;           // residual: request list
+  const int* rej_k;              // residual: rejection position per request
+  const float* rej_lseP;         // residual: target lse (natural) per request
+  const unsigned int* n_rej;     // residual: number of listed requests
+  int* status;
+  int R, R_max, V, rank, gamma, j, act, bias_at_first, swz_mask, n_part;
+  float inv_T;
+  int sampled;
+  uint32_t k0, k1;
+};
+
+template <typename T>
+__device__ __forceinline__ int unpack16(const uint4& q, float* w) {
+  if constexpr (sizeof(T) == 2) {
+    w[0] = bf16lo(q.x); w[1] = bf16hi(q.x); w[2] = bf16lo(q.y); w[3] = bf16hi(q.y);
+    w[4] = bf16lo(q.z); w[5] = bf16hi(q.z); w[6] = bf16lo(q.w); w[7] = bf16hi(q.w);
+    return 8;
+  } else {
+    w[0] = __uint_as_float(q.x); w[1] = __uint_as_float(q.y);
+    w[2] = __uint_as_float(q.z); w[3] = __uint_as_float(q.w);
+    return 4;
+  }
+}
+
+template <typename T, int MODE>
+__global__ void __launch_bounds__(kSimtThreads) simt_bias_kernel(SimtParams p) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  constexpr int epc = 16 / (int)sizeof(T);
+  const int rank = p.rank;
+  const int nch = rank / epc;
+  const int mstride = rank + 4;
+  unsigned char* Ws = smem;
+  float* ms = reinterpret_cast<float*>(smem + (size_t)kSimtTileV * nch * 16);
+
+  __shared__ int s_prev[kSimtRC];
+  __shared__ int s_req[kSimtRC];
+  __shared__ int s_row[kSimtRC];       // row of U (r*gamma + position)
+  __shared__ int s_bias[kSimtRC];
+  __shared__ float s_lseq[kSimtRC];
+  __shared__ float s_lsep[kSimtRC];
+  __shared__ uint32_t s_rid[kSimtRC];
+  __shared__ int s_pos[kSimtRC];
+  __shared__ Lse2 red_l[8][kSimtRPT];
+  __shared__ unsigned long long red_k[8][kSimtRPT];
+  __shared__ unsigned long long red_k2[8][kSimtRPT];
+  __shared__ float red_f[8][kSimtRPT];
+  __shared__ float red_f2[8][kSimtRPT];
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int vg = tid & (kSimtTileV - 1), half = tid >> 7;
+  const int ntiles = (p.V + kSimtTileV - 1) / kSimtTileV;
+  const T* U = static_cast<const T*>(p.U);
+  const T* E = static_cast<const T*>(p.E);
+  const T* W = static_cast<const T*>(p.W);
+  const T* P = static_cast<const T*>(p.P);
+
+  const int nreq = (MODE == kModeStep) ? p.R : (int)min(*p.n_rej, (unsigned)p.R);
+
+  for (int r0 = 0; r0 < nreq; r0 += kSimtRC) {
+    const int nr = min(kSimtRC, nreq - r0);
+    __syncthreads();
+    if (tid < kSimtRC) {
+      int prev = 0, req = 0, row = 0, bias = 0, pos = 0;
+      float lq = 0.f, lp = 0.f;
+      if (tid < nr) {
+        if constexpr (MODE == kModeStep) {
+          req = r0 + tid;
+          pos = p.j;
+          prev = (p.j == 0) ? p.prev_tok[req]
+                            : (int)key_index(p.keys[(size_t)(p.j - 1) * p.R_max + req]);
+        } else {
+          req = p.rej_list[r0 + tid];
+          pos = p.rej_k[req];
+          prev = (pos == 0) ? p.prev_tok[req] : p.tokens[(size_t)req * p.gamma + pos - 1];
+          lq = p.lse_q[(size_t)req * p.gamma + pos];
+          lp = p.rej_lseP[req];
+        }
+        if (prev < 0 || prev >= p.V) {
+          set_status(p.status, kErrArg);
+          prev = 0;
+        }
+        bias = (pos > 0 || p.bias_at_first) ? 1 : 0;
+        row = req * p.gamma + pos;
+      }
+      s_prev[tid] = prev;
+      s_req[tid] = req;
+      s_row[tid] = row;
+      s_bias[tid] = bias;
+      s_lseq[tid] = lq;
+      s_lsep[tid] = lp;
+      s_pos[tid] = pos;
+      s_rid[tid] = p.req_id ? p.req_id[req] : (uint32_t)req;
+    }
+    __syncthreads();
+    for (int idx = tid; idx < kSimtRC * rank; idx += kSimtThreads) {
+      const int rr = idx / rank, k = idx - rr * rank;
+      float m = 0.f;
+      if (rr < nr && s_bias[rr]) m = act_apply(ld_elem(E, (size_t)s_prev[rr] * rank + k), p.act);
+      ms[rr * mstride + k] = m;
+    }
+
+    Lse2 st[kSimtRPT];
+    unsigned long long best[kSimtRPT], best2[kSimtRPT];
+    float fsum[kSimtRPT], fsum2[kSimtRPT];
+#pragma unroll
+    for (int i = 0; i < kSimtRPT; ++i) {
+      st[i] = lse2_empty();
+      best[i] = 0ull;
+      best2[i] = 0ull;
+      fsum[i] = 0.f;
+      fsum2[i] = 0.f;
+    }
+
+    for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+      const int v0 = tile * kSimtTileV;
+      __syncthreads();
+      const int total = kSimtTileV * nch;
+      for (int c = tid; c < total; c += kSimtThreads) {
+        const int row = c / nch, ch = c - row * nch;
+        const int v = v0 + row;
+        uint4 val = make_uint4(0u, 0u, 0u, 0u);
+        if (v < p.V) val = ld_keep16(W + (size_t)v * rank + ch * epc);
+        *reinterpret_cast<uint4*>(Ws + ((size_t)row * nch + (ch ^ (row & p.swz_mask))) * 16) = val;
+      }
+      __syncthreads();
+      const int v = v0 + vg;
+      if (v >= p.V) continue;
+      float acc[kSimtRPT];
+#pragma unroll
+      for (int i = 0; i < kSimtRPT; ++i) acc[i] = 0.f;
+      const unsigned char* wrow = Ws + (size_t)vg * nch * 16;
+      for (int ch = 0; ch < nch; ++ch) {
+        const uint4 q = *reinterpret_cast<const uint4*>(wrow + (ch ^ (vg & p.swz_mask)) * 16);
+        float w[8];
+        unpack16<T>(q, w);
+#pragma unroll
+        for (int i = 0; i < kSimtRPT; ++i) {
+          const float* mrow = ms + (half * kSimtRPT + i) * mstride + ch * epc;
+#pragma unroll
+          for (int e = 0; e < epc; ++e) acc[i] = fmaf(w[e], mrow[e], acc[i]);
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < kSimtRPT; ++i) {
+        const int rr = half * kSimtRPT + i;
+        if (rr >= nr) continue;
+        const float x = acc[i] + ld_elem(U, (size_t)s_row[rr] * p.V + v);
+        const uint32_t rid = s_rid[rr];
+        if constexpr (MODE == kModeStep) {
+          const float xs = p.sampled ? x * p.inv_T : x;
+          const float x2 = xs * kLog2e;
+          const float M = fmaxf(st[i].m, x2);
+          st[i].s = st[i].s * exp2f(st[i].m - M) + exp2f(x2 - M);
+          st[i].m = M;
+          float z = xs;
+          if (p.sampled) {
+            const Philox4 ph = philox4x32_10((uint32_t)v >> 2, (uint32_t)p.j, rid, 0u, p.k0, p.k1);
+            z += gumbel_from_word(philox_pick(ph, v & 3));
+          }
+          const unsigned long long key = make_key(z, (uint32_t)v);
+          best[i] = key > best[i] ? key : best[i];
+        } else {
+          // residual: res = max(0, p - q) with q = exp(l/T - lse_q), p = exp(P/T - lseP)
+          const int req = s_req[rr], pos = s_pos[rr];
+          const float pl = ld_elem(P, ((size_t)req * (p.gamma + 1) + pos) * p.V + v) * p.inv_T - s_lsep[rr];
+          const float ql = x * p.inv_T - s_lseq[rr];
+          const float pv = __expf(pl);
+          const float qv = __expf(ql);
+          const Philox4 ph = philox4x32_10((uint32_t)v >> 2, (uint32_t)pos, rid, 2u, p.k0, p.k1);
+          const float g = gumbel_from_word(philox_pick(ph, v & 3));
+          if (pl > ql) {
+            // log(p - q) = pl + log(1 - exp(ql - pl)), kept accurate when p ~ q
+            const float lr = pl + log1pf(-__expf(ql - pl));
+            const unsigned long long key = make_key(lr + g, (uint32_t)v);
+            best[i] = key > best[i] ? key : best[i];
+            fsum[i] += pv - qv;
+          }
+          const unsigned long long key2 = make_key(pl + g, (uint32_t)v);
+          best2[i] = key2 > best2[i] ? key2 : best2[i];
+          fsum2[i] += pv;
+        }
+      }
+    }
+
+    // CTA reduction per request: 4 warps per half.
+#pragma unroll
+    for (int i = 0; i < kSimtRPT; ++i) {
+      const Lse2 l = warp_lse2(st[i]);
+      const unsigned long long k = warp_max_u64(best[i]);
+      const unsigned long long k2 = warp_max_u64(best2[i]);
+      const float f = warp_sum(fsum[i]);
+      const float f2 = warp_sum(fsum2[i]);
+      if (lane == 0) {
+        red_l[warp][i] = l;
+        red_k[warp][i] = k;
+        red_k2[warp][i] = k2;
+        red_f[warp][i] = f;
+        red_f2[warp][i] = f2;
+      }
+    }
+    __syncthreads();
+    if (tid < kSimtRC && tid < nr) {
+      const int h = tid / kSimtRPT, i = tid % kSimtRPT;
+      Lse2 l = lse2_empty();
+      unsigned long long k = 0ull, k2 = 0ull;
+      float f = 0.f, f2 = 0.f;
+      for (int w = h * 4; w < h * 4 + 4; ++w) {
+        l = lse2_merge(l, red_l[w][i]);
+        k = red_k[w][i] > k ? red_k[w][i] : k;
+        k2 = red_k2[w][i] > k2 ? red_k2[w][i] : k2;
+        f += red_f[w][i];
+        f2 += red_f2[w][i];
+      }
+      const int req = s_req[tid];
+      if constexpr (MODE == kModeStep) {
+        if (k) atomicMax(&p.keys[(size_t)p.j * p.R_max + req], k);
+        p.parts[((size_t)p.j * p.n_part + blockIdx.x) * p.R_max + req] = make_float2(l.m, l.s);
+      } else {
+        if (k) atomicMax(&p.keys[req], k);
+        if (k2) atomicMax(&p.keys[p.R_max + req], k2);
+        atomicAdd(&p.res_sums[req], f);
+        atomicAdd(&p.res_sums[p.R_max + req], f2);
+      }
+    }
+  }
+}
+
+static size_t simt_smem_bytes(int rank, int elem_bytes) {
+  return (size_t)kSimtTileV * rank * elem_bytes + (size_t)kSimtRC * (rank + 4) * sizeof(float);
+}
+
+template <typename T, int MODE>
+static cudaError_t launch_simt_typed(const SimtParams& sp, int grid, cudaStream_t s) {
+  const size_t smem = simt_smem_bytes(sp.rank, (int)sizeof(T));
+  cudaError_t e = cudaFuncSetAttribute(simt_bias_kernel<T, MODE>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  simt_bias_kernel<T, MODE><<<grid, kSimtThreads, smem, s>>>(sp);
+  return cudaGetLastError();
+}
+
+static cudaError_t launch_simt(const SimtParams& sp, int dtype, int grid, cudaStream_t s, int mode) {
+  if (dtype == 1) {
+    return mode == kModeStep ? launch_simt_typed<__nv_bfloat16, kModeStep>(sp, grid, s)
+                             : launch_simt_typed<__nv_bfloat16, kModeResidual>(sp, grid, s);
+  }
+  return mode == kModeStep ? launch_simt_typed<float, kModeStep>(sp, grid, s)
+                           : launch_simt_typed<float, kModeResidual>(sp, grid, s);
+}
+
+static SimtParams base_params(const Ctx& ctx, int R, int V, int rank, int gamma, int act,
+                              int bias_at_first, float temperature, uint64_t seed) {
+  SimtParams sp{};
+  sp.status = ctx.ws.status;
+  sp.R = R;
+  sp.R_max = ctx.cfg.R_max;
+  sp.V = V;
+  sp.rank = rank;
+  sp.gamma = gamma;
+  sp.act = act;
+  sp.bias_at_first = bias_at_first;
+  sp.swz_mask = chunk_swizzle_mask(rank * (ctx.cfg.dtype == 1 ? 2 : 4) / 16);
+  sp.n_part = ctx.n_part;
+  sp.sampled = temperature > 0.f ? 1 : 0;
+  sp.inv_T = temperature > 0.f ? 1.f / temperature : 1.f;
+  sp.k0 = (uint32_t)(seed & 0xFFFFFFFFull);
+  sp.k1 = (uint32_t)(seed >> 32);
+  return sp;
+}
+
+int simt_grid(const Ctx& ctx, int V) {
+  const int ntiles = (V + kSimtTileV - 1) / kSimtTileV;
+  return ntiles < ctx.n_part ? ntiles : ctx.n_part;
+}
+
+cudaError_t launch_propose_simt(const Ctx& ctx, const ProposeArgs& a, cudaStream_t s) {
+  SimtParams sp = base_params(ctx, a.R, a.V, a.rank, a.gamma, a.act, a.bias_at_first,
+                              a.temperature, a.seed);
+  sp.U = a.U;
+  sp.E = a.E;
+  sp.W = a.W;
+  sp.prev_tok = a.prev_tok;
+  sp.req_id = a.req_id;
+  sp.keys = ctx.ws.keys;
+  sp.parts = ctx.ws.lse_parts;
+  cudaError_t e = cudaMemsetAsync(ctx.ws.keys, 0,
+                                  sizeof(unsigned long long) * (size_t)a.gamma * ctx.cfg.R_max, s);
+  if (e != cudaSuccess) return e;
+  const int grid = simt_grid(ctx, a.V);
+  for (int j = 0; j < a.gamma; ++j) {
+    sp.j = j;
+    e = launch_simt(sp, ctx.cfg.dtype, grid, s, kModeStep);
+    if (e != cudaSuccess) return e;
+    count_launch(ctx);
+  }
+  return cudaSuccess;
+}
+
+cudaError_t launch_residual_simt(const Ctx& ctx, const VerifyArgs& a, cudaStream_t s) {
+  SimtParams sp = base_params(ctx, a.R, a.V, a.rank, a.gamma, a.act, a.bias_at_first,
+                              a.temperature, a.seed);
+  sp.U = a.U;
+  sp.E = a.E;
+  sp.W = a.W;
+  sp.P = a.P;
+  sp.prev_tok = a.prev_tok;
+  sp.tokens = a.tokens;
+  sp.req_id = a.req_id;
+  sp.lse_q = a.lse_q;
+  sp.keys = ctx.ws.res_keys;
+  sp.res_sums = ctx.ws.res_sums;
+  sp.rej_list = ctx.ws.rej_list;
+  sp.rej_k = ctx.ws.rej_k;
+  sp.rej_lseP = ctx.ws.rej_lseP;
+  sp.n_rej = ctx.ws.counters + 1;
+  count_launch(ctx);
+  return launch_simt(sp, ctx.cfg.dtype, simt_grid(ctx, a.V), s, kModeResidual);
+}
+
+// ---------------------------------------------------------------------------
+// Finalize: per (r, j) combine the CTA partials into lse_q, take the token
+// from the argmax key and the (scaled) logit of the chosen token; per r the
+// prefix survival in fp64 ("DSpark 论文精读" 3.1).
+// ---------------------------------------------------------------------------
+struct FinParams {
+  const void* U;
+  const void* E;
+  const void* W;
+  const float* conf;
+  const int32_t* prev_tok;
+  const unsigned long long* keys;
+  const float2* parts;
+  int* status;
+  int32_t* tokens;
+  float* lse_q;
+  float* logit_at_tok;
+  float* survival;
+  int R, R_max, V, rank, gamma, act, bias_at_first, n_part, n_used, sampled;
+  float inv_T;
+};
+
+template <typename T>
+__global__ void __launch_bounds__(256) propose_finalize_kernel(FinParams p) {
+  const int lane = threadIdx.x & 31;
+  const int pair = blockIdx.x * 8 + (threadIdx.x >> 5);
+  const T* U = static_cast<const T*>(p.U);
+  const T* E = static_cast<const T*>(p.E);
+  const T* W = static_cast<const T*>(p.W);
+
+  const int g = blockIdx.x * blockDim.x + threadIdx.x;
+  if (g < p.R) {
+    double acc = 1.0;
+    for (int j = 0; j < p.gamma; ++j) {
+      float c = p.conf[(size_t)g * p.gamma + j];
+      if (!isfinite(c)) {
+        set_status(p.status, kErrNonfinite);
+        c = 0.f;
+      }
+      c = fminf(fmaxf(c, 0.f), 1.f);
+      acc *= (double)c;
+      p.survival[(size_t)g * p.gamma + j] = (float)acc;
+    }
+  }
+  if (pair >= p.R * p.gamma) return;
+  const int r = pair / p.gamma, j = pair - r * p.gamma;
+  Lse2 l = lse2_empty();
+  for (int c = lane; c < p.n_used; c += 32) {
+    const float2 q = p.parts[((size_t)j * p.n_part + c) * p.R_max + r];
+    l = lse2_merge(l, Lse2{q.x, q.y});
+  }
+  l = warp_lse2(l);
+  const unsigned long long key = p.keys[(size_t)j * p.R_max + r];
+  const uint32_t x = key_index(key);
+  const float lse = lse2_value(l);
+  float logit;
+  if (!p.sampled) {
+    logit = key_value(key);
+  } else {
+    float dot = 0.f;
+    if ((j > 0 || p.bias_at_first) && x < (uint32_t)p.V) {
+      int prev = (j == 0) ? p.prev_tok[r] : (int)key_index(p.keys[(size_t)(j - 1) * p.R_max + r]);
+      if (prev < 0 || prev >= p.V) prev = 0;
+      for (int k = lane; k < p.rank; k += 32)
+        dot = fmaf(act_apply(ld_elem(E, (size_t)prev * p.rank + k), p.act),
+                   ld_elem(W, (size_t)x * p.rank + k), dot);
+      dot = warp_sum(dot);
+    }
+    const float u = x < (uint32_t)p.V ? ld_elem(U, ((size_t)r * p.gamma + j) * p.V + x) : 0.f;
+    logit = (u + dot) * p.inv_T;
+  }
+  if (lane == 0) {
+    p.tokens[(size_t)r * p.gamma + j] = (int32_t)x;
+    p.lse_q[(size_t)r * p.gamma + j] = lse;
+    p.logit_at_tok[(size_t)r * p.gamma + j] = logit;
+    if (!isfinite(lse) || !isfinite(logit) || key == 0ull) set_status(p.status, kErrNonfinite);
+  }
+}
+
+cudaError_t launch_propose_finalize_n(const Ctx& ctx, const ProposeArgs& a, int n_used,
+                                      cudaStream_t s) {
+  FinParams p{};
+  p.U = a.U;
+  p.E = a.E;
+  p.W = a.W;
+  p.conf = a.conf;
+  p.prev_tok = a.prev_tok;
+  p.keys = ctx.ws.keys;
+  p.parts = ctx.ws.lse_parts;
+  p.status = ctx.ws.status;
+  p.tokens = a.tokens;
+  p.lse_q = a.lse_q;
+  p.logit_at_tok = a.logit_at_tok;
+  p.survival = a.survival;
+  p.R = a.R;
+  p.R_max = ctx.cfg.R_max;
+  p.V = a.V;
+  p.rank = a.rank;
+  p.gamma = a.gamma;
+  p.act = a.act;
+  p.bias_at_first = a.bias_at_first;
+  p.n_part = ctx.n_part;
+  p.n_used = n_used;
+  p.sampled = a.temperature > 0.f ? 1 : 0;
+  p.inv_T = a.temperature > 0.f ? 1.f / a.temperature : 1.f;
+  const int pairs = a.R * a.gamma;
+  int grid = (pairs + 7) / 8;
+  const int gsurv = (a.R + 255) / 256;
+  if (grid < gsurv) grid = gsurv;
+  if (ctx.cfg.dtype == 1)
+    propose_finalize_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(p);
+  else
+    propose_finalize_kernel<float><<<grid, 256, 0, s>>>(p);
+  count_launch(ctx);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_propose_finalize(const Ctx& ctx, const ProposeArgs& a, cudaStream_t s) {
+  return launch_propose_finalize_n(ctx, a, simt_grid(ctx, a.V), s);
+}
+
+}  // namespace dsd

@@ -1,0 +1,278 @@
+"""Parity of the CUDA path (through the C ABI) with the fp64 oracle on the
+same seeded inputs.  Small cases span several vocabulary tiles with a ragged
+tail and request counts that are not multiples of the CTA batching; the
+full-size workloads are checked on sampled requests / blocks."""
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import dsd_oracle as O
+from semi_autoregressive_draft_gb300 import synth
+from tests import parity
+
+pytestmark = pytest.mark.gpu
+
+DEV = torch.device("cuda", 0)
+
+
+@pytest.fixture(scope="module")
+def dsd():
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    from semi_autoregressive_draft_gb300 import build as b
+
+    b.build()
+    import semi_autoregressive_draft_gb300 as m
+
+    return m
+
+
+def host(x):
+    return {k: synth.to_numpy(v) for k, v in x.items() if isinstance(v, torch.Tensor)}
+
+
+def run_cycle(dsd, spec, engine="auto", act="none", bias_at_first=True, keep_all=False):
+    x = synth.cycle_inputs(spec, device=DEV)
+    ctx = dsd.Context(spec.V, spec.r, spec.G, spec.R, dtype=spec.dtype, act=act,
+                      bias_at_first=bias_at_first, engine=engine)
+    T = spec.temperature
+    prop = ctx.propose(x["U"], x["E"], x["W"], x["conf"], x["prev_tok"], req_id=x["req_id"],
+                       temperature=T, seed=x["seed"])
+    sch = ctx.schedule(prop["survival"], x["sps"])
+    keep = sch["keep_len"]
+    if keep_all:
+        keep = torch.full_like(keep, spec.G)
+    ver = ctx.verify(x["P"], prop["tokens"], keep, U=x["U"], E=x["E"], W=x["W"],
+                     prev_tok=x["prev_tok"], lse_q=prop["lse_q"],
+                     logit_at_tok=prop["logit_at_tok"], req_id=x["req_id"], temperature=T,
+                     seed=x["seed"])
+    assert ctx.sync_status() == 0
+    k = {n: t.cpu().numpy() for n, t in {**prop, **sch, **ver}.items()}
+    k["keep_used"] = keep.cpu().numpy()
+    ctx.close()
+    return x, k
+
+
+def oracle_cycle(spec, x, act="none", bias_at_first=True, keep_all=False):
+    h = host(x)
+    rid = h["req_id"].astype(np.int64)
+    T = spec.temperature
+    prop = O.propose(h["U"], h["E"], h["W"], h["conf"], h["prev_tok"], rid, T, x["seed"],
+                     bias_at_first, act)
+    sch = O.schedule(prop["survival"].astype(np.float32), h["sps"])
+    keep = np.full(spec.R, spec.G) if keep_all else sch["keep_len"]
+    ver = O.verify(h["P"], h["U"], h["E"], h["W"], h["prev_tok"], prop["tokens"], keep, rid, T,
+                   x["seed"], bias_at_first, act)
+    return prop, sch, ver, keep
+
+
+def check_cycle(spec, x, k, act="none", bias_at_first=True, keep_all=False, max_exempt=0.05):
+    prop, sch, ver, keep = oracle_cycle(spec, x, act, bias_at_first, keep_all)
+    rep = parity.compare_propose(k, prop)
+    parity.compare_schedule(k["keep_len"], k["theta_B"], sch)
+    ex = parity.draft_exempt(prop["margin"])
+    draft_ex = np.array([ex[r, :keep[r] + 1].any() if keep[r] < spec.G else ex[r].any()
+                         for r in range(spec.R)])
+    if not draft_ex.any():
+        assert np.array_equal(k["keep_used"], keep)
+    vrep = parity.compare_verify(k["accept_len"], k["next_token"], ver, spec.temperature, keep,
+                                 draft_ex)
+    total = rep.checked + rep.exempt
+    assert rep.exempt <= max_exempt * total + 1, f"too many exemptions: {rep}"
+    return rep, vrep, ver
+
+
+SMALL = dict(V=2568, R=19, ew_std=0.3)        # 21 tiles of 128 with an 8-row tail
+
+
+@pytest.mark.parametrize("engine", ["simt", "auto"])
+@pytest.mark.parametrize("temperature", [0.0, 1.0, 0.6])
+def test_cycle_bf16_small(dsd, engine, temperature):
+    spec = synth.scaled(synth.CYCLE_SPECS["greedy"], temperature=temperature, seed=21,
+                        p_noise=1.0 if temperature else 0.5, **SMALL)
+    x, k = run_cycle(dsd, spec, engine)
+    check_cycle(spec, x, k)
+
+
+def test_cycle_bf16_no_pruning_covers_all_positions(dsd):
+    spec = synth.scaled(synth.CYCLE_SPECS["sampled"], seed=22, **SMALL)
+    x, k = run_cycle(dsd, spec, keep_all=True)
+    _, vrep, ver = check_cycle(spec, x, k, keep_all=True)
+    assert vrep.checked > 0
+    # every accept length 0..gamma is possible; some rejections happened
+    assert (ver["accept_len"] < spec.G).any()
+
+
+def test_cycle_f32_tiny_config(dsd):
+    spec = synth.CYCLE_SPECS["tiny"]
+    x, k = run_cycle(dsd, spec)
+    check_cycle(spec, x, k)
+    assert k["keep_len"].tolist() == [7]      # constant SPS over B <= 8 keeps all
+
+
+@pytest.mark.parametrize("temperature", [0.0, 1.0])
+def test_cycle_f32_rank32_ragged(dsd, temperature):
+    spec = synth.scaled(synth.CYCLE_SPECS["tiny"], R=5, V=1000, ew_std=0.5,
+                        temperature=temperature, seed=23)
+    x, k = run_cycle(dsd, spec)
+    check_cycle(spec, x, k)
+
+
+@pytest.mark.parametrize("act,baf", [("silu", True), ("none", False)])
+def test_cycle_variants(dsd, act, baf):
+    spec = synth.scaled(synth.CYCLE_SPECS["greedy"], seed=24, temperature=1.0, **SMALL)
+    x, k = run_cycle(dsd, spec, act=act, bias_at_first=baf)
+    check_cycle(spec, x, k, act=act, bias_at_first=baf)
+
+
+def test_single_position_and_single_request(dsd):
+    spec = synth.scaled(synth.CYCLE_SPECS["greedy"], R=1, G=1, V=1032, ew_std=0.5, seed=25)
+    x, k = run_cycle(dsd, spec)
+    check_cycle(spec, x, k)
+
+
+def test_propose_is_deterministic_and_keyed_by_request_id(dsd):
+    spec = synth.scaled(synth.CYCLE_SPECS["sampled"], seed=26, **SMALL)
+    x = synth.cycle_inputs(spec, device=DEV)
+    ctx = dsd.Context(spec.V, spec.r, spec.G, spec.R, dtype="bf16")
+    a = ctx.propose(x["U"], x["E"], x["W"], x["conf"], x["prev_tok"], x["req_id"], 1.0, 7)
+    b = ctx.propose(x["U"], x["E"], x["W"], x["conf"], x["prev_tok"], x["req_id"], 1.0, 7)
+    assert torch.equal(a["tokens"], b["tokens"]) and torch.equal(a["lse_q"], b["lse_q"])
+    perm = torch.randperm(spec.R, generator=torch.Generator().manual_seed(0)).to(DEV)
+    c = ctx.propose(x["U"][perm].contiguous(), x["E"], x["W"], x["conf"][perm].contiguous(),
+                    x["prev_tok"][perm].contiguous(), x["req_id"][perm].contiguous(), 1.0, 7)
+    assert torch.equal(c["tokens"], a["tokens"][perm])
+    assert ctx.sync_status() == 0
+    ctx.close()
+
+
+def test_schedule_against_oracle_random_tables(dsd):
+    rng = np.random.default_rng(27)
+    ctx = dsd.Context(4096, 64, 7, 300, dtype="bf16")
+    for trial in range(12):
+        R = int(rng.integers(1, 300))
+        conf = rng.beta(rng.uniform(1, 10), 2, size=(R, 7)).astype(np.float32)
+        if trial % 3 == 0:
+            conf[:, 2:] = 1.0                 # equal survivals within a request
+        if trial % 4 == 1:
+            conf = np.round(conf * 4) / 4     # many exact ties across requests
+        n = int(rng.integers(R, R * 8 + 2))
+        B = np.arange(1, n + 1)
+        knee = rng.uniform(0, n)
+        sps = (1.0 / (1e-3 + rng.uniform(1e-6, 1e-4) * np.maximum(0, B - knee))).astype(np.float32)
+        surv = O.survival(conf).astype(np.float32)
+        out = ctx.schedule(torch.as_tensor(surv, device=DEV), torch.as_tensor(sps, device=DEV))
+        ref = O.schedule(surv, sps)
+        parity.compare_schedule(out["keep_len"].cpu().numpy(), out["theta_B"].cpu().numpy(), ref)
+    with pytest.raises(dsd.DsdError):
+        ctx.schedule(torch.ones((10, 7), device=DEV), torch.ones(5, device=DEV))
+    assert ctx.sync_status() == 0
+    ctx.close()
+
+
+def test_verify_greedy_hand_case(dsd):
+    P = torch.zeros((1, 4, 8), dtype=torch.float32)
+    P[0, 0, 0] = 5
+    P[0, 1, 3] = 4
+    P[0, 2, 1] = 6
+    P[0, 3, 3] = 9
+    ctx = dsd.Context(8, 8, 3, 1, dtype="f32")
+    tokens = torch.tensor([[0, 3, 2]], dtype=torch.int32, device=DEV)
+    for kl, acc, nxt in [(3, 2, 1), (2, 2, 1), (1, 1, 3), (0, 0, 0)]:
+        out = ctx.verify(P.to(DEV), tokens, torch.tensor([kl], dtype=torch.int32, device=DEV))
+        assert (int(out["accept_len"][0]), int(out["next_token"][0])) == (acc, nxt)
+    assert ctx.sync_status() == 0
+    ctx.close()
+
+
+@pytest.mark.parametrize("N,V", [(9, 2568), (3, 1000)])
+def test_overlap_small(dsd, N, V):
+    spec = synth.OverlapSpec(N=N, V=V, ragged_frac=0.5, seed=28)
+    ox = synth.overlap_inputs(spec, device=DEV)
+    ox["valid_len"][0] = 0
+    ctx = dsd.Context(V, 64, spec.G, 8, dtype="bf16")
+    out = ctx.overlap(ox["P"], ox["Q"], ox["valid_len"])
+    assert ctx.sync_status() == 0
+    ref = O.overlap(synth.to_numpy(ox["P"]), synth.to_numpy(ox["Q"]), synth.to_numpy(ox["valid_len"]))
+    parity.compare_overlap({k: v.cpu().numpy() for k, v in out.items()}, ref)
+    # empty call
+    e = ctx.overlap(ox["P"][:0], ox["Q"][:0], ox["valid_len"][:0])
+    assert float(e["mean_tau"][0]) == 0.0 and torch.all(e["accept_rate"] == 0)
+    ctx.close()
+
+
+def test_nonfinite_logits_are_reported(dsd):
+    spec = synth.scaled(synth.CYCLE_SPECS["greedy"], seed=29, **SMALL)
+    x = synth.cycle_inputs(spec, device=DEV)
+    x["U"][3, 2, 100] = float("nan")
+    ctx = dsd.Context(spec.V, spec.r, spec.G, spec.R, dtype="bf16")
+    ctx.propose(x["U"], x["E"], x["W"], x["conf"], x["prev_tok"], x["req_id"], 0.0, 1)
+    assert ctx.sync_status() == -6
+    assert ctx.sync_status() == 0           # status is cleared after reading
+    ctx.close()
+
+
+def test_empty_batch_is_a_noop(dsd):
+    ctx = dsd.Context(1032, 64, 7, 4, dtype="bf16")
+    z = torch.empty((0, 7, 1032), dtype=torch.bfloat16, device=DEV)
+    e = torch.zeros((1032, 64), dtype=torch.bfloat16, device=DEV)
+    out = ctx.propose(z, e, e, torch.empty((0, 7), device=DEV),
+                      torch.empty((0,), dtype=torch.int32, device=DEV))
+    assert out["tokens"].numel() == 0
+    assert ctx.sync_status() == 0
+    ctx.close()
+
+
+# ----------------------------------------------------------- full-size checks
+
+def _subset(x, idx):
+    return {k: (v[idx].contiguous() if isinstance(v, torch.Tensor) and k in
+                ("U", "P", "conf", "prev_tok", "req_id") else v) for k, v in x.items()}
+
+
+@pytest.mark.parametrize("name,n_sample", [("greedy", 16), ("sampled", 6), ("highconc", 6)])
+def test_full_size_cycle_sampled_requests(dsd, name, n_sample):
+    spec = synth.CYCLE_SPECS[name]
+    x, k = run_cycle(dsd, spec)
+    rng = np.random.default_rng(30)
+    idx = np.sort(rng.choice(spec.R, size=n_sample, replace=False))
+    h = host(x)
+    rid = h["req_id"].astype(np.int64)
+    T = spec.temperature
+    # schedule over the whole batch needs only the (cheap) survivals
+    surv = O.survival(h["conf"]).astype(np.float32)
+    sch = O.schedule(surv, h["sps"])
+    parity.compare_schedule(k["keep_len"], k["theta_B"], sch)
+    hs = {n: v[idx] for n, v in h.items() if n in ("U", "P", "conf", "prev_tok")}
+    prop = O.propose(hs["U"], h["E"], h["W"], hs["conf"], hs["prev_tok"], rid[idx], T, x["seed"])
+    kk = {n: k[n][idx] for n in ("tokens", "lse_q", "logit_at_tok", "survival")}
+    parity.compare_propose(kk, prop)
+    keep = sch["keep_len"][idx]
+    ver = O.verify(hs["P"], hs["U"], h["E"], h["W"], hs["prev_tok"], prop["tokens"], keep,
+                   rid[idx], T, x["seed"])
+    ex = parity.draft_exempt(prop["margin"])
+    draft_ex = np.array([ex[i, :min(keep[i] + 1, spec.G)].any() for i in range(len(idx))])
+    parity.compare_verify(k["accept_len"][idx], k["next_token"][idx], ver, T, keep, draft_ex)
+
+
+def test_full_size_overlap_sampled_blocks(dsd):
+    spec = synth.OverlapSpec()
+    ox = synth.overlap_inputs(spec, device=DEV)
+    ctx = dsd.Context(spec.V, 64, spec.G, 8, dtype="bf16")
+    out = ctx.overlap(ox["P"], ox["Q"], ox["valid_len"])
+    assert ctx.sync_status() == 0
+    rng = np.random.default_rng(31)
+    vl = synth.to_numpy(ox["valid_len"])
+    ragged = np.flatnonzero(vl < spec.G)
+    idx = np.sort(np.concatenate([rng.choice(spec.N, 10, replace=False), ragged[:4]]))
+    ref = O.overlap(synth.to_numpy(ox["P"][idx]), synth.to_numpy(ox["Q"][idx]), vl[idx])
+    a_k = out["a"].cpu().numpy()[idx]
+    assert np.max(np.abs(a_k - ref["a"])) <= parity.PROB_TOL
+    assert np.max(np.abs(out["tau"].cpu().numpy()[idx] - ref["tau"])) <= parity.PROB_TOL
+    # aggregates over all blocks from the kernel's own per-block values
+    a_all = out["a"].cpu().numpy().astype(np.float64)
+    vmask = np.arange(spec.G)[None, :] < vl[:, None]
+    ar = (a_all * vmask).sum(0) / np.maximum(vmask.sum(0), 1)
+    assert np.max(np.abs(out["accept_rate"].cpu().numpy() - ar)) <= 1e-5
+    ctx.close()
