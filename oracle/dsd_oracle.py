@@ -151,7 +151,7 @@ def top2_margin(z):
 
 
 def _f64(a):
-    return np.asarray(a).astype(np.float64)
+    return np.asarray(a, dtype=np.float64)
 
 
 # ---------------------------------------------------------------------------
