@@ -1,0 +1,526 @@
+#!/usr/bin/env python
+"""Throughput of one DSpark draft-verify cycle (propose -> schedule -> verify)
+for a whole serving batch on one GB300, through the C ABI.
+
+Default workload: R = 256 requests, gamma = 7, V = 151936, Markov rank 256,
+bf16 tables, greedy, SPS(B) flat at 1e3 steps/s up to B = 256 then ~1/B
+(1024 entries).  Inputs are seeded synthetic tensors resident in HBM; each
+timed step is one cycle.  The three phases are captured as CUDA graphs and
+replayed back to back, bracketed by CUDA events on the launching stream; L2
+is flushed (a 512 MB write) between steps, outside the events.
+
+Prints ONE JSON line (rank 0).  --impl reference times the fp64 CPU oracle on
+the host cores on bounded samples of the same workload instead.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "draft-verify cycles/sec and tokens/sec at V=151936,γ=7,R=256; % of HBM roofline"
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
+KERNEL_SOURCES = {
+    "simt_bias_kernel": ["propose_simt.cu", "dsd_common.cuh"],
+    "propose_tc_kernel": ["propose_tc.cu", "dsd_common.cuh"],
+}
+FALLBACK_HBM_GBS = 6800.0
+
+
+# ------------------------------------------------------------------ helpers
+
+def env_int(name, default):
+    try:
+        return int(os.environ.get(name, default))
+    except ValueError:
+        return default
+
+
+def dist_info():
+    return env_int("RANK", 0), env_int("LOCAL_RANK", 0), env_int("WORLD_SIZE", 1)
+
+
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    """Max of a per-rank scalar over all ranks (identity when world == 1)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def source_hash(kernel: str) -> str:
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES.get(kernel, []):
+        with open(os.path.join(ROOT, "semi_autoregressive_draft_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_for(kernel: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary, or None when the
+    kernel source changed since the counters were taken."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            table = json.load(f)
+    except (OSError, ValueError):
+        return None
+    ent = table.get(kernel, {}).get(workload)
+    if not ent or ent.get("source_hash") != source_hash(kernel):
+        return None
+    return ent.get("dram_bytes_per_launch")
+
+
+def hbm_peak():
+    try:
+        with open(PEAKS_FILE) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except (OSError, ValueError, KeyError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms while active."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str | None):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+               "-lms", "200"]
+        if self.gpu_id:
+            cmd += ["--id=" + self.gpu_id]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        return self.summary()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+def gpu_uuid(device_index: int):
+    import torch
+
+    try:
+        u = str(torch.cuda.get_device_properties(device_index).uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        return None
+
+
+# --------------------------------------------------------------- workloads
+
+def cycle_spec(name):
+    from semi_autoregressive_draft_gb300 import synth
+
+    return synth.CYCLE_SPECS[name]
+
+
+def workload_label(spec):
+    mode = "greedy" if spec.temperature == 0 else f"sampled T={spec.temperature:g}"
+    return (f"{spec.name}: R={spec.R} gamma={spec.G} V={spec.V} r={spec.r} {spec.dtype} "
+            f"{mode}, SPS {spec.sps_kind}")
+
+
+def propose_alg_bytes(spec):
+    """Bytes the propose phase must move: every U row once, the projection W
+    once (compulsory; every draft step needs all of it, and it can stay in
+    L2 across steps), the gathered E rows, confidences, previous tokens and
+    the four [R, gamma] outputs."""
+    esz = 2 if spec.dtype == "bf16" else 4
+    R, G, V, r = spec.R, spec.G, spec.V, spec.r
+    return (R * G * V * esz + V * r * esz + R * G * r * esz + R * G * 4 + R * 4
+            + 4 * R * G * 4)
+
+
+def verify_alg_bytes(spec, B):
+    esz = 2 if spec.dtype == "bf16" else 4
+    return B * spec.V * esz
+
+
+# --------------------------------------------------------------- CPU oracle
+
+def oracle_sample_cycle(spec, h, n_req, seed, idx=None):
+    """Time the fp64 oracle on a bounded sample: the schedule of the whole
+    batch plus propose and verify of n_req requests; returns estimated
+    seconds per full-batch cycle and the sample description."""
+    import numpy as np
+
+    from oracle import dsd_oracle as O
+
+    R = spec.R
+    if idx is None:
+        idx = np.arange(n_req)
+    rid = h["req_id"].astype(np.int64)
+    t0 = time.perf_counter()
+    surv_all = O.survival(h["conf"]).astype(np.float32)
+    sch = O.schedule(surv_all, h["sps"])
+    t1 = time.perf_counter()
+    prop = O.propose(h["U"][idx], h["E"], h["W"], h["conf"][idx], h["prev_tok"][idx], rid[idx],
+                     spec.temperature, seed)
+    O.verify(h["P"][idx], h["U"][idx], h["E"], h["W"], h["prev_tok"][idx], prop["tokens"],
+             sch["keep_len"][idx], rid[idx], spec.temperature, seed)
+    t2 = time.perf_counter()
+    per_req = (t2 - t1) / len(idx)
+    est = (t1 - t0) + per_req * R
+    desc = (f"schedule of all {R} requests + propose/verify of {len(idx)} of {R} requests "
+            f"(all {spec.G} positions, full V={spec.V}; E, W widened to fp64 once); cycle time "
+            f"extrapolated linearly in requests ({t2 - t0:.1f} s measured)")
+    return est, desc, t2 - t0
+
+
+def host_arrays(x, rows=None):
+    """Host copies for the oracle: the per-request logit rows only for the
+    first `rows` requests (the sample), everything else in full."""
+    from semi_autoregressive_draft_gb300 import synth
+
+    out = {}
+    for k in ("U", "E", "W", "P", "conf", "prev_tok", "req_id", "sps"):
+        t = x[k]
+        if rows is not None and k in ("U", "P"):
+            t = t[:rows]
+        out[k] = synth.to_numpy(t)
+    return out
+
+
+# --------------------------------------------------------------------- arms
+
+def run_reference(args):
+    rank, local_rank, world = dist_info()
+    if rank != 0:
+        return 0
+    import numpy as np
+    import torch
+
+    from semi_autoregressive_draft_gb300 import synth
+
+    spec = cycle_spec(args.workload)
+    x = synth.cycle_inputs(spec, device="cpu")
+    h = host_arrays(x)
+    for k in ("E", "W"):
+        h[k] = h[k].astype(np.float64)
+    n_req = 1
+    for _ in range(args.warmup):
+        oracle_sample_cycle(spec, h, n_req, x["seed"])
+    times = []
+    desc = ""
+    for s in range(args.steps):
+        idx = np.array([(s * 37) % spec.R])
+        est, desc, _ = oracle_sample_cycle(spec, h, n_req, x["seed"], idx)
+        times.append(est)
+    desc = desc.replace("propose/verify of 1 of", "propose/verify of 1 (a different one each step) of")
+    sec = statistics.mean(times)
+    value = 1.0 / sec
+    cores = os.cpu_count()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "cycles/s",
+        "tokens_per_s": None, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": sec * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": workload_label(spec), "R": spec.R, "gamma": spec.G, "V": spec.V,
+                   "rank": spec.r},
+        "cpu_baseline": {"value": value, "unit": "cycles/s", "cores": cores, "kind": "oracle",
+                         "sample": "each step: " + desc},
+        "e2e": {"value": value, "unit": "cycles/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "notes": "fp64 numpy oracle on the host cores; no GPU involved",
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args):
+    import numpy as np
+    import torch
+
+    rank, local_rank, world = dist_info()
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+
+    import semi_autoregressive_draft_gb300 as dsd
+    from semi_autoregressive_draft_gb300 import build as _build
+    from semi_autoregressive_draft_gb300 import synth
+
+    if not os.path.exists(dsd.LIB_PATH):
+        _build.build()
+    spec = cycle_spec(args.workload)
+    x = synth.cycle_inputs(spec, device=dev)
+    ctx = dsd.Context(spec.V, spec.r, spec.G, spec.R, dtype=spec.dtype, engine=args.engine,
+                      device=local_rank)
+    T, seed = spec.temperature, x["seed"]
+    out = ctx.cycle_outputs(spec.R)
+    stream = torch.cuda.Stream(device=dev)
+    flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+
+    def propose():
+        dsd.dsd_propose(ctx.handle, spec.R, x["U"], x["E"], x["W"], x["conf"], x["prev_tok"],
+                        x["req_id"], T, seed, out["tokens"], out["lse_q"], out["logit_at_tok"],
+                        out["survival"], None, local_rank)
+
+    def schedule():
+        dsd.dsd_schedule(ctx.handle, spec.R, out["survival"], x["sps"], x["sps"].numel(),
+                         out["keep_len"], out["theta_B"], None, local_rank)
+
+    def verify():
+        dsd.dsd_verify(ctx.handle, spec.R, x["P"], x["U"], x["E"], x["W"], x["prev_tok"],
+                       out["tokens"], out["lse_q"], out["logit_at_tok"], out["keep_len"],
+                       x["req_id"], T, seed, out["accept_len"], out["next_token"], None,
+                       local_rank)
+
+    with torch.cuda.stream(stream):
+        for _ in range(2):               # eager warm-up (sets kernel attributes)
+            propose(); schedule(); verify()
+    stream.synchronize()
+    assert ctx.sync_status(stream) == 0
+    graphs = []
+    for fn in (propose, schedule, verify):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            fn()
+        graphs.append(g)
+    launches_before_warm = ctx.launch_count()
+    launches_per_cycle_eager = None
+
+    def replay_cycle(ev=None):
+        if ev:
+            ev[0].record(stream)
+        graphs[0].replay()
+        if ev:
+            ev[1].record(stream)
+        graphs[1].replay()
+        if ev:
+            ev[2].record(stream)
+        graphs[2].replay()
+        if ev:
+            ev[3].record(stream)
+
+    # count kernels per cycle from the library's own launch counter
+    c0 = ctx.launch_count()
+    with torch.cuda.stream(stream):
+        propose(); schedule(); verify()
+    launches_per_cycle_eager = ctx.launch_count() - c0
+    del launches_before_warm
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            flush.zero_()
+            replay_cycle()
+    stream.synchronize()
+
+    clocks = ClockSampler(gpu_uuid(local_rank)) if rank == 0 else None
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    if clocks:
+        clocks.start()
+        time.sleep(0.3)
+    w0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        for i in range(args.steps):
+            flush.zero_()
+            replay_cycle(evs[i])
+    stream.synchronize()
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    wall = time.perf_counter() - w0
+    clk = clocks.stop() if clocks else None
+    st = ctx.sync_status(stream)
+    if st != 0:
+        raise RuntimeError(f"device status {st} after the timed region")
+
+    cyc_ms = [e[0].elapsed_time(e[3]) for e in evs]
+    prop_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    sch_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    ver_ms = [e[2].elapsed_time(e[3]) for e in evs]
+    mean_cyc = statistics.mean(cyc_ms)
+    mean_cyc_max = max_over_ranks(mean_cyc, world, dev)
+    value = world * 1e3 / mean_cyc_max
+    acc = out["accept_len"].cpu().numpy()
+    keep = out["keep_len"].cpu().numpy()
+    tokens_per_cycle = int((acc + 1).sum())
+    B = int((keep + 1).sum())
+
+    # e2e: same cycle from pinned host buffers through dsd_cycle_host
+    e2e = None
+    if not args.no_e2e:
+        hU = x["U"].cpu().pin_memory()
+        hP = x["P"].cpu().pin_memory()
+        hc = x["conf"].cpu().pin_memory()
+        hp = x["prev_tok"].cpu().pin_memory()
+        hr = x["req_id"].cpu().pin_memory()
+        ho = None
+        for _ in range(max(1, min(args.warmup, 3))):
+            ho = ctx.cycle_host(hU, x["E"], x["W"], hc, hp, hP, x["sps"], req_id_host=hr,
+                                temperature=T, seed=seed, out=ho, stream=stream)
+        n_e2e = max(3, min(args.steps, 10))
+        barrier(world)
+        t0 = time.perf_counter()
+        for _ in range(n_e2e):
+            ho = ctx.cycle_host(hU, x["E"], x["W"], hc, hp, hP, x["sps"], req_id_host=hr,
+                                temperature=T, seed=seed, out=ho, stream=stream)
+        t_e2e = (time.perf_counter() - t0) / n_e2e
+        t_e2e = max_over_ranks(t_e2e, world, dev)
+        h2d = sum(synth.bytes_of(t) for t in (hU, hP, hc, hp, hr))
+        d2h = sum(synth.bytes_of(ho[k]) for k in ("tokens", "keep_len", "accept_len", "next_token"))
+        assert np.array_equal(ho["accept_len"].numpy(), acc)
+        e2e = {"value": world / t_e2e, "unit": "cycles/s", "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": t_e2e * 1e3,
+               "path": "dsd_cycle_host (pinned host inputs, staging copies inside the call)"}
+
+    peak, peak_kind = hbm_peak()
+    pbytes = propose_alg_bytes(spec)
+    prop_mean_s = statistics.mean(prop_ms) / 1e3
+    achieved = pbytes / prop_mean_s / 1e9
+    engine_kernel = "propose_tc_kernel" if ctx_engine_is_tc(ctx, spec) else "simt_bias_kernel"
+    roofline = {"bound": "hbm", "kernel": f"propose phase ({engine_kernel})",
+                "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)",
+                "traffic": traffic_for(engine_kernel, spec.name),
+                "alg_bytes_per_launch": pbytes,
+                "alg_bytes_note": "U rows once + W once + gathered E rows + small I/O"}
+    vbytes = verify_alg_bytes(spec, B)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu:
+        h = host_arrays(x, rows=args.cpu_requests)
+        for k in ("E", "W"):
+            h[k] = h[k].astype(np.float64)
+        est, desc, spent = oracle_sample_cycle(spec, h, args.cpu_requests, seed)
+        cpu = {"value": 1.0 / est, "unit": "cycles/s", "cores": os.cpu_count(), "kind": "oracle",
+               "sample": desc, "cpu_seconds": spent}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "cycles/s",
+        "tokens_per_s": value * tokens_per_cycle, "tokens_per_cycle": tokens_per_cycle,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": mean_cyc_max,
+        "wall_ms_per_step_incl_flush": wall * 1e3 / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": spec.dtype, "accumulate": "fp32", "data": "synthetic",
+        "config": {"workload": workload_label(spec), "R": spec.R, "gamma": spec.G, "V": spec.V,
+                   "rank": spec.r, "temperature": spec.temperature, "engine": args.engine,
+                   "verify_batch_B": B, "parallelism": f"replicas x{world}",
+                   "l2": "flushed between steps (512 MB write outside the events); inputs 1.2 GB"},
+        "phases_ms": {"propose": statistics.mean(prop_ms), "schedule": statistics.mean(sch_ms),
+                      "verify": statistics.mean(ver_ms)},
+        "verify_alg_GBps": vbytes / (statistics.mean(ver_ms) / 1e3) / 1e9,
+        "roofline": roofline,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": int(launches_per_cycle_eager * args.steps),
+        "clocks": clk,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    ctx.close()
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+    return 0
+
+
+def ctx_engine_is_tc(ctx, spec):
+    if spec.dtype != "bf16":
+        return False
+    import semi_autoregressive_draft_gb300 as dsd
+
+    return getattr(dsd, "TC_AVAILABLE", False) and spec.R >= 16
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="highconc",
+                    choices=["highconc", "greedy", "sampled", "tiny"])
+    ap.add_argument("--engine", default="auto", choices=["auto", "simt", "tcgen05"])
+    ap.add_argument("--cpu-requests", type=int, default=128,
+                    help="requests in the CPU-baseline sample")
+    ap.add_argument("--ref-requests", type=int, default=16,
+                    help="requests per step of the reference (oracle) arm")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    args = ap.parse_args(argv)
+    args.warmup = max(args.warmup, 3)   # at least 3 untimed warm-up steps
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())
