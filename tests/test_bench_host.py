@@ -1,0 +1,68 @@
+"""Host-side logic of bench.py: the replica aggregation used when it runs
+under torchrun (world size 2, gloo, on CPU) and the JSON helpers."""
+
+import json
+import os
+import socket
+
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+import bench
+
+
+def _free_port():
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    port = s.getsockname()[1]
+    s.close()
+    return port
+
+
+def _worker(rank, world, port, out):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world), LOCAL_RANK=str(rank))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    r, lr, w = bench.dist_info()
+    assert (r, lr, w) == (rank, rank, world)
+    bench.barrier(world)
+    step_ms = 10.0 + 5.0 * rank           # rank 1 is the slow one
+    m = bench.max_over_ranks(step_ms, world, torch.device("cpu"))
+    out[rank] = m
+    dist.destroy_process_group()
+
+
+def test_max_over_ranks_gloo_world_size_2():
+    port = _free_port()
+    mgr = mp.Manager()
+    out = mgr.dict()
+    mp.spawn(_worker, args=(2, port, out), nprocs=2, join=True)
+    assert out[0] == out[1] == 15.0
+    # whole-job value of two replicas = 2 cycles per max step time
+    assert 2 * 1e3 / out[0] == pytest.approx(133.333, rel=1e-4)
+
+
+def test_single_rank_is_identity():
+    assert bench.max_over_ranks(3.5, 1) == 3.5
+
+
+def test_algorithmic_bytes_of_the_high_concurrency_workload():
+    spec = bench.cycle_spec("highconc")
+    b = bench.propose_alg_bytes(spec)
+    # U 256*7*151936*2 + W 151936*256*2 + E rows + small I/O
+    assert b == 256 * 7 * 151936 * 2 + 151936 * 256 * 2 + 256 * 7 * 256 * 2 + 256 * 7 * 4 \
+        + 256 * 4 + 4 * 256 * 7 * 4
+    assert 620e6 < b < 630e6
+
+
+def test_traffic_lookup_is_null_when_source_changed(tmp_path, monkeypatch):
+    f = tmp_path / "traffic.json"
+    f.write_text(json.dumps({"simt_bias_kernel": {"greedy": {
+        "source_hash": "0" * 16, "dram_bytes_per_launch": 123}}}))
+    monkeypatch.setattr(bench, "TRAFFIC_FILE", str(f))
+    assert bench.traffic_for("simt_bias_kernel", "greedy") is None
+    f.write_text(json.dumps({"simt_bias_kernel": {"greedy": {
+        "source_hash": bench.source_hash("simt_bias_kernel"), "dram_bytes_per_launch": 123}}}))
+    assert bench.traffic_for("simt_bias_kernel", "greedy") == 123
