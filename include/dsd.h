@@ -240,6 +240,38 @@ int dsd_overlap(dsd_ctx* ctx, int N, const void* P_logits, const void* Q_logits,
                 const int32_t* valid_len, float* a, float* l1, float* tau,
                 float* accept_rate, float* mean_tau, void* stream);
 
+/*
+ * dsd_propose_noalloc -- dsd_propose for callers that cannot allocate device
+ * memory.  The paper has no counterpart: this is a library convenience.
+ *
+ * Some callers cannot call cudaMalloc: an inference engine that hands all of
+ * device memory to its own pool and forbids plugins to allocate, code that
+ * runs while a stream is being captured in a mode that forbids allocation,
+ * or a latency-critical loop that must not pay an allocation's implicit
+ * synchronisation.  They cannot create a dsd_ctx, whose workspace is
+ * allocated, so this call takes the configuration fields directly (their
+ * meaning and limits as in dsd_config) and computes exactly what dsd_propose
+ * computes with the CUDA-core engine, on the current device.
+ *
+ * Its scratch (argmax keys and log-sum-exp partials, about 2 MB) is a
+ * fixed-size array in the library's device memory, held by every GPU that
+ * loads the library until the process exits.  Limits: R * gamma <= 1024;
+ * larger calls return DSD_ERR_SHAPE without launching anything.  The call
+ * allocates nothing (no cudaMalloc, cudaFree or allocating library routine).
+ * All calls on a device share that array and each call leaves its contents
+ * behind; the parts that must start at zero are cleared at the start of
+ * every call.  Calls whose executions overlap on the GPU (other streams,
+ * other host threads) race on the array: serialise them.  The first call on
+ * a device looks up the array's device address with that device current;
+ * make that first call before any stream capture.  Device-side problems
+ * (non-finite logits) show up as non-finite lse_q / logit_at_tok values.
+ */
+int dsd_propose_noalloc(int V, int rank, int gamma, int dtype, int act, int bias_at_first,
+                        int R, const void* U, const void* E, const void* W, const float* conf,
+                        const int32_t* prev_tok, const uint32_t* req_id, float temperature,
+                        uint64_t seed, int32_t* tokens, float* lse_q, float* logit_at_tok,
+                        float* survival, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -35,6 +35,7 @@ EXPORTED = [
     "dsd_create", "dsd_destroy", "dsd_last_error", "dsd_sync_status", "dsd_workspace_bytes",
     "dsd_launch_count",
     "dsd_propose", "dsd_schedule", "dsd_verify", "dsd_cycle", "dsd_cycle_host", "dsd_overlap",
+    "dsd_propose_noalloc",
 ]
 
 
@@ -83,6 +84,8 @@ def load_library(path: str | None = None):
         "dsd_cycle_host": (_I, [_P, _I, _P, _P, _P, _P, _P, _P, _P, _P, _I, _F, _U64,
                                 _P, _P, _P, _P, _P]),
         "dsd_overlap": (_I, [_P, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
+        "dsd_propose_noalloc": (_I, [_I, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _F,
+                                     _U64, _P, _P, _P, _P, _P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -186,6 +189,22 @@ def dsd_overlap(ctx, N, P_logits, Q_logits, valid_len, a, l1, tau, accept_rate, 
     _check(ctx, load_library().dsd_overlap(
         ctx, N, _ptr(P_logits), _ptr(Q_logits), _ptr(valid_len), _ptr(a), _ptr(l1), _ptr(tau),
         _ptr(accept_rate), _ptr(mean_tau), _stream(stream, device)))
+
+
+def dsd_propose_noalloc(V, rank, gamma, dtype, act, bias_at_first, R, U, E, W, conf, prev_tok,
+                        req_id, temperature, seed, tokens, lse_q, logit_at_tok, survival,
+                        stream=None, device=0):
+    """Propose without a context and without allocating device memory (for
+    callers that may not allocate); scratch lives in a fixed array inside the
+    library.  R * gamma <= 1024."""
+    rc = load_library().dsd_propose_noalloc(
+        int(V), int(rank), int(gamma), DTYPES[dtype] if isinstance(dtype, str) else int(dtype),
+        ACTS[act] if isinstance(act, str) else int(act), int(bool(bias_at_first)), int(R),
+        _ptr(U), _ptr(E), _ptr(W), _ptr(conf), _ptr(prev_tok), _ptr(req_id), float(temperature),
+        int(seed) & (2 ** 64 - 1), _ptr(tokens), _ptr(lse_q), _ptr(logit_at_tok), _ptr(survival),
+        _stream(stream, device))
+    if rc != DSD_OK:
+        raise DsdError(rc, "dsd_propose_noalloc")
 
 
 # ------------------------------------------------------------ convenience
