@@ -57,6 +57,7 @@ size_t carve(dsd_ctx* c, unsigned char* base) {
   w.res_keys = reinterpret_cast<unsigned long long*>(take(sizeof(unsigned long long) * 2 * (size_t)Rm));
   w.res_sums = reinterpret_cast<float*>(take(sizeof(float) * 2 * (size_t)Rm));
   w.ov_parts = reinterpret_cast<float*>(take(sizeof(float) * 64));
+  w.gbar = reinterpret_cast<unsigned int*>(take(sizeof(unsigned int) * 64));
   if (base) c->ws = w;
   return off;
 }
@@ -91,7 +92,7 @@ bool use_tc(const dsd_ctx* ctx, int R) {
   if (ctx->cfg.dtype != DSD_BF16) return false;
   if (ctx->cfg.engine == DSD_ENGINE_SIMT) return false;
   if (ctx->cfg.engine == DSD_ENGINE_TCGEN05) return true;
-  return R >= 16 && ctx->cfg.rank % 64 == 0;
+  return R >= 16 && ctx->cfg.rank % 64 == 0 && ctx->cfg.act == DSD_ACT_NONE;
 }
 
 }  // namespace

@@ -1,19 +1,592 @@
-// tcgen05 path of the Markov-head bias projection (not built yet).
+// tcgen05 (5th-generation tensor core) engine of dsd_propose: all gamma
+// sequential draft steps of a batch of up to 256 requests in ONE persistent
+// cooperative launch, one CTA per SM.
+//
+// Pages: "Qwen3.8-Flash-Next DSpark 训练实验", Baseline 架构 / Markov 顺序修正
+// (m_i = W_1[t_{i-1}], b_i = W_2 m_i, l_i = l_i^0 + b_i, greedy argmax over the
+// full vocabulary); "DSpark notes" 2.3 (one lookup plus one low-rank
+// projection per step); "DSpark 论文精读" 2.2 (x_j ~ Softmax(U_j + b)).
+//
+// Per draft step j the bias projection of the whole batch is the GEMM
+//     D[R, V] = M[R, r] * W[V, r]^T,    M[r_, :] = E[x_{r_, j-1}, :]
+// with requests on the MMA's M dimension (two 128-row M-tiles for R = 256)
+// and the vocabulary on N (tiles of 128).  Each CTA owns a contiguous range
+// of vocabulary tiles for all steps.  Warp roles (12 warps):
+//   warp 0      TMA producer of W tiles ([128 vocab x 64 K] boxes, 128-byte
+//               swizzle, L2 evict-last: W stays resident across the steps)
+//   warp 1      TMEM allocator and the single thread that issues tcgen05.mma
+//               (M = 128, N = 128, K = 16 per instruction) into two
+//               double-buffered fp32 accumulators per M-tile (512 columns)
+//   warp 2      TMA producer of U tiles ([128 requests x 64 vocab] boxes of
+//               the [V, gamma, R] view, evict-first: U is read once)
+//   warps 4-11  epilogue: thread = one request row.  tcgen05.ld brings 32
+//               accumulator columns, U comes from shared memory, and the
+//               biased logits are folded into a running base-2 log-sum-exp and
+//               an argmax (greedy) or Gumbel-max (sampled) key; they never
+//               leave registers.  The same warps gather the next step's A
+//               operand (rows of E for the tokens just chosen) into shared
+//               memory in the UMMA K-major 128-byte-swizzled layout.
+// Between steps the CTAs publish per-request partials (atomicMax of the
+// packed argmax key, (m, s) log-sum-exp partial) and meet at a grid barrier
+// whose wait is bounded: on time-out the kernel records DSD_ERR_TIMEOUT,
+// stops issuing work, waits (bounded) for its own copies in flight, frees
+// its TMEM and returns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <stdio.h>
 
 #include "dsd_common.cuh"
+#include "tc_ptx.cuh"
 
 namespace dsd {
 
-int tc_supported(const Ctx&, char* why, size_t why_len) {
-  snprintf(why, why_len, "tcgen05 propose engine not available in this build");
-  return 0;
+namespace {
+
+constexpr int kTcThreads = 384;
+constexpr int kTileN = 128;          // vocabulary rows per tile (UMMA N)
+constexpr int kTileM = 128;          // requests per M-tile (UMMA M)
+constexpr int kMaxMT = 2;            // M-tiles per launch (R <= 256)
+constexpr int kKChunk = 64;          // K elements per 128-byte swizzle row
+constexpr int kMaxKC = 4;            // rank <= 256
+constexpr int kStageBytes = 16384;   // one [128 x 64] bf16 box
+constexpr int kNB = 3;               // W ring stages
+constexpr int kNU = 3;               // U ring slots
+constexpr int kTmemCols = 512;
+constexpr uint32_t kIdesc = tc::idesc_bf16_f32(kTileM, kTileN);
+
+constexpr int kOffA = 0;
+constexpr int kOffB = kOffA + kMaxMT * kMaxKC * kStageBytes;  // 128 KB
+constexpr int kOffU = kOffB + kNB * kStageBytes;              // +48 KB
+constexpr int kOffBar = kOffU + kNU * kStageBytes;            // +48 KB
+constexpr int kNumBars = 2 * kNB + 2 * kNU + 4 + 2;
+constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 64 + 1024;  // + alignment slack
+static_assert(kSmemBytes <= 232448, "shared memory budget of one CTA");
+
+constexpr uint32_t kSpinLimit = 1u << 22;        // mbarrier polls before giving up
+constexpr uint32_t kGridSpinLimit = 1u << 22;    // grid-barrier polls (with nanosleep)
+
+struct TcParams {
+  const __nv_bfloat16* E;
+  const int32_t* prev_tok;
+  const uint32_t* req_id;
+  unsigned long long* keys;  // [gamma][R_max]
+  float2* parts;             // [gamma][n_part][R_max]
+  unsigned int* gbar;        // grid barrier counter of this launch (zeroed)
+  int* status;
+  int R, R_max, r_off, V, rank, gamma, bias_at_first, n_part, ntiles, MT, sampled;
+  float inv_T;
+  uint32_t k0, k1;
+};
+
+struct Bars {
+  uint64_t* bfull;
+  uint64_t* bempty;
+  uint64_t* ufull;
+  uint64_t* uempty;
+  uint64_t* accfull;
+  uint64_t* accempty;
+  uint64_t* aready;
+  uint64_t* mmadone;
+};
+
+__device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                         int* status) {
+  for (uint32_t i = 0; i < kSpinLimit; ++i) {
+    if (tc::mbar_try_wait(bar, parity)) return true;
+    if ((i & 255u) == 255u && *abort_flag) return false;
+  }
+  set_status(status, kErrTimeout);
+  *abort_flag = 1;
+  return false;
 }
 
-int tc_grid(const Ctx& ctx) { return ctx.num_sms; }
+// Bounded wait that ignores the abort flag: used to drain copies in flight
+// before the CTA exits.
+__device__ __forceinline__ void drain_bar(uint64_t* bar, uint32_t parity) {
+  for (uint32_t i = 0; i < (1u << 20); ++i)
+    if (tc::mbar_try_wait(bar, parity)) return;
+}
 
-cudaError_t launch_propose_tc(const Ctx&, const ProposeArgs&, cudaStream_t) {
-  return cudaErrorNotSupported;
+// Warp-uniform bounded wait: lane 0 polls, the verdict is broadcast, so the
+// warp stays converged for the .sync.aligned tcgen05 instructions after it.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                          int* status) {
+  int ok = 0;
+  if ((threadIdx.x & 31) == 0) ok = wait_bar(bar, parity, abort_flag, status) ? 1 : 0;
+  ok = __shfl_sync(0xffffffffu, ok, 0);
+  __syncwarp();
+  return ok != 0;
+}
+__device__ __forceinline__ bool warp_aborted(volatile int* abort_flag) {
+  int a = 0;
+  if ((threadIdx.x & 31) == 0) a = *abort_flag;
+  return __shfl_sync(0xffffffffu, a, 0) != 0;
+}
+
+__device__ __forceinline__ void named_bar_epilogue() {
+  asm volatile("bar.sync 1, 256;" ::: "memory");
+}
+
+__device__ __forceinline__ unsigned int ld_acquire_u32(const unsigned int* p) {
+  unsigned int v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Process 32 consecutive columns of one request row: x = acc + u (fp32),
+// masked beyond V; fold into the base-2 log-sum-exp and the argmax key.
+struct RowState {
+  float m2, s, best_z;
+  uint32_t best_v;
+};
+
+__device__ __forceinline__ void fold32(RowState& st, const uint32_t (&acc)[32],
+                                       const uint4 (&u)[4], int v0, int V, const TcParams& p,
+                                       int pos, uint32_t rid) {
+  float xs[32];
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    const uint32_t w[4] = {u[c].x, u[c].y, u[c].z, u[c].w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      xs[c * 8 + 2 * e] = __uint_as_float(acc[c * 8 + 2 * e]) + bf16lo(w[e]);
+      xs[c * 8 + 2 * e + 1] = __uint_as_float(acc[c * 8 + 2 * e + 1]) + bf16hi(w[e]);
+    }
+  }
+  if (v0 + 32 > V) {
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+      if (v0 + i >= V) xs[i] = -INFINITY;
+  }
+  if (p.sampled) {
+#pragma unroll
+    for (int i = 0; i < 32; ++i) xs[i] *= p.inv_T;
+  }
+  float cm = -INFINITY;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) cm = fmaxf(cm, xs[i]);
+  const float M = fmaxf(st.m2, cm * kLog2e);
+  if (M != -INFINITY) {
+    float acc_s = 0.f;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) acc_s += exp2f(fmaf(xs[i], kLog2e, -M));
+    st.s = st.s * exp2f(st.m2 - M) + acc_s;
+    st.m2 = M;
+  }
+  if (!p.sampled) {
+    if (cm > st.best_z) {
+      int idx = 31;
+#pragma unroll
+      for (int i = 31; i >= 0; --i)
+        if (xs[i] == cm) idx = i;
+      st.best_z = cm;
+      st.best_v = (uint32_t)(v0 + idx);
+    }
+  } else {
+    float zb = st.best_z;
+    uint32_t vb = st.best_v;
+#pragma unroll
+    for (int g = 0; g < 8; ++g) {
+      const uint32_t v = (uint32_t)(v0 + 4 * g);
+      const Philox4 ph = philox4x32_10(v >> 2, (uint32_t)pos, rid, 0u, p.k0, p.k1);
+      const float z0 = xs[4 * g + 0] + gumbel_from_word(ph.x);
+      const float z1 = xs[4 * g + 1] + gumbel_from_word(ph.y);
+      const float z2 = xs[4 * g + 2] + gumbel_from_word(ph.z);
+      const float z3 = xs[4 * g + 3] + gumbel_from_word(ph.w);
+      if (z0 > zb) { zb = z0; vb = v + 0; }
+      if (z1 > zb) { zb = z1; vb = v + 1; }
+      if (z2 > zb) { zb = z2; vb = v + 2; }
+      if (z3 > zb) { zb = z3; vb = v + 3; }
+    }
+    st.best_z = zb;
+    st.best_v = vb;
+  }
+}
+
+__global__ void __launch_bounds__(kTcThreads, 1)
+    propose_tc_kernel(const __grid_constant__ CUtensorMap tmW,
+                      const __grid_constant__ CUtensorMap tmU, const TcParams p) {
+  extern __shared__ unsigned char smem_raw[];
+  const uint32_t raw = tc::smem_u32(smem_raw);
+  unsigned char* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
+  unsigned char* sA = smem + kOffA;
+  unsigned char* sB = smem + kOffB;
+  unsigned char* sU = smem + kOffU;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
+  Bars b{bars, bars + kNB, bars + 2 * kNB, bars + 2 * kNB + kNU, bars + 2 * kNB + 2 * kNU,
+         bars + 2 * kNB + 2 * kNU + 2, bars + 2 * kNB + 2 * kNU + 4,
+         bars + 2 * kNB + 2 * kNU + 5};
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + kNumBars);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + kNumBars) + 1;
+  volatile int* stop_all = reinterpret_cast<volatile int*>(bars + kNumBars) + 2;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int MT = p.MT;
+  const int KC = p.rank / kKChunk;
+  const int G = p.gamma;
+  const int t0 = (int)(((long long)blockIdx.x * p.ntiles) / gridDim.x);
+  const int t1 = (int)(((long long)(blockIdx.x + 1) * p.ntiles) / gridDim.x);
+  const int nt = t1 - t0;
+  // U boxes of a step: every tile has two 64-column halves per M-tile, except
+  // that a second half lying wholly beyond V is never loaded.
+  const bool last_half_skipped = (t1 == p.ntiles) && ((t1 - 1) * kTileN + 64 >= p.V);
+  const int boxes_per_step = nt * 2 * MT - (last_half_skipped ? MT : 0);
+
+  if (tid == 0) {
+    for (int i = 0; i < kNB; ++i) {
+      tc::mbar_init(&b.bfull[i], 1);
+      tc::mbar_init(&b.bempty[i], 1);
+    }
+    for (int i = 0; i < kNU; ++i) {
+      tc::mbar_init(&b.ufull[i], 1);
+      tc::mbar_init(&b.uempty[i], 4);
+    }
+    for (int i = 0; i < 2; ++i) {
+      tc::mbar_init(&b.accfull[i], 1);
+      tc::mbar_init(&b.accempty[i], 4 * MT);
+    }
+    tc::mbar_init(b.aready, 8);
+    tc::mbar_init(b.mmadone, 1);
+    *abort_flag = 0;
+    *stop_all = 0;
+    tc::mbar_fence_init();
+    tc::fence_proxy_async_smem();
+    tc::prefetch_tensormap(&tmW);
+    tc::prefetch_tensormap(&tmU);
+  }
+  if (warp == 1) {
+    tc::tmem_alloc(tmem_holder, kTmemCols);
+    tc::tmem_relinquish();
+  }
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tmem_base = *tmem_holder;
+
+  if (warp == 0) {
+    // ------------------------------------------------------ W producer
+    if (lane == 0) {
+      const uint64_t pol = policy_evict_last();
+      uint32_t it = 0;
+      for (int j = 0; j < G && !*abort_flag; ++j)
+        for (int t = t0; t < t1 && !*abort_flag; ++t)
+          for (int kc = 0; kc < KC; ++kc, ++it) {
+            const int s = it % kNB;
+            if (!wait_bar(&b.bempty[s], ((it / kNB) & 1) ^ 1, abort_flag, p.status)) break;
+            tc::mbar_arrive_expect_tx(&b.bfull[s], kStageBytes);
+            tc::tma_load_2d(sB + s * kStageBytes, &tmW, &b.bfull[s], kc * kKChunk, t * kTileN, pol);
+          }
+      // wait (bounded) for the copies this thread issued last in each stage
+      for (uint32_t k = (it > kNB ? it - kNB : 0); k < it; ++k)
+        drain_bar(&b.bfull[k % kNB], (k / kNB) & 1);
+    }
+  } else if (warp == 2) {
+    // ------------------------------------------------------ U producer
+    if (lane == 0) {
+      const uint64_t pol = policy_evict_first();
+      uint32_t it = 0;
+      for (int j = 0; j < G && !*abort_flag; ++j)
+        for (int t = t0; t < t1 && !*abort_flag; ++t)
+          for (int h = 0; h < 2; ++h) {
+            const int vx = t * kTileN + h * 64;
+            if (vx >= p.V) continue;
+            for (int m = 0; m < MT; ++m, ++it) {
+              const int s = it % kNU;
+              if (!wait_bar(&b.uempty[s], ((it / kNU) & 1) ^ 1, abort_flag, p.status)) break;
+              tc::mbar_arrive_expect_tx(&b.ufull[s], kStageBytes);
+              tc::tma_load_3d(sU + s * kStageBytes, &tmU, &b.ufull[s], vx, j,
+                              p.r_off + m * kTileM, pol);
+            }
+          }
+      for (uint32_t k = (it > kNU ? it - kNU : 0); k < it; ++k)
+        drain_bar(&b.ufull[k % kNU], (k / kNU) & 1);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      uint32_t bit = 0, tcount = 0;
+      bool ok = true;
+      for (int j = 0; j < G && ok; ++j) {
+        ok = wait_bar(b.aready, j & 1, abort_flag, p.status);
+        tc::tc_fence_after();
+        for (int t = t0; t < t1 && ok; ++t, ++tcount) {
+          const int buf = tcount & 1;
+          ok = wait_bar(&b.accempty[buf], ((tcount >> 1) & 1) ^ 1, abort_flag, p.status);
+          if (!ok) break;
+          tc::tc_fence_after();
+          for (int kc = 0; kc < KC; ++kc, ++bit) {
+            const int s = bit % kNB;
+            ok = wait_bar(&b.bfull[s], (bit / kNB) & 1, abort_flag, p.status);
+            if (!ok) break;
+            tc::tc_fence_after();
+            const uint32_t b_base = tc::smem_u32(sB + s * kStageBytes);
+            for (int m = 0; m < MT; ++m) {
+              const uint32_t d_tmem = tmem_base + (uint32_t)((buf * 2 + m) * kTileN);
+              const uint32_t a_base = tc::smem_u32(sA + (m * kMaxKC + kc) * kStageBytes);
+#pragma unroll
+              for (int ks = 0; ks < kKChunk / 16; ++ks) {
+                tc::umma_bf16(d_tmem, tc::sdesc_kmajor_sw128(a_base + ks * 32),
+                              tc::sdesc_kmajor_sw128(b_base + ks * 32), kIdesc,
+                              (kc | ks) != 0 ? 1u : 0u);
+              }
+            }
+            tc::umma_commit(&b.bempty[s]);
+          }
+          if (ok) tc::umma_commit(&b.accfull[buf]);
+        }
+      }
+      // all issued MMAs complete before TMEM is released
+      tc::umma_commit(b.mmadone);
+      for (uint32_t i = 0; i < kSpinLimit; ++i)
+        if (tc::mbar_try_wait(b.mmadone, 0)) break;
+    }
+  } else if (warp >= 4) {
+    // ------------------------------------------------------ epilogue
+    const int e = warp - 4;          // 0..7
+    const int g = e >> 2;            // M-tile of this warp
+    const int q = warp & 3;          // TMEM lane quarter this warp may access
+    const int row = q * 32 + lane;   // row within the M-tile
+    const int r = p.r_off + g * kTileM + row;
+    const bool active = g < MT;
+    const bool valid = active && r < p.R;
+    const uint32_t rid = valid ? (p.req_id ? p.req_id[r] : (uint32_t)r) : 0u;
+    uint32_t tcount = 0;
+    const int rows_total = MT * kTileM;
+    for (int j = 0; j < G; ++j) {
+      // ---- A operand of step j: rows of E for the previous tokens ----
+      const bool biased = (j > 0) || p.bias_at_first;
+      for (int ri = e; ri < rows_total; ri += 8) {
+        const int rr = p.r_off + ri;
+        int tok = 0;
+        bool use = biased && rr < p.R;
+        if (use) {
+          tok = (j == 0) ? p.prev_tok[rr]
+                         : (int)key_index(__ldcg(&p.keys[(size_t)(j - 1) * p.R_max + rr]));
+          if (tok < 0 || tok >= p.V) {
+            set_status(p.status, kErrArg);
+            tok = 0;
+          }
+        }
+        const int mt = ri / kTileM, ir = ri % kTileM;
+        for (int c = lane; c < p.rank / 8; c += 32) {
+          uint4 v = make_uint4(0u, 0u, 0u, 0u);
+          if (use) v = ld_keep16(p.E + (size_t)tok * p.rank + c * 8);
+          const int kc = c >> 3, cc = c & 7;
+          *reinterpret_cast<uint4*>(sA + (mt * kMaxKC + kc) * kStageBytes + ir * 128 +
+                                    ((cc ^ (ir & 7)) << 4)) = v;
+        }
+      }
+      tc::fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(b.aready);
+
+      // ---- tiles ----
+      RowState st{-INFINITY, 0.f, -INFINITY, 0u};
+      for (int tt = 0; tt < nt; ++tt, ++tcount) {
+        if (!active || warp_aborted(abort_flag)) continue;
+        const int t = t0 + tt;
+        const int buf = tcount & 1;
+        if (!warp_wait(&b.accfull[buf], (tcount >> 1) & 1, abort_flag, p.status)) continue;
+        tc::tc_fence_after();
+        for (int h = 0; h < 2; ++h) {
+          const int vx = t * kTileN + h * 64;
+          if (vx >= p.V) continue;
+          const uint32_t uit = (uint32_t)(j * boxes_per_step + tt * 2 * MT + h * MT + g);
+          const int s = uit % kNU;
+          if (!warp_wait(&b.ufull[s], (uit / kNU) & 1, abort_flag, p.status)) break;
+          const unsigned char* urow = sU + s * kStageBytes + row * 128;
+#pragma unroll
+          for (int half = 0; half < 2; ++half) {
+            uint32_t acc[32];
+            tc::tmem_ld_32x32b_x32(tmem_base + ((uint32_t)(q * 32) << 16) +
+                                       (uint32_t)((buf * 2 + g) * kTileN + h * 64 + half * 32),
+                                   acc);
+            uint4 u[4];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+              const int cl = half * 4 + c;
+              u[c] = *reinterpret_cast<const uint4*>(urow + ((cl ^ (row & 7)) << 4));
+            }
+            tc::tmem_wait_ld();
+            fold32(st, acc, u, vx + half * 32, p.V, p, j, rid);
+          }
+          __syncwarp();
+          if (lane == 0) tc::mbar_arrive(&b.uempty[s]);
+        }
+        tc::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(&b.accempty[buf]);
+      }
+
+      // ---- publish this CTA's partials of step j ----
+      if (valid) {
+        if (st.best_z != -INFINITY || st.s != 0.f)
+          atomicMax(&p.keys[(size_t)j * p.R_max + r], make_key(st.best_z, st.best_v));
+        p.parts[((size_t)j * p.n_part + blockIdx.x) * p.R_max + r] = make_float2(st.m2, st.s);
+      }
+      __threadfence();
+      named_bar_epilogue();
+      if (j + 1 < G) {
+        // ---- grid barrier (bounded) ----
+        if (e == 0 && lane == 0 && !*abort_flag) {
+          atomicAdd(p.gbar, 1u);
+          const unsigned int target = (unsigned int)(j + 1) * gridDim.x;
+          bool done = false;
+          for (uint32_t i = 0; i < kGridSpinLimit; ++i) {
+            if (ld_acquire_u32(p.gbar) >= target) {
+              done = true;
+              break;
+            }
+            __nanosleep(64);
+          }
+          if (!done) {
+            set_status(p.status, kErrTimeout);
+            *abort_flag = 1;
+          }
+        }
+        // one thread decides for all eight epilogue warps, so that they all
+        // leave (or all continue) together and the named barrier stays matched
+        if (e == 0 && lane == 0) *stop_all = *abort_flag;
+        named_bar_epilogue();
+        if (*stop_all) {
+          // let the MMA warp leave its wait for the next step's operand
+          if (lane == 0) tc::mbar_arrive(b.aready);
+          break;
+        }
+      }
+    }
+  }
+  __syncthreads();
+  if (warp == 1) {
+    tc::tc_fence_after();
+    tc::tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  }
+  return fn;
+}
+
+}  // namespace
+
+int tc_supported(const Ctx& ctx, char* why, size_t why_len) {
+  if (ctx.cfg.dtype != 1) {
+    snprintf(why, why_len, "tcgen05 engine needs bf16 tables");
+    return 0;
+  }
+  if (ctx.cfg.rank % kKChunk != 0 || ctx.cfg.rank > kMaxKC * kKChunk) {
+    snprintf(why, why_len, "tcgen05 engine needs a Markov rank that is a multiple of 64, <= 256");
+    return 0;
+  }
+  if (ctx.cfg.act != kActNone) {
+    snprintf(why, why_len, "tcgen05 engine runs without an activation (bf16 operands)");
+    return 0;
+  }
+  if (!encode_fn()) {
+    snprintf(why, why_len, "cuTensorMapEncodeTiled is not available from the driver");
+    return 0;
+  }
+  int coop = 0, smem = 0;
+  cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, ctx.cfg.device);
+  cudaDeviceGetAttribute(&smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, ctx.cfg.device);
+  if (!coop || smem < kSmemBytes) {
+    snprintf(why, why_len, "device lacks cooperative launch or %d bytes of shared memory",
+             kSmemBytes);
+    return 0;
+  }
+  return 1;
+}
+
+int tc_grid(const Ctx& ctx) {
+  const int ntiles = (ctx.cfg.V + kTileN - 1) / kTileN;
+  return ntiles < ctx.num_sms ? ntiles : ctx.num_sms;
+}
+
+cudaError_t launch_propose_tc(const Ctx& ctx, const ProposeArgs& a, cudaStream_t s) {
+  PFN_cuTensorMapEncodeTiled_v12000 encode = encode_fn();
+  if (!encode) return cudaErrorNotSupported;
+  CUtensorMap tmW, tmU;
+  {
+    const cuuint64_t dims[2] = {(cuuint64_t)a.rank, (cuuint64_t)a.V};
+    const cuuint64_t strides[1] = {(cuuint64_t)a.rank * 2};
+    const cuuint32_t box[2] = {kKChunk, kTileN};
+    const cuuint32_t estr[2] = {1, 1};
+    if (encode(&tmW, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(a.W), dims, strides,
+               box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  {
+    const cuuint64_t dims[3] = {(cuuint64_t)a.V, (cuuint64_t)a.gamma, (cuuint64_t)a.R};
+    const cuuint64_t strides[2] = {(cuuint64_t)a.V * 2, (cuuint64_t)a.V * 2 * a.gamma};
+    const cuuint32_t box[3] = {64, 1, kTileM};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    if (encode(&tmU, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(a.U), dims, strides,
+               box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  cudaError_t e = cudaMemsetAsync(ctx.ws.keys, 0,
+                                  sizeof(unsigned long long) * (size_t)a.gamma * ctx.cfg.R_max, s);
+  if (e != cudaSuccess) return e;
+  const int groups = (a.R + kMaxMT * kTileM - 1) / (kMaxMT * kTileM);
+  e = cudaMemsetAsync(ctx.ws.gbar, 0, sizeof(unsigned int) * (size_t)groups, s);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(propose_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           kSmemBytes);
+  if (e != cudaSuccess) return e;
+
+  TcParams p{};
+  p.E = static_cast<const __nv_bfloat16*>(a.E);
+  p.prev_tok = a.prev_tok;
+  p.req_id = a.req_id;
+  p.keys = ctx.ws.keys;
+  p.parts = ctx.ws.lse_parts;
+  p.status = ctx.ws.status;
+  p.R = a.R;
+  p.R_max = ctx.cfg.R_max;
+  p.V = a.V;
+  p.rank = a.rank;
+  p.gamma = a.gamma;
+  p.bias_at_first = a.bias_at_first;
+  p.n_part = ctx.n_part;
+  p.ntiles = (a.V + kTileN - 1) / kTileN;
+  p.sampled = a.temperature > 0.f ? 1 : 0;
+  p.inv_T = a.temperature > 0.f ? 1.f / a.temperature : 1.f;
+  p.k0 = (uint32_t)(a.seed & 0xFFFFFFFFull);
+  p.k1 = (uint32_t)(a.seed >> 32);
+  const int grid = tc_grid(ctx);
+
+  for (int gi = 0; gi < groups; ++gi) {
+    p.r_off = gi * kMaxMT * kTileM;
+    const int rem = a.R - p.r_off;
+    p.MT = rem > kTileM ? 2 : 1;
+    p.gbar = ctx.ws.gbar + gi;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kTcThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, propose_tc_kernel, tmW, tmU, p);
+    if (e != cudaSuccess) return e;
+    count_launch(ctx);
+  }
+  return cudaSuccess;
 }
 
 }  // namespace dsd
