@@ -35,6 +35,7 @@ TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 KERNEL_SOURCES = {
     "simt_bias_kernel": ["propose_simt.cu", "dsd_common.cuh"],
     "propose_tc_kernel": ["propose_tc.cu", "dsd_common.cuh"],
+    "propose_mma_kernel": ["propose_mma.cu", "dsd_common.cuh"],
 }
 FALLBACK_HBM_GBS = 6800.0
 
@@ -444,7 +445,9 @@ def run_ours(args):
     pbytes = propose_alg_bytes(spec)
     prop_mean_s = statistics.mean(prop_ms) / 1e3
     achieved = pbytes / prop_mean_s / 1e9
-    engine_kernel = "propose_tc_kernel" if ctx_engine_is_tc(ctx, spec) else "simt_bias_kernel"
+    engine_used = ctx.last_engine()
+    engine_kernel = {"tcgen05": "propose_tc_kernel", "mma": "propose_mma_kernel"}.get(
+        engine_used, "simt_bias_kernel")
     roofline = {"bound": "hbm", "kernel": f"propose phase ({engine_kernel})",
                 "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                 "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)",
@@ -470,7 +473,8 @@ def run_ours(args):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": spec.dtype, "accumulate": "fp32", "data": "synthetic",
         "config": {"workload": workload_label(spec), "R": spec.R, "gamma": spec.G, "V": spec.V,
-                   "rank": spec.r, "temperature": spec.temperature, "engine": args.engine,
+                   "rank": spec.r, "temperature": spec.temperature,
+                   "engine": f"{args.engine} -> {engine_used}",
                    "verify_batch_B": B, "parallelism": f"replicas x{world}",
                    "l2": "flushed between steps (512 MB write outside the events); inputs 1.2 GB"},
         "phases_ms": {"propose": statistics.mean(prop_ms), "schedule": statistics.mean(sch_ms),
@@ -492,14 +496,6 @@ def run_ours(args):
     return 0
 
 
-def ctx_engine_is_tc(ctx, spec):
-    if spec.dtype != "bf16":
-        return False
-    import semi_autoregressive_draft_gb300 as dsd
-
-    return getattr(dsd, "TC_AVAILABLE", False) and spec.R >= 16
-
-
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -508,7 +504,7 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="highconc",
                     choices=["highconc", "greedy", "sampled", "tiny"])
-    ap.add_argument("--engine", default="auto", choices=["auto", "simt", "tcgen05"])
+    ap.add_argument("--engine", default="auto", choices=["auto", "simt", "mma"])
     ap.add_argument("--cpu-requests", type=int, default=128,
                     help="requests in the CPU-baseline sample")
     ap.add_argument("--ref-requests", type=int, default=16,

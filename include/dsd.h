@@ -70,9 +70,17 @@ enum dsd_status {
 
 enum dsd_dtype { DSD_F32 = 0, DSD_BF16 = 1 };
 enum dsd_act { DSD_ACT_NONE = 0, DSD_ACT_SILU = 1 };
-/* Propose engine: AUTO picks tcgen05 tensor cores for bf16 batches of at
- * least 16 requests and the CUDA-core path otherwise. */
-enum dsd_engine { DSD_ENGINE_AUTO = 0, DSD_ENGINE_SIMT = 1, DSD_ENGINE_TCGEN05 = 2 };
+/* Propose engine.  AUTO picks the warp-level tensor-core engine (MMA) for
+ * bf16 tables, no activation and batches of at least 16 requests, and the
+ * CUDA-core engine (SIMT) otherwise.  TCGEN05 (5th-generation tensor cores
+ * with TMEM accumulators) is built but disabled: dsd_propose returns
+ * DSD_ERR_UNSUPPORTED for it. */
+enum dsd_engine {
+  DSD_ENGINE_AUTO = 0,
+  DSD_ENGINE_SIMT = 1,
+  DSD_ENGINE_TCGEN05 = 2,
+  DSD_ENGINE_MMA = 3
+};
 
 typedef struct dsd_config {
   int V;             /* vocabulary size, multiple of 8 */
@@ -110,6 +118,11 @@ size_t dsd_workspace_bytes(const dsd_ctx* ctx);
 /* Number of kernels this context has launched so far (host-side count of
  * every <<<>>> launch made by the calls below; memsets are not counted). */
 uint64_t dsd_launch_count(const dsd_ctx* ctx);
+
+/* Engine that ran the last dsd_propose on this context: DSD_ENGINE_SIMT,
+ * DSD_ENGINE_MMA or DSD_ENGINE_TCGEN05 (DSD_ENGINE_AUTO before the first
+ * call). */
+int dsd_last_engine(const dsd_ctx* ctx);
 
 /*
  * dsd_propose -- sequential Markov-head proposal plus prefix survival.

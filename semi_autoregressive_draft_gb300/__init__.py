@@ -29,11 +29,11 @@ STATUS_NAMES = {
 DTYPES = {"f32": 0, "bf16": 1}
 TORCH_DTYPES = {"f32": torch.float32, "bf16": torch.bfloat16}
 ACTS = {"none": 0, "silu": 1}
-ENGINES = {"auto": 0, "simt": 1, "tcgen05": 2}
+ENGINES = {"auto": 0, "simt": 1, "tcgen05": 2, "mma": 3}
 
 EXPORTED = [
     "dsd_create", "dsd_destroy", "dsd_last_error", "dsd_sync_status", "dsd_workspace_bytes",
-    "dsd_launch_count",
+    "dsd_launch_count", "dsd_last_engine",
     "dsd_propose", "dsd_schedule", "dsd_verify", "dsd_cycle", "dsd_cycle_host", "dsd_overlap",
     "dsd_propose_noalloc",
 ]
@@ -76,6 +76,7 @@ def load_library(path: str | None = None):
         "dsd_sync_status": (_I, [_P, _P]),
         "dsd_workspace_bytes": (ctypes.c_size_t, [_P]),
         "dsd_launch_count": (_U64, [_P]),
+        "dsd_last_engine": (_I, [_P]),
         "dsd_propose": (_I, [_P, _I, _P, _P, _P, _P, _P, _P, _F, _U64, _P, _P, _P, _P, _P]),
         "dsd_schedule": (_I, [_P, _I, _P, _P, _I, _P, _P, _P]),
         "dsd_verify": (_I, [_P, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _F, _U64, _P, _P, _P]),
@@ -245,6 +246,11 @@ class Context:
 
     def launch_count(self):
         return int(load_library().dsd_launch_count(self.handle))
+
+    def last_engine(self):
+        """'simt' or 'tcgen05': the engine of the last propose call."""
+        code = int(load_library().dsd_last_engine(self.handle))
+        return {v: k for k, v in ENGINES.items()}.get(code, "auto")
 
     def sync_status(self, stream=None):
         return dsd_sync_status(self.handle, stream, self.device)

@@ -24,6 +24,7 @@ SOURCES = [
     "dsd_api.cu",
     "propose_simt.cu",
     "propose_tc.cu",
+    "propose_mma.cu",
     "propose_noalloc.cu",
     "schedule.cu",
     "verify.cu",

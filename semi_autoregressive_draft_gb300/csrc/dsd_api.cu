@@ -88,11 +88,17 @@ int check_temperature(dsd_ctx* ctx, float T) {
   return DSD_OK;
 }
 
-bool use_tc(const dsd_ctx* ctx, int R) {
-  if (ctx->cfg.dtype != DSD_BF16) return false;
-  if (ctx->cfg.engine == DSD_ENGINE_SIMT) return false;
-  if (ctx->cfg.engine == DSD_ENGINE_TCGEN05) return true;
-  return R >= 16 && ctx->cfg.rank % 64 == 0 && ctx->cfg.act == DSD_ACT_NONE;
+// The warp-level tensor-core engine needs bf16 operands with no activation
+// (the gathered rows are used as stored) and a rank that is a multiple of 64.
+bool mma_ok(const dsd_ctx* ctx) {
+  return ctx->cfg.dtype == DSD_BF16 && ctx->cfg.rank % 64 == 0 && ctx->cfg.rank <= 256 &&
+         ctx->cfg.act == DSD_ACT_NONE;
+}
+
+bool use_mma(const dsd_ctx* ctx, int R) {
+  if (!mma_ok(ctx)) return false;
+  if (ctx->cfg.engine == DSD_ENGINE_MMA) return true;
+  return ctx->cfg.engine == DSD_ENGINE_AUTO && R >= 16;
 }
 
 }  // namespace
@@ -117,8 +123,10 @@ int dsd_create(const dsd_config* cfg, dsd_ctx** out) {
   if (cfg->R_max < 1 || (long long)cfg->R_max * cfg->gamma > kMaxSchedItems) return DSD_ERR_SHAPE;
   if (cfg->dtype != DSD_F32 && cfg->dtype != DSD_BF16) return DSD_ERR_DTYPE;
   if (cfg->act != DSD_ACT_NONE && cfg->act != DSD_ACT_SILU) return DSD_ERR_ARG;
-  if (cfg->engine < DSD_ENGINE_AUTO || cfg->engine > DSD_ENGINE_TCGEN05) return DSD_ERR_ARG;
-  if (cfg->engine == DSD_ENGINE_TCGEN05 && cfg->dtype != DSD_BF16) return DSD_ERR_DTYPE;
+  if (cfg->engine < DSD_ENGINE_AUTO || cfg->engine > DSD_ENGINE_MMA) return DSD_ERR_ARG;
+  if ((cfg->engine == DSD_ENGINE_TCGEN05 || cfg->engine == DSD_ENGINE_MMA) &&
+      cfg->dtype != DSD_BF16)
+    return DSD_ERR_DTYPE;
 
   int ndev = 0;
   if (cudaGetDeviceCount(&ndev) != cudaSuccess || cfg->device < 0 || cfg->device >= ndev)
@@ -167,6 +175,8 @@ const char* dsd_last_error(const dsd_ctx* ctx) { return ctx ? ctx->err : "null c
 size_t dsd_workspace_bytes(const dsd_ctx* ctx) { return ctx ? ctx->ws_bytes : 0; }
 
 uint64_t dsd_launch_count(const dsd_ctx* ctx) { return ctx ? ctx->launches : 0; }
+
+int dsd_last_engine(const dsd_ctx* ctx) { return ctx ? ctx->last_engine : 0; }
 
 int dsd_sync_status(dsd_ctx* ctx, void* stream) {
   int rc = check_ctx(ctx);
@@ -222,16 +232,23 @@ int dsd_propose(dsd_ctx* ctx, int R, const void* U, const void* E, const void* W
   a.survival = survival;
   cudaError_t e;
   int n_used;
-  char why[256];
-  const bool tc_ok = tc_supported(*ctx, why, sizeof(why)) != 0;
-  if (ctx->cfg.engine == DSD_ENGINE_TCGEN05 && !tc_ok)
-    return fail(ctx, DSD_ERR_UNSUPPORTED, "%s", why);
-  if (use_tc(ctx, R) && tc_ok) {
+  if (ctx->cfg.engine == DSD_ENGINE_TCGEN05) {
+    char why[256];
+    if (!tc_supported(*ctx, why, sizeof(why))) return fail(ctx, DSD_ERR_UNSUPPORTED, "%s", why);
     e = launch_propose_tc(*ctx, a, s);
     n_used = tc_grid(*ctx);
+    ctx->last_engine = DSD_ENGINE_TCGEN05;
+  } else if (ctx->cfg.engine == DSD_ENGINE_MMA && !mma_ok(ctx)) {
+    return fail(ctx, DSD_ERR_UNSUPPORTED,
+                "MMA engine needs bf16 tables, no activation and rank %% 64 == 0 (<= 256)");
+  } else if (use_mma(ctx, R)) {
+    e = launch_propose_mma(*ctx, a, s);
+    n_used = mma_vranges(*ctx, R);
+    ctx->last_engine = DSD_ENGINE_MMA;
   } else {
     e = launch_propose_simt(*ctx, a, s);
     n_used = simt_grid(*ctx, a.V);
+    ctx->last_engine = DSD_ENGINE_SIMT;
   }
   if (e != cudaSuccess) return cuda_fail(ctx, e, "propose launch");
   e = launch_propose_finalize_n(*ctx, a, n_used, s);

@@ -62,6 +62,7 @@ struct Ctx {
   size_t stage_bytes;
   char err[512];
   mutable unsigned long long launches;  // kernels launched by this context
+  int last_engine;                      // engine of the last propose (enum dsd_engine)
 };
 
 inline void count_launch(const Ctx& c, int n = 1) { c.launches += (unsigned long long)n; }
@@ -85,6 +86,8 @@ struct ProposeArgs {
 
 cudaError_t launch_propose_simt(const Ctx& ctx, const ProposeArgs& a, cudaStream_t s);
 cudaError_t launch_propose_tc(const Ctx& ctx, const ProposeArgs& a, cudaStream_t s);
+cudaError_t launch_propose_mma(const Ctx& ctx, const ProposeArgs& a, cudaStream_t s);
+int mma_vranges(const Ctx& ctx, int R);
 cudaError_t launch_propose_finalize(const Ctx& ctx, const ProposeArgs& a, cudaStream_t s);
 
 cudaError_t launch_schedule(const Ctx& ctx, int R, const float* survival, const float* sps,

@@ -1,17 +1,16 @@
-// tcgen05 (5th-generation tensor core) engine of dsd_propose: all gamma
-// sequential draft steps of a batch of up to 256 requests in ONE persistent
-// cooperative launch, one CTA per SM.
+// tcgen05 (5th-generation tensor core) engine of dsd_propose: one launch per
+// draft step for a batch of up to 256 requests, one CTA per SM.
 //
 // Pages: "Qwen3.8-Flash-Next DSpark 训练实验", Baseline 架构 / Markov 顺序修正
 // (m_i = W_1[t_{i-1}], b_i = W_2 m_i, l_i = l_i^0 + b_i, greedy argmax over the
 // full vocabulary); "DSpark notes" 2.3 (one lookup plus one low-rank
 // projection per step); "DSpark 论文精读" 2.2 (x_j ~ Softmax(U_j + b)).
 //
-// Per draft step j the bias projection of the whole batch is the GEMM
+// Draft step j's bias projection for the whole batch is the GEMM
 //     D[R, V] = M[R, r] * W[V, r]^T,    M[r_, :] = E[x_{r_, j-1}, :]
 // with requests on the MMA's M dimension (two 128-row M-tiles for R = 256)
 // and the vocabulary on N (tiles of 128).  Each CTA owns a contiguous range
-// of vocabulary tiles for all steps.  Warp roles (12 warps):
+// of vocabulary tiles.  Warp roles (12 warps):
 //   warp 0      TMA producer of W tiles ([128 vocab x 64 K] boxes, 128-byte
 //               swizzle, L2 evict-last: W stays resident across the steps)
 //   warp 1      TMEM allocator and the single thread that issues tcgen05.mma
@@ -19,18 +18,19 @@
 //               double-buffered fp32 accumulators per M-tile (512 columns)
 //   warp 2      TMA producer of U tiles ([128 requests x 64 vocab] boxes of
 //               the [V, gamma, R] view, evict-first: U is read once)
-//   warps 4-11  epilogue: thread = one request row.  tcgen05.ld brings 32
-//               accumulator columns, U comes from shared memory, and the
-//               biased logits are folded into a running base-2 log-sum-exp and
-//               an argmax (greedy) or Gumbel-max (sampled) key; they never
-//               leave registers.  The same warps gather the next step's A
-//               operand (rows of E for the tokens just chosen) into shared
-//               memory in the UMMA K-major 128-byte-swizzled layout.
-// Between steps the CTAs publish per-request partials (atomicMax of the
-// packed argmax key, (m, s) log-sum-exp partial) and meet at a grid barrier
-// whose wait is bounded: on time-out the kernel records DSD_ERR_TIMEOUT,
-// stops issuing work, waits (bounded) for its own copies in flight, frees
-// its TMEM and returns.
+//   warps 4-11  epilogue: first they gather the A operand (rows of E for the
+//               tokens chosen at step j-1) into shared memory in the UMMA
+//               K-major 128-byte-swizzled layout; then thread = one request
+//               row: tcgen05.ld brings 32 accumulator columns, U comes from
+//               shared memory, and the biased logits are folded into a running
+//               base-2 log-sum-exp and an argmax (greedy) or Gumbel-max
+//               (sampled) key; they never leave registers.
+// At the end each CTA publishes per-request partials: atomicMax of the packed
+// argmax key and an (m, s) log-sum-exp partial.  The next step's launch reads
+// the keys, so the kernel boundary is the batch-wide synchronisation between
+// steps.  Every mbarrier wait is bounded: on time-out the kernel records
+// DSD_ERR_TIMEOUT, stops issuing work, waits (bounded) for its own copies in
+// flight, frees its TMEM and returns.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <stdio.h>
@@ -62,8 +62,15 @@ constexpr int kNumBars = 2 * kNB + 2 * kNU + 4 + 2;
 constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 64 + 1024;  // + alignment slack
 static_assert(kSmemBytes <= 232448, "shared memory budget of one CTA");
 
+#ifdef DSD_TC_CHECKS
+// Self-checking build: an out-of-range index records a distinct status code
+// (-100 - site) and the access is skipped instead of performed.
+#define TC_CHECK(cond, site) (((cond)) ? true : (set_status(p.status, -100 - (site)), false))
+#else
+#define TC_CHECK(cond, site) true
+#endif
+
 constexpr uint32_t kSpinLimit = 1u << 22;        // mbarrier polls before giving up
-constexpr uint32_t kGridSpinLimit = 1u << 22;    // grid-barrier polls (with nanosleep)
 
 struct TcParams {
   const __nv_bfloat16* E;
@@ -71,8 +78,8 @@ struct TcParams {
   const uint32_t* req_id;
   unsigned long long* keys;  // [gamma][R_max]
   float2* parts;             // [gamma][n_part][R_max]
-  unsigned int* gbar;        // grid barrier counter of this launch (zeroed)
   int* status;
+  int j;                     // draft position of this launch
   int R, R_max, r_off, V, rank, gamma, bias_at_first, n_part, ntiles, MT, sampled;
   float inv_T;
   uint32_t k0, k1;
@@ -123,16 +130,6 @@ __device__ __forceinline__ bool warp_aborted(volatile int* abort_flag) {
   return __shfl_sync(0xffffffffu, a, 0) != 0;
 }
 
-__device__ __forceinline__ void named_bar_epilogue() {
-  asm volatile("bar.sync 1, 256;" ::: "memory");
-}
-
-__device__ __forceinline__ unsigned int ld_acquire_u32(const unsigned int* p) {
-  unsigned int v;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-
 // Process 32 consecutive columns of one request row: x = acc + u (fp32),
 // masked beyond V; fold into the base-2 log-sum-exp and the argmax key.
 struct RowState {
@@ -169,8 +166,8 @@ __device__ __forceinline__ void fold32(RowState& st, const uint32_t (&acc)[32],
   if (M != -INFINITY) {
     float acc_s = 0.f;
 #pragma unroll
-    for (int i = 0; i < 32; ++i) acc_s += exp2f(fmaf(xs[i], kLog2e, -M));
-    st.s = st.s * exp2f(st.m2 - M) + acc_s;
+    for (int i = 0; i < 32; ++i) acc_s += tc::ex2(fmaf(xs[i], kLog2e, -M));
+    st.s = st.s * tc::ex2(st.m2 - M) + acc_s;
     st.m2 = M;
   }
   if (!p.sampled) {
@@ -218,19 +215,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
          bars + 2 * kNB + 2 * kNU + 5};
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + kNumBars);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + kNumBars) + 1;
-  volatile int* stop_all = reinterpret_cast<volatile int*>(bars + kNumBars) + 2;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int MT = p.MT;
   const int KC = p.rank / kKChunk;
-  const int G = p.gamma;
+  const int j = p.j;
   const int t0 = (int)(((long long)blockIdx.x * p.ntiles) / gridDim.x);
   const int t1 = (int)(((long long)(blockIdx.x + 1) * p.ntiles) / gridDim.x);
   const int nt = t1 - t0;
-  // U boxes of a step: every tile has two 64-column halves per M-tile, except
-  // that a second half lying wholly beyond V is never loaded.
-  const bool last_half_skipped = (t1 == p.ntiles) && ((t1 - 1) * kTileN + 64 >= p.V);
-  const int boxes_per_step = nt * 2 * MT - (last_half_skipped ? MT : 0);
 
   if (tid == 0) {
     for (int i = 0; i < kNB; ++i) {
@@ -248,15 +240,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     tc::mbar_init(b.aready, 8);
     tc::mbar_init(b.mmadone, 1);
     *abort_flag = 0;
-    *stop_all = 0;
     tc::mbar_fence_init();
     tc::fence_proxy_async_smem();
     tc::prefetch_tensormap(&tmW);
     tc::prefetch_tensormap(&tmU);
   }
   if (warp == 1) {
+    __syncwarp();
     tc::tmem_alloc(tmem_holder, kTmemCols);
     tc::tmem_relinquish();
+    tc::tc_fence_before();
   }
   __syncthreads();
   tc::tc_fence_after();
@@ -267,77 +260,79 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (lane == 0) {
       const uint64_t pol = policy_evict_last();
       uint32_t it = 0;
-      for (int j = 0; j < G && !*abort_flag; ++j)
-        for (int t = t0; t < t1 && !*abort_flag; ++t)
-          for (int kc = 0; kc < KC; ++kc, ++it) {
-            const int s = it % kNB;
-            if (!wait_bar(&b.bempty[s], ((it / kNB) & 1) ^ 1, abort_flag, p.status)) break;
-            tc::mbar_arrive_expect_tx(&b.bfull[s], kStageBytes);
-            tc::tma_load_2d(sB + s * kStageBytes, &tmW, &b.bfull[s], kc * kKChunk, t * kTileN, pol);
-          }
-      // wait (bounded) for the copies this thread issued last in each stage
+      for (int t = t0; t < t1 && !*abort_flag; ++t)
+        for (int kc = 0; kc < KC; ++kc, ++it) {
+          const int s = it % kNB;
+          if (!wait_bar(&b.bempty[s], ((it / kNB) & 1) ^ 1, abort_flag, p.status)) break;
+          tc::mbar_arrive_expect_tx(&b.bfull[s], kStageBytes);
+          tc::tma_load_2d(sB + s * kStageBytes, &tmW, &b.bfull[s], kc * kKChunk, t * kTileN, pol);
+        }
+      // Tail: wait (bounded) for the copies issued last in each stage, then
+      // for the consumer's release of every stage.  The releases are
+      // tcgen05.commit arrivals, delivered to the mbarriers asynchronously when
+      // the MMAs finish and not ordered with the other commits, so without this
+      // wait an arrival could reach this CTA's shared memory after it exits.
       for (uint32_t k = (it > kNB ? it - kNB : 0); k < it; ++k)
         drain_bar(&b.bfull[k % kNB], (k / kNB) & 1);
+      for (uint32_t k = (it > kNB ? it - kNB : 0); k < it; ++k)
+        drain_bar(&b.bempty[k % kNB], (k / kNB) & 1);
     }
   } else if (warp == 2) {
     // ------------------------------------------------------ U producer
     if (lane == 0) {
       const uint64_t pol = policy_evict_first();
       uint32_t it = 0;
-      for (int j = 0; j < G && !*abort_flag; ++j)
-        for (int t = t0; t < t1 && !*abort_flag; ++t)
-          for (int h = 0; h < 2; ++h) {
-            const int vx = t * kTileN + h * 64;
-            if (vx >= p.V) continue;
-            for (int m = 0; m < MT; ++m, ++it) {
-              const int s = it % kNU;
-              if (!wait_bar(&b.uempty[s], ((it / kNU) & 1) ^ 1, abort_flag, p.status)) break;
-              tc::mbar_arrive_expect_tx(&b.ufull[s], kStageBytes);
-              tc::tma_load_3d(sU + s * kStageBytes, &tmU, &b.ufull[s], vx, j,
-                              p.r_off + m * kTileM, pol);
-            }
+      for (int t = t0; t < t1 && !*abort_flag; ++t)
+        for (int h = 0; h < 2; ++h) {
+          const int vx = t * kTileN + h * 64;
+          if (vx >= p.V) continue;
+          for (int m = 0; m < MT; ++m, ++it) {
+            const int s = it % kNU;
+            if (!wait_bar(&b.uempty[s], ((it / kNU) & 1) ^ 1, abort_flag, p.status)) break;
+            tc::mbar_arrive_expect_tx(&b.ufull[s], kStageBytes);
+            tc::tma_load_3d(sU + s * kStageBytes, &tmU, &b.ufull[s], vx, j,
+                            p.r_off + m * kTileM, pol);
           }
+        }
       for (uint32_t k = (it > kNU ? it - kNU : 0); k < it; ++k)
         drain_bar(&b.ufull[k % kNU], (k / kNU) & 1);
+      for (uint32_t k = (it > kNU ? it - kNU : 0); k < it; ++k)
+        drain_bar(&b.uempty[k % kNU], (k / kNU) & 1);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------ MMA issuer
     if (lane == 0) {
       uint32_t bit = 0, tcount = 0;
-      bool ok = true;
-      for (int j = 0; j < G && ok; ++j) {
-        ok = wait_bar(b.aready, j & 1, abort_flag, p.status);
+      bool ok = wait_bar(b.aready, 0, abort_flag, p.status);
+      tc::tc_fence_after();
+      for (int t = t0; t < t1 && ok; ++t, ++tcount) {
+        const int buf = tcount & 1;
+        ok = wait_bar(&b.accempty[buf], ((tcount >> 1) & 1) ^ 1, abort_flag, p.status);
+        if (!ok) break;
         tc::tc_fence_after();
-        for (int t = t0; t < t1 && ok; ++t, ++tcount) {
-          const int buf = tcount & 1;
-          ok = wait_bar(&b.accempty[buf], ((tcount >> 1) & 1) ^ 1, abort_flag, p.status);
+        for (int kc = 0; kc < KC; ++kc, ++bit) {
+          const int s = bit % kNB;
+          ok = wait_bar(&b.bfull[s], (bit / kNB) & 1, abort_flag, p.status);
           if (!ok) break;
           tc::tc_fence_after();
-          for (int kc = 0; kc < KC; ++kc, ++bit) {
-            const int s = bit % kNB;
-            ok = wait_bar(&b.bfull[s], (bit / kNB) & 1, abort_flag, p.status);
-            if (!ok) break;
-            tc::tc_fence_after();
-            const uint32_t b_base = tc::smem_u32(sB + s * kStageBytes);
-            for (int m = 0; m < MT; ++m) {
-              const uint32_t d_tmem = tmem_base + (uint32_t)((buf * 2 + m) * kTileN);
-              const uint32_t a_base = tc::smem_u32(sA + (m * kMaxKC + kc) * kStageBytes);
+          const uint32_t b_base = tc::smem_u32(sB + s * kStageBytes);
+          for (int m = 0; m < MT; ++m) {
+            const uint32_t d_tmem = tmem_base + (uint32_t)((buf * 2 + m) * kTileN);
+            const uint32_t a_base = tc::smem_u32(sA + (m * kMaxKC + kc) * kStageBytes);
 #pragma unroll
-              for (int ks = 0; ks < kKChunk / 16; ++ks) {
-                tc::umma_bf16(d_tmem, tc::sdesc_kmajor_sw128(a_base + ks * 32),
-                              tc::sdesc_kmajor_sw128(b_base + ks * 32), kIdesc,
-                              (kc | ks) != 0 ? 1u : 0u);
-              }
+            for (int ks = 0; ks < kKChunk / 16; ++ks) {
+              tc::umma_bf16(d_tmem, tc::sdesc_kmajor_sw128(a_base + ks * 32),
+                            tc::sdesc_kmajor_sw128(b_base + ks * 32), kIdesc,
+                            (kc | ks) != 0 ? 1u : 0u);
             }
-            tc::umma_commit(&b.bempty[s]);
           }
-          if (ok) tc::umma_commit(&b.accfull[buf]);
+          tc::umma_commit(&b.bempty[s]);
         }
+        if (ok) tc::umma_commit(&b.accfull[buf]);
       }
       // all issued MMAs complete before TMEM is released
       tc::umma_commit(b.mmadone);
-      for (uint32_t i = 0; i < kSpinLimit; ++i)
-        if (tc::mbar_try_wait(b.mmadone, 0)) break;
+      drain_bar(b.mmadone, 0);
     }
   } else if (warp >= 4) {
     // ------------------------------------------------------ epilogue
@@ -349,114 +344,107 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const bool active = g < MT;
     const bool valid = active && r < p.R;
     const uint32_t rid = valid ? (p.req_id ? p.req_id[r] : (uint32_t)r) : 0u;
-    uint32_t tcount = 0;
     const int rows_total = MT * kTileM;
-    for (int j = 0; j < G; ++j) {
-      // ---- A operand of step j: rows of E for the previous tokens ----
+
+    // ---- A operand: rows of E for the tokens of step j-1 ----
+    // This warp fills rows e, e+8, ...: lane k fetches the token of row e+8k,
+    // then rows are copied 16 at a time (16 loads in flight per lane) into
+    // the 128-byte-swizzled K-major layout of the UMMA descriptors.
+    {
       const bool biased = (j > 0) || p.bias_at_first;
-      for (int ri = e; ri < rows_total; ri += 8) {
-        const int rr = p.r_off + ri;
-        int tok = 0;
-        bool use = biased && rr < p.R;
-        if (use) {
-          tok = (j == 0) ? p.prev_tok[rr]
-                         : (int)key_index(__ldcg(&p.keys[(size_t)(j - 1) * p.R_max + rr]));
-          if (tok < 0 || tok >= p.V) {
+      const int rows_per_warp = rows_total / 8;
+      int my_tok = -1;
+      if (lane < rows_per_warp) {
+        const int rr = p.r_off + e + 8 * lane;
+        if (biased && rr < p.R) {
+          int tk = (j == 0) ? p.prev_tok[rr]
+                            : (int)key_index(__ldcg(&p.keys[(size_t)(j - 1) * p.R_max + rr]));
+          if (tk < 0 || tk >= p.V) {
             set_status(p.status, kErrArg);
-            tok = 0;
+            tk = 0;
           }
+          my_tok = tk;
         }
-        const int mt = ri / kTileM, ir = ri % kTileM;
-        for (int c = lane; c < p.rank / 8; c += 32) {
-          uint4 v = make_uint4(0u, 0u, 0u, 0u);
-          if (use) v = ld_keep16(p.E + (size_t)tok * p.rank + c * 8);
-          const int kc = c >> 3, cc = c & 7;
-          *reinterpret_cast<uint4*>(sA + (mt * kMaxKC + kc) * kStageBytes + ir * 128 +
-                                    ((cc ^ (ir & 7)) << 4)) = v;
+      }
+      const int cpr = p.rank / 8;    // 16-byte chunks per row
+      for (int k0 = 0; k0 < rows_per_warp; k0 += 16) {
+        uint4 v[16];
+#pragma unroll
+        for (int kk = 0; kk < 16; ++kk) {
+          const int tok = __shfl_sync(0xffffffffu, my_tok, (k0 + kk) & 31);
+          v[kk] = make_uint4(0u, 0u, 0u, 0u);
+          if (k0 + kk < rows_per_warp && tok >= 0 && lane < cpr &&
+              TC_CHECK((size_t)tok * p.rank + lane * 8 + 8 <= (size_t)p.V * p.rank, 2))
+            v[kk] = __ldcg(reinterpret_cast<const uint4*>(p.E + (size_t)tok * p.rank + lane * 8));
+        }
+#pragma unroll
+        for (int kk = 0; kk < 16; ++kk) {
+          const int ri = e + 8 * (k0 + kk);
+          if (k0 + kk >= rows_per_warp || lane >= cpr) continue;
+          const int mt = ri / kTileM, ir = ri % kTileM;
+          const int kc = lane >> 3, cc = lane & 7;
+          const size_t off = (size_t)(mt * kMaxKC + kc) * kStageBytes + ir * 128 +
+                             ((cc ^ (ir & 7)) << 4);
+          if (TC_CHECK(off + 16 <= (size_t)kMaxMT * kMaxKC * kStageBytes, 1))
+            *reinterpret_cast<uint4*>(sA + off) = v[kk];
         }
       }
       tc::fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(b.aready);
+    }
 
-      // ---- tiles ----
-      RowState st{-INFINITY, 0.f, -INFINITY, 0u};
-      for (int tt = 0; tt < nt; ++tt, ++tcount) {
-        if (!active || warp_aborted(abort_flag)) continue;
-        const int t = t0 + tt;
-        const int buf = tcount & 1;
-        if (!warp_wait(&b.accfull[buf], (tcount >> 1) & 1, abort_flag, p.status)) continue;
-        tc::tc_fence_after();
-        for (int h = 0; h < 2; ++h) {
-          const int vx = t * kTileN + h * 64;
-          if (vx >= p.V) continue;
-          const uint32_t uit = (uint32_t)(j * boxes_per_step + tt * 2 * MT + h * MT + g);
-          const int s = uit % kNU;
-          if (!warp_wait(&b.ufull[s], (uit / kNU) & 1, abort_flag, p.status)) break;
-          const unsigned char* urow = sU + s * kStageBytes + row * 128;
+    // ---- tiles ----
+    RowState st{-INFINITY, 0.f, -INFINITY, 0u};
+    uint32_t tcount = 0, uit = 0;
+    for (int tt = 0; tt < nt && active; ++tt, ++tcount) {
+      if (warp_aborted(abort_flag)) break;
+      const int t = t0 + tt;
+      const int buf = tcount & 1;
+      if (!warp_wait(&b.accfull[buf], (tcount >> 1) & 1, abort_flag, p.status)) break;
+      tc::tc_fence_after();
+      for (int h = 0; h < 2; ++h) {
+        const int vx = t * kTileN + h * 64;
+        if (vx >= p.V) continue;
+        // boxes are issued (h, m) in order, MT per half: this group's box
+        const uint32_t my = uit + (uint32_t)g;
+        uit += (uint32_t)MT;
+        const int s = my % kNU;
+        if (!warp_wait(&b.ufull[s], (my / kNU) & 1, abort_flag, p.status)) break;
+        const unsigned char* urow = sU + s * kStageBytes + row * 128;
 #pragma unroll
-          for (int half = 0; half < 2; ++half) {
-            uint32_t acc[32];
-            tc::tmem_ld_32x32b_x32(tmem_base + ((uint32_t)(q * 32) << 16) +
-                                       (uint32_t)((buf * 2 + g) * kTileN + h * 64 + half * 32),
-                                   acc);
-            uint4 u[4];
+        for (int half = 0; half < 2; ++half) {
+          uint4 u[4];
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-              const int cl = half * 4 + c;
-              u[c] = *reinterpret_cast<const uint4*>(urow + ((cl ^ (row & 7)) << 4));
-            }
-            tc::tmem_wait_ld();
-            fold32(st, acc, u, vx + half * 32, p.V, p, j, rid);
+          for (int c = 0; c < 4; ++c) {
+            const int cl = half * 4 + c;
+            u[c] = *reinterpret_cast<const uint4*>(urow + ((cl ^ (row & 7)) << 4));
           }
+          uint32_t acc[32];
           __syncwarp();
-          if (lane == 0) tc::mbar_arrive(&b.uempty[s]);
+          tc::tmem_ld_32x32b_x32_wait(tmem_base + ((uint32_t)(q * 32) << 16) +
+                                          (uint32_t)((buf * 2 + g) * kTileN + h * 64 + half * 32),
+                                      acc);
+          fold32(st, acc, u, vx + half * 32, p.V, p, j, rid);
         }
-        tc::tc_fence_before();
         __syncwarp();
-        if (lane == 0) tc::mbar_arrive(&b.accempty[buf]);
+        if (lane == 0) tc::mbar_arrive(&b.uempty[s]);
       }
+      tc::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(&b.accempty[buf]);
+    }
 
-      // ---- publish this CTA's partials of step j ----
-      if (valid) {
-        if (st.best_z != -INFINITY || st.s != 0.f)
-          atomicMax(&p.keys[(size_t)j * p.R_max + r], make_key(st.best_z, st.best_v));
-        p.parts[((size_t)j * p.n_part + blockIdx.x) * p.R_max + r] = make_float2(st.m2, st.s);
-      }
-      __threadfence();
-      named_bar_epilogue();
-      if (j + 1 < G) {
-        // ---- grid barrier (bounded) ----
-        if (e == 0 && lane == 0 && !*abort_flag) {
-          atomicAdd(p.gbar, 1u);
-          const unsigned int target = (unsigned int)(j + 1) * gridDim.x;
-          bool done = false;
-          for (uint32_t i = 0; i < kGridSpinLimit; ++i) {
-            if (ld_acquire_u32(p.gbar) >= target) {
-              done = true;
-              break;
-            }
-            __nanosleep(64);
-          }
-          if (!done) {
-            set_status(p.status, kErrTimeout);
-            *abort_flag = 1;
-          }
-        }
-        // one thread decides for all eight epilogue warps, so that they all
-        // leave (or all continue) together and the named barrier stays matched
-        if (e == 0 && lane == 0) *stop_all = *abort_flag;
-        named_bar_epilogue();
-        if (*stop_all) {
-          // let the MMA warp leave its wait for the next step's operand
-          if (lane == 0) tc::mbar_arrive(b.aready);
-          break;
-        }
-      }
+    // ---- publish this CTA's partials of step j ----
+    if (valid && TC_CHECK(blockIdx.x < (unsigned)p.n_part && r < p.R_max, 5)) {
+      atomicMax(&p.keys[(size_t)j * p.R_max + r], make_key(st.best_z, st.best_v));
+      p.parts[((size_t)j * p.n_part + blockIdx.x) * p.R_max + r] = make_float2(st.m2, st.s);
     }
   }
+  tc::tc_fence_before();
   __syncthreads();
   if (warp == 1) {
+    __syncwarp();
     tc::tc_fence_after();
     tc::tmem_dealloc(tmem_base, kTmemCols);
   }
@@ -480,6 +468,13 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }  // namespace
 
 int tc_supported(const Ctx& ctx, char* why, size_t why_len) {
+  // Disabled: under CUDA-graph replay after an L2 flush this kernel hit a
+  // launch failure about once per 15-70 cycles (never in eager runs); the
+  // cause is not identified, so nothing selects it until it is.
+  (void)ctx;
+  snprintf(why, why_len,
+           "tcgen05 propose engine disabled: unresolved launch failure under graph replay");
+  return 0;
   if (ctx.cfg.dtype != 1) {
     snprintf(why, why_len, "tcgen05 engine needs bf16 tables");
     return 0;
@@ -496,12 +491,10 @@ int tc_supported(const Ctx& ctx, char* why, size_t why_len) {
     snprintf(why, why_len, "cuTensorMapEncodeTiled is not available from the driver");
     return 0;
   }
-  int coop = 0, smem = 0;
-  cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, ctx.cfg.device);
+  int smem = 0;
   cudaDeviceGetAttribute(&smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, ctx.cfg.device);
-  if (!coop || smem < kSmemBytes) {
-    snprintf(why, why_len, "device lacks cooperative launch or %d bytes of shared memory",
-             kSmemBytes);
+  if (smem < kSmemBytes) {
+    snprintf(why, why_len, "device lacks %d bytes of shared memory per block", kSmemBytes);
     return 0;
   }
   return 1;
@@ -539,9 +532,6 @@ cudaError_t launch_propose_tc(const Ctx& ctx, const ProposeArgs& a, cudaStream_t
   cudaError_t e = cudaMemsetAsync(ctx.ws.keys, 0,
                                   sizeof(unsigned long long) * (size_t)a.gamma * ctx.cfg.R_max, s);
   if (e != cudaSuccess) return e;
-  const int groups = (a.R + kMaxMT * kTileM - 1) / (kMaxMT * kTileM);
-  e = cudaMemsetAsync(ctx.ws.gbar, 0, sizeof(unsigned int) * (size_t)groups, s);
-  if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(propose_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            kSmemBytes);
   if (e != cudaSuccess) return e;
@@ -566,25 +556,20 @@ cudaError_t launch_propose_tc(const Ctx& ctx, const ProposeArgs& a, cudaStream_t
   p.k0 = (uint32_t)(a.seed & 0xFFFFFFFFull);
   p.k1 = (uint32_t)(a.seed >> 32);
   const int grid = tc_grid(ctx);
+  const int groups = (a.R + kMaxMT * kTileM - 1) / (kMaxMT * kTileM);
 
-  for (int gi = 0; gi < groups; ++gi) {
-    p.r_off = gi * kMaxMT * kTileM;
-    const int rem = a.R - p.r_off;
-    p.MT = rem > kTileM ? 2 : 1;
-    p.gbar = ctx.ws.gbar + gi;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(kTcThreads);
-    cfg.dynamicSmemBytes = kSmemBytes;
-    cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeCooperative;
-    attr[0].val.cooperative = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, propose_tc_kernel, tmW, tmU, p);
-    if (e != cudaSuccess) return e;
-    count_launch(ctx);
+  // Steps in order; within a step, request groups of <= 256 are independent.
+  for (int j = 0; j < a.gamma; ++j) {
+    p.j = j;
+    for (int gi = 0; gi < groups; ++gi) {
+      p.r_off = gi * kMaxMT * kTileM;
+      const int rem = a.R - p.r_off;
+      p.MT = rem > kTileM ? 2 : 1;
+      propose_tc_kernel<<<grid, kTcThreads, kSmemBytes, s>>>(tmW, tmU, p);
+      e = cudaGetLastError();
+      if (e != cudaSuccess) return e;
+      count_launch(ctx);
+    }
   }
   return cudaSuccess;
 }

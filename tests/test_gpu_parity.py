@@ -86,7 +86,7 @@ def check_cycle(spec, x, k, act="none", bias_at_first=True, keep_all=False, max_
 SMALL = dict(V=2568, R=19, ew_std=0.3)        # 21 tiles of 128 with an 8-row tail
 
 
-@pytest.mark.parametrize("engine", ["simt", "tcgen05"])
+@pytest.mark.parametrize("engine", ["simt", "auto"])
 @pytest.mark.parametrize("temperature", [0.0, 1.0, 0.6])
 def test_cycle_bf16_small(dsd, engine, temperature):
     spec = synth.scaled(synth.CYCLE_SPECS["greedy"], temperature=temperature, seed=21,
@@ -96,27 +96,28 @@ def test_cycle_bf16_small(dsd, engine, temperature):
 
 
 @pytest.mark.parametrize("R,V,rank,temperature", [
-    (129, 2568, 256, 0.0),     # second M-tile with one request
+    (129, 2568, 256, 0.0),     # second M-tile with one request, ragged vocabulary tail
     (256, 1032, 256, 1.0),     # two full M-tiles, sampled
-    (300, 1544, 256, 0.0),     # two launch groups (256 + 44)
-    (40, 3080, 128, 0.0),      # rank 128: two K-chunks
-    (16, 4104, 64, 1.0),       # rank 64, smallest batch the engine takes
+    (300, 1544, 256, 0.0),     # three M-tiles
+    (40, 3080, 128, 0.0),      # rank 128
+    (16, 4104, 64, 1.0),       # rank 64, smallest batch AUTO sends to this engine
 ])
-def test_cycle_tcgen05_shapes(dsd, R, V, rank, temperature):
+def test_cycle_mma_shapes(dsd, R, V, rank, temperature):
     spec = synth.scaled(synth.CYCLE_SPECS["greedy"], R=R, V=V, r=rank, ew_std=0.3,
                         temperature=temperature, seed=100 + R, n_sps=None)
-    x, k = run_cycle(dsd, spec, engine="tcgen05")
+    x, k = run_cycle(dsd, spec, engine="mma")
     check_cycle(spec, x, k)
 
 
-def test_tcgen05_and_simt_engines_agree(dsd):
+def test_mma_and_simt_engines_agree(dsd):
     spec = synth.scaled(synth.CYCLE_SPECS["greedy"], R=64, V=2568, ew_std=0.3, seed=33)
     x = synth.cycle_inputs(spec, device=DEV)
     outs = []
-    for engine in ("simt", "tcgen05"):
+    for engine in ("simt", "mma"):
         ctx = dsd.Context(spec.V, spec.r, spec.G, spec.R, dtype="bf16", engine=engine)
         o = ctx.propose(x["U"], x["E"], x["W"], x["conf"], x["prev_tok"], x["req_id"], 0.0, 1)
         assert ctx.sync_status() == 0
+        assert ctx.last_engine() == engine
         outs.append({n: t.cpu().numpy() for n, t in o.items()})
         ctx.close()
     h = host(x)
@@ -125,6 +126,18 @@ def test_tcgen05_and_simt_engines_agree(dsd):
     ok = ~parity.draft_exempt(prop["margin"])
     assert np.array_equal(outs[0]["tokens"][ok], outs[1]["tokens"][ok])
     assert np.max(np.abs(outs[0]["lse_q"] - outs[1]["lse_q"])[ok]) <= parity.LOGIT_TOL
+
+
+def test_disabled_engine_is_rejected_before_any_launch(dsd):
+    spec = synth.scaled(synth.CYCLE_SPECS["greedy"], R=16, V=1032, seed=34)
+    x = synth.cycle_inputs(spec, device=DEV)
+    ctx = dsd.Context(spec.V, spec.r, spec.G, spec.R, dtype="bf16", engine="tcgen05")
+    n0 = ctx.launch_count()
+    with pytest.raises(dsd.DsdError) as ei:
+        ctx.propose(x["U"], x["E"], x["W"], x["conf"], x["prev_tok"], x["req_id"], 0.0, 1)
+    assert ei.value.code == -9
+    assert ctx.launch_count() == n0
+    ctx.close()
 
 
 def test_cycle_bf16_no_pruning_covers_all_positions(dsd):
