@@ -504,7 +504,7 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="highconc",
                     choices=["highconc", "greedy", "sampled", "tiny"])
-    ap.add_argument("--engine", default="auto", choices=["auto", "simt", "mma"])
+    ap.add_argument("--engine", default="auto", choices=["auto", "simt", "mma", "tcgen05"])
     ap.add_argument("--cpu-requests", type=int, default=128,
                     help="requests in the CPU-baseline sample")
     ap.add_argument("--ref-requests", type=int, default=16,

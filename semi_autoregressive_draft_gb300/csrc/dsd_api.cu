@@ -95,12 +95,6 @@ bool mma_ok(const dsd_ctx* ctx) {
          ctx->cfg.act == DSD_ACT_NONE;
 }
 
-bool use_mma(const dsd_ctx* ctx, int R) {
-  if (!mma_ok(ctx)) return false;
-  if (ctx->cfg.engine == DSD_ENGINE_MMA) return true;
-  return ctx->cfg.engine == DSD_ENGINE_AUTO && R >= 16;
-}
-
 }  // namespace
 
 namespace dsd {
@@ -110,6 +104,17 @@ cudaError_t launch_propose_finalize_n(const Ctx& ctx, const ProposeArgs& a, int 
 int tc_supported(const Ctx& ctx, char* why, size_t why_len);
 int tc_grid(const Ctx& ctx);
 }  // namespace dsd
+
+namespace {
+// AUTO sends batches of at least 16 requests to the tcgen05 engine when the
+// configuration allows it; smaller batches stream W through the CUDA-core
+// engine, whose GEMV shape wastes no MMA rows.
+bool auto_uses_tc(const dsd_ctx* ctx, int R) {
+  if (ctx->cfg.engine != DSD_ENGINE_AUTO || R < 16) return false;
+  char why[256];
+  return dsd::tc_supported(*ctx, why, sizeof(why)) != 0;
+}
+}  // namespace
 
 extern "C" {
 
@@ -232,7 +237,7 @@ int dsd_propose(dsd_ctx* ctx, int R, const void* U, const void* E, const void* W
   a.survival = survival;
   cudaError_t e;
   int n_used;
-  if (ctx->cfg.engine == DSD_ENGINE_TCGEN05) {
+  if (ctx->cfg.engine == DSD_ENGINE_TCGEN05 || auto_uses_tc(ctx, R)) {
     char why[256];
     if (!tc_supported(*ctx, why, sizeof(why))) return fail(ctx, DSD_ERR_UNSUPPORTED, "%s", why);
     e = launch_propose_tc(*ctx, a, s);
@@ -241,7 +246,7 @@ int dsd_propose(dsd_ctx* ctx, int R, const void* U, const void* E, const void* W
   } else if (ctx->cfg.engine == DSD_ENGINE_MMA && !mma_ok(ctx)) {
     return fail(ctx, DSD_ERR_UNSUPPORTED,
                 "MMA engine needs bf16 tables, no activation and rank %% 64 == 0 (<= 256)");
-  } else if (use_mma(ctx, R)) {
+  } else if (ctx->cfg.engine == DSD_ENGINE_MMA) {
     e = launch_propose_mma(*ctx, a, s);
     n_used = mma_vranges(*ctx, R);
     ctx->last_engine = DSD_ENGINE_MMA;

@@ -16,15 +16,24 @@
 //   warp 1      TMEM allocator and the single thread that issues tcgen05.mma
 //               (M = 128, N = 128, K = 16 per instruction) into two
 //               double-buffered fp32 accumulators per M-tile (512 columns)
-//   warp 2      TMA producer of U tiles ([128 requests x 64 vocab] boxes of
-//               the [V, gamma, R] view, evict-first: U is read once)
-//   warps 4-11  epilogue: first they gather the A operand (rows of E for the
-//               tokens chosen at step j-1) into shared memory in the UMMA
-//               K-major 128-byte-swizzled layout; then thread = one request
-//               row: tcgen05.ld brings 32 accumulator columns, U comes from
-//               shared memory, and the biased logits are folded into a running
-//               base-2 log-sum-exp and an argmax (greedy) or Gumbel-max
-//               (sampled) key; they never leave registers.
+//   warps 2, 3  TMA producers of U, one per M-tile: [128 requests x 32 vocab]
+//               boxes of the [V, gamma, R] view (64-byte swizzle,
+//               evict-first: U is read once), each into its own ring
+//   warps 4-11  epilogue, four warps per M-tile: first they gather the A
+//               operand (rows of E for the tokens chosen at step j-1) into
+//               shared memory in the UMMA K-major 128-byte-swizzled layout;
+//               then thread = one request row: tcgen05.ld brings 32
+//               accumulator columns, U comes from shared memory, and the
+//               biased logits are folded into a running base-2 log-sum-exp
+//               and an argmax (greedy) or Gumbel-max (sampled) key; they never
+//               leave registers.
+//
+// Every mbarrier has exactly one consumer role that waits on each of its
+// phases in order (a parity wait cannot tell phase k from phase k + 2, so no
+// waiter may skip a phase).  That is why each M-tile has its own U ring and
+// producer: with one ring shared by both M-tiles, a group's consecutive waits
+// on a slot would skip the other group's phase.
+//
 // At the end each CTA publishes per-request partials: atomicMax of the packed
 // argmax key and an (m, s) log-sum-exp partial.  The next step's launch reads
 // the keys, so the kernel boundary is the batch-wide synchronisation between
@@ -48,19 +57,24 @@ constexpr int kTileM = 128;          // requests per M-tile (UMMA M)
 constexpr int kMaxMT = 2;            // M-tiles per launch (R <= 256)
 constexpr int kKChunk = 64;          // K elements per 128-byte swizzle row
 constexpr int kMaxKC = 4;            // rank <= 256
-constexpr int kStageBytes = 16384;   // one [128 x 64] bf16 box
+constexpr int kWStage = 16384;       // one [128 x 64] bf16 W box
 constexpr int kNB = 3;               // W ring stages
-constexpr int kNU = 3;               // U ring slots
+constexpr int kUCols = 32;           // vocabulary columns per U box
+constexpr int kUBox = kTileM * kUCols * 2;   // 8 KB, rows of 64 bytes
+constexpr int kNU = 3;               // U ring slots per M-tile
+constexpr int kUPerTile = kTileN / kUCols;   // U boxes per M-tile and tile
 constexpr int kTmemCols = 512;
 constexpr uint32_t kIdesc = tc::idesc_bf16_f32(kTileM, kTileN);
 
 constexpr int kOffA = 0;
-constexpr int kOffB = kOffA + kMaxMT * kMaxKC * kStageBytes;  // 128 KB
-constexpr int kOffU = kOffB + kNB * kStageBytes;              // +48 KB
-constexpr int kOffBar = kOffU + kNU * kStageBytes;            // +48 KB
-constexpr int kNumBars = 2 * kNB + 2 * kNU + 4 + 2;
+constexpr int kOffB = kOffA + kMaxMT * kMaxKC * kWStage;   // 128 KB of A
+constexpr int kOffU = kOffB + kNB * kWStage;               // + 48 KB of W
+constexpr int kOffBar = kOffU + kMaxMT * kNU * kUBox;      // + 48 KB of U
+// bfull, bempty, ufull[2], uempty[2], accfull[2], accempty[2], aready, mmadone
+constexpr int kNumBars = 2 * kNB + 2 * kMaxMT * kNU + 4 + 2;
 constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 64 + 1024;  // + alignment slack
 static_assert(kSmemBytes <= 232448, "shared memory budget of one CTA");
+static_assert(kOffB % 1024 == 0 && kOffU % 1024 == 0, "swizzled boxes need aligned bases");
 
 #ifdef DSD_TC_CHECKS
 // Self-checking build: an out-of-range index records a distinct status code
@@ -86,12 +100,12 @@ struct TcParams {
 };
 
 struct Bars {
-  uint64_t* bfull;
-  uint64_t* bempty;
-  uint64_t* ufull;
-  uint64_t* uempty;
-  uint64_t* accfull;
-  uint64_t* accempty;
+  uint64_t* bfull;      // [kNB]
+  uint64_t* bempty;     // [kNB]
+  uint64_t* ufull;      // [kMaxMT][kNU]
+  uint64_t* uempty;     // [kMaxMT][kNU]
+  uint64_t* accfull;    // [2]
+  uint64_t* accempty;   // [2]
   uint64_t* aready;
   uint64_t* mmadone;
 };
@@ -130,44 +144,60 @@ __device__ __forceinline__ bool warp_aborted(volatile int* abort_flag) {
   return __shfl_sync(0xffffffffu, a, 0) != 0;
 }
 
-// Process 32 consecutive columns of one request row: x = acc + u (fp32),
-// masked beyond V; fold into the base-2 log-sum-exp and the argmax key.
 struct RowState {
   float m2, s, best_z;
   uint32_t best_v;
 };
 
+// Process 32 consecutive columns of one request row: x = acc + u (fp32),
+// masked beyond V; fold into the base-2 log-sum-exp and the argmax key.
+// Pairs of columns go through the packed fp32x2 pipe.
 __device__ __forceinline__ void fold32(RowState& st, const uint32_t (&acc)[32],
-                                       const uint4 (&u)[4], int v0, int V, const TcParams& p,
-                                       int pos, uint32_t rid) {
+                                       const uint4 (&u)[4], int v0, const TcParams& p,
+                                       uint32_t rid) {
   float xs[32];
 #pragma unroll
   for (int c = 0; c < 4; ++c) {
     const uint32_t w[4] = {u[c].x, u[c].y, u[c].z, u[c].w};
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-      xs[c * 8 + 2 * e] = __uint_as_float(acc[c * 8 + 2 * e]) + bf16lo(w[e]);
-      xs[c * 8 + 2 * e + 1] = __uint_as_float(acc[c * 8 + 2 * e + 1]) + bf16hi(w[e]);
+      const int i = c * 8 + 2 * e;
+      const uint64_t x2 = tc::add2(tc::pack2(__uint_as_float(acc[i]), __uint_as_float(acc[i + 1])),
+                                   tc::pack2(bf16lo(w[e]), bf16hi(w[e])));
+      tc::unpack2(x2, xs[i], xs[i + 1]);
     }
   }
-  if (v0 + 32 > V) {
+  if (v0 + 32 > p.V) {
 #pragma unroll
     for (int i = 0; i < 32; ++i)
-      if (v0 + i >= V) xs[i] = -INFINITY;
+      if (v0 + i >= p.V) xs[i] = -INFINITY;
   }
   if (p.sampled) {
+    const uint64_t t2 = tc::pack2(p.inv_T, p.inv_T);
 #pragma unroll
-    for (int i = 0; i < 32; ++i) xs[i] *= p.inv_T;
+    for (int i = 0; i < 32; i += 2) {
+      const uint64_t x2 = tc::mul2(tc::pack2(xs[i], xs[i + 1]), t2);
+      tc::unpack2(x2, xs[i], xs[i + 1]);
+    }
   }
-  float cm = -INFINITY;
+  float cm = tc::max3(xs[0], xs[1], xs[2]);
 #pragma unroll
-  for (int i = 0; i < 32; ++i) cm = fmaxf(cm, xs[i]);
+  for (int i = 3; i < 31; i += 2) cm = tc::max3(cm, xs[i], xs[i + 1]);
+  cm = fmaxf(cm, xs[31]);
   const float M = fmaxf(st.m2, cm * kLog2e);
   if (M != -INFINITY) {
-    float acc_s = 0.f;
+    const uint64_t l2 = tc::pack2(kLog2e, kLog2e);
+    const uint64_t nm = tc::pack2(-M, -M);
+    uint64_t s2 = tc::pack2(0.f, 0.f);
 #pragma unroll
-    for (int i = 0; i < 32; ++i) acc_s += tc::ex2(fmaf(xs[i], kLog2e, -M));
-    st.s = st.s * tc::ex2(st.m2 - M) + acc_s;
+    for (int i = 0; i < 32; i += 2) {
+      float a, b;
+      tc::unpack2(tc::fma2(tc::pack2(xs[i], xs[i + 1]), l2, nm), a, b);
+      s2 = tc::add2(s2, tc::pack2(tc::ex2(a), tc::ex2(b)));
+    }
+    float slo, shi;
+    tc::unpack2(s2, slo, shi);
+    st.s = st.s * tc::ex2(st.m2 - M) + (slo + shi);
     st.m2 = M;
   }
   if (!p.sampled) {
@@ -185,7 +215,7 @@ __device__ __forceinline__ void fold32(RowState& st, const uint32_t (&acc)[32],
 #pragma unroll
     for (int g = 0; g < 8; ++g) {
       const uint32_t v = (uint32_t)(v0 + 4 * g);
-      const Philox4 ph = philox4x32_10(v >> 2, (uint32_t)pos, rid, 0u, p.k0, p.k1);
+      const Philox4 ph = philox4x32_10(v >> 2, (uint32_t)p.j, rid, 0u, p.k0, p.k1);
       const float z0 = xs[4 * g + 0] + gumbel_from_word(ph.x);
       const float z1 = xs[4 * g + 1] + gumbel_from_word(ph.y);
       const float z2 = xs[4 * g + 2] + gumbel_from_word(ph.z);
@@ -210,9 +240,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   unsigned char* sB = smem + kOffB;
   unsigned char* sU = smem + kOffU;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
-  Bars b{bars, bars + kNB, bars + 2 * kNB, bars + 2 * kNB + kNU, bars + 2 * kNB + 2 * kNU,
-         bars + 2 * kNB + 2 * kNU + 2, bars + 2 * kNB + 2 * kNU + 4,
-         bars + 2 * kNB + 2 * kNU + 5};
+  Bars b;
+  b.bfull = bars;
+  b.bempty = b.bfull + kNB;
+  b.ufull = b.bempty + kNB;
+  b.uempty = b.ufull + kMaxMT * kNU;
+  b.accfull = b.uempty + kMaxMT * kNU;
+  b.accempty = b.accfull + 2;
+  b.aready = b.accempty + 2;
+  b.mmadone = b.aready + 1;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + kNumBars);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + kNumBars) + 1;
 
@@ -229,7 +265,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       tc::mbar_init(&b.bfull[i], 1);
       tc::mbar_init(&b.bempty[i], 1);
     }
-    for (int i = 0; i < kNU; ++i) {
+    for (int i = 0; i < kMaxMT * kNU; ++i) {
       tc::mbar_init(&b.ufull[i], 1);
       tc::mbar_init(&b.uempty[i], 4);
     }
@@ -264,40 +300,42 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         for (int kc = 0; kc < KC; ++kc, ++it) {
           const int s = it % kNB;
           if (!wait_bar(&b.bempty[s], ((it / kNB) & 1) ^ 1, abort_flag, p.status)) break;
-          tc::mbar_arrive_expect_tx(&b.bfull[s], kStageBytes);
-          tc::tma_load_2d(sB + s * kStageBytes, &tmW, &b.bfull[s], kc * kKChunk, t * kTileN, pol);
+          tc::mbar_arrive_expect_tx(&b.bfull[s], kWStage);
+          tc::tma_load_2d(sB + s * kWStage, &tmW, &b.bfull[s], kc * kKChunk, t * kTileN, pol);
         }
       // Tail: wait (bounded) for the copies issued last in each stage, then
       // for the consumer's release of every stage.  The releases are
       // tcgen05.commit arrivals, delivered to the mbarriers asynchronously when
-      // the MMAs finish and not ordered with the other commits, so without this
-      // wait an arrival could reach this CTA's shared memory after it exits.
+      // the MMAs finish, so without this wait an arrival could reach this
+      // CTA's shared memory after it exits.
       for (uint32_t k = (it > kNB ? it - kNB : 0); k < it; ++k)
         drain_bar(&b.bfull[k % kNB], (k / kNB) & 1);
       for (uint32_t k = (it > kNB ? it - kNB : 0); k < it; ++k)
         drain_bar(&b.bempty[k % kNB], (k / kNB) & 1);
     }
-  } else if (warp == 2) {
-    // ------------------------------------------------------ U producer
-    if (lane == 0) {
+  } else if (warp == 2 || warp == 3) {
+    // ------------------------------------------- U producer of M-tile g
+    const int g = warp - 2;
+    if (lane == 0 && g < MT) {
       const uint64_t pol = policy_evict_first();
+      uint64_t* full = b.ufull + g * kNU;
+      uint64_t* empty = b.uempty + g * kNU;
+      unsigned char* ring = sU + g * kNU * kUBox;
       uint32_t it = 0;
       for (int t = t0; t < t1 && !*abort_flag; ++t)
-        for (int h = 0; h < 2; ++h) {
-          const int vx = t * kTileN + h * 64;
-          if (vx >= p.V) continue;
-          for (int m = 0; m < MT; ++m, ++it) {
-            const int s = it % kNU;
-            if (!wait_bar(&b.uempty[s], ((it / kNU) & 1) ^ 1, abort_flag, p.status)) break;
-            tc::mbar_arrive_expect_tx(&b.ufull[s], kStageBytes);
-            tc::tma_load_3d(sU + s * kStageBytes, &tmU, &b.ufull[s], vx, j,
-                            p.r_off + m * kTileM, pol);
-          }
+        for (int h = 0; h < kUPerTile; ++h) {
+          const int vx = t * kTileN + h * kUCols;
+          if (vx >= p.V) break;
+          const int s = it % kNU;
+          if (!wait_bar(&empty[s], ((it / kNU) & 1) ^ 1, abort_flag, p.status)) break;
+          tc::mbar_arrive_expect_tx(&full[s], kUBox);
+          tc::tma_load_3d(ring + s * kUBox, &tmU, &full[s], vx, j, p.r_off + g * kTileM, pol);
+          ++it;
         }
       for (uint32_t k = (it > kNU ? it - kNU : 0); k < it; ++k)
-        drain_bar(&b.ufull[k % kNU], (k / kNU) & 1);
+        drain_bar(&full[k % kNU], (k / kNU) & 1);
       for (uint32_t k = (it > kNU ? it - kNU : 0); k < it; ++k)
-        drain_bar(&b.uempty[k % kNU], (k / kNU) & 1);
+        drain_bar(&empty[k % kNU], (k / kNU) & 1);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------ MMA issuer
@@ -315,10 +353,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           ok = wait_bar(&b.bfull[s], (bit / kNB) & 1, abort_flag, p.status);
           if (!ok) break;
           tc::tc_fence_after();
-          const uint32_t b_base = tc::smem_u32(sB + s * kStageBytes);
+          const uint32_t b_base = tc::smem_u32(sB + s * kWStage);
           for (int m = 0; m < MT; ++m) {
             const uint32_t d_tmem = tmem_base + (uint32_t)((buf * 2 + m) * kTileN);
-            const uint32_t a_base = tc::smem_u32(sA + (m * kMaxKC + kc) * kStageBytes);
+            const uint32_t a_base = tc::smem_u32(sA + (m * kMaxKC + kc) * kWStage);
 #pragma unroll
             for (int ks = 0; ks < kKChunk / 16; ++ks) {
               tc::umma_bf16(d_tmem, tc::sdesc_kmajor_sw128(a_base + ks * 32),
@@ -383,9 +421,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           if (k0 + kk >= rows_per_warp || lane >= cpr) continue;
           const int mt = ri / kTileM, ir = ri % kTileM;
           const int kc = lane >> 3, cc = lane & 7;
-          const size_t off = (size_t)(mt * kMaxKC + kc) * kStageBytes + ir * 128 +
+          const size_t off = (size_t)(mt * kMaxKC + kc) * kWStage + ir * 128 +
                              ((cc ^ (ir & 7)) << 4);
-          if (TC_CHECK(off + 16 <= (size_t)kMaxMT * kMaxKC * kStageBytes, 1))
+          if (TC_CHECK(off + 16 <= (size_t)kMaxMT * kMaxKC * kWStage, 1))
             *reinterpret_cast<uint4*>(sA + off) = v[kk];
         }
       }
@@ -396,6 +434,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
     // ---- tiles ----
     RowState st{-INFINITY, 0.f, -INFINITY, 0u};
+    uint64_t* full = b.ufull + g * kNU;
+    uint64_t* empty = b.uempty + g * kNU;
+    const unsigned char* ring = sU + g * kNU * kUBox;
     uint32_t tcount = 0, uit = 0;
     for (int tt = 0; tt < nt && active; ++tt, ++tcount) {
       if (warp_aborted(abort_flag)) break;
@@ -403,32 +444,27 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const int buf = tcount & 1;
       if (!warp_wait(&b.accfull[buf], (tcount >> 1) & 1, abort_flag, p.status)) break;
       tc::tc_fence_after();
-      for (int h = 0; h < 2; ++h) {
-        const int vx = t * kTileN + h * 64;
-        if (vx >= p.V) continue;
-        // boxes are issued (h, m) in order, MT per half: this group's box
-        const uint32_t my = uit + (uint32_t)g;
-        uit += (uint32_t)MT;
-        const int s = my % kNU;
-        if (!warp_wait(&b.ufull[s], (my / kNU) & 1, abort_flag, p.status)) break;
-        const unsigned char* urow = sU + s * kStageBytes + row * 128;
+      for (int h = 0; h < kUPerTile; ++h) {
+        const int vx = t * kTileN + h * kUCols;
+        if (vx >= p.V) break;
+        const int s = uit % kNU;
+        if (!warp_wait(&full[s], (uit / kNU) & 1, abort_flag, p.status)) break;
+        // 64-byte swizzle: 16-byte chunk c of row `row` sits at chunk
+        // c ^ ((row >> 1) & 3) of that row.
+        const unsigned char* urow = ring + s * kUBox + row * (kUCols * 2);
+        uint4 u[4];
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          uint4 u[4];
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            const int cl = half * 4 + c;
-            u[c] = *reinterpret_cast<const uint4*>(urow + ((cl ^ (row & 7)) << 4));
-          }
-          uint32_t acc[32];
-          __syncwarp();
-          tc::tmem_ld_32x32b_x32_wait(tmem_base + ((uint32_t)(q * 32) << 16) +
-                                          (uint32_t)((buf * 2 + g) * kTileN + h * 64 + half * 32),
-                                      acc);
-          fold32(st, acc, u, vx + half * 32, p.V, p, j, rid);
-        }
+        for (int c = 0; c < 4; ++c)
+          u[c] = *reinterpret_cast<const uint4*>(urow + ((c ^ ((row >> 1) & 3)) << 4));
         __syncwarp();
-        if (lane == 0) tc::mbar_arrive(&b.uempty[s]);
+        if (lane == 0) tc::mbar_arrive(&empty[s]);   // the slot's data is in registers
+        ++uit;
+        __syncwarp();
+        uint32_t acc[32];
+        tc::tmem_ld_32x32b_x32_wait(tmem_base + ((uint32_t)(q * 32) << 16) +
+                                        (uint32_t)((buf * 2 + g) * kTileN + h * kUCols),
+                                    acc);
+        fold32(st, acc, u, vx, p, rid);
       }
       tc::tc_fence_before();
       __syncwarp();
@@ -468,13 +504,6 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }  // namespace
 
 int tc_supported(const Ctx& ctx, char* why, size_t why_len) {
-  // Disabled: under CUDA-graph replay after an L2 flush this kernel hit a
-  // launch failure about once per 15-70 cycles (never in eager runs); the
-  // cause is not identified, so nothing selects it until it is.
-  (void)ctx;
-  snprintf(why, why_len,
-           "tcgen05 propose engine disabled: unresolved launch failure under graph replay");
-  return 0;
   if (ctx.cfg.dtype != 1) {
     snprintf(why, why_len, "tcgen05 engine needs bf16 tables");
     return 0;
@@ -522,10 +551,10 @@ cudaError_t launch_propose_tc(const Ctx& ctx, const ProposeArgs& a, cudaStream_t
   {
     const cuuint64_t dims[3] = {(cuuint64_t)a.V, (cuuint64_t)a.gamma, (cuuint64_t)a.R};
     const cuuint64_t strides[2] = {(cuuint64_t)a.V * 2, (cuuint64_t)a.V * 2 * a.gamma};
-    const cuuint32_t box[3] = {64, 1, kTileM};
+    const cuuint32_t box[3] = {kUCols, 1, kTileM};
     const cuuint32_t estr[3] = {1, 1, 1};
     if (encode(&tmU, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(a.U), dims, strides,
-               box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }

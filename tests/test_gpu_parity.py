@@ -128,10 +128,47 @@ def test_mma_and_simt_engines_agree(dsd):
     assert np.max(np.abs(outs[0]["lse_q"] - outs[1]["lse_q"])[ok]) <= parity.LOGIT_TOL
 
 
-def test_disabled_engine_is_rejected_before_any_launch(dsd):
+@pytest.mark.parametrize("R,V,rank,temperature", [
+    (129, 2568, 256, 0.0),     # second M-tile with one request, ragged vocabulary tail
+    (256, 1032, 256, 1.0),     # two full M-tiles, sampled
+    (256, 2600, 256, 0.0),     # two M-tiles, last tile ends in a ragged second U box
+    (300, 1544, 256, 0.0),     # a second launch per step for requests 256..299
+    (40, 3080, 128, 0.0),      # rank 128
+    (16, 4104, 64, 1.0),       # rank 64
+])
+def test_cycle_tc_shapes(dsd, R, V, rank, temperature):
+    spec = synth.scaled(synth.CYCLE_SPECS["greedy"], R=R, V=V, r=rank, ew_std=0.3,
+                        temperature=temperature, seed=200 + R, n_sps=None)
+    x, k = run_cycle(dsd, spec, engine="tcgen05")
+    check_cycle(spec, x, k)
+
+
+def test_tc_mma_simt_engines_agree(dsd):
+    """Tokens identical and lse within tolerance across the three engines at
+    two full M-tiles, on rows whose top-2 margin is not a near tie."""
+    spec = synth.scaled(synth.CYCLE_SPECS["greedy"], R=256, V=4104, ew_std=0.3, seed=35)
+    x = synth.cycle_inputs(spec, device=DEV)
+    outs = []
+    for engine in ("simt", "mma", "tcgen05"):
+        ctx = dsd.Context(spec.V, spec.r, spec.G, spec.R, dtype="bf16", engine=engine)
+        o = ctx.propose(x["U"], x["E"], x["W"], x["conf"], x["prev_tok"], x["req_id"], 0.0, 1)
+        assert ctx.sync_status() == 0
+        assert ctx.last_engine() == engine
+        outs.append({n: t.cpu().numpy() for n, t in o.items()})
+        ctx.close()
+    h = host(x)
+    prop = O.propose(h["U"], h["E"], h["W"], h["conf"], h["prev_tok"],
+                     h["req_id"].astype(np.int64), 0.0, 1)
+    ok = ~parity.draft_exempt(prop["margin"])
+    for o in outs[1:]:
+        assert np.array_equal(outs[0]["tokens"][ok], o["tokens"][ok])
+        assert np.max(np.abs(outs[0]["lse_q"] - o["lse_q"])[ok]) <= parity.LOGIT_TOL
+
+
+def test_tc_engine_rejects_unsupported_config_before_any_launch(dsd):
     spec = synth.scaled(synth.CYCLE_SPECS["greedy"], R=16, V=1032, seed=34)
     x = synth.cycle_inputs(spec, device=DEV)
-    ctx = dsd.Context(spec.V, spec.r, spec.G, spec.R, dtype="bf16", engine="tcgen05")
+    ctx = dsd.Context(spec.V, spec.r, spec.G, spec.R, dtype="bf16", act="silu", engine="tcgen05")
     n0 = ctx.launch_count()
     with pytest.raises(dsd.DsdError) as ei:
         ctx.propose(x["U"], x["E"], x["W"], x["conf"], x["prev_tok"], x["req_id"], 0.0, 1)
@@ -320,4 +357,20 @@ def test_full_size_overlap_sampled_blocks(dsd):
     vmask = np.arange(spec.G)[None, :] < vl[:, None]
     ar = (a_all * vmask).sum(0) / np.maximum(vmask.sum(0), 1)
     assert np.max(np.abs(out["accept_rate"].cpu().numpy() - ar)) <= 1e-5
+    ctx.close()
+
+
+@pytest.mark.parametrize("R,dtype,act,expect", [
+    (16, "bf16", "none", "tcgen05"),
+    (15, "bf16", "none", "simt"),
+    (64, "f32", "none", "simt"),
+    (64, "bf16", "silu", "simt"),
+])
+def test_auto_engine_choice(dsd, R, dtype, act, expect):
+    spec = synth.scaled(synth.CYCLE_SPECS["greedy"], R=R, V=1032, seed=36, dtype=dtype)
+    x = synth.cycle_inputs(spec, device=DEV)
+    ctx = dsd.Context(spec.V, spec.r, spec.G, spec.R, dtype=dtype, act=act, engine="auto")
+    ctx.propose(x["U"], x["E"], x["W"], x["conf"], x["prev_tok"], x["req_id"], 0.0, 1)
+    assert ctx.sync_status() == 0
+    assert ctx.last_engine() == expect
     ctx.close()
