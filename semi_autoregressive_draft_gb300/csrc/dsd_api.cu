@@ -102,7 +102,7 @@ int simt_grid(const Ctx& ctx, int V);
 cudaError_t launch_propose_finalize_n(const Ctx& ctx, const ProposeArgs& a, int n_used,
                                       cudaStream_t s);
 int tc_supported(const Ctx& ctx, char* why, size_t why_len);
-int tc_grid(const Ctx& ctx);
+int tc_vranges(const Ctx& ctx, int R);
 }  // namespace dsd
 
 namespace {
@@ -241,7 +241,7 @@ int dsd_propose(dsd_ctx* ctx, int R, const void* U, const void* E, const void* W
     char why[256];
     if (!tc_supported(*ctx, why, sizeof(why))) return fail(ctx, DSD_ERR_UNSUPPORTED, "%s", why);
     e = launch_propose_tc(*ctx, a, s);
-    n_used = tc_grid(*ctx);
+    n_used = tc_vranges(*ctx, R);
     ctx->last_engine = DSD_ENGINE_TCGEN05;
   } else if (ctx->cfg.engine == DSD_ENGINE_MMA && !mma_ok(ctx)) {
     return fail(ctx, DSD_ERR_UNSUPPORTED,

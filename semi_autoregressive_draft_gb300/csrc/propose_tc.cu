@@ -1,5 +1,6 @@
 // tcgen05 (5th-generation tensor core) engine of dsd_propose: one launch per
-// draft step for a batch of up to 256 requests, one CTA per SM.
+// draft step; CTA = one 128-request M-tile x a contiguous range of 128-wide
+// vocabulary tiles, one CTA per SM.
 //
 // Pages: "Qwen3.8-Flash-Next DSpark 训练实验", Baseline 架构 / Markov 顺序修正
 // (m_i = W_1[t_{i-1}], b_i = W_2 m_i, l_i = l_i^0 + b_i, greedy argmax over the
@@ -8,38 +9,42 @@
 //
 // Draft step j's bias projection for the whole batch is the GEMM
 //     D[R, V] = M[R, r] * W[V, r]^T,    M[r_, :] = E[x_{r_, j-1}, :]
-// with requests on the MMA's M dimension (two 128-row M-tiles for R = 256)
-// and the vocabulary on N (tiles of 128).  Each CTA owns a contiguous range
-// of vocabulary tiles.  Warp roles (12 warps):
+// with requests on the MMA's M dimension and the vocabulary on N.  The grid
+// is (M-tiles) x (vocabulary ranges), so the CTAs of one range read the same
+// W tiles at about the same time and all but the first read them from L2.
+// Warp roles (12 warps):
 //   warp 0      TMA producer of W tiles ([128 vocab x 64 K] boxes, 128-byte
 //               swizzle, L2 evict-last: W stays resident across the steps)
+//               into a 4-stage ring
 //   warp 1      TMEM allocator and the single thread that issues tcgen05.mma
-//               (M = 128, N = 128, K = 16 per instruction) into two
-//               double-buffered fp32 accumulators per M-tile (512 columns)
-//   warps 2, 3  TMA producers of U, one per M-tile: [128 requests x 32 vocab]
-//               boxes of the [V, gamma, R] view (64-byte swizzle,
-//               evict-first: U is read once), each into its own ring
-//   warps 4-11  epilogue, four warps per M-tile: first they gather the A
-//               operand (rows of E for the tokens chosen at step j-1) into
-//               shared memory in the UMMA K-major 128-byte-swizzled layout;
-//               then thread = one request row: tcgen05.ld brings 32
-//               accumulator columns, U comes from shared memory, and the
-//               biased logits are folded into a running base-2 log-sum-exp
-//               and an argmax (greedy) or Gumbel-max (sampled) key; they never
-//               leave registers.
+//               (M = 128, N = 128, K = 16 per instruction) into four fp32
+//               accumulator buffers of 128 columns (512 columns)
+//   warps 2, 3  TMA producers of U, one per 64-column half of each tile:
+//               [128 requests x 64 vocab] boxes of the [V, gamma, R] view
+//               (128-byte swizzle, evict-first: U is read once), each into its
+//               own 3-slot ring
+//   warps 4-11  epilogue, four warps (the four TMEM lane quarters) per column
+//               half: first they gather the A operand (rows of E for the tokens
+//               chosen at step j-1) into shared memory in the UMMA K-major
+//               128-byte-swizzled layout; then thread = one request row and
+//               64 columns per tile: tcgen05.ld brings 32 accumulator columns
+//               at a time, U comes from shared memory, and the biased logits
+//               are folded into a running base-2 log-sum-exp and an argmax
+//               (greedy) or Gumbel-max (sampled) key; they never leave
+//               registers.
 //
 // Every mbarrier has exactly one consumer role that waits on each of its
 // phases in order (a parity wait cannot tell phase k from phase k + 2, so no
-// waiter may skip a phase).  That is why each M-tile has its own U ring and
-// producer: with one ring shared by both M-tiles, a group's consecutive waits
-// on a slot would skip the other group's phase.
+// waiter may skip a phase).  That is why each column half has its own U ring
+// and producer: with one ring shared by both halves, a group's consecutive
+// waits on a slot would skip the other group's phase.
 //
 // At the end each CTA publishes per-request partials: atomicMax of the packed
-// argmax key and an (m, s) log-sum-exp partial.  The next step's launch reads
-// the keys, so the kernel boundary is the batch-wide synchronisation between
-// steps.  Every mbarrier wait is bounded: on time-out the kernel records
-// DSD_ERR_TIMEOUT, stops issuing work, waits (bounded) for its own copies in
-// flight, frees its TMEM and returns.
+// argmax key and an (m, s) log-sum-exp partial per vocabulary range.  The
+// next step's launch reads the keys, so the kernel boundary is the batch-wide
+// synchronisation between steps.  Every mbarrier wait is bounded: on time-out
+// the kernel records DSD_ERR_TIMEOUT, stops issuing work, waits (bounded) for
+// its own copies in flight, frees its TMEM and returns.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <stdio.h>
@@ -54,27 +59,26 @@ namespace {
 constexpr int kTcThreads = 384;
 constexpr int kTileN = 128;          // vocabulary rows per tile (UMMA N)
 constexpr int kTileM = 128;          // requests per M-tile (UMMA M)
-constexpr int kMaxMT = 2;            // M-tiles per launch (R <= 256)
 constexpr int kKChunk = 64;          // K elements per 128-byte swizzle row
 constexpr int kMaxKC = 4;            // rank <= 256
-constexpr int kWStage = 16384;       // one [128 x 64] bf16 W box
-constexpr int kNB = 3;               // W ring stages
-constexpr int kUCols = 32;           // vocabulary columns per U box
-constexpr int kUBox = kTileM * kUCols * 2;   // 8 KB, rows of 64 bytes
-constexpr int kNU = 3;               // U ring slots per M-tile
-constexpr int kUPerTile = kTileN / kUCols;   // U boxes per M-tile and tile
-constexpr int kTmemCols = 512;
+constexpr int kBox = 16384;          // one [128 x 64] bf16 box (W or U)
+constexpr int kNB = 4;               // W ring stages
+constexpr int kHalf = 64;            // vocabulary columns per U box (half a tile)
+constexpr int kNU = 3;               // U ring slots per column half
+constexpr int kNAcc = 4;             // accumulator buffers of kTileN columns
+constexpr int kTmemCols = kNAcc * kTileN;
 constexpr uint32_t kIdesc = tc::idesc_bf16_f32(kTileM, kTileN);
 
 constexpr int kOffA = 0;
-constexpr int kOffB = kOffA + kMaxMT * kMaxKC * kWStage;   // 128 KB of A
-constexpr int kOffU = kOffB + kNB * kWStage;               // + 48 KB of W
-constexpr int kOffBar = kOffU + kMaxMT * kNU * kUBox;      // + 48 KB of U
-// bfull, bempty, ufull[2], uempty[2], accfull[2], accempty[2], aready, mmadone
-constexpr int kNumBars = 2 * kNB + 2 * kMaxMT * kNU + 4 + 2;
+constexpr int kOffB = kOffA + kMaxKC * kBox;            // 64 KB of A
+constexpr int kOffU = kOffB + kNB * kBox;               // + 64 KB of W
+constexpr int kOffBar = kOffU + 2 * kNU * kBox;         // + 96 KB of U
+// bfull, bempty, ufull[2], uempty[2], accfull, accempty, aready, mmadone
+constexpr int kNumBars = 2 * kNB + 4 * kNU + 2 * kNAcc + 2;
 constexpr int kSmemBytes = kOffBar + kNumBars * 8 + 64 + 1024;  // + alignment slack
 static_assert(kSmemBytes <= 232448, "shared memory budget of one CTA");
 static_assert(kOffB % 1024 == 0 && kOffU % 1024 == 0, "swizzled boxes need aligned bases");
+static_assert(kTmemCols == 512, "TMEM allocation is a power of two <= 512 columns");
 
 #ifdef DSD_TC_CHECKS
 // Self-checking build: an out-of-range index records a distinct status code
@@ -94,7 +98,7 @@ struct TcParams {
   float2* parts;             // [gamma][n_part][R_max]
   int* status;
   int j;                     // draft position of this launch
-  int R, R_max, r_off, V, rank, gamma, bias_at_first, n_part, ntiles, MT, sampled;
+  int R, R_max, V, rank, gamma, bias_at_first, n_part, n_vr, ntiles, sampled;
   float inv_T;
   uint32_t k0, k1;
 };
@@ -102,10 +106,10 @@ struct TcParams {
 struct Bars {
   uint64_t* bfull;      // [kNB]
   uint64_t* bempty;     // [kNB]
-  uint64_t* ufull;      // [kMaxMT][kNU]
-  uint64_t* uempty;     // [kMaxMT][kNU]
-  uint64_t* accfull;    // [2]
-  uint64_t* accempty;   // [2]
+  uint64_t* ufull;      // [2][kNU]
+  uint64_t* uempty;     // [2][kNU]
+  uint64_t* accfull;    // [kNAcc]
+  uint64_t* accempty;   // [kNAcc]
   uint64_t* aready;
   uint64_t* mmadone;
 };
@@ -151,10 +155,10 @@ struct RowState {
 
 // Process 32 consecutive columns of one request row: x = acc + u (fp32),
 // masked beyond V; fold into the base-2 log-sum-exp and the argmax key.
-// Pairs of columns go through the packed fp32x2 pipe.
-__device__ __forceinline__ void fold32(RowState& st, const uint32_t (&acc)[32],
-                                       const uint4 (&u)[4], int v0, const TcParams& p,
-                                       uint32_t rid) {
+// Pairs of columns go through the packed fp32x2 pipe; the maximum and the
+// sum are trees, so the dependent chains are a few instructions deep.
+__device__ __forceinline__ void fold32(RowState& st, const uint32_t (&acc)[32], const uint4* u,
+                                       int v0, const TcParams& p, uint32_t rid) {
   float xs[32];
 #pragma unroll
   for (int c = 0; c < 4; ++c) {
@@ -180,32 +184,49 @@ __device__ __forceinline__ void fold32(RowState& st, const uint32_t (&acc)[32],
       tc::unpack2(x2, xs[i], xs[i + 1]);
     }
   }
-  float cm = tc::max3(xs[0], xs[1], xs[2]);
+  // maxima of the eight groups of four, then of the chunk
+  float gm[8];
 #pragma unroll
-  for (int i = 3; i < 31; i += 2) cm = tc::max3(cm, xs[i], xs[i + 1]);
-  cm = fmaxf(cm, xs[31]);
+  for (int g = 0; g < 8; ++g)
+    gm[g] = fmaxf(tc::max3(xs[4 * g], xs[4 * g + 1], xs[4 * g + 2]), xs[4 * g + 3]);
+  const float cm = fmaxf(tc::max3(gm[0], gm[1], gm[2]),
+                         fmaxf(tc::max3(gm[3], gm[4], gm[5]), fmaxf(gm[6], gm[7])));
   const float M = fmaxf(st.m2, cm * kLog2e);
   if (M != -INFINITY) {
     const uint64_t l2 = tc::pack2(kLog2e, kLog2e);
     const uint64_t nm = tc::pack2(-M, -M);
-    uint64_t s2 = tc::pack2(0.f, 0.f);
+    uint64_t e2[16];
 #pragma unroll
-    for (int i = 0; i < 32; i += 2) {
+    for (int i = 0; i < 16; ++i) {
       float a, b;
-      tc::unpack2(tc::fma2(tc::pack2(xs[i], xs[i + 1]), l2, nm), a, b);
-      s2 = tc::add2(s2, tc::pack2(tc::ex2(a), tc::ex2(b)));
+      tc::unpack2(tc::fma2(tc::pack2(xs[2 * i], xs[2 * i + 1]), l2, nm), a, b);
+      e2[i] = tc::pack2(tc::ex2(a), tc::ex2(b));
     }
+#pragma unroll
+    for (int w = 8; w >= 1; w >>= 1)
+#pragma unroll
+      for (int i = 0; i < w; ++i) e2[i] = tc::add2(e2[i], e2[i + w]);
     float slo, shi;
-    tc::unpack2(s2, slo, shi);
+    tc::unpack2(e2[0], slo, shi);
     st.s = st.s * tc::ex2(st.m2 - M) + (slo + shi);
     st.m2 = M;
   }
   if (!p.sampled) {
     if (cm > st.best_z) {
-      int idx = 31;
+      // lowest index attaining the maximum: first group, then within it
+      int g = 7;
 #pragma unroll
-      for (int i = 31; i >= 0; --i)
-        if (xs[i] == cm) idx = i;
+      for (int k = 6; k >= 0; --k)
+        if (gm[k] == cm) g = k;
+      float a0 = xs[0], a1 = xs[1], a2 = xs[2];
+#pragma unroll
+      for (int k = 1; k < 8; ++k)
+        if (g == k) {
+          a0 = xs[4 * k];
+          a1 = xs[4 * k + 1];
+          a2 = xs[4 * k + 2];
+        }
+      const int idx = 4 * g + (a0 == cm ? 0 : a1 == cm ? 1 : a2 == cm ? 2 : 3);
       st.best_z = cm;
       st.best_v = (uint32_t)(v0 + idx);
     }
@@ -244,20 +265,21 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   b.bfull = bars;
   b.bempty = b.bfull + kNB;
   b.ufull = b.bempty + kNB;
-  b.uempty = b.ufull + kMaxMT * kNU;
-  b.accfull = b.uempty + kMaxMT * kNU;
-  b.accempty = b.accfull + 2;
-  b.aready = b.accempty + 2;
+  b.uempty = b.ufull + 2 * kNU;
+  b.accfull = b.uempty + 2 * kNU;
+  b.accempty = b.accfull + kNAcc;
+  b.aready = b.accempty + kNAcc;
   b.mmadone = b.aready + 1;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + kNumBars);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + kNumBars) + 1;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int MT = p.MT;
   const int KC = p.rank / kKChunk;
   const int j = p.j;
-  const int t0 = (int)(((long long)blockIdx.x * p.ntiles) / gridDim.x);
-  const int t1 = (int)(((long long)(blockIdx.x + 1) * p.ntiles) / gridDim.x);
+  const int mt = blockIdx.x / p.n_vr, vr = blockIdx.x - mt * p.n_vr;
+  const int r0 = mt * kTileM;        // first request of this CTA's M-tile
+  const int t0 = (int)(((long long)vr * p.ntiles) / p.n_vr);
+  const int t1 = (int)(((long long)(vr + 1) * p.ntiles) / p.n_vr);
   const int nt = t1 - t0;
 
   if (tid == 0) {
@@ -265,13 +287,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       tc::mbar_init(&b.bfull[i], 1);
       tc::mbar_init(&b.bempty[i], 1);
     }
-    for (int i = 0; i < kMaxMT * kNU; ++i) {
+    for (int i = 0; i < 2 * kNU; ++i) {
       tc::mbar_init(&b.ufull[i], 1);
       tc::mbar_init(&b.uempty[i], 4);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kNAcc; ++i) {
       tc::mbar_init(&b.accfull[i], 1);
-      tc::mbar_init(&b.accempty[i], 4 * MT);
+      tc::mbar_init(&b.accempty[i], 8);
     }
     tc::mbar_init(b.aready, 8);
     tc::mbar_init(b.mmadone, 1);
@@ -300,8 +322,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         for (int kc = 0; kc < KC; ++kc, ++it) {
           const int s = it % kNB;
           if (!wait_bar(&b.bempty[s], ((it / kNB) & 1) ^ 1, abort_flag, p.status)) break;
-          tc::mbar_arrive_expect_tx(&b.bfull[s], kWStage);
-          tc::tma_load_2d(sB + s * kWStage, &tmW, &b.bfull[s], kc * kKChunk, t * kTileN, pol);
+          tc::mbar_arrive_expect_tx(&b.bfull[s], kBox);
+          tc::tma_load_2d(sB + s * kBox, &tmW, &b.bfull[s], kc * kKChunk, t * kTileN, pol);
         }
       // Tail: wait (bounded) for the copies issued last in each stage, then
       // for the consumer's release of every stage.  The releases are
@@ -314,24 +336,23 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         drain_bar(&b.bempty[k % kNB], (k / kNB) & 1);
     }
   } else if (warp == 2 || warp == 3) {
-    // ------------------------------------------- U producer of M-tile g
-    const int g = warp - 2;
-    if (lane == 0 && g < MT) {
+    // ------------------------------------- U producer of column half hs
+    const int hs = warp - 2;
+    if (lane == 0) {
       const uint64_t pol = policy_evict_first();
-      uint64_t* full = b.ufull + g * kNU;
-      uint64_t* empty = b.uempty + g * kNU;
-      unsigned char* ring = sU + g * kNU * kUBox;
+      uint64_t* full = b.ufull + hs * kNU;
+      uint64_t* empty = b.uempty + hs * kNU;
+      unsigned char* ring = sU + hs * kNU * kBox;
       uint32_t it = 0;
-      for (int t = t0; t < t1 && !*abort_flag; ++t)
-        for (int h = 0; h < kUPerTile; ++h) {
-          const int vx = t * kTileN + h * kUCols;
-          if (vx >= p.V) break;
-          const int s = it % kNU;
-          if (!wait_bar(&empty[s], ((it / kNU) & 1) ^ 1, abort_flag, p.status)) break;
-          tc::mbar_arrive_expect_tx(&full[s], kUBox);
-          tc::tma_load_3d(ring + s * kUBox, &tmU, &full[s], vx, j, p.r_off + g * kTileM, pol);
-          ++it;
-        }
+      for (int t = t0; t < t1 && !*abort_flag; ++t) {
+        const int vx = t * kTileN + hs * kHalf;
+        if (vx >= p.V) break;
+        const int s = it % kNU;
+        if (!wait_bar(&empty[s], ((it / kNU) & 1) ^ 1, abort_flag, p.status)) break;
+        tc::mbar_arrive_expect_tx(&full[s], kBox);
+        tc::tma_load_3d(ring + s * kBox, &tmU, &full[s], vx, j, r0, pol);
+        ++it;
+      }
       for (uint32_t k = (it > kNU ? it - kNU : 0); k < it; ++k)
         drain_bar(&full[k % kNU], (k / kNU) & 1);
       for (uint32_t k = (it > kNU ? it - kNU : 0); k < it; ++k)
@@ -340,29 +361,27 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      uint32_t bit = 0, tcount = 0;
+      uint32_t bit = 0;
       bool ok = wait_bar(b.aready, 0, abort_flag, p.status);
       tc::tc_fence_after();
-      for (int t = t0; t < t1 && ok; ++t, ++tcount) {
-        const int buf = tcount & 1;
-        ok = wait_bar(&b.accempty[buf], ((tcount >> 1) & 1) ^ 1, abort_flag, p.status);
+      const uint32_t a_base = tc::smem_u32(sA);
+      for (int tt = 0; tt < nt && ok; ++tt) {
+        const int buf = tt % kNAcc;
+        ok = wait_bar(&b.accempty[buf], ((tt / kNAcc) & 1) ^ 1, abort_flag, p.status);
         if (!ok) break;
         tc::tc_fence_after();
+        const uint32_t d_tmem = tmem_base + (uint32_t)(buf * kTileN);
         for (int kc = 0; kc < KC; ++kc, ++bit) {
           const int s = bit % kNB;
           ok = wait_bar(&b.bfull[s], (bit / kNB) & 1, abort_flag, p.status);
           if (!ok) break;
           tc::tc_fence_after();
-          const uint32_t b_base = tc::smem_u32(sB + s * kWStage);
-          for (int m = 0; m < MT; ++m) {
-            const uint32_t d_tmem = tmem_base + (uint32_t)((buf * 2 + m) * kTileN);
-            const uint32_t a_base = tc::smem_u32(sA + (m * kMaxKC + kc) * kWStage);
+          const uint32_t b_base = tc::smem_u32(sB + s * kBox);
 #pragma unroll
-            for (int ks = 0; ks < kKChunk / 16; ++ks) {
-              tc::umma_bf16(d_tmem, tc::sdesc_kmajor_sw128(a_base + ks * 32),
-                            tc::sdesc_kmajor_sw128(b_base + ks * 32), kIdesc,
-                            (kc | ks) != 0 ? 1u : 0u);
-            }
+          for (int ks = 0; ks < kKChunk / 16; ++ks) {
+            tc::umma_bf16(d_tmem, tc::sdesc_kmajor_sw128(a_base + kc * kBox + ks * 32),
+                          tc::sdesc_kmajor_sw128(b_base + ks * 32), kIdesc,
+                          (kc | ks) != 0 ? 1u : 0u);
           }
           tc::umma_commit(&b.bempty[s]);
         }
@@ -375,25 +394,23 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   } else if (warp >= 4) {
     // ------------------------------------------------------ epilogue
     const int e = warp - 4;          // 0..7
-    const int g = e >> 2;            // M-tile of this warp
+    const int hs = e >> 2;           // column half of each tile
     const int q = warp & 3;          // TMEM lane quarter this warp may access
     const int row = q * 32 + lane;   // row within the M-tile
-    const int r = p.r_off + g * kTileM + row;
-    const bool active = g < MT;
-    const bool valid = active && r < p.R;
+    const int r = r0 + row;
+    const bool valid = r < p.R;
+    const bool warp_rows = r0 + q * 32 < p.R;   // does this warp hold any request?
     const uint32_t rid = valid ? (p.req_id ? p.req_id[r] : (uint32_t)r) : 0u;
-    const int rows_total = MT * kTileM;
 
     // ---- A operand: rows of E for the tokens of step j-1 ----
-    // This warp fills rows e, e+8, ...: lane k fetches the token of row e+8k,
-    // then rows are copied 16 at a time (16 loads in flight per lane) into
-    // the 128-byte-swizzled K-major layout of the UMMA descriptors.
+    // This warp fills rows e, e+8, ..., e+120: lane k < 16 fetches the token
+    // of row e+8k, then the 16 rows are copied (16 loads in flight per lane)
+    // into the 128-byte-swizzled K-major layout of the UMMA descriptors.
     {
       const bool biased = (j > 0) || p.bias_at_first;
-      const int rows_per_warp = rows_total / 8;
       int my_tok = -1;
-      if (lane < rows_per_warp) {
-        const int rr = p.r_off + e + 8 * lane;
+      if (lane < 16) {
+        const int rr = r0 + e + 8 * lane;
         if (biased && rr < p.R) {
           int tk = (j == 0) ? p.prev_tok[rr]
                             : (int)key_index(__ldcg(&p.keys[(size_t)(j - 1) * p.R_max + rr]));
@@ -405,25 +422,22 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
       }
       const int cpr = p.rank / 8;    // 16-byte chunks per row
-      for (int k0 = 0; k0 < rows_per_warp; k0 += 16) {
-        uint4 v[16];
+      uint4 v[16];
+#pragma unroll
+      for (int kk = 0; kk < 16; ++kk) {
+        const int tok = __shfl_sync(0xffffffffu, my_tok, kk);
+        v[kk] = make_uint4(0u, 0u, 0u, 0u);
+        if (tok >= 0 && lane < cpr &&
+            TC_CHECK((size_t)tok * p.rank + lane * 8 + 8 <= (size_t)p.V * p.rank, 2))
+          v[kk] = __ldcg(reinterpret_cast<const uint4*>(p.E + (size_t)tok * p.rank + lane * 8));
+      }
+      if (lane < cpr) {
+        const int kc = lane >> 3, cc = lane & 7;
 #pragma unroll
         for (int kk = 0; kk < 16; ++kk) {
-          const int tok = __shfl_sync(0xffffffffu, my_tok, (k0 + kk) & 31);
-          v[kk] = make_uint4(0u, 0u, 0u, 0u);
-          if (k0 + kk < rows_per_warp && tok >= 0 && lane < cpr &&
-              TC_CHECK((size_t)tok * p.rank + lane * 8 + 8 <= (size_t)p.V * p.rank, 2))
-            v[kk] = __ldcg(reinterpret_cast<const uint4*>(p.E + (size_t)tok * p.rank + lane * 8));
-        }
-#pragma unroll
-        for (int kk = 0; kk < 16; ++kk) {
-          const int ri = e + 8 * (k0 + kk);
-          if (k0 + kk >= rows_per_warp || lane >= cpr) continue;
-          const int mt = ri / kTileM, ir = ri % kTileM;
-          const int kc = lane >> 3, cc = lane & 7;
-          const size_t off = (size_t)(mt * kMaxKC + kc) * kWStage + ir * 128 +
-                             ((cc ^ (ir & 7)) << 4);
-          if (TC_CHECK(off + 16 <= (size_t)kMaxMT * kMaxKC * kWStage, 1))
+          const int ir = e + 8 * kk;
+          const size_t off = (size_t)kc * kBox + ir * 128 + ((cc ^ (ir & 7)) << 4);
+          if (TC_CHECK(off + 16 <= (size_t)kMaxKC * kBox, 1))
             *reinterpret_cast<uint4*>(sA + off) = v[kk];
         }
       }
@@ -434,47 +448,68 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
     // ---- tiles ----
     RowState st{-INFINITY, 0.f, -INFINITY, 0u};
-    uint64_t* full = b.ufull + g * kNU;
-    uint64_t* empty = b.uempty + g * kNU;
-    const unsigned char* ring = sU + g * kNU * kUBox;
-    uint32_t tcount = 0, uit = 0;
-    for (int tt = 0; tt < nt && active; ++tt, ++tcount) {
+    uint64_t* full = b.ufull + hs * kNU;
+    uint64_t* empty = b.uempty + hs * kNU;
+    const unsigned char* ring = sU + hs * kNU * kBox;
+    uint32_t uit = 0;
+    for (int tt = 0; tt < nt; ++tt) {
       if (warp_aborted(abort_flag)) break;
       const int t = t0 + tt;
-      const int buf = tcount & 1;
-      if (!warp_wait(&b.accfull[buf], (tcount >> 1) & 1, abort_flag, p.status)) break;
+      const int buf = tt % kNAcc;
+      if (!warp_wait(&b.accfull[buf], (tt / kNAcc) & 1, abort_flag, p.status)) break;
       tc::tc_fence_after();
-      for (int h = 0; h < kUPerTile; ++h) {
-        const int vx = t * kTileN + h * kUCols;
-        if (vx >= p.V) break;
+      const int vx = t * kTileN + hs * kHalf;
+      if (vx < p.V) {
         const int s = uit % kNU;
         if (!warp_wait(&full[s], (uit / kNU) & 1, abort_flag, p.status)) break;
-        // 64-byte swizzle: 16-byte chunk c of row `row` sits at chunk
-        // c ^ ((row >> 1) & 3) of that row.
-        const unsigned char* urow = ring + s * kUBox + row * (kUCols * 2);
-        uint4 u[4];
+        ++uit;
+        // 128-byte swizzle: 16-byte chunk c of row `row` sits at chunk
+        // c ^ (row & 7) of that row.
+        uint4 u[8];
+        const unsigned char* urow = ring + s * kBox + row * 128;
+        if (warp_rows) {
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
-          u[c] = *reinterpret_cast<const uint4*>(urow + ((c ^ ((row >> 1) & 3)) << 4));
+          for (int c = 0; c < 8; ++c)
+            u[c] = *reinterpret_cast<const uint4*>(urow + ((c ^ (row & 7)) << 4));
+        }
         __syncwarp();
         if (lane == 0) tc::mbar_arrive(&empty[s]);   // the slot's data is in registers
-        ++uit;
         __syncwarp();
-        uint32_t acc[32];
-        tc::tmem_ld_32x32b_x32_wait(tmem_base + ((uint32_t)(q * 32) << 16) +
-                                        (uint32_t)((buf * 2 + g) * kTileN + h * kUCols),
-                                    acc);
-        fold32(st, acc, u, vx, p, rid);
+        if (warp_rows) {
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            const int v0 = vx + c * 32;
+            if (v0 >= p.V) break;
+            uint32_t acc[32];
+            tc::tmem_ld_32x32b_x32_wait(tmem_base + ((uint32_t)(q * 32) << 16) +
+                                            (uint32_t)(buf * kTileN + hs * kHalf + c * 32),
+                                        acc);
+            fold32(st, acc, u + 4 * c, v0, p, rid);
+          }
+        }
       }
       tc::tc_fence_before();
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(&b.accempty[buf]);
     }
 
-    // ---- publish this CTA's partials of step j ----
-    if (valid && TC_CHECK(blockIdx.x < (unsigned)p.n_part && r < p.R_max, 5)) {
-      atomicMax(&p.keys[(size_t)j * p.R_max + r], make_key(st.best_z, st.best_v));
-      p.parts[((size_t)j * p.n_part + blockIdx.x) * p.R_max + r] = make_float2(st.m2, st.s);
+    // ---- merge the two column halves of each row, publish step j's partial ----
+    // The A region is free: the last accumulator barrier this warp waited on
+    // was committed after every MMA that reads A, so they have all completed.
+    RowState* xch = reinterpret_cast<RowState*>(sA);
+    if (hs == 1) xch[row] = st;
+    asm volatile("bar.sync 1, 256;" ::: "memory");   // the eight epilogue warps
+    if (hs == 0) {
+      const RowState o = xch[row];
+      const Lse2 l = lse2_merge(Lse2{st.m2, st.s}, Lse2{o.m2, o.s});
+      if (o.best_z > st.best_z || (o.best_z == st.best_z && o.best_v < st.best_v)) {
+        st.best_z = o.best_z;
+        st.best_v = o.best_v;
+      }
+      if (valid && TC_CHECK(vr < p.n_part && r < p.R_max, 5)) {
+        atomicMax(&p.keys[(size_t)j * p.R_max + r], make_key(st.best_z, st.best_v));
+        p.parts[((size_t)j * p.n_part + vr) * p.R_max + r] = make_float2(l.m, l.s);
+      }
     }
   }
   tc::tc_fence_before();
@@ -529,9 +564,15 @@ int tc_supported(const Ctx& ctx, char* why, size_t why_len) {
   return 1;
 }
 
-int tc_grid(const Ctx& ctx) {
+// Vocabulary ranges per M-tile: the grid is M-tiles x ranges, one CTA per SM.
+int tc_vranges(const Ctx& ctx, int R) {
+  const int MT = (R + kTileM - 1) / kTileM;
   const int ntiles = (ctx.cfg.V + kTileN - 1) / kTileN;
-  return ntiles < ctx.num_sms ? ntiles : ctx.num_sms;
+  int n = ctx.num_sms / (MT > 0 ? MT : 1);
+  if (n < 1) n = 1;
+  if (n > ntiles) n = ntiles;
+  if (n > ctx.n_part) n = ctx.n_part;
+  return n;
 }
 
 cudaError_t launch_propose_tc(const Ctx& ctx, const ProposeArgs& a, cudaStream_t s) {
@@ -551,10 +592,10 @@ cudaError_t launch_propose_tc(const Ctx& ctx, const ProposeArgs& a, cudaStream_t
   {
     const cuuint64_t dims[3] = {(cuuint64_t)a.V, (cuuint64_t)a.gamma, (cuuint64_t)a.R};
     const cuuint64_t strides[2] = {(cuuint64_t)a.V * 2, (cuuint64_t)a.V * 2 * a.gamma};
-    const cuuint32_t box[3] = {kUCols, 1, kTileM};
+    const cuuint32_t box[3] = {kHalf, 1, kTileM};
     const cuuint32_t estr[3] = {1, 1, 1};
     if (encode(&tmU, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(a.U), dims, strides,
-               box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+               box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }
@@ -584,21 +625,16 @@ cudaError_t launch_propose_tc(const Ctx& ctx, const ProposeArgs& a, cudaStream_t
   p.inv_T = a.temperature > 0.f ? 1.f / a.temperature : 1.f;
   p.k0 = (uint32_t)(a.seed & 0xFFFFFFFFull);
   p.k1 = (uint32_t)(a.seed >> 32);
-  const int grid = tc_grid(ctx);
-  const int groups = (a.R + kMaxMT * kTileM - 1) / (kMaxMT * kTileM);
+  p.n_vr = tc_vranges(ctx, a.R);
+  const int grid = ((a.R + kTileM - 1) / kTileM) * p.n_vr;
 
-  // Steps in order; within a step, request groups of <= 256 are independent.
+  // One launch per step: the next step's A operand needs every CTA's argmax.
   for (int j = 0; j < a.gamma; ++j) {
     p.j = j;
-    for (int gi = 0; gi < groups; ++gi) {
-      p.r_off = gi * kMaxMT * kTileM;
-      const int rem = a.R - p.r_off;
-      p.MT = rem > kTileM ? 2 : 1;
-      propose_tc_kernel<<<grid, kTcThreads, kSmemBytes, s>>>(tmW, tmU, p);
-      e = cudaGetLastError();
-      if (e != cudaSuccess) return e;
-      count_launch(ctx);
-    }
+    propose_tc_kernel<<<grid, kTcThreads, kSmemBytes, s>>>(tmW, tmU, p);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    count_launch(ctx);
   }
   return cudaSuccess;
 }
