@@ -153,10 +153,26 @@ struct RowState {
   uint32_t best_v;
 };
 
+// x = u (bf16, widened exactly) + acc (fp32) for the two halves of one
+// 32-bit word of U, one instruction each.
+__device__ __forceinline__ void add_bf16x2(uint32_t w, uint32_t a_lo, uint32_t a_hi, float& lo,
+                                           float& hi) {
+  asm("{\n\t.reg .b16 l, h;\n\tmov.b32 {l, h}, %2;\n\t"
+      "add.rn.f32.bf16 %0, l, %3;\n\tadd.rn.f32.bf16 %1, h, %4;\n\t}"
+      : "=f"(lo), "=f"(hi)
+      : "r"(w), "f"(__uint_as_float(a_lo)), "f"(__uint_as_float(a_hi)));
+}
+
+// Largest jump of the running base-2 maximum that is folded without
+// rescaling: terms of the running sum stay below 2^kLagBits.
+constexpr float kLagBits = 8.f;
+
 // Process 32 consecutive columns of one request row: x = acc + u (fp32),
 // masked beyond V; fold into the base-2 log-sum-exp and the argmax key.
-// Pairs of columns go through the packed fp32x2 pipe; the maximum and the
-// sum are trees, so the dependent chains are a few instructions deep.
+// The log-sum-exp state (m2, s) means sum = s * 2^m2.  Its reference m2 is
+// only raised when the chunk maximum exceeds it by more than kLagBits, so
+// the exponentials of a chunk do not wait for the chunk's maximum; pairs of
+// columns go through the packed fp32x2 pipe and the sum is a tree.
 __device__ __forceinline__ void fold32(RowState& st, const uint32_t (&acc)[32], const uint4* u,
                                        int v0, const TcParams& p, uint32_t rid) {
   float xs[32];
@@ -166,9 +182,7 @@ __device__ __forceinline__ void fold32(RowState& st, const uint32_t (&acc)[32], 
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       const int i = c * 8 + 2 * e;
-      const uint64_t x2 = tc::add2(tc::pack2(__uint_as_float(acc[i]), __uint_as_float(acc[i + 1])),
-                                   tc::pack2(bf16lo(w[e]), bf16hi(w[e])));
-      tc::unpack2(x2, xs[i], xs[i + 1]);
+      add_bf16x2(w[e], acc[i], acc[i + 1], xs[i], xs[i + 1]);
     }
   }
   if (v0 + 32 > p.V) {
@@ -191,10 +205,14 @@ __device__ __forceinline__ void fold32(RowState& st, const uint32_t (&acc)[32], 
     gm[g] = fmaxf(tc::max3(xs[4 * g], xs[4 * g + 1], xs[4 * g + 2]), xs[4 * g + 3]);
   const float cm = fmaxf(tc::max3(gm[0], gm[1], gm[2]),
                          fmaxf(tc::max3(gm[3], gm[4], gm[5]), fmaxf(gm[6], gm[7])));
-  const float M = fmaxf(st.m2, cm * kLog2e);
-  if (M != -INFINITY) {
+  const float cm2 = cm * kLog2e;
+  if (cm2 > st.m2 + kLagBits) {       // rare after the first chunks
+    st.s *= tc::ex2(st.m2 - cm2);     // 0 while the state is empty
+    st.m2 = cm2;
+  }
+  if (st.m2 != -INFINITY) {
     const uint64_t l2 = tc::pack2(kLog2e, kLog2e);
-    const uint64_t nm = tc::pack2(-M, -M);
+    const uint64_t nm = tc::pack2(-st.m2, -st.m2);
     uint64_t e2[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
@@ -208,8 +226,7 @@ __device__ __forceinline__ void fold32(RowState& st, const uint32_t (&acc)[32], 
       for (int i = 0; i < w; ++i) e2[i] = tc::add2(e2[i], e2[i + w]);
     float slo, shi;
     tc::unpack2(e2[0], slo, shi);
-    st.s = st.s * tc::ex2(st.m2 - M) + (slo + shi);
-    st.m2 = M;
+    st.s += slo + shi;
   }
   if (!p.sampled) {
     if (cm > st.best_z) {
@@ -282,6 +299,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const int t1 = (int)(((long long)(vr + 1) * p.ntiles) / p.n_vr);
   const int nt = t1 - t0;
 
+  // The next draft step's grid may start on SMs as this one's CTAs exit: it
+  // initialises and prefetches W and U (inputs) while this step drains, and
+  // waits for this step's argmax keys in griddepcontrol.wait below.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (tid == 0) {
     for (int i = 0; i < kNB; ++i) {
       tc::mbar_init(&b.bfull[i], 1);
@@ -401,6 +422,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const bool valid = r < p.R;
     const bool warp_rows = r0 + q * 32 < p.R;   // does this warp hold any request?
     const uint32_t rid = valid ? (p.req_id ? p.req_id[r] : (uint32_t)r) : 0u;
+
+    // The keys of step j-1 come from the previous grid: wait until it has
+    // completed and its writes are visible (a no-op without a programmatic
+    // dependency).
+    asm volatile("griddepcontrol.wait;" ::: "memory");
 
     // ---- A operand: rows of E for the tokens of step j-1 ----
     // This warp fills rows e, e+8, ..., e+120: lane k < 16 fetches the token
@@ -629,10 +655,23 @@ cudaError_t launch_propose_tc(const Ctx& ctx, const ProposeArgs& a, cudaStream_t
   const int grid = ((a.R + kTileM - 1) / kTileM) * p.n_vr;
 
   // One launch per step: the next step's A operand needs every CTA's argmax.
+  // Steps after the first are launched with a programmatic dependency on the
+  // previous step (see griddepcontrol in the kernel); the first follows the
+  // memset of the keys in plain stream order.
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kTcThreads);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = s;
+  cfg.attrs = attr;
   for (int j = 0; j < a.gamma; ++j) {
     p.j = j;
-    propose_tc_kernel<<<grid, kTcThreads, kSmemBytes, s>>>(tmW, tmU, p);
-    e = cudaGetLastError();
+    cfg.numAttrs = j > 0 ? 1 : 0;
+    e = cudaLaunchKernelEx(&cfg, propose_tc_kernel, tmW, tmU, p);
+    if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     count_launch(ctx);
   }
