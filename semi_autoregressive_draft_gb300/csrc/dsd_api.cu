@@ -57,7 +57,8 @@ size_t carve(dsd_ctx* c, unsigned char* base) {
   w.res_keys = reinterpret_cast<unsigned long long*>(take(sizeof(unsigned long long) * 2 * (size_t)Rm));
   w.res_sums = reinterpret_cast<float*>(take(sizeof(float) * 2 * (size_t)Rm));
   w.ov_parts = reinterpret_cast<float*>(take(sizeof(float) * 64));
-  w.gbar = reinterpret_cast<unsigned int*>(take(sizeof(unsigned int) * 64));
+  w.sched_order = reinterpret_cast<int*>(take(sizeof(int) * (size_t)Rm * G));
+  w.tickets = reinterpret_cast<unsigned int*>(take(sizeof(unsigned int) * 64));
   if (base) c->ws = w;
   return off;
 }

@@ -23,31 +23,34 @@ __device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w <
 __device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
 // L2 cache policies: evict-first for rows read exactly once (U, P, Q),
-// evict-last for tables reused across steps and CTAs (W, E).
+// evict-last for tables reused across steps and CTAs (W, E).  The policy is
+// a constant, so these are plain (non-volatile) asm the compiler can hoist
+// out of loops instead of re-creating it for every load.
 __device__ __forceinline__ uint64_t policy_evict_first() {
   uint64_t pol;
-  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  asm("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
   return pol;
 }
 __device__ __forceinline__ uint64_t policy_evict_last() {
   uint64_t pol;
-  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+  asm("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
   return pol;
 }
-// Streaming 16-byte load: no L1 allocation, evict-first in L2.
+// Streaming 16-byte load of read-only data: no L1 allocation, evict-first
+// in L2.  Not volatile: the compiler may schedule independent loads early.
 __device__ __forceinline__ uint4 ld_stream16(const void* p) {
   uint4 r;
-  asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], %5;"
-               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-               : "l"(p), "l"(policy_evict_first()));
+  asm("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], %5;"
+      : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+      : "l"(p), "l"(policy_evict_first()));
   return r;
 }
 // 16-byte load kept in L2 (reused tables: W, E).
 __device__ __forceinline__ uint4 ld_keep16(const void* p) {
   uint4 r;
-  asm volatile("ld.global.nc.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], %5;"
-               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-               : "l"(p), "l"(policy_evict_last()));
+  asm("ld.global.nc.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], %5;"
+      : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+      : "l"(p), "l"(policy_evict_last()));
   return r;
 }
 

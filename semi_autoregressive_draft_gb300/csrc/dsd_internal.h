@@ -43,7 +43,8 @@ struct Workspace {
   unsigned long long* res_keys; // [2][R_max] residual key, fallback key
   float* res_sums;              // [2][R_max] sum of the residual, sum of p
   float* ov_parts;              // scratch of the overlap kernels
-  unsigned int* gbar;           // [64] grid-barrier counters of the tcgen05 propose launches
+  int* sched_order;             // [R_max*gamma] slot indices in schedule (sorted) order
+  unsigned int* tickets;        // [64] last-CTA tickets; each user resets its own to zero
 };
 
 struct Config {

@@ -385,25 +385,28 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       uint32_t bit = 0;
       bool ok = wait_bar(b.aready, 0, abort_flag, p.status);
       tc::tc_fence_after();
-      const uint32_t a_base = tc::smem_u32(sA);
+      // Descriptors of the first A box and the first W stage; the others
+      // differ only in the start-address field, which counts 16-byte units.
+      // Every operand lies inside this CTA's shared memory (< 2^18 bytes), so
+      // adding an offset in those units never carries out of the field.
+      const uint64_t da0 = tc::sdesc_kmajor_sw128(tc::smem_u32(sA));
+      const uint64_t db0 = tc::sdesc_kmajor_sw128(tc::smem_u32(sB));
       for (int tt = 0; tt < nt && ok; ++tt) {
         const int buf = tt % kNAcc;
         ok = wait_bar(&b.accempty[buf], ((tt / kNAcc) & 1) ^ 1, abort_flag, p.status);
         if (!ok) break;
-        tc::tc_fence_after();
+        tc::tc_fence_after();    // the epilogue's TMEM reads of this buffer are done
         const uint32_t d_tmem = tmem_base + (uint32_t)(buf * kTileN);
         for (int kc = 0; kc < KC; ++kc, ++bit) {
           const int s = bit % kNB;
+          // TMA data: the mbarrier's completion makes it visible to the MMA
           ok = wait_bar(&b.bfull[s], (bit / kNB) & 1, abort_flag, p.status);
           if (!ok) break;
-          tc::tc_fence_after();
-          const uint32_t b_base = tc::smem_u32(sB + s * kBox);
+          const uint64_t da = da0 + (uint64_t)((kc * kBox) >> 4);
+          const uint64_t db = db0 + (uint64_t)((s * kBox) >> 4);
 #pragma unroll
-          for (int ks = 0; ks < kKChunk / 16; ++ks) {
-            tc::umma_bf16(d_tmem, tc::sdesc_kmajor_sw128(a_base + kc * kBox + ks * 32),
-                          tc::sdesc_kmajor_sw128(b_base + ks * 32), kIdesc,
-                          (kc | ks) != 0 ? 1u : 0u);
-          }
+          for (int ks = 0; ks < kKChunk / 16; ++ks)   // K = 16 is 32 bytes = 2 units
+            tc::umma_bf16(d_tmem, da + 2 * ks, db + 2 * ks, kIdesc, (kc | ks) != 0 ? 1u : 0u);
           tc::umma_commit(&b.bempty[s]);
         }
         if (ok) tc::umma_commit(&b.accfull[buf]);

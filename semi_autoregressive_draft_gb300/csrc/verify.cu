@@ -26,6 +26,17 @@ cudaError_t launch_residual_simt(const Ctx& ctx, const VerifyArgs& a, cudaStream
 
 constexpr int kRowThreads = 256;
 
+__device__ __forceinline__ float max_nan(float a, float b) {
+  float r;
+  asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ float max3_nan(float a, float b, float c) {
+  float r;
+  asm("max.NaN.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
 __global__ void __launch_bounds__(1024) verify_rows_build(const int32_t* keep_len, int R, int gamma,
                                                           int2* rows, int* row_off, int* B_out,
                                                           int* status) {
@@ -78,6 +89,7 @@ __global__ void __launch_bounds__(1024) verify_rows_build(const int32_t* keep_le
 }
 
 struct RowsParams {
+  int* status;
   const void* P;
   const int32_t* keep_len;
   const uint32_t* req_id;
@@ -110,53 +122,89 @@ __global__ void __launch_bounds__(kRowThreads) verify_rows(RowsParams p) {
     const int v_end = min(p.V, v_begin + p.chunk);
     Lse2 st = lse2_empty();
     unsigned long long best = 0ull;
-    for (int v0 = v_begin + tid * epc; v0 < v_end; v0 += kRowThreads * epc) {
-      const uint4 q = ld_stream16(row + v0);
-      float x[8];
-      if constexpr (sizeof(T) == 2) {
-        x[0] = bf16lo(q.x); x[1] = bf16hi(q.x); x[2] = bf16lo(q.y); x[3] = bf16hi(q.y);
-        x[4] = bf16lo(q.z); x[5] = bf16hi(q.z); x[6] = bf16lo(q.w); x[7] = bf16hi(q.w);
-      } else {
-        x[0] = __uint_as_float(q.x); x[1] = __uint_as_float(q.y);
-        x[2] = __uint_as_float(q.z); x[3] = __uint_as_float(q.w);
+    // Greedy: running maximum value and its lowest index; a chunk's index is
+    // looked up only when its maximum beats the running one.  NaN propagates
+    // through max.NaN and is reported.
+    float bz = -INFINITY;
+    uint32_t bv = 0xFFFFFFFFu;
+    bool nan_seen = false;
+    const int v_first = v_begin + tid * epc;
+    // Four 16-byte loads in flight per thread: with one, the grid keeps too
+    // few bytes in flight to cover the HBM latency.
+    constexpr int kUnroll = 4;
+    for (int vb = v_first; vb < v_end; vb += kUnroll * kRowThreads * epc) {
+      uint4 q[kUnroll];
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) {
+        const int v0 = vb + u * kRowThreads * epc;
+        q[u] = v0 < v_end ? ld_stream16(row + v0) : make_uint4(0u, 0u, 0u, 0u);
       }
-      if (!p.sampled) {
 #pragma unroll
-        for (int e = 0; e < epc; ++e) {
-          const unsigned long long key = make_key(x[e], (uint32_t)(v0 + e));
-          best = key > best ? key : best;
+      for (int u = 0; u < kUnroll; ++u) {
+        const int v0 = vb + u * kRowThreads * epc;
+        if (v0 >= v_end) break;
+        float x[8];
+        if constexpr (sizeof(T) == 2) {
+          x[0] = bf16lo(q[u].x); x[1] = bf16hi(q[u].x); x[2] = bf16lo(q[u].y); x[3] = bf16hi(q[u].y);
+          x[4] = bf16lo(q[u].z); x[5] = bf16hi(q[u].z); x[6] = bf16lo(q[u].w); x[7] = bf16hi(q[u].w);
+        } else {
+          x[0] = __uint_as_float(q[u].x); x[1] = __uint_as_float(q[u].y);
+          x[2] = __uint_as_float(q[u].z); x[3] = __uint_as_float(q[u].w);
         }
-      } else {
-        float cmax = -INFINITY;
+        if (!p.sampled) {
+          float m = max3_nan(x[0], x[1], x[2]);
 #pragma unroll
-        for (int e = 0; e < epc; ++e) {
-          x[e] *= p.inv_T;
-          cmax = fmaxf(cmax, x[e] * kLog2e);
-        }
-        const float M = fmaxf(st.m, cmax);
-        float s = st.s * exp2f(st.m - M);
+          for (int e = 3; e < epc; e += 2)
+            m = e + 1 < epc ? max3_nan(m, x[e], x[e + 1]) : max_nan(m, x[e]);
+          if (!(m <= bz)) {          // a larger maximum, or NaN
+            if (m != m) {
+              nan_seen = true;
+            } else {
+              int idx = epc - 1;
 #pragma unroll
-        for (int e = 0; e < epc; ++e) s += exp2f(fmaf(x[e], kLog2e, -M));
-        st.m = M;
-        st.s = s;
-        if (bonus) {
+              for (int e = epc - 2; e >= 0; --e)
+                if (x[e] == m) idx = e;
+              bz = m;
+              bv = (uint32_t)(v0 + idx);
+            }
+          }
+        } else {
+          float cmax = -INFINITY;
 #pragma unroll
-          for (int e = 0; e < epc; e += 4) {
-            const uint32_t v = (uint32_t)(v0 + e);
-            const Philox4 ph = philox4x32_10(v >> 2, (uint32_t)t, rid, 3u, p.k0, p.k1);
-            // v0 is a multiple of 4 (epc-aligned), so words map to v .. v+3
-            const float z0 = x[e + 0] + gumbel_from_word(ph.x);
-            const float z1 = x[e + 1] + gumbel_from_word(ph.y);
-            const float z2 = x[e + 2] + gumbel_from_word(ph.z);
-            const float z3 = x[e + 3] + gumbel_from_word(ph.w);
-            unsigned long long k;
-            k = make_key(z0, v + 0); best = k > best ? k : best;
-            k = make_key(z1, v + 1); best = k > best ? k : best;
-            k = make_key(z2, v + 2); best = k > best ? k : best;
-            k = make_key(z3, v + 3); best = k > best ? k : best;
+          for (int e = 0; e < epc; ++e) {
+            x[e] *= p.inv_T;
+            cmax = fmaxf(cmax, x[e] * kLog2e);
+          }
+          const float M = fmaxf(st.m, cmax);
+          float s = st.s * exp2f(st.m - M);
+#pragma unroll
+          for (int e = 0; e < epc; ++e) s += exp2f(fmaf(x[e], kLog2e, -M));
+          st.m = M;
+          st.s = s;
+          if (bonus) {
+#pragma unroll
+            for (int e = 0; e < epc; e += 4) {
+              const uint32_t v = (uint32_t)(v0 + e);
+              const Philox4 ph = philox4x32_10(v >> 2, (uint32_t)t, rid, 3u, p.k0, p.k1);
+              // v0 is a multiple of 4 (epc-aligned), so words map to v .. v+3
+              const float z0 = x[e + 0] + gumbel_from_word(ph.x);
+              const float z1 = x[e + 1] + gumbel_from_word(ph.y);
+              const float z2 = x[e + 2] + gumbel_from_word(ph.z);
+              const float z3 = x[e + 3] + gumbel_from_word(ph.w);
+              unsigned long long k;
+              k = make_key(z0, v + 0); best = k > best ? k : best;
+              k = make_key(z1, v + 1); best = k > best ? k : best;
+              k = make_key(z2, v + 2); best = k > best ? k : best;
+              k = make_key(z3, v + 3); best = k > best ? k : best;
+            }
           }
         }
       }
+    }
+    if (!p.sampled && v_first < v_end) {
+      if (nan_seen) set_status(p.status, kErrNonfinite);
+      // every element was -inf: the first one holds the maximum
+      best = make_key(bz, bv == 0xFFFFFFFFu ? (uint32_t)v_first : bv);
     }
     st = warp_lse2(st);
     best = warp_max_u64(best);
@@ -299,6 +347,7 @@ cudaError_t launch_verify(const Ctx& ctx, const VerifyArgs& a, cudaStream_t s) {
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
   RowsParams rp{};
+  rp.status = ws.status;
   rp.P = a.P;
   rp.keep_len = a.keep_len;
   rp.req_id = a.req_id;
