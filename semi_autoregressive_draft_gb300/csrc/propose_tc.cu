@@ -14,8 +14,9 @@
 // W tiles at about the same time and all but the first read them from L2.
 // Warp roles (12 warps):
 //   warp 0      TMA producer of W tiles ([128 vocab x 64 K] boxes, 128-byte
-//               swizzle, L2 evict-last: W stays resident across the steps)
-//               into a 4-stage ring
+//               swizzle, L2 evict-last: W stays resident across the steps),
+//               two boxes per ring stage and barrier
+//               into a 2-stage ring (64 KB)
 //   warp 1      TMEM allocator and the single thread that issues tcgen05.mma
 //               (M = 128, N = 128, K = 16 per instruction) into four fp32
 //               accumulator buffers of 128 columns (512 columns)
@@ -62,7 +63,8 @@ constexpr int kTileM = 128;          // requests per M-tile (UMMA M)
 constexpr int kKChunk = 64;          // K elements per 128-byte swizzle row
 constexpr int kMaxKC = 4;            // rank <= 256
 constexpr int kBox = 16384;          // one [128 x 64] bf16 box (W or U)
-constexpr int kNB = 4;               // W ring stages
+constexpr int kCPS = 2;              // W boxes (K-chunks) per ring stage: one barrier each way
+constexpr int kNB = 2;               // W ring stages
 constexpr int kHalf = 64;            // vocabulary columns per U box (half a tile)
 constexpr int kNU = 3;               // U ring slots per column half
 constexpr int kNAcc = 4;             // accumulator buffers of kTileN columns
@@ -71,7 +73,7 @@ constexpr uint32_t kIdesc = tc::idesc_bf16_f32(kTileM, kTileN);
 
 constexpr int kOffA = 0;
 constexpr int kOffB = kOffA + kMaxKC * kBox;            // 64 KB of A
-constexpr int kOffU = kOffB + kNB * kBox;               // + 64 KB of W
+constexpr int kOffU = kOffB + kNB * kCPS * kBox;        // + 64 KB of W
 constexpr int kOffBar = kOffU + 2 * kNU * kBox;         // + 96 KB of U
 // bfull, bempty, ufull[2], uempty[2], accfull, accempty, aready, mmadone
 constexpr int kNumBars = 2 * kNB + 4 * kNU + 2 * kNAcc + 2;
@@ -340,11 +342,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const uint64_t pol = policy_evict_last();
       uint32_t it = 0;
       for (int t = t0; t < t1 && !*abort_flag; ++t)
-        for (int kc = 0; kc < KC; ++kc, ++it) {
+        for (int k0 = 0; k0 < KC; k0 += kCPS, ++it) {
           const int s = it % kNB;
+          const int nch = KC - k0 < kCPS ? KC - k0 : kCPS;
           if (!wait_bar(&b.bempty[s], ((it / kNB) & 1) ^ 1, abort_flag, p.status)) break;
-          tc::mbar_arrive_expect_tx(&b.bfull[s], kBox);
-          tc::tma_load_2d(sB + s * kBox, &tmW, &b.bfull[s], kc * kKChunk, t * kTileN, pol);
+          tc::mbar_arrive_expect_tx(&b.bfull[s], (uint32_t)(nch * kBox));
+          for (int c = 0; c < nch; ++c)
+            tc::tma_load_2d(sB + (s * kCPS + c) * kBox, &tmW, &b.bfull[s], (k0 + c) * kKChunk,
+                            t * kTileN, pol);
         }
       // Tail: wait (bounded) for the copies issued last in each stage, then
       // for the consumer's release of every stage.  The releases are
@@ -397,16 +402,20 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (!ok) break;
         tc::tc_fence_after();    // the epilogue's TMEM reads of this buffer are done
         const uint32_t d_tmem = tmem_base + (uint32_t)(buf * kTileN);
-        for (int kc = 0; kc < KC; ++kc, ++bit) {
+        for (int k0 = 0; k0 < KC; k0 += kCPS, ++bit) {
           const int s = bit % kNB;
+          const int nch = KC - k0 < kCPS ? KC - k0 : kCPS;
           // TMA data: the mbarrier's completion makes it visible to the MMA
           ok = wait_bar(&b.bfull[s], (bit / kNB) & 1, abort_flag, p.status);
           if (!ok) break;
-          const uint64_t da = da0 + (uint64_t)((kc * kBox) >> 4);
-          const uint64_t db = db0 + (uint64_t)((s * kBox) >> 4);
+          for (int c = 0; c < nch; ++c) {
+            const int kc = k0 + c;
+            const uint64_t da = da0 + (uint64_t)((kc * kBox) >> 4);
+            const uint64_t db = db0 + (uint64_t)(((s * kCPS + c) * kBox) >> 4);
 #pragma unroll
-          for (int ks = 0; ks < kKChunk / 16; ++ks)   // K = 16 is 32 bytes = 2 units
-            tc::umma_bf16(d_tmem, da + 2 * ks, db + 2 * ks, kIdesc, (kc | ks) != 0 ? 1u : 0u);
+            for (int ks = 0; ks < kKChunk / 16; ++ks)   // K = 16 is 32 bytes = 2 units
+              tc::umma_bf16(d_tmem, da + 2 * ks, db + 2 * ks, kIdesc, (kc | ks) != 0 ? 1u : 0u);
+          }
           tc::umma_commit(&b.bempty[s]);
         }
         if (ok) tc::umma_commit(&b.accfull[buf]);
