@@ -37,6 +37,8 @@ KERNEL_SOURCES = {
     "simt_bias_kernel": ["propose_simt.cu", "dsd_common.cuh"],
     "propose_tc_kernel": ["propose_tc.cu", "dsd_common.cuh"],
     "propose_mma_kernel": ["propose_mma.cu", "dsd_common.cuh"],
+    "verify_rows": ["verify.cu", "dsd_common.cuh"],
+    "overlap_rows": ["overlap.cu", "dsd_common.cuh"],
 }
 FALLBACK_HBM_GBS = 6800.0
 
@@ -82,8 +84,9 @@ def source_hash(kernel: str) -> str:
 
 
 def traffic_for(kernel: str, workload: str):
-    """DRAM bytes per launch from the committed ncu summary, or None when the
-    kernel source changed since the counters were taken."""
+    """DRAM bytes (read + write) per roofline unit from the committed ncu
+    summary, or None when the kernel source changed since the counters were
+    taken."""
     try:
         with open(TRAFFIC_FILE) as f:
             table = json.load(f)
@@ -92,7 +95,7 @@ def traffic_for(kernel: str, workload: str):
     ent = table.get(kernel, {}).get(workload)
     if not ent or ent.get("source_hash") != source_hash(kernel):
         return None
-    return ent.get("dram_bytes_per_launch")
+    return ent.get("dram_bytes")
 
 
 def hbm_peak():
@@ -351,7 +354,7 @@ def run_overlap(args, dsd, synth, dev, world):
                      "unit": "GB/s", "frac": achieved / peak,
                      "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)",
                      "traffic": traffic_for("overlap_rows", "overlap"),
-                     "alg_bytes_per_launch": alg,
+                     "alg_bytes": alg, "per": "one overlap call",
                      "alg_bytes_note": "valid P and Q rows once + a, l1 [N, gamma] + valid_len"},
         "cpu_baseline": None, "e2e": None,
         "gpu_launches": launches, "clocks": clk,
@@ -530,7 +533,8 @@ def run_ours(args):
                 "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                 "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)",
                 "traffic": traffic_for(engine_kernel, spec.name),
-                "alg_bytes_per_launch": pbytes,
+                "alg_bytes": pbytes,
+                "per": "propose phase (the gamma draft-step launches and the finalize)",
                 "alg_bytes_note": "U rows once + W once + gathered E rows + small I/O"}
     vbytes = verify_alg_bytes(spec, B)
 

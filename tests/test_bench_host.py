@@ -60,9 +60,9 @@ def test_algorithmic_bytes_of_the_high_concurrency_workload():
 def test_traffic_lookup_is_null_when_source_changed(tmp_path, monkeypatch):
     f = tmp_path / "traffic.json"
     f.write_text(json.dumps({"simt_bias_kernel": {"greedy": {
-        "source_hash": "0" * 16, "dram_bytes_per_launch": 123}}}))
+        "source_hash": "0" * 16, "dram_bytes": 123}}}))
     monkeypatch.setattr(bench, "TRAFFIC_FILE", str(f))
     assert bench.traffic_for("simt_bias_kernel", "greedy") is None
     f.write_text(json.dumps({"simt_bias_kernel": {"greedy": {
-        "source_hash": bench.source_hash("simt_bias_kernel"), "dram_bytes_per_launch": 123}}}))
+        "source_hash": bench.source_hash("simt_bias_kernel"), "dram_bytes": 123}}}))
     assert bench.traffic_for("simt_bias_kernel", "greedy") == 123
