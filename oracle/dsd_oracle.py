@@ -22,6 +22,9 @@ section:
               survival, overlap identity), 3.2 (hardware-aware prefix scheduler)
   [WALK]   "DeepSpec 训练全流程详解（以 Qwen3 + DSpark 为例）"
            -- 4.3 Propose, 4.4 Verify (rejection test, residual, bonus token)
+           -- 3.4 (loss: CE, L1 alignment, confidence BCE, their weights)
+  ([READ] 4.1 also gives the loss forward: position-decayed CE + L1 and the
+  confidence BCE against the soft accept-rate label.)
 
 Readings where the pages are silent or disagree (each one is listed with its
 reason in the repository's design notes):
@@ -41,6 +44,10 @@ reason in the repository's design notes):
   * scheduler sort key (a desc, r asc, j asc); Theta must strictly improve;
     SPS table is 1-based (sps[B-1] = SPS(B)); B beyond the table is infeasible;
   * conf is clamped to [0, 1];
+  * loss: every position of every row is valid (no loss mask), so [WALK]
+    3.4's masked sum over all tokens divided by the total weight equals
+    [READ] 4.1's per-position batch mean weighted by normalised w_j; the
+    confidence label 1 - L1/2 is clamped to [0, 1] against rounding;
   * overlap: a_i is reported as sum(min(p,q)) unclamped; positions i >=
     valid_len have a_i = 0; a block is valid when valid_len >= 1.
 
@@ -423,6 +430,76 @@ def overlap(P_logits, Q_logits, valid_len):
     valid = vl >= 1
     mean_tau = float(np.mean(tau[valid])) if np.any(valid) else 0.0
     return dict(a=a, l1=l1, tau=tau, accept_rate=accept_rate, mean_tau=mean_tau)
+
+
+# ---------------------------------------------------------------------------
+# Teacher-forced Markov bias and the DSpark loss forward  ([READ] 2.3
+# VanillaMarkov.apply_block_logits: the bias of every block position at once
+# from known previous tokens; [READ] 4.1 位置指数衰减与分布 L1 对齐损失)
+# ---------------------------------------------------------------------------
+
+def position_weights(gamma: int, decay: float = 4.0):
+    """w_j = exp(-j / decay), normalised to sum 1 ([READ] 4.1)."""
+    w = np.exp(-np.arange(gamma, dtype=np.float64) / decay)
+    return w / np.sum(w)
+
+
+def bce_with_logits(z, y):
+    """Binary cross-entropy of the logit z against the soft label y:
+    -(y log sigma(z) + (1 - y) log(1 - sigma(z))), with
+    log sigma(z) = -log(1 + e^-z) and log(1 - sigma(z)) = -log(1 + e^z)."""
+    z = float(z)
+    y = float(y)
+    log_sig = -np.logaddexp(0.0, -z)
+    log_one_minus = -np.logaddexp(0.0, z)
+    return -(y * log_sig + (1.0 - y) * log_one_minus)
+
+
+def loss_forward(U, E, W, prev_tokens, P, target_tokens, conf_logits,
+                 bias_at_first=True, act="none", ce_alpha=0.1, l1_alpha=0.9,
+                 conf_alpha=1.0, decay=4.0):
+    """DSpark loss forward over B blocks of gamma teacher-forced positions.
+
+    For each block b and position j (prev_tokens[b, j] is the known token
+    before position j; position 0 is biased unless bias_at_first is False):
+        l[v]   = U[b, j, v] + b_j[v],  b_j = W E[prev_tokens[b, j]]
+        q      = softmax(l),  p = softmax(P[b, j])
+        l1     = sum_v |p - q|
+        a      = clamp(1 - l1 / 2, 0, 1)          (soft accept-rate label)
+        ce     = logsumexp(l) - l[target_tokens[b, j]]     (-log q(x*))
+        bce    = BCE(conf_logits[b, j], a)
+    Aggregates with w = position_weights(gamma, decay):
+        ce_loss   = sum_j w_j mean_b ce[b, j]
+        l1_loss   = sum_j w_j mean_b l1[b, j]
+        conf_loss = mean_{b, j} bce[b, j]
+        loss      = ce_alpha ce_loss + l1_alpha l1_loss + conf_alpha conf_loss"""
+    U = np.asarray(U)
+    B, G, V = U.shape
+    prev = np.asarray(prev_tokens).astype(np.int64)
+    tgt = np.asarray(target_tokens).astype(np.int64)
+    z = _f64(conf_logits)
+    l1 = np.zeros((B, G))
+    a = np.zeros((B, G))
+    ce = np.zeros((B, G))
+    bce = np.zeros((B, G))
+    for b in range(B):
+        for j in range(G):
+            l = _f64(U[b, j])
+            if j > 0 or bias_at_first:
+                l = l + markov_bias(E, W, int(prev[b, j]), act)
+            q = softmax(l)
+            p = softmax(_f64(P[b, j]))
+            l1[b, j] = np.sum(np.abs(p - q))
+            a[b, j] = min(1.0, max(0.0, 1.0 - 0.5 * l1[b, j]))
+            ce[b, j] = logsumexp(l) - l[int(tgt[b, j])]
+            bce[b, j] = bce_with_logits(z[b, j], a[b, j])
+    w = position_weights(G, decay)
+    ce_loss = float(np.sum(w * np.mean(ce, axis=0))) if B else 0.0
+    l1_loss = float(np.sum(w * np.mean(l1, axis=0))) if B else 0.0
+    conf_loss = float(np.mean(bce)) if B else 0.0
+    loss = ce_alpha * ce_loss + l1_alpha * l1_loss + conf_alpha * conf_loss
+    return dict(l1=l1, accept=a, ce=ce, bce=bce, ce_loss=ce_loss, l1_loss=l1_loss,
+                conf_loss=conf_loss, loss=loss)
 
 
 # ---------------------------------------------------------------------------

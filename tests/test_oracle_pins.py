@@ -429,3 +429,127 @@ def test_overlap_valid_len_aggregation_by_hand():
     assert out["tau"][2] == 1.0
     assert out["mean_tau"] == pytest.approx((tau0 + tau1) / 2, rel=1e-12)
     assert out["accept_rate"] == pytest.approx([0.7, 0.65, 0.6, 0.6, 0.5, 0.4, 0.3], rel=1e-12)
+
+
+# ---------------------------------------------------------------------------
+# Teacher-forced loss forward ([READ] 4.1)
+# ---------------------------------------------------------------------------
+
+def test_loss_position_weights_match_the_page():
+    g = _golden("loss_position_weights.json")
+    w = O.position_weights(g["gamma"], g["decay"])
+    assert abs(w.sum() - 1.0) < 1e-15
+    assert abs(w[6] / w[0] - g["w6_page_rounded"]) < 5e-4
+    raw = w / w[0]
+    for j, v in enumerate(g["w_first_four_page_rounded"]):
+        assert abs(raw[j] - v) < 5e-3
+
+
+def test_bce_with_logits_special_values():
+    assert abs(O.bce_with_logits(0.0, 0.5) - np.log(2.0)) < 1e-15
+    assert abs(O.bce_with_logits(0.0, 1.0) - np.log(2.0)) < 1e-15
+    # y = 1: -log sigma(z); y = 0: -log(1 - sigma(z)); symmetric in (z, y) -> (-z, 1 - y)
+    for z in (-30.0, -2.5, 0.3, 4.0, 30.0):
+        sig = 1.0 / (1.0 + np.exp(-z))
+        assert abs(O.bce_with_logits(z, 1.0) + np.log(sig)) < 1e-12 * max(1.0, abs(z))
+        assert abs(O.bce_with_logits(z, 0.25) - O.bce_with_logits(-z, 0.75)) < 1e-12
+    # minimum over y is at y = sigma(z) (the entropy of sigma(z))
+    z = 1.3
+    sig = 1.0 / (1.0 + np.exp(-z))
+    ent = -(sig * np.log(sig) + (1 - sig) * np.log(1 - sig))
+    assert abs(O.bce_with_logits(z, sig) - ent) < 1e-12
+
+
+def _loss_inputs(B=3, G=4, V=24, r=6, seed=5, scale=1.0):
+    rng = np.random.default_rng(seed)
+    U = rng.normal(0, 2.0, (B, G, V))
+    E = rng.normal(0, scale, (V, r))
+    W = rng.normal(0, scale, (V, r))
+    prev = rng.integers(0, V, (B, G))
+    P = U + rng.normal(0, 0.7, (B, G, V))
+    tgt = rng.integers(0, V, (B, G))
+    z = rng.normal(0, 1.5, (B, G))
+    return U, E, W, prev, P, tgt, z
+
+
+def test_loss_equal_distributions():
+    # P equals the draft logits up to a per-row constant: p = q, so
+    # l1 = 0, a = 1, and the confidence loss is -log sigma(z)
+    U, E, W, prev, _, tgt, z = _loss_inputs()
+    B, G, V = U.shape
+    P = np.empty_like(U)
+    for b in range(B):
+        for j in range(G):
+            P[b, j] = U[b, j] + O.markov_bias(E, W, int(prev[b, j])) + 3.0 * b - j
+    out = O.loss_forward(U, E, W, prev, P, tgt, z)
+    assert np.max(out["l1"]) < 1e-12
+    assert np.all(np.abs(out["accept"] - 1.0) < 1e-12)
+    assert abs(out["conf_loss"] - np.mean(np.logaddexp(0.0, -z))) < 1e-12
+    assert abs(out["l1_loss"]) < 1e-12
+
+
+def test_loss_uniform_draft_cross_entropy_is_log_v():
+    U, E, W, prev, P, tgt, z = _loss_inputs()
+    U0 = np.zeros_like(U)
+    E0 = np.zeros_like(E)
+    out = O.loss_forward(U0, E0, W, prev, P, tgt, z)
+    assert np.all(np.abs(out["ce"] - np.log(U.shape[2])) < 1e-12)
+
+
+def test_loss_disjoint_supports_have_zero_accept():
+    B, G, V = 2, 3, 8
+    U = np.full((B, G, V), -200.0)
+    P = np.full((B, G, V), -200.0)
+    U[..., 0] = 0.0
+    P[..., 5] = 0.0
+    E = np.zeros((V, 4))
+    W = np.zeros((V, 4))
+    out = O.loss_forward(U, E, W, np.zeros((B, G), int), P, np.zeros((B, G), int),
+                         np.zeros((B, G)))
+    assert np.all(np.abs(out["l1"] - 2.0) < 1e-12)
+    assert np.all(out["accept"] == 0.0)
+
+
+def test_loss_total_is_the_weighted_combination():
+    U, E, W, prev, P, tgt, z = _loss_inputs(seed=9)
+    base = O.loss_forward(U, E, W, prev, P, tgt, z)
+    only_ce = O.loss_forward(U, E, W, prev, P, tgt, z, ce_alpha=1.0, l1_alpha=0.0, conf_alpha=0.0)
+    only_l1 = O.loss_forward(U, E, W, prev, P, tgt, z, ce_alpha=0.0, l1_alpha=1.0, conf_alpha=0.0)
+    only_cf = O.loss_forward(U, E, W, prev, P, tgt, z, ce_alpha=0.0, l1_alpha=0.0, conf_alpha=1.0)
+    assert abs(only_ce["loss"] - base["ce_loss"]) < 1e-15
+    assert abs(only_l1["loss"] - base["l1_loss"]) < 1e-15
+    assert abs(only_cf["loss"] - base["conf_loss"]) < 1e-15
+    assert abs(base["loss"] - (0.1 * base["ce_loss"] + 0.9 * base["l1_loss"] + base["conf_loss"])) < 1e-12
+
+
+def test_loss_matches_torch_functional_on_cpu():
+    # An independent implementation of the same definitions with PyTorch's CPU
+    # softmax / cross_entropy / binary_cross_entropy_with_logits in float64.
+    torch = pytest.importorskip("torch")
+    F = torch.nn.functional
+    U, E, W, prev, P, tgt, z = _loss_inputs(B=4, G=5, V=40, r=8, seed=13, scale=0.6)
+    for baf in (True, False):
+        out = O.loss_forward(U, E, W, prev, P, tgt, z, bias_at_first=baf)
+        Ut = torch.tensor(U, dtype=torch.float64)
+        emb = torch.tensor(E, dtype=torch.float64)[torch.tensor(prev)]           # [B, G, r]
+        bias = emb @ torch.tensor(W, dtype=torch.float64).T                      # [B, G, V]
+        if not baf:
+            bias[:, 0] = 0.0
+        dl = Ut + bias
+        p = F.softmax(torch.tensor(P, dtype=torch.float64), dim=-1)
+        q = F.softmax(dl, dim=-1)
+        l1 = (p - q).abs().sum(-1)
+        acc = (1.0 - 0.5 * l1).clamp(0.0, 1.0)
+        ce = F.cross_entropy(dl.transpose(1, 2), torch.tensor(tgt), reduction="none")
+        G = U.shape[1]
+        w = torch.exp(-torch.arange(G, dtype=torch.float64) / 4.0)
+        w = w / w.sum()
+        wce = (ce.mean(0) * w).sum()
+        wl1 = (l1.mean(0) * w).sum()
+        cl = F.binary_cross_entropy_with_logits(torch.tensor(z, dtype=torch.float64), acc)
+        assert np.max(np.abs(out["l1"] - l1.numpy())) < 1e-12
+        assert np.max(np.abs(out["ce"] - ce.numpy())) < 1e-10
+        assert abs(out["ce_loss"] - float(wce)) < 1e-10
+        assert abs(out["l1_loss"] - float(wl1)) < 1e-12
+        assert abs(out["conf_loss"] - float(cl)) < 1e-12
+        assert abs(out["loss"] - float(0.1 * wce + 0.9 * wl1 + cl)) < 1e-10
