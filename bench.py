@@ -35,10 +35,11 @@ PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 KERNEL_SOURCES = {
     "simt_bias_kernel": ["propose_simt.cu", "dsd_common.cuh"],
-    "propose_tc_kernel": ["propose_tc.cu", "dsd_common.cuh"],
+    "propose_tc_kernel": ["propose_tc.cu", "tc_common.cuh", "tc_ptx.cuh", "dsd_common.cuh"],
     "propose_mma_kernel": ["propose_mma.cu", "dsd_common.cuh"],
     "verify_rows": ["verify.cu", "dsd_common.cuh"],
     "overlap_rows": ["overlap.cu", "dsd_common.cuh"],
+    "loss_tc_kernel": ["loss_tc.cu", "tc_common.cuh", "tc_ptx.cuh", "dsd_common.cuh"],
 }
 FALLBACK_HBM_GBS = 6800.0
 
@@ -363,6 +364,73 @@ def run_overlap(args, dsd, synth, dev, world):
     return line
 
 
+def run_loss(args, dsd, synth, dev, world):
+    """The teacher-forced DSpark loss forward on one training sample's anchors
+    (512 blocks x gamma positions, full vocabulary); inputs (2.2 GB) exceed L2.
+    One call is two launches of loss_tc_kernel (normalisers, then L1) and a
+    one-CTA fp64 finalize."""
+    import torch
+
+    spec = synth.LossSpec()
+    x = synth.loss_inputs(spec, device=dev)
+    ctx = dsd.Context(spec.V, spec.r, spec.G, spec.B, dtype="bf16", device=dev.index)
+    stream = torch.cuda.Stream(device=dev)
+    args_ = (x["U"], x["E"], x["W"], x["prev_tok"], x["P"], x["target"], x["conf_logit"])
+    out = None
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            out = ctx.loss_forward(*args_, out=out, stream=stream)
+    stream.synchronize()
+    assert ctx.sync_status(stream) == 0
+    c0 = ctx.launch_count()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+    clocks = ClockSampler(gpu_uuid(dev.index))
+    clocks.start()
+    time.sleep(0.3)
+    barrier(world)
+    with torch.cuda.stream(stream):
+        for e in evs:
+            e[0].record(stream)
+            out = ctx.loss_forward(*args_, out=out, stream=stream)
+            e[1].record(stream)
+    stream.synchronize()
+    clk = clocks.stop()
+    assert ctx.sync_status(stream) == 0
+    launches = ctx.launch_count() - c0
+    ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
+    ms = max_over_ranks(ms, world, dev)
+    rows = spec.B * spec.G
+    # per launch of loss_tc_kernel: U and P rows once, W once, the E rows, the
+    # per-row inputs and the partials it writes
+    per_pass = (2 * rows * spec.V * 2 + spec.V * spec.r * 2 + rows * spec.r * 2
+                + rows * 12 + rows * 16 * 5)
+    peak, peak_kind = hbm_peak()
+    # the two passes take all but the finalize's few microseconds of the call
+    achieved = 2 * per_pass / (ms / 1e3) / 1e9
+    line = {
+        "metric": "teacher-forced DSpark loss rows/s (CE + L1 + confidence BCE, Markov bias "
+                  "on tcgen05) at B=512 blocks, gamma=7, V=151936, rank 256",
+        "value": world * rows / (ms / 1e3), "unit": "rows/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "accumulate": "fp32 (fp64 finalize)", "data": "synthetic",
+        "config": {"workload": f"loss: B={spec.B} gamma={spec.G} V={spec.V} rank={spec.r} bf16",
+                   "rows": rows, "l2": "inputs 2.2 GB, larger than L2"},
+        "roofline": {"bound": "hbm", "kernel": "loss_tc_kernel", "achieved": achieved,
+                     "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)",
+                     "traffic": traffic_for("loss_tc_kernel", "loss"),
+                     "alg_bytes": per_pass, "per": "one launch (one pass over U, P and W)",
+                     "alg_bytes_note": "U and P rows + W + E rows + per-row inputs and "
+                                       "partials; two launches per call, timed together",
+                     "single_read_frac": achieved / 2 / peak},
+        "cpu_baseline": None, "e2e": None,
+        "gpu_launches": launches, "clocks": clk,
+    }
+    ctx.close()
+    return line
+
+
 def run_ours(args):
     import numpy as np
     import torch
@@ -381,8 +449,9 @@ def run_ours(args):
 
     if not os.path.exists(dsd.LIB_PATH):
         _build.build()
-    if args.workload == "overlap":
-        line = run_overlap(args, dsd, synth, dev, world)
+    if args.workload in ("overlap", "loss"):
+        run = run_overlap if args.workload == "overlap" else run_loss
+        line = run(args, dsd, synth, dev, world)
         if rank == 0:
             print(json.dumps(line), flush=True)
         return 0
@@ -586,7 +655,7 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="highconc",
-                    choices=["highconc", "greedy", "sampled", "tiny", "overlap"])
+                    choices=["highconc", "greedy", "sampled", "tiny", "overlap", "loss"])
     ap.add_argument("--engine", default="auto", choices=["auto", "simt", "mma", "tcgen05"])
     ap.add_argument("--cpu-requests", type=int, default=128,
                     help="requests in the CPU-baseline sample")
@@ -597,7 +666,7 @@ def main(argv=None):
     args = ap.parse_args(argv)
     args.warmup = max(args.warmup, 3)   # at least 3 untimed warm-up steps
     if args.impl == "reference":
-        if args.workload == "overlap":
+        if args.workload in ("overlap", "loss"):
             ap.error("the reference arm times the draft-verify cycle workloads")
         return run_reference(args)
     return run_ours(args)

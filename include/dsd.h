@@ -11,8 +11,10 @@
  *           2.3 串行头的两种形态
  *   [READ]  "DSpark 论文精读：置信度调度推测解码、半自回归生成与大模型推理加速":
  *           2.2, 2.3, 3.1, 3.2
- *   [WALK]  "DeepSpec 训练全流程详解（以 Qwen3 + DSpark 为例）": 4.3 Propose,
- *           4.4 Verify
+ *   [WALK]  "DeepSpec 训练全流程详解（以 Qwen3 + DSpark 为例）": 3.4 Loss,
+ *           4.3 Propose, 4.4 Verify
+ * dsd_loss_forward is the training-side twin: the teacher-forced DSpark loss
+ * ([READ] 4.1; [WALK] 3.4).
  *
  * Conventions for every call below.
  *   - Tensor arguments are DEVICE pointers owned by the caller, row-major and
@@ -254,6 +256,50 @@ int dsd_cycle_host(dsd_ctx* ctx, int R, const void* U_host, const void* E, const
 int dsd_overlap(dsd_ctx* ctx, int N, const void* P_logits, const void* Q_logits,
                 const int32_t* valid_len, float* a, float* l1, float* tau,
                 float* accept_rate, float* mean_tau, void* stream);
+
+/*
+ * dsd_loss_forward -- teacher-forced DSpark training loss, forward only
+ * ([READ] 4.1 position-decayed L1 alignment; [WALK] 3.4 compute_dspark_loss;
+ * [TRAIN] Markov 顺序修正 for the biased logits).
+ *
+ * Row n = b * gamma + j (block b < B, position j < gamma) has the known
+ * previous token prev_tok[n] (the anchor at j = 0, the ground-truth token
+ * j - 1 after it), so
+ *   l      = U[b, j, :] + W E[prev_tok[n], :]     (bias skipped at j = 0 when
+ *                                                  bias_at_first == 0)
+ *   q = softmax(l),  p = softmax(P[b, j, :])
+ *   l1[n]  = sum_v |p_v - q_v|,   accept[n] = clamp(1 - l1[n] / 2, 0, 1)
+ *   ce[n]  = logsumexp(l) - l[target[n]]
+ *   bce[n] = -(a log sigmoid(z) + (1 - a) log(1 - sigmoid(z))),
+ *            z = conf_logit[n], a = accept[n]
+ *   w_j    = exp(-j / decay) / sum_{i < gamma} exp(-i / decay)
+ *   losses = { ce_loss   = sum_j w_j * mean_b ce,
+ *              l1_loss   = sum_j w_j * mean_b l1,
+ *              conf_loss = mean_n bce,
+ *              total     = ce_alpha ce_loss + l1_alpha l1_loss + conf_alpha conf_loss }
+ * The pages' defaults are decay 4, ce_alpha 0.1, l1_alpha 0.9, conf_alpha 1.
+ * The biased logits never reach HBM: the bias GEMM runs on the tcgen05
+ * tensor cores fused with both softmaxes, in two passes over the vocabulary
+ * (normalisers, then L1); the per-row values and losses are reduced in fp64.
+ *
+ * U, P       [B, gamma, V]  bf16   draft base logits, target logits
+ * E, W       [V, rank]      bf16   Markov tables (as dsd_propose)
+ * prev_tok   [B, gamma]     i32    previous token of every row
+ * target     [B, gamma]     i32    ground-truth token of every row
+ * conf_logit [B, gamma]     f32    confidence-head logits
+ * row_out    [4, B*gamma]   f32 out or NULL: l1, accept, ce, bce per row
+ * losses     [4]            f32 out: ce_loss, l1_loss, conf_loss, total
+ * Needs the tensor-core engine's configuration (bf16 tables, no activation,
+ * rank a multiple of 64 up to 256), else DSD_ERR_UNSUPPORTED before any
+ * launch; B <= R_max.  B == 0 writes zeros to losses.  prev_tok or target
+ * outside [0, V) is DSD_ERR_ARG on the device side (recorded; the row's bias
+ * is zero and its ce NaN), non-finite results DSD_ERR_NONFINITE -- see
+ * dsd_sync_status.
+ */
+int dsd_loss_forward(dsd_ctx* ctx, int B, const void* U, const void* E, const void* W,
+                     const int32_t* prev_tok, const void* P, const int32_t* target,
+                     const float* conf_logit, float ce_alpha, float l1_alpha, float conf_alpha,
+                     float decay, float* row_out, float* losses, void* stream);
 
 /*
  * dsd_propose_noalloc -- dsd_propose for callers that cannot allocate device

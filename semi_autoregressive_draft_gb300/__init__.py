@@ -35,7 +35,7 @@ EXPORTED = [
     "dsd_create", "dsd_destroy", "dsd_last_error", "dsd_sync_status", "dsd_workspace_bytes",
     "dsd_launch_count", "dsd_last_engine",
     "dsd_propose", "dsd_schedule", "dsd_verify", "dsd_cycle", "dsd_cycle_host", "dsd_overlap",
-    "dsd_propose_noalloc",
+    "dsd_propose_noalloc", "dsd_loss_forward",
 ]
 
 
@@ -85,6 +85,8 @@ def load_library(path: str | None = None):
         "dsd_cycle_host": (_I, [_P, _I, _P, _P, _P, _P, _P, _P, _P, _P, _I, _F, _U64,
                                 _P, _P, _P, _P, _P]),
         "dsd_overlap": (_I, [_P, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
+        "dsd_loss_forward": (_I, [_P, _I, _P, _P, _P, _P, _P, _P, _P, _F, _F, _F, _F, _P, _P,
+                                  _P]),
         "dsd_propose_noalloc": (_I, [_I, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _F,
                                      _U64, _P, _P, _P, _P, _P]),
     }
@@ -190,6 +192,14 @@ def dsd_overlap(ctx, N, P_logits, Q_logits, valid_len, a, l1, tau, accept_rate, 
     _check(ctx, load_library().dsd_overlap(
         ctx, N, _ptr(P_logits), _ptr(Q_logits), _ptr(valid_len), _ptr(a), _ptr(l1), _ptr(tau),
         _ptr(accept_rate), _ptr(mean_tau), _stream(stream, device)))
+
+
+def dsd_loss_forward(ctx, B, U, E, W, prev_tok, P, target, conf_logit, ce_alpha, l1_alpha,
+                     conf_alpha, decay, row_out, losses, stream=None, device=0):
+    _check(ctx, load_library().dsd_loss_forward(
+        ctx, B, _ptr(U), _ptr(E), _ptr(W), _ptr(prev_tok), _ptr(P), _ptr(target),
+        _ptr(conf_logit), ce_alpha, l1_alpha, conf_alpha, decay, _ptr(row_out), _ptr(losses),
+        _stream(stream, device)))
 
 
 def dsd_propose_noalloc(V, rank, gamma, dtype, act, bias_at_first, R, U, E, W, conf, prev_tok,
@@ -353,4 +363,22 @@ class Context:
                         mean_tau=self._empty((1,), torch.float32))
         dsd_overlap(self.handle, N, P_logits, Q_logits, valid_len, o["a"], o["l1"], o["tau"],
                     o["accept_rate"], o["mean_tau"], stream, self.device)
+        return o
+
+    def loss_forward(self, U, E, W, prev_tok, P, target, conf_logit, ce_alpha=0.1, l1_alpha=0.9,
+                     conf_alpha=1.0, decay=4.0, rows=True, out=None, stream=None):
+        """Teacher-forced DSpark loss forward.  Returns dict(losses=[4] f32:
+        ce_loss, l1_loss, conf_loss, total) and, with rows=True, row=[4, B*gamma]
+        f32: l1, accept, ce, bce per row n = b * gamma + j."""
+        B = U.shape[0]
+        for n, t in (("U", U), ("E", E), ("W", W), ("P", P)):
+            self._check_in(n, t, self.torch_dtype)
+        self._check_in("prev_tok", prev_tok, torch.int32)
+        self._check_in("target", target, torch.int32)
+        self._check_in("conf_logit", conf_logit, torch.float32)
+        o = out or dict(losses=self._empty((4,), torch.float32),
+                        row=self._empty((4, B * self.gamma), torch.float32) if rows else None)
+        dsd_loss_forward(self.handle, B, U, E, W, prev_tok, P, target, conf_logit, ce_alpha,
+                         l1_alpha, conf_alpha, decay, o.get("row"), o["losses"], stream,
+                         self.device)
         return o

@@ -29,6 +29,7 @@ SOURCES = [
     "schedule.cu",
     "verify.cu",
     "overlap.cu",
+    "loss_tc.cu",
 ]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",

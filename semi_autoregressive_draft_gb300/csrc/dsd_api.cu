@@ -59,6 +59,10 @@ size_t carve(dsd_ctx* c, unsigned char* base) {
   w.ov_parts = reinterpret_cast<float*>(take(sizeof(float) * 64));
   w.sched_order = reinterpret_cast<int*>(take(sizeof(int) * (size_t)Rm * G));
   w.tickets = reinterpret_cast<unsigned int*>(take(sizeof(unsigned int) * 64));
+  const size_t loss_rows = (size_t)Rm * G;
+  w.loss_parts1 = reinterpret_cast<float4*>(take(sizeof(float4) * c->num_sms * loss_rows));
+  w.loss_parts2 = reinterpret_cast<float*>(take(sizeof(float) * c->num_sms * loss_rows));
+  w.loss_ltgt = reinterpret_cast<float*>(take(sizeof(float) * loss_rows));
   if (base) c->ws = w;
   return off;
 }
@@ -437,6 +441,58 @@ int dsd_overlap(dsd_ctx* ctx, int N, const void* P_logits, const void* Q_logits,
   o.mean_tau = mean_tau;
   cudaError_t e = launch_overlap(*ctx, o, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(ctx, e, "overlap launch");
+  return DSD_OK;
+}
+
+int dsd_loss_forward(dsd_ctx* ctx, int B, const void* U, const void* E, const void* W,
+                     const int32_t* prev_tok, const void* P, const int32_t* target,
+                     const float* conf_logit, float ce_alpha, float l1_alpha, float conf_alpha,
+                     float decay, float* row_out, float* losses, void* stream) {
+  int rc = check_ctx(ctx);
+  if (rc) return rc;
+  if ((rc = check_R(ctx, B))) return rc;
+  if (!losses) return fail(ctx, DSD_ERR_ARG, "dsd_loss_forward: losses is NULL");
+  const float fs[3] = {ce_alpha, l1_alpha, conf_alpha};
+  for (float f : fs)
+    if (!(f == f) || f > 3.0e38f || f < -3.0e38f)
+      return fail(ctx, DSD_ERR_ARG, "dsd_loss_forward: loss weights must be finite");
+  if (!(decay > 0.f) || decay > 3.0e38f)
+    return fail(ctx, DSD_ERR_ARG, "dsd_loss_forward: decay must be finite and > 0");
+  char why[256];
+  if (!dsd::tc_supported(*ctx, why, sizeof(why)))
+    return fail(ctx, DSD_ERR_UNSUPPORTED, "dsd_loss_forward: %s", why);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (B == 0) {
+    cudaError_t e = cudaMemsetAsync(losses, 0, 4 * sizeof(float), s);
+    if (e != cudaSuccess) return cuda_fail(ctx, e, "loss memset");
+    return DSD_OK;
+  }
+  if ((rc = check_table(ctx, U, "U")) || (rc = check_table(ctx, E, "E")) ||
+      (rc = check_table(ctx, W, "W")) || (rc = check_table(ctx, P, "P")))
+    return rc;
+  if (!prev_tok || !target || !conf_logit)
+    return fail(ctx, DSD_ERR_ARG, "dsd_loss_forward: NULL argument");
+  LossArgs a{};
+  a.B = B;
+  a.V = ctx->cfg.V;
+  a.rank = ctx->cfg.rank;
+  a.gamma = ctx->cfg.gamma;
+  a.bias_at_first = ctx->cfg.bias_at_first;
+  a.U = U;
+  a.E = E;
+  a.W = W;
+  a.P = P;
+  a.prev_tok = prev_tok;
+  a.target = target;
+  a.conf_logit = conf_logit;
+  a.ce_alpha = ce_alpha;
+  a.l1_alpha = l1_alpha;
+  a.conf_alpha = conf_alpha;
+  a.decay = decay;
+  a.row_out = row_out;
+  a.losses = losses;
+  cudaError_t e = launch_loss(*ctx, a, s);
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "loss launch");
   return DSD_OK;
 }
 

@@ -45,6 +45,9 @@ struct Workspace {
   float* ov_parts;              // scratch of the overlap kernels
   int* sched_order;             // [R_max*gamma] slot indices in schedule (sorted) order
   unsigned int* tickets;        // [64] last-CTA tickets; each user resets its own to zero
+  float4* loss_parts1;          // [num_sms][R_max*gamma] log-sum-exp partials of the loss
+  float* loss_parts2;           // [num_sms][R_max*gamma] L1 partials of the loss
+  float* loss_ltgt;             // [R_max*gamma] draft logit at the target token
 };
 
 struct Config {
@@ -127,6 +130,22 @@ struct OverlapArgs {
 };
 
 cudaError_t launch_overlap(const Ctx& ctx, const OverlapArgs& a, cudaStream_t s);
+
+struct LossArgs {
+  int B, V, rank, gamma, bias_at_first;
+  const void* U;
+  const void* E;
+  const void* W;
+  const void* P;
+  const int32_t* prev_tok;
+  const int32_t* target;
+  const float* conf_logit;
+  double ce_alpha, l1_alpha, conf_alpha, decay;
+  float* row_out;
+  float* losses;
+};
+
+cudaError_t launch_loss(const Ctx& ctx, const LossArgs& a, cudaStream_t s);
 
 // Swizzle mask for 16-byte chunks of a staged table row (see propose_simt.cu).
 inline int chunk_swizzle_mask(int chunks_per_row) {

@@ -46,12 +46,9 @@
 // synchronisation between steps.  Every mbarrier wait is bounded: on time-out
 // the kernel records DSD_ERR_TIMEOUT, stops issuing work, waits (bounded) for
 // its own copies in flight, frees its TMEM and returns.
-#include <cuda.h>
-#include <cudaTypedefs.h>
 #include <stdio.h>
 
-#include "dsd_common.cuh"
-#include "tc_ptx.cuh"
+#include "tc_common.cuh"
 
 namespace dsd {
 
@@ -90,8 +87,6 @@ static_assert(kTmemCols == 512, "TMEM allocation is a power of two <= 512 column
 #define TC_CHECK(cond, site) true
 #endif
 
-constexpr uint32_t kSpinLimit = 1u << 22;        // mbarrier polls before giving up
-
 struct TcParams {
   const __nv_bfloat16* E;
   const int32_t* prev_tok;
@@ -116,40 +111,6 @@ struct Bars {
   uint64_t* aready;
   uint64_t* mmadone;
 };
-
-__device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                         int* status) {
-  for (uint32_t i = 0; i < kSpinLimit; ++i) {
-    if (tc::mbar_try_wait(bar, parity)) return true;
-    if ((i & 255u) == 255u && *abort_flag) return false;
-  }
-  set_status(status, kErrTimeout);
-  *abort_flag = 1;
-  return false;
-}
-
-// Bounded wait that ignores the abort flag: used to drain copies in flight
-// before the CTA exits.
-__device__ __forceinline__ void drain_bar(uint64_t* bar, uint32_t parity) {
-  for (uint32_t i = 0; i < (1u << 20); ++i)
-    if (tc::mbar_try_wait(bar, parity)) return;
-}
-
-// Warp-uniform bounded wait: lane 0 polls, the verdict is broadcast, so the
-// warp stays converged for the .sync.aligned tcgen05 instructions after it.
-__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                          int* status) {
-  int ok = 0;
-  if ((threadIdx.x & 31) == 0) ok = wait_bar(bar, parity, abort_flag, status) ? 1 : 0;
-  ok = __shfl_sync(0xffffffffu, ok, 0);
-  __syncwarp();
-  return ok != 0;
-}
-__device__ __forceinline__ bool warp_aborted(volatile int* abort_flag) {
-  int a = 0;
-  if ((threadIdx.x & 31) == 0) a = *abort_flag;
-  return __shfl_sync(0xffffffffu, a, 0) != 0;
-}
 
 struct RowState {
   float m2, s, best_z;
@@ -578,7 +539,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   }
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+}  // namespace
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   static bool tried = false;
   if (!tried) {
@@ -593,8 +556,6 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-}  // namespace
-
 int tc_supported(const Ctx& ctx, char* why, size_t why_len) {
   if (ctx.cfg.dtype != 1) {
     snprintf(why, why_len, "tcgen05 engine needs bf16 tables");
@@ -608,7 +569,7 @@ int tc_supported(const Ctx& ctx, char* why, size_t why_len) {
     snprintf(why, why_len, "tcgen05 engine runs without an activation (bf16 operands)");
     return 0;
   }
-  if (!encode_fn()) {
+  if (!tensor_map_encoder()) {
     snprintf(why, why_len, "cuTensorMapEncodeTiled is not available from the driver");
     return 0;
   }
@@ -633,7 +594,7 @@ int tc_vranges(const Ctx& ctx, int R) {
 }
 
 cudaError_t launch_propose_tc(const Ctx& ctx, const ProposeArgs& a, cudaStream_t s) {
-  PFN_cuTensorMapEncodeTiled_v12000 encode = encode_fn();
+  PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
   if (!encode) return cudaErrorNotSupported;
   CUtensorMap tmW, tmU;
   {

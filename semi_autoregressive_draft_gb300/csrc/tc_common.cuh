@@ -1,0 +1,57 @@
+// Pieces shared by the tcgen05 kernels (propose_tc.cu, loss_tc.cu): bounded
+// mbarrier waits and the driver's tensor-map encoder.
+//
+// Every mbarrier wait is bounded: after kSpinLimit polls the waiter records
+// DSD_ERR_TIMEOUT, raises the CTA's abort flag (the other roles see it and
+// stop issuing work) and returns false.  Nothing traps.
+#pragma once
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "dsd_common.cuh"
+#include "tc_ptx.cuh"
+
+namespace dsd {
+
+constexpr uint32_t kSpinLimit = 1u << 22;        // mbarrier polls before giving up
+
+__device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                         int* status) {
+  for (uint32_t i = 0; i < kSpinLimit; ++i) {
+    if (tc::mbar_try_wait(bar, parity)) return true;
+    if ((i & 255u) == 255u && *abort_flag) return false;
+  }
+  set_status(status, kErrTimeout);
+  *abort_flag = 1;
+  return false;
+}
+
+// Bounded wait that ignores the abort flag: used to drain copies in flight
+// before the CTA exits.
+__device__ __forceinline__ void drain_bar(uint64_t* bar, uint32_t parity) {
+  for (uint32_t i = 0; i < (1u << 20); ++i)
+    if (tc::mbar_try_wait(bar, parity)) return;
+}
+
+// Warp-uniform bounded wait: lane 0 polls, the verdict is broadcast, so the
+// warp stays converged for the .sync.aligned tcgen05 instructions after it.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                          int* status) {
+  int ok = 0;
+  if ((threadIdx.x & 31) == 0) ok = wait_bar(bar, parity, abort_flag, status) ? 1 : 0;
+  ok = __shfl_sync(0xffffffffu, ok, 0);
+  __syncwarp();
+  return ok != 0;
+}
+__device__ __forceinline__ bool warp_aborted(volatile int* abort_flag) {
+  int a = 0;
+  if ((threadIdx.x & 31) == 0) a = *abort_flag;
+  return __shfl_sync(0xffffffffu, a, 0) != 0;
+}
+
+// cuTensorMapEncodeTiled from the driver (nullptr if unavailable); defined in
+// propose_tc.cu.
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
+
+}  // namespace dsd

@@ -1,7 +1,8 @@
 // Thin inline-PTX wrappers for sm_100-family features used by the tensor-core
-// propose engine: mbarriers, TMA tensor loads, tcgen05 (TMEM allocation,
-// UMMA issue/commit, TMEM loads) and the UMMA shared-memory / instruction
-// descriptors.  Written from the PTX ISA's description of these instructions.
+// kernels: mbarriers, TMA tensor loads, tcgen05 (TMEM allocation, UMMA
+// issue/commit with A from shared or tensor memory, TMEM loads and stores)
+// and the UMMA shared-memory / instruction descriptors.  Written from the PTX
+// ISA's description of these instructions.
 #pragma once
 
 #include <stdint.h>
@@ -109,6 +110,18 @@ __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a_desc, uint
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+// Same with the A operand in tensor memory: A[M x K] sits in TMEM lanes 0..M-1,
+// two bf16 of consecutive K per 32-bit column starting at a_tmem.
+__device__ __forceinline__ void umma_bf16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                             uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // Arrive on an mbarrier once all previously issued tcgen05.mma of this thread
 // have completed (their shared-memory operands may then be overwritten).
 __device__ __forceinline__ void umma_commit(uint64_t* bar) {
@@ -158,6 +171,26 @@ __device__ __forceinline__ void tmem_ld_32x32b_x32_wait(uint32_t taddr, uint32_t
         "=r"(r[31])
       : "r"(taddr)
       : "memory");
+}
+
+// 32 lanes x 32 consecutive 32-bit columns: thread i of the warp writes lane
+// (base lane + i), columns col .. col+31.  The registers are read when the
+// store is issued; tcgen05.wait::st orders its completion before later
+// tcgen05 operations of other threads (with the fences around a barrier).
+__device__ __forceinline__ void tmem_st_32x32b_x32(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+      "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]),
+      "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),
+      "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
 // ------------------------------------------------- async copy global->shared

@@ -21,6 +21,14 @@ the five workloads of the benchmark suite:
            peaks; P = Q + N(0, sigma^2), sigma ~ U[0.2, 2] per block; 15% of
            blocks have 1..6 trailing invalid positions.
 
+  loss     B=512 blocks x 7 positions (one training sample's 512 anchors,
+           "DeepSpec 训练全流程详解" 3.3 Step 1), V=151936, r=256, bf16;
+           U ~ N(0,3^2) + 8 on a Zipf(1.1) token; target = that token, or a
+           uniform token with probability 0.2; prev_tok = the block's anchor
+           token (uniform) at j = 0 and target[j-1] after it (teacher
+           forcing); P = U + N(0, sigma^2), sigma ~ U[0.2, 2] per block;
+           E, W ~ N(0,0.02^2); conf_logit ~ N(0, 1.5^2).
+
 P has gamma+1 rows per request: row gamma (the bonus row) is a fresh draw with
 U's recipe plus the same noise.  Big tensors are drawn with a seeded
 torch.Generator on the requested device; small ones (tokens, confidences,
@@ -83,6 +91,23 @@ class OverlapSpec:
     sigma_hi: float = 2.0
     ragged_frac: float = 0.15
     seed: int = 4
+
+
+@dataclass
+class LossSpec:
+    name: str = "loss"
+    B: int = 512
+    G: int = BLOCK
+    V: int = QWEN3_VOCAB
+    r: int = MARKOV_RANK
+    u_std: float = 3.0
+    boost: float = 8.0
+    ew_std: float = 0.02
+    sigma_lo: float = 0.2
+    sigma_hi: float = 2.0
+    target_noise: float = 0.2
+    conf_std: float = 1.5
+    seed: int = 5
 
 
 def scaled(spec: CycleSpec, **kw) -> CycleSpec:
@@ -212,6 +237,44 @@ def overlap_inputs(spec: OverlapSpec, device="cpu", chunk_blocks: int = 256):
     return dict(P=P, Q=Q, valid_len=vl)
 
 
+def loss_inputs(spec: LossSpec, device="cpu", chunk_blocks: int = 128):
+    """U, P [B,G,V] bf16; E, W [V,r] bf16; prev_tok, target [B,G] i32;
+    conf_logit [B,G] f32.  Drawn chunk by chunk so the fp32 temporaries stay
+    small."""
+    B, G, V, r = spec.B, spec.G, spec.V, spec.r
+    rng = np.random.default_rng(spec.seed)
+    gen = torch.Generator(device=device)
+    gen.manual_seed(spec.seed)
+    perm = rng.permutation(V)
+    sigma = rng.uniform(spec.sigma_lo, spec.sigma_hi, size=B).astype(np.float32)
+    peak = _boost_tokens(rng, B * G, V, "zipf", perm).reshape(B, G)
+    noisy = rng.random((B, G)) < spec.target_noise
+    target = np.where(noisy, rng.integers(0, V, size=(B, G)), peak).astype(np.int32)
+    prev_tok = np.empty((B, G), dtype=np.int32)
+    prev_tok[:, 0] = rng.integers(0, V, size=B)
+    prev_tok[:, 1:] = target[:, :-1]
+    conf_logit = (rng.standard_normal((B, G)) * spec.conf_std).astype(np.float32)
+    U = torch.empty((B, G, V), dtype=torch.bfloat16, device=device)
+    P = torch.empty((B, G, V), dtype=torch.bfloat16, device=device)
+    peak_t = torch.as_tensor(peak.reshape(-1), device=device)
+    for b0 in range(0, B, chunk_blocks):
+        b1 = min(B, b0 + chunk_blocks)
+        n = (b1 - b0) * G
+        u = torch.randn((n, V), generator=gen, device=device, dtype=torch.float32) * spec.u_std
+        u[torch.arange(n, device=device), peak_t[b0 * G:b1 * G]] += spec.boost
+        u = u.view(b1 - b0, G, V).to(torch.bfloat16)
+        s = torch.as_tensor(sigma[b0:b1], device=device).view(-1, 1, 1)
+        p = u.float() + torch.randn((b1 - b0, G, V), generator=gen, device=device) * s
+        U[b0:b1] = u
+        P[b0:b1] = p.to(torch.bfloat16)
+    E = (torch.randn((V, r), generator=gen, device=device) * spec.ew_std).to(torch.bfloat16)
+    W = (torch.randn((V, r), generator=gen, device=device) * spec.ew_std).to(torch.bfloat16)
+    return dict(U=U, P=P, E=E, W=W,
+                prev_tok=torch.as_tensor(prev_tok, device=device),
+                target=torch.as_tensor(target, device=device),
+                conf_logit=torch.as_tensor(conf_logit, device=device))
+
+
 def to_numpy(t: torch.Tensor) -> np.ndarray:
     """Exact widening to a host numpy array (bf16 -> fp32 is exact)."""
     if t.dtype == torch.bfloat16:
@@ -228,7 +291,7 @@ def fmt_spec(spec) -> str:
 
 
 __all__ = [
-    "CycleSpec", "OverlapSpec", "CYCLE_SPECS", "scaled", "cycle_inputs",
-    "overlap_inputs", "overlap_valid_len", "sps_table", "to_numpy", "bytes_of",
+    "CycleSpec", "OverlapSpec", "LossSpec", "CYCLE_SPECS", "scaled", "cycle_inputs",
+    "overlap_inputs", "loss_inputs", "overlap_valid_len", "sps_table", "to_numpy", "bytes_of",
     "QWEN3_VOCAB", "BLOCK", "MARKOV_RANK",
 ]
