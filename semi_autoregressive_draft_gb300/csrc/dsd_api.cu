@@ -63,6 +63,7 @@ size_t carve(dsd_ctx* c, unsigned char* base) {
   w.loss_parts1 = reinterpret_cast<float4*>(take(sizeof(float4) * c->num_sms * loss_rows));
   w.loss_parts2 = reinterpret_cast<float*>(take(sizeof(float) * c->num_sms * loss_rows));
   w.loss_ltgt = reinterpret_cast<float*>(take(sizeof(float) * loss_rows));
+  w.loss_red = reinterpret_cast<double*>(take(sizeof(double) * 64 * 3));
   if (base) c->ws = w;
   return off;
 }

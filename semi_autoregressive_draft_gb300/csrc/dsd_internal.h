@@ -48,6 +48,7 @@ struct Workspace {
   float4* loss_parts1;          // [num_sms][R_max*gamma] log-sum-exp partials of the loss
   float* loss_parts2;           // [num_sms][R_max*gamma] L1 partials of the loss
   float* loss_ltgt;             // [R_max*gamma] draft logit at the target token
+  double* loss_red;             // [64][3] per-CTA sums of the loss finalize
 };
 
 struct Config {

@@ -22,8 +22,8 @@
 //           range holds it);
 //   pass 2: each row merges its partials into log2-normalisers, then the
 //           partial sums of |2^(P log2e - lp) - 2^(l log2e - lq)| per range;
-//   finalize (loss_finalize_kernel, one CTA): per-row L1, accept, CE and
-//           BCE in fp64, and the weighted batch losses.
+//   finalize (loss_finalize_kernel): per-row L1, accept, CE and BCE, and the
+//           position-weighted batch losses summed in fp64.
 // Pass 2 is launched with a programmatic dependency on pass 1: its grid
 // initialises, allocates TMEM, gathers A and starts streaming while pass 1
 // drains, and waits for pass 1's partials only before its first tile.  It
@@ -48,6 +48,7 @@
 //
 // Every mbarrier has exactly one consumer role that waits on each of its
 // phases in order, and every wait is bounded (tc_common.cuh).
+#include <math.h>
 #include <stdio.h>
 
 #include "tc_common.cuh"
@@ -447,18 +448,21 @@ __global__ void __launch_bounds__(kLThreads, 1)
         ++uit;
         const unsigned char* ubox = ring + s * kSlot;
         const unsigned char* pbox = ubox + kBox;
+        // Both chunks go to registers first and the slot is released before
+        // any arithmetic, so the producer can refill it while this tile is
+        // computed: with two slots per half nearly the whole ring is in flight.
+        uint4 uu[8], pp[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          uu[i] = box_chunk(ubox, row, i);
+          pp[i] = box_chunk(pbox, row, i);
+        }
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(&empty[s]);
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
-          uint4 u[4], pw[4];
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            u[i] = box_chunk(ubox, row, 4 * c + i);
-            pw[i] = box_chunk(pbox, row, 4 * c + i);
-          }
-          if (c == 1) {   // both chunks are in registers: release the slot
-            __syncwarp();
-            if (lane == 0) tc::mbar_arrive(&empty[s]);
-          }
+          const uint4* u = uu + 4 * c;
+          const uint4* pw = pp + 4 * c;
           const int v0 = vx + c * 32;
           if (warp_rows && v0 < p.V) {
             uint32_t acc[32];
@@ -534,7 +538,8 @@ __global__ void __launch_bounds__(kLThreads, 1)
   }
 }
 
-constexpr int kFinThreads = 1024;
+constexpr int kFinThreads = 256;
+constexpr int kFinWarps = kFinThreads / 32;
 
 struct FinParams {
   const float4* parts1;
@@ -544,23 +549,31 @@ struct FinParams {
   const float* conf_logit;
   float* row_out;            // [4][rows] (l1, accept, ce, bce) or nullptr
   float* losses;             // [4] (ce_loss, l1_loss, conf_loss, total)
+  double* red;               // [gridDim.x][3] per-CTA sums
+  unsigned int* ticket;      // zero between calls
   int* status;
   int rows, rows_max, n_vr, gamma, V;
-  double ce_alpha, l1_alpha, conf_alpha, decay;
+  double w[kMaxGamma];       // normalised position weights (host, fp64)
+  double ce_alpha, l1_alpha, conf_alpha;
 };
 
-// Per row, in fp64: L1 = sum of the range partials; accept = clamp(1 - L1/2);
-// CE = logsumexp(l) - l[target]; BCE with logits of the confidence against
-// accept, max(z, 0) - z a + log(1 + e^-|z|).  Then the position-weighted
-// batch means (w_j = e^(-j/decay) / sum_i e^(-i/decay)) and the total.
+// One thread per row: L1 = sum of the range partials; accept =
+// clamp(1 - L1/2, 0, 1); CE = logsumexp(l) - l[target]; BCE with logits of
+// the confidence against accept, max(z, 0) - z a + log(1 + e^-|z|).  The
+// transcendentals are fp32 (their rounding is far below the fp32 inputs'
+// own), the sums fp64.  Each CTA reduces its rows' w_j CE, w_j L1 and BCE;
+// the last CTA to finish (a ticket) adds the CTA sums in CTA order, so the
+// result does not depend on which CTA finishes last.
 __global__ void __launch_bounds__(kFinThreads) loss_finalize_kernel(FinParams p) {
-  __shared__ double red[3][kFinThreads / 32];
+  __shared__ double red[3][kFinWarps];
+  __shared__ int am_last;
+  // launched behind pass 2 with a programmatic dependency: wait for its
+  // partials (and, through it, pass 1's)
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  double wtot = 0.0;
-  for (int j = 0; j < p.gamma; ++j) wtot += exp(-(double)j / p.decay);
+  const int n = blockIdx.x * kFinThreads + tid;
   double s_ce = 0.0, s_l1 = 0.0, s_bce = 0.0;
-  bool bad = false;
-  for (int n = tid; n < p.rows; n += kFinThreads) {
+  if (n < p.rows) {
     Lse2 aq = lse2_empty();
     double l1 = 0.0;
     for (int v = 0; v < p.n_vr; ++v) {
@@ -569,31 +582,31 @@ __global__ void __launch_bounds__(kFinThreads) loss_finalize_kernel(FinParams p)
       l1 += (double)__ldcg(&p.parts2[(size_t)v * p.rows_max + n]);
     }
     const int tg = p.target[n];
-    double ce;
+    float ce;
     if (tg < 0 || tg >= p.V) {
       set_status(p.status, kErrArg);
-      ce = nan("");
+      ce = __int_as_float(0x7fc00000);   // NaN
     } else {
-      ce = ((double)aq.m + log2((double)aq.s)) * 0.69314718055994530942 - (double)__ldcg(&p.ltgt[n]);
+      ce = lse2_value(aq) - __ldcg(&p.ltgt[n]);
     }
     double a = 1.0 - 0.5 * l1;
     if (a < 0.0) a = 0.0;       // a NaN stays NaN and is reported below
     if (a > 1.0) a = 1.0;
-    const double z = (double)p.conf_logit[n];
-    const double bce = fmax(z, 0.0) - z * a + log1p(exp(-fabs(z)));
-    const double w = exp(-(double)(n % p.gamma) / p.decay) / wtot;
-    s_ce += w * ce;
-    s_l1 += w * l1;
-    s_bce += bce;
-    if (!isfinite(ce) || !isfinite(l1) || !isfinite(bce)) bad = true;
+    const float z = p.conf_logit[n];
+    const float af = (float)a;
+    const float bce = fmaxf(z, 0.f) - z * af + log1pf(expf(-fabsf(z)));
+    const double w = p.w[n % p.gamma];
+    s_ce = w * (double)ce;
+    s_l1 = w * l1;
+    s_bce = (double)bce;
+    if (!isfinite(ce) || !isfinite(l1) || !isfinite(bce)) set_status(p.status, kErrNonfinite);
     if (p.row_out) {
       p.row_out[n] = (float)l1;
-      p.row_out[(size_t)p.rows + n] = (float)a;
-      p.row_out[2 * (size_t)p.rows + n] = (float)ce;
-      p.row_out[3 * (size_t)p.rows + n] = (float)bce;
+      p.row_out[(size_t)p.rows + n] = af;
+      p.row_out[2 * (size_t)p.rows + n] = ce;
+      p.row_out[3 * (size_t)p.rows + n] = bce;
     }
   }
-  if (bad) set_status(p.status, kErrNonfinite);
   s_ce = warp_sum_f64(s_ce);
   s_l1 = warp_sum_f64(s_l1);
   s_bce = warp_sum_f64(s_bce);
@@ -603,24 +616,28 @@ __global__ void __launch_bounds__(kFinThreads) loss_finalize_kernel(FinParams p)
     red[2][warp] = s_bce;
   }
   __syncthreads();
-  if (warp == 0) {
-    s_ce = red[0][lane];
-    s_l1 = red[1][lane];
-    s_bce = red[2][lane];
-    s_ce = warp_sum_f64(s_ce);
-    s_l1 = warp_sum_f64(s_l1);
-    s_bce = warp_sum_f64(s_bce);
-    if (lane == 0) {
-      const double B = (double)(p.rows / p.gamma);
-      const double ce_loss = s_ce / B, l1_loss = s_l1 / B, conf_loss = s_bce / (double)p.rows;
-      p.losses[0] = (float)ce_loss;
-      p.losses[1] = (float)l1_loss;
-      p.losses[2] = (float)conf_loss;
-      p.losses[3] = (float)(p.ce_alpha * ce_loss + p.l1_alpha * l1_loss + p.conf_alpha * conf_loss);
-    }
+  if (tid < 3) {
+    double t = 0.0;
+    for (int w = 0; w < kFinWarps; ++w) t += red[tid][w];
+    p.red[blockIdx.x * 3 + tid] = t;
   }
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) am_last = (atomicAdd(p.ticket, 1u) == gridDim.x - 1) ? 1 : 0;
+  __syncthreads();
+  if (!am_last || tid != 0) return;
+  __threadfence();
+  double t[3] = {0.0, 0.0, 0.0};
+  for (unsigned b = 0; b < gridDim.x; ++b)
+    for (int i = 0; i < 3; ++i) t[i] += __ldcg(&p.red[b * 3 + i]);
+  const double B = (double)(p.rows / p.gamma);
+  const double ce_loss = t[0] / B, l1_loss = t[1] / B, conf_loss = t[2] / (double)p.rows;
+  p.losses[0] = (float)ce_loss;
+  p.losses[1] = (float)l1_loss;
+  p.losses[2] = (float)conf_loss;
+  p.losses[3] = (float)(p.ce_alpha * ce_loss + p.l1_alpha * l1_loss + p.conf_alpha * conf_loss);
+  *p.ticket = 0u;   // ready for the next call (kernels on the stream run in order)
 }
-static_assert(kFinThreads / 32 == 32, "one warp reduces the per-warp sums");
 
 }  // namespace
 
@@ -725,17 +742,28 @@ cudaError_t launch_loss(const Ctx& ctx, const LossArgs& a, cudaStream_t s) {
   f.conf_logit = a.conf_logit;
   f.row_out = a.row_out;
   f.losses = a.losses;
+  f.red = ctx.ws.loss_red;
+  f.ticket = ctx.ws.tickets + 1;
   f.status = ctx.ws.status;
   f.rows = rows;
   f.rows_max = p.rows_max;
   f.n_vr = p.n_vr;
   f.gamma = a.gamma;
   f.V = a.V;
+  double wsum = 0.0;
+  for (int j = 0; j < a.gamma; ++j) wsum += exp(-(double)j / a.decay);
+  for (int j = 0; j < a.gamma; ++j) f.w[j] = exp(-(double)j / a.decay) / wsum;
   f.ce_alpha = a.ce_alpha;
   f.l1_alpha = a.l1_alpha;
   f.conf_alpha = a.conf_alpha;
-  f.decay = a.decay;
-  loss_finalize_kernel<<<1, kFinThreads, 0, s>>>(f);
+  cudaLaunchConfig_t fcfg = {};
+  fcfg.gridDim = dim3((rows + kFinThreads - 1) / kFinThreads);
+  fcfg.blockDim = dim3(kFinThreads);
+  fcfg.stream = s;
+  fcfg.attrs = attr + 1;    // programmatic dependency on pass 2
+  fcfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&fcfg, loss_finalize_kernel, f);
+  if (e != cudaSuccess) return e;
   count_launch(ctx);
   return cudaGetLastError();
 }
