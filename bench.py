@@ -38,7 +38,7 @@ KERNEL_SOURCES = {
     "propose_tc_kernel": ["propose_tc.cu", "tc_common.cuh", "tc_ptx.cuh", "dsd_common.cuh"],
     "propose_mma_kernel": ["propose_mma.cu", "dsd_common.cuh"],
     "verify_rows": ["verify.cu", "dsd_common.cuh"],
-    "overlap_rows": ["overlap.cu", "dsd_common.cuh"],
+    "overlap_split": ["overlap.cu", "tc_common.cuh", "tc_ptx.cuh", "dsd_common.cuh"],
     "loss_tc_kernel": ["loss_tc.cu", "tc_common.cuh", "tc_ptx.cuh", "dsd_common.cuh"],
 }
 FALLBACK_HBM_GBS = 6800.0
@@ -310,7 +310,7 @@ def run_overlap(args, dsd, synth, dev, world):
     import numpy as np
     import torch
 
-    spec = synth.OverlapSpec()
+    spec = synth.OverlapSpec(N=args.blocks) if args.blocks else synth.OverlapSpec()
     ox = synth.overlap_inputs(spec, device=dev)
     ctx = dsd.Context(spec.V, 64, spec.G, 8, dtype="bf16", device=dev.index)
     stream = torch.cuda.Stream(device=dev)
@@ -343,18 +343,19 @@ def run_overlap(args, dsd, synth, dev, world):
     peak, peak_kind = hbm_peak()
     achieved = alg / (ms / 1e3) / 1e9
     line = {
-        "metric": "overlap blocks/s (a = sum min(p, q), tau_prob) at N=4096, gamma=7, V=151936",
+        "metric": f"overlap blocks/s (a = sum min(p, q), tau_prob) at N={spec.N}, gamma={spec.G}, "
+                  f"V={spec.V}",
         "value": world * spec.N / (ms / 1e3), "unit": "blocks/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "accumulate": "fp32", "data": "synthetic",
         "config": {"workload": f"overlap: N={spec.N} gamma={spec.G} V={spec.V} bf16, "
                                f"{spec.ragged_frac:.0%} ragged blocks",
-                   "valid_rows": valid_rows, "l2": "inputs 17.4 GB, larger than L2"},
-        "roofline": {"bound": "hbm", "kernel": "overlap_rows", "achieved": achieved, "peak": peak,
+                   "valid_rows": valid_rows, "l2": f"inputs {2 * spec.N * spec.G * spec.V * 2 / 1e9:.1f} GB, larger than L2"},
+        "roofline": {"bound": "hbm", "kernel": "overlap_split", "achieved": achieved, "peak": peak,
                      "unit": "GB/s", "frac": achieved / peak,
                      "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)",
-                     "traffic": traffic_for("overlap_rows", "overlap"),
+                     "traffic": traffic_for("overlap_split", "overlap"),
                      "alg_bytes": alg, "per": "one overlap call",
                      "alg_bytes_note": "valid P and Q rows once + a, l1 [N, gamma] + valid_len"},
         "cpu_baseline": None, "e2e": None,
@@ -661,6 +662,8 @@ def main(argv=None):
                     help="requests in the CPU-baseline sample")
     ap.add_argument("--ref-requests", type=int, default=16,
                     help="requests per step of the reference (oracle) arm")
+    ap.add_argument("--blocks", type=int, default=0,
+                    help="overlap workload: blocks N instead of 4096 (small profiling cases)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     args = ap.parse_args(argv)

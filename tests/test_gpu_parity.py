@@ -268,7 +268,10 @@ def test_verify_greedy_hand_case(dsd):
     ctx.close()
 
 
-@pytest.mark.parametrize("N,V", [(9, 2568), (3, 1000)])
+# (9, 2568) and (3, 1000): ragged last slices of the eight-CTA split;
+# (64, 2568): many clusters resident per SM; (2, 240000): a large vocabulary
+# (60 KB slices).
+@pytest.mark.parametrize("N,V", [(9, 2568), (3, 1000), (64, 2568), (2, 240000)])
 def test_overlap_small(dsd, N, V):
     spec = synth.OverlapSpec(N=N, V=V, ragged_frac=0.5, seed=28)
     ox = synth.overlap_inputs(spec, device=DEV)
@@ -281,6 +284,27 @@ def test_overlap_small(dsd, N, V):
     # empty call
     e = ctx.overlap(ox["P"][:0], ox["Q"][:0], ox["valid_len"][:0])
     assert float(e["mean_tau"][0]) == 0.0 and torch.all(e["accept_rate"] == 0)
+    ctx.close()
+
+
+def test_overlap_masked_and_nonfinite(dsd):
+    """-inf logits (a masked vocabulary range) are zero-probability entries;
+    a NaN logit on a valid position is reported as non-finite."""
+    spec = synth.OverlapSpec(N=5, V=2568, ragged_frac=0.0, seed=31)
+    ox = synth.overlap_inputs(spec, device=DEV)
+    P, Q = ox["P"].clone(), ox["Q"].clone()
+    P[0, 0, :700] = float("-inf")          # whole 16-byte chunks of several threads
+    Q[0, 0, 1000:1800] = float("-inf")
+    P[1, 2, ::3] = float("-inf")
+    Q[1, 2, 1::3] = float("-inf")
+    ctx = dsd.Context(spec.V, 64, spec.G, 8, dtype="bf16")
+    out = ctx.overlap(P, Q, ox["valid_len"])
+    assert ctx.sync_status() == 0
+    ref = O.overlap(synth.to_numpy(P), synth.to_numpy(Q), synth.to_numpy(ox["valid_len"]))
+    parity.compare_overlap({k: v.cpu().numpy() for k, v in out.items()}, ref)
+    P[2, 1, 17] = float("nan")
+    ctx.overlap(P, Q, ox["valid_len"])
+    assert ctx.sync_status() == -6
     ctx.close()
 
 
