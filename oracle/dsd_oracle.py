@@ -518,3 +518,112 @@ def cycle(U, E, W, conf, prev_tok, P, sps, req_id=None, temperature=0.0,
     ver = verify(P, U, E, W, prev_tok, prop["tokens"], kl, req_id,
                  temperature, seed, bias_at_first, act)
     return dict(propose=prop, schedule=sch, verify=ver, keep_len=kl)
+
+
+# ---------------------------------------------------------------------------
+# Confidence side: the confidence head, static threshold truncation and the
+# calibration metrics of the survival probabilities
+# ([TRAIN] Confidence head 与训练目标; [WALK] 4.3 Propose;
+#  [READ] 3.1 prefix survival and its monitoring, 5 reliability diagram)
+# ---------------------------------------------------------------------------
+
+def sigmoid(z):
+    """1 / (1 + e^-z), written per sign so neither branch overflows."""
+    z = float(z)
+    if z >= 0.0:
+        return 1.0 / (1.0 + np.exp(-z))
+    e = np.exp(z)
+    return e / (1.0 + e)
+
+
+def confidence_head(h, E, w_c, b_c, prev_tok, tokens):
+    """Per-position confidence of the drafted tokens ([TRAIN] Confidence head):
+        s[r, j] = w_c . [h[r, j]; m[r, j]] + b_c,   c[r, j] = sigmoid(s[r, j])
+    with m[r, j] = E[t_{j-1}] the Markov table row of the token before
+    position j (the anchor prev_tok[r] at j = 0, the drafted tokens[r, j-1]
+    after it) and w_c of length H + r (h part first).  Returns the logits s,
+    the confidences c and the prefix survival a = survival(c)."""
+    h = _f64(h)
+    R, G, H = h.shape
+    w = _f64(w_c)
+    rank = np.asarray(E).shape[1]
+    if w.shape != (H + rank,):
+        raise ValueError("w_c must have H + rank entries")
+    s = np.zeros((R, G))
+    c = np.zeros((R, G))
+    for r in range(R):
+        for j in range(G):
+            t = int(prev_tok[r]) if j == 0 else int(tokens[r, j - 1])
+            x = np.concatenate([h[r, j], _f64(E[t])])
+            s[r, j] = float(np.dot(w, x)) + float(b_c)
+            c[r, j] = sigmoid(s[r, j])
+    return dict(logit=s, conf=c, survival=survival(c))
+
+
+def threshold_keep(conf, threshold):
+    """Static confidence truncation ([WALK] 4.3: proposal_len =
+    min(block, first position whose confidence is below the threshold)):
+    keep[r] = number of leading positions j with conf[r, j] >= threshold.
+    A threshold of 0 keeps every position."""
+    c = _f64(conf)
+    R, G = c.shape
+    keep = np.zeros(R, dtype=np.int64)
+    for r in range(R):
+        k = 0
+        while k < G and c[r, k] >= threshold:
+            k += 1
+        keep[r] = k
+    return keep
+
+
+def calibration(conf, accept_len, n_bins=10):
+    """Calibration of predicted survival against realised acceptance
+    ([READ] 3.1: per-step error and the cumulative-product bias; [READ] 5:
+    reliability diagram and ECE).  conf [M, gamma] are the predicted per-step
+    confidences (clamped to [0, 1]); accept_len [M] the accepted prefix
+    lengths of full-block verification.  With a = survival(conf):
+      realised survival     y[r, j] = 1 if j < accept_len[r] else 0
+      tested positions      j <= accept_len[r] (and j < gamma), whose
+                            realised step outcome is y[r, j]
+      abs_error    = mean over tested positions of |conf - y|
+      cumprod_bias = mean over all positions of (a - y)   (> 0: optimistic)
+      pos_pred[j], pos_real[j] = means over requests of a[:, j] and y[:, j]
+      reliability bins of a: b = min(floor(a n_bins), n_bins - 1); per bin
+      the count, the mean of a and the mean of y (0 for an empty bin)
+      ece = sum_b count_b / (M gamma) |mean a_b - mean y_b|
+    Empty means are 0."""
+    c = np.clip(_f64(conf), 0.0, 1.0)
+    M, G = c.shape
+    L = np.asarray(accept_len).astype(np.int64)
+    if np.any(L < 0) or np.any(L > G):
+        raise ValueError("accept_len outside 0..gamma")
+    a = survival(c)
+    cnt = np.zeros(n_bins, dtype=np.int64)
+    sp = np.zeros(n_bins)
+    sr = np.zeros(n_bins)
+    err_sum, n_tested, bias_sum = 0.0, 0, 0.0
+    pos_pred = np.zeros(G)
+    pos_real = np.zeros(G)
+    for r in range(M):
+        for j in range(G):
+            y = 1.0 if j < L[r] else 0.0
+            if j <= L[r]:
+                err_sum += abs(c[r, j] - y)
+                n_tested += 1
+            bias_sum += a[r, j] - y
+            pos_pred[j] += a[r, j]
+            pos_real[j] += y
+            b = min(int(np.floor(a[r, j] * n_bins)), n_bins - 1)
+            cnt[b] += 1
+            sp[b] += a[r, j]
+            sr[b] += y
+    total = M * G
+    mean_pred = np.where(cnt > 0, sp / np.maximum(cnt, 1), 0.0)
+    mean_real = np.where(cnt > 0, sr / np.maximum(cnt, 1), 0.0)
+    ece = float(np.sum(cnt / total * np.abs(mean_pred - mean_real))) if total else 0.0
+    return dict(count=cnt, mean_pred=mean_pred, mean_real=mean_real, ece=ece,
+                abs_error=err_sum / n_tested if n_tested else 0.0,
+                cumprod_bias=bias_sum / total if total else 0.0,
+                n_tested=n_tested,
+                pos_pred=pos_pred / M if M else pos_pred,
+                pos_real=pos_real / M if M else pos_real)

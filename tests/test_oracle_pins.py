@@ -553,3 +553,76 @@ def test_loss_matches_torch_functional_on_cpu():
         assert abs(out["l1_loss"] - float(wl1)) < 1e-12
         assert abs(out["conf_loss"] - float(cl)) < 1e-12
         assert abs(out["loss"] - float(0.1 * wce + 0.9 * wl1 + cl)) < 1e-10
+
+
+# ---------------------------------------------------------------------------
+# Confidence side ([TRAIN] confidence head; [WALK] 4.3; [READ] 3.1, 5)
+# ---------------------------------------------------------------------------
+
+def test_threshold_keep_by_hand():
+    c = np.array([[0.9, 0.8, 0.4, 0.9],
+                  [0.3, 0.9, 0.9, 0.9],
+                  [0.7, 0.7, 0.7, 0.7],
+                  [0.7, np.nan, 0.9, 0.9]])
+    assert list(O.threshold_keep(c, 0.5)) == [2, 0, 4, 1]
+    assert list(O.threshold_keep(c[:3], 0.0)) == [4, 4, 4]      # 0 keeps everything
+    assert list(O.threshold_keep(c[:3], 1.01)) == [0, 0, 0]
+    assert list(O.threshold_keep(c, 0.7)) == [2, 0, 4, 1]        # >= keeps a tie
+
+
+def test_confidence_head_by_hand():
+    # H = 2, rank 2, V = 3.  w_c = (1, -1 | 2, 0.5), b_c = -0.5
+    E = np.array([[1.0, 0.0], [0.0, 2.0], [-1.0, 1.0]])
+    h = np.array([[[0.5, 0.25], [1.0, 1.0], [0.0, 3.0]]])      # R = 1, gamma = 3
+    w = np.array([1.0, -1.0, 2.0, 0.5])
+    out = O.confidence_head(h, E, w, -0.5, prev_tok=[2], tokens=np.array([[1, 0, 2]]))
+    # j = 0 uses E[prev_tok] = E[2]; j = 1 uses E[tokens[0]] = E[1]; j = 2 uses E[0]
+    s = [0.25 + (-2.0 + 0.5) - 0.5, 0.0 + (0.0 + 1.0) - 0.5, -3.0 + 2.0 - 0.5]
+    assert np.allclose(out["logit"][0], s, atol=1e-15)
+    c = [1.0 / (1.0 + np.exp(-v)) for v in s]
+    assert np.allclose(out["conf"][0], c, rtol=1e-14)
+    assert np.allclose(out["survival"][0], np.cumprod(c), rtol=1e-14)
+    assert O.sigmoid(0.0) == 0.5 and O.sigmoid(800.0) == 1.0 and O.sigmoid(-800.0) == 0.0
+
+
+def _page_cumprod_batch(G=6):
+    # 5^G requests whose accepted prefix length L satisfies P(L >= k) = 0.8^k exactly
+    L = []
+    for k in range(G + 1):
+        ge = 5 ** (G - k) * 4 ** k
+        gt = 5 ** (G - k - 1) * 4 ** (k + 1) if k < G else 0
+        L += [k] * (ge - gt)
+    return np.array(L)
+
+
+def test_calibration_reproduces_the_page_example():
+    g = _golden("calibration_cumprod_example.json")
+    G = g["gamma"]
+    L = _page_cumprod_batch(G)
+    c = np.full((len(L), G), g["predicted_step"])
+    out = O.calibration(c, L, n_bins=10)
+    assert abs(out["pos_pred"][G - 1] - g["predicted_survival_pos6_page_rounded"]) < 5e-4
+    assert abs(out["pos_real"][G - 1] - g["true_survival_pos6_page_rounded"]) < 5e-4
+    ratio = out["pos_pred"][G - 1] / out["pos_real"][G - 1]
+    assert round(100 * (ratio - 1)) == g["overestimate_page_percent"]
+    # the empirical step acceptance is exactly the true step probability
+    assert np.allclose(out["pos_real"], g["true_step"] ** np.arange(1, G + 1), rtol=1e-12)
+    # abs error over tested positions: 0.8 * |0.85 - 1| + 0.2 * |0.85 - 0| = 0.29
+    assert abs(out["abs_error"] - 0.29) < 1e-12
+    # each position's survival falls in its own bin, so ECE = the mean bias
+    assert abs(out["ece"] - out["cumprod_bias"]) < 1e-12
+    bias = np.mean(0.85 ** np.arange(1, G + 1) - 0.8 ** np.arange(1, G + 1))
+    assert abs(out["cumprod_bias"] - bias) < 1e-12
+
+
+def test_calibration_perfect_and_edges():
+    # gamma = 1, c = 0.5, half of the requests accepted: perfectly calibrated
+    out = O.calibration(np.full((4, 1), 0.5), [1, 1, 0, 0], n_bins=4)
+    assert out["ece"] == 0.0 and out["cumprod_bias"] == 0.0 and out["abs_error"] == 0.5
+    assert list(out["count"]) == [0, 0, 4, 0] and out["n_tested"] == 4
+    # survival 1 goes to the last bin, 0 to the first; untested positions
+    # (after the first rejection) do not count toward the step error
+    out = O.calibration(np.array([[1.0, 0.0, 1.0]]), [1], n_bins=5)
+    assert list(out["count"]) == [2, 0, 0, 0, 1]
+    assert out["n_tested"] == 2 and out["abs_error"] == 0.0
+    assert abs(out["ece"] - 0.0) < 1e-15
