@@ -564,8 +564,11 @@ def threshold_keep(conf, threshold):
     """Static confidence truncation ([WALK] 4.3: proposal_len =
     min(block, first position whose confidence is below the threshold)):
     keep[r] = number of leading positions j with conf[r, j] >= threshold.
-    A threshold of 0 keeps every position."""
+    A threshold of 0 keeps every position.  The threshold is an fp32
+    argument of the library call, so it is rounded to fp32 here too and the
+    comparison is the fp32 one (exact in fp64 after widening both)."""
     c = _f64(conf)
+    threshold = float(np.float32(threshold))
     R, G = c.shape
     keep = np.zeros(R, dtype=np.int64)
     for r in range(R):
