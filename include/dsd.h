@@ -6,15 +6,17 @@
  * and dsd_overlap is the separate offline-metric call.  Sources, by page title
  * and section:
  *   [TRAIN] "Qwen3.8-Flash-Next DSpark 训练实验": 评估口径/离线指标;
- *           Baseline 架构/Markov 顺序修正
+ *           Baseline 架构/Markov 顺序修正; Confidence head 与训练目标
  *   [NOTES] "DSpark notes" (h.sjds.net/a/571373): 2.2 Sequential Stage;
  *           2.3 串行头的两种形态
  *   [READ]  "DSpark 论文精读：置信度调度推测解码、半自回归生成与大模型推理加速":
- *           2.2, 2.3, 3.1, 3.2
+ *           2.2, 2.3, 3.1, 3.2, 4.1, 5
  *   [WALK]  "DeepSpec 训练全流程详解（以 Qwen3 + DSpark 为例）": 3.4 Loss,
  *           4.3 Propose, 4.4 Verify
  * dsd_loss_forward is the training-side twin: the teacher-forced DSpark loss
- * ([READ] 4.1; [WALK] 3.4).
+ * ([READ] 4.1; [WALK] 3.4).  dsd_confidence_head, dsd_threshold_keep and
+ * dsd_calibration cover the scheduler's input: the confidence head, the
+ * static truncation it replaces, and the calibration of its survivals.
  *
  * Conventions for every call below.
  *   - Tensor arguments are DEVICE pointers owned by the caller, row-major and
@@ -300,6 +302,65 @@ int dsd_loss_forward(dsd_ctx* ctx, int B, const void* U, const void* E, const vo
                      const int32_t* prev_tok, const void* P, const int32_t* target,
                      const float* conf_logit, float ce_alpha, float l1_alpha, float conf_alpha,
                      float decay, float* row_out, float* losses, void* stream);
+
+/*
+ * dsd_confidence_head -- per-position confidence of the drafted tokens
+ * ([TRAIN] Confidence head 与训练目标: s = w_c^T [h; m] + b_c, c = sigmoid(s),
+ * with m the Markov representation W_1[t_{i-1}] before the bias projection)
+ * and its prefix survival ([READ] 3.1), the scheduler's input.
+ *
+ *   s[r, j] = w_c[0:H] . h[r, j, :] + w_c[H:H+rank] . E[t, :] + b_c,
+ *             t = prev_tok[r] at j = 0, tokens[r, j-1] after it
+ *   conf[r, j] = sigmoid(s[r, j])
+ *   survival[r, j] = prod_{i <= j} conf[r, i]   (fp64 product, rounded)
+ * h [R, gamma, H], E [V, rank], w_c [H + rank] in the context's dtype,
+ * device, 16-byte aligned; H a positive multiple of 8.  prev_tok [R],
+ * tokens [R, gamma] i32 (as written by dsd_propose).  conf, survival
+ * [R, gamma] f32 out.  A token outside [0, V) sets DSD_ERR_ARG in the status
+ * word (row 0 of E is used); a non-finite logit sets DSD_ERR_NONFINITE (its
+ * confidence is written as 0).  Host-side argument errors return before any
+ * launch.  R == 0 is a no-op.  One launch.
+ */
+int dsd_confidence_head(dsd_ctx* ctx, int R, int H, const void* h, const void* E, const void* w_c,
+                        float b_c, const int32_t* prev_tok, const int32_t* tokens, float* conf,
+                        float* survival, void* stream);
+
+/*
+ * dsd_threshold_keep -- static confidence truncation, the baseline the
+ * scheduler replaces ([WALK] 4.3 Propose: proposal_len = min(block, first
+ * position whose confidence is below the threshold); [READ] 5 threshold
+ * sweep).
+ *   keep_len[r] = number of leading positions j with conf[r, j] >= threshold
+ * conf [R, gamma] f32 device; keep_len [R] i32 device out.  A NaN
+ * confidence ends the kept prefix; a NaN threshold is DSD_ERR_NONFINITE.
+ * R == 0 is a no-op.  One launch.
+ */
+int dsd_threshold_keep(dsd_ctx* ctx, int R, const float* conf, float threshold, int32_t* keep_len,
+                       void* stream);
+
+/*
+ * dsd_calibration -- calibration of predicted survival against realised
+ * acceptance ([READ] 3.1: per-step error and cumulative-product bias of the
+ * confidence head; [READ] 5: reliability diagram, ECE).
+ *
+ * conf [M, gamma] f32: predicted per-step confidences (clamped to [0, 1]);
+ * accept_len [M] i32 in 0..gamma: accepted prefix lengths of full-block
+ * verification.  With a = prod_{i <= j} conf[r, i] (fp64) and the realised
+ * survival y[r, j] = (j < accept_len[r]):
+ *   bins [3][n_bins] f32 out: per reliability bin b = min(floor(a n_bins),
+ *     n_bins - 1) (taken in fp64): count, mean a, mean y (0 when empty)
+ *   pos [2][gamma] f32 out: mean a and mean y per position
+ *   metrics [4] f32 out: ECE = sum_b count_b / (M gamma) |mean a - mean y|;
+ *     abs_error = mean |conf - y| over tested positions (j <= accept_len);
+ *     cumprod_bias = mean (a - y) over all positions (> 0: optimistic);
+ *     the number of tested positions
+ * 1 <= n_bins <= 64.  A non-finite confidence sets DSD_ERR_NONFINITE (it is
+ * taken as 0), an accept_len outside 0..gamma DSD_ERR_ARG (clamped).  Uses
+ * the context's workspace: calls on one context must not overlap on the
+ * GPU.  M == 0 writes zeros.  One launch.
+ */
+int dsd_calibration(dsd_ctx* ctx, int M, const float* conf, const int32_t* accept_len, int n_bins,
+                    float* bins, float* pos, float* metrics, void* stream);
 
 /*
  * dsd_propose_noalloc -- dsd_propose for callers that cannot allocate device

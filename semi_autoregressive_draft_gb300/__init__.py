@@ -35,7 +35,8 @@ EXPORTED = [
     "dsd_create", "dsd_destroy", "dsd_last_error", "dsd_sync_status", "dsd_workspace_bytes",
     "dsd_launch_count", "dsd_last_engine",
     "dsd_propose", "dsd_schedule", "dsd_verify", "dsd_cycle", "dsd_cycle_host", "dsd_overlap",
-    "dsd_propose_noalloc", "dsd_loss_forward",
+    "dsd_propose_noalloc", "dsd_loss_forward", "dsd_confidence_head", "dsd_threshold_keep",
+    "dsd_calibration",
 ]
 
 
@@ -87,6 +88,9 @@ def load_library(path: str | None = None):
         "dsd_overlap": (_I, [_P, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
         "dsd_loss_forward": (_I, [_P, _I, _P, _P, _P, _P, _P, _P, _P, _F, _F, _F, _F, _P, _P,
                                   _P]),
+        "dsd_confidence_head": (_I, [_P, _I, _I, _P, _P, _P, _F, _P, _P, _P, _P, _P]),
+        "dsd_threshold_keep": (_I, [_P, _I, _P, _F, _P, _P]),
+        "dsd_calibration": (_I, [_P, _I, _P, _P, _I, _P, _P, _P, _P]),
         "dsd_propose_noalloc": (_I, [_I, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _F,
                                      _U64, _P, _P, _P, _P, _P]),
     }
@@ -200,6 +204,24 @@ def dsd_loss_forward(ctx, B, U, E, W, prev_tok, P, target, conf_logit, ce_alpha,
         ctx, B, _ptr(U), _ptr(E), _ptr(W), _ptr(prev_tok), _ptr(P), _ptr(target),
         _ptr(conf_logit), ce_alpha, l1_alpha, conf_alpha, decay, _ptr(row_out), _ptr(losses),
         _stream(stream, device)))
+
+
+def dsd_confidence_head(ctx, R, H, h, E, w_c, b_c, prev_tok, tokens, conf, survival,
+                        stream=None, device=0):
+    _check(ctx, load_library().dsd_confidence_head(
+        ctx, R, H, _ptr(h), _ptr(E), _ptr(w_c), b_c, _ptr(prev_tok), _ptr(tokens), _ptr(conf),
+        _ptr(survival), _stream(stream, device)))
+
+
+def dsd_threshold_keep(ctx, R, conf, threshold, keep_len, stream=None, device=0):
+    _check(ctx, load_library().dsd_threshold_keep(ctx, R, _ptr(conf), threshold, _ptr(keep_len),
+                                                  _stream(stream, device)))
+
+
+def dsd_calibration(ctx, M, conf, accept_len, n_bins, bins, pos, metrics, stream=None, device=0):
+    _check(ctx, load_library().dsd_calibration(ctx, M, _ptr(conf), _ptr(accept_len), n_bins,
+                                               _ptr(bins), _ptr(pos), _ptr(metrics),
+                                               _stream(stream, device)))
 
 
 def dsd_propose_noalloc(V, rank, gamma, dtype, act, bias_at_first, R, U, E, W, conf, prev_tok,
@@ -363,6 +385,41 @@ class Context:
                         mean_tau=self._empty((1,), torch.float32))
         dsd_overlap(self.handle, N, P_logits, Q_logits, valid_len, o["a"], o["l1"], o["tau"],
                     o["accept_rate"], o["mean_tau"], stream, self.device)
+        return o
+
+    def confidence_head(self, h, E, w_c, b_c, prev_tok, tokens, out=None, stream=None):
+        """conf = sigmoid(w_c . [h; E[t_prev]] + b_c) and its prefix survival,
+        both [R, gamma] f32.  h is [R, gamma, H]."""
+        R, G, H = h.shape
+        for n, t in (("h", h), ("E", E), ("w_c", w_c)):
+            self._check_in(n, t, self.torch_dtype)
+        self._check_in("prev_tok", prev_tok, torch.int32)
+        self._check_in("tokens", tokens, torch.int32)
+        o = out or dict(conf=self._empty((R, G), torch.float32),
+                        survival=self._empty((R, G), torch.float32))
+        dsd_confidence_head(self.handle, R, H, h, E, w_c, float(b_c), prev_tok, tokens, o["conf"],
+                            o["survival"], stream, self.device)
+        return o
+
+    def threshold_keep(self, conf, threshold, out=None, stream=None):
+        """keep_len [R] i32: leading positions with conf >= threshold."""
+        self._check_in("conf", conf, torch.float32)
+        keep = out if out is not None else self._empty((conf.shape[0],), torch.int32)
+        dsd_threshold_keep(self.handle, conf.shape[0], conf, float(threshold), keep, stream,
+                           self.device)
+        return keep
+
+    def calibration(self, conf, accept_len, n_bins=10, out=None, stream=None):
+        """Reliability bins, per-position survival and (ece, abs_error,
+        cumprod_bias, tested positions) of predicted survival against
+        realised acceptance."""
+        self._check_in("conf", conf, torch.float32)
+        self._check_in("accept_len", accept_len, torch.int32)
+        o = out or dict(bins=self._empty((3, n_bins), torch.float32),
+                        pos=self._empty((2, self.gamma), torch.float32),
+                        metrics=self._empty((4,), torch.float32))
+        dsd_calibration(self.handle, conf.shape[0], conf, accept_len, n_bins, o["bins"], o["pos"],
+                        o["metrics"], stream, self.device)
         return o
 
     def loss_forward(self, U, E, W, prev_tok, P, target, conf_logit, ce_alpha=0.1, l1_alpha=0.9,

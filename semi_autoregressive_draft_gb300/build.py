@@ -30,6 +30,7 @@ SOURCES = [
     "verify.cu",
     "overlap.cu",
     "loss_tc.cu",
+    "confidence.cu",
 ]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",

@@ -1,0 +1,284 @@
+// Confidence side of the scheduler's input: the confidence head, the static
+// threshold truncation it replaces, and calibration metrics of the survival
+// probabilities.
+//
+// Pages: "Qwen3.8-Flash-Next DSpark 训练实验", Confidence head 与训练目标
+// (s = w_c . [h; m] + b_c with m = W_1[t_prev], c = sigmoid(s));
+// "DeepSpec 训练全流程详解（以 Qwen3 + DSpark 为例）", 4.3 Propose
+// (proposal_len = min(block, first position below the threshold));
+// "DSpark 论文精读", 3.1 (prefix survival a = prod c, why the
+// cumulative-product bias is monitored) and 5 (reliability diagram, ECE).
+//
+// confidence_head_kernel: one CTA per request, one warp per position: the
+//   dot products of the row's hidden state (H values) and of the Markov row
+//   of the previous token (rank values) with w_c, 16-byte loads, fp32 sums;
+//   then warp 0 forms c = sigmoid(s) and the survival prefix products in fp64.
+// threshold_keep_kernel: one thread per request.
+// calibration_kernel: a grid-stride pass, one thread per request: survival
+//   in fp64, reliability bin floor(a n_bins) taken in fp64 (the oracle's
+//   precision), per-CTA shared-memory sums, then global fp64 sums; the last
+//   CTA to finish (a ticket) forms the means, the ECE and the errors and
+//   clears the sums for the next call.
+#include "dsd_common.cuh"
+
+namespace dsd {
+
+namespace {
+
+// 16 bytes of dtype T as fp32 values (8 for bf16, 4 for f32)
+template <typename T>
+__device__ __forceinline__ int chunk_to_f32(uint4 q, float* x) {
+  if constexpr (sizeof(T) == 2) {
+    x[0] = bf16lo(q.x); x[1] = bf16hi(q.x); x[2] = bf16lo(q.y); x[3] = bf16hi(q.y);
+    x[4] = bf16lo(q.z); x[5] = bf16hi(q.z); x[6] = bf16lo(q.w); x[7] = bf16hi(q.w);
+    return 8;
+  } else {
+    x[0] = __uint_as_float(q.x); x[1] = __uint_as_float(q.y);
+    x[2] = __uint_as_float(q.z); x[3] = __uint_as_float(q.w);
+    return 4;
+  }
+}
+
+// sum over one warp's lanes of a[i] * b[i], i < n (n a multiple of the
+// elements per 16 bytes; both arrays 16-byte aligned)
+template <typename T>
+__device__ __forceinline__ float warp_dot(const T* a, const T* b, int n, int lane) {
+  constexpr int epc = 16 / (int)sizeof(T);
+  float acc = 0.f;
+  for (int v = lane * epc; v < n; v += 32 * epc) {
+    float x[8], y[8];
+    const int k = chunk_to_f32<T>(ld_stream16(a + v), x);
+    chunk_to_f32<T>(__ldg(reinterpret_cast<const uint4*>(b + v)), y);
+#pragma unroll
+    for (int e = 0; e < 8; ++e)
+      if (e < k) acc = fmaf(x[e], y[e], acc);
+  }
+  return warp_sum(acc);
+}
+
+__device__ __forceinline__ float sigmoid_f(float z) {
+  if (z >= 0.f) return 1.f / (1.f + expf(-z));
+  const float e = expf(z);
+  return e / (1.f + e);
+}
+
+template <typename T>
+__global__ void __launch_bounds__(32 * kMaxGamma) confidence_head_kernel(
+    const T* __restrict__ h, const T* __restrict__ E, const T* __restrict__ w_c, float b_c,
+    const int32_t* __restrict__ prev_tok, const int32_t* __restrict__ tokens, int H, int rank,
+    int V, int gamma, float* conf, float* survival, int* status) {
+  __shared__ float s_logit[kMaxGamma];
+  const int r = blockIdx.x, j = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (j < gamma) {
+    int t = j == 0 ? prev_tok[r] : tokens[(size_t)r * gamma + j - 1];
+    if (t < 0 || t >= V) {
+      if (lane == 0) set_status(status, kErrArg);
+      t = 0;
+    }
+    const float sh = warp_dot<T>(h + ((size_t)r * gamma + j) * H, w_c, H, lane);
+    const float sm = warp_dot<T>(E + (size_t)t * rank, w_c + H, rank, lane);
+    if (lane == 0) s_logit[j] = sh + sm + b_c;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    double acc = 1.0;
+    for (int i = 0; i < gamma; ++i) {
+      float c = sigmoid_f(s_logit[i]);
+      if (!isfinite(c)) {
+        set_status(status, kErrNonfinite);
+        c = 0.f;
+      }
+      conf[(size_t)r * gamma + i] = c;
+      acc *= (double)fminf(fmaxf(c, 0.f), 1.f);
+      survival[(size_t)r * gamma + i] = (float)acc;
+    }
+  }
+}
+
+__global__ void threshold_keep_kernel(const float* conf, int R, int gamma, float threshold,
+                                      int32_t* keep_len) {
+  const int r = blockIdx.x * blockDim.x + threadIdx.x;
+  if (r >= R) return;
+  int k = 0;
+  while (k < gamma && conf[(size_t)r * gamma + k] >= threshold) ++k;   // NaN stops
+  keep_len[r] = k;
+}
+
+
+constexpr int kCalThreads = 256;
+
+struct CalParams {
+  const float* conf;          // [M, gamma]
+  const int32_t* accept_len;  // [M]
+  int M, gamma, n_bins;
+  double* acc;                // [2 kMaxCalBins + 2 + 2 kMaxGamma] zero between calls
+  unsigned long long* cnt;    // [kMaxCalBins + 1] zero between calls (last: tested positions)
+  unsigned int* ticket;       // zero between calls
+  float* bins;                // [3][n_bins]: count, mean survival, mean realised survival
+  float* pos;                 // [2][gamma]: mean survival, realised survival rate per position
+  float* metrics;             // [4]: ece, abs_error, cumprod_bias, tested positions
+  int* status;
+};
+
+__global__ void __launch_bounds__(kCalThreads) calibration_kernel(CalParams p) {
+  __shared__ double sp[kMaxCalBins], sr[kMaxCalBins], spp[kMaxGamma], spr[kMaxGamma], se[2];
+  __shared__ unsigned long long sc[kMaxCalBins + 1];
+  __shared__ int am_last;
+  const int tid = threadIdx.x;
+  for (int i = tid; i < kMaxCalBins; i += kCalThreads) {
+    sp[i] = sr[i] = 0.0;
+    sc[i] = 0ull;
+  }
+  if (tid < kMaxGamma) spp[tid] = spr[tid] = 0.0;
+  if (tid < 2) se[tid] = 0.0;
+  if (tid == 0) sc[kMaxCalBins] = 0ull;
+  __syncthreads();
+  double err = 0.0, bias = 0.0, lp[kMaxGamma], lr[kMaxGamma];
+  for (int j = 0; j < kMaxGamma; ++j) lp[j] = lr[j] = 0.0;
+  unsigned long long tested = 0ull;
+  for (int r = blockIdx.x * kCalThreads + tid; r < p.M; r += gridDim.x * kCalThreads) {
+    int L = p.accept_len[r];
+    if (L < 0 || L > p.gamma) {
+      set_status(p.status, kErrArg);
+      L = L < 0 ? 0 : p.gamma;
+    }
+    double a = 1.0;
+    for (int j = 0; j < p.gamma; ++j) {
+      float cf = p.conf[(size_t)r * p.gamma + j];
+      if (!isfinite(cf)) {
+        set_status(p.status, kErrNonfinite);
+        cf = 0.f;
+      }
+      const double c = (double)fminf(fmaxf(cf, 0.f), 1.f);
+      a *= c;
+      const double y = j < L ? 1.0 : 0.0;
+      if (j <= L) {
+        err += fabs(c - y);
+        ++tested;
+      }
+      bias += a - y;
+      lp[j] += a;
+      lr[j] += y;
+      int b = (int)floor(a * (double)p.n_bins);
+      b = b < p.n_bins - 1 ? b : p.n_bins - 1;
+      atomicAdd(&sc[b], 1ull);
+      atomicAdd(&sp[b], a);
+      atomicAdd(&sr[b], y);
+    }
+  }
+  for (int j = 0; j < p.gamma; ++j) {
+    const double a = warp_sum_f64(lp[j]), y = warp_sum_f64(lr[j]);
+    if ((tid & 31) == 0) {
+      atomicAdd(&spp[j], a);
+      atomicAdd(&spr[j], y);
+    }
+  }
+  err = warp_sum_f64(err);
+  bias = warp_sum_f64(bias);
+  if ((tid & 31) == 0) {
+    atomicAdd(&se[0], err);
+    atomicAdd(&se[1], bias);
+  }
+  atomicAdd(&sc[kMaxCalBins], tested);
+  __syncthreads();
+  // this CTA's sums into the global ones
+  for (int i = tid; i < p.n_bins; i += kCalThreads) {
+    if (sc[i]) {
+      atomicAdd(&p.cnt[i], sc[i]);
+      atomicAdd(&p.acc[i], sp[i]);
+      atomicAdd(&p.acc[kMaxCalBins + i], sr[i]);
+    }
+  }
+  if (tid < p.gamma) {
+    atomicAdd(&p.acc[2 * kMaxCalBins + 2 + tid], spp[tid]);
+    atomicAdd(&p.acc[2 * kMaxCalBins + 2 + kMaxGamma + tid], spr[tid]);
+  }
+  if (tid == 0) {
+    atomicAdd(&p.acc[2 * kMaxCalBins], se[0]);
+    atomicAdd(&p.acc[2 * kMaxCalBins + 1], se[1]);
+    atomicAdd(&p.cnt[kMaxCalBins], sc[kMaxCalBins]);
+  }
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) am_last = (atomicAdd(p.ticket, 1u) == gridDim.x - 1) ? 1 : 0;
+  __syncthreads();
+  if (!am_last || tid != 0) return;
+  __threadfence();
+  const double total = (double)p.M * p.gamma;
+  double ece = 0.0;
+  for (int b = 0; b < p.n_bins; ++b) {
+    const unsigned long long n = __ldcg(&p.cnt[b]);
+    const double mp = n ? __ldcg(&p.acc[b]) / (double)n : 0.0;
+    const double mr = n ? __ldcg(&p.acc[kMaxCalBins + b]) / (double)n : 0.0;
+    p.bins[b] = (float)n;
+    p.bins[p.n_bins + b] = (float)mp;
+    p.bins[2 * p.n_bins + b] = (float)mr;
+    ece += (double)n / total * fabs(mp - mr);
+    p.cnt[b] = 0ull;
+    p.acc[b] = 0.0;
+    p.acc[kMaxCalBins + b] = 0.0;
+  }
+  for (int j = 0; j < p.gamma; ++j) {
+    double* a = p.acc + 2 * kMaxCalBins + 2;
+    p.pos[j] = p.M ? (float)(__ldcg(&a[j]) / p.M) : 0.f;
+    p.pos[p.gamma + j] = p.M ? (float)(__ldcg(&a[kMaxGamma + j]) / p.M) : 0.f;
+    a[j] = a[kMaxGamma + j] = 0.0;
+  }
+  const unsigned long long nt = __ldcg(&p.cnt[kMaxCalBins]);
+  p.metrics[0] = p.M ? (float)ece : 0.f;
+  p.metrics[1] = nt ? (float)(__ldcg(&p.acc[2 * kMaxCalBins]) / (double)nt) : 0.f;
+  p.metrics[2] = p.M ? (float)(__ldcg(&p.acc[2 * kMaxCalBins + 1]) / total) : 0.f;
+  p.metrics[3] = (float)nt;
+  p.acc[2 * kMaxCalBins] = p.acc[2 * kMaxCalBins + 1] = 0.0;
+  p.cnt[kMaxCalBins] = 0ull;
+  *p.ticket = 0u;   // ready for the next call (kernels on the stream run in order)
+}
+}  // namespace
+
+cudaError_t launch_confidence_head(const Ctx& ctx, const ConfHeadArgs& a, cudaStream_t s) {
+  if (a.R == 0) return cudaSuccess;
+  const dim3 grid(a.R), block(32 * a.gamma);
+  if (a.dtype == 1)
+    confidence_head_kernel<__nv_bfloat16><<<grid, block, 0, s>>>(
+        static_cast<const __nv_bfloat16*>(a.h), static_cast<const __nv_bfloat16*>(a.E),
+        static_cast<const __nv_bfloat16*>(a.w_c), a.b_c, a.prev_tok, a.tokens, a.H, a.rank, a.V,
+        a.gamma, a.conf, a.survival, ctx.ws.status);
+  else
+    confidence_head_kernel<float><<<grid, block, 0, s>>>(
+        static_cast<const float*>(a.h), static_cast<const float*>(a.E),
+        static_cast<const float*>(a.w_c), a.b_c, a.prev_tok, a.tokens, a.H, a.rank, a.V, a.gamma,
+        a.conf, a.survival, ctx.ws.status);
+  count_launch(ctx);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_threshold_keep(const Ctx& ctx, int R, const float* conf, float threshold,
+                                  int32_t* keep_len, cudaStream_t s) {
+  if (R == 0) return cudaSuccess;
+  threshold_keep_kernel<<<(R + 255) / 256, 256, 0, s>>>(conf, R, ctx.cfg.gamma, threshold, keep_len);
+  count_launch(ctx);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_calibration(const Ctx& ctx, const CalArgs& a, cudaStream_t s) {
+  CalParams p{};
+  p.conf = a.conf;
+  p.accept_len = a.accept_len;
+  p.M = a.M;
+  p.gamma = a.gamma;
+  p.n_bins = a.n_bins;
+  p.acc = ctx.ws.cal_acc;
+  p.cnt = ctx.ws.cal_cnt;
+  p.ticket = ctx.ws.tickets + 2;
+  p.bins = a.bins;
+  p.pos = a.pos;
+  p.metrics = a.metrics;
+  p.status = ctx.ws.status;
+  int grid = (a.M + kCalThreads - 1) / kCalThreads;
+  grid = grid < 1 ? 1 : (grid > 2 * ctx.num_sms ? 2 * ctx.num_sms : grid);
+  calibration_kernel<<<grid, kCalThreads, 0, s>>>(p);
+  count_launch(ctx);
+  return cudaGetLastError();
+}
+
+}  // namespace dsd

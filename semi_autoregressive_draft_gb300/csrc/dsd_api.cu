@@ -5,6 +5,7 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <cmath>
 #include <new>
 
 #include "../../include/dsd.h"
@@ -64,6 +65,8 @@ size_t carve(dsd_ctx* c, unsigned char* base) {
   w.loss_parts2 = reinterpret_cast<float*>(take(sizeof(float) * c->num_sms * loss_rows));
   w.loss_ltgt = reinterpret_cast<float*>(take(sizeof(float) * loss_rows));
   w.loss_red = reinterpret_cast<double*>(take(sizeof(double) * 64 * 3));
+  w.cal_acc = reinterpret_cast<double*>(take(sizeof(double) * (2 * kMaxCalBins + 2 + 2 * kMaxGamma)));
+  w.cal_cnt = reinterpret_cast<unsigned long long*>(take(sizeof(unsigned long long) * (kMaxCalBins + 1)));
   if (base) c->ws = w;
   return off;
 }
@@ -494,6 +497,79 @@ int dsd_loss_forward(dsd_ctx* ctx, int B, const void* U, const void* E, const vo
   a.losses = losses;
   cudaError_t e = launch_loss(*ctx, a, s);
   if (e != cudaSuccess) return cuda_fail(ctx, e, "loss launch");
+  return DSD_OK;
+}
+
+int dsd_confidence_head(dsd_ctx* ctx, int R, int H, const void* h, const void* E, const void* w_c,
+                        float b_c, const int32_t* prev_tok, const int32_t* tokens, float* conf,
+                        float* survival, void* stream) {
+  int rc = check_ctx(ctx);
+  if (rc) return rc;
+  if (R < 0) return fail(ctx, DSD_ERR_ARG, "R = %d < 0", R);
+  if (H <= 0 || H % 8 != 0) return fail(ctx, DSD_ERR_ALIGN, "H = %d must be a positive multiple of 8", H);
+  if (!std::isfinite(b_c)) return fail(ctx, DSD_ERR_NONFINITE, "b_c is not finite");
+  if (R == 0) return DSD_OK;
+  if ((long long)R * ctx->cfg.gamma > 0x7fffffffLL) return fail(ctx, DSD_ERR_SHAPE, "R too large");
+  if ((rc = check_table(ctx, h, "h")) || (rc = check_table(ctx, E, "E")) ||
+      (rc = check_table(ctx, w_c, "w_c")))
+    return rc;
+  if (!prev_tok || !tokens || !conf || !survival)
+    return fail(ctx, DSD_ERR_ARG, "dsd_confidence_head: NULL argument");
+  ConfHeadArgs a{};
+  a.R = R;
+  a.H = H;
+  a.V = ctx->cfg.V;
+  a.rank = ctx->cfg.rank;
+  a.gamma = ctx->cfg.gamma;
+  a.dtype = ctx->cfg.dtype;
+  a.h = h;
+  a.E = E;
+  a.w_c = w_c;
+  a.b_c = b_c;
+  a.prev_tok = prev_tok;
+  a.tokens = tokens;
+  a.conf = conf;
+  a.survival = survival;
+  cudaError_t e = launch_confidence_head(*ctx, a, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "confidence head launch");
+  return DSD_OK;
+}
+
+int dsd_threshold_keep(dsd_ctx* ctx, int R, const float* conf, float threshold, int32_t* keep_len,
+                       void* stream) {
+  int rc = check_ctx(ctx);
+  if (rc) return rc;
+  if (R < 0) return fail(ctx, DSD_ERR_ARG, "R = %d < 0", R);
+  if (std::isnan(threshold)) return fail(ctx, DSD_ERR_NONFINITE, "threshold is NaN");
+  if (R == 0) return DSD_OK;
+  if (!conf || !keep_len) return fail(ctx, DSD_ERR_ARG, "dsd_threshold_keep: NULL argument");
+  cudaError_t e = launch_threshold_keep(*ctx, R, conf, threshold, keep_len,
+                                        static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "threshold launch");
+  return DSD_OK;
+}
+
+int dsd_calibration(dsd_ctx* ctx, int M, const float* conf, const int32_t* accept_len, int n_bins,
+                    float* bins, float* pos, float* metrics, void* stream) {
+  int rc = check_ctx(ctx);
+  if (rc) return rc;
+  if (M < 0) return fail(ctx, DSD_ERR_ARG, "M = %d < 0", M);
+  if (n_bins < 1 || n_bins > kMaxCalBins)
+    return fail(ctx, DSD_ERR_ARG, "n_bins = %d outside 1..%d", n_bins, kMaxCalBins);
+  if (!bins || !pos || !metrics) return fail(ctx, DSD_ERR_ARG, "dsd_calibration: NULL argument");
+  if (M > 0 && (!conf || !accept_len)) return fail(ctx, DSD_ERR_ARG, "dsd_calibration: NULL argument");
+  if ((long long)M * ctx->cfg.gamma > 0x7fffffffLL) return fail(ctx, DSD_ERR_SHAPE, "M too large");
+  CalArgs a{};
+  a.M = M;
+  a.gamma = ctx->cfg.gamma;
+  a.n_bins = n_bins;
+  a.conf = conf;
+  a.accept_len = accept_len;
+  a.bins = bins;
+  a.pos = pos;
+  a.metrics = metrics;
+  cudaError_t e = launch_calibration(*ctx, a, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "calibration launch");
   return DSD_OK;
 }
 

@@ -12,6 +12,7 @@ constexpr int kActNone = 0;
 constexpr int kActSilu = 1;
 
 constexpr int kMaxGamma = 16;
+constexpr int kMaxCalBins = 64;      // reliability bins of dsd_calibration
 constexpr int kMaxSchedItems = 4096;  // R_max * gamma
 constexpr int kVerifySplits = 8;      // V chunks per verified row
 
@@ -49,6 +50,8 @@ struct Workspace {
   float* loss_parts2;           // [num_sms][R_max*gamma] L1 partials of the loss
   float* loss_ltgt;             // [R_max*gamma] draft logit at the target token
   double* loss_red;             // [64][3] per-CTA sums of the loss finalize
+  double* cal_acc;              // [2 kMaxCalBins + 2 + 2 kMaxGamma] calibration sums (zero between calls)
+  unsigned long long* cal_cnt;  // [kMaxCalBins + 1] calibration counts (zero between calls)
 };
 
 struct Config {
@@ -131,6 +134,30 @@ struct OverlapArgs {
 };
 
 cudaError_t launch_overlap(const Ctx& ctx, const OverlapArgs& a, cudaStream_t s);
+
+struct ConfHeadArgs {
+  int R, H, V, rank, gamma, dtype;
+  const void* h;
+  const void* E;
+  const void* w_c;
+  float b_c;
+  const int32_t* prev_tok;
+  const int32_t* tokens;
+  float* conf;
+  float* survival;
+};
+cudaError_t launch_confidence_head(const Ctx& ctx, const ConfHeadArgs& a, cudaStream_t s);
+cudaError_t launch_threshold_keep(const Ctx& ctx, int R, const float* conf, float threshold,
+                                  int32_t* keep_len, cudaStream_t s);
+struct CalArgs {
+  int M, gamma, n_bins;
+  const float* conf;
+  const int32_t* accept_len;
+  float* bins;
+  float* pos;
+  float* metrics;
+};
+cudaError_t launch_calibration(const Ctx& ctx, const CalArgs& a, cudaStream_t s);
 
 struct LossArgs {
   int B, V, rank, gamma, bias_at_first;

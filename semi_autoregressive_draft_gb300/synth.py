@@ -29,6 +29,18 @@ the five workloads of the benchmark suite:
            forcing); P = U + N(0, sigma^2), sigma ~ U[0.2, 2] per block;
            E, W ~ N(0,0.02^2); conf_logit ~ N(0, 1.5^2).
 
+  confidence  R requests x 7 positions, hidden size H (2560 for the pages'
+           draft backbone), Markov rank r: h ~ N(0,1); w_c ~ N(0, 0.5^2 / H)
+           on the hidden part and N(0, 0.5^2 / r) / 0.02 on the Markov part
+           (so both halves move the logit by about 0.5); b_c = 1.2 (a mean
+           confidence near 0.77); E ~ N(0, 0.02^2); prev_tok and drafted
+           tokens uniform.
+  calibration  M requests x 7 positions: predicted per-step confidence
+           c ~ Beta(6,2) * 0.97^j; realised accept lengths drawn as the
+           leading successes of Bernoulli(max(0, c - 0.05)) chains (a head
+           that is 5 points optimistic, as in the paper-reading page's
+           example).
+
 P has gamma+1 rows per request: row gamma (the bonus row) is a fresh draw with
 U's recipe plus the same noise.  Big tensors are drawn with a seeded
 torch.Generator on the requested device; small ones (tokens, confidences,
@@ -295,3 +307,33 @@ __all__ = [
     "overlap_inputs", "loss_inputs", "overlap_valid_len", "sps_table", "to_numpy", "bytes_of",
     "QWEN3_VOCAB", "BLOCK", "MARKOV_RANK",
 ]
+
+
+def confidence_inputs(R: int, G: int, H: int, V: int, r: int, seed: int = 7,
+                      dtype: str = "bf16", device="cpu"):
+    """h [R,G,H], E [V,r], w_c [H+r] in dtype; b_c float; prev_tok [R],
+    tokens [R,G] i32 (see the module docstring)."""
+    rng = np.random.default_rng(seed)
+    td = _torch_dtype(dtype)
+    h = rng.standard_normal((R, G, H), dtype=np.float32)
+    E = (rng.standard_normal((V, r), dtype=np.float32) * 0.02).astype(np.float32)
+    w = np.concatenate([rng.standard_normal(H, dtype=np.float32) * (0.5 / np.sqrt(H)),
+                        rng.standard_normal(r, dtype=np.float32) * (0.5 / np.sqrt(r) / 0.02)])
+    prev_tok = rng.integers(0, V, size=R).astype(np.int32)
+    tokens = rng.integers(0, V, size=(R, G)).astype(np.int32)
+    to = lambda a: torch.as_tensor(a).to(device=device, dtype=td)
+    return dict(h=to(h), E=to(E), w_c=to(w.astype(np.float32)), b_c=1.2,
+                prev_tok=torch.as_tensor(prev_tok, device=device),
+                tokens=torch.as_tensor(tokens, device=device))
+
+
+def calibration_inputs(M: int, G: int, seed: int = 8, device="cpu"):
+    """conf [M,G] f32 predicted per-step confidences; accept_len [M] i32
+    (see the module docstring)."""
+    rng = np.random.default_rng(seed)
+    c = (rng.beta(6.0, 2.0, size=(M, G)) * 0.97 ** np.arange(G)).astype(np.float32)
+    u = rng.random((M, G))
+    ok = u < np.maximum(c.astype(np.float64) - 0.05, 0.0)
+    acc = np.where(ok.all(axis=1), G, np.argmin(ok, axis=1)).astype(np.int32)
+    return dict(conf=torch.as_tensor(c, device=device),
+                accept_len=torch.as_tensor(acc, device=device))
