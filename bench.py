@@ -39,6 +39,7 @@ KERNEL_SOURCES = {
     "propose_mma_kernel": ["propose_mma.cu", "dsd_common.cuh"],
     "verify_rows": ["verify.cu", "dsd_common.cuh"],
     "overlap_split": ["overlap.cu", "tc_common.cuh", "tc_ptx.cuh", "dsd_common.cuh"],
+    "confidence_head_kernel": ["confidence.cu", "dsd_common.cuh"],
     "loss_tc_kernel": ["loss_tc.cu", "tc_common.cuh", "tc_ptx.cuh", "dsd_common.cuh"],
 }
 FALLBACK_HBM_GBS = 6800.0
@@ -432,6 +433,81 @@ def run_loss(args, dsd, synth, dev, world):
     return line
 
 
+def run_confidence(args, dsd, synth, dev, world):
+    """The confidence side on the high-concurrency batch: the confidence head
+    on R=256 requests x gamma positions (hidden size 2560, rank 256, V=151936;
+    9.2 MB of hidden states, so L2 is flushed between steps outside the
+    events), timed alone; calibration of 1M requests is timed beside it."""
+    import torch
+
+    R, G, H, V, r = 256, 7, 2560, 151936, 256
+    x = synth.confidence_inputs(R, G, H, V, r, seed=7, dtype="bf16", device=dev)
+    cal = synth.calibration_inputs(1 << 20, G, seed=8, device=dev)
+    ctx = dsd.Context(V, r, G, R, dtype="bf16", device=dev.index)
+    stream = torch.cuda.Stream(device=dev)
+    flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    head_args = (x["h"], x["E"], x["w_c"], x["b_c"], x["prev_tok"], x["tokens"])
+    out = cout = None
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            out = ctx.confidence_head(*head_args, out=out, stream=stream)
+            cout = ctx.calibration(cal["conf"], cal["accept_len"], 10, out=cout, stream=stream)
+    stream.synchronize()
+    assert ctx.sync_status(stream) == 0
+    c0 = ctx.launch_count()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    clocks = ClockSampler(gpu_uuid(dev.index))
+    clocks.start()
+    time.sleep(0.3)
+    barrier(world)
+    with torch.cuda.stream(stream):
+        for e in evs:
+            flush.zero_()
+            e[0].record(stream)
+            out = ctx.confidence_head(*head_args, out=out, stream=stream)
+            e[1].record(stream)
+            flush.zero_()
+            e[2].record(stream)
+            cout = ctx.calibration(cal["conf"], cal["accept_len"], 10, out=cout, stream=stream)
+            e[3].record(stream)
+    stream.synchronize()
+    clk = clocks.stop()
+    assert ctx.sync_status(stream) == 0
+    launches = ctx.launch_count() - c0
+    ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
+    ms = max_over_ranks(ms, world, dev)
+    cal_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in evs)
+    rows = R * G
+    # per launch: every hidden row once, the Markov rows, w_c, tokens and outputs
+    alg = rows * H * 2 + rows * r * 2 + (H + r) * 2 + rows * 4 + R * 4 + 2 * rows * 4
+    cal_alg = (1 << 20) * G * 4 + (1 << 20) * 4
+    peak, peak_kind = hbm_peak()
+    achieved = alg / (ms / 1e3) / 1e9
+    line = {
+        "metric": f"confidence-head rows/s (sigmoid(w_c . [h; E[t_prev]] + b_c) and survival) "
+                  f"at R={R}, gamma={G}, H={H}, rank {r}",
+        "value": world * rows / (ms / 1e3), "unit": "rows/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "accumulate": "fp32 (fp64 survival)", "data": "synthetic",
+        "config": {"workload": f"confidence: R={R} gamma={G} H={H} V={V} rank={r} bf16",
+                   "l2": "flushed between steps (512 MB write outside the events); "
+                         "inputs 9.2 MB"},
+        "roofline": {"bound": "hbm", "kernel": "confidence_head_kernel", "achieved": achieved,
+                     "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)",
+                     "traffic": None, "alg_bytes": alg, "per": "one launch",
+                     "alg_bytes_note": "hidden rows + Markov rows + w_c + tokens + outputs"},
+        "calibration": {"requests": 1 << 20, "ms": cal_ms,
+                        "achieved_gbs": cal_alg / (cal_ms / 1e3) / 1e9,
+                        "frac": cal_alg / (cal_ms / 1e3) / 1e9 / peak},
+        "cpu_baseline": None, "e2e": None,
+        "gpu_launches": launches, "clocks": clk,
+    }
+    ctx.close()
+    return line
+
+
 def run_ours(args):
     import numpy as np
     import torch
@@ -450,8 +526,9 @@ def run_ours(args):
 
     if not os.path.exists(dsd.LIB_PATH):
         _build.build()
-    if args.workload in ("overlap", "loss"):
-        run = run_overlap if args.workload == "overlap" else run_loss
+    if args.workload in ("overlap", "loss", "confidence"):
+        run = {"overlap": run_overlap, "loss": run_loss,
+               "confidence": run_confidence}[args.workload]
         line = run(args, dsd, synth, dev, world)
         if rank == 0:
             print(json.dumps(line), flush=True)
@@ -656,7 +733,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="highconc",
-                    choices=["highconc", "greedy", "sampled", "tiny", "overlap", "loss"])
+                    choices=["highconc", "greedy", "sampled", "tiny", "overlap", "loss",
+                             "confidence"])
     ap.add_argument("--engine", default="auto", choices=["auto", "simt", "mma", "tcgen05"])
     ap.add_argument("--cpu-requests", type=int, default=128,
                     help="requests in the CPU-baseline sample")
@@ -669,7 +747,7 @@ def main(argv=None):
     args = ap.parse_args(argv)
     args.warmup = max(args.warmup, 3)   # at least 3 untimed warm-up steps
     if args.impl == "reference":
-        if args.workload in ("overlap", "loss"):
+        if args.workload in ("overlap", "loss", "confidence"):
             ap.error("the reference arm times the draft-verify cycle workloads")
         return run_reference(args)
     return run_ours(args)

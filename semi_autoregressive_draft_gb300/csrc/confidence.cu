@@ -9,10 +9,11 @@
 // "DSpark 论文精读", 3.1 (prefix survival a = prod c, why the
 // cumulative-product bias is monitored) and 5 (reliability diagram, ECE).
 //
-// confidence_head_kernel: one CTA per request, one warp per position: the
-//   dot products of the row's hidden state (H values) and of the Markov row
-//   of the previous token (rank values) with w_c, 16-byte loads, fp32 sums;
-//   then warp 0 forms c = sigmoid(s) and the survival prefix products in fp64.
+// confidence_head_kernel: one CTA per request, two warps per position: the
+//   dot products of the row's hidden state (H values, split over the two
+//   warps, four 16-byte loads in flight per lane) and of the Markov row of
+//   the previous token (rank values) with w_c, fp32 sums; then thread 0
+//   forms c = sigmoid(s) and the survival prefix products in fp64.
 // threshold_keep_kernel: one thread per request.
 // calibration_kernel: a grid-stride pass, one thread per request: survival
 //   in fp64, reliability bin floor(a n_bins) taken in fp64 (the oracle's
@@ -41,17 +42,36 @@ __device__ __forceinline__ int chunk_to_f32(uint4 q, float* x) {
 
 // sum over one warp's lanes of a[i] * b[i], i < n (n a multiple of the
 // elements per 16 bytes; both arrays 16-byte aligned)
+// The warp covers 16-byte chunks first, first + nw, first + 2 nw, ... of the
+// 32-chunk groups (nw warps share one dot product).
 template <typename T>
-__device__ __forceinline__ float warp_dot(const T* a, const T* b, int n, int lane) {
+__device__ __forceinline__ float warp_dot(const T* a, const T* b, int n, int lane, int first,
+                                          int nw) {
   constexpr int epc = 16 / (int)sizeof(T);
+  constexpr int kDepth = 4;   // 16-byte loads of each operand in flight per lane
+  const int step = nw * 32 * epc;
   float acc = 0.f;
-  for (int v = lane * epc; v < n; v += 32 * epc) {
-    float x[8], y[8];
-    const int k = chunk_to_f32<T>(ld_stream16(a + v), x);
-    chunk_to_f32<T>(__ldg(reinterpret_cast<const uint4*>(b + v)), y);
+  for (int v0 = (first * 32 + lane) * epc; v0 < n; v0 += kDepth * step) {
+    uint4 qa[kDepth], qb[kDepth];
 #pragma unroll
-    for (int e = 0; e < 8; ++e)
-      if (e < k) acc = fmaf(x[e], y[e], acc);
+    for (int d = 0; d < kDepth; ++d) {
+      const int v = v0 + d * step;
+      if (v < n) {
+        qa[d] = ld_stream16(a + v);
+        qb[d] = __ldg(reinterpret_cast<const uint4*>(b + v));
+      }
+    }
+#pragma unroll
+    for (int d = 0; d < kDepth; ++d) {
+      if (v0 + d * step < n) {
+        float x[8], y[8];
+        const int k = chunk_to_f32<T>(qa[d], x);
+        chunk_to_f32<T>(qb[d], y);
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+          if (e < k) acc = fmaf(x[e], y[e], acc);
+      }
+    }
   }
   return warp_sum(acc);
 }
@@ -62,28 +82,35 @@ __device__ __forceinline__ float sigmoid_f(float z) {
   return e / (1.f + e);
 }
 
+constexpr int kHeadWarps = 2;   // warps per position
+
 template <typename T>
-__global__ void __launch_bounds__(32 * kMaxGamma) confidence_head_kernel(
+__global__ void __launch_bounds__(32 * kHeadWarps * kMaxGamma) confidence_head_kernel(
     const T* __restrict__ h, const T* __restrict__ E, const T* __restrict__ w_c, float b_c,
     const int32_t* __restrict__ prev_tok, const int32_t* __restrict__ tokens, int H, int rank,
     int V, int gamma, float* conf, float* survival, int* status) {
-  __shared__ float s_logit[kMaxGamma];
-  const int r = blockIdx.x, j = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  __shared__ float s_part[kMaxGamma][kHeadWarps];
+  const int r = blockIdx.x, w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int j = w / kHeadWarps, half = w % kHeadWarps;
   if (j < gamma) {
-    int t = j == 0 ? prev_tok[r] : tokens[(size_t)r * gamma + j - 1];
-    if (t < 0 || t >= V) {
-      if (lane == 0) set_status(status, kErrArg);
-      t = 0;
+    float v = warp_dot<T>(h + ((size_t)r * gamma + j) * H, w_c, H, lane, half, kHeadWarps);
+    if (half == 0) {
+      int t = j == 0 ? prev_tok[r] : tokens[(size_t)r * gamma + j - 1];
+      if (t < 0 || t >= V) {
+        if (lane == 0) set_status(status, kErrArg);
+        t = 0;
+      }
+      v += warp_dot<T>(E + (size_t)t * rank, w_c + H, rank, lane, 0, 1);
     }
-    const float sh = warp_dot<T>(h + ((size_t)r * gamma + j) * H, w_c, H, lane);
-    const float sm = warp_dot<T>(E + (size_t)t * rank, w_c + H, rank, lane);
-    if (lane == 0) s_logit[j] = sh + sm + b_c;
+    if (lane == 0) s_part[j][half] = v;
   }
   __syncthreads();
   if (threadIdx.x == 0) {
     double acc = 1.0;
     for (int i = 0; i < gamma; ++i) {
-      float c = sigmoid_f(s_logit[i]);
+      float sl = b_c;
+      for (int k = 0; k < kHeadWarps; ++k) sl += s_part[i][k];
+      float c = sigmoid_f(sl);
       if (!isfinite(c)) {
         set_status(status, kErrNonfinite);
         c = 0.f;
@@ -120,83 +147,105 @@ struct CalParams {
   int* status;
 };
 
+// Values in [0, 1] are summed per CTA as integers in units of 2^-40 (exact
+// integer atomics in shared memory; the launch gives a CTA at most 2^22
+// values, below the 2^24 that would overflow 64 bits), then added to the
+// fp64 sums of the grid.  The rounding, 2^-41 per value, is far below fp32.
+constexpr double kFix = 1099511627776.0;   // 2^40
+
+__device__ __forceinline__ unsigned long long to_fix(double v) { return __double2ull_rn(v * kFix); }
+
 __global__ void __launch_bounds__(kCalThreads) calibration_kernel(CalParams p) {
-  __shared__ double sp[kMaxCalBins], sr[kMaxCalBins], spp[kMaxGamma], spr[kMaxGamma], se[2];
-  __shared__ unsigned long long sc[kMaxCalBins + 1];
+  __shared__ unsigned long long sc[kMaxCalBins], sp[kMaxCalBins], spp[kMaxGamma], se;
+  __shared__ unsigned int sr[kMaxCalBins], spr[kMaxGamma], st;
   __shared__ int am_last;
   const int tid = threadIdx.x;
   for (int i = tid; i < kMaxCalBins; i += kCalThreads) {
-    sp[i] = sr[i] = 0.0;
-    sc[i] = 0ull;
+    sc[i] = sp[i] = 0ull;
+    sr[i] = 0u;
   }
-  if (tid < kMaxGamma) spp[tid] = spr[tid] = 0.0;
-  if (tid < 2) se[tid] = 0.0;
-  if (tid == 0) sc[kMaxCalBins] = 0ull;
+  if (tid < kMaxGamma) {
+    spp[tid] = 0ull;
+    spr[tid] = 0u;
+  }
+  if (tid == 0) {
+    se = 0ull;
+    st = 0u;
+  }
   __syncthreads();
-  double err = 0.0, bias = 0.0, lp[kMaxGamma], lr[kMaxGamma];
-  for (int j = 0; j < kMaxGamma; ++j) lp[j] = lr[j] = 0.0;
-  unsigned long long tested = 0ull;
-  for (int r = blockIdx.x * kCalThreads + tid; r < p.M; r += gridDim.x * kCalThreads) {
-    int L = p.accept_len[r];
+  unsigned long long err = 0ull, lp[kMaxGamma];
+  unsigned int tested = 0u, lr[kMaxGamma];
+  for (int j = 0; j < kMaxGamma; ++j) {
+    lp[j] = 0ull;
+    lr[j] = 0u;
+  }
+  // Every lane of a warp runs the same iterations (lanes past M take part
+  // with bin -1), so the bin updates can be combined per warp: lanes with
+  // the same bin add their counts and sums and one of them does the atomics.
+  const int lane = tid & 31;
+  for (int r0 = blockIdx.x * kCalThreads; r0 < p.M; r0 += gridDim.x * kCalThreads) {
+    const int r = r0 + tid;
+    const bool live = r < p.M;
+    int L = live ? p.accept_len[r] : 0;
     if (L < 0 || L > p.gamma) {
       set_status(p.status, kErrArg);
       L = L < 0 ? 0 : p.gamma;
     }
     double a = 1.0;
     for (int j = 0; j < p.gamma; ++j) {
-      float cf = p.conf[(size_t)r * p.gamma + j];
+      float cf = live ? p.conf[(size_t)r * p.gamma + j] : 0.f;
       if (!isfinite(cf)) {
         set_status(p.status, kErrNonfinite);
         cf = 0.f;
       }
       const double c = (double)fminf(fmaxf(cf, 0.f), 1.f);
       a *= c;
-      const double y = j < L ? 1.0 : 0.0;
-      if (j <= L) {
-        err += fabs(c - y);
-        ++tested;
+      const unsigned int y = (live && j < L) ? 1u : 0u;
+      const unsigned long long qa = live ? to_fix(a) : 0ull;
+      if (live) {
+        if (j <= L) {
+          err += to_fix(fabs(c - (double)y));
+          ++tested;
+        }
+        lp[j] += qa;
+        lr[j] += y;
       }
-      bias += a - y;
-      lp[j] += a;
-      lr[j] += y;
       int b = (int)floor(a * (double)p.n_bins);
-      b = b < p.n_bins - 1 ? b : p.n_bins - 1;
-      atomicAdd(&sc[b], 1ull);
-      atomicAdd(&sp[b], a);
-      atomicAdd(&sr[b], y);
+      b = !live ? -1 : (b < p.n_bins - 1 ? b : p.n_bins - 1);
+      const unsigned peers = __match_any_sync(0xffffffffu, b);
+      const unsigned n = __popc(peers);
+      const unsigned ys = __reduce_add_sync(peers, y);
+      const unsigned lo = __reduce_add_sync(peers, (unsigned)(qa & 0xFFFFFull));
+      const unsigned hi = __reduce_add_sync(peers, (unsigned)(qa >> 20));
+      if (b >= 0 && lane == __ffs(peers) - 1) {
+        atomicAdd(&sc[b], (unsigned long long)n);
+        atomicAdd(&sp[b], ((unsigned long long)hi << 20) + lo);
+        if (ys) atomicAdd(&sr[b], ys);
+      }
     }
   }
   for (int j = 0; j < p.gamma; ++j) {
-    const double a = warp_sum_f64(lp[j]), y = warp_sum_f64(lr[j]);
-    if ((tid & 31) == 0) {
-      atomicAdd(&spp[j], a);
-      atomicAdd(&spr[j], y);
-    }
+    if (lp[j]) atomicAdd(&spp[j], lp[j]);
+    if (lr[j]) atomicAdd(&spr[j], lr[j]);
   }
-  err = warp_sum_f64(err);
-  bias = warp_sum_f64(bias);
-  if ((tid & 31) == 0) {
-    atomicAdd(&se[0], err);
-    atomicAdd(&se[1], bias);
-  }
-  atomicAdd(&sc[kMaxCalBins], tested);
+  if (err) atomicAdd(&se, err);
+  if (tested) atomicAdd(&st, tested);
   __syncthreads();
-  // this CTA's sums into the global ones
+  // this CTA's sums into the grid's
   for (int i = tid; i < p.n_bins; i += kCalThreads) {
     if (sc[i]) {
       atomicAdd(&p.cnt[i], sc[i]);
-      atomicAdd(&p.acc[i], sp[i]);
-      atomicAdd(&p.acc[kMaxCalBins + i], sr[i]);
+      atomicAdd(&p.acc[i], (double)sp[i] / kFix);
+      atomicAdd(&p.acc[kMaxCalBins + i], (double)sr[i]);
     }
   }
   if (tid < p.gamma) {
-    atomicAdd(&p.acc[2 * kMaxCalBins + 2 + tid], spp[tid]);
-    atomicAdd(&p.acc[2 * kMaxCalBins + 2 + kMaxGamma + tid], spr[tid]);
+    atomicAdd(&p.acc[2 * kMaxCalBins + 2 + tid], (double)spp[tid] / kFix);
+    atomicAdd(&p.acc[2 * kMaxCalBins + 2 + kMaxGamma + tid], (double)spr[tid]);
   }
   if (tid == 0) {
-    atomicAdd(&p.acc[2 * kMaxCalBins], se[0]);
-    atomicAdd(&p.acc[2 * kMaxCalBins + 1], se[1]);
-    atomicAdd(&p.cnt[kMaxCalBins], sc[kMaxCalBins]);
+    atomicAdd(&p.acc[2 * kMaxCalBins], (double)se / kFix);
+    atomicAdd(&p.cnt[kMaxCalBins], (unsigned long long)st);
   }
   __threadfence();
   __syncthreads();
@@ -218,8 +267,10 @@ __global__ void __launch_bounds__(kCalThreads) calibration_kernel(CalParams p) {
     p.acc[b] = 0.0;
     p.acc[kMaxCalBins + b] = 0.0;
   }
+  double bias_sum = 0.0;   // sum of (a - y) over all positions
   for (int j = 0; j < p.gamma; ++j) {
     double* a = p.acc + 2 * kMaxCalBins + 2;
+    bias_sum += __ldcg(&a[j]) - __ldcg(&a[kMaxGamma + j]);
     p.pos[j] = p.M ? (float)(__ldcg(&a[j]) / p.M) : 0.f;
     p.pos[p.gamma + j] = p.M ? (float)(__ldcg(&a[kMaxGamma + j]) / p.M) : 0.f;
     a[j] = a[kMaxGamma + j] = 0.0;
@@ -227,7 +278,7 @@ __global__ void __launch_bounds__(kCalThreads) calibration_kernel(CalParams p) {
   const unsigned long long nt = __ldcg(&p.cnt[kMaxCalBins]);
   p.metrics[0] = p.M ? (float)ece : 0.f;
   p.metrics[1] = nt ? (float)(__ldcg(&p.acc[2 * kMaxCalBins]) / (double)nt) : 0.f;
-  p.metrics[2] = p.M ? (float)(__ldcg(&p.acc[2 * kMaxCalBins + 1]) / total) : 0.f;
+  p.metrics[2] = p.M ? (float)(bias_sum / total) : 0.f;
   p.metrics[3] = (float)nt;
   p.acc[2 * kMaxCalBins] = p.acc[2 * kMaxCalBins + 1] = 0.0;
   p.cnt[kMaxCalBins] = 0ull;
@@ -237,7 +288,7 @@ __global__ void __launch_bounds__(kCalThreads) calibration_kernel(CalParams p) {
 
 cudaError_t launch_confidence_head(const Ctx& ctx, const ConfHeadArgs& a, cudaStream_t s) {
   if (a.R == 0) return cudaSuccess;
-  const dim3 grid(a.R), block(32 * a.gamma);
+  const dim3 grid(a.R), block(32 * kHeadWarps * a.gamma);
   if (a.dtype == 1)
     confidence_head_kernel<__nv_bfloat16><<<grid, block, 0, s>>>(
         static_cast<const __nv_bfloat16*>(a.h), static_cast<const __nv_bfloat16*>(a.E),
@@ -276,6 +327,9 @@ cudaError_t launch_calibration(const Ctx& ctx, const CalArgs& a, cudaStream_t s)
   p.status = ctx.ws.status;
   int grid = (a.M + kCalThreads - 1) / kCalThreads;
   grid = grid < 1 ? 1 : (grid > 2 * ctx.num_sms ? 2 * ctx.num_sms : grid);
+  // at most 2^22 values per CTA, so its 2^-40 fixed-point sums cannot overflow
+  const long long min_grid = ((long long)a.M * a.gamma + (1 << 22) - 1) >> 22;
+  if (grid < min_grid) grid = (int)min_grid;
   calibration_kernel<<<grid, kCalThreads, 0, s>>>(p);
   count_launch(ctx);
   return cudaGetLastError();
