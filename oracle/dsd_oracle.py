@@ -192,13 +192,37 @@ def survival(conf):
 # logit bias v), i.e. b[v] = sum_k W[v, k] * m[k].
 # ---------------------------------------------------------------------------
 
-def markov_bias(E, W, prev: int, act: str = "none"):
+def markov_rep(E, prev: int, act: str = "none"):
+    """m = act(E[prev]): the Markov representation of the previous token."""
     m = _f64(E[prev])
     if act == "silu":
         m = m / (1.0 + np.exp(-m))
     elif act != "none":
         raise ValueError(act)
-    return _f64(W) @ m
+    return m
+
+
+def markov_bias(E, W, prev: int, act: str = "none"):
+    return _f64(W) @ markov_rep(E, prev, act)
+
+
+def gated_rep(E, W_g, h, prev: int, act: str = "none"):
+    """The gated Markov head's representation ([READ] 2.3, GatedMarkovHead):
+        m = act(E[prev]),  g = sigmoid(W_g [h; m]),  returns g * m
+    W_g is [rank, H + rank] (the hidden-state columns first), h the backbone
+    hidden state of this position [H]; the bias is then W (g * m)."""
+    m = markov_rep(E, prev, act)
+    z = _f64(W_g) @ np.concatenate([_f64(h), m])
+    g = np.array([sigmoid(v) for v in z])
+    return g * m
+
+
+def head_bias(E, W, prev: int, act="none", gate=None, r=0, j=0):
+    """Bias of the vanilla head (gate None) or of the gated head, gate =
+    dict(h=[R, gamma, H], W_g=[rank, H + rank]) at request r, position j."""
+    if gate is None:
+        return markov_bias(E, W, prev, act)
+    return _f64(W) @ gated_rep(E, gate["W_g"], np.asarray(gate["h"])[r, j], prev, act)
 
 
 # ---------------------------------------------------------------------------
@@ -206,7 +230,7 @@ def markov_bias(E, W, prev: int, act: str = "none"):
 # ---------------------------------------------------------------------------
 
 def propose(U, E, W, conf, prev_tok, req_id=None, temperature=0.0, seed=0,
-            bias_at_first=True, act="none"):
+            bias_at_first=True, act="none", gate=None):
     """Sequential Markov-head proposal for a batch of R requests.
 
     For each request r and position j = 0..gamma-1:
@@ -233,7 +257,7 @@ def propose(U, E, W, conf, prev_tok, req_id=None, temperature=0.0, seed=0,
         for j in range(G):
             ell = _f64(U[r, j])
             if j > 0 or bias_at_first:
-                ell = ell + markov_bias(E, W, prev, act)
+                ell = ell + head_bias(E, W, prev, act, gate, r, j)
             if T == 0.0:
                 z = ell
                 lse_q[r, j] = logsumexp(ell)
@@ -303,16 +327,16 @@ def schedule(a, sps):
 # a6/a7: target verification  ([WALK] 4.4; [READ] 2.1, 3.1)
 # ---------------------------------------------------------------------------
 
-def _draft_logits(U, E, W, prev_tok, tokens, r, t, bias_at_first, act):
+def _draft_logits(U, E, W, prev_tok, tokens, r, t, bias_at_first, act, gate=None):
     ell = _f64(U[r, t])
     prev = int(prev_tok[r]) if t == 0 else int(tokens[r, t - 1])
     if t > 0 or bias_at_first:
-        ell = ell + markov_bias(E, W, prev, act)
+        ell = ell + head_bias(E, W, prev, act, gate, r, t)
     return ell
 
 
 def verify(P, U, E, W, prev_tok, tokens, keep_len, req_id=None,
-           temperature=0.0, seed=0, bias_at_first=True, act="none"):
+           temperature=0.0, seed=0, bias_at_first=True, act="none", gate=None):
     """Rejection verification of the kept prefix of every request.
 
     P is [R, gamma+1, V]: row t scores draft token x_t, row keep_len[r] gives
@@ -353,7 +377,7 @@ def verify(P, U, E, W, prev_tok, tokens, keep_len, req_id=None,
             else:
                 p = softmax(_f64(P[r, t]) / T)
                 q = softmax(_draft_logits(U, E, W, prev_tok, tokens, r, t,
-                                          bias_at_first, act) / T)
+                                          bias_at_first, act, gate) / T)
                 accept_prob = min(1.0, p[x] / q[x])
                 u = accept_uniform(seed, t, req)
                 accept_gap[r] = min(accept_gap[r], abs(u - accept_prob))
@@ -509,14 +533,14 @@ def loss_forward(U, E, W, prev_tokens, P, target_tokens, conf_logits,
 # ---------------------------------------------------------------------------
 
 def cycle(U, E, W, conf, prev_tok, P, sps, req_id=None, temperature=0.0,
-          seed=0, bias_at_first=True, act="none", keep_len=None):
+          seed=0, bias_at_first=True, act="none", keep_len=None, gate=None):
     prop = propose(U, E, W, conf, prev_tok, req_id, temperature, seed,
-                   bias_at_first, act)
+                   bias_at_first, act, gate)
     a32 = prop["survival"].astype(np.float32)       # the schedule's input type
     sch = schedule(a32, sps)
     kl = sch["keep_len"] if keep_len is None else np.asarray(keep_len)
     ver = verify(P, U, E, W, prev_tok, prop["tokens"], kl, req_id,
-                 temperature, seed, bias_at_first, act)
+                 temperature, seed, bias_at_first, act, gate)
     return dict(propose=prop, schedule=sch, verify=ver, keep_len=kl)
 
 

@@ -626,3 +626,54 @@ def test_calibration_perfect_and_edges():
     assert list(out["count"]) == [2, 0, 0, 0, 1]
     assert out["n_tested"] == 2 and out["abs_error"] == 0.0
     assert abs(out["ece"] - 0.0) < 1e-15
+
+
+# ---------------------------------------------------------------------------
+# Gated Markov head ([READ] 2.3 GatedMarkovHead: g = sigmoid(W_g [h; m]),
+# b = W_up (g * m))
+# ---------------------------------------------------------------------------
+
+def test_gated_head_by_hand():
+    # rank 2, H = 1, V = 3; previous token 1 with E[1] = (1, -2), h = (3)
+    E = np.array([[0.0, 0.0], [1.0, -2.0], [5.0, 5.0]])
+    W = np.array([[1.0, 0.0], [0.0, 1.0], [2.0, 1.0]])         # [V, rank]
+    W_g = np.array([[1.0, 0.0, 0.0],                           # z_0 = h = 3
+                    [0.0, 0.0, 1.0]])                          # z_1 = m_1 = -2
+    gm = O.gated_rep(E, W_g, np.array([3.0]), 1)
+    s3, sm2 = 1.0 / (1.0 + np.exp(-3.0)), 1.0 / (1.0 + np.exp(2.0))
+    assert np.allclose(gm, [s3 * 1.0, sm2 * -2.0], rtol=1e-14)
+    b = O.head_bias(E, W, 1, gate=dict(h=np.array([[[3.0]]]), W_g=W_g), r=0, j=0)
+    assert np.allclose(b, [s3, -2.0 * sm2, 2.0 * s3 - 2.0 * sm2], rtol=1e-14)
+
+
+def test_gated_head_limits():
+    rng = np.random.default_rng(3)
+    V, r, H = 40, 8, 5
+    E = rng.normal(0, 1, (V, r))
+    W = rng.normal(0, 1, (V, r))
+    h = rng.normal(0, 1, (1, 1, H))
+    zero = dict(h=h, W_g=np.zeros((r, H + r)))
+    # a zero gate matrix opens every gate half way: half the vanilla bias
+    assert np.allclose(O.head_bias(E, W, 7, gate=zero), 0.5 * O.markov_bias(E, W, 7), rtol=1e-13)
+    # a constant hidden unit with a large weight saturates the gates
+    hc = np.ones((1, 1, H))
+    Wg = np.zeros((r, H + r))
+    Wg[:, 0] = 60.0
+    assert np.allclose(O.head_bias(E, W, 7, gate=dict(h=hc, W_g=Wg)),
+                       O.markov_bias(E, W, 7), rtol=1e-12, atol=1e-12)
+    Wg[:, 0] = -60.0
+    assert np.max(np.abs(O.head_bias(E, W, 7, gate=dict(h=hc, W_g=Wg)))) < 1e-20
+
+
+def test_gated_propose_single_step_by_hand():
+    # gamma = 1: x = argmax(U_0 + W (g * m)) with m = E[prev]
+    E = np.array([[0.0, 0.0], [1.0, -2.0], [5.0, 5.0]])
+    W = np.array([[1.0, 0.0], [0.0, 1.0], [2.0, 1.0]])
+    W_g = np.array([[1.0, 0.0, 0.0], [0.0, 0.0, 1.0]])
+    h = np.array([[[3.0]]])
+    U = np.array([[[0.5, 0.0, 0.0]]])
+    out = O.propose(U, E, W, np.array([[0.9]]), [1], gate=dict(h=h, W_g=W_g))
+    s3, sm2 = 1.0 / (1.0 + np.exp(-3.0)), 1.0 / (1.0 + np.exp(2.0))
+    ell = [0.5 + s3, -2.0 * sm2, 2.0 * s3 - 2.0 * sm2]   # 1.4526, -0.2384, 1.6670
+    assert int(out["tokens"][0, 0]) == int(np.argmax(ell)) == 2
+    assert abs(out["logit_at_tok"][0, 0] - ell[2]) < 1e-14
