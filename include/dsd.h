@@ -17,6 +17,7 @@
  * ([READ] 4.1; [WALK] 3.4).  dsd_confidence_head, dsd_threshold_keep and
  * dsd_calibration cover the scheduler's input: the confidence head, the
  * static truncation it replaces, and the calibration of its survivals.
+ * dsd_propose_gated / dsd_verify_gated run the gated Markov head.
  *
  * Conventions for every call below.
  *   - Tensor arguments are DEVICE pointers owned by the caller, row-major and
@@ -302,6 +303,41 @@ int dsd_loss_forward(dsd_ctx* ctx, int B, const void* U, const void* E, const vo
                      const int32_t* prev_tok, const void* P, const int32_t* target,
                      const float* conf_logit, float ce_alpha, float l1_alpha, float conf_alpha,
                      float decay, float* row_out, float* losses, void* stream);
+
+/*
+ * dsd_propose_gated -- dsd_propose with the gated Markov head ([READ] 2.3,
+ * GatedMarkovHead; [NOTES] 2.3):
+ *   m_j = act(E[x_{j-1}]),  g_j = sigmoid(W_g [h_j; m_j]),
+ *   l_j = U_j + W (g_j * m_j)
+ * and the same greedy / Gumbel selection, lse_q, logit_at_tok and survival
+ * as dsd_propose.  h [R, gamma, H] (the backbone hidden states) and W_g
+ * [rank, H + rank] (hidden-state columns first) in the context's dtype,
+ * device, 16-byte aligned; H a positive multiple of 8.  gated_rep
+ * [R, gamma, rank] f32 out: g_j * m_j per position (0 at position 0 when the
+ * context has bias_at_first = 0); dsd_verify_gated reads it.  Runs on the
+ * CUDA-core engine whatever the context's engine: one launch for the
+ * hidden-state part of every gate, then per draft position a gate launch and
+ * a bias launch, then the finalize.  Errors as dsd_propose; a non-finite gate
+ * argument sets DSD_ERR_NONFINITE.
+ */
+int dsd_propose_gated(dsd_ctx* ctx, int R, const void* U, const void* E, const void* W,
+                      const void* h, int H, const void* W_g, const float* conf,
+                      const int32_t* prev_tok, const uint32_t* req_id, float temperature,
+                      uint64_t seed, int32_t* tokens, float* lse_q, float* logit_at_tok,
+                      float* survival, float* gated_rep, void* stream);
+
+/*
+ * dsd_verify_gated -- dsd_verify for proposals of dsd_propose_gated: the
+ * rejected position's draft distribution is recomputed with the gated
+ * representation gated_rep [R, gamma, rank] f32 (as written by
+ * dsd_propose_gated) in place of act(E[prev]).  Same arguments, outputs and
+ * errors as dsd_verify otherwise; gated_rep may be NULL when temperature = 0.
+ */
+int dsd_verify_gated(dsd_ctx* ctx, int R, const void* P, const void* U, const void* E,
+                     const void* W, const float* gated_rep, const int32_t* prev_tok,
+                     const int32_t* tokens, const float* lse_q, const float* logit_at_tok,
+                     const int32_t* keep_len, const uint32_t* req_id, float temperature,
+                     uint64_t seed, int32_t* accept_len, int32_t* next_token, void* stream);
 
 /*
  * dsd_confidence_head -- per-position confidence of the drafted tokens

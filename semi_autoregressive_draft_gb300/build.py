@@ -31,6 +31,7 @@ SOURCES = [
     "overlap.cu",
     "loss_tc.cu",
     "confidence.cu",
+    "gated.cu",
 ]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",

@@ -67,6 +67,7 @@ size_t carve(dsd_ctx* c, unsigned char* base) {
   w.loss_red = reinterpret_cast<double*>(take(sizeof(double) * 64 * 3));
   w.cal_acc = reinterpret_cast<double*>(take(sizeof(double) * (2 * kMaxCalBins + 2 + 2 * kMaxGamma)));
   w.cal_cnt = reinterpret_cast<unsigned long long*>(take(sizeof(unsigned long long) * (kMaxCalBins + 1)));
+  w.gate_zh = reinterpret_cast<float*>(take(sizeof(float) * (size_t)Rm * G * c->cfg.rank));
   if (base) c->ws = w;
   return off;
 }
@@ -285,11 +286,12 @@ int dsd_schedule(dsd_ctx* ctx, int R, const float* survival, const float* sps, i
   return DSD_OK;
 }
 
-int dsd_verify(dsd_ctx* ctx, int R, const void* P, const void* U, const void* E, const void* W,
-               const int32_t* prev_tok, const int32_t* tokens, const float* lse_q,
-               const float* logit_at_tok, const int32_t* keep_len, const uint32_t* req_id,
-               float temperature, uint64_t seed, int32_t* accept_len, int32_t* next_token,
-               void* stream) {
+static int verify_impl(dsd_ctx* ctx, int R, const void* P, const void* U, const void* E,
+                       const void* W, const int32_t* prev_tok, const int32_t* tokens,
+                       const float* lse_q, const float* logit_at_tok, const int32_t* keep_len,
+                       const uint32_t* req_id, float temperature, uint64_t seed,
+                       int32_t* accept_len, int32_t* next_token, const float* gated_rep,
+                       void* stream) {
   int rc = check_ctx(ctx);
   if (rc) return rc;
   if ((rc = check_R(ctx, R))) return rc;
@@ -327,8 +329,81 @@ int dsd_verify(dsd_ctx* ctx, int R, const void* P, const void* U, const void* E,
   a.seed = seed;
   a.accept_len = accept_len;
   a.next_token = next_token;
+  a.gated_rep = gated_rep;
   cudaError_t e = launch_verify(*ctx, a, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(ctx, e, "verify launch");
+  return DSD_OK;
+}
+
+int dsd_verify(dsd_ctx* ctx, int R, const void* P, const void* U, const void* E, const void* W,
+               const int32_t* prev_tok, const int32_t* tokens, const float* lse_q,
+               const float* logit_at_tok, const int32_t* keep_len, const uint32_t* req_id,
+               float temperature, uint64_t seed, int32_t* accept_len, int32_t* next_token,
+               void* stream) {
+  return verify_impl(ctx, R, P, U, E, W, prev_tok, tokens, lse_q, logit_at_tok, keep_len, req_id,
+                     temperature, seed, accept_len, next_token, nullptr, stream);
+}
+
+int dsd_verify_gated(dsd_ctx* ctx, int R, const void* P, const void* U, const void* E,
+                     const void* W, const float* gated_rep, const int32_t* prev_tok,
+                     const int32_t* tokens, const float* lse_q, const float* logit_at_tok,
+                     const int32_t* keep_len, const uint32_t* req_id, float temperature,
+                     uint64_t seed, int32_t* accept_len, int32_t* next_token, void* stream) {
+  int rc = check_ctx(ctx);
+  if (rc) return rc;
+  if (R > 0 && temperature > 0.f && !gated_rep)
+    return fail(ctx, DSD_ERR_ARG, "dsd_verify_gated: gated_rep is NULL");
+  return verify_impl(ctx, R, P, U, E, W, prev_tok, tokens, lse_q, logit_at_tok, keep_len, req_id,
+                     temperature, seed, accept_len, next_token, gated_rep, stream);
+}
+
+int dsd_propose_gated(dsd_ctx* ctx, int R, const void* U, const void* E, const void* W,
+                      const void* h, int H, const void* W_g, const float* conf,
+                      const int32_t* prev_tok, const uint32_t* req_id, float temperature,
+                      uint64_t seed, int32_t* tokens, float* lse_q, float* logit_at_tok,
+                      float* survival, float* gated_rep, void* stream) {
+  int rc = check_ctx(ctx);
+  if (rc) return rc;
+  if ((rc = check_R(ctx, R))) return rc;
+  if ((rc = check_temperature(ctx, temperature))) return rc;
+  if (H <= 0 || H % 8 != 0) return fail(ctx, DSD_ERR_ALIGN, "H = %d must be a positive multiple of 8", H);
+  if (R == 0) return DSD_OK;
+  if ((rc = check_table(ctx, U, "U")) || (rc = check_table(ctx, E, "E")) ||
+      (rc = check_table(ctx, W, "W")) || (rc = check_table(ctx, h, "h")) ||
+      (rc = check_table(ctx, W_g, "W_g")))
+    return rc;
+  if (!conf || !prev_tok || !tokens || !lse_q || !logit_at_tok || !survival || !gated_rep)
+    return fail(ctx, DSD_ERR_ARG, "dsd_propose_gated: NULL argument");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  ProposeArgs a{};
+  a.R = R;
+  a.V = ctx->cfg.V;
+  a.rank = ctx->cfg.rank;
+  a.gamma = ctx->cfg.gamma;
+  a.dtype = ctx->cfg.dtype;
+  a.act = ctx->cfg.act;
+  a.bias_at_first = ctx->cfg.bias_at_first;
+  a.U = U;
+  a.E = E;
+  a.W = W;
+  a.conf = conf;
+  a.prev_tok = prev_tok;
+  a.req_id = req_id;
+  a.temperature = temperature;
+  a.seed = seed;
+  a.tokens = tokens;
+  a.lse_q = lse_q;
+  a.logit_at_tok = logit_at_tok;
+  a.survival = survival;
+  a.gate_h = h;
+  a.W_g = W_g;
+  a.H = H;
+  a.gated_rep = gated_rep;
+  cudaError_t e = launch_propose_simt(*ctx, a, s);
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "gated propose launch");
+  ctx->last_engine = DSD_ENGINE_SIMT;
+  e = launch_propose_finalize_n(*ctx, a, simt_grid(*ctx, a.V), s);
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "propose finalize launch");
   return DSD_OK;
 }
 

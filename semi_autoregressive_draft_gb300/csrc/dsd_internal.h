@@ -52,6 +52,7 @@ struct Workspace {
   double* loss_red;             // [64][3] per-CTA sums of the loss finalize
   double* cal_acc;              // [2 kMaxCalBins + 2 + 2 kMaxGamma] calibration sums (zero between calls)
   unsigned long long* cal_cnt;  // [kMaxCalBins + 1] calibration counts (zero between calls)
+  float* gate_zh;               // [R_max * gamma][rank] hidden-state part of the gated head's gate
 };
 
 struct Config {
@@ -90,9 +91,16 @@ struct ProposeArgs {
   float* lse_q;
   float* logit_at_tok;
   float* survival;
+  // gated Markov head (gate_h == nullptr: the plain head)
+  const void* gate_h;   // [R, gamma, H] backbone hidden states
+  const void* W_g;      // [rank, H + rank]
+  int H;
+  float* gated_rep;     // [R, gamma, rank] f32 out: g * m per position
 };
 
 cudaError_t launch_propose_simt(const Ctx& ctx, const ProposeArgs& a, cudaStream_t s);
+cudaError_t launch_gate_h(const Ctx& ctx, const ProposeArgs& a, cudaStream_t s);
+cudaError_t launch_gate_step(const Ctx& ctx, const ProposeArgs& a, int j, cudaStream_t s);
 cudaError_t launch_propose_tc(const Ctx& ctx, const ProposeArgs& a, cudaStream_t s);
 cudaError_t launch_propose_mma(const Ctx& ctx, const ProposeArgs& a, cudaStream_t s);
 int mma_vranges(const Ctx& ctx, int R);
@@ -103,6 +111,7 @@ cudaError_t launch_schedule(const Ctx& ctx, int R, const float* survival, const 
 
 struct VerifyArgs {
   int R, V, rank, gamma, dtype, act, bias_at_first;
+  const float* gated_rep;   // gated head: [R, gamma, rank] representations (else nullptr)
   const void* P;
   const void* U;
   const void* E;

@@ -1,0 +1,184 @@
+// Gated Markov head ("DSpark 论文精读" 2.3, GatedMarkovHead):
+//     m_j = act(E[x_{j-1}]),  g_j = sigmoid(W_g [h_j; m_j]),  b_j = W (g_j * m_j)
+// W_g is [rank, H + rank], its hidden-state columns first.
+//
+// The gate's argument splits into a part that does not depend on the drafted
+// tokens, W_g[:, :H] h_j, and one that does, W_g[:, H:] m_j.  The first is
+// one dense product for all positions of the batch before the sequential
+// stage (gate_h_kernel, [R gamma, H] x [H, rank] on CUDA cores, 64 x 64
+// output tiles); the second is a [rank, rank] matrix-vector product per
+// request at each draft step (gate_step_kernel, one CTA per request, one warp
+// per output row at a time, 16-byte loads of W_g), which writes the gated
+// representation g * m.  The CUDA-core bias kernel then reads that
+// representation instead of gathering rows of E, and so does the verifier's
+// residual pass.
+#include "dsd_common.cuh"
+
+namespace dsd {
+
+namespace {
+
+constexpr int kGhBM = 64, kGhBN = 64, kGhBK = 32, kGhThreads = 256;
+
+template <typename T>
+__device__ __forceinline__ void load8(const T* p, float* x) {
+  const uint4 q = __ldg(reinterpret_cast<const uint4*>(p));
+  if constexpr (sizeof(T) == 2) {
+    x[0] = bf16lo(q.x); x[1] = bf16hi(q.x); x[2] = bf16lo(q.y); x[3] = bf16hi(q.y);
+    x[4] = bf16lo(q.z); x[5] = bf16hi(q.z); x[6] = bf16lo(q.w); x[7] = bf16hi(q.w);
+  } else {
+    const uint4 q2 = __ldg(reinterpret_cast<const uint4*>(p) + 1);
+    x[0] = __uint_as_float(q.x); x[1] = __uint_as_float(q.y);
+    x[2] = __uint_as_float(q.z); x[3] = __uint_as_float(q.w);
+    x[4] = __uint_as_float(q2.x); x[5] = __uint_as_float(q2.y);
+    x[6] = __uint_as_float(q2.z); x[7] = __uint_as_float(q2.w);
+  }
+}
+
+// Zh[n, k] = sum_{c < H} h[n, c] W_g[k, c] for n < rows, k < rank.  H and
+// rank are multiples of 8; a group of eight consecutive c is either wholly
+// inside H or wholly outside.
+template <typename T>
+__global__ void __launch_bounds__(kGhThreads) gate_h_kernel(const T* __restrict__ h,
+                                                            const T* __restrict__ W_g, int rows,
+                                                            int H, int rank, float* Zh) {
+  __shared__ __align__(16) float As[kGhBK][kGhBM + 4];
+  __shared__ __align__(16) float Bs[kGhBK][kGhBN + 4];
+  const int tid = threadIdx.x;
+  const int n0 = blockIdx.y * kGhBM, k0 = blockIdx.x * kGhBN;
+  const int tm = (tid / 16) * 4, tn = (tid % 16) * 4;   // this thread's 4 x 4 outputs
+  float acc[4][4] = {};
+  // loader: one group of 8 K-values of one row of A and of B per thread
+  const int lr = tid / 4, lc = (tid % 4) * 8;
+  for (int c0 = 0; c0 < H; c0 += kGhBK) {
+    float xa[8], xb[8];
+    const int c = c0 + lc;
+    const int na = n0 + lr, kb = k0 + lr;
+    if (c < H && na < rows) load8<T>(h + (size_t)na * H + c, xa);
+    else for (int e = 0; e < 8; ++e) xa[e] = 0.f;
+    if (c < H && kb < rank) load8<T>(W_g + (size_t)kb * (H + rank) + c, xb);
+    else for (int e = 0; e < 8; ++e) xb[e] = 0.f;
+    __syncthreads();
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      As[lc + e][lr] = xa[e];
+      Bs[lc + e][lr] = xb[e];
+    }
+    __syncthreads();
+#pragma unroll 8
+    for (int kk = 0; kk < kGhBK; ++kk) {
+      const float4 a = *reinterpret_cast<const float4*>(&As[kk][tm]);
+      const float4 b = *reinterpret_cast<const float4*>(&Bs[kk][tn]);
+      const float av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) acc[i][q] = fmaf(av[i], bv[q], acc[i][q]);
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int n = n0 + tm + i;
+    if (n >= rows) continue;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int k = k0 + tn + q;
+      if (k < rank) Zh[(size_t)n * rank + k] = acc[i][q];
+    }
+  }
+}
+
+struct GateStepParams {
+  const void* E;
+  const void* W_g;
+  const float* Zh;                 // [R gamma, rank]
+  const int32_t* prev_tok;
+  const unsigned long long* keys;  // [gamma][R_max] argmax keys of the draft steps
+  float* A;                        // [R, gamma, rank] gated representation out
+  int* status;
+  int R_max, V, H, rank, gamma, j, act, bias_at_first;
+};
+
+template <typename T>
+__global__ void __launch_bounds__(256) gate_step_kernel(GateStepParams p) {
+  extern __shared__ float ms[];   // [rank]
+  const int r = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const size_t row = (size_t)r * p.gamma + p.j;
+  float* out = p.A + row * p.rank;
+  if (p.j == 0 && !p.bias_at_first) {   // position 0 carries no bias
+    for (int k = tid; k < p.rank; k += blockDim.x) out[k] = 0.f;
+    return;
+  }
+  int prev = p.j == 0 ? p.prev_tok[r] : (int)key_index(p.keys[(size_t)(p.j - 1) * p.R_max + r]);
+  if (prev < 0 || prev >= p.V) {
+    if (tid == 0) set_status(p.status, kErrArg);
+    prev = 0;
+  }
+  const T* E = static_cast<const T*>(p.E);
+  const T* Wg = static_cast<const T*>(p.W_g);
+  for (int k = tid; k < p.rank; k += blockDim.x)
+    ms[k] = act_apply(ld_elem(E, (size_t)prev * p.rank + k), p.act);
+  __syncthreads();
+  for (int k = warp; k < p.rank; k += blockDim.x / 32) {
+    const T* wrow = Wg + (size_t)k * (p.H + p.rank) + p.H;
+    float dot = 0.f;
+    for (int c = lane * 8; c < p.rank; c += 32 * 8) {
+      float w[8];
+      load8<T>(wrow + c, w);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) dot = fmaf(w[e], ms[c + e], dot);
+    }
+    dot = warp_sum(dot);
+    if (lane == 0) {
+      const float z = p.Zh[row * p.rank + k] + dot;
+      const float g = z >= 0.f ? 1.f / (1.f + expf(-z)) : expf(z) / (1.f + expf(z));
+      if (!isfinite(z)) set_status(p.status, kErrNonfinite);
+      out[k] = g * ms[k];
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_gate_h(const Ctx& ctx, const ProposeArgs& a, cudaStream_t s) {
+  const int rows = a.R * a.gamma;
+  const dim3 grid((a.rank + kGhBN - 1) / kGhBN, (rows + kGhBM - 1) / kGhBM);
+  if (a.dtype == 1)
+    gate_h_kernel<__nv_bfloat16><<<grid, kGhThreads, 0, s>>>(
+        static_cast<const __nv_bfloat16*>(a.gate_h), static_cast<const __nv_bfloat16*>(a.W_g),
+        rows, a.H, a.rank, ctx.ws.gate_zh);
+  else
+    gate_h_kernel<float><<<grid, kGhThreads, 0, s>>>(static_cast<const float*>(a.gate_h),
+                                                     static_cast<const float*>(a.W_g), rows, a.H,
+                                                     a.rank, ctx.ws.gate_zh);
+  count_launch(ctx);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gate_step(const Ctx& ctx, const ProposeArgs& a, int j, cudaStream_t s) {
+  GateStepParams p{};
+  p.E = a.E;
+  p.W_g = a.W_g;
+  p.Zh = ctx.ws.gate_zh;
+  p.prev_tok = a.prev_tok;
+  p.keys = ctx.ws.keys;
+  p.A = a.gated_rep;
+  p.status = ctx.ws.status;
+  p.R_max = ctx.cfg.R_max;
+  p.V = a.V;
+  p.H = a.H;
+  p.rank = a.rank;
+  p.gamma = a.gamma;
+  p.j = j;
+  p.act = a.act;
+  p.bias_at_first = a.bias_at_first;
+  const size_t smem = sizeof(float) * a.rank;
+  if (a.dtype == 1)
+    gate_step_kernel<__nv_bfloat16><<<a.R, 256, smem, s>>>(p);
+  else
+    gate_step_kernel<float><<<a.R, 256, smem, s>>>(p);
+  count_launch(ctx);
+  return cudaGetLastError();
+}
+
+}  // namespace dsd

@@ -37,6 +37,7 @@ struct SimtParams {
   const int32_t* tokens;         // residual mode: draft tokens [R, gamma]
   const uint32_t* req_id;
   const float* lse_q;            // residual mode
+  const float* A;                // gated head: [R, gamma, rank] representations (else nullptr)
   unsigned long long* keys;      // step: [gamma][R_max]; residual: [2][R_max]
   float2* parts;                 // step: [gamma][n_part][R_max]
   float* res_sums;               // residual: [2][R_max]
@@ -137,7 +138,9 @@ __global__ void __launch_bounds__(kSimtThreads) simt_bias_kernel(SimtParams p) {
     for (int idx = tid; idx < kSimtRC * rank; idx += kSimtThreads) {
       const int rr = idx / rank, k = idx - rr * rank;
       float m = 0.f;
-      if (rr < nr && s_bias[rr]) m = act_apply(ld_elem(E, (size_t)s_prev[rr] * rank + k), p.act);
+      if (rr < nr && s_bias[rr])
+        m = p.A ? p.A[((size_t)s_req[rr] * p.gamma + s_pos[rr]) * rank + k]
+                : act_apply(ld_elem(E, (size_t)s_prev[rr] * rank + k), p.act);
       ms[rr * mstride + k] = m;
     }
 
@@ -329,8 +332,17 @@ cudaError_t launch_propose_simt(const Ctx& ctx, const ProposeArgs& a, cudaStream
                                   sizeof(unsigned long long) * (size_t)a.gamma * ctx.cfg.R_max, s);
   if (e != cudaSuccess) return e;
   const int grid = simt_grid(ctx, a.V);
+  if (a.gate_h) {   // gated head: the hidden-state part of every gate, once
+    sp.A = a.gated_rep;
+    e = launch_gate_h(ctx, a, s);
+    if (e != cudaSuccess) return e;
+  }
   for (int j = 0; j < a.gamma; ++j) {
     sp.j = j;
+    if (a.gate_h) {
+      e = launch_gate_step(ctx, a, j, s);
+      if (e != cudaSuccess) return e;
+    }
     e = launch_simt(sp, ctx.cfg.dtype, grid, s, kModeStep);
     if (e != cudaSuccess) return e;
     count_launch(ctx);
@@ -349,6 +361,7 @@ cudaError_t launch_residual_simt(const Ctx& ctx, const VerifyArgs& a, cudaStream
   sp.tokens = a.tokens;
   sp.req_id = a.req_id;
   sp.lse_q = a.lse_q;
+  sp.A = a.gated_rep;
   sp.keys = ctx.ws.res_keys;
   sp.res_sums = ctx.ws.res_sums;
   sp.rej_list = ctx.ws.rej_list;
@@ -370,6 +383,7 @@ struct FinParams {
   const void* W;
   const float* conf;
   const int32_t* prev_tok;
+  const float* A;                 // gated head representations, or nullptr
   const unsigned long long* keys;
   const float2* parts;
   int* status;
@@ -422,8 +436,9 @@ __global__ void __launch_bounds__(256) propose_finalize_kernel(FinParams p) {
     if ((j > 0 || p.bias_at_first) && x < (uint32_t)p.V) {
       int prev = (j == 0) ? p.prev_tok[r] : (int)key_index(p.keys[(size_t)(j - 1) * p.R_max + r]);
       if (prev < 0 || prev >= p.V) prev = 0;
+      const float* arow = p.A ? p.A + ((size_t)r * p.gamma + j) * p.rank : nullptr;
       for (int k = lane; k < p.rank; k += 32)
-        dot = fmaf(act_apply(ld_elem(E, (size_t)prev * p.rank + k), p.act),
+        dot = fmaf(arow ? arow[k] : act_apply(ld_elem(E, (size_t)prev * p.rank + k), p.act),
                    ld_elem(W, (size_t)x * p.rank + k), dot);
       dot = warp_sum(dot);
     }
@@ -446,6 +461,7 @@ cudaError_t launch_propose_finalize_n(const Ctx& ctx, const ProposeArgs& a, int 
   p.W = a.W;
   p.conf = a.conf;
   p.prev_tok = a.prev_tok;
+  p.A = a.gate_h ? a.gated_rep : nullptr;
   p.keys = ctx.ws.keys;
   p.parts = ctx.ws.lse_parts;
   p.status = ctx.ws.status;

@@ -35,6 +35,10 @@ the five workloads of the benchmark suite:
            (so both halves move the logit by about 0.5); b_c = 1.2 (a mean
            confidence near 0.77); E ~ N(0, 0.02^2); prev_tok and drafted
            tokens uniform.
+  gated    the gated Markov head's extra inputs for a cycle workload: hidden
+           states h ~ N(0,1) [R, gamma, H]; W_g [rank, H + rank] with the
+           hidden columns ~ N(0, 1/H) and the Markov columns ~ N(0, 1/rank) /
+           e_std (each half moves a gate's argument by about 1).
   calibration  M requests x 7 positions: predicted per-step confidence
            c ~ Beta(6,2) * 0.97^j; realised accept lengths drawn as the
            leading successes of Bernoulli(max(0, c - 0.05)) chains (a head
@@ -337,3 +341,16 @@ def calibration_inputs(M: int, G: int, seed: int = 8, device="cpu"):
     acc = np.where(ok.all(axis=1), G, np.argmin(ok, axis=1)).astype(np.int32)
     return dict(conf=torch.as_tensor(c, device=device),
                 accept_len=torch.as_tensor(acc, device=device))
+
+
+def gate_inputs(R: int, G: int, H: int, r: int, e_std: float, seed: int = 9,
+                dtype: str = "bf16", device="cpu"):
+    """h [R,G,H] and W_g [r, H+r] in dtype (see the module docstring)."""
+    rng = np.random.default_rng(seed)
+    td = _torch_dtype(dtype)
+    h = rng.standard_normal((R, G, H), dtype=np.float32)
+    Wg = np.concatenate([rng.standard_normal((r, H), dtype=np.float32) / np.sqrt(H),
+                         rng.standard_normal((r, r), dtype=np.float32) / np.sqrt(r) / e_std],
+                        axis=1)
+    to = lambda a: torch.as_tensor(a).to(device=device, dtype=td)
+    return dict(h=to(h), W_g=to(Wg.astype(np.float32)))
