@@ -67,7 +67,8 @@ size_t carve(dsd_ctx* c, unsigned char* base) {
   w.loss_red = reinterpret_cast<double*>(take(sizeof(double) * 64 * 3));
   w.cal_acc = reinterpret_cast<double*>(take(sizeof(double) * (2 * kMaxCalBins + 2 + 2 * kMaxGamma)));
   w.cal_cnt = reinterpret_cast<unsigned long long*>(take(sizeof(unsigned long long) * (kMaxCalBins + 1)));
-  w.gate_zh = reinterpret_cast<float*>(take(sizeof(float) * (size_t)Rm * G * c->cfg.rank));
+  // split-K partials of the gate's hidden-state part
+  w.gate_zh = reinterpret_cast<float*>(take(sizeof(float) * kGateZhFactor * (size_t)Rm * G * c->cfg.rank));
   if (base) c->ws = w;
   return off;
 }

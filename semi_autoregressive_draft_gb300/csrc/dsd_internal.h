@@ -13,6 +13,7 @@ constexpr int kActSilu = 1;
 
 constexpr int kMaxGamma = 16;
 constexpr int kMaxCalBins = 64;      // reliability bins of dsd_calibration
+constexpr int kGateZhFactor = 4;     // gated head: split-K partials held for 4 x (R_max gamma) rows
 constexpr int kMaxSchedItems = 4096;  // R_max * gamma
 constexpr int kVerifySplits = 8;      // V chunks per verified row
 

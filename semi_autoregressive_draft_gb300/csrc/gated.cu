@@ -6,9 +6,10 @@
 // tokens, W_g[:, :H] h_j, and one that does, W_g[:, H:] m_j.  The first is
 // one dense product for all positions of the batch before the sequential
 // stage (gate_h_kernel, [R gamma, H] x [H, rank] on CUDA cores, 64 x 64
-// output tiles); the second is a [rank, rank] matrix-vector product per
-// request at each draft step (gate_step_kernel, one CTA per request, one warp
-// per output row at a time, 16-byte loads of W_g), which writes the gated
+// output tiles, split over H into partials); the second is a [rank, rank]
+// matrix-vector product per request at each draft step (gate_step_kernel,
+// one CTA per request and 32 gate outputs, one warp per output row at a time,
+// 16-byte loads of W_g), which also adds the partials and writes the gated
 // representation g * m.  The CUDA-core bias kernel then reads that
 // representation instead of gathering rows of E, and so does the verifier's
 // residual pass.
@@ -19,6 +20,7 @@ namespace dsd {
 namespace {
 
 constexpr int kGhBM = 64, kGhBN = 64, kGhBK = 32, kGhThreads = 256;
+constexpr int kGsOut = 32;         // gate outputs per CTA of gate_step_kernel
 
 template <typename T>
 __device__ __forceinline__ void load8(const T* p, float* x) {
@@ -35,13 +37,15 @@ __device__ __forceinline__ void load8(const T* p, float* x) {
   }
 }
 
-// Zh[n, k] = sum_{c < H} h[n, c] W_g[k, c] for n < rows, k < rank.  H and
-// rank are multiples of 8; a group of eight consecutive c is either wholly
-// inside H or wholly outside.
+// Zh[s, n, k] = sum over c in split s (columns s width .. + width, below H)
+// of h[n, c] W_g[k, c], for n < rows, k < rank (width a multiple of 32).  The splits are
+// summed in order by gate_step_kernel, so the result does not depend on
+// scheduling.  H and rank are multiples of 8; a group of eight consecutive c
+// is either wholly inside H or wholly outside.
 template <typename T>
 __global__ void __launch_bounds__(kGhThreads) gate_h_kernel(const T* __restrict__ h,
                                                             const T* __restrict__ W_g, int rows,
-                                                            int H, int rank, float* Zh) {
+                                                            int H, int rank, int width, float* Zh) {
   __shared__ __align__(16) float As[kGhBK][kGhBM + 4];
   __shared__ __align__(16) float Bs[kGhBK][kGhBN + 4];
   const int tid = threadIdx.x;
@@ -50,13 +54,15 @@ __global__ void __launch_bounds__(kGhThreads) gate_h_kernel(const T* __restrict_
   float acc[4][4] = {};
   // loader: one group of 8 K-values of one row of A and of B per thread
   const int lr = tid / 4, lc = (tid % 4) * 8;
-  for (int c0 = 0; c0 < H; c0 += kGhBK) {
+  const int cs = blockIdx.z * width, ce = min(H, cs + width);
+  Zh += (size_t)blockIdx.z * rows * rank;
+  for (int c0 = cs; c0 < ce; c0 += kGhBK) {
     float xa[8], xb[8];
     const int c = c0 + lc;
     const int na = n0 + lr, kb = k0 + lr;
-    if (c < H && na < rows) load8<T>(h + (size_t)na * H + c, xa);
+    if (c < ce && na < rows) load8<T>(h + (size_t)na * H + c, xa);
     else for (int e = 0; e < 8; ++e) xa[e] = 0.f;
-    if (c < H && kb < rank) load8<T>(W_g + (size_t)kb * (H + rank) + c, xb);
+    if (c < ce && kb < rank) load8<T>(W_g + (size_t)kb * (H + rank) + c, xb);
     else for (int e = 0; e < 8; ++e) xb[e] = 0.f;
     __syncthreads();
 #pragma unroll
@@ -91,7 +97,8 @@ __global__ void __launch_bounds__(kGhThreads) gate_h_kernel(const T* __restrict_
 struct GateStepParams {
   const void* E;
   const void* W_g;
-  const float* Zh;                 // [R gamma, rank]
+  const float* Zh;                 // [n_split][R gamma][rank] split-K partials
+  int n_split, rows;
   const int32_t* prev_tok;
   const unsigned long long* keys;  // [gamma][R_max] argmax keys of the draft steps
   float* A;                        // [R, gamma, rank] gated representation out
@@ -103,10 +110,11 @@ template <typename T>
 __global__ void __launch_bounds__(256) gate_step_kernel(GateStepParams p) {
   extern __shared__ float ms[];   // [rank]
   const int r = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int k0 = blockIdx.y * kGsOut, k1 = min(p.rank, k0 + kGsOut);   // this CTA's outputs
   const size_t row = (size_t)r * p.gamma + p.j;
   float* out = p.A + row * p.rank;
   if (p.j == 0 && !p.bias_at_first) {   // position 0 carries no bias
-    for (int k = tid; k < p.rank; k += blockDim.x) out[k] = 0.f;
+    for (int k = k0 + tid; k < k1; k += blockDim.x) out[k] = 0.f;
     return;
   }
   int prev = p.j == 0 ? p.prev_tok[r] : (int)key_index(p.keys[(size_t)(p.j - 1) * p.R_max + r]);
@@ -119,7 +127,7 @@ __global__ void __launch_bounds__(256) gate_step_kernel(GateStepParams p) {
   for (int k = tid; k < p.rank; k += blockDim.x)
     ms[k] = act_apply(ld_elem(E, (size_t)prev * p.rank + k), p.act);
   __syncthreads();
-  for (int k = warp; k < p.rank; k += blockDim.x / 32) {
+  for (int k = k0 + warp; k < k1; k += blockDim.x / 32) {
     const T* wrow = Wg + (size_t)k * (p.H + p.rank) + p.H;
     float dot = 0.f;
     for (int c = lane * 8; c < p.rank; c += 32 * 8) {
@@ -130,7 +138,8 @@ __global__ void __launch_bounds__(256) gate_step_kernel(GateStepParams p) {
     }
     dot = warp_sum(dot);
     if (lane == 0) {
-      const float z = p.Zh[row * p.rank + k] + dot;
+      float z = dot;
+      for (int sp = 0; sp < p.n_split; ++sp) z += p.Zh[((size_t)sp * p.rows + row) * p.rank + k];
       const float g = z >= 0.f ? 1.f / (1.f + expf(-z)) : expf(z) / (1.f + expf(z));
       if (!isfinite(z)) set_status(p.status, kErrNonfinite);
       out[k] = g * ms[k];
@@ -140,17 +149,36 @@ __global__ void __launch_bounds__(256) gate_step_kernel(GateStepParams p) {
 
 }  // namespace
 
+// Split of the hidden columns: enough CTAs to cover every SM, within the
+// workspace (kGateZhFactor x R_max gamma rows of partials) and at least 32
+// columns per split.
+static void gate_split(const Ctx& ctx, int rows, int H, int rank, int* n_split, int* width) {
+  const int tiles = ((rank + kGhBN - 1) / kGhBN) * ((rows + kGhBM - 1) / kGhBM);
+  int n = (ctx.num_sms + tiles - 1) / tiles;
+  const int cap = kGateZhFactor * ctx.cfg.R_max * ctx.cfg.gamma / (rows > 0 ? rows : 1);
+  n = n < cap ? n : cap;
+  const int most = (H + 31) / 32;
+  n = n < most ? n : most;
+  n = n < 1 ? 1 : n;
+  int w = (H + n - 1) / n;
+  w = (w + 31) / 32 * 32;
+  *width = w;
+  *n_split = (H + w - 1) / w;
+}
+
 cudaError_t launch_gate_h(const Ctx& ctx, const ProposeArgs& a, cudaStream_t s) {
   const int rows = a.R * a.gamma;
-  const dim3 grid((a.rank + kGhBN - 1) / kGhBN, (rows + kGhBM - 1) / kGhBM);
+  int n_split, width;
+  gate_split(ctx, rows, a.H, a.rank, &n_split, &width);
+  const dim3 grid((a.rank + kGhBN - 1) / kGhBN, (rows + kGhBM - 1) / kGhBM, n_split);
   if (a.dtype == 1)
     gate_h_kernel<__nv_bfloat16><<<grid, kGhThreads, 0, s>>>(
         static_cast<const __nv_bfloat16*>(a.gate_h), static_cast<const __nv_bfloat16*>(a.W_g),
-        rows, a.H, a.rank, ctx.ws.gate_zh);
+        rows, a.H, a.rank, width, ctx.ws.gate_zh);
   else
     gate_h_kernel<float><<<grid, kGhThreads, 0, s>>>(static_cast<const float*>(a.gate_h),
                                                      static_cast<const float*>(a.W_g), rows, a.H,
-                                                     a.rank, ctx.ws.gate_zh);
+                                                     a.rank, width, ctx.ws.gate_zh);
   count_launch(ctx);
   return cudaGetLastError();
 }
@@ -160,6 +188,9 @@ cudaError_t launch_gate_step(const Ctx& ctx, const ProposeArgs& a, int j, cudaSt
   p.E = a.E;
   p.W_g = a.W_g;
   p.Zh = ctx.ws.gate_zh;
+  p.rows = a.R * a.gamma;
+  int width;
+  gate_split(ctx, p.rows, a.H, a.rank, &p.n_split, &width);
   p.prev_tok = a.prev_tok;
   p.keys = ctx.ws.keys;
   p.A = a.gated_rep;
@@ -173,10 +204,11 @@ cudaError_t launch_gate_step(const Ctx& ctx, const ProposeArgs& a, int j, cudaSt
   p.act = a.act;
   p.bias_at_first = a.bias_at_first;
   const size_t smem = sizeof(float) * a.rank;
+  const dim3 grid(a.R, (a.rank + kGsOut - 1) / kGsOut);
   if (a.dtype == 1)
-    gate_step_kernel<__nv_bfloat16><<<a.R, 256, smem, s>>>(p);
+    gate_step_kernel<__nv_bfloat16><<<grid, 256, smem, s>>>(p);
   else
-    gate_step_kernel<float><<<a.R, 256, smem, s>>>(p);
+    gate_step_kernel<float><<<grid, 256, smem, s>>>(p);
   count_launch(ctx);
   return cudaGetLastError();
 }
