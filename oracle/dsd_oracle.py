@@ -229,8 +229,16 @@ def head_bias(E, W, prev: int, act="none", gate=None, r=0, j=0):
 # a2-a4: sequential propose  ([TRAIN] Markov 顺序修正; [READ] 2.2, 2.3)
 # ---------------------------------------------------------------------------
 
+def top_k(ell, K):
+    """The K largest entries of ell, largest first; equal values in index
+    order (lowest first).  Returns (indices, values)."""
+    ell = np.asarray(ell, dtype=np.float64)
+    order = np.lexsort((np.arange(ell.size), -ell))[:K]
+    return order, ell[order]
+
+
 def propose(U, E, W, conf, prev_tok, req_id=None, temperature=0.0, seed=0,
-            bias_at_first=True, act="none", gate=None):
+            bias_at_first=True, act="none", gate=None, candidates=0):
     """Sequential Markov-head proposal for a batch of R requests.
 
     For each request r and position j = 0..gamma-1:
@@ -242,7 +250,14 @@ def propose(U, E, W, conf, prev_tok, req_id=None, temperature=0.0, seed=0,
 
     Returns a dict with tokens [R,G] int, lse_q [R,G], logit_at_tok [R,G],
     survival [R,G] (fp64) and margin [R,G] (top-2 gap of the decision
-    variable, for the near-tie exemption rule)."""
+    variable, for the near-tie exemption rule).
+
+    With candidates = K > 0 also the Markov candidate set of every position
+    ([TRAIN] Prefix reranker, 候选与前缀表示: C_i = Top16(l_i) of the Markov-
+    corrected scores, with the tokens drafted in this round as predecessors): cand_tok [R,G,K] and
+    cand_logit [R,G,K] (the biased logits l, largest first, ties by lowest
+    token index) and cand_gap [R,G] (the gap between the K-th and the
+    (K+1)-th largest l, for the near-tie exemption of the set's boundary)."""
     U = np.asarray(U)
     R, G, V = U.shape
     if req_id is None:
@@ -252,6 +267,10 @@ def propose(U, E, W, conf, prev_tok, req_id=None, temperature=0.0, seed=0,
     lse_q = np.zeros((R, G))
     logit_at_tok = np.zeros((R, G))
     margin = np.zeros((R, G))
+    K = int(candidates)
+    cand_tok = np.zeros((R, G, K), dtype=np.int64)
+    cand_logit = np.zeros((R, G, K))
+    cand_gap = np.full((R, G), np.inf)
     for r in range(R):
         prev = int(prev_tok[r])
         for j in range(G):
@@ -265,13 +284,22 @@ def propose(U, E, W, conf, prev_tok, req_id=None, temperature=0.0, seed=0,
                 s = ell / T
                 z = s + vocab_gumbel(seed, j, int(req_id[r]), STREAM_DRAFT, V)
                 lse_q[r, j] = logsumexp(s)
+            if K:
+                idx, val = top_k(ell, K + 1)
+                cand_tok[r, j] = idx[:K]
+                cand_logit[r, j] = val[:K]
+                if idx.size > K:
+                    cand_gap[r, j] = val[K - 1] - val[K]
             x = int(np.argmax(z))              # first maximum: lowest index
             tokens[r, j] = x
             margin[r, j] = top2_margin(z)
             logit_at_tok[r, j] = ell[x] if T == 0.0 else ell[x] / T
             prev = x
-    return dict(tokens=tokens, lse_q=lse_q, logit_at_tok=logit_at_tok,
-                survival=survival(conf), margin=margin)
+    out = dict(tokens=tokens, lse_q=lse_q, logit_at_tok=logit_at_tok,
+               survival=survival(conf), margin=margin)
+    if K:
+        out.update(cand_tok=cand_tok, cand_logit=cand_logit, cand_gap=cand_gap)
+    return out
 
 
 # ---------------------------------------------------------------------------

@@ -677,3 +677,46 @@ def test_gated_propose_single_step_by_hand():
     ell = [0.5 + s3, -2.0 * sm2, 2.0 * s3 - 2.0 * sm2]   # 1.4526, -0.2384, 1.6670
     assert int(out["tokens"][0, 0]) == int(np.argmax(ell)) == 2
     assert abs(out["logit_at_tok"][0, 0] - ell[2]) < 1e-14
+
+
+# ---------------------------------------------------------------------------
+# Markov top-16 candidate set ([TRAIN] Prefix reranker, 候选与前缀表示)
+# ---------------------------------------------------------------------------
+
+def test_top_k_by_hand():
+    idx, val = O.top_k([0.5, 3.0, -1.0, 3.0, 2.0, 0.5], 4)
+    assert list(idx) == [1, 3, 4, 0] and list(val) == [3.0, 3.0, 2.0, 0.5]   # ties: lower index
+    idx, _ = O.top_k([1.0, 2.0], 5)                                          # K > V: everything
+    assert list(idx) == [1, 0]
+
+
+def test_candidates_without_markov_table_are_the_sorted_base_logits():
+    rng = np.random.default_rng(11)
+    R, G, V, r = 2, 3, 50, 4
+    U = rng.normal(0, 1, (R, G, V))
+    out = O.propose(U, np.zeros((V, r)), rng.normal(0, 1, (V, r)), np.full((R, G), 0.9),
+                    [3, 7], candidates=16)
+    for q in range(R):
+        for j in range(G):
+            ref = np.argsort(-U[q, j], kind="stable")[:16]
+            assert list(out["cand_tok"][q, j]) == list(ref)
+            assert np.array_equal(out["cand_logit"][q, j], U[q, j][ref])
+            assert out["cand_tok"][q, j, 0] == out["tokens"][q, j]     # greedy = top-1
+
+
+def test_candidates_follow_the_drafted_chain():
+    # each position's set is the top of U_j + W E[x_{j-1}] with x the drafted token
+    rng = np.random.default_rng(12)
+    R, G, V, r = 1, 4, 60, 6
+    U = rng.normal(0, 1, (R, G, V))
+    E = rng.normal(0, 1, (V, r))
+    W = rng.normal(0, 1, (V, r))
+    out = O.propose(U, E, W, np.full((R, G), 0.9), [5], candidates=16)
+    prev = 5
+    for j in range(G):
+        ell = U[0, j] + (E @ W.T)[prev]          # the dense V x V transition row
+        ref = np.argsort(-ell, kind="stable")[:16]
+        assert list(out["cand_tok"][0, j]) == list(ref)
+        assert np.allclose(out["cand_logit"][0, j], ell[ref], atol=1e-12)
+        prev = int(out["tokens"][0, j])
+        assert prev == ref[0]
