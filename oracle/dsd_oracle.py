@@ -256,7 +256,7 @@ def propose(U, E, W, conf, prev_tok, req_id=None, temperature=0.0, seed=0,
     ([TRAIN] Prefix reranker, 候选与前缀表示: C_i = Top16(l_i) of the Markov-
     corrected scores, with the tokens drafted in this round as predecessors): cand_tok [R,G,K] and
     cand_logit [R,G,K] (the biased logits l, largest first, ties by lowest
-    token index) and cand_gap [R,G] (the gap between the K-th and the
+    token index; token -1 and logit -inf past V when V < K) and cand_gap [R,G] (the gap between the K-th and the
     (K+1)-th largest l, for the near-tie exemption of the set's boundary)."""
     U = np.asarray(U)
     R, G, V = U.shape
@@ -286,8 +286,11 @@ def propose(U, E, W, conf, prev_tok, req_id=None, temperature=0.0, seed=0,
                 lse_q[r, j] = logsumexp(s)
             if K:
                 idx, val = top_k(ell, K + 1)
-                cand_tok[r, j] = idx[:K]
-                cand_logit[r, j] = val[:K]
+                n = min(K, idx.size)
+                cand_tok[r, j] = -1                 # a vocabulary smaller than K:
+                cand_logit[r, j] = -np.inf          # the missing entries are -1 / -inf
+                cand_tok[r, j, :n] = idx[:n]
+                cand_logit[r, j, :n] = val[:n]
                 if idx.size > K:
                     cand_gap[r, j] = val[K - 1] - val[K]
             x = int(np.argmax(z))              # first maximum: lowest index
