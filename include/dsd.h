@@ -6,7 +6,8 @@
  * and dsd_overlap is the separate offline-metric call.  Sources, by page title
  * and section:
  *   [TRAIN] "Qwen3.8-Flash-Next DSpark 训练实验": 评估口径/离线指标;
- *           Baseline 架构/Markov 顺序修正; Confidence head 与训练目标
+ *           Baseline 架构/Markov 顺序修正; Confidence head 与训练目标;
+ *           Prefix reranker/候选与前缀表示
  *   [NOTES] "DSpark notes" (h.sjds.net/a/571373): 2.2 Sequential Stage;
  *           2.3 串行头的两种形态
  *   [READ]  "DSpark 论文精读：置信度调度推测解码、半自回归生成与大模型推理加速":
@@ -17,7 +18,8 @@
  * ([READ] 4.1; [WALK] 3.4).  dsd_confidence_head, dsd_threshold_keep and
  * dsd_calibration cover the scheduler's input: the confidence head, the
  * static truncation it replaces, and the calibration of its survivals.
- * dsd_propose_gated / dsd_verify_gated run the gated Markov head.
+ * dsd_propose_gated / dsd_verify_gated run the gated Markov head;
+ * dsd_propose_candidates also returns the Markov top-16 candidate sets.
  *
  * Conventions for every call below.
  *   - Tensor arguments are DEVICE pointers owned by the caller, row-major and
@@ -338,6 +340,28 @@ int dsd_verify_gated(dsd_ctx* ctx, int R, const void* P, const void* U, const vo
                      const int32_t* tokens, const float* lse_q, const float* logit_at_tok,
                      const int32_t* keep_len, const uint32_t* req_id, float temperature,
                      uint64_t seed, int32_t* accept_len, int32_t* next_token, void* stream);
+
+/*
+ * dsd_propose_candidates -- dsd_propose plus the Markov candidate set of
+ * every draft position ([TRAIN] Prefix reranker, 候选与前缀表示:
+ * C_i = Top16(l_i) of the Markov-corrected scores l_i = l_i^0 + W E[t_{i-1}],
+ * with this round's drafted tokens as predecessors): the set a reranker
+ * scores.  Same arguments and outputs as dsd_propose, plus
+ *   cand_tok [R, gamma, 16] i32 out: the 16 largest biased logits' tokens,
+ *     largest first, equal logits in token order (-1 past V when V < 16)
+ *   cand_logit [R, gamma, 16] f32 out: those biased logits (not divided by
+ *     the temperature)
+ * Runs on the CUDA-core engine whatever the context's engine; the biased
+ * logits stay in registers: each CTA keeps per request a sorted top-16 of
+ * its vocabulary tiles in shared memory, and one more launch merges the
+ * CTAs' lists.  R <= 32 (DSD_ERR_CAPACITY otherwise); other errors as
+ * dsd_propose.
+ */
+int dsd_propose_candidates(dsd_ctx* ctx, int R, const void* U, const void* E, const void* W,
+                           const float* conf, const int32_t* prev_tok, const uint32_t* req_id,
+                           float temperature, uint64_t seed, int32_t* tokens, float* lse_q,
+                           float* logit_at_tok, float* survival, int32_t* cand_tok,
+                           float* cand_logit, void* stream);
 
 /*
  * dsd_confidence_head -- per-position confidence of the drafted tokens

@@ -36,7 +36,7 @@ EXPORTED = [
     "dsd_launch_count", "dsd_last_engine",
     "dsd_propose", "dsd_schedule", "dsd_verify", "dsd_cycle", "dsd_cycle_host", "dsd_overlap",
     "dsd_propose_noalloc", "dsd_loss_forward", "dsd_confidence_head", "dsd_threshold_keep",
-    "dsd_calibration", "dsd_propose_gated", "dsd_verify_gated",
+    "dsd_calibration", "dsd_propose_gated", "dsd_verify_gated", "dsd_propose_candidates",
 ]
 
 
@@ -88,6 +88,8 @@ def load_library(path: str | None = None):
         "dsd_overlap": (_I, [_P, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
         "dsd_loss_forward": (_I, [_P, _I, _P, _P, _P, _P, _P, _P, _P, _F, _F, _F, _F, _P, _P,
                                   _P]),
+        "dsd_propose_candidates": (_I, [_P, _I, _P, _P, _P, _P, _P, _P, _F, _U64, _P, _P, _P, _P,
+                                        _P, _P, _P]),
         "dsd_propose_gated": (_I, [_P, _I, _P, _P, _P, _P, _I, _P, _P, _P, _P, _F, _U64, _P, _P,
                                    _P, _P, _P, _P]),
         "dsd_verify_gated": (_I, [_P, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _F, _U64,
@@ -208,6 +210,15 @@ def dsd_loss_forward(ctx, B, U, E, W, prev_tok, P, target, conf_logit, ce_alpha,
         ctx, B, _ptr(U), _ptr(E), _ptr(W), _ptr(prev_tok), _ptr(P), _ptr(target),
         _ptr(conf_logit), ce_alpha, l1_alpha, conf_alpha, decay, _ptr(row_out), _ptr(losses),
         _stream(stream, device)))
+
+
+def dsd_propose_candidates(ctx, R, U, E, W, conf, prev_tok, req_id, temperature, seed, tokens,
+                           lse_q, logit_at_tok, survival, cand_tok, cand_logit, stream=None,
+                           device=0):
+    _check(ctx, load_library().dsd_propose_candidates(
+        ctx, R, _ptr(U), _ptr(E), _ptr(W), _ptr(conf), _ptr(prev_tok), _ptr(req_id), temperature,
+        seed, _ptr(tokens), _ptr(lse_q), _ptr(logit_at_tok), _ptr(survival), _ptr(cand_tok),
+        _ptr(cand_logit), _stream(stream, device)))
 
 
 def dsd_propose_gated(ctx, R, U, E, W, h, H, W_g, conf, prev_tok, req_id, temperature, seed,
@@ -334,6 +345,28 @@ class Context:
                         survival=self._empty((R, G), torch.float32))
         dsd_propose(self.handle, R, U, E, W, conf, prev_tok, req_id, temperature, seed,
                     o["tokens"], o["lse_q"], o["logit_at_tok"], o["survival"], stream, self.device)
+        return o
+
+    def propose_candidates(self, U, E, W, conf, prev_tok, req_id=None, temperature=0.0, seed=0,
+                           out=None, stream=None):
+        """dsd_propose plus the Markov top-16 candidate set of every position:
+        cand_tok [R, gamma, 16] i32 and cand_logit [R, gamma, 16] f32."""
+        R = U.shape[0]
+        for n, t in (("U", U), ("E", E), ("W", W)):
+            self._check_in(n, t, self.torch_dtype)
+        self._check_in("conf", conf, torch.float32)
+        self._check_in("prev_tok", prev_tok, torch.int32)
+        self._check_in("req_id", req_id, torch.int32)
+        G = self.gamma
+        o = out or dict(tokens=self._empty((R, G), torch.int32),
+                        lse_q=self._empty((R, G), torch.float32),
+                        logit_at_tok=self._empty((R, G), torch.float32),
+                        survival=self._empty((R, G), torch.float32),
+                        cand_tok=self._empty((R, G, 16), torch.int32),
+                        cand_logit=self._empty((R, G, 16), torch.float32))
+        dsd_propose_candidates(self.handle, R, U, E, W, conf, prev_tok, req_id, temperature, seed,
+                               o["tokens"], o["lse_q"], o["logit_at_tok"], o["survival"],
+                               o["cand_tok"], o["cand_logit"], stream, self.device)
         return o
 
     def propose_gated(self, U, E, W, h, W_g, conf, prev_tok, req_id=None, temperature=0.0,

@@ -69,6 +69,9 @@ size_t carve(dsd_ctx* c, unsigned char* base) {
   w.cal_cnt = reinterpret_cast<unsigned long long*>(take(sizeof(unsigned long long) * (kMaxCalBins + 1)));
   // split-K partials of the gate's hidden-state part
   w.gate_zh = reinterpret_cast<float*>(take(sizeof(float) * kGateZhFactor * (size_t)Rm * G * c->cfg.rank));
+  const int cand_R = Rm < kCandMaxR ? Rm : kCandMaxR;
+  w.cand_parts = reinterpret_cast<unsigned long long*>(
+      take(sizeof(unsigned long long) * (size_t)G * c->n_part * cand_R * kCandK));
   if (base) c->ws = w;
   return off;
 }
@@ -646,6 +649,57 @@ int dsd_calibration(dsd_ctx* ctx, int M, const float* conf, const int32_t* accep
   a.metrics = metrics;
   cudaError_t e = launch_calibration(*ctx, a, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(ctx, e, "calibration launch");
+  return DSD_OK;
+}
+
+int dsd_propose_candidates(dsd_ctx* ctx, int R, const void* U, const void* E, const void* W,
+                           const float* conf, const int32_t* prev_tok, const uint32_t* req_id,
+                           float temperature, uint64_t seed, int32_t* tokens, float* lse_q,
+                           float* logit_at_tok, float* survival, int32_t* cand_tok,
+                           float* cand_logit, void* stream) {
+  int rc = check_ctx(ctx);
+  if (rc) return rc;
+  if ((rc = check_R(ctx, R))) return rc;
+  if ((rc = check_temperature(ctx, temperature))) return rc;
+  if (R > kCandMaxR)
+    return fail(ctx, DSD_ERR_CAPACITY, "R = %d > %d requests per candidate call", R, kCandMaxR);
+  if (R == 0) return DSD_OK;
+  if ((rc = check_table(ctx, U, "U")) || (rc = check_table(ctx, E, "E")) ||
+      (rc = check_table(ctx, W, "W")))
+    return rc;
+  if (!conf || !prev_tok || !tokens || !lse_q || !logit_at_tok || !survival || !cand_tok ||
+      !cand_logit)
+    return fail(ctx, DSD_ERR_ARG, "dsd_propose_candidates: NULL argument");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  ProposeArgs a{};
+  a.R = R;
+  a.V = ctx->cfg.V;
+  a.rank = ctx->cfg.rank;
+  a.gamma = ctx->cfg.gamma;
+  a.dtype = ctx->cfg.dtype;
+  a.act = ctx->cfg.act;
+  a.bias_at_first = ctx->cfg.bias_at_first;
+  a.U = U;
+  a.E = E;
+  a.W = W;
+  a.conf = conf;
+  a.prev_tok = prev_tok;
+  a.req_id = req_id;
+  a.temperature = temperature;
+  a.seed = seed;
+  a.tokens = tokens;
+  a.lse_q = lse_q;
+  a.logit_at_tok = logit_at_tok;
+  a.survival = survival;
+  a.cand_tok = cand_tok;
+  a.cand_logit = cand_logit;
+  cudaError_t e = launch_propose_simt(*ctx, a, s);
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "candidate propose launch");
+  ctx->last_engine = DSD_ENGINE_SIMT;
+  const int n_used = simt_grid(*ctx, a.V);
+  e = launch_propose_finalize_n(*ctx, a, n_used, s);
+  if (e == cudaSuccess) e = launch_cand_finalize(*ctx, a, n_used, s);
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "propose finalize launch");
   return DSD_OK;
 }
 

@@ -13,6 +13,8 @@ constexpr int kActSilu = 1;
 
 constexpr int kMaxGamma = 16;
 constexpr int kMaxCalBins = 64;      // reliability bins of dsd_calibration
+constexpr int kCandK = 16;           // Markov candidate set size (top-16)
+constexpr int kCandMaxR = 32;        // requests per call of dsd_propose_candidates
 constexpr int kGateZhFactor = 4;     // gated head: split-K partials held for 4 x (R_max gamma) rows
 constexpr int kMaxSchedItems = 4096;  // R_max * gamma
 constexpr int kVerifySplits = 8;      // V chunks per verified row
@@ -53,7 +55,8 @@ struct Workspace {
   double* loss_red;             // [64][3] per-CTA sums of the loss finalize
   double* cal_acc;              // [2 kMaxCalBins + 2 + 2 kMaxGamma] calibration sums (zero between calls)
   unsigned long long* cal_cnt;  // [kMaxCalBins + 1] calibration counts (zero between calls)
-  float* gate_zh;               // [R_max * gamma][rank] hidden-state part of the gated head's gate
+  float* gate_zh;               // split-K partials of the gated head's hidden-state gate part
+  unsigned long long* cand_parts;  // [gamma][n_part][min(R_max, kCandMaxR)][kCandK] candidate keys
 };
 
 struct Config {
@@ -97,7 +100,11 @@ struct ProposeArgs {
   const void* W_g;      // [rank, H + rank]
   int H;
   float* gated_rep;     // [R, gamma, rank] f32 out: g * m per position
+  // Markov candidate sets (cand_tok == nullptr: none)
+  int32_t* cand_tok;    // [R, gamma, kCandK]
+  float* cand_logit;    // [R, gamma, kCandK]
 };
+cudaError_t launch_cand_finalize(const Ctx& ctx, const ProposeArgs& a, int n_used, cudaStream_t s);
 
 cudaError_t launch_propose_simt(const Ctx& ctx, const ProposeArgs& a, cudaStream_t s);
 cudaError_t launch_gate_h(const Ctx& ctx, const ProposeArgs& a, cudaStream_t s);

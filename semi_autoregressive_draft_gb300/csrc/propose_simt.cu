@@ -38,6 +38,8 @@ struct SimtParams {
   const uint32_t* req_id;
   const float* lse_q;            // residual mode
   const float* A;                // gated head: [R, gamma, rank] representations (else nullptr)
+  unsigned long long* cand_parts;  // candidate lists: [gamma][n_part][cand_R][kCandK] keys
+  int cand, cand_R;              // step mode: also keep the CTA's top-kCandK per request
   unsigned long long* keys;      // step: [gamma][R_max]; residual: [2][R_max]
   float2* parts;                 // step: [gamma][n_part][R_max]
   float* res_sums;               // residual: [2][R_max]
@@ -65,6 +67,46 @@ __device__ __forceinline__ int unpack16(const uint4& q, float* w) {
   }
 }
 
+// Candidate lists of one CTA: per request a sorted top-kCandK of packed
+// (biased logit, token) keys, a threshold (its kCandK-th key, or 0 while it
+// is not full) and an append buffer for one tile (at most kSimtTileV keys).
+// One warp merges a request's buffer into its list: kCandK rounds of a
+// warp-wide maximum over the list and the buffer (keys are unique: the token
+// index is part of the key).
+__device__ __forceinline__ void cand_merge(unsigned long long* list, unsigned long long* buf,
+                                           unsigned long long* thr, int* cnt, int nr, int warp,
+                                           int lane) {
+  for (int rr = warp; rr < nr; rr += kSimtThreads / 32) {
+    const int n = cnt[rr];
+    if (n == 0) continue;
+    unsigned long long k[1 + kSimtTileV / 32];
+    k[0] = lane < kCandK ? list[rr * kCandK + lane] : 0ull;
+#pragma unroll
+    for (int q = 0; q < kSimtTileV / 32; ++q) {
+      const int i = lane + 32 * q;
+      k[q + 1] = i < n ? buf[rr * kSimtTileV + i] : 0ull;
+    }
+    __syncwarp();
+    for (int t = 0; t < kCandK; ++t) {
+      unsigned long long m = 0ull;
+#pragma unroll
+      for (int q = 0; q < 1 + kSimtTileV / 32; ++q) m = k[q] > m ? k[q] : m;
+      const unsigned long long wm = warp_max_u64(m);
+      if (wm != 0ull && m == wm) {
+#pragma unroll
+        for (int q = 0; q < 1 + kSimtTileV / 32; ++q)
+          if (k[q] == wm) k[q] = 0ull;
+      }
+      if (lane == 0) list[rr * kCandK + t] = wm;
+    }
+    __syncwarp();
+    if (lane == 0) {
+      thr[rr] = list[rr * kCandK + kCandK - 1];
+      cnt[rr] = 0;
+    }
+  }
+}
+
 template <typename T, int MODE>
 __global__ void __launch_bounds__(kSimtThreads) simt_bias_kernel(SimtParams p) {
   extern __shared__ __align__(16) unsigned char smem[];
@@ -74,6 +116,12 @@ __global__ void __launch_bounds__(kSimtThreads) simt_bias_kernel(SimtParams p) {
   const int mstride = rank + 4;
   unsigned char* Ws = smem;
   float* ms = reinterpret_cast<float*>(smem + (size_t)kSimtTileV * nch * 16);
+  // candidate lists (step mode with p.cand), after ms
+  unsigned long long* c_list = reinterpret_cast<unsigned long long*>(ms + (size_t)kSimtRC * (rank + 4));
+  unsigned long long* c_buf = c_list + kSimtRC * kCandK;
+  unsigned long long* c_thr = c_buf + kSimtRC * kSimtTileV;
+  int* c_cnt = reinterpret_cast<int*>(c_thr + kSimtRC);
+  const bool cand = (MODE == kModeStep) && p.cand;
 
   __shared__ int s_prev[kSimtRC];
   __shared__ int s_req[kSimtRC];
@@ -143,6 +191,13 @@ __global__ void __launch_bounds__(kSimtThreads) simt_bias_kernel(SimtParams p) {
                 : act_apply(ld_elem(E, (size_t)s_prev[rr] * rank + k), p.act);
       ms[rr * mstride + k] = m;
     }
+    if (cand) {
+      for (int i = tid; i < kSimtRC * kCandK; i += kSimtThreads) c_list[i] = 0ull;
+      if (tid < kSimtRC) {
+        c_thr[tid] = 0ull;
+        c_cnt[tid] = 0;
+      }
+    }
 
     Lse2 st[kSimtRPT];
     unsigned long long best[kSimtRPT], best2[kSimtRPT];
@@ -159,6 +214,7 @@ __global__ void __launch_bounds__(kSimtThreads) simt_bias_kernel(SimtParams p) {
     for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
       const int v0 = tile * kSimtTileV;
       __syncthreads();
+      if (cand) cand_merge(c_list, c_buf, c_thr, c_cnt, nr, warp, lane);   // the previous tile's
       const int total = kSimtTileV * nch;
       for (int c = tid; c < total; c += kSimtThreads) {
         const int row = c / nch, ch = c - row * nch;
@@ -192,6 +248,10 @@ __global__ void __launch_bounds__(kSimtThreads) simt_bias_kernel(SimtParams p) {
         const float x = acc[i] + ld_elem(U, (size_t)s_row[rr] * p.V + v);
         const uint32_t rid = s_rid[rr];
         if constexpr (MODE == kModeStep) {
+          if (cand) {
+            const unsigned long long ck = make_key(x, (uint32_t)v);
+            if (ck > c_thr[rr]) c_buf[rr * kSimtTileV + atomicAdd(&c_cnt[rr], 1)] = ck;
+          }
           const float xs = p.sampled ? x * p.inv_T : x;
           const float x2 = xs * kLog2e;
           const float M = fmaxf(st[i].m, x2);
@@ -267,16 +327,30 @@ __global__ void __launch_bounds__(kSimtThreads) simt_bias_kernel(SimtParams p) {
         atomicAdd(&p.res_sums[p.R_max + req], f2);
       }
     }
+    if (cand) {   // the last tile's candidates, then this CTA's lists
+      __syncthreads();
+      cand_merge(c_list, c_buf, c_thr, c_cnt, nr, warp, lane);
+      __syncthreads();
+      for (int i = tid; i < nr * kCandK; i += kSimtThreads) {
+        const int rr = i / kCandK, q = i - rr * kCandK;
+        p.cand_parts[(((size_t)p.j * p.n_part + blockIdx.x) * p.cand_R + s_req[rr]) * kCandK + q] =
+            c_list[i];
+      }
+    }
   }
 }
 
-static size_t simt_smem_bytes(int rank, int elem_bytes) {
-  return (size_t)kSimtTileV * rank * elem_bytes + (size_t)kSimtRC * (rank + 4) * sizeof(float);
+static size_t simt_smem_bytes(int rank, int elem_bytes, bool cand) {
+  size_t b = (size_t)kSimtTileV * rank * elem_bytes + (size_t)kSimtRC * (rank + 4) * sizeof(float);
+  if (cand)
+    b += sizeof(unsigned long long) * ((size_t)kSimtRC * (kCandK + kSimtTileV + 1)) +
+         sizeof(int) * kSimtRC;
+  return b;
 }
 
 template <typename T, int MODE>
 static cudaError_t launch_simt_typed(const SimtParams& sp, int grid, cudaStream_t s) {
-  const size_t smem = simt_smem_bytes(sp.rank, (int)sizeof(T));
+  const size_t smem = simt_smem_bytes(sp.rank, (int)sizeof(T), MODE == kModeStep && sp.cand);
   cudaError_t e = cudaFuncSetAttribute(simt_bias_kernel<T, MODE>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
@@ -332,6 +406,11 @@ cudaError_t launch_propose_simt(const Ctx& ctx, const ProposeArgs& a, cudaStream
                                   sizeof(unsigned long long) * (size_t)a.gamma * ctx.cfg.R_max, s);
   if (e != cudaSuccess) return e;
   const int grid = simt_grid(ctx, a.V);
+  if (a.cand_tok) {   // keep the Markov candidate lists of every step
+    sp.cand = 1;
+    sp.cand_parts = ctx.ws.cand_parts;
+    sp.cand_R = ctx.cfg.R_max < kCandMaxR ? ctx.cfg.R_max : kCandMaxR;
+  }
   if (a.gate_h) {   // gated head: the hidden-state part of every gate, once
     sp.A = a.gated_rep;
     e = launch_gate_h(ctx, a, s);
@@ -494,6 +573,67 @@ cudaError_t launch_propose_finalize_n(const Ctx& ctx, const ProposeArgs& a, int 
 
 cudaError_t launch_propose_finalize(const Ctx& ctx, const ProposeArgs& a, cudaStream_t s) {
   return launch_propose_finalize_n(ctx, a, simt_grid(ctx, a.V), s);
+}
+
+// ---------------------------------------------------------------------------
+// Candidate sets: per (r, j) the top-kCandK of the CTAs' sorted lists.  Lane
+// l of the row's warp owns lists l, l + 32, ... (at most kCandLPL); each of
+// kCandK rounds takes the warp-wide maximum of the list heads and advances
+// the list that held it.
+// ---------------------------------------------------------------------------
+constexpr int kCandLPL = 16;   // lists per lane: n_used <= 512
+
+__global__ void __launch_bounds__(256) cand_finalize_kernel(const unsigned long long* parts,
+                                                            int n_used, int n_part, int cand_R,
+                                                            int R, int gamma, int32_t* tok,
+                                                            float* logit) {
+  const int lane = threadIdx.x & 31;
+  const int row = blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
+  if (row >= R * gamma) return;
+  const int r = row / gamma, j = row - r * gamma;
+  const unsigned long long* base = parts + (size_t)j * n_part * cand_R * kCandK;
+  unsigned long long head[kCandLPL];
+  int pos[kCandLPL];
+#pragma unroll
+  for (int i = 0; i < kCandLPL; ++i) {
+    const int c = lane + 32 * i;
+    pos[i] = 0;
+    head[i] = c < n_used ? base[((size_t)c * cand_R + r) * kCandK] : 0ull;
+  }
+  for (int t = 0; t < kCandK; ++t) {
+    unsigned long long lm = 0ull;
+    int li = 0;
+#pragma unroll
+    for (int i = 0; i < kCandLPL; ++i)
+      if (head[i] > lm) {
+        lm = head[i];
+        li = i;
+      }
+    const unsigned long long wm = warp_max_u64(lm);
+    if (wm != 0ull && lm == wm) {
+#pragma unroll
+      for (int i = 0; i < kCandLPL; ++i)
+        if (i == li) {
+          ++pos[i];
+          head[i] = pos[i] < kCandK
+                        ? base[((size_t)(lane + 32 * i) * cand_R + r) * kCandK + pos[i]]
+                        : 0ull;
+        }
+    }
+    if (lane == 0) {
+      tok[(size_t)row * kCandK + t] = wm ? (int32_t)key_index(wm) : -1;
+      logit[(size_t)row * kCandK + t] = wm ? key_value(wm) : -INFINITY;
+    }
+  }
+}
+
+cudaError_t launch_cand_finalize(const Ctx& ctx, const ProposeArgs& a, int n_used, cudaStream_t s) {
+  const int rows = a.R * a.gamma;
+  const int cand_R = ctx.cfg.R_max < kCandMaxR ? ctx.cfg.R_max : kCandMaxR;
+  cand_finalize_kernel<<<(rows + 7) / 8, 256, 0, s>>>(ctx.ws.cand_parts, n_used, ctx.n_part, cand_R,
+                                                      a.R, a.gamma, a.cand_tok, a.cand_logit);
+  count_launch(ctx);
+  return cudaGetLastError();
 }
 
 }  // namespace dsd
