@@ -586,6 +586,75 @@ def run_gated(args, dsd, synth, dev, world):
     return line
 
 
+def run_candidates(args, dsd, synth, dev, world):
+    """The proposal with the Markov top-16 candidate sets on the greedy
+    workload (R=16, gamma=7, V=151936, rank 256), CUDA-core engine; beside it
+    the plain proposal on the same engine; L2 flushed between steps."""
+    import torch
+
+    spec = synth.CYCLE_SPECS["greedy"]
+    x = synth.cycle_inputs(spec, device=dev)
+    ctx = dsd.Context(spec.V, spec.r, spec.G, spec.R, dtype="bf16", engine="simt",
+                      device=dev.index)
+    stream = torch.cuda.Stream(device=dev)
+    flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    pa = (x["U"], x["E"], x["W"], x["conf"], x["prev_tok"])
+    out = plain = None
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            out = ctx.propose_candidates(*pa, req_id=x["req_id"], out=out, stream=stream)
+            plain = ctx.propose(*pa, req_id=x["req_id"], out=plain, stream=stream)
+    stream.synchronize()
+    assert ctx.sync_status(stream) == 0
+    c0 = ctx.launch_count()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    clocks = ClockSampler(gpu_uuid(dev.index))
+    clocks.start()
+    time.sleep(0.3)
+    barrier(world)
+    with torch.cuda.stream(stream):
+        for e in evs:
+            flush.zero_()
+            e[0].record(stream)
+            out = ctx.propose_candidates(*pa, req_id=x["req_id"], out=out, stream=stream)
+            e[1].record(stream)
+            flush.zero_()
+            e[2].record(stream)
+            plain = ctx.propose(*pa, req_id=x["req_id"], out=plain, stream=stream)
+            e[3].record(stream)
+    stream.synchronize()
+    clk = clocks.stop()
+    assert ctx.sync_status(stream) == 0
+    launches = ctx.launch_count() - c0
+    ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
+    ms = max_over_ranks(ms, world, dev)
+    plain_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in evs)
+    R, G, V, r = spec.R, spec.G, spec.V, spec.r
+    alg = G * V * r * 2 + R * G * V * 2 + R * G * r * 2 + R * G * 16 * 8
+    peak, peak_kind = hbm_peak()
+    achieved = alg / (ms / 1e3) / 1e9
+    line = {
+        "metric": "draft tokens/s with Markov top-16 candidate sets (CUDA-core engine) at R=16, "
+                  "gamma=7, V=151936, rank 256",
+        "value": world * R * G / (ms / 1e3), "unit": "draft tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "accumulate": "fp32", "data": "synthetic",
+        "config": {"workload": f"candidates: R={R} gamma={G} V={V} rank={r} bf16 greedy",
+                   "l2": "flushed between steps (512 MB write outside the events)"},
+        "plain_propose_ms": plain_ms,
+        "roofline": {"bound": "hbm", "kernel": "simt_bias_kernel", "achieved": achieved,
+                     "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)",
+                     "traffic": None, "alg_bytes": alg, "per": "one call",
+                     "alg_bytes_note": "W per step + U rows + E rows + candidate sets"},
+        "cpu_baseline": None, "e2e": None,
+        "gpu_launches": launches, "clocks": clk,
+    }
+    ctx.close()
+    return line
+
+
 def run_ours(args):
     import numpy as np
     import torch
@@ -604,9 +673,9 @@ def run_ours(args):
 
     if not os.path.exists(dsd.LIB_PATH):
         _build.build()
-    if args.workload in ("overlap", "loss", "confidence", "gated"):
+    if args.workload in ("overlap", "loss", "confidence", "gated", "candidates"):
         run = {"overlap": run_overlap, "loss": run_loss, "confidence": run_confidence,
-               "gated": run_gated}[args.workload]
+               "gated": run_gated, "candidates": run_candidates}[args.workload]
         line = run(args, dsd, synth, dev, world)
         if rank == 0:
             print(json.dumps(line), flush=True)
@@ -812,7 +881,7 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="highconc",
                     choices=["highconc", "greedy", "sampled", "tiny", "overlap", "loss",
-                             "confidence", "gated"])
+                             "confidence", "gated", "candidates"])
     ap.add_argument("--engine", default="auto", choices=["auto", "simt", "mma", "tcgen05"])
     ap.add_argument("--cpu-requests", type=int, default=128,
                     help="requests in the CPU-baseline sample")
@@ -825,7 +894,7 @@ def main(argv=None):
     args = ap.parse_args(argv)
     args.warmup = max(args.warmup, 3)   # at least 3 untimed warm-up steps
     if args.impl == "reference":
-        if args.workload in ("overlap", "loss", "confidence", "gated"):
+        if args.workload in ("overlap", "loss", "confidence", "gated", "candidates"):
             ap.error("the reference arm times the draft-verify cycle workloads")
         return run_reference(args)
     return run_ours(args)
