@@ -101,7 +101,10 @@ struct RowsParams {
   uint32_t k0, k1;
 };
 
-template <typename T>
+// SAMPLED is p.sampled as a template argument, so the greedy rows (a
+// running maximum only) get their own lean instantiation with more loads in
+// flight.
+template <typename T, bool SAMPLED>
 __global__ void __launch_bounds__(kRowThreads) verify_rows(RowsParams p) {
   constexpr int epc = 16 / (int)sizeof(T);
   __shared__ Lse2 red_l[kRowThreads / 32];
@@ -129,9 +132,10 @@ __global__ void __launch_bounds__(kRowThreads) verify_rows(RowsParams p) {
     uint32_t bv = 0xFFFFFFFFu;
     bool nan_seen = false;
     const int v_first = v_begin + tid * epc;
-    // Four 16-byte loads in flight per thread: with one, the grid keeps too
-    // few bytes in flight to cover the HBM latency.
-    constexpr int kUnroll = 4;
+    // Several 16-byte loads in flight per thread (eight for greedy rows,
+    // four with the sampled path's larger register set): with one, the grid
+    // keeps too few bytes in flight to cover the HBM latency.
+    constexpr int kUnroll = SAMPLED ? 4 : 8;
     for (int vb = v_first; vb < v_end; vb += kUnroll * kRowThreads * epc) {
       uint4 q[kUnroll];
 #pragma unroll
@@ -151,7 +155,7 @@ __global__ void __launch_bounds__(kRowThreads) verify_rows(RowsParams p) {
           x[0] = __uint_as_float(q[u].x); x[1] = __uint_as_float(q[u].y);
           x[2] = __uint_as_float(q[u].z); x[3] = __uint_as_float(q[u].w);
         }
-        if (!p.sampled) {
+        if constexpr (!SAMPLED) {
           float m = max3_nan(x[0], x[1], x[2]);
 #pragma unroll
           for (int e = 3; e < epc; e += 2)
@@ -201,7 +205,7 @@ __global__ void __launch_bounds__(kRowThreads) verify_rows(RowsParams p) {
         }
       }
     }
-    if (!p.sampled && v_first < v_end) {
+    if (!SAMPLED && v_first < v_end) {
       if (nan_seen) set_status(p.status, kErrNonfinite);
       // every element was -inf: the first one holds the maximum
       best = make_key(bz, bv == 0xFFFFFFFFu ? (uint32_t)v_first : bv);
@@ -365,10 +369,17 @@ cudaError_t launch_verify(const Ctx& ctx, const VerifyArgs& a, cudaStream_t s) {
   rp.k0 = k0;
   rp.k1 = k1;
   const int grid_rows = ctx.num_sms * 4;
-  if (ctx.cfg.dtype == 1)
-    verify_rows<__nv_bfloat16><<<grid_rows, kRowThreads, 0, s>>>(rp);
-  else
-    verify_rows<float><<<grid_rows, kRowThreads, 0, s>>>(rp);
+  if (ctx.cfg.dtype == 1) {
+    if (sampled)
+      verify_rows<__nv_bfloat16, true><<<grid_rows, kRowThreads, 0, s>>>(rp);
+    else
+      verify_rows<__nv_bfloat16, false><<<grid_rows, kRowThreads, 0, s>>>(rp);
+  } else {
+    if (sampled)
+      verify_rows<float, true><<<grid_rows, kRowThreads, 0, s>>>(rp);
+    else
+      verify_rows<float, false><<<grid_rows, kRowThreads, 0, s>>>(rp);
+  }
   count_launch(ctx);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
