@@ -809,12 +809,23 @@ def run_ours(args):
                                 temperature=T, seed=seed, out=ho, stream=stream)
         t_e2e = (time.perf_counter() - t0) / n_e2e
         t_e2e = max_over_ranks(t_e2e, world, dev)
-        h2d = sum(synth.bytes_of(t) for t in (hU, hP, hc, hp, hr))
+        in_place = ctx.last_p_in_place()
+        if in_place:
+            # P read in place: the kept rows (and, sampled, each rejected row
+            # once more for the residual) cross the CPU-GPU link
+            row = spec.V * (2 if spec.dtype == "bf16" else 4)
+            rejected = int((acc < keep).sum()) if T > 0 else 0
+            p_bytes = (B + rejected) * row
+        else:
+            p_bytes = synth.bytes_of(hP)
+        h2d = sum(synth.bytes_of(t) for t in (hU, hc, hp, hr)) + p_bytes
         d2h = sum(synth.bytes_of(ho[k]) for k in ("tokens", "keep_len", "accept_len", "next_token"))
         assert np.array_equal(ho["accept_len"].numpy(), acc)
         e2e = {"value": world / t_e2e, "unit": "cycles/s", "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "ms_per_step": t_e2e * 1e3,
-               "path": "dsd_cycle_host (pinned host inputs, staging copies inside the call)"}
+               "path": "dsd_cycle_host (pinned host inputs; U staged by copy, P read in place "
+                       "over the CPU-GPU link, only the kept rows)" if in_place else
+                       "dsd_cycle_host (pinned host inputs, staging copies inside the call)"}
 
     peak, peak_kind = hbm_peak()
     pbytes = propose_alg_bytes(spec)
@@ -834,10 +845,11 @@ def run_ours(args):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
-        h = host_arrays(x, rows=args.cpu_requests)
+        n_cpu = min(args.cpu_requests, spec.R)
+        h = host_arrays(x, rows=n_cpu)
         for k in ("E", "W"):
             h[k] = h[k].astype(np.float64)
-        est, desc, spent = oracle_sample_cycle(spec, h, args.cpu_requests, seed)
+        est, desc, spent = oracle_sample_cycle(spec, h, n_cpu, seed)
         cpu = {"value": 1.0 / est, "unit": "cycles/s", "cores": os.cpu_count(), "kind": "oracle",
                "sample": desc, "cpu_seconds": spent}
 

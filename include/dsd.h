@@ -132,6 +132,9 @@ uint64_t dsd_launch_count(const dsd_ctx* ctx);
  * DSD_ENGINE_MMA or DSD_ENGINE_TCGEN05 (DSD_ENGINE_AUTO before the first
  * call). */
 int dsd_last_engine(const dsd_ctx* ctx);
+/* 1 if the last dsd_cycle_host call read P in place from host memory, 0 if
+ * it staged P on the device. */
+int dsd_last_p_in_place(const dsd_ctx* ctx);
 
 /*
  * dsd_propose -- sequential Markov-head proposal plus prefix survival.
@@ -228,12 +231,16 @@ int dsd_cycle(dsd_ctx* ctx, int R, const void* U, const void* E, const void* W,
 
 /*
  * dsd_cycle_host -- one cycle from HOST buffers.  The per-cycle inputs
- * (U, P, conf, prev_tok, req_id) are copied host->device into staging
- * buffers owned by the context (allocated on the first call, sized for
- * R_max), the cycle runs, and tokens, keep_len, accept_len and next_token
- * are copied back to the host.  E, W and sps are device pointers (model
- * constants resident on the GPU).  Pinned host memory makes the copies
- * asynchronous; the call returns after the results are on the host.
+ * (U, conf, prev_tok, req_id) are copied host->device into staging buffers
+ * owned by the context (allocated on the first call, sized for R_max), the
+ * cycle runs, and tokens, keep_len, accept_len and next_token are copied
+ * back to the host.  P is read in place when the GPU can address P_host
+ * (pinned memory): verification reads only the rows the scheduler keeps,
+ * so only those cross the CPU-GPU link; pageable P is staged in full.
+ * dsd_last_p_in_place tells which happened.  E, W and sps are device
+ * pointers (model constants resident on the GPU).  The caller must not
+ * modify P_host until the call returns; the call returns after the results
+ * are on the host.
  */
 int dsd_cycle_host(dsd_ctx* ctx, int R, const void* U_host, const void* E, const void* W,
                    const float* conf_host, const int32_t* prev_tok_host,

@@ -33,7 +33,7 @@ ENGINES = {"auto": 0, "simt": 1, "tcgen05": 2, "mma": 3}
 
 EXPORTED = [
     "dsd_create", "dsd_destroy", "dsd_last_error", "dsd_sync_status", "dsd_workspace_bytes",
-    "dsd_launch_count", "dsd_last_engine",
+    "dsd_launch_count", "dsd_last_engine", "dsd_last_p_in_place",
     "dsd_propose", "dsd_schedule", "dsd_verify", "dsd_cycle", "dsd_cycle_host", "dsd_overlap",
     "dsd_propose_noalloc", "dsd_loss_forward", "dsd_confidence_head", "dsd_threshold_keep",
     "dsd_calibration", "dsd_propose_gated", "dsd_verify_gated", "dsd_propose_candidates",
@@ -78,6 +78,7 @@ def load_library(path: str | None = None):
         "dsd_workspace_bytes": (ctypes.c_size_t, [_P]),
         "dsd_launch_count": (_U64, [_P]),
         "dsd_last_engine": (_I, [_P]),
+        "dsd_last_p_in_place": (_I, [_P]),
         "dsd_propose": (_I, [_P, _I, _P, _P, _P, _P, _P, _P, _F, _U64, _P, _P, _P, _P, _P]),
         "dsd_schedule": (_I, [_P, _I, _P, _P, _I, _P, _P, _P]),
         "dsd_verify": (_I, [_P, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _F, _U64, _P, _P, _P]),
@@ -315,6 +316,10 @@ class Context:
         """'simt' or 'tcgen05': the engine of the last propose call."""
         code = int(load_library().dsd_last_engine(self.handle))
         return {v: k for k, v in ENGINES.items()}.get(code, "auto")
+
+    def last_p_in_place(self):
+        """True if the last cycle_host call read P in place from host memory."""
+        return bool(load_library().dsd_last_p_in_place(self.handle))
 
     def sync_status(self, stream=None):
         return dsd_sync_status(self.handle, stream, self.device)

@@ -196,6 +196,7 @@ size_t dsd_workspace_bytes(const dsd_ctx* ctx) { return ctx ? ctx->ws_bytes : 0;
 uint64_t dsd_launch_count(const dsd_ctx* ctx) { return ctx ? ctx->launches : 0; }
 
 int dsd_last_engine(const dsd_ctx* ctx) { return ctx ? ctx->last_engine : 0; }
+int dsd_last_p_in_place(const dsd_ctx* ctx) { return ctx ? ctx->last_p_in_place : 0; }
 
 int dsd_sync_status(dsd_ctx* ctx, void* stream) {
   int rc = check_ctx(ctx);
@@ -473,13 +474,29 @@ int dsd_cycle_host(dsd_ctx* ctx, int R, const void* U_host, const void* E, const
     if (e != cudaSuccess) return cuda_fail(ctx, e, "cudaMemcpyAsync");   \
   } while (0)
   DSD_CPY(b + o_U, U_host, (size_t)R * G * V * esz, cudaMemcpyHostToDevice);
-  DSD_CPY(b + o_P, P_host, (size_t)R * G1 * V * esz, cudaMemcpyHostToDevice);
+  // P is read in place when the GPU can address the caller's (pinned) host
+  // buffer: verification reads only the kept rows, so only those cross the
+  // CPU-GPU link.  Otherwise (pageable memory) the whole of P is staged.
+  const void* P_dev = nullptr;
+  {
+    cudaPointerAttributes pa;
+    if (cudaPointerGetAttributes(&pa, P_host) == cudaSuccess && pa.type == cudaMemoryTypeHost &&
+        pa.devicePointer != nullptr && aligned16(pa.devicePointer))
+      P_dev = pa.devicePointer;
+    else
+      (void)cudaGetLastError();
+  }
+  if (!P_dev) {
+    DSD_CPY(b + o_P, P_host, (size_t)R * G1 * V * esz, cudaMemcpyHostToDevice);
+    P_dev = b + o_P;
+  }
+  ctx->last_p_in_place = (P_dev != b + o_P) ? 1 : 0;
   DSD_CPY(b + o_conf, conf_host, sizeof(float) * R * G, cudaMemcpyHostToDevice);
   DSD_CPY(b + o_prev, prev_tok_host, sizeof(int32_t) * R, cudaMemcpyHostToDevice);
   if (req_id_host) DSD_CPY(b + o_req, req_id_host, sizeof(uint32_t) * R, cudaMemcpyHostToDevice);
   rc = dsd_cycle(ctx, R, b + o_U, E, W, reinterpret_cast<float*>(b + o_conf),
                  reinterpret_cast<int32_t*>(b + o_prev),
-                 req_id_host ? reinterpret_cast<uint32_t*>(b + o_req) : nullptr, b + o_P, sps,
+                 req_id_host ? reinterpret_cast<uint32_t*>(b + o_req) : nullptr, P_dev, sps,
                  n_sps, temperature, seed, reinterpret_cast<int32_t*>(b + o_tok),
                  reinterpret_cast<float*>(b + o_lse), reinterpret_cast<float*>(b + o_lg),
                  reinterpret_cast<float*>(b + o_sv), reinterpret_cast<int32_t*>(b + o_keep),

@@ -76,6 +76,7 @@ struct Ctx {
   char err[512];
   mutable unsigned long long launches;  // kernels launched by this context
   int last_engine;                      // engine of the last propose (enum dsd_engine)
+  int last_p_in_place;                  // dsd_cycle_host: 1 if P was read in place from host memory
 };
 
 inline void count_launch(const Ctx& c, int n = 1) { c.launches += (unsigned long long)n; }

@@ -398,3 +398,28 @@ def test_auto_engine_choice(dsd, R, dtype, act, expect):
     assert ctx.sync_status() == 0
     assert ctx.last_engine() == expect
     ctx.close()
+
+
+@pytest.mark.parametrize("temperature", [0.0, 1.0])
+def test_cycle_host_matches_the_device_cycle(dsd, temperature):
+    """dsd_cycle_host from host buffers gives the device cycle's results: with
+    pinned P (read in place over the CPU-GPU link) and with pageable P
+    (staged on the device)."""
+    spec = synth.scaled(synth.CYCLE_SPECS["greedy"], temperature=temperature, seed=33,
+                        p_noise=1.0 if temperature else 0.5, **SMALL)
+    x = synth.cycle_inputs(spec, device=DEV)
+    ctx = dsd.Context(spec.V, spec.r, spec.G, spec.R, dtype="bf16")
+    dev = ctx.cycle(x["U"], x["E"], x["W"], x["conf"], x["prev_tok"], x["P"], x["sps"],
+                    req_id=x["req_id"], temperature=temperature, seed=x["seed"])
+    host = {k: x[k].cpu() for k in ("U", "conf", "prev_tok", "req_id", "P")}
+    for pinned in (True, False):
+        h = {k: (v.pin_memory() if pinned else v) for k, v in host.items()}
+        if not pinned:
+            h["U"] = h["U"].pin_memory()
+        out = ctx.cycle_host(h["U"], x["E"], x["W"], h["conf"], h["prev_tok"], h["P"], x["sps"],
+                             req_id_host=h["req_id"], temperature=temperature, seed=x["seed"])
+        assert ctx.sync_status() == 0
+        assert ctx.last_p_in_place() == pinned
+        for k in ("tokens", "keep_len", "accept_len", "next_token"):
+            assert torch.equal(out[k], dev[k].cpu()), (pinned, k)
+    ctx.close()
