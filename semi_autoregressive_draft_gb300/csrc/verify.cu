@@ -210,7 +210,7 @@ __global__ void __launch_bounds__(kRowThreads) verify_rows(RowsParams p) {
       // every element was -inf: the first one holds the maximum
       best = make_key(bz, bv == 0xFFFFFFFFu ? (uint32_t)v_first : bv);
     }
-    st = warp_lse2(st);
+    if constexpr (SAMPLED) st = warp_lse2(st);   // greedy rows have no normaliser
     best = warp_max_u64(best);
     if (lane == 0) {
       red_l[warp] = st;
@@ -221,7 +221,7 @@ __global__ void __launch_bounds__(kRowThreads) verify_rows(RowsParams p) {
       Lse2 l = lse2_empty();
       unsigned long long k = 0ull;
       for (int w = 0; w < kRowThreads / 32; ++w) {
-        l = lse2_merge(l, red_l[w]);
+        if constexpr (SAMPLED) l = lse2_merge(l, red_l[w]);
         k = red_k[w] > k ? red_k[w] : k;
       }
       p.parts[item] = RowPart{l.m, l.s, k};
