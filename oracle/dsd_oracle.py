@@ -313,6 +313,9 @@ def schedule(a, sps):
     """Greedy global allocation maximising Theta = tau * SPS(B).
 
     a is [R, gamma] (prefix survival, non-increasing in j); sps[B-1] = SPS(B).
+    A survival is a product of probabilities, so values outside [0, 1] are
+    clamped to it (the reading taken for confidences, applied to the
+    scheduler's own input).
     Start from l_r = 0: B = R, tau = R, Theta* = R * SPS(R).  Visit the
     (r, j) items in order of a descending (ties: r, then j ascending); each
     visit adds one verify slot (B += 1) and its expected token (tau += a).
@@ -323,7 +326,7 @@ def schedule(a, sps):
     Returns dict(keep_len [R] int, theta, B, theta_gap) where theta_gap is the
     relative gap between Theta* and the best Theta at any other cut (used to
     count near-ties)."""
-    a = _f64(a)
+    a = np.clip(_f64(a), 0.0, 1.0)
     sps = _f64(sps)
     R, G = a.shape
     n_sps = sps.shape[0]
