@@ -7,8 +7,10 @@ bf16 tables, greedy, SPS(B) flat at 1e3 steps/s up to B = 256 then ~1/B
 (1024 entries).  Inputs are seeded synthetic tensors resident in HBM; each
 timed step is one cycle, captured as a single CUDA graph and bracketed by
 CUDA events on the launching stream; L2 is flushed (a 512 MB write) between
-steps, outside the events.  A second pass replays one graph per phase, with
-an event between phases, for the phase breakdown and the propose roofline.
+steps, outside the events.  The cycle is the library's one-call dsd_cycle,
+which runs the schedule inside the proposal's last launch.  A second pass
+replays dsd_propose, dsd_schedule and dsd_verify as one graph each, with an
+event between them, for the phase breakdown and the propose roofline.
 
 Prints ONE JSON line (rank 0).  --impl reference times the fp64 CPU oracle on
 the host cores on bounded samples of the same workload instead.
@@ -198,11 +200,27 @@ def workload_label(spec):
             f"{mode}, SPS {spec.sps_kind}")
 
 
+def propose_step_bytes(spec):
+    """Bytes one draft-step launch must move: the U rows of its position, all
+    of the projection W (every step projects onto the whole vocabulary, and
+    the step before evicts most of it from L2 while streaming its own U
+    rows), the gathered E rows and the argmax keys."""
+    esz = 2 if spec.dtype == "bf16" else 4
+    R, V, r = spec.R, spec.V, spec.r
+    return R * V * esz + V * r * esz + R * r * esz + R * 8
+
+
 def propose_alg_bytes(spec):
-    """Bytes the propose phase must move: every U row once, the projection W
-    once (compulsory; every draft step needs all of it, and it can stay in
-    L2 across steps), the gathered E rows, confidences, previous tokens and
-    the four [R, gamma] outputs."""
+    """Bytes of the propose phase with W counted once per draft step: gamma
+    step launches plus the confidences, previous tokens and the four
+    [R, gamma] outputs."""
+    R, G = spec.R, spec.G
+    return G * propose_step_bytes(spec) + R * G * 4 + R * 4 + 4 * R * G * 4
+
+
+def propose_w_once_bytes(spec):
+    """The phase's compulsory bytes: every U row once and W once for the
+    whole phase (the lower bound if W stayed in L2 across the steps)."""
     esz = 2 if spec.dtype == "bf16" else 4
     R, G, V, r = spec.R, spec.G, spec.V, spec.r
     return (R * G * V * esz + V * r * esz + R * G * r * esz + R * G * 4 + R * 4
@@ -704,15 +722,24 @@ def run_ours(args):
                        x["req_id"], T, seed, out["accept_len"], out["next_token"], None,
                        local_rank)
 
+    def cycle():
+        # the public one-call cycle: the schedule runs inside the proposal's
+        # last launch
+        dsd.dsd_cycle(ctx.handle, spec.R, x["U"], x["E"], x["W"], x["conf"], x["prev_tok"],
+                      x["req_id"], x["P"], x["sps"], x["sps"].numel(), T, seed, out["tokens"],
+                      out["lse_q"], out["logit_at_tok"], out["survival"], out["keep_len"],
+                      out["theta_B"], out["accept_len"], out["next_token"], None, local_rank)
+
     with torch.cuda.stream(stream):
         for _ in range(2):               # eager warm-up (sets kernel attributes)
             propose(); schedule(); verify()
+            cycle()
     stream.synchronize()
     assert ctx.sync_status(stream) == 0
     # the timed cycle is one graph; one graph per phase serves the breakdown
     g_cycle = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g_cycle, stream=stream):
-        propose(); schedule(); verify()
+        cycle()
     graphs = []
     for fn in (propose, schedule, verify):
         g = torch.cuda.CUDAGraph()
@@ -738,7 +765,7 @@ def run_ours(args):
     # count kernels per cycle from the library's own launch counter
     c0 = ctx.launch_count()
     with torch.cuda.stream(stream):
-        propose(); schedule(); verify()
+        cycle()
     launches_per_cycle_eager = ctx.launch_count() - c0
     del launches_before_warm
 
@@ -789,6 +816,31 @@ def run_ours(args):
     tokens_per_cycle = int((acc + 1).sum())
     B = int((keep + 1).sum())
 
+    # acceptance of the scheduled cycle, and of one untimed pass that keeps
+    # every draft position (l = gamma for all requests), so the histogram and
+    # the per-position conditional accept rate cover every position
+    keep_all = torch.full_like(out["keep_len"], spec.G)
+    acc_all_t = torch.empty_like(out["accept_len"])
+    nxt_all = torch.empty_like(out["next_token"])
+    with torch.cuda.stream(stream):
+        dsd.dsd_verify(ctx.handle, spec.R, x["P"], x["U"], x["E"], x["W"], x["prev_tok"],
+                       out["tokens"], out["lse_q"], out["logit_at_tok"], keep_all,
+                       x["req_id"], T, seed, acc_all_t, nxt_all, None, local_rank)
+    stream.synchronize()
+    acc_all = acc_all_t.cpu().numpy()
+    acceptance = {
+        "scheduled": {"accept_len_hist": np.bincount(acc, minlength=spec.G + 1).tolist(),
+                      "keep_len_hist": np.bincount(keep, minlength=spec.G + 1).tolist(),
+                      "mean_accept_len": float(acc.mean())},
+        "keep_all": {"accept_len_hist": np.bincount(acc_all, minlength=spec.G + 1).tolist(),
+                     "per_position_accept_rate": [
+                         float((acc_all > i).sum() / max(1, (acc_all >= i).sum()))
+                         for i in range(spec.G)],
+                     "mean_accept_len": float(acc_all.mean())},
+        "note": "per_position_accept_rate[i] = #(accept_len > i) / #(accept_len >= i), "
+                "the rate at which position i is accepted once it is tested",
+    }
+
     # e2e: same cycle from pinned host buffers through dsd_cycle_host
     e2e = None
     if not args.no_e2e:
@@ -831,6 +883,7 @@ def run_ours(args):
     pbytes = propose_alg_bytes(spec)
     prop_mean_s = statistics.mean(prop_ms) / 1e3
     achieved = pbytes / prop_mean_s / 1e9
+    w_once = propose_w_once_bytes(spec) / prop_mean_s / 1e9
     engine_used = ctx.last_engine()
     engine_kernel = {"tcgen05": "propose_tc_kernel", "mma": "propose_mma_kernel"}.get(
         engine_used, "simt_bias_kernel")
@@ -838,9 +891,15 @@ def run_ours(args):
                 "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                 "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)",
                 "traffic": traffic_for(engine_kernel, spec.name),
-                "alg_bytes": pbytes,
-                "per": "propose phase (the gamma draft-step launches and the finalize)",
-                "alg_bytes_note": "U rows once + W once + gathered E rows + small I/O"}
+                "alg_bytes": propose_step_bytes(spec),
+                "per": "one draft-step launch; achieved = gamma launches' bytes + the phase's "
+                       "small I/O over the propose phase's mean time (gamma launches and the "
+                       "finalize)",
+                "alg_bytes_note": "per launch: the U rows of one position + all of W + the "
+                                  "gathered E rows + the argmax keys",
+                "w_once": {"achieved": w_once, "frac": w_once / peak,
+                           "alg_bytes": propose_w_once_bytes(spec),
+                           "note": "the same time against U rows once + W once per phase"}}
     vbytes = verify_alg_bytes(spec, B)
 
     cpu = None
@@ -867,8 +926,11 @@ def run_ours(args):
                    "l2": "flushed between steps (512 MB write outside the events); inputs 1.2 GB"},
         "phases_ms": {"propose": statistics.mean(prop_ms), "schedule": statistics.mean(sch_ms),
                       "verify": statistics.mean(ver_ms),
-                      "note": "separate pass, one graph per phase (adds a graph launch each)"},
+                      "note": "separate pass through dsd_propose, dsd_schedule and dsd_verify, "
+                              "one graph each (adds a graph launch each); the timed cycle "
+                              "(dsd_cycle) runs the schedule inside the proposal's last launch"},
         "verify_alg_GBps": vbytes / (statistics.mean(ver_ms) / 1e3) / 1e9,
+        "acceptance": acceptance,
         "roofline": roofline,
         "cpu_baseline": cpu,
         "e2e": e2e,

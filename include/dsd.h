@@ -180,13 +180,17 @@ int dsd_propose(dsd_ctx* ctx, int R, const void* U, const void* E, const void* W
  * the strictly largest Theta.  Because survival is non-increasing in j the
  * kept slots form a prefix of every request.
  *
- * survival [R, gamma] f32        (dsd_propose's output, values in [0, 1])
+ * survival [R, gamma] f32        (dsd_propose's output, values in [0, 1];
+ *                                 others are clamped to [0, 1], non-finite
+ *                                 ones count as 0 and set DSD_ERR_NONFINITE
+ *                                 in the status word)
  * sps      [n_sps]    f32        sps[B-1] = SPS(B), steps/s at verify batch B
  * keep_len [R]        i32  out   l_r in 0..gamma
  * theta_B  [2]        f32  out   {Theta*, B*}
  * R > n_sps returns DSD_ERR_CAPACITY; slots that would push B past n_sps are
- * never taken.  Also records B* and the verify row list in the workspace for
- * a following dsd_verify on the same stream.
+ * never taken.  The running sums are exact (integers in units of 2^-48), so
+ * the cut matches an exact evaluation of Theta up to fp64 rounding of the
+ * final products.
  */
 int dsd_schedule(dsd_ctx* ctx, int R, const float* survival, const float* sps, int n_sps,
                  int32_t* keep_len, float* theta_B, void* stream);
@@ -220,7 +224,11 @@ int dsd_verify(dsd_ctx* ctx, int R, const void* P, const void* U, const void* E,
 /*
  * dsd_cycle -- dsd_propose, dsd_schedule and dsd_verify back to back on one
  * stream ([WALK] 4.2 serving loop, one iteration, whole batch).  Outputs as
- * the three calls; theta_B may be NULL.
+ * the three calls; theta_B may be NULL.  The schedule depends on the
+ * confidences only, so it runs in extra CTAs of the proposal's last launch,
+ * from the survivals computed there exactly as dsd_propose computes its
+ * survival output (same allocation as dsd_schedule on that output).
+ * Argument errors of any of the three return before any launch.
  */
 int dsd_cycle(dsd_ctx* ctx, int R, const void* U, const void* E, const void* W,
               const float* conf, const int32_t* prev_tok, const uint32_t* req_id,

@@ -49,16 +49,16 @@ size_t carve(dsd_ctx* c, unsigned char* base) {
   w.counters = reinterpret_cast<unsigned int*>(take(sizeof(unsigned int) * 16));
   w.keys = reinterpret_cast<unsigned long long*>(take(sizeof(unsigned long long) * (size_t)G * Rm));
   w.lse_parts = reinterpret_cast<float2*>(take(sizeof(float2) * (size_t)G * c->n_part * Rm));
-  w.sched_B = reinterpret_cast<int*>(take(sizeof(int) * 4));
-  w.rows = reinterpret_cast<int2*>(take(sizeof(int2) * (size_t)Rm * (G + 1)));
   w.vparts = reinterpret_cast<RowPart*>(take(sizeof(RowPart) * (size_t)Rm * (G + 1) * kVerifySplits));
   w.rej_list = reinterpret_cast<int*>(take(sizeof(int) * (size_t)Rm));
-  w.rej_k = reinterpret_cast<int*>(take(sizeof(int) * 2 * (size_t)Rm));  // + row offsets
+  w.rej_k = reinterpret_cast<int*>(take(sizeof(int) * (size_t)Rm));
   w.rej_lseP = reinterpret_cast<float*>(take(sizeof(float) * (size_t)Rm));
   w.res_keys = reinterpret_cast<unsigned long long*>(take(sizeof(unsigned long long) * 2 * (size_t)Rm));
   w.res_sums = reinterpret_cast<float*>(take(sizeof(float) * 2 * (size_t)Rm));
   w.ov_parts = reinterpret_cast<float*>(take(sizeof(float) * 64));
-  w.sched_order = reinterpret_cast<int*>(take(sizeof(int) * (size_t)Rm * G));
+  w.sched_theta = reinterpret_cast<unsigned long long*>(
+      take(sizeof(unsigned long long) * (kMaxSchedItems + 1)));   // + the running maximum
+  w.sched_order = reinterpret_cast<int*>(take(sizeof(int) * kMaxSchedItems));
   w.tickets = reinterpret_cast<unsigned int*>(take(sizeof(unsigned int) * 64));
   const size_t loss_rows = (size_t)Rm * G;
   w.loss_parts1 = reinterpret_cast<float4*>(take(sizeof(float4) * c->num_sms * loss_rows));
@@ -215,10 +215,13 @@ int dsd_sync_status(dsd_ctx* ctx, void* stream) {
   return st;
 }
 
-int dsd_propose(dsd_ctx* ctx, int R, const void* U, const void* E, const void* W,
-                const float* conf, const int32_t* prev_tok, const uint32_t* req_id,
-                float temperature, uint64_t seed, int32_t* tokens, float* lse_q,
-                float* logit_at_tok, float* survival, void* stream) {
+// dsd_propose, optionally with the cycle's schedule folded into the
+// finalize launch (sps != nullptr).
+static int propose_impl(dsd_ctx* ctx, int R, const void* U, const void* E, const void* W,
+                        const float* conf, const int32_t* prev_tok, const uint32_t* req_id,
+                        float temperature, uint64_t seed, int32_t* tokens, float* lse_q,
+                        float* logit_at_tok, float* survival, const float* sps, int n_sps,
+                        int32_t* keep_len, float* theta_B, void* stream) {
   int rc = check_ctx(ctx);
   if (rc) return rc;
   if ((rc = check_R(ctx, R))) return rc;
@@ -250,6 +253,12 @@ int dsd_propose(dsd_ctx* ctx, int R, const void* U, const void* E, const void* W
   a.lse_q = lse_q;
   a.logit_at_tok = logit_at_tok;
   a.survival = survival;
+  if (sps) {
+    a.sched_sps = sps;
+    a.sched_n_sps = n_sps;
+    a.sched_keep = keep_len;
+    a.sched_theta = theta_B;
+  }
   cudaError_t e;
   int n_used;
   if (ctx->cfg.engine == DSD_ENGINE_TCGEN05 || auto_uses_tc(ctx, R)) {
@@ -274,6 +283,14 @@ int dsd_propose(dsd_ctx* ctx, int R, const void* U, const void* E, const void* W
   e = launch_propose_finalize_n(*ctx, a, n_used, s);
   if (e != cudaSuccess) return cuda_fail(ctx, e, "propose finalize launch");
   return DSD_OK;
+}
+
+int dsd_propose(dsd_ctx* ctx, int R, const void* U, const void* E, const void* W,
+                const float* conf, const int32_t* prev_tok, const uint32_t* req_id,
+                float temperature, uint64_t seed, int32_t* tokens, float* lse_q,
+                float* logit_at_tok, float* survival, void* stream) {
+  return propose_impl(ctx, R, U, E, W, conf, prev_tok, req_id, temperature, seed, tokens, lse_q,
+                      logit_at_tok, survival, nullptr, 0, nullptr, nullptr, stream);
 }
 
 int dsd_schedule(dsd_ctx* ctx, int R, const float* survival, const float* sps, int n_sps,
@@ -335,6 +352,17 @@ static int verify_impl(dsd_ctx* ctx, int R, const void* P, const void* U, const 
   a.accept_len = accept_len;
   a.next_token = next_token;
   a.gated_rep = gated_rep;
+  // Where P lives decides how it is read: device memory through bulk copies
+  // into shared memory, anything else (pinned host memory read in place,
+  // managed or system memory) with plain loads.  One pointer is remembered.
+  if (P != ctx->p_class_ptr) {
+    cudaPointerAttributes attr{};
+    const cudaError_t pe = cudaPointerGetAttributes(&attr, P);
+    if (pe != cudaSuccess) (void)cudaGetLastError();
+    ctx->p_class_host = (pe == cudaSuccess && attr.type == cudaMemoryTypeDevice) ? 0 : 1;
+    ctx->p_class_ptr = P;
+  }
+  a.P_on_host = ctx->p_class_host;
   cudaError_t e = launch_verify(*ctx, a, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(ctx, e, "verify launch");
   return DSD_OK;
@@ -417,10 +445,17 @@ int dsd_cycle(dsd_ctx* ctx, int R, const void* U, const void* E, const void* W, 
               int n_sps, float temperature, uint64_t seed, int32_t* tokens, float* lse_q,
               float* logit_at_tok, float* survival, int32_t* keep_len, float* theta_B,
               int32_t* accept_len, int32_t* next_token, void* stream) {
-  int rc = dsd_propose(ctx, R, U, E, W, conf, prev_tok, req_id, temperature, seed, tokens, lse_q,
-                       logit_at_tok, survival, stream);
+  // the schedule depends on the confidences only: it runs in extra CTAs of
+  // the proposal's finalize launch
+  int rc = check_ctx(ctx);
   if (rc) return rc;
-  rc = dsd_schedule(ctx, R, survival, sps, n_sps, keep_len, theta_B, stream);
+  if ((rc = check_R(ctx, R))) return rc;
+  if (R == 0) return DSD_OK;
+  if (!sps || !keep_len) return fail(ctx, DSD_ERR_ARG, "dsd_cycle: NULL argument");
+  if (n_sps < 1) return fail(ctx, DSD_ERR_ARG, "n_sps = %d", n_sps);
+  if (R > n_sps) return fail(ctx, DSD_ERR_CAPACITY, "R = %d exceeds the SPS table (%d)", R, n_sps);
+  rc = propose_impl(ctx, R, U, E, W, conf, prev_tok, req_id, temperature, seed, tokens, lse_q,
+                    logit_at_tok, survival, sps, n_sps, keep_len, theta_B, stream);
   if (rc) return rc;
   return dsd_verify(ctx, R, P, U, E, W, prev_tok, tokens, lse_q, logit_at_tok, keep_len, req_id,
                     temperature, seed, accept_len, next_token, stream);

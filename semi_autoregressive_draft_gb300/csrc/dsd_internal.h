@@ -38,8 +38,6 @@ struct Workspace {
   unsigned int* counters;       // [16] tickets / barrier counters (zeroed per call)
   unsigned long long* keys;     // [gamma][R_max] argmax keys of the propose steps
   float2* lse_parts;            // [gamma][n_part][R_max] (m, s) partials
-  int* sched_B;                 // [1] verify batch B* of the last schedule
-  int2* rows;                   // [R_max*(gamma+1)] verify rows (r, t)
   RowPart* vparts;              // [R_max*(gamma+1)][kVerifySplits]
   int* rej_list;                // [R_max] requests with a rejection (sampled verify)
   int* rej_k;                   // [R_max] rejection position per request
@@ -47,7 +45,8 @@ struct Workspace {
   unsigned long long* res_keys; // [2][R_max] residual key, fallback key
   float* res_sums;              // [2][R_max] sum of the residual, sum of p
   float* ov_parts;              // scratch of the overlap kernels
-  int* sched_order;             // [R_max*gamma] slot indices in schedule (sorted) order
+  unsigned long long* sched_theta;  // [kMaxSchedItems + 1] Theta bits per cut; last: their maximum
+  int* sched_order;             // [kMaxSchedItems] slot at each position of the schedule order
   unsigned int* tickets;        // [64] last-CTA tickets; each user resets its own to zero
   float4* loss_parts1;          // [num_sms][R_max*gamma] log-sum-exp partials of the loss
   float* loss_parts2;           // [num_sms][R_max*gamma] L1 partials of the loss
@@ -77,6 +76,8 @@ struct Ctx {
   mutable unsigned long long launches;  // kernels launched by this context
   int last_engine;                      // engine of the last propose (enum dsd_engine)
   int last_p_in_place;                  // dsd_cycle_host: 1 if P was read in place from host memory
+  const void* p_class_ptr;              // last P given to verification, and whether it is
+  int p_class_host;                     //   not device memory (read with plain loads)
 };
 
 inline void count_launch(const Ctx& c, int n = 1) { c.launches += (unsigned long long)n; }
@@ -104,6 +105,12 @@ struct ProposeArgs {
   // Markov candidate sets (cand_tok == nullptr: none)
   int32_t* cand_tok;    // [R, gamma, kCandK]
   float* cand_logit;    // [R, gamma, kCandK]
+  // the schedule of the whole cycle, run by extra CTAs of the finalize
+  // (sched_keep == nullptr: none)
+  const float* sched_sps;
+  int sched_n_sps;
+  int32_t* sched_keep;
+  float* sched_theta;
 };
 cudaError_t launch_cand_finalize(const Ctx& ctx, const ProposeArgs& a, int n_used, cudaStream_t s);
 
@@ -135,6 +142,7 @@ struct VerifyArgs {
   uint64_t seed;
   int32_t* accept_len;
   int32_t* next_token;
+  int P_on_host;            // P is host memory read in place: plain loads, no bulk copies
 };
 
 cudaError_t launch_verify(const Ctx& ctx, const VerifyArgs& a, cudaStream_t s);

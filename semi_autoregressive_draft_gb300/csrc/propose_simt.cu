@@ -18,6 +18,7 @@
 // never leave registers.  At the end the CTA reduces per request and
 // publishes one atomicMax key and one (m, s) partial per request.
 #include "dsd_common.cuh"
+#include "schedule.cuh"
 
 namespace dsd {
 
@@ -472,10 +473,18 @@ struct FinParams {
   float* survival;
   int R, R_max, V, rank, gamma, act, bias_at_first, n_part, n_used, sampled;
   float inv_T;
+  int n_fin;            // CTAs of the finalize; any further CTAs run the schedule
+  SchedParams sp;
 };
 
 template <typename T>
 __global__ void __launch_bounds__(256) propose_finalize_kernel(FinParams p) {
+  static_assert(kSchedThreads == 256, "schedule CTAs share the finalize's block size");
+  if ((int)blockIdx.x >= p.n_fin) {
+    extern __shared__ __align__(16) unsigned char sched_smem[];
+    schedule_cta(p.sp, blockIdx.x - p.n_fin, gridDim.x - p.n_fin, sched_smem);
+    return;
+  }
   const int lane = threadIdx.x & 31;
   const int pair = blockIdx.x * 8 + (threadIdx.x >> 5);
   const T* U = static_cast<const T*>(p.U);
@@ -563,10 +572,30 @@ cudaError_t launch_propose_finalize_n(const Ctx& ctx, const ProposeArgs& a, int 
   int grid = (pairs + 7) / 8;
   const int gsurv = (a.R + 255) / 256;
   if (grid < gsurv) grid = gsurv;
-  if (ctx.cfg.dtype == 1)
-    propose_finalize_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(p);
-  else
-    propose_finalize_kernel<float><<<grid, 256, 0, s>>>(p);
+  p.n_fin = grid;
+  size_t smem = 0;
+  if (a.sched_keep) {
+    // the cycle's schedule in extra CTAs, from the confidences directly
+    p.sp = make_sched_params(ctx, a.R, nullptr, a.conf, a.sched_sps, a.sched_n_sps, a.sched_keep,
+                             a.sched_theta);
+    grid += schedule_ctas(ctx, a.R);
+    smem = schedule_smem_bytes(a.R, a.gamma);
+  }
+  if (ctx.cfg.dtype == 1) {
+    if (smem > 48 * 1024) {
+      cudaError_t e = cudaFuncSetAttribute(propose_finalize_kernel<__nv_bfloat16>,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (e != cudaSuccess) return e;
+    }
+    propose_finalize_kernel<__nv_bfloat16><<<grid, 256, smem, s>>>(p);
+  } else {
+    if (smem > 48 * 1024) {
+      cudaError_t e = cudaFuncSetAttribute(propose_finalize_kernel<float>,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (e != cudaSuccess) return e;
+    }
+    propose_finalize_kernel<float><<<grid, 256, smem, s>>>(p);
+  }
   count_launch(ctx);
   return cudaGetLastError();
 }

@@ -3,17 +3,18 @@
 // "DSpark 论文精读" 2.1 and 3.1).
 //
 // Kernels, in stream order:
-//   verify_rows_build  one CTA: row list (r, t) for t = 0..keep_len[r] and the
-//                      per-request row offsets (exclusive scan of keep_len+1).
-//   verify_rows        persistent grid over (row, vocabulary split) items:
-//                      streams only the B kept rows of P once (16-byte loads,
-//                      evict-first), producing per split the base-2 lse of
-//                      P/T and an argmax key (greedy: argmax P; sampled: the
-//                      stream-3 Gumbel-max of the bonus row).
-//   verify_decide      one warp per request: merges the splits, runs the
-//                      accept tests in order and stops at the first
-//                      rejection; writes accept_len and (unless a residual
-//                      draw is needed) next_token.
+//   verify_rows        persistent grid over (row, vocabulary split) items.
+//                      Every CTA first scans keep_len + 1 into the row
+//                      offsets in shared memory (row b belongs to the request
+//                      whose offset range holds it), then streams only the B
+//                      kept rows of P once (16-byte loads, evict-first),
+//                      producing per split the base-2 lse of P/T and an
+//                      argmax key (greedy: argmax P; sampled: the stream-3
+//                      Gumbel-max of the bonus row).  The last CTA to finish
+//                      (a ticket) decides every request, one thread each:
+//                      it merges the splits, runs the accept tests in order
+//                      and stops at the first rejection; writes accept_len
+//                      and (unless a residual draw is needed) next_token.
 //   residual pass      sampled only, requests with a rejection: recompute
 //                      q_k from U, E, W (the CUDA-core bias path) and draw
 //                      from norm(max(0, p_k - q_k)) by Gumbel-max (stream 2).
@@ -25,7 +26,6 @@ namespace dsd {
 cudaError_t launch_residual_simt(const Ctx& ctx, const VerifyArgs& a, cudaStream_t s);
 
 constexpr int kRowThreads = 256;
-
 __device__ __forceinline__ float max_nan(float a, float b) {
   float r;
   asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
@@ -37,248 +37,61 @@ __device__ __forceinline__ float max3_nan(float a, float b, float c) {
   return r;
 }
 
-__global__ void __launch_bounds__(1024) verify_rows_build(const int32_t* keep_len, int R, int gamma,
-                                                          int2* rows, int* row_off, int* B_out,
-                                                          int* status) {
-  __shared__ int warp_tot[32];
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int IPT = (R + 1023) / 1024;
-  const int r0 = tid * IPT;
-  int local = 0;
-  for (int t = 0; t < IPT; ++t) {
-    const int r = r0 + t;
-    if (r < R) {
-      int L = keep_len[r];
-      if (L < 0 || L > gamma) {
-        set_status(status, kErrArg);
-        L = L < 0 ? 0 : gamma;
-      }
-      local += L + 1;
-    }
-  }
-  int incl = local;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int y = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += y;
-  }
-  if (lane == 31) warp_tot[warp] = incl;
-  __syncthreads();
-  if (warp == 0) {
-    const int w = warp_tot[lane];
-    int wi = w;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, wi, o);
-      if (lane >= o) wi += y;
-    }
-    warp_tot[lane] = wi - w;
-    if (lane == 31) *B_out = wi;
-  }
-  __syncthreads();
-  int off = warp_tot[warp] + incl - local;
-  for (int t = 0; t < IPT; ++t) {
-    const int r = r0 + t;
-    if (r >= R) break;
-    int L = keep_len[r];
-    L = L < 0 ? 0 : (L > gamma ? gamma : L);
-    row_off[r] = off;
-    for (int q = 0; q <= L; ++q) rows[off + q] = make_int2(r, q);
-    off += L + 1;
-  }
-}
-
 struct RowsParams {
   int* status;
   const void* P;
   const int32_t* keep_len;
   const uint32_t* req_id;
-  const int2* rows;
-  const int* B;
   RowPart* parts;
-  int V, gamma, chunk, sampled;
-  float inv_T;
-  uint32_t k0, k1;
-};
-
-// SAMPLED is p.sampled as a template argument, so the greedy rows (a
-// running maximum only) get their own lean instantiation with more loads in
-// flight.
-template <typename T, bool SAMPLED>
-__global__ void __launch_bounds__(kRowThreads) verify_rows(RowsParams p) {
-  constexpr int epc = 16 / (int)sizeof(T);
-  __shared__ Lse2 red_l[kRowThreads / 32];
-  __shared__ unsigned long long red_k[kRowThreads / 32];
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int n_items = (*p.B) * kVerifySplits;
-  const T* P = static_cast<const T*>(p.P);
-  for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
-    const int b = item / kVerifySplits, sp = item - b * kVerifySplits;
-    const int2 rt = p.rows[b];
-    const int r = rt.x, t = rt.y;
-    int L = p.keep_len[r];
-    L = L < 0 ? 0 : (L > p.gamma ? p.gamma : L);
-    const bool bonus = (t == L);
-    const uint32_t rid = p.req_id ? p.req_id[r] : (uint32_t)r;
-    const T* row = P + ((size_t)r * (p.gamma + 1) + t) * p.V;
-    const int v_begin = sp * p.chunk;
-    const int v_end = min(p.V, v_begin + p.chunk);
-    Lse2 st = lse2_empty();
-    unsigned long long best = 0ull;
-    // Greedy: running maximum value and its lowest index; a chunk's index is
-    // looked up only when its maximum beats the running one.  NaN propagates
-    // through max.NaN and is reported.
-    float bz = -INFINITY;
-    uint32_t bv = 0xFFFFFFFFu;
-    bool nan_seen = false;
-    const int v_first = v_begin + tid * epc;
-    // Several 16-byte loads in flight per thread (eight for greedy rows,
-    // four with the sampled path's larger register set): with one, the grid
-    // keeps too few bytes in flight to cover the HBM latency.
-    constexpr int kUnroll = SAMPLED ? 4 : 8;
-    for (int vb = v_first; vb < v_end; vb += kUnroll * kRowThreads * epc) {
-      uint4 q[kUnroll];
-#pragma unroll
-      for (int u = 0; u < kUnroll; ++u) {
-        const int v0 = vb + u * kRowThreads * epc;
-        q[u] = v0 < v_end ? ld_stream16(row + v0) : make_uint4(0u, 0u, 0u, 0u);
-      }
-#pragma unroll
-      for (int u = 0; u < kUnroll; ++u) {
-        const int v0 = vb + u * kRowThreads * epc;
-        if (v0 >= v_end) break;
-        float x[8];
-        if constexpr (sizeof(T) == 2) {
-          x[0] = bf16lo(q[u].x); x[1] = bf16hi(q[u].x); x[2] = bf16lo(q[u].y); x[3] = bf16hi(q[u].y);
-          x[4] = bf16lo(q[u].z); x[5] = bf16hi(q[u].z); x[6] = bf16lo(q[u].w); x[7] = bf16hi(q[u].w);
-        } else {
-          x[0] = __uint_as_float(q[u].x); x[1] = __uint_as_float(q[u].y);
-          x[2] = __uint_as_float(q[u].z); x[3] = __uint_as_float(q[u].w);
-        }
-        if constexpr (!SAMPLED) {
-          float m = max3_nan(x[0], x[1], x[2]);
-#pragma unroll
-          for (int e = 3; e < epc; e += 2)
-            m = e + 1 < epc ? max3_nan(m, x[e], x[e + 1]) : max_nan(m, x[e]);
-          if (!(m <= bz)) {          // a larger maximum, or NaN
-            if (m != m) {
-              nan_seen = true;
-            } else {
-              int idx = epc - 1;
-#pragma unroll
-              for (int e = epc - 2; e >= 0; --e)
-                if (x[e] == m) idx = e;
-              bz = m;
-              bv = (uint32_t)(v0 + idx);
-            }
-          }
-        } else {
-          float cmax = -INFINITY;
-#pragma unroll
-          for (int e = 0; e < epc; ++e) {
-            x[e] *= p.inv_T;
-            cmax = fmaxf(cmax, x[e] * kLog2e);
-          }
-          const float M = fmaxf(st.m, cmax);
-          float s = st.s * exp2f(st.m - M);
-#pragma unroll
-          for (int e = 0; e < epc; ++e) s += exp2f(fmaf(x[e], kLog2e, -M));
-          st.m = M;
-          st.s = s;
-          if (bonus) {
-#pragma unroll
-            for (int e = 0; e < epc; e += 4) {
-              const uint32_t v = (uint32_t)(v0 + e);
-              const Philox4 ph = philox4x32_10(v >> 2, (uint32_t)t, rid, 3u, p.k0, p.k1);
-              // v0 is a multiple of 4 (epc-aligned), so words map to v .. v+3
-              const float z0 = x[e + 0] + gumbel_from_word(ph.x);
-              const float z1 = x[e + 1] + gumbel_from_word(ph.y);
-              const float z2 = x[e + 2] + gumbel_from_word(ph.z);
-              const float z3 = x[e + 3] + gumbel_from_word(ph.w);
-              unsigned long long k;
-              k = make_key(z0, v + 0); best = k > best ? k : best;
-              k = make_key(z1, v + 1); best = k > best ? k : best;
-              k = make_key(z2, v + 2); best = k > best ? k : best;
-              k = make_key(z3, v + 3); best = k > best ? k : best;
-            }
-          }
-        }
-      }
-    }
-    if (!SAMPLED && v_first < v_end) {
-      if (nan_seen) set_status(p.status, kErrNonfinite);
-      // every element was -inf: the first one holds the maximum
-      best = make_key(bz, bv == 0xFFFFFFFFu ? (uint32_t)v_first : bv);
-    }
-    if constexpr (SAMPLED) st = warp_lse2(st);   // greedy rows have no normaliser
-    best = warp_max_u64(best);
-    if (lane == 0) {
-      red_l[warp] = st;
-      red_k[warp] = best;
-    }
-    __syncthreads();
-    if (tid == 0) {
-      Lse2 l = lse2_empty();
-      unsigned long long k = 0ull;
-      for (int w = 0; w < kRowThreads / 32; ++w) {
-        if constexpr (SAMPLED) l = lse2_merge(l, red_l[w]);
-        k = red_k[w] > k ? red_k[w] : k;
-      }
-      p.parts[item] = RowPart{l.m, l.s, k};
-    }
-    __syncthreads();
-  }
-}
-
-struct DecideParams {
-  const void* P;
+  unsigned int* ticket;     // CTAs finished, zero between calls
+  // the decision
   const int32_t* tokens;
   const float* lse_q;
   const float* logit_at_tok;
-  const int32_t* keep_len;
-  const uint32_t* req_id;
-  const int* row_off;
-  const RowPart* parts;
   int32_t* accept_len;
   int32_t* next_token;
   int* rej_list;
   int* rej_k;
   float* rej_lseP;
   unsigned int* n_rej;
-  int* status;
   int R, V, gamma, sampled;
   float inv_T;
   uint32_t k0, k1;
 };
 
+// One thread decides request r, whose rows start at item row `off` and
+// whose kept prefix has L tokens: merge the splits of each row, run the
+// accept tests in order, stop at the first rejection.  The parts were
+// written by other CTAs before their ticket, so they are read from L2.
 template <typename T>
-__global__ void __launch_bounds__(256) verify_decide(DecideParams p) {
-  const int lane = threadIdx.x & 31;
-  const int r = blockIdx.x * 8 + (threadIdx.x >> 5);
-  if (r >= p.R) return;
+__device__ void decide_request(const RowsParams& p, int r, int off, int L, int splits) {
   const T* P = static_cast<const T*>(p.P);
-  int L = p.keep_len[r];
-  L = L < 0 ? 0 : (L > p.gamma ? p.gamma : L);
-  const int off = p.row_off[r];
   const uint32_t rid = p.req_id ? p.req_id[r] : (uint32_t)r;
   int k = L;
   float lseP_k = 0.f;
+  unsigned long long key_k = 0ull;   // merged argmax key of row k, when known
   for (int t = 0; t < L; ++t) {
-    // merge the splits of row t (lanes 0..kVerifySplits-1)
-    Lse2 l = lse2_empty();
-    unsigned long long key = 0ull;
-    if (lane < kVerifySplits) {
-      const RowPart rp = p.parts[(size_t)(off + t) * kVerifySplits + lane];
-      l = Lse2{rp.m, rp.s};
-      key = rp.key;
-    }
-    l = warp_lse2(l);
-    key = warp_max_u64(key);
+    const uint4* rp = reinterpret_cast<const uint4*>(p.parts + (size_t)(off + t) * kVerifySplits);
+    uint4 w[kVerifySplits];
+#pragma unroll
+    for (int q = 0; q < kVerifySplits; ++q)
+      w[q] = q < splits ? __ldcg(rp + q) : make_uint4(0xFF800000u, 0u, 0u, 0u);  // empty: m = -inf, s = 0, key 0
     int x = p.tokens[(size_t)r * p.gamma + t];
     bool ok;
     if (!p.sampled) {
+      unsigned long long key = 0ull;
+#pragma unroll
+      for (int q = 0; q < kVerifySplits; ++q) {
+        const unsigned long long kq = ((unsigned long long)w[q].w << 32) | w[q].z;
+        key = kq > key ? kq : key;
+      }
       ok = (int)key_index(key) == x;
+      key_k = key;
     } else {
+      Lse2 l = lse2_empty();
+#pragma unroll
+      for (int q = 0; q < kVerifySplits; ++q)
+        l = lse2_merge(l, Lse2{__uint_as_float(w[q].x), __uint_as_float(w[q].y)});
       if (x < 0 || x >= p.V) {
         set_status(p.status, kErrArg);
         x = 0;
@@ -301,21 +114,273 @@ __global__ void __launch_bounds__(256) verify_decide(DecideParams p) {
   }
   int next = -1;
   if (!p.sampled || k == L) {
-    unsigned long long key = 0ull;
-    if (lane < kVerifySplits) key = p.parts[(size_t)(off + k) * kVerifySplits + lane].key;
-    key = warp_max_u64(key);
+    // greedy correction (row k rejected its token) or the bonus row L
+    unsigned long long key = key_k;
+    if (k == L) {
+      const uint4* rp = reinterpret_cast<const uint4*>(p.parts + (size_t)(off + L) * kVerifySplits);
+      key = 0ull;
+#pragma unroll
+      for (int q = 0; q < kVerifySplits; ++q) {
+        if (q >= splits) break;
+        const uint4 wq = __ldcg(rp + q);
+        const unsigned long long kq = ((unsigned long long)wq.w << 32) | wq.z;
+        key = kq > key ? kq : key;
+      }
+    }
     next = (int)key_index(key);
     if (key == 0ull) set_status(p.status, kErrNonfinite);
-  } else if (lane == 0) {
+  } else {
     const unsigned int slot = atomicAdd(p.n_rej, 1u);
     p.rej_list[slot] = r;
     p.rej_k[r] = k;
     p.rej_lseP[r] = lseP_k;
   }
-  if (lane == 0) {
-    p.accept_len[r] = k;
-    p.next_token[r] = next;
+  p.accept_len[r] = k;
+  p.next_token[r] = next;
+}
+
+// Per-thread state of one item: the online log-sum-exp of P/T (sampled), the
+// Gumbel-max key of a bonus row (sampled), or the running maximum and its
+// lowest index (greedy).
+struct RowFold {
+  Lse2 st;
+  unsigned long long best;
+  float bz;
+  uint32_t bv;
+  bool nan_seen;
+};
+
+__device__ __forceinline__ RowFold rowfold_empty() {
+  RowFold f;
+  f.st = lse2_empty();
+  f.best = 0ull;
+  f.bz = -INFINITY;
+  f.bv = 0xFFFFFFFFu;
+  f.nan_seen = false;
+  return f;
+}
+
+// Fold one 16-byte vector of row t (vocabulary positions v0 ..) into f.
+// Greedy: a vector's index is looked up only when its maximum beats the
+// running one; NaN propagates through max.NaN and is reported.
+template <typename T, bool SAMPLED>
+__device__ __forceinline__ void fold_vec(RowFold& f, uint4 q, int v0, bool bonus, uint32_t t,
+                                         uint32_t rid, const RowsParams& p) {
+  constexpr int epc = 16 / (int)sizeof(T);
+  float x[8];
+  if constexpr (sizeof(T) == 2) {
+    x[0] = bf16lo(q.x); x[1] = bf16hi(q.x); x[2] = bf16lo(q.y); x[3] = bf16hi(q.y);
+    x[4] = bf16lo(q.z); x[5] = bf16hi(q.z); x[6] = bf16lo(q.w); x[7] = bf16hi(q.w);
+  } else {
+    x[0] = __uint_as_float(q.x); x[1] = __uint_as_float(q.y);
+    x[2] = __uint_as_float(q.z); x[3] = __uint_as_float(q.w);
   }
+  if constexpr (!SAMPLED) {
+    float m = max3_nan(x[0], x[1], x[2]);
+#pragma unroll
+    for (int e = 3; e < epc; e += 2)
+      m = e + 1 < epc ? max3_nan(m, x[e], x[e + 1]) : max_nan(m, x[e]);
+    if (!(m <= f.bz)) {          // a larger maximum, or NaN
+      if (m != m) {
+        f.nan_seen = true;
+      } else {
+        int idx = epc - 1;
+#pragma unroll
+        for (int e = epc - 2; e >= 0; --e)
+          if (x[e] == m) idx = e;
+        f.bz = m;
+        f.bv = (uint32_t)(v0 + idx);
+      }
+    }
+  } else {
+    float cmax = -INFINITY;
+#pragma unroll
+    for (int e = 0; e < epc; ++e) {
+      x[e] *= p.inv_T;
+      cmax = fmaxf(cmax, x[e] * kLog2e);
+    }
+    const float M = fmaxf(f.st.m, cmax);
+    float s = f.st.s * exp2f(f.st.m - M);
+#pragma unroll
+    for (int e = 0; e < epc; ++e) s += exp2f(fmaf(x[e], kLog2e, -M));
+    f.st.m = M;
+    f.st.s = s;
+    if (bonus) {
+#pragma unroll
+      for (int e = 0; e < epc; e += 4) {
+        const uint32_t v = (uint32_t)(v0 + e);
+        const Philox4 ph = philox4x32_10(v >> 2, t, rid, 3u, p.k0, p.k1);
+        // v0 is a multiple of 4 (epc-aligned), so words map to v .. v+3
+        const float z0 = x[e + 0] + gumbel_from_word(ph.x);
+        const float z1 = x[e + 1] + gumbel_from_word(ph.y);
+        const float z2 = x[e + 2] + gumbel_from_word(ph.z);
+        const float z3 = x[e + 3] + gumbel_from_word(ph.w);
+        unsigned long long k;
+        k = make_key(z0, v + 0); f.best = k > f.best ? k : f.best;
+        k = make_key(z1, v + 1); f.best = k > f.best ? k : f.best;
+        k = make_key(z2, v + 2); f.best = k > f.best ? k : f.best;
+        k = make_key(z3, v + 3); f.best = k > f.best ? k : f.best;
+      }
+    }
+  }
+}
+
+// Shared memory of the row pass besides the ring: the row offsets and the
+// block reduction.
+struct RowsShared {
+  Lse2 red_l[kRowThreads / 32];
+  unsigned long long red_k[kRowThreads / 32];
+  int scan_w[kRowThreads / 32];
+  int last;
+};
+
+// Row offsets: exclusive scan of clamp(keep_len) + 1 into s_off[0..R], with
+// s_off[R] = B.  Row b belongs to the request r with s_off[r] <= b <
+// s_off[r + 1].
+__device__ __forceinline__ void row_offsets(const RowsParams& p, int* s_off, RowsShared& sh) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int IPT = (p.R + kRowThreads - 1) / kRowThreads;
+  const int r0 = tid * IPT;
+  int local = 0;
+  for (int q = 0; q < IPT; ++q) {
+    const int r = r0 + q;
+    if (r < p.R) {
+      int L = p.keep_len[r];
+      if (L < 0 || L > p.gamma) {
+        if (blockIdx.x == 0) set_status(p.status, kErrArg);
+        L = L < 0 ? 0 : p.gamma;
+      }
+      s_off[r] = L + 1;          // the row count, turned into an offset below
+      local += L + 1;
+    }
+  }
+  int incl = local;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) sh.scan_w[warp] = incl;
+  __syncthreads();
+  int wbase = 0;
+  for (int w = 0; w < warp; ++w) wbase += sh.scan_w[w];
+  int off = wbase + incl - local;
+  for (int q = 0; q < IPT; ++q) {
+    const int r = r0 + q;
+    if (r < p.R) {
+      const int n = s_off[r];
+      s_off[r] = off;
+      off += n;
+    }
+  }
+  if (tid == kRowThreads - 1) s_off[p.R] = off;   // the last thread ends at B
+  __syncthreads();
+}
+
+// The request of row b: the largest r with s_off[r] <= b.
+__device__ __forceinline__ int row_request(const int* s_off, int R, int b) {
+  int lo = 0, hi = R - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (s_off[mid] <= b)
+      lo = mid;
+    else
+      hi = mid - 1;
+  }
+  return lo;
+}
+
+// Block reduction of one item's folds; thread 0 writes the item's part.
+template <bool SAMPLED>
+__device__ __forceinline__ void finish_item(const RowsParams& p, RowFold& f, int part, int v_first,
+                                            int v_end, RowsShared& sh) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (!SAMPLED && v_first < v_end) {
+    if (f.nan_seen) set_status(p.status, kErrNonfinite);
+    // every element was -inf: the first one holds the maximum
+    f.best = make_key(f.bz, f.bv == 0xFFFFFFFFu ? (uint32_t)v_first : f.bv);
+  }
+  if constexpr (SAMPLED) f.st = warp_lse2(f.st);   // greedy rows have no normaliser
+  f.best = warp_max_u64(f.best);
+  if (lane == 0) {
+    sh.red_l[warp] = f.st;
+    sh.red_k[warp] = f.best;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    Lse2 l = lse2_empty();
+    unsigned long long k = 0ull;
+    for (int w = 0; w < kRowThreads / 32; ++w) {
+      if constexpr (SAMPLED) l = lse2_merge(l, sh.red_l[w]);
+      k = sh.red_k[w] > k ? sh.red_k[w] : k;
+    }
+    p.parts[part] = RowPart{l.m, l.s, k};
+  }
+  __syncthreads();
+}
+
+// The last CTA to finish (a ticket) decides every request, one thread each.
+template <typename T>
+__device__ __forceinline__ void decide_all(const RowsParams& p, const int* s_off, int splits,
+                                           RowsShared& sh) {
+  const int tid = threadIdx.x;
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) sh.last = (atomicAdd(p.ticket, 1u) == gridDim.x - 1) ? 1 : 0;
+  __syncthreads();
+  if (!sh.last) return;
+  __threadfence();
+  for (int r = tid; r < p.R; r += kRowThreads)
+    decide_request<T>(p, r, s_off[r], s_off[r + 1] - s_off[r] - 1, splits);
+  if (tid == 0) *p.ticket = 0u;   // ready for the next call on the stream
+}
+
+// Plain-load row pass, for P in host memory read in place (or a ring that
+// does not fit): items are spread over a persistent grid, several 16-byte
+// loads in flight per thread (eight for greedy rows, four with the sampled
+// path's larger register set).
+template <typename T, bool SAMPLED>
+__global__ void __launch_bounds__(kRowThreads, 4) verify_rows(RowsParams p) {
+  constexpr int epc = 16 / (int)sizeof(T);
+  extern __shared__ int s_off[];   // [R + 1]
+  __shared__ RowsShared sh;
+  row_offsets(p, s_off, sh);
+  // Rows are split into as many vocabulary chunks as keep every CTA busy
+  // with about one item (at most kVerifySplits): fewer, longer items stream
+  // more bytes per block reduction.
+  const int B = s_off[p.R];
+  const int splits = max(1, min(kVerifySplits, (int)gridDim.x / B));
+  const int chunk = ((p.V + splits - 1) / splits + epc - 1) / epc * epc;
+  const int n_items = B * splits;
+  const T* P = static_cast<const T*>(p.P);
+  for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
+    const int b = item / splits, sp = item - b * splits;
+    const int r = row_request(s_off, p.R, b), t = b - s_off[r];
+    const bool bonus = (t == s_off[r + 1] - s_off[r] - 1);
+    const uint32_t rid = p.req_id ? p.req_id[r] : (uint32_t)r;
+    const T* row = P + ((size_t)r * (p.gamma + 1) + t) * p.V;
+    const int v_begin = sp * chunk;
+    const int v_end = min(p.V, v_begin + chunk);
+    const int v_first = v_begin + (int)threadIdx.x * epc;
+    RowFold f = rowfold_empty();
+    constexpr int kUnroll = SAMPLED ? 4 : 8;
+    for (int vb = v_first; vb < v_end; vb += kUnroll * kRowThreads * epc) {
+      uint4 q[kUnroll];
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) {
+        const int v0 = vb + u * kRowThreads * epc;
+        q[u] = v0 < v_end ? ld_stream16(row + v0) : make_uint4(0u, 0u, 0u, 0u);
+      }
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) {
+        const int v0 = vb + u * kRowThreads * epc;
+        if (v0 >= v_end) break;
+        fold_vec<T, SAMPLED>(f, q[u], v0, bonus, (uint32_t)t, rid, p);
+      }
+    }
+    finish_item<SAMPLED>(p, f, b * kVerifySplits + sp, v_first, v_end, sh);
+  }
+  decide_all<T>(p, s_off, splits, sh);
 }
 
 __global__ void verify_finish(const int* rej_list, const unsigned int* n_rej,
@@ -336,81 +401,52 @@ cudaError_t launch_verify(const Ctx& ctx, const VerifyArgs& a, cudaStream_t s) {
   const int sampled = a.temperature > 0.f ? 1 : 0;
   const float inv_T = sampled ? 1.f / a.temperature : 1.f;
   const uint32_t k0 = (uint32_t)(a.seed & 0xFFFFFFFFull), k1 = (uint32_t)(a.seed >> 32);
-  int* row_off = ws.rej_k + ctx.cfg.R_max;  // carved next to rej_k
-  cudaError_t e = cudaMemsetAsync(ws.counters, 0, 16 * sizeof(unsigned int), s);
-  if (e != cudaSuccess) return e;
+  cudaError_t e;
   if (sampled) {
+    e = cudaMemsetAsync(ws.counters, 0, 16 * sizeof(unsigned int), s);
+    if (e != cudaSuccess) return e;
     e = cudaMemsetAsync(ws.res_keys, 0, 2 * sizeof(unsigned long long) * ctx.cfg.R_max, s);
     if (e != cudaSuccess) return e;
     e = cudaMemsetAsync(ws.res_sums, 0, 2 * sizeof(float) * ctx.cfg.R_max, s);
     if (e != cudaSuccess) return e;
   }
-  verify_rows_build<<<1, 1024, 0, s>>>(a.keep_len, a.R, a.gamma, ws.rows, row_off, ws.sched_B,
-                                       ws.status);
-  count_launch(ctx);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
   RowsParams rp{};
   rp.status = ws.status;
   rp.P = a.P;
   rp.keep_len = a.keep_len;
   rp.req_id = a.req_id;
-  rp.rows = ws.rows;
-  rp.B = ws.sched_B;
   rp.parts = ws.vparts;
+  rp.ticket = ws.tickets + 3;
+  rp.tokens = a.tokens;
+  rp.lse_q = a.lse_q;
+  rp.logit_at_tok = a.logit_at_tok;
+  rp.accept_len = a.accept_len;
+  rp.next_token = a.next_token;
+  rp.rej_list = ws.rej_list;
+  rp.rej_k = ws.rej_k;
+  rp.rej_lseP = ws.rej_lseP;
+  rp.n_rej = ws.counters + 1;
+  rp.R = a.R;
   rp.V = a.V;
   rp.gamma = a.gamma;
-  const int epc = ctx.cfg.dtype == 1 ? 8 : 4;
-  int chunk = (a.V + kVerifySplits - 1) / kVerifySplits;
-  chunk = (chunk + epc - 1) / epc * epc;
-  rp.chunk = chunk;
   rp.sampled = sampled;
   rp.inv_T = inv_T;
   rp.k0 = k0;
   rp.k1 = k1;
   const int grid_rows = ctx.num_sms * 4;
+  const size_t smem = (size_t)(a.R + 1) * sizeof(int);
   if (ctx.cfg.dtype == 1) {
     if (sampled)
-      verify_rows<__nv_bfloat16, true><<<grid_rows, kRowThreads, 0, s>>>(rp);
+      verify_rows<__nv_bfloat16, true><<<grid_rows, kRowThreads, smem, s>>>(rp);
     else
-      verify_rows<__nv_bfloat16, false><<<grid_rows, kRowThreads, 0, s>>>(rp);
+      verify_rows<__nv_bfloat16, false><<<grid_rows, kRowThreads, smem, s>>>(rp);
   } else {
     if (sampled)
-      verify_rows<float, true><<<grid_rows, kRowThreads, 0, s>>>(rp);
+      verify_rows<float, true><<<grid_rows, kRowThreads, smem, s>>>(rp);
     else
-      verify_rows<float, false><<<grid_rows, kRowThreads, 0, s>>>(rp);
+      verify_rows<float, false><<<grid_rows, kRowThreads, smem, s>>>(rp);
   }
-  count_launch(ctx);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
-
-  DecideParams dp{};
-  dp.P = a.P;
-  dp.tokens = a.tokens;
-  dp.lse_q = a.lse_q;
-  dp.logit_at_tok = a.logit_at_tok;
-  dp.keep_len = a.keep_len;
-  dp.req_id = a.req_id;
-  dp.row_off = row_off;
-  dp.parts = ws.vparts;
-  dp.accept_len = a.accept_len;
-  dp.next_token = a.next_token;
-  dp.rej_list = ws.rej_list;
-  dp.rej_k = ws.rej_k;
-  dp.rej_lseP = ws.rej_lseP;
-  dp.n_rej = ws.counters + 1;
-  dp.status = ws.status;
-  dp.R = a.R;
-  dp.V = a.V;
-  dp.gamma = a.gamma;
-  dp.sampled = sampled;
-  dp.inv_T = inv_T;
-  dp.k0 = k0;
-  dp.k1 = k1;
-  const int grid_dec = (a.R + 7) / 8;
-  if (ctx.cfg.dtype == 1)
-    verify_decide<__nv_bfloat16><<<grid_dec, 256, 0, s>>>(dp);
-  else
-    verify_decide<float><<<grid_dec, 256, 0, s>>>(dp);
   count_launch(ctx);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
 

@@ -50,11 +50,18 @@ def test_single_rank_is_identity():
 
 def test_algorithmic_bytes_of_the_high_concurrency_workload():
     spec = bench.cycle_spec("highconc")
+    # one draft step: U rows of one position + all of W + E rows + argmax keys
+    step = bench.propose_step_bytes(spec)
+    assert step == 256 * 151936 * 2 + 151936 * 256 * 2 + 256 * 256 * 2 + 256 * 8
+    # the phase: seven steps + confidences, previous tokens, four outputs
     b = bench.propose_alg_bytes(spec)
-    # U 256*7*151936*2 + W 151936*256*2 + E rows + small I/O
-    assert b == 256 * 7 * 151936 * 2 + 151936 * 256 * 2 + 256 * 7 * 256 * 2 + 256 * 7 * 4 \
+    assert b == 7 * step + 256 * 7 * 4 + 256 * 4 + 4 * 256 * 7 * 4
+    assert 1.08e9 < b < 1.10e9
+    # W once per phase: U 256*7*151936*2 + W 151936*256*2 + E rows + small I/O
+    w1 = bench.propose_w_once_bytes(spec)
+    assert w1 == 256 * 7 * 151936 * 2 + 151936 * 256 * 2 + 256 * 7 * 256 * 2 + 256 * 7 * 4 \
         + 256 * 4 + 4 * 256 * 7 * 4
-    assert 620e6 < b < 630e6
+    assert 620e6 < w1 < 630e6
 
 
 def test_traffic_lookup_is_null_when_source_changed(tmp_path, monkeypatch):

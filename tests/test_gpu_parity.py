@@ -253,6 +253,71 @@ def test_schedule_against_oracle_random_tables(dsd):
     ctx.close()
 
 
+def test_schedule_unsorted_clamped_and_maximum_size(dsd):
+    # any survival table: runs that are not sorted, values outside [0, 1]
+    # (clamped on both sides), exact ties, and the largest table R * gamma =
+    # 4096 the scheduler holds
+    rng = np.random.default_rng(29)
+    for R, G in ((512, 8), (37, 5), (1, 16), (585, 7)):
+        ctx = dsd.Context(4096, 64, G, R, dtype="bf16")
+        for trial in range(3):
+            surv = rng.uniform(-0.2, 1.2, size=(R, G)).astype(np.float32)
+            if trial == 1:
+                surv = np.round(surv * 8) / 8            # many exact ties
+            if trial == 2:
+                surv = np.sort(surv, axis=1)             # ascending runs
+            n = R * (G + 1)
+            B = np.arange(1, n + 1)
+            sps = (1.0 / (1e-3 + rng.uniform(1e-6, 1e-4) * np.maximum(0, B - rng.uniform(0, n)))
+                   ).astype(np.float32)
+            out = ctx.schedule(torch.as_tensor(surv, device=DEV), torch.as_tensor(sps, device=DEV))
+            ref = O.schedule(surv, sps)
+            parity.compare_schedule(out["keep_len"].cpu().numpy(), out["theta_B"].cpu().numpy(),
+                                    ref)
+        assert ctx.sync_status() == 0
+        bad = torch.full((R, G), 0.5, device=DEV)
+        bad[0, 0] = float("nan")
+        ctx.schedule(bad, torch.ones(R * (G + 1), device=DEV))
+        assert ctx.sync_status() == -6
+        ctx.close()
+
+
+def test_repeated_verify_calls_on_one_context(dsd):
+    # the per-request item counters return to zero after every call: the
+    # same context verifies several keep patterns in a row
+    spec = synth.scaled(synth.CYCLE_SPECS["greedy"], temperature=1.0, seed=31, p_noise=1.0,
+                        r=64, **SMALL)
+    x = synth.cycle_inputs(spec, device=DEV)
+    ctx = dsd.Context(spec.V, spec.r, spec.G, spec.R, dtype=spec.dtype)
+    prop = ctx.propose(x["U"], x["E"], x["W"], x["conf"], x["prev_tok"], req_id=x["req_id"],
+                       temperature=1.0, seed=x["seed"])
+    h = host(x)
+    rid = h["req_id"].astype(np.int64)
+    oprop = O.propose(h["U"], h["E"], h["W"], h["conf"], h["prev_tok"], rid, 1.0, x["seed"])
+    parity.compare_propose({n: t.cpu().numpy() for n, t in prop.items()}, oprop)
+    ex = parity.draft_exempt(oprop["margin"])
+    rng = np.random.default_rng(32)
+    for trial in range(4):
+        for T in (1.0, 0.0):
+            keep = rng.integers(0, spec.G + 1, size=spec.R).astype(np.int32)
+            if trial == 0:
+                keep[:] = spec.G
+            ver = ctx.verify(x["P"], prop["tokens"], torch.as_tensor(keep, device=DEV), U=x["U"],
+                             E=x["E"], W=x["W"], prev_tok=x["prev_tok"], lse_q=prop["lse_q"],
+                             logit_at_tok=prop["logit_at_tok"], req_id=x["req_id"],
+                             temperature=T, seed=x["seed"])
+            # T = 0: greedy verification of the sampled proposal (only the
+            # argmax of each target row decides)
+            over = O.verify(h["P"], h["U"], h["E"], h["W"], h["prev_tok"], oprop["tokens"], keep,
+                            rid, T, x["seed"])
+            draft_ex = np.array([ex[r, :keep[r] + 1].any() if keep[r] < spec.G else ex[r].any()
+                                 for r in range(spec.R)])
+            parity.compare_verify(ver["accept_len"].cpu().numpy(), ver["next_token"].cpu().numpy(),
+                                  over, T, keep, draft_ex)
+    assert ctx.sync_status() == 0
+    ctx.close()
+
+
 def test_verify_greedy_hand_case(dsd):
     P = torch.zeros((1, 4, 8), dtype=torch.float32)
     P[0, 0, 0] = 5
@@ -422,4 +487,36 @@ def test_cycle_host_matches_the_device_cycle(dsd, temperature):
         assert ctx.last_p_in_place() == pinned
         for k in ("tokens", "keep_len", "accept_len", "next_token"):
             assert torch.equal(out[k], dev[k].cpu()), (pinned, k)
+    ctx.close()
+
+
+@pytest.mark.parametrize("name,temperature", [("small", 0.0), ("small", 1.0), ("highconc", 0.0),
+                                              ("greedy", 0.0)])
+def test_cycle_call_matches_the_three_calls(dsd, name, temperature):
+    """dsd_cycle computes the schedule inside the proposal's last launch, from
+    the confidences; its outputs equal dsd_propose -> dsd_schedule ->
+    dsd_verify on the same inputs, bit for bit, and the schedule equals the
+    oracle's on the survivals (the whole batch)."""
+    if name == "small":
+        spec = synth.scaled(synth.CYCLE_SPECS["greedy"], temperature=temperature, seed=35,
+                            p_noise=1.0 if temperature else 0.5, **SMALL)
+    else:
+        spec = synth.CYCLE_SPECS[name]
+    x = synth.cycle_inputs(spec, device=DEV)
+    ctx = dsd.Context(spec.V, spec.r, spec.G, spec.R, dtype=spec.dtype)
+    kw = dict(req_id=x["req_id"], temperature=temperature, seed=x["seed"])
+    one = ctx.cycle(x["U"], x["E"], x["W"], x["conf"], x["prev_tok"], x["P"], x["sps"], **kw)
+    one = {k: v.clone() for k, v in one.items()}
+    prop = ctx.propose(x["U"], x["E"], x["W"], x["conf"], x["prev_tok"], **kw)
+    sch = ctx.schedule(prop["survival"], x["sps"])
+    ver = ctx.verify(x["P"], prop["tokens"], sch["keep_len"], U=x["U"], E=x["E"], W=x["W"],
+                     prev_tok=x["prev_tok"], lse_q=prop["lse_q"],
+                     logit_at_tok=prop["logit_at_tok"], **kw)
+    assert ctx.sync_status() == 0
+    three = {**prop, **sch, **ver}
+    for k in ("tokens", "lse_q", "logit_at_tok", "survival", "keep_len", "theta_B", "accept_len",
+              "next_token"):
+        assert torch.equal(one[k], three[k]), k
+    ref = O.schedule(one["survival"].cpu().numpy(), synth.to_numpy(x["sps"]))
+    parity.compare_schedule(one["keep_len"].cpu().numpy(), one["theta_B"].cpu().numpy(), ref)
     ctx.close()
