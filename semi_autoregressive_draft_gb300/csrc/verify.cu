@@ -31,6 +31,11 @@ __device__ __forceinline__ float max_nan(float a, float b) {
   asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
   return r;
 }
+__device__ __forceinline__ uint32_t bf16x2_max_nan(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("max.NaN.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
 __device__ __forceinline__ float max3_nan(float a, float b, float c) {
   float r;
   asm("max.NaN.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
@@ -71,27 +76,27 @@ __device__ void decide_request(const RowsParams& p, int r, int off, int L, int s
   float lseP_k = 0.f;
   unsigned long long key_k = 0ull;   // merged argmax key of row k, when known
   for (int t = 0; t < L; ++t) {
-    const uint4* rp = reinterpret_cast<const uint4*>(p.parts + (size_t)(off + t) * kVerifySplits);
-    uint4 w[kVerifySplits];
-#pragma unroll
-    for (int q = 0; q < kVerifySplits; ++q)
-      w[q] = q < splits ? __ldcg(rp + q) : make_uint4(0xFF800000u, 0u, 0u, 0u);  // empty: m = -inf, s = 0, key 0
+    const RowPart* rp = p.parts + (size_t)(off + t) * kVerifySplits;
     int x = p.tokens[(size_t)r * p.gamma + t];
     bool ok;
     if (!p.sampled) {
       unsigned long long key = 0ull;
 #pragma unroll
-      for (int q = 0; q < kVerifySplits; ++q) {
-        const unsigned long long kq = ((unsigned long long)w[q].w << 32) | w[q].z;
-        key = kq > key ? kq : key;
-      }
+      for (int q = 0; q < kVerifySplits; ++q)
+        if (q < splits) {
+          const unsigned long long kq = __ldcg(&rp[q].key);
+          key = kq > key ? kq : key;
+        }
       ok = (int)key_index(key) == x;
       key_k = key;
     } else {
       Lse2 l = lse2_empty();
 #pragma unroll
       for (int q = 0; q < kVerifySplits; ++q)
-        l = lse2_merge(l, Lse2{__uint_as_float(w[q].x), __uint_as_float(w[q].y)});
+        if (q < splits) {
+          const float2 ms = __ldcg(reinterpret_cast<const float2*>(rp + q));
+          l = lse2_merge(l, Lse2{ms.x, ms.y});
+        }
       if (x < 0 || x >= p.V) {
         set_status(p.status, kErrArg);
         x = 0;
@@ -117,15 +122,14 @@ __device__ void decide_request(const RowsParams& p, int r, int off, int L, int s
     // greedy correction (row k rejected its token) or the bonus row L
     unsigned long long key = key_k;
     if (k == L) {
-      const uint4* rp = reinterpret_cast<const uint4*>(p.parts + (size_t)(off + L) * kVerifySplits);
+      const RowPart* rp = p.parts + (size_t)(off + L) * kVerifySplits;
       key = 0ull;
 #pragma unroll
-      for (int q = 0; q < kVerifySplits; ++q) {
-        if (q >= splits) break;
-        const uint4 wq = __ldcg(rp + q);
-        const unsigned long long kq = ((unsigned long long)wq.w << 32) | wq.z;
-        key = kq > key ? kq : key;
-      }
+      for (int q = 0; q < kVerifySplits; ++q)
+        if (q < splits) {
+          const unsigned long long kq = __ldcg(&rp[q].key);
+          key = kq > key ? kq : key;
+        }
     }
     next = (int)key_index(key);
     if (key == 0ull) set_status(p.status, kErrNonfinite);
@@ -167,6 +171,27 @@ template <typename T, bool SAMPLED>
 __device__ __forceinline__ void fold_vec(RowFold& f, uint4 q, int v0, bool bonus, uint32_t t,
                                          uint32_t rid, const RowsParams& p) {
   constexpr int epc = 16 / (int)sizeof(T);
+  if constexpr (!SAMPLED && sizeof(T) == 2) {
+    // greedy bf16: the vector's maximum by packed bf16x2 maxima (exact); the
+    // elements are unpacked only when it beats the running maximum
+    const uint32_t m2 = bf16x2_max_nan(bf16x2_max_nan(q.x, q.y), bf16x2_max_nan(q.z, q.w));
+    const float m = max_nan(bf16lo(m2), bf16hi(m2));
+    if (!(m <= f.bz)) {          // a larger maximum, or NaN
+      if (m != m) {
+        f.nan_seen = true;
+      } else {
+        const float x[8] = {bf16lo(q.x), bf16hi(q.x), bf16lo(q.y), bf16hi(q.y),
+                            bf16lo(q.z), bf16hi(q.z), bf16lo(q.w), bf16hi(q.w)};
+        int idx = 7;
+#pragma unroll
+        for (int e = 6; e >= 0; --e)
+          if (x[e] == m) idx = e;
+        f.bz = m;
+        f.bv = (uint32_t)(v0 + idx);
+      }
+    }
+    return;
+  }
   float x[8];
   if constexpr (sizeof(T) == 2) {
     x[0] = bf16lo(q.x); x[1] = bf16hi(q.x); x[2] = bf16lo(q.y); x[3] = bf16hi(q.y);
