@@ -43,7 +43,9 @@ reason in the repository's design notes):
   * an empty residual (sum <= 1e-12 * sum p) falls back to sampling p;
   * scheduler sort key (a desc, r asc, j asc); Theta must strictly improve;
     SPS table is 1-based (sps[B-1] = SPS(B)); B beyond the table is infeasible;
-  * conf is clamped to [0, 1];
+  * conf is clamped to [0, 1], and so is the scheduler's survival input;
+  * RNN head: the output activation, unnamed on the page, is tanh; a
+    position without a bias leaves the state at zero;
   * loss: every position of every row is valid (no loss mask), so [WALK]
     3.4's masked sum over all tokens divided by the total weight equals
     [READ] 4.1's per-position batch mean weighted by normalised w_j; the
@@ -217,6 +219,49 @@ def gated_rep(E, W_g, h, prev: int, act: str = "none"):
     return g * m
 
 
+def rnn_step(E, W_rnn, h, s_prev, prev: int, act: str = "none"):
+    """One step of the RNN head ([NOTES] 2.3, the second form, RNN 头;
+    [READ] 2.3, the RNNHead row of the table of sequential heads):
+        m = act(E[prev]),  u = [s_prev; m; h]
+        g = sigmoid(W_g u)                      (gate: how much memory stays)
+        c = tanh(W_c u)                         (candidate memory)
+        s = g * s_prev + (1 - g) * c            (keep old, write new)
+        o = tanh(W_o [s; m; h])                 (the updated input, projected)
+    W_rnn is [3, rank, 2 rank + H] holding W_g, W_c, W_o, their columns in
+    the order of the concatenation (state, Markov row, hidden state); h is
+    the backbone hidden state of this position [H].  Returns (s, o); the
+    head's bias is W o."""
+    Wr = _f64(W_rnn)
+    m = markov_rep(E, prev, act)
+    hv = _f64(h)
+    u = np.concatenate([s_prev, m, hv])
+    g = np.array([sigmoid(v) for v in Wr[0] @ u])
+    c = np.tanh(Wr[1] @ u)
+    s = g * s_prev + (1.0 - g) * c
+    o = np.tanh(Wr[2] @ np.concatenate([s, m, hv]))
+    return s, o
+
+
+def rnn_reps(E, W_rnn, h, prev_tok, tokens, bias_at_first=True, act="none"):
+    """o[r, j] of every position of every request, the state starting at
+    zero for each request ([NOTES] 2.3: the state is initialised to zero);
+    the previous token of position j is prev_tok[r] for j = 0 and
+    tokens[r, j-1] after it.  A position without a bias (j = 0 when not
+    bias_at_first) has o = 0 and leaves the state at zero."""
+    h = np.asarray(h)
+    R, G = np.asarray(tokens).shape
+    rank = np.asarray(W_rnn).shape[1]
+    out = np.zeros((R, G, rank))
+    for r in range(R):
+        s = np.zeros(rank)
+        for j in range(G):
+            if j == 0 and not bias_at_first:
+                continue
+            prev = int(prev_tok[r]) if j == 0 else int(tokens[r, j - 1])
+            s, out[r, j] = rnn_step(E, W_rnn, h[r, j], s, prev, act)
+    return out
+
+
 def head_bias(E, W, prev: int, act="none", gate=None, r=0, j=0):
     """Bias of the vanilla head (gate None) or of the gated head, gate =
     dict(h=[R, gamma, H], W_g=[rank, H + rank]) at request r, position j."""
@@ -238,7 +283,7 @@ def top_k(ell, K):
 
 
 def propose(U, E, W, conf, prev_tok, req_id=None, temperature=0.0, seed=0,
-            bias_at_first=True, act="none", gate=None, candidates=0):
+            bias_at_first=True, act="none", gate=None, candidates=0, rnn=None):
     """Sequential Markov-head proposal for a batch of R requests.
 
     For each request r and position j = 0..gamma-1:
@@ -257,7 +302,11 @@ def propose(U, E, W, conf, prev_tok, req_id=None, temperature=0.0, seed=0,
     corrected scores, with the tokens drafted in this round as predecessors): cand_tok [R,G,K] and
     cand_logit [R,G,K] (the biased logits l, largest first, ties by lowest
     token index; token -1 and logit -inf past V when V < K) and cand_gap [R,G] (the gap between the K-th and the
-    (K+1)-th largest l, for the near-tie exemption of the set's boundary)."""
+    (K+1)-th largest l, for the near-tie exemption of the set's boundary).
+
+    gate = dict(h, W_g) selects the gated Markov head, rnn = dict(h, W_rnn)
+    the RNN head (rnn_step); then the result also holds rep [R,G,rank], the
+    representation that W multiplies (g * m, or o)."""
     U = np.asarray(U)
     R, G, V = U.shape
     if req_id is None:
@@ -271,12 +320,23 @@ def propose(U, E, W, conf, prev_tok, req_id=None, temperature=0.0, seed=0,
     cand_tok = np.zeros((R, G, K), dtype=np.int64)
     cand_logit = np.zeros((R, G, K))
     cand_gap = np.full((R, G), np.inf)
+    rank = np.asarray(E).shape[1]
+    rep = np.zeros((R, G, rank))
     for r in range(R):
         prev = int(prev_tok[r])
+        s_rnn = np.zeros(rank)
         for j in range(G):
             ell = _f64(U[r, j])
             if j > 0 or bias_at_first:
-                ell = ell + head_bias(E, W, prev, act, gate, r, j)
+                if rnn is not None:
+                    s_rnn, rep[r, j] = rnn_step(E, rnn["W_rnn"], np.asarray(rnn["h"])[r, j],
+                                                s_rnn, prev, act)
+                    ell = ell + _f64(W) @ rep[r, j]
+                else:
+                    if gate is not None:
+                        rep[r, j] = gated_rep(E, gate["W_g"], np.asarray(gate["h"])[r, j], prev,
+                                              act)
+                    ell = ell + head_bias(E, W, prev, act, gate, r, j)
             if T == 0.0:
                 z = ell
                 lse_q[r, j] = logsumexp(ell)
@@ -302,6 +362,8 @@ def propose(U, E, W, conf, prev_tok, req_id=None, temperature=0.0, seed=0,
                survival=survival(conf), margin=margin)
     if K:
         out.update(cand_tok=cand_tok, cand_logit=cand_logit, cand_gap=cand_gap)
+    if gate is not None or rnn is not None:
+        out.update(rep=rep)
     return out
 
 
@@ -361,16 +423,23 @@ def schedule(a, sps):
 # a6/a7: target verification  ([WALK] 4.4; [READ] 2.1, 3.1)
 # ---------------------------------------------------------------------------
 
-def _draft_logits(U, E, W, prev_tok, tokens, r, t, bias_at_first, act, gate=None):
+def _draft_logits(U, E, W, prev_tok, tokens, r, t, bias_at_first, act, gate=None, rnn=None):
     ell = _f64(U[r, t])
     prev = int(prev_tok[r]) if t == 0 else int(tokens[r, t - 1])
     if t > 0 or bias_at_first:
-        ell = ell + head_bias(E, W, prev, act, gate, r, t)
+        if rnn is not None:
+            # the RNN state at t replays the recursion over the drafted tokens
+            o = rnn_reps(E, rnn["W_rnn"], np.asarray(rnn["h"])[r:r + 1],
+                         np.asarray(prev_tok)[r:r + 1], np.asarray(tokens)[r:r + 1, :t + 1],
+                         bias_at_first, act)[0, t]
+            ell = ell + _f64(W) @ o
+        else:
+            ell = ell + head_bias(E, W, prev, act, gate, r, t)
     return ell
 
 
 def verify(P, U, E, W, prev_tok, tokens, keep_len, req_id=None,
-           temperature=0.0, seed=0, bias_at_first=True, act="none", gate=None):
+           temperature=0.0, seed=0, bias_at_first=True, act="none", gate=None, rnn=None):
     """Rejection verification of the kept prefix of every request.
 
     P is [R, gamma+1, V]: row t scores draft token x_t, row keep_len[r] gives
@@ -411,7 +480,7 @@ def verify(P, U, E, W, prev_tok, tokens, keep_len, req_id=None,
             else:
                 p = softmax(_f64(P[r, t]) / T)
                 q = softmax(_draft_logits(U, E, W, prev_tok, tokens, r, t,
-                                          bias_at_first, act, gate) / T)
+                                          bias_at_first, act, gate, rnn) / T)
                 accept_prob = min(1.0, p[x] / q[x])
                 u = accept_uniform(seed, t, req)
                 accept_gap[r] = min(accept_gap[r], abs(u - accept_prob))
@@ -567,14 +636,14 @@ def loss_forward(U, E, W, prev_tokens, P, target_tokens, conf_logits,
 # ---------------------------------------------------------------------------
 
 def cycle(U, E, W, conf, prev_tok, P, sps, req_id=None, temperature=0.0,
-          seed=0, bias_at_first=True, act="none", keep_len=None, gate=None):
+          seed=0, bias_at_first=True, act="none", keep_len=None, gate=None, rnn=None):
     prop = propose(U, E, W, conf, prev_tok, req_id, temperature, seed,
-                   bias_at_first, act, gate)
+                   bias_at_first, act, gate, rnn=rnn)
     a32 = prop["survival"].astype(np.float32)       # the schedule's input type
     sch = schedule(a32, sps)
     kl = sch["keep_len"] if keep_len is None else np.asarray(keep_len)
     ver = verify(P, U, E, W, prev_tok, prop["tokens"], kl, req_id,
-                 temperature, seed, bias_at_first, act, gate)
+                 temperature, seed, bias_at_first, act, gate, rnn)
     return dict(propose=prop, schedule=sch, verify=ver, keep_len=kl)
 
 

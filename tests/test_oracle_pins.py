@@ -680,6 +680,104 @@ def test_gated_propose_single_step_by_hand():
 
 
 # ---------------------------------------------------------------------------
+# RNN head ([NOTES] 2.3, RNN 头; [READ] 2.3 RNNHead): u = [s; m; h],
+# g = sigmoid(W_g u), c = tanh(W_c u), s' = g s + (1 - g) c,
+# o = tanh(W_o [s'; m; h]), b = W o, s = 0 at the start of the block
+# ---------------------------------------------------------------------------
+
+def _sig(x):
+    return 1.0 / (1.0 + math.exp(-x))
+
+
+def test_rnn_step_by_hand():
+    # rank 1, H = 1: the gate reads the Markov row, the candidate the hidden
+    # state, the output the new state
+    E = np.array([[0.5], [-1.0]])
+    W_rnn = np.array([[[0.0, 2.0, 0.0]],      # W_g: z = 2 m
+                      [[0.0, 0.0, 1.0]],      # W_c: c = tanh(h)
+                      [[1.0, 0.0, 0.0]]])     # W_o: o = tanh(s')
+    s1, o1 = O.rnn_step(E, W_rnn, np.array([1.0]), np.zeros(1), 0)
+    g1 = _sig(1.0)                           # z = 2 * 0.5
+    assert abs(s1[0] - (1.0 - g1) * math.tanh(1.0)) < 1e-15
+    assert abs(o1[0] - math.tanh((1.0 - g1) * math.tanh(1.0))) < 1e-15
+    # second step: previous token 1 (m = -1), h = 0, so c = 0 and the state
+    # only decays by its gate sigmoid(-2)
+    s2, o2 = O.rnn_step(E, W_rnn, np.array([0.0]), s1, 1)
+    assert abs(s2[0] - _sig(-2.0) * s1[0]) < 1e-15
+    assert abs(o2[0] - math.tanh(_sig(-2.0) * s1[0])) < 1e-15
+    # the same two steps through rnn_reps (state from zero, tokens chained)
+    reps = O.rnn_reps(E, W_rnn, np.array([[[1.0], [0.0]]]), [0], np.array([[1, 0]]))
+    assert np.allclose(reps[0, :, 0], [o1[0], o2[0]], rtol=0, atol=1e-15)
+
+
+def test_rnn_head_without_candidate_is_the_markov_head_on_tanh_rows():
+    # W_c = 0 keeps the state at zero; W_o = [0, I, 0] outputs tanh(m), so the
+    # head's bias is W tanh(E[prev]): the plain Markov head on the table tanh(E)
+    rng = np.random.default_rng(21)
+    R, G, V, r, H = 3, 4, 60, 5, 7
+    E = rng.normal(0, 1, (V, r))
+    W = rng.normal(0, 1, (V, r))
+    U = rng.normal(0, 2, (R, G, V))
+    W_rnn = np.zeros((3, r, 2 * r + H))
+    W_rnn[0] = rng.normal(0, 1, (r, 2 * r + H))     # any gate
+    W_rnn[2][:, r:2 * r] = np.eye(r)
+    h = rng.normal(0, 1, (R, G, H))
+    conf = np.full((R, G), 0.8)
+    prev = rng.integers(0, V, R)
+    for T in (0.0, 1.0):
+        a = O.propose(U, E, W, conf, prev, None, T, 5, rnn=dict(h=h, W_rnn=W_rnn))
+        b = O.propose(U, np.tanh(E), W, conf, prev, None, T, 5)
+        assert np.array_equal(a["tokens"], b["tokens"])
+        assert np.allclose(a["lse_q"], b["lse_q"], rtol=0, atol=1e-12)
+        assert np.allclose(a["logit_at_tok"], b["logit_at_tok"], rtol=0, atol=1e-12)
+
+
+def test_rnn_state_is_a_geometric_filter_of_the_history():
+    # W_g = 0 (every gate 1/2), c = tanh(m), o = tanh(s):
+    #   s_j = sum_{i <= j} 2^-(j - i + 1) tanh(m_i)
+    rng = np.random.default_rng(22)
+    V, r, H, G = 30, 3, 2, 6
+    E = rng.normal(0, 1, (V, r))
+    W_rnn = np.zeros((3, r, 2 * r + H))
+    W_rnn[1][:, r:2 * r] = np.eye(r)
+    W_rnn[2][:, :r] = np.eye(r)
+    tokens = rng.integers(0, V, (1, G))
+    prev = [int(rng.integers(0, V))]
+    reps = O.rnn_reps(E, W_rnn, rng.normal(0, 1, (1, G, H)), prev, tokens)
+    chain = [prev[0]] + list(tokens[0, :-1])
+    for j in range(G):
+        s = sum(0.5 ** (j - i + 1) * np.tanh(E[chain[i]]) for i in range(j + 1))
+        assert np.allclose(reps[0, j], np.tanh(s), rtol=0, atol=1e-14)
+    # without a bias at the first position, position 0 has no output and the
+    # recursion starts at position 1 from a zero state
+    reps0 = O.rnn_reps(E, W_rnn, np.zeros((1, G, H)), prev, tokens, bias_at_first=False)
+    assert np.all(reps0[0, 0] == 0.0)
+    for j in range(1, G):
+        s = sum(0.5 ** (j - i + 1) * np.tanh(E[chain[i]]) for i in range(1, j + 1))
+        assert np.allclose(reps0[0, j], np.tanh(s), rtol=0, atol=1e-14)
+
+
+def test_rnn_verify_replays_the_drafted_states():
+    # the verifier's q at a position equals the proposal's, which needs the
+    # RNN state rebuilt from the drafted prefix: a keep-all verification of
+    # the drafted tokens against P = the draft logits accepts everything
+    rng = np.random.default_rng(23)
+    R, G, V, r, H = 2, 4, 25, 3, 4
+    E = rng.normal(0, 1, (V, r))
+    W = rng.normal(0, 1, (V, r))
+    U = rng.normal(0, 1, (R, G, V))
+    rnn = dict(h=rng.normal(0, 1, (R, G, H)), W_rnn=rng.normal(0, 0.7, (3, r, 2 * r + H)))
+    prev = rng.integers(0, V, R)
+    out = O.propose(U, E, W, np.full((R, G), 0.9), prev, None, 1.0, 9, rnn=rnn)
+    P = np.zeros((R, G + 1, V))
+    for q in range(R):
+        for t in range(G):
+            P[q, t] = U[q, t] + W @ out["rep"][q, t]
+    ver = O.verify(P, U, E, W, prev, out["tokens"], np.full(R, G), None, 1.0, 9, rnn=rnn)
+    assert list(ver["accept_len"]) == [G] * R
+
+
+# ---------------------------------------------------------------------------
 # Markov top-16 candidate set ([TRAIN] Prefix reranker, 候选与前缀表示)
 # ---------------------------------------------------------------------------
 
