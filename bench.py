@@ -526,26 +526,39 @@ def run_confidence(args, dsd, synth, dev, world):
     return line
 
 
-def run_gated(args, dsd, synth, dev, world):
-    """The gated Markov head's proposal on the greedy workload (R=16 requests,
-    gamma=7, V=151936, rank 256) with backbone hidden size 2560, on the
-    CUDA-core engine; L2 flushed between steps outside the events.  Beside it,
-    the plain head's proposal on the same engine."""
+def run_hidden_head(args, dsd, synth, dev, world, head):
+    """A head that reads the backbone's hidden state -- the gated Markov head
+    (head = "gated") or the RNN head ("rnn") -- proposing on the greedy
+    workload (R=16 requests, gamma=7, V=151936, rank 256) with backbone
+    hidden size 2560, on the CUDA-core engine; L2 flushed between steps
+    outside the events.  Beside it, the plain head's proposal on the same
+    engine."""
     import torch
 
     spec = synth.CYCLE_SPECS["greedy"]
     H = 2560
+    R, G, V, r = spec.R, spec.G, spec.V, spec.r
     x = synth.cycle_inputs(spec, device=dev)
-    gx = synth.gate_inputs(spec.R, spec.G, H, spec.r, spec.ew_std, seed=66, device=dev)
     ctx = dsd.Context(spec.V, spec.r, spec.G, spec.R, dtype="bf16", engine="simt",
                       device=dev.index)
+    if head == "gated":
+        hx = synth.gate_inputs(R, G, H, r, spec.ew_std, seed=66, device=dev)
+        pa = (x["U"], x["E"], x["W"], hx["h"], hx["W_g"], x["conf"], x["prev_tok"])
+        call = ctx.propose_gated
+        weights = r * (H + r) * 2
+        name, note = "gated-Markov-head", "W per step + U rows + h + W_g + E rows + gated reps"
+    else:
+        hx = synth.rnn_inputs(R, G, H, r, spec.ew_std, seed=67, device=dev)
+        pa = (x["U"], x["E"], x["W"], hx["h"], hx["W_rnn"], x["conf"], x["prev_tok"])
+        call = ctx.propose_rnn
+        weights = 3 * r * (2 * r + H) * 2
+        name, note = "RNN-head", "W per step + U rows + h + W_rnn + E rows + o_j"
     stream = torch.cuda.Stream(device=dev)
     flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
-    pa = (x["U"], x["E"], x["W"], gx["h"], gx["W_g"], x["conf"], x["prev_tok"])
     out = plain = None
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
-            out = ctx.propose_gated(*pa, req_id=x["req_id"], out=out, stream=stream)
+            out = call(*pa, req_id=x["req_id"], out=out, stream=stream)
             plain = ctx.propose(x["U"], x["E"], x["W"], x["conf"], x["prev_tok"],
                                 req_id=x["req_id"], out=plain, stream=stream)
     stream.synchronize()
@@ -560,7 +573,7 @@ def run_gated(args, dsd, synth, dev, world):
         for e in evs:
             flush.zero_()
             e[0].record(stream)
-            out = ctx.propose_gated(*pa, req_id=x["req_id"], out=out, stream=stream)
+            out = call(*pa, req_id=x["req_id"], out=out, stream=stream)
             e[1].record(stream)
             flush.zero_()
             e[2].record(stream)
@@ -574,34 +587,42 @@ def run_gated(args, dsd, synth, dev, world):
     ms = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
     ms = max_over_ranks(ms, world, dev)
     plain_ms = statistics.mean(e[2].elapsed_time(e[3]) for e in evs)
-    R, G, V, r = spec.R, spec.G, spec.V, spec.r
     # per call: W every step (the CUDA-core engine re-reads it), every U row,
-    # h and W_g once, the E rows, the gated representation written and read
-    alg = (G * V * r * 2 + R * G * V * 2 + R * G * H * 2 + r * (H + r) * 2 + R * G * r * 2
+    # h and the head's weights once, the E rows, the representation written
+    # and read
+    alg = (G * V * r * 2 + R * G * V * 2 + R * G * H * 2 + weights + R * G * r * 2
            + 2 * R * G * r * 4)
     peak, peak_kind = hbm_peak()
     achieved = alg / (ms / 1e3) / 1e9
     line = {
-        "metric": "gated-Markov-head draft tokens/s (CUDA-core engine) at R=16, gamma=7, "
+        "metric": f"{name} draft tokens/s (CUDA-core engine) at R=16, gamma=7, "
                   "V=151936, rank 256, H=2560",
         "value": world * R * G / (ms / 1e3), "unit": "draft tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "accumulate": "fp32", "data": "synthetic",
-        "config": {"workload": f"gated: R={R} gamma={G} V={V} rank={r} H={H} bf16 greedy",
+        "config": {"workload": f"{head}: R={R} gamma={G} V={V} rank={r} H={H} bf16 greedy",
                    "l2": "flushed between steps (512 MB write outside the events); "
                          "inputs 0.6 GB per call"},
         "plain_head_ms": plain_ms,
         "roofline": {"bound": "hbm", "kernel": "simt_bias_kernel", "achieved": achieved,
                      "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)",
-                     "traffic": None, "alg_bytes": alg, "per": "one gated propose call",
-                     "alg_bytes_note": "W per step + U rows + h + W_g + E rows + gated reps"},
+                     "traffic": None, "alg_bytes": alg, "per": f"one {head} propose call",
+                     "alg_bytes_note": note},
         "cpu_baseline": None, "e2e": None,
         "gpu_launches": launches, "clocks": clk,
     }
     ctx.close()
     return line
+
+
+def run_gated(args, dsd, synth, dev, world):
+    return run_hidden_head(args, dsd, synth, dev, world, "gated")
+
+
+def run_rnn(args, dsd, synth, dev, world):
+    return run_hidden_head(args, dsd, synth, dev, world, "rnn")
 
 
 def run_candidates(args, dsd, synth, dev, world):
@@ -691,9 +712,9 @@ def run_ours(args):
 
     if not os.path.exists(dsd.LIB_PATH):
         _build.build()
-    if args.workload in ("overlap", "loss", "confidence", "gated", "candidates"):
+    if args.workload in ("overlap", "loss", "confidence", "gated", "rnn", "candidates"):
         run = {"overlap": run_overlap, "loss": run_loss, "confidence": run_confidence,
-               "gated": run_gated, "candidates": run_candidates}[args.workload]
+               "gated": run_gated, "rnn": run_rnn, "candidates": run_candidates}[args.workload]
         line = run(args, dsd, synth, dev, world)
         if rank == 0:
             print(json.dumps(line), flush=True)
@@ -955,7 +976,7 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="highconc",
                     choices=["highconc", "greedy", "sampled", "tiny", "overlap", "loss",
-                             "confidence", "gated", "candidates"])
+                             "confidence", "gated", "rnn", "candidates"])
     ap.add_argument("--engine", default="auto", choices=["auto", "simt", "mma", "tcgen05"])
     ap.add_argument("--cpu-requests", type=int, default=128,
                     help="requests in the CPU-baseline sample")
@@ -968,7 +989,7 @@ def main(argv=None):
     args = ap.parse_args(argv)
     args.warmup = max(args.warmup, 3)   # at least 3 untimed warm-up steps
     if args.impl == "reference":
-        if args.workload in ("overlap", "loss", "confidence", "gated", "candidates"):
+        if args.workload in ("overlap", "loss", "confidence", "gated", "rnn", "candidates"):
             ap.error("the reference arm times the draft-verify cycle workloads")
         return run_reference(args)
     return run_ours(args)

@@ -18,7 +18,8 @@
  * ([READ] 4.1; [WALK] 3.4).  dsd_confidence_head, dsd_threshold_keep and
  * dsd_calibration cover the scheduler's input: the confidence head, the
  * static truncation it replaces, and the calibration of its survivals.
- * dsd_propose_gated / dsd_verify_gated run the gated Markov head;
+ * dsd_propose_gated / dsd_verify_gated run the gated Markov head and
+ * dsd_propose_rnn / dsd_verify_rnn the RNN head;
  * dsd_propose_candidates also returns the Markov top-16 candidate sets.
  *
  * Conventions for every call below.
@@ -355,6 +356,46 @@ int dsd_verify_gated(dsd_ctx* ctx, int R, const void* P, const void* U, const vo
                      const int32_t* tokens, const float* lse_q, const float* logit_at_tok,
                      const int32_t* keep_len, const uint32_t* req_id, float temperature,
                      uint64_t seed, int32_t* accept_len, int32_t* next_token, void* stream);
+
+/*
+ * dsd_propose_rnn -- dsd_propose with the RNN head ([NOTES] 2.3, its second
+ * form; [READ] 2.3, RNNHead): a gated recurrent state over the drafted
+ * prefix, from zero at the start of the block,
+ *   m_j = act(E[x_{j-1}]),  u_j = [s_{j-1}; m_j; h_j],
+ *   g = sigmoid(W_g u_j),  c = tanh(W_c u_j),  s_j = g * s_{j-1} + (1 - g) * c,
+ *   o_j = tanh(W_o [s_j; m_j; h_j]),  l_j = U_j + W o_j
+ * (tanh for the output nonlinearity, which the page leaves unnamed), and the
+ * same greedy / Gumbel selection, lse_q, logit_at_tok and survival as
+ * dsd_propose.  h [R, gamma, H] (the backbone hidden states) and W_rnn
+ * [3, rank, 2 rank + H] (W_g, W_c, W_o; columns: state, Markov row, hidden
+ * state) in the context's dtype, device, 16-byte aligned; H a positive
+ * multiple of 8.  rnn_rep [R, gamma, rank] f32 out: o_j per position (0 at
+ * position 0 when the context has bias_at_first = 0; the recursion then
+ * starts at position 1); dsd_verify_rnn reads it.  Runs on the CUDA-core
+ * engine whatever the context's engine: one launch for the hidden-state
+ * parts of all three matrices, then per draft position a state launch, an
+ * output launch and a bias launch, then the finalize.  Errors as
+ * dsd_propose; a non-finite gate, candidate or output argument sets
+ * DSD_ERR_NONFINITE.
+ */
+int dsd_propose_rnn(dsd_ctx* ctx, int R, const void* U, const void* E, const void* W,
+                    const void* h, int H, const void* W_rnn, const float* conf,
+                    const int32_t* prev_tok, const uint32_t* req_id, float temperature,
+                    uint64_t seed, int32_t* tokens, float* lse_q, float* logit_at_tok,
+                    float* survival, float* rnn_rep, void* stream);
+
+/*
+ * dsd_verify_rnn -- dsd_verify for proposals of dsd_propose_rnn: the
+ * rejected position's draft distribution is recomputed with o_j from
+ * rnn_rep [R, gamma, rank] f32 (as written by dsd_propose_rnn).  Same
+ * arguments, outputs and errors as dsd_verify otherwise; rnn_rep may be
+ * NULL when temperature = 0.
+ */
+int dsd_verify_rnn(dsd_ctx* ctx, int R, const void* P, const void* U, const void* E,
+                   const void* W, const float* rnn_rep, const int32_t* prev_tok,
+                   const int32_t* tokens, const float* lse_q, const float* logit_at_tok,
+                   const int32_t* keep_len, const uint32_t* req_id, float temperature,
+                   uint64_t seed, int32_t* accept_len, int32_t* next_token, void* stream);
 
 /*
  * dsd_propose_candidates -- dsd_propose plus the Markov candidate set of

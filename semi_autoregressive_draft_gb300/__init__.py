@@ -37,6 +37,7 @@ EXPORTED = [
     "dsd_propose", "dsd_schedule", "dsd_verify", "dsd_cycle", "dsd_cycle_host", "dsd_overlap",
     "dsd_propose_noalloc", "dsd_loss_forward", "dsd_confidence_head", "dsd_threshold_keep",
     "dsd_calibration", "dsd_propose_gated", "dsd_verify_gated", "dsd_propose_candidates",
+    "dsd_propose_rnn", "dsd_verify_rnn",
 ]
 
 
@@ -95,6 +96,10 @@ def load_library(path: str | None = None):
                                    _P, _P, _P, _P]),
         "dsd_verify_gated": (_I, [_P, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _F, _U64,
                                   _P, _P, _P]),
+        "dsd_propose_rnn": (_I, [_P, _I, _P, _P, _P, _P, _I, _P, _P, _P, _P, _F, _U64, _P, _P,
+                                 _P, _P, _P, _P]),
+        "dsd_verify_rnn": (_I, [_P, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _F, _U64,
+                                _P, _P, _P]),
         "dsd_confidence_head": (_I, [_P, _I, _I, _P, _P, _P, _F, _P, _P, _P, _P, _P]),
         "dsd_threshold_keep": (_I, [_P, _I, _P, _F, _P, _P]),
         "dsd_calibration": (_I, [_P, _I, _P, _P, _I, _P, _P, _P, _P]),
@@ -235,6 +240,23 @@ def dsd_verify_gated(ctx, R, P, U, E, W, gated_rep, prev_tok, tokens, lse_q, log
                      device=0):
     _check(ctx, load_library().dsd_verify_gated(
         ctx, R, _ptr(P), _ptr(U), _ptr(E), _ptr(W), _ptr(gated_rep), _ptr(prev_tok),
+        _ptr(tokens), _ptr(lse_q), _ptr(logit_at_tok), _ptr(keep_len), _ptr(req_id), temperature,
+        seed, _ptr(accept_len), _ptr(next_token), _stream(stream, device)))
+
+
+def dsd_propose_rnn(ctx, R, U, E, W, h, H, W_rnn, conf, prev_tok, req_id, temperature, seed,
+                    tokens, lse_q, logit_at_tok, survival, rnn_rep, stream=None, device=0):
+    _check(ctx, load_library().dsd_propose_rnn(
+        ctx, R, _ptr(U), _ptr(E), _ptr(W), _ptr(h), H, _ptr(W_rnn), _ptr(conf), _ptr(prev_tok),
+        _ptr(req_id), temperature, seed, _ptr(tokens), _ptr(lse_q), _ptr(logit_at_tok),
+        _ptr(survival), _ptr(rnn_rep), _stream(stream, device)))
+
+
+def dsd_verify_rnn(ctx, R, P, U, E, W, rnn_rep, prev_tok, tokens, lse_q, logit_at_tok,
+                   keep_len, req_id, temperature, seed, accept_len, next_token, stream=None,
+                   device=0):
+    _check(ctx, load_library().dsd_verify_rnn(
+        ctx, R, _ptr(P), _ptr(U), _ptr(E), _ptr(W), _ptr(rnn_rep), _ptr(prev_tok),
         _ptr(tokens), _ptr(lse_q), _ptr(logit_at_tok), _ptr(keep_len), _ptr(req_id), temperature,
         seed, _ptr(accept_len), _ptr(next_token), _stream(stream, device)))
 
@@ -407,6 +429,41 @@ class Context:
         dsd_verify_gated(self.handle, R, P, U, E, W, gated_rep, prev_tok, tokens, lse_q,
                          logit_at_tok, keep_len, req_id, temperature, seed, o["accept_len"],
                          o["next_token"], stream, self.device)
+        return o
+
+    def propose_rnn(self, U, E, W, h, W_rnn, conf, prev_tok, req_id=None, temperature=0.0,
+                    seed=0, out=None, stream=None):
+        """dsd_propose with the RNN head; h [R, gamma, H], W_rnn
+        [3, rank, 2 rank + H].  Also returns rnn_rep [R, gamma, rank] f32."""
+        R, G, H = h.shape
+        for n, t in (("U", U), ("E", E), ("W", W), ("h", h), ("W_rnn", W_rnn)):
+            self._check_in(n, t, self.torch_dtype)
+        self._check_in("conf", conf, torch.float32)
+        self._check_in("prev_tok", prev_tok, torch.int32)
+        self._check_in("req_id", req_id, torch.int32)
+        o = out or dict(tokens=self._empty((R, G), torch.int32),
+                        lse_q=self._empty((R, G), torch.float32),
+                        logit_at_tok=self._empty((R, G), torch.float32),
+                        survival=self._empty((R, G), torch.float32),
+                        rnn_rep=self._empty((R, G, self.rank), torch.float32))
+        dsd_propose_rnn(self.handle, R, U, E, W, h, H, W_rnn, conf, prev_tok, req_id, temperature,
+                        seed, o["tokens"], o["lse_q"], o["logit_at_tok"], o["survival"],
+                        o["rnn_rep"], stream, self.device)
+        return o
+
+    def verify_rnn(self, P, tokens, keep_len, rnn_rep=None, U=None, E=None, W=None,
+                   prev_tok=None, lse_q=None, logit_at_tok=None, req_id=None, temperature=0.0,
+                   seed=0, out=None, stream=None):
+        R = P.shape[0]
+        self._check_in("P", P, self.torch_dtype)
+        self._check_in("tokens", tokens, torch.int32)
+        self._check_in("keep_len", keep_len, torch.int32)
+        self._check_in("rnn_rep", rnn_rep, torch.float32)
+        o = out or dict(accept_len=self._empty((R,), torch.int32),
+                        next_token=self._empty((R,), torch.int32))
+        dsd_verify_rnn(self.handle, R, P, U, E, W, rnn_rep, prev_tok, tokens, lse_q,
+                       logit_at_tok, keep_len, req_id, temperature, seed, o["accept_len"],
+                       o["next_token"], stream, self.device)
         return o
 
     def schedule(self, survival, sps, out=None, stream=None):

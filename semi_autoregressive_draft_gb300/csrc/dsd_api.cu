@@ -69,6 +69,7 @@ size_t carve(dsd_ctx* c, unsigned char* base) {
   w.cal_cnt = reinterpret_cast<unsigned long long*>(take(sizeof(unsigned long long) * (kMaxCalBins + 1)));
   // split-K partials of the gate's hidden-state part
   w.gate_zh = reinterpret_cast<float*>(take(sizeof(float) * kGateZhFactor * (size_t)Rm * G * c->cfg.rank));
+  w.rnn_state = reinterpret_cast<float*>(take(sizeof(float) * 2 * (size_t)Rm * c->cfg.rank));
   const int cand_R = Rm < kCandMaxR ? Rm : kCandMaxR;
   w.cand_parts = reinterpret_cast<unsigned long long*>(
       take(sizeof(unsigned long long) * (size_t)G * c->n_part * cand_R * kCandK));
@@ -377,6 +378,19 @@ int dsd_verify(dsd_ctx* ctx, int R, const void* P, const void* U, const void* E,
                      temperature, seed, accept_len, next_token, nullptr, stream);
 }
 
+int dsd_verify_rnn(dsd_ctx* ctx, int R, const void* P, const void* U, const void* E,
+                   const void* W, const float* rnn_rep, const int32_t* prev_tok,
+                   const int32_t* tokens, const float* lse_q, const float* logit_at_tok,
+                   const int32_t* keep_len, const uint32_t* req_id, float temperature,
+                   uint64_t seed, int32_t* accept_len, int32_t* next_token, void* stream) {
+  int rc = check_ctx(ctx);
+  if (rc) return rc;
+  if (R > 0 && temperature > 0.f && !rnn_rep)
+    return fail(ctx, DSD_ERR_ARG, "dsd_verify_rnn: rnn_rep is NULL");
+  return verify_impl(ctx, R, P, U, E, W, prev_tok, tokens, lse_q, logit_at_tok, keep_len, req_id,
+                     temperature, seed, accept_len, next_token, rnn_rep, stream);
+}
+
 int dsd_verify_gated(dsd_ctx* ctx, int R, const void* P, const void* U, const void* E,
                      const void* W, const float* gated_rep, const int32_t* prev_tok,
                      const int32_t* tokens, const float* lse_q, const float* logit_at_tok,
@@ -390,11 +404,14 @@ int dsd_verify_gated(dsd_ctx* ctx, int R, const void* P, const void* U, const vo
                      temperature, seed, accept_len, next_token, gated_rep, stream);
 }
 
-int dsd_propose_gated(dsd_ctx* ctx, int R, const void* U, const void* E, const void* W,
-                      const void* h, int H, const void* W_g, const float* conf,
-                      const int32_t* prev_tok, const uint32_t* req_id, float temperature,
-                      uint64_t seed, int32_t* tokens, float* lse_q, float* logit_at_tok,
-                      float* survival, float* gated_rep, void* stream) {
+// The heads that read the backbone's hidden state: the gated Markov head
+// (W_g) or the RNN head (W_rnn), on the CUDA-core engine.
+static int propose_hidden_head(dsd_ctx* ctx, const char* name, int R, const void* U,
+                               const void* E, const void* W, const void* h, int H,
+                               const void* W_g, const void* W_rnn, const float* conf,
+                               const int32_t* prev_tok, const uint32_t* req_id,
+                               float temperature, uint64_t seed, int32_t* tokens, float* lse_q,
+                               float* logit_at_tok, float* survival, float* rep, void* stream) {
   int rc = check_ctx(ctx);
   if (rc) return rc;
   if ((rc = check_R(ctx, R))) return rc;
@@ -403,10 +420,10 @@ int dsd_propose_gated(dsd_ctx* ctx, int R, const void* U, const void* E, const v
   if (R == 0) return DSD_OK;
   if ((rc = check_table(ctx, U, "U")) || (rc = check_table(ctx, E, "E")) ||
       (rc = check_table(ctx, W, "W")) || (rc = check_table(ctx, h, "h")) ||
-      (rc = check_table(ctx, W_g, "W_g")))
+      (rc = check_table(ctx, W_g ? W_g : W_rnn, W_g ? "W_g" : "W_rnn")))
     return rc;
-  if (!conf || !prev_tok || !tokens || !lse_q || !logit_at_tok || !survival || !gated_rep)
-    return fail(ctx, DSD_ERR_ARG, "dsd_propose_gated: NULL argument");
+  if (!conf || !prev_tok || !tokens || !lse_q || !logit_at_tok || !survival || !rep)
+    return fail(ctx, DSD_ERR_ARG, "%s: NULL argument", name);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   ProposeArgs a{};
   a.R = R;
@@ -430,14 +447,37 @@ int dsd_propose_gated(dsd_ctx* ctx, int R, const void* U, const void* E, const v
   a.survival = survival;
   a.gate_h = h;
   a.W_g = W_g;
+  a.rnn_W = W_rnn;
   a.H = H;
-  a.gated_rep = gated_rep;
+  a.gated_rep = rep;
   cudaError_t e = launch_propose_simt(*ctx, a, s);
-  if (e != cudaSuccess) return cuda_fail(ctx, e, "gated propose launch");
+  if (e != cudaSuccess) return cuda_fail(ctx, e, name);
   ctx->last_engine = DSD_ENGINE_SIMT;
   e = launch_propose_finalize_n(*ctx, a, simt_grid(*ctx, a.V), s);
   if (e != cudaSuccess) return cuda_fail(ctx, e, "propose finalize launch");
   return DSD_OK;
+}
+
+int dsd_propose_gated(dsd_ctx* ctx, int R, const void* U, const void* E, const void* W,
+                      const void* h, int H, const void* W_g, const float* conf,
+                      const int32_t* prev_tok, const uint32_t* req_id, float temperature,
+                      uint64_t seed, int32_t* tokens, float* lse_q, float* logit_at_tok,
+                      float* survival, float* gated_rep, void* stream) {
+  if (ctx && !W_g) return fail(ctx, DSD_ERR_ARG, "dsd_propose_gated: W_g is NULL");
+  return propose_hidden_head(ctx, "dsd_propose_gated", R, U, E, W, h, H, W_g, nullptr, conf,
+                             prev_tok, req_id, temperature, seed, tokens, lse_q, logit_at_tok,
+                             survival, gated_rep, stream);
+}
+
+int dsd_propose_rnn(dsd_ctx* ctx, int R, const void* U, const void* E, const void* W,
+                    const void* h, int H, const void* W_rnn, const float* conf,
+                    const int32_t* prev_tok, const uint32_t* req_id, float temperature,
+                    uint64_t seed, int32_t* tokens, float* lse_q, float* logit_at_tok,
+                    float* survival, float* rnn_rep, void* stream) {
+  if (ctx && !W_rnn) return fail(ctx, DSD_ERR_ARG, "dsd_propose_rnn: W_rnn is NULL");
+  return propose_hidden_head(ctx, "dsd_propose_rnn", R, U, E, W, h, H, nullptr, W_rnn, conf,
+                             prev_tok, req_id, temperature, seed, tokens, lse_q, logit_at_tok,
+                             survival, rnn_rep, stream);
 }
 
 int dsd_cycle(dsd_ctx* ctx, int R, const void* U, const void* E, const void* W, const float* conf,

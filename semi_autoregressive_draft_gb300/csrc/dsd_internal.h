@@ -15,7 +15,7 @@ constexpr int kMaxGamma = 16;
 constexpr int kMaxCalBins = 64;      // reliability bins of dsd_calibration
 constexpr int kCandK = 16;           // Markov candidate set size (top-16)
 constexpr int kCandMaxR = 32;        // requests per call of dsd_propose_candidates
-constexpr int kGateZhFactor = 4;     // gated head: split-K partials held for 4 x (R_max gamma) rows
+constexpr int kGateZhFactor = 12;    // gated / RNN heads: split-K partials, 12 x R_max gamma x rank floats
 constexpr int kMaxSchedItems = 4096;  // R_max * gamma
 constexpr int kVerifySplits = 8;      // V chunks per verified row
 
@@ -54,7 +54,8 @@ struct Workspace {
   double* loss_red;             // [64][3] per-CTA sums of the loss finalize
   double* cal_acc;              // [2 kMaxCalBins + 2 + 2 kMaxGamma] calibration sums (zero between calls)
   unsigned long long* cal_cnt;  // [kMaxCalBins + 1] calibration counts (zero between calls)
-  float* gate_zh;               // split-K partials of the gated head's hidden-state gate part
+  float* gate_zh;               // split-K partials of the gated / RNN heads' hidden-state parts
+  float* rnn_state;             // [2][R_max][rank] RNN head state, ping-pong over the draft steps
   unsigned long long* cand_parts;  // [gamma][n_part][min(R_max, kCandMaxR)][kCandK] candidate keys
 };
 
@@ -101,7 +102,10 @@ struct ProposeArgs {
   const void* gate_h;   // [R, gamma, H] backbone hidden states
   const void* W_g;      // [rank, H + rank]
   int H;
-  float* gated_rep;     // [R, gamma, rank] f32 out: g * m per position
+  float* gated_rep;     // [R, gamma, rank] f32 out: g * m per position (o_j for the RNN head)
+  // RNN head (rnn_W != nullptr; gate_h, H and gated_rep then hold its hidden
+  // states, their width and its per-position output o_j)
+  const void* rnn_W;    // [3, rank, 2 rank + H]: W_g, W_c, W_o
   // Markov candidate sets (cand_tok == nullptr: none)
   int32_t* cand_tok;    // [R, gamma, kCandK]
   float* cand_logit;    // [R, gamma, kCandK]
@@ -117,6 +121,8 @@ cudaError_t launch_cand_finalize(const Ctx& ctx, const ProposeArgs& a, int n_use
 cudaError_t launch_propose_simt(const Ctx& ctx, const ProposeArgs& a, cudaStream_t s);
 cudaError_t launch_gate_h(const Ctx& ctx, const ProposeArgs& a, cudaStream_t s);
 cudaError_t launch_gate_step(const Ctx& ctx, const ProposeArgs& a, int j, cudaStream_t s);
+cudaError_t launch_rnn_h(const Ctx& ctx, const ProposeArgs& a, cudaStream_t s);
+cudaError_t launch_rnn_step(const Ctx& ctx, const ProposeArgs& a, int j, cudaStream_t s);
 cudaError_t launch_propose_tc(const Ctx& ctx, const ProposeArgs& a, cudaStream_t s);
 cudaError_t launch_propose_mma(const Ctx& ctx, const ProposeArgs& a, cudaStream_t s);
 int mma_vranges(const Ctx& ctx, int R);

@@ -1,3 +1,6 @@
+// Gated Markov head and RNN head, the sequential heads that read the
+// backbone's hidden state.
+//
 // Gated Markov head ("DSpark 论文精读" 2.3, GatedMarkovHead):
 //     m_j = act(E[x_{j-1}]),  g_j = sigmoid(W_g [h_j; m_j]),  b_j = W (g_j * m_j)
 // W_g is [rank, H + rank], its hidden-state columns first.
@@ -13,6 +16,18 @@
 // representation g * m.  The CUDA-core bias kernel then reads that
 // representation instead of gathering rows of E, and so does the verifier's
 // residual pass.
+//
+// RNN head ("DSpark notes" 2.3, the second form; "DSpark 论文精读" 2.3,
+// RNNHead): with u_j = [s_{j-1}; m_j; h_j],
+//     g = sigmoid(W_g u), c = tanh(W_c u), s_j = g * s_{j-1} + (1 - g) * c,
+//     o_j = tanh(W_o [s_j; m_j; h_j]),  b_j = W o_j,  s = 0 at the start.
+// W_rnn is [3, rank, 2 rank + H] (W_g, W_c, W_o; columns: state, Markov
+// row, hidden state).  The hidden-state parts of all three, for every
+// position, are one dense product before the sequential stage (the same
+// kernel as the gate's); each draft step then runs rnn_state_kernel (gate,
+// candidate and state update: the state and Markov columns of W_g and W_c)
+// and rnn_out_kernel (o_j from the new state), which writes the
+// representation the bias kernel and the verifier's residual pass read.
 #include "dsd_common.cuh"
 
 namespace dsd {
@@ -38,14 +53,17 @@ __device__ __forceinline__ void load8(const T* p, float* x) {
 }
 
 // Zh[s, n, k] = sum over c in split s (columns s width .. + width, below H)
-// of h[n, c] W_g[k, c], for n < rows, k < rank (width a multiple of 32).  The splits are
-// summed in order by gate_step_kernel, so the result does not depend on
-// scheduling.  H and rank are multiples of 8; a group of eight consecutive c
-// is either wholly inside H or wholly outside.
+// of h[n, c] Wh[k, c], for n < rows, k < n_out (width a multiple of 32),
+// where row k of Wh starts at W + k ld + c_off.  The splits are summed in
+// order by the step kernels, so the result does not depend on scheduling.
+// H, ld and c_off are multiples of 8; a group of eight consecutive c is
+// either wholly inside H or wholly outside.
 template <typename T>
 __global__ void __launch_bounds__(kGhThreads) gate_h_kernel(const T* __restrict__ h,
-                                                            const T* __restrict__ W_g, int rows,
-                                                            int H, int rank, int width, float* Zh) {
+                                                            const T* __restrict__ W, int rows,
+                                                            int H, int n_out, int ld, int c_off,
+                                                            int width, float* Zh) {
+  const int rank = n_out;   // output columns of Zh
   __shared__ __align__(16) float As[kGhBK][kGhBM + 4];
   __shared__ __align__(16) float Bs[kGhBK][kGhBN + 4];
   const int tid = threadIdx.x;
@@ -62,7 +80,7 @@ __global__ void __launch_bounds__(kGhThreads) gate_h_kernel(const T* __restrict_
     const int na = n0 + lr, kb = k0 + lr;
     if (c < ce && na < rows) load8<T>(h + (size_t)na * H + c, xa);
     else for (int e = 0; e < 8; ++e) xa[e] = 0.f;
-    if (c < ce && kb < rank) load8<T>(W_g + (size_t)kb * (H + rank) + c, xb);
+    if (c < ce && kb < rank) load8<T>(W + (size_t)kb * ld + c_off + c, xb);
     else for (int e = 0; e < 8; ++e) xb[e] = 0.f;
     __syncthreads();
 #pragma unroll
@@ -147,15 +165,136 @@ __global__ void __launch_bounds__(256) gate_step_kernel(GateStepParams p) {
   }
 }
 
+struct RnnStepParams {
+  const void* E;
+  const void* W_rnn;               // [3][rank][2 rank + H]
+  const float* Zh;                 // [n_split][R gamma][3 rank] hidden-state parts
+  int n_split, rows;
+  const int32_t* prev_tok;
+  const unsigned long long* keys;  // [gamma][R_max] argmax keys of the draft steps
+  const float* s_prev;             // [R_max][rank] state after the previous position
+  float* s_new;                    // [R_max][rank] state after this position
+  float* A;                        // [R, gamma, rank] o_j out
+  int* status;
+  int R_max, V, H, rank, gamma, j, act, bias_at_first;
+  int first;                       // this is the first biased position: s_prev is zero
+};
+
+// The previous token of request r at step p.j (the anchor at j = 0).
+__device__ __forceinline__ int rnn_prev_token(const RnnStepParams& p, int r) {
+  int prev = p.j == 0 ? p.prev_tok[r] : (int)key_index(p.keys[(size_t)(p.j - 1) * p.R_max + r]);
+  if (prev < 0 || prev >= p.V) {
+    if (threadIdx.x == 0) set_status(p.status, kErrArg);
+    prev = 0;
+  }
+  return prev;
+}
+
+__device__ __forceinline__ float sigmoid_f(float z) {
+  return z >= 0.f ? 1.f / (1.f + expf(-z)) : expf(z) / (1.f + expf(z));
+}
+
+// Dot of a weight row's first 2 rank columns with [a; b] (a, b in shared
+// memory), one warp.
+template <typename T>
+__device__ __forceinline__ float rnn_dot2(const T* wrow, const float* a, const float* b, int rank) {
+  const int lane = threadIdx.x & 31;
+  float dot = 0.f;
+  for (int c = lane * 8; c < 2 * rank; c += 32 * 8) {
+    float w[8];
+    load8<T>(wrow + c, w);
+    const float* x = c < rank ? a + c : b + (c - rank);   // rank % 8 == 0: no group straddles
+#pragma unroll
+    for (int e = 0; e < 8; ++e) dot = fmaf(w[e], x[e], dot);
+  }
+  return warp_sum(dot);
+}
+
+// Gate, candidate and state update of one step: CTA = one request and 32
+// state units, one warp per unit at a time.
+template <typename T>
+__global__ void __launch_bounds__(256) rnn_state_kernel(RnnStepParams p) {
+  extern __shared__ float sm[];   // [rank] previous state, [rank] Markov row
+  float* sp = sm;
+  float* ms = sm + p.rank;
+  const int r = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int k0 = blockIdx.y * kGsOut, k1 = min(p.rank, k0 + kGsOut);
+  if (p.j == 0 && !p.bias_at_first) return;   // no bias, the state stays zero
+  const int prev = rnn_prev_token(p, r);
+  const T* E = static_cast<const T*>(p.E);
+  const T* Wr = static_cast<const T*>(p.W_rnn);
+  for (int k = tid; k < p.rank; k += blockDim.x) {
+    ms[k] = act_apply(ld_elem(E, (size_t)prev * p.rank + k), p.act);
+    sp[k] = p.first ? 0.f : p.s_prev[(size_t)r * p.rank + k];
+  }
+  __syncthreads();
+  const size_t row = (size_t)r * p.gamma + p.j;
+  const int ld = 2 * p.rank + p.H;
+  for (int k = k0 + warp; k < k1; k += blockDim.x / 32) {
+    const float dg = rnn_dot2<T>(Wr + (size_t)k * ld, sp, ms, p.rank);
+    const float dc = rnn_dot2<T>(Wr + (size_t)(p.rank + k) * ld, sp, ms, p.rank);
+    if (lane == 0) {
+      float zg = dg, zc = dc;
+      for (int q = 0; q < p.n_split; ++q) {
+        const float* z = p.Zh + ((size_t)q * p.rows + row) * 3 * p.rank;
+        zg += z[k];
+        zc += z[p.rank + k];
+      }
+      if (!isfinite(zg) || !isfinite(zc)) set_status(p.status, kErrNonfinite);
+      const float g = sigmoid_f(zg);
+      const float c = tanhf(zc);
+      p.s_new[(size_t)r * p.rank + k] = g * sp[k] + (1.f - g) * c;
+    }
+  }
+}
+
+// Output of one step: o_j = tanh(W_o [s_j; m_j; h_j]), the representation
+// the bias projection multiplies.
+template <typename T>
+__global__ void __launch_bounds__(256) rnn_out_kernel(RnnStepParams p) {
+  extern __shared__ float sm[];   // [rank] new state, [rank] Markov row
+  float* sn = sm;
+  float* ms = sm + p.rank;
+  const int r = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int k0 = blockIdx.y * kGsOut, k1 = min(p.rank, k0 + kGsOut);
+  const size_t row = (size_t)r * p.gamma + p.j;
+  float* out = p.A + row * p.rank;
+  if (p.j == 0 && !p.bias_at_first) {   // position 0 carries no bias
+    for (int k = k0 + tid; k < k1; k += blockDim.x) out[k] = 0.f;
+    return;
+  }
+  const int prev = rnn_prev_token(p, r);
+  const T* E = static_cast<const T*>(p.E);
+  const T* Wr = static_cast<const T*>(p.W_rnn);
+  for (int k = tid; k < p.rank; k += blockDim.x) {
+    ms[k] = act_apply(ld_elem(E, (size_t)prev * p.rank + k), p.act);
+    sn[k] = p.s_new[(size_t)r * p.rank + k];
+  }
+  __syncthreads();
+  const int ld = 2 * p.rank + p.H;
+  for (int k = k0 + warp; k < k1; k += blockDim.x / 32) {
+    const float d = rnn_dot2<T>(Wr + (size_t)(2 * p.rank + k) * ld, sn, ms, p.rank);
+    if (lane == 0) {
+      float z = d;
+      for (int q = 0; q < p.n_split; ++q)
+        z += p.Zh[((size_t)q * p.rows + row) * 3 * p.rank + 2 * p.rank + k];
+      if (!isfinite(z)) set_status(p.status, kErrNonfinite);
+      out[k] = tanhf(z);
+    }
+  }
+}
+
 }  // namespace
 
 // Split of the hidden columns: enough CTAs to cover every SM, within the
-// workspace (kGateZhFactor x R_max gamma rows of partials) and at least 32
-// columns per split.
-static void gate_split(const Ctx& ctx, int rows, int H, int rank, int* n_split, int* width) {
-  const int tiles = ((rank + kGhBN - 1) / kGhBN) * ((rows + kGhBM - 1) / kGhBM);
+// workspace (kGateZhFactor x R_max gamma x rank floats of partials) and at
+// least 32 columns per split.
+static void gate_split(const Ctx& ctx, int rows, int H, int n_out, int* n_split, int* width) {
+  const int tiles = ((n_out + kGhBN - 1) / kGhBN) * ((rows + kGhBM - 1) / kGhBM);
   int n = (ctx.num_sms + tiles - 1) / tiles;
-  const int cap = kGateZhFactor * ctx.cfg.R_max * ctx.cfg.gamma / (rows > 0 ? rows : 1);
+  const long long cap_floats = (long long)kGateZhFactor * ctx.cfg.R_max * ctx.cfg.gamma * ctx.cfg.rank;
+  const long long per_split = (long long)(rows > 0 ? rows : 1) * n_out;
+  const int cap = (int)(cap_floats / per_split);
   n = n < cap ? n : cap;
   const int most = (H + 31) / 32;
   n = n < most ? n : most;
@@ -166,21 +305,28 @@ static void gate_split(const Ctx& ctx, int rows, int H, int rank, int* n_split, 
   *n_split = (H + w - 1) / w;
 }
 
-cudaError_t launch_gate_h(const Ctx& ctx, const ProposeArgs& a, cudaStream_t s) {
+// Hidden-state parts of every position: n_out weight rows of length H
+// starting at column c_off of rows ld apart.
+static cudaError_t launch_hidden(const Ctx& ctx, const ProposeArgs& a, const void* Wt, int n_out,
+                                 int ld, int c_off, cudaStream_t s) {
   const int rows = a.R * a.gamma;
   int n_split, width;
-  gate_split(ctx, rows, a.H, a.rank, &n_split, &width);
-  const dim3 grid((a.rank + kGhBN - 1) / kGhBN, (rows + kGhBM - 1) / kGhBM, n_split);
+  gate_split(ctx, rows, a.H, n_out, &n_split, &width);
+  const dim3 grid((n_out + kGhBN - 1) / kGhBN, (rows + kGhBM - 1) / kGhBM, n_split);
   if (a.dtype == 1)
     gate_h_kernel<__nv_bfloat16><<<grid, kGhThreads, 0, s>>>(
-        static_cast<const __nv_bfloat16*>(a.gate_h), static_cast<const __nv_bfloat16*>(a.W_g),
-        rows, a.H, a.rank, width, ctx.ws.gate_zh);
+        static_cast<const __nv_bfloat16*>(a.gate_h), static_cast<const __nv_bfloat16*>(Wt), rows,
+        a.H, n_out, ld, c_off, width, ctx.ws.gate_zh);
   else
     gate_h_kernel<float><<<grid, kGhThreads, 0, s>>>(static_cast<const float*>(a.gate_h),
-                                                     static_cast<const float*>(a.W_g), rows, a.H,
-                                                     a.rank, width, ctx.ws.gate_zh);
+                                                     static_cast<const float*>(Wt), rows, a.H,
+                                                     n_out, ld, c_off, width, ctx.ws.gate_zh);
   count_launch(ctx);
   return cudaGetLastError();
+}
+
+cudaError_t launch_gate_h(const Ctx& ctx, const ProposeArgs& a, cudaStream_t s) {
+  return launch_hidden(ctx, a, a.W_g, a.rank, a.H + a.rank, 0, s);
 }
 
 cudaError_t launch_gate_step(const Ctx& ctx, const ProposeArgs& a, int j, cudaStream_t s) {
@@ -210,6 +356,47 @@ cudaError_t launch_gate_step(const Ctx& ctx, const ProposeArgs& a, int j, cudaSt
   else
     gate_step_kernel<float><<<grid, 256, smem, s>>>(p);
   count_launch(ctx);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_rnn_h(const Ctx& ctx, const ProposeArgs& a, cudaStream_t s) {
+  return launch_hidden(ctx, a, a.rnn_W, 3 * a.rank, 2 * a.rank + a.H, 2 * a.rank, s);
+}
+
+cudaError_t launch_rnn_step(const Ctx& ctx, const ProposeArgs& a, int j, cudaStream_t s) {
+  RnnStepParams p{};
+  p.E = a.E;
+  p.W_rnn = a.rnn_W;
+  p.Zh = ctx.ws.gate_zh;
+  p.rows = a.R * a.gamma;
+  int width;
+  gate_split(ctx, p.rows, a.H, 3 * a.rank, &p.n_split, &width);
+  p.prev_tok = a.prev_tok;
+  p.keys = ctx.ws.keys;
+  // the state ping-pongs between two buffers: position j writes buffer j % 2
+  p.s_prev = ctx.ws.rnn_state + (size_t)((j + 1) % 2) * ctx.cfg.R_max * a.rank;
+  p.s_new = ctx.ws.rnn_state + (size_t)(j % 2) * ctx.cfg.R_max * a.rank;
+  p.A = a.gated_rep;
+  p.status = ctx.ws.status;
+  p.R_max = ctx.cfg.R_max;
+  p.V = a.V;
+  p.H = a.H;
+  p.rank = a.rank;
+  p.gamma = a.gamma;
+  p.j = j;
+  p.act = a.act;
+  p.bias_at_first = a.bias_at_first;
+  p.first = (j == 0 || (j == 1 && !a.bias_at_first)) ? 1 : 0;
+  const size_t smem = sizeof(float) * 2 * a.rank;
+  const dim3 grid(a.R, (a.rank + kGsOut - 1) / kGsOut);
+  if (a.dtype == 1) {
+    rnn_state_kernel<__nv_bfloat16><<<grid, 256, smem, s>>>(p);
+    rnn_out_kernel<__nv_bfloat16><<<grid, 256, smem, s>>>(p);
+  } else {
+    rnn_state_kernel<float><<<grid, 256, smem, s>>>(p);
+    rnn_out_kernel<float><<<grid, 256, smem, s>>>(p);
+  }
+  count_launch(ctx, 2);
   return cudaGetLastError();
 }
 

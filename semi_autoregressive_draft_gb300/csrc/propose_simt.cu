@@ -412,15 +412,15 @@ cudaError_t launch_propose_simt(const Ctx& ctx, const ProposeArgs& a, cudaStream
     sp.cand_parts = ctx.ws.cand_parts;
     sp.cand_R = ctx.cfg.R_max < kCandMaxR ? ctx.cfg.R_max : kCandMaxR;
   }
-  if (a.gate_h) {   // gated head: the hidden-state part of every gate, once
+  if (a.gate_h) {   // gated or RNN head: the hidden-state parts of every position, once
     sp.A = a.gated_rep;
-    e = launch_gate_h(ctx, a, s);
+    e = a.rnn_W ? launch_rnn_h(ctx, a, s) : launch_gate_h(ctx, a, s);
     if (e != cudaSuccess) return e;
   }
   for (int j = 0; j < a.gamma; ++j) {
     sp.j = j;
-    if (a.gate_h) {
-      e = launch_gate_step(ctx, a, j, s);
+    if (a.gate_h) {   // this step's representation from the tokens of the last
+      e = a.rnn_W ? launch_rnn_step(ctx, a, j, s) : launch_gate_step(ctx, a, j, s);
       if (e != cudaSuccess) return e;
     }
     e = launch_simt(sp, ctx.cfg.dtype, grid, s, kModeStep);

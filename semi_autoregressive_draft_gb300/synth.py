@@ -39,6 +39,11 @@ the five workloads of the benchmark suite:
            states h ~ N(0,1) [R, gamma, H]; W_g [rank, H + rank] with the
            hidden columns ~ N(0, 1/H) and the Markov columns ~ N(0, 1/rank) /
            e_std (each half moves a gate's argument by about 1).
+  rnn      the RNN head's extra inputs: h as for the gated head; W_rnn
+           [3, rank, 2 rank + H] (gate, candidate, output) with the state
+           columns ~ N(0, 1/rank), the Markov columns ~ N(0, 1/rank) / e_std
+           and the hidden columns ~ N(0, 1/H), so each block of columns moves
+           an argument by about 1.
   calibration  M requests x 7 positions: predicted per-step confidence
            c ~ Beta(6,2) * 0.97^j; realised accept lengths drawn as the
            leading successes of Bernoulli(max(0, c - 0.05)) chains (a head
@@ -354,3 +359,17 @@ def gate_inputs(R: int, G: int, H: int, r: int, e_std: float, seed: int = 9,
                         axis=1)
     to = lambda a: torch.as_tensor(a).to(device=device, dtype=td)
     return dict(h=to(h), W_g=to(Wg.astype(np.float32)))
+
+
+def rnn_inputs(R: int, G: int, H: int, r: int, e_std: float, seed: int = 10,
+               dtype: str = "bf16", device="cpu"):
+    """h [R,G,H] and W_rnn [3, r, 2r+H] in dtype (see the module docstring)."""
+    rng = np.random.default_rng(seed)
+    td = _torch_dtype(dtype)
+    h = rng.standard_normal((R, G, H), dtype=np.float32)
+    Wr = np.concatenate([rng.standard_normal((3, r, r), dtype=np.float32) / np.sqrt(r),
+                         rng.standard_normal((3, r, r), dtype=np.float32) / np.sqrt(r) / e_std,
+                         rng.standard_normal((3, r, H), dtype=np.float32) / np.sqrt(H)],
+                        axis=2)
+    to = lambda a: torch.as_tensor(a).to(device=device, dtype=td)
+    return dict(h=to(h), W_rnn=to(Wr.astype(np.float32)))
