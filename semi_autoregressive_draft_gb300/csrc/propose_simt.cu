@@ -55,6 +55,18 @@ struct SimtParams {
   uint32_t k0, k1;
 };
 
+// 16-byte asynchronous copy global -> shared with an L2 cache policy, and
+// the wait for all of this thread's copies.
+__device__ __forceinline__ void cp_async_keep16(void* dst, const void* src, uint64_t pol) {
+  const uint32_t d = (uint32_t)__cvta_generic_to_shared(dst);
+  asm volatile("cp.async.cg.shared.global.L2::cache_hint [%0], [%1], 16, %2;" ::"r"(d), "l"(src),
+               "l"(pol)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+}
+
 template <typename T>
 __device__ __forceinline__ int unpack16(const uint4& q, float* w) {
   if constexpr (sizeof(T) == 2) {
@@ -184,13 +196,28 @@ __global__ void __launch_bounds__(kSimtThreads) simt_bias_kernel(SimtParams p) {
       s_rid[tid] = p.req_id ? p.req_id[req] : (uint32_t)req;
     }
     __syncthreads();
-    for (int idx = tid; idx < kSimtRC * rank; idx += kSimtThreads) {
-      const int rr = idx / rank, k = idx - rr * rank;
-      float m = 0.f;
-      if (rr < nr && s_bias[rr])
-        m = p.A ? p.A[((size_t)s_req[rr] * p.gamma + s_pos[rr]) * rank + k]
-                : act_apply(ld_elem(E, (size_t)s_prev[rr] * rank + k), p.act);
-      ms[rr * mstride + k] = m;
+    // the Markov rows (or the head's representations), 16 bytes per load
+    if (p.A) {
+      for (int idx = tid; idx < kSimtRC * (rank / 4); idx += kSimtThreads) {
+        const int rr = idx / (rank / 4), k = (idx - rr * (rank / 4)) * 4;
+        float4 m = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (rr < nr && s_bias[rr])
+          m = __ldg(reinterpret_cast<const float4*>(
+              p.A + ((size_t)s_req[rr] * p.gamma + s_pos[rr]) * rank + k));
+        *reinterpret_cast<float4*>(ms + rr * mstride + k) = m;
+      }
+    } else {
+      for (int idx = tid; idx < kSimtRC * nch; idx += kSimtThreads) {
+        const int rr = idx / nch, k = (idx - rr * nch) * epc;
+        float m[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        if (rr < nr && s_bias[rr]) {
+          unpack16<T>(ld_keep16(E + (size_t)s_prev[rr] * rank + k), m);
+#pragma unroll
+          for (int e = 0; e < epc; ++e) m[e] = act_apply(m[e], p.act);
+        }
+#pragma unroll
+        for (int e = 0; e < epc; ++e) ms[rr * mstride + k + e] = m[e];
+      }
     }
     if (cand) {
       for (int i = tid; i < kSimtRC * kCandK; i += kSimtThreads) c_list[i] = 0ull;
@@ -216,16 +243,34 @@ __global__ void __launch_bounds__(kSimtThreads) simt_bias_kernel(SimtParams p) {
       const int v0 = tile * kSimtTileV;
       __syncthreads();
       if (cand) cand_merge(c_list, c_buf, c_thr, c_cnt, nr, warp, lane);   // the previous tile's
+      // the W tile by asynchronous 16-byte copies: all of them in flight at
+      // once, no registers held (rows past V are zero-filled)
       const int total = kSimtTileV * nch;
+      const uint64_t pol = policy_evict_last();
       for (int c = tid; c < total; c += kSimtThreads) {
         const int row = c / nch, ch = c - row * nch;
         const int v = v0 + row;
-        uint4 val = make_uint4(0u, 0u, 0u, 0u);
-        if (v < p.V) val = ld_keep16(W + (size_t)v * rank + ch * epc);
-        *reinterpret_cast<uint4*>(Ws + ((size_t)row * nch + (ch ^ (row & p.swz_mask))) * 16) = val;
+        unsigned char* dst = Ws + ((size_t)row * nch + (ch ^ (row & p.swz_mask))) * 16;
+        if (v < p.V)
+          cp_async_keep16(dst, W + (size_t)v * rank + ch * epc, pol);
+        else
+          *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
       }
-      __syncthreads();
+      // this thread's U (and, residual, P) entries of the tile, loaded while
+      // the W copies are in flight
       const int v = v0 + vg;
+      float uval[kSimtRPT], pval[kSimtRPT];
+#pragma unroll
+      for (int i = 0; i < kSimtRPT; ++i) {
+        const int rr = half * kSimtRPT + i;
+        const bool ok = rr < nr && v < p.V;
+        uval[i] = ok ? ld_elem(U, (size_t)s_row[rr] * p.V + v) : 0.f;
+        pval[i] = 0.f;
+        if constexpr (MODE == kModeResidual)
+          if (ok) pval[i] = ld_elem(P, ((size_t)s_req[rr] * (p.gamma + 1) + s_pos[rr]) * p.V + v);
+      }
+      cp_async_wait();
+      __syncthreads();
       if (v >= p.V) continue;
       float acc[kSimtRPT];
 #pragma unroll
@@ -246,7 +291,7 @@ __global__ void __launch_bounds__(kSimtThreads) simt_bias_kernel(SimtParams p) {
       for (int i = 0; i < kSimtRPT; ++i) {
         const int rr = half * kSimtRPT + i;
         if (rr >= nr) continue;
-        const float x = acc[i] + ld_elem(U, (size_t)s_row[rr] * p.V + v);
+        const float x = acc[i] + uval[i];
         const uint32_t rid = s_rid[rr];
         if constexpr (MODE == kModeStep) {
           if (cand) {
@@ -267,8 +312,8 @@ __global__ void __launch_bounds__(kSimtThreads) simt_bias_kernel(SimtParams p) {
           best[i] = key > best[i] ? key : best[i];
         } else {
           // residual: res = max(0, p - q) with q = exp(l/T - lse_q), p = exp(P/T - lseP)
-          const int req = s_req[rr], pos = s_pos[rr];
-          const float pl = ld_elem(P, ((size_t)req * (p.gamma + 1) + pos) * p.V + v) * p.inv_T - s_lsep[rr];
+          const int pos = s_pos[rr];
+          const float pl = pval[i] * p.inv_T - s_lsep[rr];
           const float ql = x * p.inv_T - s_lseq[rr];
           const float pv = __expf(pl);
           const float qv = __expf(ql);
