@@ -11,7 +11,7 @@
 // stage (gate_h_kernel, [R gamma, H] x [H, rank] on CUDA cores, 64 x 64
 // output tiles, split over H into partials); the second is a [rank, rank]
 // matrix-vector product per request at each draft step (gate_step_kernel,
-// one CTA per request and 32 gate outputs, one warp per output row at a time,
+// one CTA per request and 8 gate outputs, one warp per output row,
 // 16-byte loads of W_g), which also adds the partials and writes the gated
 // representation g * m.  The CUDA-core bias kernel then reads that
 // representation instead of gathering rows of E, and so does the verifier's
@@ -35,7 +35,7 @@ namespace dsd {
 namespace {
 
 constexpr int kGhBM = 64, kGhBN = 64, kGhBK = 32, kGhThreads = 256;
-constexpr int kGsOut = 32;         // gate outputs per CTA of gate_step_kernel
+constexpr int kGsOut = 8;          // outputs per CTA of the per-step kernels: one per warp
 
 template <typename T>
 __device__ __forceinline__ void load8(const T* p, float* x) {
@@ -210,8 +210,8 @@ __device__ __forceinline__ float rnn_dot2(const T* wrow, const float* a, const f
   return warp_sum(dot);
 }
 
-// Gate, candidate and state update of one step: CTA = one request and 32
-// state units, one warp per unit at a time.
+// Gate, candidate and state update of one step: CTA = one request and 8
+// state units, one warp per unit.
 template <typename T>
 __global__ void __launch_bounds__(256) rnn_state_kernel(RnnStepParams p) {
   extern __shared__ float sm[];   // [rank] previous state, [rank] Markov row
