@@ -12,11 +12,14 @@
 // stages the W tile in shared memory (16-byte chunks XOR-swizzled by row so
 // that eight consecutive rows read by a quarter-warp hit distinct banks) and
 // the gathered rows m = act(E[prev]) of up to 16 requests in fp32.  Thread
-// (vg, half) owns vocabulary entry v0 + vg and 8 requests; it computes the 8
-// bias values from shared memory, adds U and folds the biased logit into a
-// running base-2 log-sum-exp and a packed argmax key.  The biased logits
-// never leave registers.  At the end the CTA reduces per request and
-// publishes one atomicMax key and one (m, s) partial per request.
+// (vp, qq) owns vocabulary entries v0 + vp and v0 + vp + 64 and requests
+// 4 qq .. 4 qq + 3, so each 16-byte chunk of W read from shared memory feeds
+// four requests and each chunk of a Markov row two vocabulary entries; it
+// computes the 8 bias values, adds U and folds each biased logit into a
+// running base-2 log-sum-exp and a packed argmax key per request.  The
+// biased logits never leave registers.  At the end the CTA reduces per
+// request and publishes one atomicMax key and one (m, s) partial per
+// request.
 #include "dsd_common.cuh"
 #include "schedule.cuh"
 
@@ -25,7 +28,10 @@ namespace dsd {
 constexpr int kSimtThreads = 256;
 constexpr int kSimtTileV = 128;
 constexpr int kSimtRC = 16;   // requests per pass
-constexpr int kSimtRPT = 8;   // requests per thread
+constexpr int kSimtRPT = 4;   // requests per thread
+constexpr int kSimtRows = 2;  // vocabulary rows per thread (vp and vp + kSimtTileV / 2)
+constexpr int kSimtHalfV = kSimtTileV / kSimtRows;
+static_assert(kSimtThreads == kSimtHalfV * (kSimtRC / kSimtRPT), "thread = (row pair, request group)");
 
 enum SimtMode { kModeStep = 0, kModeResidual = 1 };
 
@@ -151,7 +157,10 @@ __global__ void __launch_bounds__(kSimtThreads) simt_bias_kernel(SimtParams p) {
   __shared__ float red_f2[8][kSimtRPT];
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int vg = tid & (kSimtTileV - 1), half = tid >> 7;
+  // thread = vocabulary rows vp and vp + 64 of the tile x requests
+  // 4 qq .. 4 qq + 3: each 16-byte chunk of a W row read from shared memory
+  // feeds four requests, each chunk of a Markov row two vocabulary rows
+  const int vp = tid & (kSimtHalfV - 1), qq = tid / kSimtHalfV;
   const int ntiles = (p.V + kSimtTileV - 1) / kSimtTileV;
   const T* U = static_cast<const T*>(p.U);
   const T* E = static_cast<const T*>(p.E);
@@ -258,40 +267,56 @@ __global__ void __launch_bounds__(kSimtThreads) simt_bias_kernel(SimtParams p) {
       }
       // this thread's U (and, residual, P) entries of the tile, loaded while
       // the W copies are in flight
-      const int v = v0 + vg;
-      float uval[kSimtRPT], pval[kSimtRPT];
+      float uval[kSimtRows][kSimtRPT], pval[kSimtRows][kSimtRPT];
 #pragma unroll
-      for (int i = 0; i < kSimtRPT; ++i) {
-        const int rr = half * kSimtRPT + i;
-        const bool ok = rr < nr && v < p.V;
-        uval[i] = ok ? ld_elem(U, (size_t)s_row[rr] * p.V + v) : 0.f;
-        pval[i] = 0.f;
-        if constexpr (MODE == kModeResidual)
-          if (ok) pval[i] = ld_elem(P, ((size_t)s_req[rr] * (p.gamma + 1) + s_pos[rr]) * p.V + v);
+      for (int rho = 0; rho < kSimtRows; ++rho) {
+        const int v = v0 + vp + rho * kSimtHalfV;
+#pragma unroll
+        for (int i = 0; i < kSimtRPT; ++i) {
+          const int rr = qq * kSimtRPT + i;
+          const bool ok = rr < nr && v < p.V;
+          uval[rho][i] = ok ? ld_elem(U, (size_t)s_row[rr] * p.V + v) : 0.f;
+          pval[rho][i] = 0.f;
+          if constexpr (MODE == kModeResidual)
+            if (ok)
+              pval[rho][i] = ld_elem(P, ((size_t)s_req[rr] * (p.gamma + 1) + s_pos[rr]) * p.V + v);
+        }
       }
       cp_async_wait();
       __syncthreads();
-      if (v >= p.V) continue;
-      float acc[kSimtRPT];
+      if (v0 + vp >= p.V) continue;   // both rows past the vocabulary
+      float acc[kSimtRows][kSimtRPT];
 #pragma unroll
-      for (int i = 0; i < kSimtRPT; ++i) acc[i] = 0.f;
-      const unsigned char* wrow = Ws + (size_t)vg * nch * 16;
+      for (int rho = 0; rho < kSimtRows; ++rho)
+#pragma unroll
+        for (int i = 0; i < kSimtRPT; ++i) acc[rho][i] = 0.f;
+      const int r1 = vp + kSimtHalfV;
+      const unsigned char* wrow0 = Ws + (size_t)vp * nch * 16;
+      const unsigned char* wrow1 = Ws + (size_t)r1 * nch * 16;
       for (int ch = 0; ch < nch; ++ch) {
-        const uint4 q = *reinterpret_cast<const uint4*>(wrow + (ch ^ (vg & p.swz_mask)) * 16);
-        float w[8];
-        unpack16<T>(q, w);
+        const uint4 q0 = *reinterpret_cast<const uint4*>(wrow0 + (ch ^ (vp & p.swz_mask)) * 16);
+        const uint4 q1 = *reinterpret_cast<const uint4*>(wrow1 + (ch ^ (r1 & p.swz_mask)) * 16);
+        float w0[8], w1[8];
+        unpack16<T>(q0, w0);
+        unpack16<T>(q1, w1);
 #pragma unroll
         for (int i = 0; i < kSimtRPT; ++i) {
-          const float* mrow = ms + (half * kSimtRPT + i) * mstride + ch * epc;
+          const float* mrow = ms + (qq * kSimtRPT + i) * mstride + ch * epc;
 #pragma unroll
-          for (int e = 0; e < epc; ++e) acc[i] = fmaf(w[e], mrow[e], acc[i]);
+          for (int e = 0; e < epc; ++e) {
+            acc[0][i] = fmaf(w0[e], mrow[e], acc[0][i]);
+            acc[1][i] = fmaf(w1[e], mrow[e], acc[1][i]);
+          }
         }
       }
 #pragma unroll
+      for (int rho = 0; rho < kSimtRows; ++rho)
+#pragma unroll
       for (int i = 0; i < kSimtRPT; ++i) {
-        const int rr = half * kSimtRPT + i;
-        if (rr >= nr) continue;
-        const float x = acc[i] + uval[i];
+        const int v = v0 + vp + rho * kSimtHalfV;
+        const int rr = qq * kSimtRPT + i;
+        if (rr >= nr || v >= p.V) continue;
+        const float x = acc[rho][i] + uval[rho][i];
         const uint32_t rid = s_rid[rr];
         if constexpr (MODE == kModeStep) {
           if (cand) {
@@ -313,7 +338,7 @@ __global__ void __launch_bounds__(kSimtThreads) simt_bias_kernel(SimtParams p) {
         } else {
           // residual: res = max(0, p - q) with q = exp(l/T - lse_q), p = exp(P/T - lseP)
           const int pos = s_pos[rr];
-          const float pl = pval[i] * p.inv_T - s_lsep[rr];
+          const float pl = pval[rho][i] * p.inv_T - s_lsep[rr];
           const float ql = x * p.inv_T - s_lseq[rr];
           const float pv = __expf(pl);
           const float qv = __expf(ql);
@@ -333,7 +358,7 @@ __global__ void __launch_bounds__(kSimtThreads) simt_bias_kernel(SimtParams p) {
       }
     }
 
-    // CTA reduction per request: 4 warps per half.
+    // CTA reduction per request: the two warps of its request group.
 #pragma unroll
     for (int i = 0; i < kSimtRPT; ++i) {
       const Lse2 l = warp_lse2(st[i]);
@@ -351,11 +376,12 @@ __global__ void __launch_bounds__(kSimtThreads) simt_bias_kernel(SimtParams p) {
     }
     __syncthreads();
     if (tid < kSimtRC && tid < nr) {
-      const int h = tid / kSimtRPT, i = tid % kSimtRPT;
+      const int g = tid / kSimtRPT, i = tid % kSimtRPT;
+      constexpr int kWarpsPerGroup = kSimtHalfV / 32;
       Lse2 l = lse2_empty();
       unsigned long long k = 0ull, k2 = 0ull;
       float f = 0.f, f2 = 0.f;
-      for (int w = h * 4; w < h * 4 + 4; ++w) {
+      for (int w = g * kWarpsPerGroup; w < (g + 1) * kWarpsPerGroup; ++w) {
         l = lse2_merge(l, red_l[w][i]);
         k = red_k[w][i] > k ? red_k[w][i] : k;
         k2 = red_k2[w][i] > k2 ? red_k2[w][i] : k2;
