@@ -138,6 +138,17 @@ int dsd_last_engine(const dsd_ctx* ctx);
 int dsd_last_p_in_place(const dsd_ctx* ctx);
 
 /*
+ * dsd_gumbel_noise -- the Gumbel noise every sampled path draws from a
+ * Philox word (the stream words of R5 below): out[i] = -ln(-ln u_i),
+ * u_i = ((words[i] >> 9) + 0.5) * 2^-23, as the kernels compute it (the
+ * hardware base-2 logarithm, and the Taylor series of -ln(1 - d) for
+ * u > 15/16), so its accuracy can be checked.  words [n] u32 and out [n]
+ * f32 are device pointers; asynchronous on the stream.  n < 0 or a NULL
+ * pointer with n > 0 returns DSD_ERR_ARG.  Needs no context.
+ */
+int dsd_gumbel_noise(const uint32_t* words, float* out, int n, void* stream);
+
+/*
  * dsd_propose -- sequential Markov-head proposal plus prefix survival.
  * [TRAIN] Markov 顺序修正; [NOTES] 2.2-2.3; [READ] 2.2, 2.3, 3.1.
  *

@@ -37,7 +37,7 @@ EXPORTED = [
     "dsd_propose", "dsd_schedule", "dsd_verify", "dsd_cycle", "dsd_cycle_host", "dsd_overlap",
     "dsd_propose_noalloc", "dsd_loss_forward", "dsd_confidence_head", "dsd_threshold_keep",
     "dsd_calibration", "dsd_propose_gated", "dsd_verify_gated", "dsd_propose_candidates",
-    "dsd_propose_rnn", "dsd_verify_rnn",
+    "dsd_propose_rnn", "dsd_verify_rnn", "dsd_gumbel_noise",
 ]
 
 
@@ -96,6 +96,7 @@ def load_library(path: str | None = None):
                                    _P, _P, _P, _P]),
         "dsd_verify_gated": (_I, [_P, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _F, _U64,
                                   _P, _P, _P]),
+        "dsd_gumbel_noise": (_I, [_P, _P, _I, _P]),
         "dsd_propose_rnn": (_I, [_P, _I, _P, _P, _P, _P, _I, _P, _P, _P, _P, _F, _U64, _P, _P,
                                  _P, _P, _P, _P]),
         "dsd_verify_rnn": (_I, [_P, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _F, _U64,
@@ -242,6 +243,16 @@ def dsd_verify_gated(ctx, R, P, U, E, W, gated_rep, prev_tok, tokens, lse_q, log
         ctx, R, _ptr(P), _ptr(U), _ptr(E), _ptr(W), _ptr(gated_rep), _ptr(prev_tok),
         _ptr(tokens), _ptr(lse_q), _ptr(logit_at_tok), _ptr(keep_len), _ptr(req_id), temperature,
         seed, _ptr(accept_len), _ptr(next_token), _stream(stream, device)))
+
+
+def dsd_gumbel_noise(words, out, stream=None, device=0):
+    """out[i] = the Gumbel noise of Philox word words[i] (int32 / uint32 bits,
+    device tensors), as the sampled kernels draw it."""
+    rc = load_library().dsd_gumbel_noise(_ptr(words), _ptr(out), int(words.numel()),
+                                         _stream(stream, device))
+    if rc != 0:
+        raise DsdError(rc, "dsd_gumbel_noise")
+    return out
 
 
 def dsd_propose_rnn(ctx, R, U, E, W, h, H, W_rnn, conf, prev_tok, req_id, temperature, seed,

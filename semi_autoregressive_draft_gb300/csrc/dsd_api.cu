@@ -9,6 +9,7 @@
 #include <new>
 
 #include "../../include/dsd.h"
+#include "dsd_common.cuh"
 #include "dsd_internal.h"
 
 using namespace dsd;
@@ -198,6 +199,19 @@ uint64_t dsd_launch_count(const dsd_ctx* ctx) { return ctx ? ctx->launches : 0; 
 
 int dsd_last_engine(const dsd_ctx* ctx) { return ctx ? ctx->last_engine : 0; }
 int dsd_last_p_in_place(const dsd_ctx* ctx) { return ctx ? ctx->last_p_in_place : 0; }
+
+static __global__ void gumbel_noise_kernel(const uint32_t* words, float* out, int n) {
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x)
+    out[i] = dsd::gumbel_from_word(words[i]);
+}
+
+int dsd_gumbel_noise(const uint32_t* words, float* out, int n, void* stream) {
+  if (n < 0 || (n > 0 && (!words || !out))) return DSD_ERR_ARG;
+  if (n == 0) return DSD_OK;
+  const int grid = (n + 255) / 256 < 4096 ? (n + 255) / 256 : 4096;
+  gumbel_noise_kernel<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(words, out, n);
+  return cudaGetLastError() == cudaSuccess ? DSD_OK : DSD_ERR_CUDA;
+}
 
 int dsd_sync_status(dsd_ctx* ctx, void* stream) {
   int rc = check_ctx(ctx);
