@@ -367,17 +367,6 @@ static int verify_impl(dsd_ctx* ctx, int R, const void* P, const void* U, const 
   a.accept_len = accept_len;
   a.next_token = next_token;
   a.gated_rep = gated_rep;
-  // Where P lives decides how it is read: device memory through bulk copies
-  // into shared memory, anything else (pinned host memory read in place,
-  // managed or system memory) with plain loads.  One pointer is remembered.
-  if (P != ctx->p_class_ptr) {
-    cudaPointerAttributes attr{};
-    const cudaError_t pe = cudaPointerGetAttributes(&attr, P);
-    if (pe != cudaSuccess) (void)cudaGetLastError();
-    ctx->p_class_host = (pe == cudaSuccess && attr.type == cudaMemoryTypeDevice) ? 0 : 1;
-    ctx->p_class_ptr = P;
-  }
-  a.P_on_host = ctx->p_class_host;
   cudaError_t e = launch_verify(*ctx, a, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(ctx, e, "verify launch");
   return DSD_OK;

@@ -77,8 +77,6 @@ struct Ctx {
   mutable unsigned long long launches;  // kernels launched by this context
   int last_engine;                      // engine of the last propose (enum dsd_engine)
   int last_p_in_place;                  // dsd_cycle_host: 1 if P was read in place from host memory
-  const void* p_class_ptr;              // last P given to verification, and whether it is
-  int p_class_host;                     //   not device memory (read with plain loads)
 };
 
 inline void count_launch(const Ctx& c, int n = 1) { c.launches += (unsigned long long)n; }
@@ -148,7 +146,6 @@ struct VerifyArgs {
   uint64_t seed;
   int32_t* accept_len;
   int32_t* next_token;
-  int P_on_host;            // P is host memory read in place: plain loads, no bulk copies
 };
 
 cudaError_t launch_verify(const Ctx& ctx, const VerifyArgs& a, cudaStream_t s);
