@@ -73,3 +73,12 @@ def test_traffic_lookup_is_null_when_source_changed(tmp_path, monkeypatch):
     f.write_text(json.dumps({"simt_bias_kernel": {"greedy": {
         "source_hash": bench.source_hash("simt_bias_kernel"), "dram_bytes": 123}}}))
     assert bench.traffic_for("simt_bias_kernel", "greedy") == 123
+
+
+def test_tensor_report_of_the_high_concurrency_workload():
+    spec = bench.cycle_spec("highconc")
+    rep = bench.tensor_report(spec, 1e-3, "tcgen05")
+    # 2 R r V flops per draft step, seven steps: 139.4 GFLOP per phase
+    assert rep["flops_per_phase"] == 2.0 * 256 * 256 * 151936 * 7
+    assert abs(rep["achieved_tflops"] - rep["flops_per_phase"] / 1e-3 / 1e12) < 1e-9
+    assert rep["frac"] == rep["achieved_tflops"] / rep["peak_tflops"]
