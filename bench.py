@@ -80,10 +80,18 @@ def barrier(world):
 
 
 def source_hash(kernel: str) -> str:
+    """Hash of a kernel's source files with comments and blank space removed,
+    so that only a change of the code voids the stored counters."""
+    import re
+
     h = hashlib.sha256()
     for f in KERNEL_SOURCES.get(kernel, []):
-        with open(os.path.join(ROOT, "semi_autoregressive_draft_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "semi_autoregressive_draft_gb300", "csrc", f),
+                  encoding="utf-8") as fh:
+            text = fh.read()
+        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", " ", text)
+        h.update(" ".join(text.split()).encode("utf-8"))
     return h.hexdigest()[:16]
 
 

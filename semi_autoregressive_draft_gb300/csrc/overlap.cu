@@ -3,18 +3,21 @@
 //
 // Per valid (block n, position i): p = softmax(P[n,i]), q = softmax(Q[n,i]),
 // a = sum_v min(p, q) and l1 = sum_v |p - q| = sum_v max(p, q) - min(p, q).
-// Both need the two log-normalisers first, so every row is read twice.
+// Both need the two log-normalisers first, so every row is read twice (from
+// shared memory in the split kernel).
 //
 // overlap_split: one cluster of eight CTAs per (n, i) pair, each CTA owning
-// one eighth of the vocabulary.  Pass 1 streams the CTA's slice of the P and
-// Q rows into base-2 log-sum-exp partials; the eight partials are exchanged
-// through distributed shared memory around a cluster barrier; pass 2 reads
-// the slice again and sums min(p, q) and max(p, q).  Splitting a pair over
-// eight CTAs makes each CTA's reuse footprint (its slice, 76 KB at V =
-// 151,936 bf16) small enough that all the slices in flight on the GPU fit in
-// L2, so pass 2 reads from L2 and every byte crosses HBM once; the many
-// resident clusters per SM hide the exchange's barrier latency.  CTA 0 adds
-// the slices' sums in rank order and writes a and l1.
+// one eighth of the vocabulary.  Two 1-D bulk copies put the CTA's slices of
+// the P and Q rows in shared memory (76 KB at V = 151,936 bf16, two CTAs per
+// SM); pass 1 reduces them to base-2 log-sum-exp partials, which every CTA
+// pushes into every peer's inbox with st.async (completing the peer's
+// mbarrier); each CTA merges the eight partials in a fixed tree (the same
+// normalisers, bit for bit, in every CTA); pass 2 sums min(p, q) =
+// 2^min(log2 p, log2 q) from shared memory, one 2^x per position.  CTA 0
+// collects the eight sums and writes a and l1 = sum p + sum q - 2 sum
+// min(p, q).  Every byte crosses HBM once.  (Clusters of 16 CTAs with half
+// the slice, four CTAs per SM, were measured slower: 3.95 against 3.51 ms
+// on 4096 blocks.)
 // overlap_rows (only when the split grid would exceed the launch limit): one
 // CTA per pair, two passes over the rows.
 // overlap_finalize: one CTA; tau per block, accept_rate per position over
