@@ -224,7 +224,8 @@ int dsd_schedule(dsd_ctx* ctx, int R, const float* survival, const float* sps, i
  * T == 0: accept iff x_t == argmax P[r,t]; next_token = argmax P[r,k].
  * accept_len [R] i32 out (k), next_token [R] i32 out.  The committed tokens
  * of request r are tokens[r, :k] followed by next_token[r].
- * keep_len must come from dsd_schedule (or any values in 0..gamma); U, E, W,
+ * keep_len must come from dsd_schedule (or any values in 0..gamma; others
+ * are clamped to it and set DSD_ERR_ARG in the status word); U, E, W,
  * prev_tok, lse_q, logit_at_tok may be NULL when T == 0.
  */
 int dsd_verify(dsd_ctx* ctx, int R, const void* P, const void* U, const void* E,

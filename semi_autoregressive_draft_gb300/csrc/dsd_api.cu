@@ -497,6 +497,10 @@ int dsd_cycle(dsd_ctx* ctx, int R, const void* U, const void* E, const void* W, 
   if (!sps || !keep_len) return fail(ctx, DSD_ERR_ARG, "dsd_cycle: NULL argument");
   if (n_sps < 1) return fail(ctx, DSD_ERR_ARG, "n_sps = %d", n_sps);
   if (R > n_sps) return fail(ctx, DSD_ERR_CAPACITY, "R = %d exceeds the SPS table (%d)", R, n_sps);
+  // verification's own argument checks, before the proposal launches
+  // anything (the proposal's checks cover U, E, W, conf and prev_tok)
+  if ((rc = check_table(ctx, P, "P"))) return rc;
+  if (!accept_len || !next_token) return fail(ctx, DSD_ERR_ARG, "dsd_cycle: NULL argument");
   rc = propose_impl(ctx, R, U, E, W, conf, prev_tok, req_id, temperature, seed, tokens, lse_q,
                     logit_at_tok, survival, sps, n_sps, keep_len, theta_B, stream);
   if (rc) return rc;

@@ -520,3 +520,22 @@ def test_cycle_call_matches_the_three_calls(dsd, name, temperature):
     ref = O.schedule(one["survival"].cpu().numpy(), synth.to_numpy(x["sps"]))
     parity.compare_schedule(one["keep_len"].cpu().numpy(), one["theta_B"].cpu().numpy(), ref)
     ctx.close()
+
+
+def test_cycle_rejects_bad_arguments_before_any_launch(dsd):
+    # an argument error of the verification half is found before the
+    # proposal launches anything
+    spec = synth.scaled(synth.CYCLE_SPECS["greedy"], seed=37, **SMALL)
+    x = synth.cycle_inputs(spec, device=DEV)
+    ctx = dsd.Context(spec.V, spec.r, spec.G, spec.R, dtype="bf16")
+    out = ctx.cycle_outputs(spec.R)
+    n0 = ctx.launch_count()
+    for P, acc in ((None, out["accept_len"]), (x["P"], None)):
+        with pytest.raises(dsd.DsdError):
+            dsd.dsd_cycle(ctx.handle, spec.R, x["U"], x["E"], x["W"], x["conf"], x["prev_tok"],
+                          x["req_id"], P, x["sps"], x["sps"].numel(), 0.0, 1, out["tokens"],
+                          out["lse_q"], out["logit_at_tok"], out["survival"], out["keep_len"],
+                          out["theta_B"], acc, out["next_token"], None, 0)
+    assert ctx.launch_count() == n0
+    assert ctx.sync_status() == 0
+    ctx.close()
