@@ -34,6 +34,14 @@
 //               (greedy) or Gumbel-max (sampled) key; they never leave
 //               registers.
 //
+// With at most 64 requests (one half-empty M-tile) rows 64..127 of A repeat
+// rows 0..63, and the warps of lane quarters 2 and 3, which would otherwise
+// hold no request, fold the second 32-column chunk of every 64-column half
+// while quarters 0 and 1 fold the first: the tensor pipe computes each bias
+// twice (it has the slack) and the per-thread epilogue work, the sampled
+// path's Philox blocks included, halves.  The copies' states merge at the
+// end through shared memory.
+//
 // Every mbarrier has exactly one consumer role that waits on each of its
 // phases in order (a parity wait cannot tell phase k from phase k + 2, so no
 // waiter may skip a phase).  That is why each column half has its own U ring
@@ -97,6 +105,8 @@ struct TcParams {
   int j;                     // draft position of this launch
   int R, R_max, V, rank, gamma, bias_at_first, n_part, n_vr, ntiles, sampled;
   int mc;                    // clusters of the two M-tiles of a range share W by multicast
+  int dup;                   // R <= 64: rows 64..127 repeat rows 0..63 and take the second
+                             // 32-column chunk of every 64-column half
   float inv_T;
   uint32_t k0, k1;
 };
@@ -407,9 +417,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int hs = e >> 2;           // column half of each tile
     const int q = warp & 3;          // TMEM lane quarter this warp may access
     const int row = q * 32 + lane;   // row within the M-tile
-    const int r = r0 + row;
+    // With dup, rows 64..127 hold the requests of rows 0..63 again, and the
+    // two copies of a request fold different 32-column chunks of each tile.
+    const int rrow = p.dup ? (row & 63) : row;   // the request's row (its U row)
+    const int r = r0 + rrow;
     const bool valid = r < p.R;
-    const bool warp_rows = r0 + q * 32 < p.R;   // does this warp hold any request?
+    const bool warp_rows = r0 + (p.dup ? (q & 1) : q) * 32 < p.R;   // any request in this warp?
     const uint32_t rid = valid ? (p.req_id ? p.req_id[r] : (uint32_t)r) : 0u;
 
     // The keys of step j-1 come from the previous grid: wait until it has
@@ -425,7 +438,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const bool biased = (j > 0) || p.bias_at_first;
       int my_tok = -1;
       if (lane < 16) {
-        const int rr = r0 + e + 8 * lane;
+        const int rr = r0 + (p.dup ? ((e + 8 * lane) & 63) : (e + 8 * lane));
         if (biased && rr < p.R) {
           int tk = (j == 0) ? p.prev_tok[rr]
                             : (int)key_index(__ldcg(&p.keys[(size_t)(j - 1) * p.R_max + rr]));
@@ -481,11 +494,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // 128-byte swizzle: 16-byte chunk c of row `row` sits at chunk
         // c ^ (row & 7) of that row.
         uint4 u[8];
-        const unsigned char* urow = ring + s * kBox + row * 128;
+        const unsigned char* urow = ring + s * kBox + rrow * 128;
         if (warp_rows) {
 #pragma unroll
           for (int c = 0; c < 8; ++c)
-            u[c] = *reinterpret_cast<const uint4*>(urow + ((c ^ (row & 7)) << 4));
+            u[c] = *reinterpret_cast<const uint4*>(urow + ((c ^ (rrow & 7)) << 4));
         }
         __syncwarp();
         if (lane == 0) tc::mbar_arrive(&empty[s]);   // the slot's data is in registers
@@ -493,6 +506,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (warp_rows) {
 #pragma unroll
           for (int c = 0; c < 2; ++c) {
+            if (p.dup && c != (q >> 1)) continue;   // the other copy folds this chunk
             const int v0 = vx + c * 32;
             if (v0 >= p.V) break;
             uint32_t acc[32];
@@ -512,19 +526,36 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // The A region is free: the last accumulator barrier this warp waited on
     // was committed after every MMA that reads A, so they have all completed.
     RowState* xch = reinterpret_cast<RowState*>(sA);
+    RowState* xch2 = xch + kTileM;   // dup: the second copy's merged state
     if (hs == 1) xch[row] = st;
     asm volatile("bar.sync 1, 256;" ::: "memory");   // the eight epilogue warps
     if (hs == 0) {
       const RowState o = xch[row];
       const Lse2 l = lse2_merge(Lse2{st.m2, st.s}, Lse2{o.m2, o.s});
+      st.m2 = l.m;
+      st.s = l.s;
       if (o.best_z > st.best_z || (o.best_z == st.best_z && o.best_v < st.best_v)) {
         st.best_z = o.best_z;
         st.best_v = o.best_v;
       }
-      if (valid && TC_CHECK(vr < p.n_part && r < p.R_max, 5)) {
-        atomicMax(&p.keys[(size_t)j * p.R_max + r], make_key(st.best_z, st.best_v));
-        p.parts[((size_t)j * p.n_part + vr) * p.R_max + r] = make_float2(l.m, l.s);
+      if (p.dup && row >= 64) xch2[row - 64] = st;
+    }
+    if (p.dup) {
+      asm volatile("bar.sync 1, 256;" ::: "memory");
+      if (hs == 0 && row < 64) {
+        const RowState o = xch2[row];
+        const Lse2 l = lse2_merge(Lse2{st.m2, st.s}, Lse2{o.m2, o.s});
+        st.m2 = l.m;
+        st.s = l.s;
+        if (o.best_z > st.best_z || (o.best_z == st.best_z && o.best_v < st.best_v)) {
+          st.best_z = o.best_z;
+          st.best_v = o.best_v;
+        }
       }
+    }
+    if (hs == 0 && (!p.dup || row < 64) && valid && TC_CHECK(vr < p.n_part && r < p.R_max, 5)) {
+      atomicMax(&p.keys[(size_t)j * p.R_max + r], make_key(st.best_z, st.best_v));
+      p.parts[((size_t)j * p.n_part + vr) * p.R_max + r] = make_float2(st.m2, st.s);
     }
   }
   tc::tc_fence_before();
@@ -647,6 +678,7 @@ cudaError_t launch_propose_tc(const Ctx& ctx, const ProposeArgs& a, cudaStream_t
   p.k1 = (uint32_t)(a.seed >> 32);
   p.n_vr = tc_vranges(ctx, a.R);
   p.mc = (a.R > kTileM && a.R <= 2 * kTileM) ? 1 : 0;
+  p.dup = a.R <= kTileM / 2 ? 1 : 0;
   const int grid = ((a.R + kTileM - 1) / kTileM) * p.n_vr;
 
   // One launch per step: the next step's A operand needs every CTA's argmax.

@@ -135,6 +135,8 @@ def test_mma_and_simt_engines_agree(dsd):
     (300, 1544, 256, 0.0),     # a second launch per step for requests 256..299
     (40, 3080, 128, 0.0),      # rank 128
     (16, 4104, 64, 1.0),       # rank 64
+    (64, 2600, 256, 1.0),      # the largest batch whose rows 64..127 repeat rows 0..63
+    (65, 1032, 256, 0.0),      # one request more: no repeated rows
 ])
 def test_cycle_tc_shapes(dsd, R, V, rank, temperature):
     spec = synth.scaled(synth.CYCLE_SPECS["greedy"], R=R, V=V, r=rank, ew_std=0.3,
