@@ -69,7 +69,8 @@ struct RowsParams {
 // accept tests in order, stop at the first rejection.  The parts were
 // written by other CTAs before their ticket, so they are read from L2.
 template <typename T>
-__device__ void decide_request(const RowsParams& p, int r, int off, int L, int splits) {
+__device__ void decide_request(const RowsParams& p, int r, int off, int L, int splits,
+                               int splits_bonus) {
   const T* P = static_cast<const T*>(p.P);
   const uint32_t rid = p.req_id ? p.req_id[r] : (uint32_t)r;
   int k = L;
@@ -126,7 +127,7 @@ __device__ void decide_request(const RowsParams& p, int r, int off, int L, int s
       key = 0ull;
 #pragma unroll
       for (int q = 0; q < kVerifySplits; ++q)
-        if (q < splits) {
+        if (q < splits_bonus) {
           const unsigned long long kq = __ldcg(&rp[q].key);
           key = kq > key ? kq : key;
         }
@@ -347,7 +348,7 @@ __device__ __forceinline__ void finish_item(const RowsParams& p, RowFold& f, int
 // The last CTA to finish (a ticket) decides every request, one thread each.
 template <typename T>
 __device__ __forceinline__ void decide_all(const RowsParams& p, const int* s_off, int splits,
-                                           RowsShared& sh) {
+                                           int splits_bonus, RowsShared& sh) {
   const int tid = threadIdx.x;
   __threadfence();
   __syncthreads();
@@ -356,7 +357,7 @@ __device__ __forceinline__ void decide_all(const RowsParams& p, const int* s_off
   if (!sh.last) return;
   __threadfence();
   for (int r = tid; r < p.R; r += kRowThreads)
-    decide_request<T>(p, r, s_off[r], s_off[r + 1] - s_off[r] - 1, splits);
+    decide_request<T>(p, r, s_off[r], s_off[r + 1] - s_off[r] - 1, splits, splits_bonus);
   if (tid == 0) *p.ticket = 0u;   // ready for the next call on the stream
 }
 
@@ -372,20 +373,62 @@ __global__ void __launch_bounds__(kRowThreads, 4) verify_rows(RowsParams p) {
   row_offsets(p, s_off, sh);
   // Rows are split into as many vocabulary chunks as keep every CTA busy
   // with about one item (at most kVerifySplits): fewer, longer items stream
-  // more bytes per block reduction.
+  // more bytes per block reduction.  Greedy rows all cost the same.  In the
+  // sampled path a bonus row also draws a Philox-Gumbel key per entry, about
+  // four times a tested row's work, so bonus rows get four times the splits
+  // and the items cost about the same: the tested rows' items come first,
+  // then the bonus rows'.
   const int B = s_off[p.R];
-  const int splits = max(1, min(kVerifySplits, (int)gridDim.x / B));
+  int splits, splits_bonus;
+  if (!SAMPLED) {
+    splits = splits_bonus = max(1, min(kVerifySplits, (int)gridDim.x / B));
+  } else {
+    const int n_tested = B - p.R;
+    splits = max(1, min(kVerifySplits / 4, (int)gridDim.x / (n_tested + 4 * p.R)));
+    splits_bonus = 4 * splits;
+  }
   const int chunk = ((p.V + splits - 1) / splits + epc - 1) / epc * epc;
-  const int n_items = B * splits;
+  const int chunk_bonus = ((p.V + splits_bonus - 1) / splits_bonus + epc - 1) / epc * epc;
+  const int n_tested_items = SAMPLED ? (B - p.R) * splits : 0;
+  const int n_items = SAMPLED ? n_tested_items + p.R * splits_bonus : B * splits;
   const T* P = static_cast<const T*>(p.P);
   for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
-    const int b = item / splits, sp = item - b * splits;
-    const int r = row_request(s_off, p.R, b), t = b - s_off[r];
+    int r, t, sp, ck;
+    if (!SAMPLED) {
+      const int b = item / splits;
+      sp = item - b * splits;
+      r = row_request(s_off, p.R, b);
+      t = b - s_off[r];
+      ck = chunk;
+    } else if (item < n_tested_items) {
+      // k-th tested row: request r holds tested rows s_off[r] - r ..
+      // s_off[r + 1] - r - 2 of the tested order
+      const int k = item / splits;
+      sp = item - k * splits;
+      int lo = 0, hi = p.R - 1;
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (s_off[mid] - mid <= k)
+          lo = mid;
+        else
+          hi = mid - 1;
+      }
+      r = lo;
+      t = k - (s_off[r] - r);
+      ck = chunk;
+    } else {
+      const int q = item - n_tested_items;
+      r = q / splits_bonus;
+      sp = q - r * splits_bonus;
+      t = s_off[r + 1] - s_off[r] - 1;
+      ck = chunk_bonus;
+    }
+    const int b = s_off[r] + t;
     const bool bonus = (t == s_off[r + 1] - s_off[r] - 1);
     const uint32_t rid = p.req_id ? p.req_id[r] : (uint32_t)r;
     const T* row = P + ((size_t)r * (p.gamma + 1) + t) * p.V;
-    const int v_begin = sp * chunk;
-    const int v_end = min(p.V, v_begin + chunk);
+    const int v_begin = sp * ck;
+    const int v_end = min(p.V, v_begin + ck);
     const int v_first = v_begin + (int)threadIdx.x * epc;
     RowFold f = rowfold_empty();
     constexpr int kUnroll = SAMPLED ? 4 : 8;
@@ -405,7 +448,7 @@ __global__ void __launch_bounds__(kRowThreads, 4) verify_rows(RowsParams p) {
     }
     finish_item<SAMPLED>(p, f, b * kVerifySplits + sp, v_first, v_end, sh);
   }
-  decide_all<T>(p, s_off, splits, sh);
+  decide_all<T>(p, s_off, splits, splits_bonus, sh);
 }
 
 __global__ void verify_finish(const int* rej_list, const unsigned int* n_rej,
