@@ -242,6 +242,7 @@ __device__ __forceinline__ void fold32(RowState& st, const uint32_t (&acc)[32], 
   }
 }
 
+template <bool DUP>   // p.dup as a compile-time constant: the R > 64 path carries none of it
 __global__ void __launch_bounds__(kTcThreads, 1)
     propose_tc_kernel(const __grid_constant__ CUtensorMap tmW,
                       const __grid_constant__ CUtensorMap tmU, const TcParams p) {
@@ -419,10 +420,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int row = q * 32 + lane;   // row within the M-tile
     // With dup, rows 64..127 hold the requests of rows 0..63 again, and the
     // two copies of a request fold different 32-column chunks of each tile.
-    const int rrow = p.dup ? (row & 63) : row;   // the request's row (its U row)
+    const int rrow = DUP ? (row & 63) : row;   // the request's row (its U row)
     const int r = r0 + rrow;
     const bool valid = r < p.R;
-    const bool warp_rows = r0 + (p.dup ? (q & 1) : q) * 32 < p.R;   // any request in this warp?
+    const bool warp_rows = r0 + (DUP ? (q & 1) : q) * 32 < p.R;   // any request in this warp?
     const uint32_t rid = valid ? (p.req_id ? p.req_id[r] : (uint32_t)r) : 0u;
 
     // The keys of step j-1 come from the previous grid: wait until it has
@@ -438,7 +439,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const bool biased = (j > 0) || p.bias_at_first;
       int my_tok = -1;
       if (lane < 16) {
-        const int rr = r0 + (p.dup ? ((e + 8 * lane) & 63) : (e + 8 * lane));
+        const int rr = r0 + (DUP ? ((e + 8 * lane) & 63) : (e + 8 * lane));
         if (biased && rr < p.R) {
           int tk = (j == 0) ? p.prev_tok[rr]
                             : (int)key_index(__ldcg(&p.keys[(size_t)(j - 1) * p.R_max + rr]));
@@ -495,25 +496,42 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // c ^ (row & 7) of that row.
         uint4 u[8];
         const unsigned char* urow = ring + s * kBox + rrow * 128;
+        const int cc = q >> 1;   // DUP: this copy's 32-column chunk of the half
         if (warp_rows) {
+          if constexpr (DUP) {
 #pragma unroll
-          for (int c = 0; c < 8; ++c)
-            u[c] = *reinterpret_cast<const uint4*>(urow + ((c ^ (rrow & 7)) << 4));
+            for (int c = 0; c < 4; ++c)
+              u[c] = *reinterpret_cast<const uint4*>(urow + (((cc * 4 + c) ^ (rrow & 7)) << 4));
+          } else {
+#pragma unroll
+            for (int c = 0; c < 8; ++c)
+              u[c] = *reinterpret_cast<const uint4*>(urow + ((c ^ (rrow & 7)) << 4));
+          }
         }
         __syncwarp();
         if (lane == 0) tc::mbar_arrive(&empty[s]);   // the slot's data is in registers
         __syncwarp();
         if (warp_rows) {
+          if constexpr (DUP) {   // one chunk: the other copy folds the other
+            const int v0 = vx + cc * 32;
+            if (v0 < p.V) {
+              uint32_t acc[32];
+              tc::tmem_ld_32x32b_x32_wait(tmem_base + ((uint32_t)(q * 32) << 16) +
+                                              (uint32_t)(buf * kTileN + hs * kHalf + cc * 32),
+                                          acc);
+              fold32(st, acc, u, v0, p, rid);
+            }
+          } else {
 #pragma unroll
-          for (int c = 0; c < 2; ++c) {
-            if (p.dup && c != (q >> 1)) continue;   // the other copy folds this chunk
-            const int v0 = vx + c * 32;
-            if (v0 >= p.V) break;
-            uint32_t acc[32];
-            tc::tmem_ld_32x32b_x32_wait(tmem_base + ((uint32_t)(q * 32) << 16) +
-                                            (uint32_t)(buf * kTileN + hs * kHalf + c * 32),
-                                        acc);
-            fold32(st, acc, u + 4 * c, v0, p, rid);
+            for (int c = 0; c < 2; ++c) {
+              const int v0 = vx + c * 32;
+              if (v0 >= p.V) break;
+              uint32_t acc[32];
+              tc::tmem_ld_32x32b_x32_wait(tmem_base + ((uint32_t)(q * 32) << 16) +
+                                              (uint32_t)(buf * kTileN + hs * kHalf + c * 32),
+                                          acc);
+              fold32(st, acc, u + 4 * c, v0, p, rid);
+            }
           }
         }
       }
@@ -538,9 +556,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         st.best_z = o.best_z;
         st.best_v = o.best_v;
       }
-      if (p.dup && row >= 64) xch2[row - 64] = st;
+      if (DUP && row >= 64) xch2[row - 64] = st;
     }
-    if (p.dup) {
+    if (DUP) {
       asm volatile("bar.sync 1, 256;" ::: "memory");
       if (hs == 0 && row < 64) {
         const RowState o = xch2[row];
@@ -553,7 +571,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
       }
     }
-    if (hs == 0 && (!p.dup || row < 64) && valid && TC_CHECK(vr < p.n_part && r < p.R_max, 5)) {
+    if (hs == 0 && (!DUP || row < 64) && valid && TC_CHECK(vr < p.n_part && r < p.R_max, 5)) {
       atomicMax(&p.keys[(size_t)j * p.R_max + r], make_key(st.best_z, st.best_v));
       p.parts[((size_t)j * p.n_part + vr) * p.R_max + r] = make_float2(st.m2, st.s);
     }
@@ -653,8 +671,11 @@ cudaError_t launch_propose_tc(const Ctx& ctx, const ProposeArgs& a, cudaStream_t
   cudaError_t e = cudaMemsetAsync(ctx.ws.keys, 0,
                                   sizeof(unsigned long long) * (size_t)a.gamma * ctx.cfg.R_max, s);
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(propose_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  e = cudaFuncSetAttribute(propose_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            kSmemBytes);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(propose_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kSmemBytes);
   if (e != cudaSuccess) return e;
 
   TcParams p{};
@@ -702,7 +723,8 @@ cudaError_t launch_propose_tc(const Ctx& ctx, const ProposeArgs& a, cudaStream_t
   for (int j = 0; j < a.gamma; ++j) {
     p.j = j;
     cfg.numAttrs = j > 0 ? 2 : 1;
-    e = cudaLaunchKernelEx(&cfg, propose_tc_kernel, tmW, tmU, p);
+    e = p.dup ? cudaLaunchKernelEx(&cfg, propose_tc_kernel<true>, tmW, tmU, p)
+              : cudaLaunchKernelEx(&cfg, propose_tc_kernel<false>, tmW, tmU, p);
     if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     count_launch(ctx);
