@@ -22,6 +22,7 @@
 // request.
 #include "dsd_common.cuh"
 #include "schedule.cuh"
+#include "tc_ptx.cuh"
 
 namespace dsd {
 
@@ -132,11 +133,14 @@ __global__ void __launch_bounds__(kSimtThreads) simt_bias_kernel(SimtParams p) {
   constexpr int epc = 16 / (int)sizeof(T);
   const int rank = p.rank;
   const int nch = rank / epc;
-  const int mstride = rank + 4;
+  // Markov rows of request pairs interleaved: pair pp holds element k of
+  // requests 2 pp and 2 pp + 1 side by side, so one 8-byte word feeds both
+  // halves of a packed fp32x2 FMA
+  const int mstride2 = 2 * rank + 8;
   unsigned char* Ws = smem;
   float* ms = reinterpret_cast<float*>(smem + (size_t)kSimtTileV * nch * 16);
   // candidate lists (step mode with p.cand), after ms
-  unsigned long long* c_list = reinterpret_cast<unsigned long long*>(ms + (size_t)kSimtRC * (rank + 4));
+  unsigned long long* c_list = reinterpret_cast<unsigned long long*>(ms + (size_t)(kSimtRC / 2) * mstride2);
   unsigned long long* c_buf = c_list + kSimtRC * kCandK;
   unsigned long long* c_thr = c_buf + kSimtRC * kSimtTileV;
   int* c_cnt = reinterpret_cast<int*>(c_thr + kSimtRC);
@@ -207,25 +211,39 @@ __global__ void __launch_bounds__(kSimtThreads) simt_bias_kernel(SimtParams p) {
     __syncthreads();
     // the Markov rows (or the head's representations), 16 bytes per load
     if (p.A) {
-      for (int idx = tid; idx < kSimtRC * (rank / 4); idx += kSimtThreads) {
-        const int rr = idx / (rank / 4), k = (idx - rr * (rank / 4)) * 4;
-        float4 m = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (rr < nr && s_bias[rr])
-          m = __ldg(reinterpret_cast<const float4*>(
-              p.A + ((size_t)s_req[rr] * p.gamma + s_pos[rr]) * rank + k));
-        *reinterpret_cast<float4*>(ms + rr * mstride + k) = m;
+      for (int idx = tid; idx < (kSimtRC / 2) * (rank / 4); idx += kSimtThreads) {
+        const int pp = idx / (rank / 4), k = (idx - pp * (rank / 4)) * 4;
+        float4 m[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int rr = 2 * pp + h;
+          m[h] = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (rr < nr && s_bias[rr])
+            m[h] = __ldg(reinterpret_cast<const float4*>(
+                p.A + ((size_t)s_req[rr] * p.gamma + s_pos[rr]) * rank + k));
+        }
+        float4* dst = reinterpret_cast<float4*>(ms + pp * mstride2 + 2 * k);
+        dst[0] = make_float4(m[0].x, m[1].x, m[0].y, m[1].y);
+        dst[1] = make_float4(m[0].z, m[1].z, m[0].w, m[1].w);
       }
     } else {
-      for (int idx = tid; idx < kSimtRC * nch; idx += kSimtThreads) {
-        const int rr = idx / nch, k = (idx - rr * nch) * epc;
-        float m[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-        if (rr < nr && s_bias[rr]) {
-          unpack16<T>(ld_keep16(E + (size_t)s_prev[rr] * rank + k), m);
+      for (int idx = tid; idx < (kSimtRC / 2) * nch; idx += kSimtThreads) {
+        const int pp = idx / nch, k = (idx - pp * nch) * epc;
+        float m[2][8];
 #pragma unroll
-          for (int e = 0; e < epc; ++e) m[e] = act_apply(m[e], p.act);
+        for (int h = 0; h < 2; ++h) {
+          const int rr = 2 * pp + h;
+#pragma unroll
+          for (int e = 0; e < 8; ++e) m[h][e] = 0.f;
+          if (rr < nr && s_bias[rr]) {
+            unpack16<T>(ld_keep16(E + (size_t)s_prev[rr] * rank + k), m[h]);
+#pragma unroll
+            for (int e = 0; e < epc; ++e) m[h][e] = act_apply(m[h][e], p.act);
+          }
         }
+        float4* dst = reinterpret_cast<float4*>(ms + pp * mstride2 + 2 * k);
 #pragma unroll
-        for (int e = 0; e < epc; ++e) ms[rr * mstride + k + e] = m[e];
+        for (int e = 0; e < epc; e += 2) dst[e / 2] = make_float4(m[0][e], m[1][e], m[0][e + 1], m[1][e + 1]);
       }
     }
     if (cand) {
@@ -285,14 +303,17 @@ __global__ void __launch_bounds__(kSimtThreads) simt_bias_kernel(SimtParams p) {
       cp_async_wait();
       __syncthreads();
       if (v0 + vp >= p.V) continue;   // both rows past the vocabulary
-      float acc[kSimtRows][kSimtRPT];
+      // accumulators of request pairs: one packed fp32x2 FMA per W element
+      // and pair (each half rounds as a scalar fmaf would)
+      uint64_t acc2[kSimtRows][kSimtRPT / 2];
 #pragma unroll
       for (int rho = 0; rho < kSimtRows; ++rho)
 #pragma unroll
-        for (int i = 0; i < kSimtRPT; ++i) acc[rho][i] = 0.f;
+        for (int h = 0; h < kSimtRPT / 2; ++h) acc2[rho][h] = 0ull;
       const int r1 = vp + kSimtHalfV;
       const unsigned char* wrow0 = Ws + (size_t)vp * nch * 16;
       const unsigned char* wrow1 = Ws + (size_t)r1 * nch * 16;
+      const float* mbase = ms + (qq * (kSimtRPT / 2)) * mstride2;
       for (int ch = 0; ch < nch; ++ch) {
         const uint4 q0 = *reinterpret_cast<const uint4*>(wrow0 + (ch ^ (vp & p.swz_mask)) * 16);
         const uint4 q1 = *reinterpret_cast<const uint4*>(wrow1 + (ch ^ (r1 & p.swz_mask)) * 16);
@@ -300,15 +321,24 @@ __global__ void __launch_bounds__(kSimtThreads) simt_bias_kernel(SimtParams p) {
         unpack16<T>(q0, w0);
         unpack16<T>(q1, w1);
 #pragma unroll
-        for (int i = 0; i < kSimtRPT; ++i) {
-          const float* mrow = ms + (qq * kSimtRPT + i) * mstride + ch * epc;
+        for (int h = 0; h < kSimtRPT / 2; ++h) {
+          const ulonglong2* mrow =
+              reinterpret_cast<const ulonglong2*>(mbase + h * mstride2 + ch * epc * 2);
 #pragma unroll
-          for (int e = 0; e < epc; ++e) {
-            acc[0][i] = fmaf(w0[e], mrow[e], acc[0][i]);
-            acc[1][i] = fmaf(w1[e], mrow[e], acc[1][i]);
+          for (int e2 = 0; e2 < epc / 2; ++e2) {
+            const ulonglong2 m2 = mrow[e2];
+            acc2[0][h] = tc::fma2(tc::pack2(w0[2 * e2], w0[2 * e2]), m2.x, acc2[0][h]);
+            acc2[1][h] = tc::fma2(tc::pack2(w1[2 * e2], w1[2 * e2]), m2.x, acc2[1][h]);
+            acc2[0][h] = tc::fma2(tc::pack2(w0[2 * e2 + 1], w0[2 * e2 + 1]), m2.y, acc2[0][h]);
+            acc2[1][h] = tc::fma2(tc::pack2(w1[2 * e2 + 1], w1[2 * e2 + 1]), m2.y, acc2[1][h]);
           }
         }
       }
+      float acc[kSimtRows][kSimtRPT];
+#pragma unroll
+      for (int rho = 0; rho < kSimtRows; ++rho)
+#pragma unroll
+        for (int h = 0; h < kSimtRPT / 2; ++h) tc::unpack2(acc2[rho][h], acc[rho][2 * h], acc[rho][2 * h + 1]);
 #pragma unroll
       for (int rho = 0; rho < kSimtRows; ++rho)
 #pragma unroll
