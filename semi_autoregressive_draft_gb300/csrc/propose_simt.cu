@@ -33,6 +33,7 @@ constexpr int kSimtRPT = 4;   // requests per thread
 constexpr int kSimtRows = 2;  // vocabulary rows per thread (vp and vp + kSimtTileV / 2)
 constexpr int kSimtHalfV = kSimtTileV / kSimtRows;
 static_assert(kSimtThreads == kSimtHalfV * (kSimtRC / kSimtRPT), "thread = (row pair, request group)");
+static_assert(kSimtRPT == 4 && kSimtHalfV % 4 == 0, "a quad of lanes shares one Philox block per request");
 
 enum SimtMode { kModeStep = 0, kModeResidual = 1 };
 
@@ -300,6 +301,32 @@ __global__ void __launch_bounds__(kSimtThreads) simt_bias_kernel(SimtParams p) {
               pval[rho][i] = ld_elem(P, ((size_t)s_req[rr] * (p.gamma + 1) + s_pos[rr]) * p.V + v);
         }
       }
+      // the Philox words of this thread's Gumbel noise, also computed while
+      // the W copies are in flight.  The four lanes of a quad hold four
+      // consecutive vocabulary entries, which share one Philox block per
+      // request: lane d of the quad computes the block of request 4 qq + d
+      // and the quad hands the words round by shuffles (every lane takes
+      // part, so this comes before any lane leaves the tile).
+      uint32_t nword[kSimtRows][kSimtRPT];
+      if (MODE == kModeResidual || p.sampled) {
+        const int d = lane & 3, qbase = lane & ~3;
+        const int rr_d = qq * kSimtRPT + d;
+        const uint32_t c1 = (MODE == kModeResidual) ? (uint32_t)s_pos[rr_d] : (uint32_t)p.j;
+        const uint32_t c3 = (MODE == kModeResidual) ? 2u : 0u;
+#pragma unroll
+        for (int rho = 0; rho < kSimtRows; ++rho) {
+          const uint32_t v = (uint32_t)(v0 + vp + rho * kSimtHalfV);
+          const Philox4 ph = philox4x32_10(v >> 2, c1, s_rid[rr_d], c3, p.k0, p.k1);
+#pragma unroll
+          for (int i = 0; i < kSimtRPT; ++i) {
+            const uint32_t x = __shfl_sync(0xffffffffu, ph.x, qbase + i);
+            const uint32_t y = __shfl_sync(0xffffffffu, ph.y, qbase + i);
+            const uint32_t z = __shfl_sync(0xffffffffu, ph.z, qbase + i);
+            const uint32_t w = __shfl_sync(0xffffffffu, ph.w, qbase + i);
+            nword[rho][i] = d == 0 ? x : (d == 1 ? y : (d == 2 ? z : w));
+          }
+        }
+      }
       cp_async_wait();
       __syncthreads();
       if (v0 + vp >= p.V) continue;   // both rows past the vocabulary
@@ -347,7 +374,6 @@ __global__ void __launch_bounds__(kSimtThreads) simt_bias_kernel(SimtParams p) {
         const int rr = qq * kSimtRPT + i;
         if (rr >= nr || v >= p.V) continue;
         const float x = acc[rho][i] + uval[rho][i];
-        const uint32_t rid = s_rid[rr];
         if constexpr (MODE == kModeStep) {
           if (cand) {
             const unsigned long long ck = make_key(x, (uint32_t)v);
@@ -359,21 +385,16 @@ __global__ void __launch_bounds__(kSimtThreads) simt_bias_kernel(SimtParams p) {
           st[i].s = st[i].s * exp2f(st[i].m - M) + exp2f(x2 - M);
           st[i].m = M;
           float z = xs;
-          if (p.sampled) {
-            const Philox4 ph = philox4x32_10((uint32_t)v >> 2, (uint32_t)p.j, rid, 0u, p.k0, p.k1);
-            z += gumbel_from_word(philox_pick(ph, v & 3));
-          }
+          if (p.sampled) z += gumbel_from_word(nword[rho][i]);
           const unsigned long long key = make_key(z, (uint32_t)v);
           best[i] = key > best[i] ? key : best[i];
         } else {
           // residual: res = max(0, p - q) with q = exp(l/T - lse_q), p = exp(P/T - lseP)
-          const int pos = s_pos[rr];
           const float pl = pval[rho][i] * p.inv_T - s_lsep[rr];
           const float ql = x * p.inv_T - s_lseq[rr];
           const float pv = __expf(pl);
           const float qv = __expf(ql);
-          const Philox4 ph = philox4x32_10((uint32_t)v >> 2, (uint32_t)pos, rid, 2u, p.k0, p.k1);
-          const float g = gumbel_from_word(philox_pick(ph, v & 3));
+          const float g = gumbel_from_word(nword[rho][i]);
           if (pl > ql) {
             // log(p - q) = pl + log(1 - exp(ql - pl)), kept accurate when p ~ q
             const float lr = pl + log1pf(-__expf(ql - pl));
