@@ -30,9 +30,9 @@
 // walks each range's tiles in reverse, so it starts on the tiles pass 1 read
 // last, which may still be in L2.
 //
-// Grid: (M-tiles of 128 rows) x (vocabulary ranges), one CTA per SM; with an
-// even number of M-tiles, clusters of two CTAs (M-tiles 2i, 2i+1 of one
-// range) share every W box by TMA multicast.  Warp roles (12 warps):
+// Grid: (M-tiles of 128 rows) x (vocabulary ranges), one CTA per SM; the
+// M-tiles of one range read the same W tiles at about the same time, so all
+// but the first read them from L2.  Warp roles (12 warps):
 //   warp 0      TMA producer of W ([128 vocab x 64 K] boxes, 128-byte
 //               swizzle), 2-stage ring of two boxes per stage (64 KB)
 //   warp 1      TMEM allocator and MMA issuer: M = 128, N = 128, K = 16 per
@@ -94,7 +94,7 @@ struct LossParams {
   float* parts2;             // [n_vr][rows_max] partial L1
   float* ltgt;               // [rows] l at the target token
   int* status;
-  int rows, rows_max, V, rank, gamma, bias_at_first, n_vr, ntiles, mc;
+  int rows, rows_max, V, rank, gamma, bias_at_first, n_vr, ntiles;
 };
 
 struct LossBars {
@@ -213,18 +213,8 @@ __global__ void __launch_bounds__(kLThreads, 1)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int KC = p.rank / kKChunk;
-  // With multicast the two CTAs of a cluster are M-tiles 2i and 2i+1 of one
-  // vocabulary range; each loads half of every W box for both.
-  const int crank = p.mc ? (int)tc::cluster_ctarank() : 0;
-  int mt, vr;
-  if (p.mc) {
-    const int cl = blockIdx.x >> 1;
-    mt = 2 * (cl / p.n_vr) + crank;
-    vr = cl % p.n_vr;
-  } else {
-    mt = blockIdx.x / p.n_vr;
-    vr = blockIdx.x % p.n_vr;
-  }
+  const int mt = blockIdx.x / p.n_vr;
+  const int vr = blockIdx.x % p.n_vr;
   const int r0 = mt * kTileM;        // first row of this CTA's M-tile
   const int t0 = (int)(((long long)vr * p.ntiles) / p.n_vr);
   const int t1 = (int)(((long long)(vr + 1) * p.ntiles) / p.n_vr);
@@ -238,7 +228,7 @@ __global__ void __launch_bounds__(kLThreads, 1)
   if (tid == 0) {
     for (int i = 0; i < kNB; ++i) {
       tc::mbar_init(&b.bfull[i], 1);
-      tc::mbar_init(&b.bempty[i], p.mc ? 2 : 1);   // both CTAs' MMAs release a shared stage
+      tc::mbar_init(&b.bempty[i], 1);
     }
     for (int i = 0; i < 2 * kNU; ++i) {
       tc::mbar_init(&b.ufull[i], 1);
@@ -264,8 +254,6 @@ __global__ void __launch_bounds__(kLThreads, 1)
     tc::tc_fence_before();
   }
   __syncthreads();
-  // the peer's multicast copies and commits may only target initialised barriers
-  if (p.mc) tc::cluster_sync();
   tc::tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
 
@@ -281,15 +269,9 @@ __global__ void __launch_bounds__(kLThreads, 1)
           const int nch = KC - k0 < kCPS ? KC - k0 : kCPS;
           if (!wait_bar(&b.bempty[s], ((it / kNB) & 1) ^ 1, abort_flag, p.status)) break;
           tc::mbar_arrive_expect_tx(&b.bfull[s], (uint32_t)(nch * kBox));
-          for (int c = 0; c < nch; ++c) {
-            if (p.mc)   // this CTA's half of the box's rows, to both CTAs
-              tc::tma_load_2d_multicast(sB + (s * kCPS + c) * kBox + crank * (kBox / 2), &tmW,
-                                        &b.bfull[s], (k0 + c) * kKChunk,
-                                        t * kTileN + crank * (kTileN / 2), 0x3, pol);
-            else
-              tc::tma_load_2d(sB + (s * kCPS + c) * kBox, &tmW, &b.bfull[s], (k0 + c) * kKChunk,
-                              t * kTileN, pol);
-          }
+          for (int c = 0; c < nch; ++c)
+            tc::tma_load_2d(sB + (s * kCPS + c) * kBox, &tmW, &b.bfull[s], (k0 + c) * kKChunk,
+                            t * kTileN, pol);
         }
       }
       // Tail: wait (bounded) for the copies issued last in each stage, then
@@ -352,10 +334,7 @@ __global__ void __launch_bounds__(kLThreads, 1)
               tc::umma_bf16_ta(d_tmem, tmem_base + (uint32_t)(kAcol + kc * 32 + ks * 8),
                                db + 2 * ks, kIdesc, (kc | ks) != 0 ? 1u : 0u);
           }
-          if (p.mc)
-            tc::umma_commit_multicast(&b.bempty[s], 0x3);   // the stage is written by both CTAs
-          else
-            tc::umma_commit(&b.bempty[s]);
+          tc::umma_commit(&b.bempty[s]);
         }
         if (ok) tc::umma_commit(&b.accfull[buf]);
       }
@@ -528,9 +507,6 @@ __global__ void __launch_bounds__(kLThreads, 1)
   }
   tc::tc_fence_before();
   __syncthreads();
-  // neither CTA of a pair leaves while its peer may still address its
-  // shared memory (multicast copies, commit arrivals)
-  if (p.mc) tc::cluster_sync();
   if (warp == 1) {
     __syncwarp();
     tc::tc_fence_after();
@@ -656,13 +632,11 @@ cudaError_t launch_loss(const Ctx& ctx, const LossArgs& a, cudaStream_t s) {
   if (!encode) return cudaErrorNotSupported;
   const int rows = a.B * a.gamma;
   const int MT = (rows + kTileM - 1) / kTileM;
-  const int mc = (MT % 2 == 0) ? 1 : 0;
   CUtensorMap tmW, tmU, tmP;
   {
     const cuuint64_t dims[2] = {(cuuint64_t)a.rank, (cuuint64_t)a.V};
     const cuuint64_t strides[1] = {(cuuint64_t)a.rank * 2};
-    // with multicast each CTA of a pair loads half of the box's rows
-    const cuuint32_t box[2] = {kKChunk, (cuuint32_t)(mc ? kTileN / 2 : kTileN)};
+    const cuuint32_t box[2] = {kKChunk, (cuuint32_t)kTileN};
     const cuuint32_t estr[2] = {1, 1};
     if (encode(&tmW, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(a.W), dims, strides,
                box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -706,16 +680,11 @@ cudaError_t launch_loss(const Ctx& ctx, const LossArgs& a, cudaStream_t s) {
   p.bias_at_first = a.bias_at_first;
   p.n_vr = loss_vranges(ctx, rows);
   p.ntiles = (a.V + kTileN - 1) / kTileN;
-  p.mc = mc;
   const int grid = MT * p.n_vr;
 
-  cudaLaunchAttribute attr[2];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = mc ? 2 : 1;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kLThreads);
@@ -723,12 +692,12 @@ cudaError_t launch_loss(const Ctx& ctx, const LossArgs& a, cudaStream_t s) {
   cfg.stream = s;
   cfg.attrs = attr;
   // pass 1 in plain stream order; pass 2 with a programmatic dependency on it
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 0;
   e = cudaLaunchKernelEx(&cfg, loss_tc_kernel<1>, tmW, tmU, tmP, p);
   if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   count_launch(ctx);
-  cfg.numAttrs = 2;
+  cfg.numAttrs = 1;
   e = cudaLaunchKernelEx(&cfg, loss_tc_kernel<2>, tmW, tmU, tmP, p);
   if (e == cudaSuccess) e = cudaGetLastError();
   if (e != cudaSuccess) return e;
@@ -760,7 +729,7 @@ cudaError_t launch_loss(const Ctx& ctx, const LossArgs& a, cudaStream_t s) {
   fcfg.gridDim = dim3((rows + kFinThreads - 1) / kFinThreads);
   fcfg.blockDim = dim3(kFinThreads);
   fcfg.stream = s;
-  fcfg.attrs = attr + 1;    // programmatic dependency on pass 2
+  fcfg.attrs = attr;        // programmatic dependency on pass 2
   fcfg.numAttrs = 1;
   e = cudaLaunchKernelEx(&fcfg, loss_finalize_kernel, f);
   if (e != cudaSuccess) return e;

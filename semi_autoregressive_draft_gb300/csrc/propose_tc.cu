@@ -104,7 +104,6 @@ struct TcParams {
   int* status;
   int j;                     // draft position of this launch
   int R, R_max, V, rank, gamma, bias_at_first, n_part, n_vr, ntiles, sampled;
-  int mc;                    // clusters of the two M-tiles of a range share W by multicast
   int dup;                   // R <= 64: rows 64..127 repeat rows 0..63 and take the second
                              // 32-column chunk of every 64-column half
   float inv_T;
@@ -268,11 +267,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int KC = p.rank / kKChunk;
   const int j = p.j;
-  // With multicast the two CTAs of a cluster are the two M-tiles of one
-  // vocabulary range; each loads half of every W box for both.
-  const int crank = p.mc ? (int)tc::cluster_ctarank() : 0;
-  const int mt = p.mc ? crank : blockIdx.x / p.n_vr;
-  const int vr = p.mc ? (int)(blockIdx.x >> 1) : blockIdx.x - mt * p.n_vr;
+  const int mt = blockIdx.x / p.n_vr;
+  const int vr = blockIdx.x - mt * p.n_vr;
   const int r0 = mt * kTileM;        // first request of this CTA's M-tile
   const int t0 = (int)(((long long)vr * p.ntiles) / p.n_vr);
   const int t1 = (int)(((long long)(vr + 1) * p.ntiles) / p.n_vr);
@@ -285,7 +281,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   if (tid == 0) {
     for (int i = 0; i < kNB; ++i) {
       tc::mbar_init(&b.bfull[i], 1);
-      tc::mbar_init(&b.bempty[i], p.mc ? 2 : 1);   // both CTAs' MMAs release a shared stage
+      tc::mbar_init(&b.bempty[i], 1);
     }
     for (int i = 0; i < 2 * kNU; ++i) {
       tc::mbar_init(&b.ufull[i], 1);
@@ -310,8 +306,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     tc::tc_fence_before();
   }
   __syncthreads();
-  // the peer's multicast copies and commits may only target initialised barriers
-  if (p.mc) tc::cluster_sync();
   tc::tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
 
@@ -326,15 +320,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           const int nch = KC - k0 < kCPS ? KC - k0 : kCPS;
           if (!wait_bar(&b.bempty[s], ((it / kNB) & 1) ^ 1, abort_flag, p.status)) break;
           tc::mbar_arrive_expect_tx(&b.bfull[s], (uint32_t)(nch * kBox));
-          for (int c = 0; c < nch; ++c) {
-            if (p.mc)   // this CTA's half of the box's rows, to both CTAs
-              tc::tma_load_2d_multicast(sB + (s * kCPS + c) * kBox + crank * (kBox / 2), &tmW,
-                                        &b.bfull[s], (k0 + c) * kKChunk,
-                                        t * kTileN + crank * (kTileN / 2), 0x3, pol);
-            else
-              tc::tma_load_2d(sB + (s * kCPS + c) * kBox, &tmW, &b.bfull[s], (k0 + c) * kKChunk,
-                              t * kTileN, pol);
-          }
+          for (int c = 0; c < nch; ++c)
+            tc::tma_load_2d(sB + (s * kCPS + c) * kBox, &tmW, &b.bfull[s], (k0 + c) * kKChunk,
+                            t * kTileN, pol);
         }
       // Tail: wait (bounded) for the copies issued last in each stage, then
       // for the consumer's release of every stage.  The releases are
@@ -401,10 +389,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             for (int ks = 0; ks < kKChunk / 16; ++ks)   // K = 16 is 32 bytes = 2 units
               tc::umma_bf16(d_tmem, da + 2 * ks, db + 2 * ks, kIdesc, (kc | ks) != 0 ? 1u : 0u);
           }
-          if (p.mc)
-            tc::umma_commit_multicast(&b.bempty[s], 0x3);   // the stage is written by both CTAs
-          else
-            tc::umma_commit(&b.bempty[s]);
+          tc::umma_commit(&b.bempty[s]);
         }
         if (ok) tc::umma_commit(&b.accfull[buf]);
       }
@@ -578,9 +563,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   }
   tc::tc_fence_before();
   __syncthreads();
-  // neither CTA of a pair leaves while its peer may still address its
-  // shared memory (multicast copies, commit arrivals)
-  if (p.mc) tc::cluster_sync();
   if (warp == 1) {
     __syncwarp();
     tc::tc_fence_after();
@@ -649,9 +631,7 @@ cudaError_t launch_propose_tc(const Ctx& ctx, const ProposeArgs& a, cudaStream_t
   {
     const cuuint64_t dims[2] = {(cuuint64_t)a.rank, (cuuint64_t)a.V};
     const cuuint64_t strides[1] = {(cuuint64_t)a.rank * 2};
-    // with multicast each CTA loads half of the box's rows
-    const int mc = (a.R > kTileM && a.R <= 2 * kTileM) ? 1 : 0;
-    const cuuint32_t box[2] = {kKChunk, (cuuint32_t)(mc ? kTileN / 2 : kTileN)};
+    const cuuint32_t box[2] = {kKChunk, (cuuint32_t)kTileN};
     const cuuint32_t estr[2] = {1, 1};
     if (encode(&tmW, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(a.W), dims, strides,
                box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -698,7 +678,6 @@ cudaError_t launch_propose_tc(const Ctx& ctx, const ProposeArgs& a, cudaStream_t
   p.k0 = (uint32_t)(a.seed & 0xFFFFFFFFull);
   p.k1 = (uint32_t)(a.seed >> 32);
   p.n_vr = tc_vranges(ctx, a.R);
-  p.mc = (a.R > kTileM && a.R <= 2 * kTileM) ? 1 : 0;
   p.dup = a.R <= kTileM / 2 ? 1 : 0;
   const int grid = ((a.R + kTileM - 1) / kTileM) * p.n_vr;
 
@@ -706,14 +685,9 @@ cudaError_t launch_propose_tc(const Ctx& ctx, const ProposeArgs& a, cudaStream_t
   // Steps after the first are launched with a programmatic dependency on the
   // previous step (see griddepcontrol in the kernel); the first follows the
   // memset of the keys in plain stream order.
-  // Two M-tiles: clusters of two CTAs (block 2 vr + m) sharing W by multicast.
-  cudaLaunchAttribute attr[2];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = p.mc ? 2 : 1;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kTcThreads);
@@ -722,7 +696,7 @@ cudaError_t launch_propose_tc(const Ctx& ctx, const ProposeArgs& a, cudaStream_t
   cfg.attrs = attr;
   for (int j = 0; j < a.gamma; ++j) {
     p.j = j;
-    cfg.numAttrs = j > 0 ? 2 : 1;
+    cfg.numAttrs = j > 0 ? 1 : 0;
     e = p.dup ? cudaLaunchKernelEx(&cfg, propose_tc_kernel<true>, tmW, tmU, p)
               : cudaLaunchKernelEx(&cfg, propose_tc_kernel<false>, tmW, tmU, p);
     if (e == cudaSuccess) e = cudaGetLastError();

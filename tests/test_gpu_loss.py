@@ -70,8 +70,8 @@ def run(dsd, spec, baf=True, R_max=None, **kw):
     return ctx, x, out, st
 
 
-# Shapes: one M-tile (no cluster), two and eight M-tiles (W multicast in
-# CTA pairs), three (odd: no multicast); ranks 64..256 including an odd
+# Shapes: one, two, three and eight M-tiles (the CTAs of one vocabulary
+# range read W at about the same time); ranks 64..256 including an odd
 # number of 64-wide K-chunks; vocabularies whose last tile is ragged in
 # either column half; gamma 1, 4, 7, 16; both readings of position 0.
 @pytest.mark.parametrize("B,G,V,r,baf", [
