@@ -1,27 +1,27 @@
 // dsd_propose_noalloc: the propose call for callers that must not allocate
 // device memory.
 //
-// Who needs it: code that runs where cudaMalloc is unavailable or forbidden,
-// e.g. a serving engine that owns every byte of device memory through its own
-// pool and does not let plugins allocate, code running while a stream is
-// being captured into a CUDA graph in a mode that forbids allocation, or
-// latency-critical paths that may not risk an allocation's implicit device
-// synchronisation.  Such callers cannot create a dsd_ctx (dsd_create
-// allocates the workspace), so this entry point takes the configuration
-// directly and keeps its scratch (the per-step argmax keys and per-CTA
-// log-sum-exp partials) in a fixed-size array in the library's own device
-// memory, which every GPU that loads the library holds until the process
-// exits.
+// Who needs it: code that may not call cudaMalloc once it runs, e.g. a
+// serving engine that hands all of device memory to its own pool at start-up
+// and does not let plugins allocate, or a latency-critical loop that must
+// not risk an allocation's implicit device synchronisation.  Such callers
+// cannot create a dsd_ctx (dsd_create allocates the workspace), so this
+// entry point takes the configuration directly and keeps its scratch (the
+// status word, the per-step argmax keys and the per-CTA log-sum-exp
+// partials) in a fixed-size array in the library's own device memory, which
+// every GPU that loads the library holds until the process exits.
 //
-// It runs the CUDA-core propose engine.  Sizes: R * gamma <= 1024, at most
-// 256 CTAs per draft step; larger calls are rejected with DSD_ERR_SHAPE.
+// It runs the CUDA-core propose engine.  Sizes: R * gamma <= 1024 and at most
+// 512 CTAs per draft step (twice the SM count up to 256 SMs, the split the
+// context call uses); larger R * gamma is rejected with DSD_ERR_SHAPE.
 // All calls on a device share the one array and each call leaves its
-// contents behind: the argmax keys are cleared at the start of every call,
-// and calls whose executions overlap on the GPU (different streams, or
-// concurrent host threads) race on the array and must be serialised by the
-// caller.  The first call on a device looks up the array's device address
-// (cudaGetSymbolAddress, with that device current); make that first call
-// before any stream capture.
+// contents behind: the status word and the argmax keys are cleared at the
+// start of every call, and calls whose executions overlap on the GPU
+// (different streams, or concurrent host threads) race on the array and
+// must be serialised by the caller.  The first call on a device looks up the
+// array's device address (cudaGetSymbolAddress, with that device current)
+// and caches it for the life of the process; make that first call before
+// any stream capture.  The cache does not survive cudaDeviceReset.
 #include <mutex>
 #include <string.h>
 
@@ -37,11 +37,11 @@ cudaError_t launch_propose_finalize_n(const Ctx& ctx, const ProposeArgs& a, int 
 namespace {
 
 constexpr int kNoallocMaxItems = 1024;  // R * gamma
-constexpr int kNoallocMaxParts = 256;   // CTAs of one propose step
+constexpr int kNoallocMaxParts = 512;   // CTAs of one propose step
 constexpr size_t kStatusBytes = 256;
 constexpr size_t kKeysBytes = sizeof(unsigned long long) * (size_t)kNoallocMaxItems;
 constexpr size_t kPartsBytes = sizeof(float2) * (size_t)kNoallocMaxItems * kNoallocMaxParts;
-constexpr size_t kScratchBytes = kStatusBytes + kKeysBytes + kPartsBytes;  // ~2 MB
+constexpr size_t kScratchBytes = kStatusBytes + kKeysBytes + kPartsBytes;  // ~4.2 MB
 
 struct DeviceScratch {
   bool ready;
@@ -93,7 +93,7 @@ extern "C" int dsd_propose_noalloc(int V, int rank, int gamma, int dtype, int ac
                                    const void* W, const float* conf, const int32_t* prev_tok,
                                    const uint32_t* req_id, float temperature, uint64_t seed,
                                    int32_t* tokens, float* lse_q, float* logit_at_tok,
-                                   float* survival, void* stream) {
+                                   float* survival, int32_t* status, void* stream) {
   if (V < 8 || V % 8 != 0) return DSD_ERR_ALIGN;
   const bool rank_ok = (rank % 64 == 0 && rank <= 256) || (rank > 0 && rank <= 64 && rank % 8 == 0);
   if (!rank_ok || gamma < 1 || gamma > dsd::kMaxGamma || R < 0) return DSD_ERR_SHAPE;
@@ -149,6 +149,10 @@ extern "C" int dsd_propose_noalloc(int V, int rank, int gamma, int dtype, int ac
   if (cudaMemsetAsync(c.ws.status, 0, sizeof(int), s) != cudaSuccess) return DSD_ERR_CUDA;
   if (dsd::launch_propose_simt(c, a, s) != cudaSuccess) return DSD_ERR_CUDA;
   if (dsd::launch_propose_finalize_n(c, a, dsd::simt_grid(c, V), s) != cudaSuccess)
+    return DSD_ERR_CUDA;
+  // the call's device status, copied in stream order (no allocation)
+  if (status && cudaMemcpyAsync(status, c.ws.status, sizeof(int32_t), cudaMemcpyDeviceToDevice,
+                                s) != cudaSuccess)
     return DSD_ERR_CUDA;
   return DSD_OK;
 }

@@ -40,13 +40,26 @@ def _outputs(R, G):
                 survival=torch.full((R, G), float("nan"), device=DEV))
 
 
-def _noalloc(dsd, spec, x, out):
+def _noalloc(dsd, spec, x, out, prev_tok=None, expect_status=0):
+    status = torch.full((1,), 99, dtype=torch.int32, device=DEV)
     dsd.dsd_propose_noalloc(spec.V, spec.r, spec.G, spec.dtype, "none", True, spec.R, x["U"],
-                            x["E"], x["W"], x["conf"], x["prev_tok"], x["req_id"],
+                            x["E"], x["W"], x["conf"],
+                            x["prev_tok"] if prev_tok is None else prev_tok, x["req_id"],
                             spec.temperature, x["seed"], out["tokens"], out["lse_q"],
-                            out["logit_at_tok"], out["survival"])
+                            out["logit_at_tok"], out["survival"], status=status)
     torch.cuda.synchronize()
+    assert int(status[0]) == expect_status
     return {k: v.cpu().numpy() for k, v in out.items()}
+
+
+def _context_propose(dsd, spec, x):
+    ctx = dsd.Context(spec.V, spec.r, spec.G, spec.R, dtype=spec.dtype, engine="simt")
+    ref = ctx.propose(x["U"], x["E"], x["W"], x["conf"], x["prev_tok"], x["req_id"],
+                      spec.temperature, x["seed"])
+    assert ctx.sync_status() == 0
+    ref = {k: v.cpu().numpy() for k, v in ref.items()}
+    ctx.close()
+    return ref
 
 
 def _same(a, b):
@@ -62,12 +75,7 @@ def test_noalloc_matches_context_propose_twice(dsd, dtype, temperature, seed):
     spec = synth.scaled(synth.CYCLE_SPECS["greedy"], R=19, V=2568, dtype=dtype, ew_std=0.3,
                         temperature=temperature, seed=seed)
     x = synth.cycle_inputs(spec, device=DEV)
-    ctx = dsd.Context(spec.V, spec.r, spec.G, spec.R, dtype=dtype, engine="simt")
-    ref = ctx.propose(x["U"], x["E"], x["W"], x["conf"], x["prev_tok"], x["req_id"],
-                      temperature, x["seed"])
-    assert ctx.sync_status() == 0
-    ref = {k: v.cpu().numpy() for k, v in ref.items()}
-    ctx.close()
+    ref = _context_propose(dsd, spec, x)
     first = _noalloc(dsd, spec, x, _outputs(spec.R, spec.G))
     second = _noalloc(dsd, spec, x, _outputs(spec.R, spec.G))
     _same(first, ref)
@@ -83,12 +91,28 @@ def test_noalloc_second_call_with_other_inputs(dsd):
     xs = synth.cycle_inputs(small, device=DEV)
     _noalloc(dsd, big, xb, _outputs(big.R, big.G))
     got = _noalloc(dsd, small, xs, _outputs(small.R, small.G))
-    ctx = dsd.Context(small.V, small.r, small.G, small.R, dtype="bf16", engine="simt")
-    ref = ctx.propose(xs["U"], xs["E"], xs["W"], xs["conf"], xs["prev_tok"], xs["req_id"], 0.0,
-                      xs["seed"])
-    ref = {k: v.cpu().numpy() for k, v in ref.items()}
-    ctx.close()
-    _same(got, ref)
+    _same(got, _context_propose(dsd, small, xs))
+
+
+def test_noalloc_more_vocabulary_tiles_than_ctas(dsd):
+    # 313 vocabulary tiles of 128: more tiles than CTAs per draft step, so
+    # every CTA walks several tiles; the split must match the context call's
+    spec = synth.scaled(synth.CYCLE_SPECS["greedy"], R=4, V=40000, ew_std=0.3, seed=47)
+    x = synth.cycle_inputs(spec, device=DEV)
+    ref = _context_propose(dsd, spec, x)
+    _same(_noalloc(dsd, spec, x, _outputs(spec.R, spec.G)), ref)
+    _same(_noalloc(dsd, spec, x, _outputs(spec.R, spec.G)), ref)
+
+
+def test_noalloc_reports_device_status_then_recovers(dsd):
+    # a prev_tok outside [0, V) is reported through the status output, and
+    # the next call, with valid inputs, reports 0 and drafts the same tokens
+    spec = synth.scaled(synth.CYCLE_SPECS["greedy"], R=6, V=2568, ew_std=0.3, seed=48)
+    x = synth.cycle_inputs(spec, device=DEV)
+    bad = x["prev_tok"].clone()
+    bad[2] = spec.V + 5
+    _noalloc(dsd, spec, x, _outputs(spec.R, spec.G), prev_tok=bad, expect_status=-1)
+    _same(_noalloc(dsd, spec, x, _outputs(spec.R, spec.G)), _context_propose(dsd, spec, x))
 
 
 def test_noalloc_rejects_sizes_beyond_its_scratch(dsd):
@@ -99,7 +123,7 @@ def test_noalloc_rejects_sizes_beyond_its_scratch(dsd):
         dsd.dsd_propose_noalloc(spec.V, spec.r, spec.G, "bf16", "none", True, spec.R, x["U"],
                                 x["E"], x["W"], x["conf"], x["prev_tok"], x["req_id"], 0.0, 1,
                                 out["tokens"], out["lse_q"], out["logit_at_tok"],
-                                out["survival"])
+                                out["survival"], status=None)
     assert ei.value.code == -4
     torch.cuda.synchronize()
     assert int(out["tokens"][0, 0]) == -7         # nothing was launched
