@@ -122,6 +122,23 @@ const char* dsd_last_error(const dsd_ctx* ctx);
  * calls made so far: DSD_OK, DSD_ERR_NONFINITE or DSD_ERR_TIMEOUT. */
 int dsd_sync_status(dsd_ctx* ctx, void* stream);
 
+/* Exercise the failure path of the bounded device waits.  The pages name no
+ * such call: their only failure handling is the scheduler's fallback under
+ * overload ([READ] 6); this diagnostic checks the library's own rule that a
+ * device wait which never completes ends in a status, not a hang.
+ * One CTA runs the same bounded mbarrier waits as the tensor-core kernels on
+ * barriers that nothing completes (no copy or tensor-core work is involved):
+ * one waiter gives up after poll_limit polls, records DSD_ERR_TIMEOUT in the
+ * context's status word and raises its CTA's abort flag; a second waiter,
+ * polling with the kernels' full limit, sees the flag and stops.
+ * poll_limit: 1 .. 2^20 (DSD_ERR_ARG otherwise, nothing launched).
+ * roles_out: optional device int32[3] (NULL: not written): [0], [1] = 1 if
+ * the first / second waiter saw its phase complete (0 expected), [2] = how
+ * many of the two left their wait (2 expected).
+ * After it, dsd_sync_status returns DSD_ERR_TIMEOUT (and clears it); the
+ * context stays usable. */
+int dsd_wait_selftest(dsd_ctx* ctx, uint32_t poll_limit, int32_t* roles_out, void* stream);
+
 /* Bytes of device workspace held by the context. */
 size_t dsd_workspace_bytes(const dsd_ctx* ctx);
 
@@ -495,32 +512,40 @@ int dsd_calibration(dsd_ctx* ctx, int M, const float* conf, const int32_t* accep
  * memory.  The paper has no counterpart: this is a library convenience.
  *
  * Some callers cannot call cudaMalloc: an inference engine that hands all of
- * device memory to its own pool and forbids plugins to allocate, code that
- * runs while a stream is being captured in a mode that forbids allocation,
+ * device memory to its own pool at start-up and forbids plugins to allocate,
  * or a latency-critical loop that must not pay an allocation's implicit
  * synchronisation.  They cannot create a dsd_ctx, whose workspace is
  * allocated, so this call takes the configuration fields directly (their
- * meaning and limits as in dsd_config) and computes exactly what dsd_propose
- * computes with the CUDA-core engine, on the current device.
+ * meaning and limits as in dsd_config) and runs dsd_propose's CUDA-core
+ * engine on the current device.  It drafts the same tokens as dsd_propose
+ * with engine DSD_ENGINE_SIMT; on devices with at most 256 SMs it splits the
+ * vocabulary the same way and its lse_q / logit_at_tok are the same values,
+ * beyond that they agree within the parity tolerance (1e-4).
  *
- * Its scratch (argmax keys and log-sum-exp partials, about 2 MB) is a
- * fixed-size array in the library's device memory, held by every GPU that
- * loads the library until the process exits.  Limits: R * gamma <= 1024;
- * larger calls return DSD_ERR_SHAPE without launching anything.  The call
- * allocates nothing (no cudaMalloc, cudaFree or allocating library routine).
- * All calls on a device share that array and each call leaves its contents
- * behind; the parts that must start at zero are cleared at the start of
- * every call.  Calls whose executions overlap on the GPU (other streams,
- * other host threads) race on the array: serialise them.  The first call on
- * a device looks up the array's device address with that device current;
- * make that first call before any stream capture.  Device-side problems
- * (non-finite logits) show up as non-finite lse_q / logit_at_tok values.
+ * Its scratch (status word, argmax keys and log-sum-exp partials, about
+ * 4.2 MB) is a fixed-size array in the library's device memory, held by
+ * every GPU that loads the library until the process exits.  Limits:
+ * R * gamma <= 1024; larger calls return DSD_ERR_SHAPE without launching
+ * anything.  The call allocates nothing (no cudaMalloc, cudaFree or
+ * allocating library routine).  All calls on a device share that array and
+ * each call leaves its contents behind; the parts that must start at zero
+ * are cleared at the start of every call.  Calls whose executions overlap on
+ * the GPU (other streams, other host threads) race on the array: serialise
+ * them.  The first call on a device looks up the array's device address
+ * with that device current and caches it for the process; make that first
+ * call before any stream capture.  The cached address does not survive
+ * cudaDeviceReset.
+ *
+ * status: optional device pointer to one int32 (NULL: not reported).  After
+ * the call's kernels it receives, in stream order, the device-side status of
+ * this call: DSD_OK, DSD_ERR_ARG (a prev_tok outside [0, V), drafted from
+ * token 0 instead) or DSD_ERR_NONFINITE (a non-finite logit or confidence).
  */
 int dsd_propose_noalloc(int V, int rank, int gamma, int dtype, int act, int bias_at_first,
                         int R, const void* U, const void* E, const void* W, const float* conf,
                         const int32_t* prev_tok, const uint32_t* req_id, float temperature,
                         uint64_t seed, int32_t* tokens, float* lse_q, float* logit_at_tok,
-                        float* survival, void* stream);
+                        float* survival, int32_t* status, void* stream);
 
 #ifdef __cplusplus
 }

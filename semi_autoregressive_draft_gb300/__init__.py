@@ -37,7 +37,7 @@ EXPORTED = [
     "dsd_propose", "dsd_schedule", "dsd_verify", "dsd_cycle", "dsd_cycle_host", "dsd_overlap",
     "dsd_propose_noalloc", "dsd_loss_forward", "dsd_confidence_head", "dsd_threshold_keep",
     "dsd_calibration", "dsd_propose_gated", "dsd_verify_gated", "dsd_propose_candidates",
-    "dsd_propose_rnn", "dsd_verify_rnn", "dsd_gumbel_noise",
+    "dsd_propose_rnn", "dsd_verify_rnn", "dsd_gumbel_noise", "dsd_wait_selftest",
 ]
 
 
@@ -97,6 +97,7 @@ def load_library(path: str | None = None):
         "dsd_verify_gated": (_I, [_P, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _F, _U64,
                                   _P, _P, _P]),
         "dsd_gumbel_noise": (_I, [_P, _P, _I, _P]),
+        "dsd_wait_selftest": (_I, [_P, ctypes.c_uint32, _P, _P]),
         "dsd_propose_rnn": (_I, [_P, _I, _P, _P, _P, _P, _I, _P, _P, _P, _P, _F, _U64, _P, _P,
                                  _P, _P, _P, _P]),
         "dsd_verify_rnn": (_I, [_P, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _F, _U64,
@@ -105,7 +106,7 @@ def load_library(path: str | None = None):
         "dsd_threshold_keep": (_I, [_P, _I, _P, _F, _P, _P]),
         "dsd_calibration": (_I, [_P, _I, _P, _P, _I, _P, _P, _P, _P]),
         "dsd_propose_noalloc": (_I, [_I, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _F,
-                                     _U64, _P, _P, _P, _P, _P]),
+                                     _U64, _P, _P, _P, _P, _P, _P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -290,18 +291,26 @@ def dsd_calibration(ctx, M, conf, accept_len, n_bins, bins, pos, metrics, stream
                                                _stream(stream, device)))
 
 
+def dsd_wait_selftest(ctx, poll_limit, roles_out=None, stream=None, device=0):
+    """Run the bounded-wait self-test kernel (a wait that never completes
+    must end in DSD_ERR_TIMEOUT, read by dsd_sync_status)."""
+    _check(ctx, load_library().dsd_wait_selftest(ctx, int(poll_limit), _ptr(roles_out),
+                                                 _stream(stream, device)))
+
+
 def dsd_propose_noalloc(V, rank, gamma, dtype, act, bias_at_first, R, U, E, W, conf, prev_tok,
                         req_id, temperature, seed, tokens, lse_q, logit_at_tok, survival,
-                        stream=None, device=0):
+                        status=None, stream=None, device=0):
     """Propose without a context and without allocating device memory (for
     callers that may not allocate); scratch lives in a fixed array inside the
-    library.  R * gamma <= 1024."""
+    library.  R * gamma <= 1024.  ``status`` (optional int32 device tensor of
+    one element) receives the call's device-side status."""
     rc = load_library().dsd_propose_noalloc(
         int(V), int(rank), int(gamma), DTYPES[dtype] if isinstance(dtype, str) else int(dtype),
         ACTS[act] if isinstance(act, str) else int(act), int(bool(bias_at_first)), int(R),
         _ptr(U), _ptr(E), _ptr(W), _ptr(conf), _ptr(prev_tok), _ptr(req_id), float(temperature),
         int(seed) & (2 ** 64 - 1), _ptr(tokens), _ptr(lse_q), _ptr(logit_at_tok), _ptr(survival),
-        _stream(stream, device))
+        _ptr(status), _stream(stream, device))
     if rc != DSD_OK:
         raise DsdError(rc, "dsd_propose_noalloc")
 

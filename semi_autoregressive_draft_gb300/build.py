@@ -32,6 +32,7 @@ SOURCES = [
     "loss_tc.cu",
     "confidence.cu",
     "gated.cu",
+    "wait_selftest.cu",
 ]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",

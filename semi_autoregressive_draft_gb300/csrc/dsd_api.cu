@@ -213,6 +213,17 @@ int dsd_gumbel_noise(const uint32_t* words, float* out, int n, void* stream) {
   return cudaGetLastError() == cudaSuccess ? DSD_OK : DSD_ERR_CUDA;
 }
 
+int dsd_wait_selftest(dsd_ctx* ctx, uint32_t poll_limit, int32_t* roles_out, void* stream) {
+  int rc = check_ctx(ctx);
+  if (rc) return rc;
+  if (poll_limit == 0 || poll_limit > (1u << 20))
+    return fail(ctx, DSD_ERR_ARG, "poll_limit %u outside [1, 2^20]", poll_limit);
+  cudaError_t e = dsd::launch_wait_selftest(*ctx, poll_limit, roles_out,
+                                            static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "wait self-test launch");
+  return DSD_OK;
+}
+
 int dsd_sync_status(dsd_ctx* ctx, void* stream) {
   int rc = check_ctx(ctx);
   if (rc) return rc;

@@ -204,6 +204,10 @@ struct LossArgs {
 
 cudaError_t launch_loss(const Ctx& ctx, const LossArgs& a, cudaStream_t s);
 
+// Self-test of the bounded mbarrier waits (wait_selftest.cu).
+cudaError_t launch_wait_selftest(const Ctx& ctx, uint32_t poll_limit, int32_t* roles_out,
+                                 cudaStream_t s);
+
 // Swizzle mask for 16-byte chunks of a staged table row (see propose_simt.cu).
 inline int chunk_swizzle_mask(int chunks_per_row) {
   if (chunks_per_row % 8 == 0) return 7;

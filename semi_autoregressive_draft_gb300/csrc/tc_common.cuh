@@ -1,7 +1,8 @@
 // Pieces shared by the tcgen05 kernels (propose_tc.cu, loss_tc.cu): bounded
 // mbarrier waits and the driver's tensor-map encoder.
 //
-// Every mbarrier wait is bounded: after kSpinLimit polls the waiter records
+// Every mbarrier wait is bounded: after kSpinLimit polls (or the limit the
+// caller passes) the waiter records
 // DSD_ERR_TIMEOUT, raises the CTA's abort flag (the other roles see it and
 // stop issuing work) and returns false.  Nothing traps.
 #pragma once
@@ -17,8 +18,8 @@ namespace dsd {
 constexpr uint32_t kSpinLimit = 1u << 22;        // mbarrier polls before giving up
 
 __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                         int* status) {
-  for (uint32_t i = 0; i < kSpinLimit; ++i) {
+                                         int* status, uint32_t limit = kSpinLimit) {
+  for (uint32_t i = 0; i < limit; ++i) {
     if (tc::mbar_try_wait(bar, parity)) return true;
     if ((i & 255u) == 255u && *abort_flag) return false;
   }
@@ -37,9 +38,9 @@ __device__ __forceinline__ void drain_bar(uint64_t* bar, uint32_t parity) {
 // Warp-uniform bounded wait: lane 0 polls, the verdict is broadcast, so the
 // warp stays converged for the .sync.aligned tcgen05 instructions after it.
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                          int* status) {
+                                          int* status, uint32_t limit = kSpinLimit) {
   int ok = 0;
-  if ((threadIdx.x & 31) == 0) ok = wait_bar(bar, parity, abort_flag, status) ? 1 : 0;
+  if ((threadIdx.x & 31) == 0) ok = wait_bar(bar, parity, abort_flag, status, limit) ? 1 : 0;
   ok = __shfl_sync(0xffffffffu, ok, 0);
   __syncwarp();
   return ok != 0;
