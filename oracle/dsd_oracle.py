@@ -438,6 +438,23 @@ def _draft_logits(U, E, W, prev_tok, tokens, r, t, bias_at_first, act, gate=None
     return ell
 
 
+def accept_probability(p_x, q_x):
+    """[WALK] 4.4 (the accept test of the verify step): the draft token x is
+    kept with probability min(1, p(x) / q(x))."""
+    return min(1.0, p_x / q_x)
+
+
+def correction_weights(p, q):
+    """[WALK] 4.4: after a rejection the next token is drawn from the residual
+    max(0, p - q), renormalised.  Returns the unnormalised weights and whether
+    the empty-residual reading applied: if sum(max(0, p - q)) <= 1e-12 sum(p),
+    which only rounding can produce, the draw falls back to p itself."""
+    res = np.maximum(0.0, p - q)
+    if np.sum(res) <= 1e-12 * np.sum(p):
+        return p, True
+    return res, False
+
+
 def verify(P, U, E, W, prev_tok, tokens, keep_len, req_id=None,
            temperature=0.0, seed=0, bias_at_first=True, act="none", gate=None, rnn=None):
     """Rejection verification of the kept prefix of every request.
@@ -481,7 +498,7 @@ def verify(P, U, E, W, prev_tok, tokens, keep_len, req_id=None,
                 p = softmax(_f64(P[r, t]) / T)
                 q = softmax(_draft_logits(U, E, W, prev_tok, tokens, r, t,
                                           bias_at_first, act, gate, rnn) / T)
-                accept_prob = min(1.0, p[x] / q[x])
+                accept_prob = accept_probability(p[x], q[x])
                 u = accept_uniform(seed, t, req)
                 accept_gap[r] = min(accept_gap[r], abs(u - accept_prob))
                 ok = u < accept_prob
@@ -494,13 +511,10 @@ def verify(P, U, E, W, prev_tok, tokens, keep_len, req_id=None,
             if T == 0.0:
                 z = _f64(P[r, k])
             else:
-                res = np.maximum(0.0, p_k - q_k)
+                w, _ = correction_weights(p_k, q_k)
                 g = vocab_gumbel(seed, k, req, STREAM_RESIDUAL, V)
-                if np.sum(res) <= 1e-12 * np.sum(p_k):
-                    z = np.log(p_k) + g
-                else:
-                    with np.errstate(divide="ignore"):
-                        z = np.where(res > 0.0, np.log(res), -np.inf) + g
+                with np.errstate(divide="ignore"):
+                    z = np.where(w > 0.0, np.log(w), -np.inf) + g
         else:
             if T == 0.0:
                 z = _f64(P[r, L])

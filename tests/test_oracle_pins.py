@@ -356,6 +356,147 @@ def test_verify_rejection_sampling_reproduces_the_target_distribution():
     assert 0.5 * np.abs(q0 - p0).sum() > 0.1
 
 
+def _random_pair(rng, V, p_zero=False, q_equal=False):
+    p = rng.dirichlet(np.full(V, 0.7))
+    if p_zero:
+        p[rng.integers(V)] = 0.0
+        p /= p.sum()
+    q = p.copy() if q_equal else rng.dirichlet(np.full(V, 0.7))
+    return p, q
+
+
+def _commit_distribution(p, q):
+    """Distribution of the token committed at one position when the draft
+    proposes x ~ q and the oracle's accept test and correction draw decide,
+    summed exactly over every draft outcome x."""
+    out = np.zeros_like(p)
+    for x in range(p.size):
+        if q[x] == 0.0:
+            continue                      # the draft never proposes x
+        a = O.accept_probability(p[x], q[x])
+        w, _ = O.correction_weights(p, q)
+        out[x] += q[x] * a
+        out += q[x] * (1.0 - a) * (w / w.sum())
+    return out
+
+
+@pytest.mark.parametrize("V", [2, 3, 4, 5])
+def test_rejection_step_is_exactly_lossless(V):
+    # [WALK] 4.4 / [READ] 3.1 (acceptance as overlap, lossless verification):
+    # sum_x q(x) [min(1, p/q) delta_{x=v} + (1 - min(1, p/q)) res(v)] = p(v)
+    # for every v, by exact enumeration over the draft outcome x
+    rng = np.random.default_rng(100 + V)
+    cases = [_random_pair(rng, V) for _ in range(40)]
+    cases += [_random_pair(rng, V, p_zero=True) for _ in range(10)]
+    cases += [_random_pair(rng, V, q_equal=True) for _ in range(3)]
+    q_one_hot = np.zeros(V)
+    q_one_hot[V - 1] = 1.0
+    cases.append((rng.dirichlet(np.ones(V)), q_one_hot))    # a point-mass draft
+    for p, q in cases:
+        assert np.max(np.abs(_commit_distribution(p, q) - p)) <= 1e-12
+    # the probability of accepting is the overlap sum_v min(p, q)
+    for p, q in cases:
+        acc = sum(q[x] * O.accept_probability(p[x], q[x]) for x in range(V) if q[x] > 0)
+        assert abs(acc - np.minimum(p, q).sum()) <= 1e-12
+
+
+def test_rejection_two_positions_joint_is_exact():
+    # Two drafted positions where both the draft q1 and the target p1 of the
+    # second position depend on the first token (the Markov head does this to
+    # q).  The first two committed tokens (a, b) must have the target's joint
+    # law p0(a) p1(b | a).  A rejection at position 0 ends the cycle; the
+    # second token then comes from the target itself, p1(. | a).
+    rng = np.random.default_rng(7)
+    for V in (2, 3, 4):
+        for _ in range(10):
+            p0, q0 = _random_pair(rng, V)
+            p1 = rng.dirichlet(np.full(V, 0.7), size=V)   # p1[a] = p1(. | a)
+            q1 = rng.dirichlet(np.full(V, 0.7), size=V)
+            J = np.zeros((V, V))
+            for x0 in range(V):
+                a0 = O.accept_probability(p0[x0], q0[x0])
+                w0, _ = O.correction_weights(p0, q0)
+                c0 = w0 / w0.sum()
+                # accepted at 0: position 1 is verified against p1(. | x0)
+                J[x0] += q0[x0] * a0 * _commit_distribution(p1[x0], q1[x0])
+                # rejected at 0: a ~ c0 and b ~ p1(. | a)
+                J += q0[x0] * (1.0 - a0) * c0[:, None] * p1
+            assert np.max(np.abs(J - p0[:, None] * p1)) <= 1e-12
+
+
+def test_correction_weights_by_hand_and_empty_residual():
+    p = np.array([0.5, 0.3, 0.2])
+    q = np.array([0.2, 0.5, 0.3])
+    w, fb = O.correction_weights(p, q)
+    assert not fb and np.allclose(w, [0.3, 0.0, 0.0], atol=1e-15)
+    w, fb = O.correction_weights(p, p.copy())
+    assert fb and np.array_equal(w, p)                 # empty residual: draw from p
+    tiny = p.copy()
+    tiny[0] += 1e-14
+    tiny[1] -= 1e-14
+    w, fb = O.correction_weights(tiny, p)               # residual 1e-14 <= 1e-12: fall back
+    assert fb and np.array_equal(w, tiny)
+    assert O.accept_probability(0.3, 0.5) == 0.6
+    assert O.accept_probability(0.5, 0.2) == 1.0
+
+
+def test_verify_uses_the_accept_threshold_and_the_empty_residual_fallback(monkeypatch):
+    # T = 1, no Markov bias (E = W = 0), so q = softmax(U[0, 0]) and
+    # p = softmax(P[0, 0]).  The draft token 3 is very unlikely under q
+    # (q(3) ~ 3e-9) and P lowers its logit by about 1e-6: accept probability
+    # about 1 - 1e-6, residual mass about 3e-15.
+    V = 4
+    U = np.array([[[0.0, 5.0, 2.0, -15.0]]])
+    P = np.zeros((1, 2, V))
+    P[0, 0] = U[0, 0]
+    P[0, 0, 3] += math.log(1.0 - 1e-6)
+    P[0, 1] = [0.0, 1.0, 0.0, 0.0]
+    E = np.zeros((V, 2))
+    W = np.zeros((V, 2))
+    tokens = np.array([[3]])
+    q = special.softmax(U[0, 0])
+    p = special.softmax(P[0, 0])
+    thr = min(1.0, p[3] / q[3])
+    assert 1.0 - 2e-6 < thr < 1.0
+    # the correction noise: +100 on token 3, so a draw from p picks 3 while
+    # a draw from the residual (which is 0 at token 3) cannot
+    monkeypatch.setattr(O, "vocab_gumbel",
+                        lambda seed, pos, req, stream, V_: np.array([0.0, 0.0, 0.0, 100.0]))
+
+    def run(u):
+        monkeypatch.setattr(O, "accept_uniform", lambda seed, t, req: u)
+        out = O.verify(P, U, E, W, np.array([0]), tokens, np.array([1]), temperature=1.0)
+        return int(out["accept_len"][0]), int(out["next_token"][0])
+
+    # u just below the threshold: accepted, then the bonus row (argmax + noise)
+    assert run(thr - 1e-9) == (1, 3)
+    # u just above: rejected; the residual sum (~3e-15) is below 1e-12 sum(p),
+    # so the correction is drawn from p and the +100 noise selects token 3
+    assert run(1.0 - 2.0 ** -24) == (0, 3)
+    # a larger gap between p and q at token 3: a real residual, which is zero
+    # at token 3, so the correction is the residual's best entry instead
+    P[0, 0, 3] = -16.0
+    q2 = special.softmax(P[0, 0])
+    res = np.maximum(0.0, q2 - q)
+    assert res.sum() > 1e-12 and res[3] == 0.0
+    assert run(1.0 - 2.0 ** -24) == (0, int(np.argmax(np.where(res > 0, np.log(res), -np.inf))))
+
+
+def test_top2_margin_by_hand():
+    assert O.top2_margin([1.0, 3.5, 2.25, -1.0]) == 1.25
+    assert O.top2_margin([2.0, 2.0, 1.0]) == 0.0
+    assert O.top2_margin([7.0]) == float("inf")
+    # the exemption rule's input from a greedy proposal: with no Markov bias
+    # each position's margin is the gap between its two largest base logits
+    U = np.zeros((1, 2, 5))
+    U[0, 0] = [0.0, 5.0, 4.9995, 1.0, -2.0]       # margin 5e-4: below 1e-3, exempt
+    U[0, 1] = [4.998, 0.0, 5.0, 3.0, 1.0]         # margin 2e-3: checked
+    out = O.propose(U, np.zeros((5, 2)), np.zeros((5, 2)), np.ones((1, 2)), np.array([0]))
+    assert out["tokens"][0].tolist() == [1, 2]
+    assert abs(out["margin"][0, 0] - 5e-4) < 1e-12
+    assert abs(out["margin"][0, 1] - 2e-3) < 1e-12
+
+
 # -------------------------------------------------------------------- overlap
 
 def test_overlap_identity_and_bounds():
