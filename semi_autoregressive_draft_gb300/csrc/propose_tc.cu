@@ -570,6 +570,375 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   }
 }
 
+// ----------------------------------------------------------------------------
+// Pair engine (an even number of M-tiles, e.g. R = 256): the two CTAs of a
+// cluster are M-tiles 2i and 2i+1 of one vocabulary range, on two SMs.  Each
+// CTA holds its own M-tile's A (gathered E rows) and U boxes as above, but
+// only HALF of every W tile: vocabulary rows [t*128, t*128+64) in the first
+// CTA of the pair, [t*128+64, t*128+128) in the second.  One thread of the
+// first CTA issues tcgen05.mma.cta_group::2 with M = 256, N = 128: the
+// tensor cores read A's rows 0..127 and B's first 64 rows from the first
+// CTA's shared memory, A's rows 128..255 and B's last 64 rows from the
+// second's, and write each CTA's 128 accumulator rows into its own TMEM.  So
+// each SM takes in 32 KB of W per tile instead of 64 KB, and every W byte
+// crosses L2 once per pair.  No load is multicast.
+//
+// Barriers (per CTA; the first CTA's copies of aready, accempty and bfull
+// collect both CTAs' arrivals):
+//   bfull[s]    2 arrivals (each CTA's W producer: arrive.expect_tx of its own
+//               bytes on the FIRST CTA's barrier) + the bytes of both halves,
+//               whose TMA loads complete there (cta_group::2 form);
+//   bempty[s]   1 arrival: the MMA thread's commit, issued to both CTAs'
+//               barriers (two plain commits);
+//   accfull[b]  1 arrival: commit to both CTAs after a tile's MMAs;
+//   accempty[b] 16 arrivals (8 epilogue warps of each CTA) on the first CTA's;
+//   aready      16 arrivals (A gathered in both CTAs) on the first CTA's;
+//   ufull/uempty per CTA, as in the single-CTA kernel.
+// Every barrier still has one consumer role that waits on each of its phases
+// in order.  Waits that see the peer's arrivals acquire at cluster scope.
+constexpr int kPCPS = 4;                 // W half-boxes (K-chunks) per ring stage: a whole tile
+constexpr int kPNB = 2;                  // W ring stages
+constexpr int kHalfBox = kBox / 2;       // [64 vocab x 64 K] bf16
+constexpr uint32_t kIdescPair = tc::idesc_bf16_f32(2 * kTileM, kTileN);
+constexpr int kPOffA = 0;
+constexpr int kPOffB = kPOffA + kMaxKC * kBox;                // 64 KB of A
+constexpr int kPOffU = kPOffB + kPNB * kPCPS * kHalfBox;      // + 64 KB of W halves
+constexpr int kPOffBar = kPOffU + 2 * kNU * kBox;             // + 96 KB of U
+constexpr int kPNumBars = 2 * kPNB + 4 * kNU + 2 * kNAcc + 2;
+constexpr int kPSmemBytes = kPOffBar + kPNumBars * 8 + 64 + 1024;
+static_assert(kPSmemBytes <= 232448, "shared memory budget of one CTA");
+static_assert(kPOffB % 1024 == 0 && kPOffU % 1024 == 0 && kHalfBox % 1024 == 0,
+              "swizzled boxes need aligned bases");
+
+// EW epilogue warps per CTA: 8 (thread = one row, 64 columns of each tile)
+// or 16 (32 columns each; the role warps hand registers to the epilogue with
+// setmaxnreg).  Column group cq = (warp - 4) / 4 of a tile, lane quarter
+// warp % 4.
+template <int EW>
+__global__ void __launch_bounds__(128 + 32 * EW, 1)
+    propose_tc_pair_kernel(const __grid_constant__ CUtensorMap tmW,
+                           const __grid_constant__ CUtensorMap tmU, const TcParams p) {
+  constexpr int kGroups = EW / 4;             // column groups per tile
+  constexpr int kGCols = kTileN / kGroups;    // columns per epilogue warp and tile
+  constexpr int kGPerHalf = kGroups / 2;      // column groups per U box (half tile)
+  constexpr int kRowsPerWarp = kTileM / EW;   // A rows each epilogue warp gathers
+  static_assert(EW == 8 || EW == 16, "8 or 16 epilogue warps");
+  extern __shared__ unsigned char smem_raw[];
+  const uint32_t raw = tc::smem_u32(smem_raw);
+  // the same offset in both CTAs (same kernel, same static shared memory), so
+  // the MMA's descriptors address the peer's operands too
+  unsigned char* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
+  unsigned char* sA = smem + kPOffA;
+  unsigned char* sB = smem + kPOffB;
+  unsigned char* sU = smem + kPOffU;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kPOffBar);
+  Bars b;
+  b.bfull = bars;
+  b.bempty = b.bfull + kPNB;
+  b.ufull = b.bempty + kPNB;
+  b.uempty = b.ufull + 2 * kNU;
+  b.accfull = b.uempty + 2 * kNU;
+  b.accempty = b.accfull + kNAcc;
+  b.aready = b.accempty + kNAcc;
+  b.mmadone = b.aready + 1;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + kPNumBars);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + kPNumBars) + 1;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int KC = p.rank / kKChunk;
+  const int j = p.j;
+  const uint32_t crank = tc::cluster_ctarank();      // 0: issues the MMAs
+  const int cid = (int)(blockIdx.x >> 1);
+  const int mt = 2 * (cid / p.n_vr) + (int)crank;
+  const int vr = cid % p.n_vr;
+  const int r0 = mt * kTileM;
+  const int t0 = (int)(((long long)vr * p.ntiles) / p.n_vr);
+  const int t1 = (int)(((long long)(vr + 1) * p.ntiles) / p.n_vr);
+  const int nt = t1 - t0;
+
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  if (tid == 0) {
+    for (int i = 0; i < kPNB; ++i) {
+      tc::mbar_init(&b.bfull[i], 2);
+      tc::mbar_init(&b.bempty[i], 1);
+    }
+    for (int i = 0; i < 2 * kNU; ++i) {
+      tc::mbar_init(&b.ufull[i], 1);
+      tc::mbar_init(&b.uempty[i], 4 * kGPerHalf);   // the warps that read a half
+    }
+    for (int i = 0; i < kNAcc; ++i) {
+      tc::mbar_init(&b.accfull[i], 1);
+      tc::mbar_init(&b.accempty[i], 2 * EW);
+    }
+    tc::mbar_init(b.aready, 2 * EW);
+    tc::mbar_init(b.mmadone, 1);
+    *abort_flag = 0;
+    tc::mbar_fence_init();
+    tc::fence_proxy_async_smem();
+    tc::prefetch_tensormap(&tmW);
+    tc::prefetch_tensormap(&tmU);
+  }
+  if (warp == 1) {
+    __syncwarp();
+    tc::tmem_alloc_pair(tmem_holder, kTmemCols);   // both CTAs, the same columns
+    tc::tmem_relinquish_pair();
+    tc::tc_fence_before();
+  }
+  __syncthreads();
+  // the peer's copies, arrivals and commits may only target initialised barriers
+  tc::cluster_sync();
+  tc::tc_fence_after();
+  const uint32_t tmem_base = *tmem_holder;
+  // cluster addresses of the first CTA's collecting barriers
+  const uint32_t bfull0 = tc::mapa(tc::smem_u32(b.bfull), 0);
+  const uint32_t accempty0 = tc::mapa(tc::smem_u32(b.accempty), 0);
+  const uint32_t aready0 = tc::mapa(tc::smem_u32(b.aready), 0);
+  if (warp < 4) {
+  // 16 epilogue warps: the role warpgroup (warps 0-3) gives registers to the
+  // four epilogue warpgroups (within the 640 x 96 the CTA was launched with:
+  // 128 x 56 + 512 x 104 <= 640 x 96)
+  if constexpr (EW == 16) asm volatile("setmaxnreg.dec.sync.aligned.u32 56;" ::: "memory");
+  if (warp == 0) {
+    // ------------------------------------- W producer: this CTA's half rows
+    if (lane == 0) {
+      const uint64_t pol = policy_evict_last();
+      uint32_t it = 0;
+      for (int t = t0; t < t1 && !*abort_flag; ++t)
+        for (int k0 = 0; k0 < KC; k0 += kPCPS, ++it) {
+          const int s = it % kPNB;
+          const int nch = KC - k0 < kPCPS ? KC - k0 : kPCPS;
+          if (!wait_bar_cl(&b.bempty[s], ((it / kPNB) & 1) ^ 1, abort_flag, p.status)) break;
+          // relaxed: the bytes, not this thread's writes, complete the phase
+          tc::mbar_arrive_expect_tx_cluster_relaxed(bfull0 + 8u * s, (uint32_t)(nch * kHalfBox));
+          for (int c = 0; c < nch; ++c)
+            tc::tma_load_2d_pair(sB + (s * kPCPS + c) * kHalfBox, &tmW, bfull0 + 8u * s,
+                                 (k0 + c) * kKChunk, t * kTileN + (int)crank * (kTileN / 2), pol);
+        }
+      // Tail: the first CTA waits (bounded) for the last stages' copies of
+      // both halves; each CTA waits for the MMA thread's release of its
+      // stages (commit arrivals land asynchronously).
+      if (crank == 0)
+        for (uint32_t k = (it > kPNB ? it - kPNB : 0); k < it; ++k)
+          drain_bar_cl(&b.bfull[k % kPNB], (k / kPNB) & 1);
+      for (uint32_t k = (it > kPNB ? it - kPNB : 0); k < it; ++k)
+        drain_bar_cl(&b.bempty[k % kPNB], (k / kPNB) & 1);
+    }
+  } else if (warp == 2 || warp == 3) {
+    // ------------------------------------- U producer of column half hs
+    const int hs = warp - 2;
+    if (lane == 0) {
+      const uint64_t pol = policy_evict_first();
+      uint64_t* full = b.ufull + hs * kNU;
+      uint64_t* empty = b.uempty + hs * kNU;
+      unsigned char* ring = sU + hs * kNU * kBox;
+      uint32_t it = 0;
+      for (int t = t0; t < t1 && !*abort_flag; ++t) {
+        const int vx = t * kTileN + hs * kHalf;
+        if (vx >= p.V) break;
+        const int s = it % kNU;
+        if (!wait_bar(&empty[s], ((it / kNU) & 1) ^ 1, abort_flag, p.status)) break;
+        tc::mbar_arrive_expect_tx(&full[s], kBox);
+        tc::tma_load_3d(ring + s * kBox, &tmU, &full[s], vx, j, r0, pol);
+        ++it;
+      }
+      for (uint32_t k = (it > kNU ? it - kNU : 0); k < it; ++k)
+        drain_bar(&full[k % kNU], (k / kNU) & 1);
+      for (uint32_t k = (it > kNU ? it - kNU : 0); k < it; ++k)
+        drain_bar(&empty[k % kNU], (k / kNU) & 1);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------- MMA issuer (first CTA only)
+    if (lane == 0 && crank == 0) {
+      uint32_t bit = 0;
+      const uint32_t bempty_own = tc::smem_u32(b.bempty);
+      const uint32_t bempty_peer = tc::mapa(bempty_own, 1);
+      const uint32_t accfull_own = tc::smem_u32(b.accfull);
+      const uint32_t accfull_peer = tc::mapa(accfull_own, 1);
+      bool ok = wait_bar_cl(b.aready, 0, abort_flag, p.status);
+      tc::tc_fence_after();
+      const uint64_t da0 = tc::sdesc_kmajor_sw128(tc::smem_u32(sA));
+      const uint64_t db0 = tc::sdesc_kmajor_sw128(tc::smem_u32(sB));
+      for (int tt = 0; tt < nt && ok; ++tt) {
+        const int buf = tt % kNAcc;
+        ok = wait_bar_cl(&b.accempty[buf], ((tt / kNAcc) & 1) ^ 1, abort_flag, p.status);
+        if (!ok) break;
+        tc::tc_fence_after();    // both CTAs' TMEM reads of this buffer are done
+        const uint32_t d_tmem = tmem_base + (uint32_t)(buf * kTileN);
+        for (int k0 = 0; k0 < KC; k0 += kPCPS, ++bit) {
+          const int s = bit % kPNB;
+          const int nch = KC - k0 < kPCPS ? KC - k0 : kPCPS;
+          ok = wait_bar_cl(&b.bfull[s], (bit / kPNB) & 1, abort_flag, p.status);
+          if (!ok) break;
+          for (int c = 0; c < nch; ++c) {
+            const int kc = k0 + c;
+            const uint64_t da = da0 + (uint64_t)((kc * kBox) >> 4);
+            const uint64_t db = db0 + (uint64_t)(((s * kPCPS + c) * kHalfBox) >> 4);
+#pragma unroll
+            for (int ks = 0; ks < kKChunk / 16; ++ks)
+              tc::umma_bf16_pair(d_tmem, da + 2 * ks, db + 2 * ks, kIdescPair,
+                                 (kc | ks) != 0 ? 1u : 0u);
+          }
+          tc::umma_commit_pair(bempty_own + 8u * s);     // the stage is free in both CTAs
+          tc::umma_commit_pair(bempty_peer + 8u * s);
+        }
+        if (ok) {
+          tc::umma_commit_pair(accfull_own + 8u * buf);
+          tc::umma_commit_pair(accfull_peer + 8u * buf);
+        }
+      }
+      // all issued MMAs (which read both CTAs' shared memory and write both
+      // TMEMs) complete before the pair passes the final cluster barrier
+      tc::umma_commit_pair(tc::smem_u32(b.mmadone));
+      drain_bar_cl(b.mmadone, 0);
+    }
+  }
+  } else {
+    // ------------------------------------------------------ epilogue
+    if constexpr (EW == 16) asm volatile("setmaxnreg.inc.sync.aligned.u32 104;" ::: "memory");
+    const int e = warp - 4;
+    const int cq = e >> 2;           // column group of each tile
+    const int hs = cq / kGPerHalf;   // U ring (column half) it reads
+    const int q = warp & 3;
+    const int row = q * 32 + lane;
+    const int r = r0 + row;
+    const bool valid = r < p.R;
+    const bool warp_rows = r0 + q * 32 < p.R;
+    const uint32_t rid = valid ? (p.req_id ? p.req_id[r] : (uint32_t)r) : 0u;
+
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+
+    // ---- A operand: rows of E for the tokens of step j-1 (this M-tile) ----
+    // This warp fills rows e, e + EW, ...: lane k < kRowsPerWarp fetches the
+    // token of row e + EW k, then the rows are copied into the 128-byte-
+    // swizzled K-major layout of the UMMA descriptors.
+    {
+      const bool biased = (j > 0) || p.bias_at_first;
+      int my_tok = -1;
+      if (lane < kRowsPerWarp) {
+        const int rr = r0 + e + EW * lane;
+        if (biased && rr < p.R) {
+          int tk = (j == 0) ? p.prev_tok[rr]
+                            : (int)key_index(__ldcg(&p.keys[(size_t)(j - 1) * p.R_max + rr]));
+          if (tk < 0 || tk >= p.V) {
+            set_status(p.status, kErrArg);
+            tk = 0;
+          }
+          my_tok = tk;
+        }
+      }
+      const int cpr = p.rank / 8;
+      uint4 v[kRowsPerWarp];
+#pragma unroll
+      for (int kk = 0; kk < kRowsPerWarp; ++kk) {
+        const int tok = __shfl_sync(0xffffffffu, my_tok, kk);
+        v[kk] = make_uint4(0u, 0u, 0u, 0u);
+        if (tok >= 0 && lane < cpr &&
+            TC_CHECK((size_t)tok * p.rank + lane * 8 + 8 <= (size_t)p.V * p.rank, 2))
+          v[kk] = __ldcg(reinterpret_cast<const uint4*>(p.E + (size_t)tok * p.rank + lane * 8));
+      }
+      if (lane < cpr) {
+        const int kc = lane >> 3, cc = lane & 7;
+#pragma unroll
+        for (int kk = 0; kk < kRowsPerWarp; ++kk) {
+          const int ir = e + EW * kk;
+          const size_t off = (size_t)kc * kBox + ir * 128 + ((cc ^ (ir & 7)) << 4);
+          if (TC_CHECK(off + 16 <= (size_t)kMaxKC * kBox, 1))
+            *reinterpret_cast<uint4*>(sA + off) = v[kk];
+        }
+      }
+      tc::fence_proxy_async_smem();      // visible to the tensor cores of either SM
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive_cluster(aready0);
+    }
+
+    // ---- tiles ----
+    RowState st{-INFINITY, 0.f, -INFINITY, 0u};
+    uint64_t* full = b.ufull + hs * kNU;
+    uint64_t* empty = b.uempty + hs * kNU;
+    const unsigned char* ring = sU + hs * kNU * kBox;
+    uint32_t uit = 0;
+    for (int tt = 0; tt < nt; ++tt) {
+      if (warp_aborted(abort_flag)) break;
+      const int t = t0 + tt;
+      const int buf = tt % kNAcc;
+      if (!warp_wait_cl(&b.accfull[buf], (tt / kNAcc) & 1, abort_flag, p.status)) break;
+      tc::tc_fence_after();
+      const int vx = t * kTileN + hs * kHalf;        // first column of this warp's U box
+      if (vx < p.V) {
+        const int s = uit % kNU;
+        if (!warp_wait(&full[s], (uit / kNU) & 1, abort_flag, p.status)) break;
+        ++uit;
+        // this warp's kGCols columns: 16-byte chunks c0 .. c0 + kGCols/8 - 1
+        // of its row of the box (128-byte swizzle: chunk c at c ^ (row & 7))
+        constexpr int kChunks = kGCols / 8;
+        const int c0 = (cq % kGPerHalf) * kChunks;
+        uint4 u[kChunks];
+        const unsigned char* urow = ring + s * kBox + row * 128;
+        if (warp_rows) {
+#pragma unroll
+          for (int c = 0; c < kChunks; ++c)
+            u[c] = *reinterpret_cast<const uint4*>(urow + (((c0 + c) ^ (row & 7)) << 4));
+        }
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(&empty[s]);
+        __syncwarp();
+        if (warp_rows) {
+#pragma unroll
+          for (int c = 0; c < kGCols / 32; ++c) {
+            const int v0 = vx + (c0 / 4 + c) * 32;
+            if (v0 >= p.V) break;
+            uint32_t acc[32];
+            tc::tmem_ld_32x32b_x32_wait(tmem_base + ((uint32_t)(q * 32) << 16) +
+                                            (uint32_t)(buf * kTileN + (v0 - t * kTileN)),
+                                        acc);
+            fold32(st, acc, u + 4 * c, v0, p, rid);
+          }
+        }
+      }
+      // The TMEM reads are complete (tcgen05.wait::ld) and ordered by the
+      // tcgen05 fence; the arrival publishes no memory writes, so it is
+      // relaxed (a release at cluster scope costs a fence per tile and warp).
+      tc::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive_cluster_relaxed(accempty0 + 8u * buf);
+    }
+
+    // ---- merge the column groups of each row, publish step j's partial ----
+    // The A region is free once this CTA's last accumulator wait has passed:
+    // that commit followed every MMA that reads A.
+    RowState* xch = reinterpret_cast<RowState*>(sA);   // [kGroups - 1][kTileM]
+    if (cq > 0) xch[(cq - 1) * kTileM + row] = st;
+    asm volatile("bar.sync 1, %0;" ::"n"(32 * EW) : "memory");   // the epilogue warps
+    if (cq == 0) {
+#pragma unroll
+      for (int k = 0; k < kGroups - 1; ++k) {
+        const RowState o = xch[k * kTileM + row];
+        const Lse2 l = lse2_merge(Lse2{st.m2, st.s}, Lse2{o.m2, o.s});
+        st.m2 = l.m;
+        st.s = l.s;
+        if (o.best_z > st.best_z || (o.best_z == st.best_z && o.best_v < st.best_v)) {
+          st.best_z = o.best_z;
+          st.best_v = o.best_v;
+        }
+      }
+      if (valid && TC_CHECK(vr < p.n_part && r < p.R_max, 5)) {
+        atomicMax(&p.keys[(size_t)j * p.R_max + r], make_key(st.best_z, st.best_v));
+        p.parts[((size_t)j * p.n_part + vr) * p.R_max + r] = make_float2(st.m2, st.s);
+      }
+    }
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  // neither CTA leaves while the pair's MMAs, copies or arrivals may still
+  // address its shared memory or TMEM
+  tc::cluster_sync();
+  if (warp == 1) {
+    __syncwarp();
+    tc::tc_fence_after();
+    tc::tmem_dealloc_pair(tmem_base, kTmemCols);
+  }
+}
+
 }  // namespace
 
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
@@ -606,8 +975,9 @@ int tc_supported(const Ctx& ctx, char* why, size_t why_len) {
   }
   int smem = 0;
   cudaDeviceGetAttribute(&smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, ctx.cfg.device);
-  if (smem < kSmemBytes) {
-    snprintf(why, why_len, "device lacks %d bytes of shared memory per block", kSmemBytes);
+  const int need = kSmemBytes > kPSmemBytes ? kSmemBytes : kPSmemBytes;
+  if (smem < need) {
+    snprintf(why, why_len, "device lacks %d bytes of shared memory per block", need);
     return 0;
   }
   return 1;
@@ -624,14 +994,23 @@ int tc_vranges(const Ctx& ctx, int R) {
   return n;
 }
 
+// An even number of M-tiles runs on CTA pairs (propose_tc_pair_kernel).
+constexpr int kPairEpiWarps = 16;
+static bool use_pair(int R) {
+  const int MT = (R + kTileM - 1) / kTileM;
+  return MT >= 2 && MT % 2 == 0;
+}
+
 cudaError_t launch_propose_tc(const Ctx& ctx, const ProposeArgs& a, cudaStream_t s) {
   PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
   if (!encode) return cudaErrorNotSupported;
+  const bool pair = use_pair(a.R);
   CUtensorMap tmW, tmU;
   {
     const cuuint64_t dims[2] = {(cuuint64_t)a.rank, (cuuint64_t)a.V};
     const cuuint64_t strides[1] = {(cuuint64_t)a.rank * 2};
-    const cuuint32_t box[2] = {kKChunk, (cuuint32_t)kTileN};
+    // a CTA of a pair loads half of each tile's vocabulary rows
+    const cuuint32_t box[2] = {kKChunk, (cuuint32_t)(pair ? kTileN / 2 : kTileN)};
     const cuuint32_t estr[2] = {1, 1};
     if (encode(&tmW, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(a.W), dims, strides,
                box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -656,6 +1035,9 @@ cudaError_t launch_propose_tc(const Ctx& ctx, const ProposeArgs& a, cudaStream_t
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(propose_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              kSmemBytes);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(propose_tc_pair_kernel<kPairEpiWarps>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, kPSmemBytes);
   if (e != cudaSuccess) return e;
 
   TcParams p{};
@@ -685,20 +1067,27 @@ cudaError_t launch_propose_tc(const Ctx& ctx, const ProposeArgs& a, cudaStream_t
   // Steps after the first are launched with a programmatic dependency on the
   // previous step (see griddepcontrol in the kernel); the first follows the
   // memset of the keys in plain stream order.
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  // Pairs: clusters of two CTAs, block 2 c + m = M-tile 2 (c / n_vr) + m of
+  // vocabulary range c % n_vr.
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = pair ? 2 : 1;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(kTcThreads);
-  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.blockDim = dim3(pair ? 128 + 32 * kPairEpiWarps : kTcThreads);
+  cfg.dynamicSmemBytes = pair ? kPSmemBytes : kSmemBytes;
   cfg.stream = s;
-  cfg.attrs = attr;
+  cfg.attrs = pair ? attr : attr + 1;
   for (int j = 0; j < a.gamma; ++j) {
     p.j = j;
-    cfg.numAttrs = j > 0 ? 1 : 0;
-    e = p.dup ? cudaLaunchKernelEx(&cfg, propose_tc_kernel<true>, tmW, tmU, p)
-              : cudaLaunchKernelEx(&cfg, propose_tc_kernel<false>, tmW, tmU, p);
+    cfg.numAttrs = (pair ? 1 : 0) + (j > 0 ? 1 : 0);
+    e = pair    ? cudaLaunchKernelEx(&cfg, propose_tc_pair_kernel<kPairEpiWarps>, tmW, tmU, p)
+        : p.dup ? cudaLaunchKernelEx(&cfg, propose_tc_kernel<true>, tmW, tmU, p)
+                : cudaLaunchKernelEx(&cfg, propose_tc_kernel<false>, tmW, tmU, p);
     if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     count_launch(ctx);

@@ -28,6 +28,31 @@ __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, volatil
   return false;
 }
 
+// The same with acquire at cluster scope, for barriers that the peer CTA of
+// a pair arrives on (or whose completions make the peer's writes visible).
+__device__ __forceinline__ bool wait_bar_cl(uint64_t* bar, uint32_t parity,
+                                            volatile int* abort_flag, int* status) {
+  for (uint32_t i = 0; i < kSpinLimit; ++i) {
+    if (tc::mbar_try_wait_cluster(bar, parity)) return true;
+    if ((i & 255u) == 255u && *abort_flag) return false;
+  }
+  set_status(status, kErrTimeout);
+  *abort_flag = 1;
+  return false;
+}
+__device__ __forceinline__ bool warp_wait_cl(uint64_t* bar, uint32_t parity,
+                                             volatile int* abort_flag, int* status) {
+  int ok = 0;
+  if ((threadIdx.x & 31) == 0) ok = wait_bar_cl(bar, parity, abort_flag, status) ? 1 : 0;
+  ok = __shfl_sync(0xffffffffu, ok, 0);
+  __syncwarp();
+  return ok != 0;
+}
+__device__ __forceinline__ void drain_bar_cl(uint64_t* bar, uint32_t parity) {
+  for (uint32_t i = 0; i < (1u << 20); ++i)
+    if (tc::mbar_try_wait_cluster(bar, parity)) return;
+}
+
 // Bounded wait that ignores the abort flag: used to drain copies in flight
 // before the CTA exits.
 __device__ __forceinline__ void drain_bar(uint64_t* bar, uint32_t parity) {

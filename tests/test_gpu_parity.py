@@ -129,10 +129,14 @@ def test_mma_and_simt_engines_agree(dsd):
 
 
 @pytest.mark.parametrize("R,V,rank,temperature", [
-    (129, 2568, 256, 0.0),     # second M-tile with one request, ragged vocabulary tail
-    (256, 1032, 256, 1.0),     # two full M-tiles, sampled
-    (256, 2600, 256, 0.0),     # two M-tiles, last tile ends in a ragged second U box
-    (300, 1544, 256, 0.0),     # a second launch per step for requests 256..299
+    (129, 2568, 256, 0.0),     # CTA pair, second M-tile with one request, ragged vocabulary tail
+    (256, 1032, 256, 1.0),     # CTA pair, two full M-tiles, sampled
+    (256, 2600, 256, 0.0),     # CTA pair, last tile ends in a ragged second U box
+    (200, 4104, 256, 1.0),     # CTA pair, partial second M-tile, sampled
+    (140, 3080, 64, 0.0),      # CTA pair at rank 64 (one K-chunk per half-box stage)
+    (450, 2568, 128, 1.0),     # four M-tiles: two CTA pairs per range, rank 128
+    (512, 1032, 256, 0.0),     # four full M-tiles
+    (300, 1544, 256, 0.0),     # three M-tiles: single CTAs (an odd count)
     (40, 3080, 128, 0.0),      # rank 128
     (16, 4104, 64, 1.0),       # rank 64
     (64, 2600, 256, 1.0),      # the largest batch whose rows 64..127 repeat rows 0..63
