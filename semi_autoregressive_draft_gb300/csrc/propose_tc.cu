@@ -597,14 +597,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 // Every barrier still has one consumer role that waits on each of its phases
 // in order.  Waits that see the peer's arrivals acquire at cluster scope.
 constexpr int kPCPS = 4;                 // W half-boxes (K-chunks) per ring stage: a whole tile
-constexpr int kPNB = 2;                  // W ring stages
+constexpr int kPNB = 3;                  // W ring stages
+constexpr int kPNU = 2;                  // U ring slots per column half
 constexpr int kHalfBox = kBox / 2;       // [64 vocab x 64 K] bf16
 constexpr uint32_t kIdescPair = tc::idesc_bf16_f32(2 * kTileM, kTileN);
 constexpr int kPOffA = 0;
 constexpr int kPOffB = kPOffA + kMaxKC * kBox;                // 64 KB of A
-constexpr int kPOffU = kPOffB + kPNB * kPCPS * kHalfBox;      // + 64 KB of W halves
-constexpr int kPOffBar = kPOffU + 2 * kNU * kBox;             // + 96 KB of U
-constexpr int kPNumBars = 2 * kPNB + 4 * kNU + 2 * kNAcc + 2;
+constexpr int kPOffU = kPOffB + kPNB * kPCPS * kHalfBox;      // + 96 KB of W halves
+constexpr int kPOffBar = kPOffU + 2 * kPNU * kBox;            // + 64 KB of U
+constexpr int kPNumBars = 2 * kPNB + 4 * kPNU + 2 * kNAcc + 2;
 constexpr int kPSmemBytes = kPOffBar + kPNumBars * 8 + 64 + 1024;
 static_assert(kPSmemBytes <= 232448, "shared memory budget of one CTA");
 static_assert(kPOffB % 1024 == 0 && kPOffU % 1024 == 0 && kHalfBox % 1024 == 0,
@@ -636,8 +637,8 @@ __global__ void __launch_bounds__(128 + 32 * EW, 1)
   b.bfull = bars;
   b.bempty = b.bfull + kPNB;
   b.ufull = b.bempty + kPNB;
-  b.uempty = b.ufull + 2 * kNU;
-  b.accfull = b.uempty + 2 * kNU;
+  b.uempty = b.ufull + 2 * kPNU;
+  b.accfull = b.uempty + 2 * kPNU;
   b.accempty = b.accfull + kNAcc;
   b.aready = b.accempty + kNAcc;
   b.mmadone = b.aready + 1;
@@ -662,7 +663,7 @@ __global__ void __launch_bounds__(128 + 32 * EW, 1)
       tc::mbar_init(&b.bfull[i], 2);
       tc::mbar_init(&b.bempty[i], 1);
     }
-    for (int i = 0; i < 2 * kNU; ++i) {
+    for (int i = 0; i < 2 * kPNU; ++i) {
       tc::mbar_init(&b.ufull[i], 1);
       tc::mbar_init(&b.uempty[i], 4 * kGPerHalf);   // the warps that read a half
     }
@@ -728,23 +729,23 @@ __global__ void __launch_bounds__(128 + 32 * EW, 1)
     const int hs = warp - 2;
     if (lane == 0) {
       const uint64_t pol = policy_evict_first();
-      uint64_t* full = b.ufull + hs * kNU;
-      uint64_t* empty = b.uempty + hs * kNU;
-      unsigned char* ring = sU + hs * kNU * kBox;
+      uint64_t* full = b.ufull + hs * kPNU;
+      uint64_t* empty = b.uempty + hs * kPNU;
+      unsigned char* ring = sU + hs * kPNU * kBox;
       uint32_t it = 0;
       for (int t = t0; t < t1 && !*abort_flag; ++t) {
         const int vx = t * kTileN + hs * kHalf;
         if (vx >= p.V) break;
-        const int s = it % kNU;
-        if (!wait_bar(&empty[s], ((it / kNU) & 1) ^ 1, abort_flag, p.status)) break;
+        const int s = it % kPNU;
+        if (!wait_bar(&empty[s], ((it / kPNU) & 1) ^ 1, abort_flag, p.status)) break;
         tc::mbar_arrive_expect_tx(&full[s], kBox);
         tc::tma_load_3d(ring + s * kBox, &tmU, &full[s], vx, j, r0, pol);
         ++it;
       }
-      for (uint32_t k = (it > kNU ? it - kNU : 0); k < it; ++k)
-        drain_bar(&full[k % kNU], (k / kNU) & 1);
-      for (uint32_t k = (it > kNU ? it - kNU : 0); k < it; ++k)
-        drain_bar(&empty[k % kNU], (k / kNU) & 1);
+      for (uint32_t k = (it > kPNU ? it - kPNU : 0); k < it; ++k)
+        drain_bar(&full[k % kPNU], (k / kPNU) & 1);
+      for (uint32_t k = (it > kPNU ? it - kPNU : 0); k < it; ++k)
+        drain_bar(&empty[k % kPNU], (k / kPNU) & 1);
     }
   } else if (warp == 1) {
     // ------------------------------------- MMA issuer (first CTA only)
@@ -853,9 +854,9 @@ __global__ void __launch_bounds__(128 + 32 * EW, 1)
 
     // ---- tiles ----
     RowState st{-INFINITY, 0.f, -INFINITY, 0u};
-    uint64_t* full = b.ufull + hs * kNU;
-    uint64_t* empty = b.uempty + hs * kNU;
-    const unsigned char* ring = sU + hs * kNU * kBox;
+    uint64_t* full = b.ufull + hs * kPNU;
+    uint64_t* empty = b.uempty + hs * kPNU;
+    const unsigned char* ring = sU + hs * kPNU * kBox;
     uint32_t uit = 0;
     for (int tt = 0; tt < nt; ++tt) {
       if (warp_aborted(abort_flag)) break;
@@ -865,8 +866,8 @@ __global__ void __launch_bounds__(128 + 32 * EW, 1)
       tc::tc_fence_after();
       const int vx = t * kTileN + hs * kHalf;        // first column of this warp's U box
       if (vx < p.V) {
-        const int s = uit % kNU;
-        if (!warp_wait(&full[s], (uit / kNU) & 1, abort_flag, p.status)) break;
+        const int s = uit % kPNU;
+        if (!warp_wait(&full[s], (uit / kPNU) & 1, abort_flag, p.status)) break;
         ++uit;
         // this warp's kGCols columns: 16-byte chunks c0 .. c0 + kGCols/8 - 1
         // of its row of the box (128-byte swizzle: chunk c at c ^ (row & 7))
