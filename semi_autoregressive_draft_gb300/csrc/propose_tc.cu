@@ -940,6 +940,442 @@ __global__ void __launch_bounds__(128 + 32 * EW, 1)
   }
 }
 
+// ----------------------------------------------------------------------------
+// Residual pass of sampled verification on the tensor cores ("DeepSpec 训练
+// 全流程详解" 4.4: after the first rejection at position k the next token is
+// drawn from norm(max(0, p_k - q_k))).  For each request in the rejection
+// list, q_k = softmax((U[r,k] + W E[x_{k-1}]) / T) is recomputed from its
+// definition with the stored lse_q, p_k = softmax(P[r,k] / T) with the row
+// pass's lse of P, and the draw is a Gumbel-max (Philox stream 2) over
+// log(p - q) where p > q; the draw from p itself (the empty-residual
+// fallback) and the two sums sum(p - q)+ and sum(p) are kept beside it.
+//
+// CTA = 64 rows of the rejection list (the list order is the row order) x a
+// vocabulary range, 12 warps as in the propose kernel with 64 rows:
+// A (the gathered E rows of x_{k-1}) holds rows 0..63 twice, so lane
+// quarters 2 and 3 fold the second 32-column chunk of each 64-column half.
+// The U and P rows of the listed (request, position) pairs are scattered in
+// memory, so warps 2 and 3 fetch them as 1-D bulk copies (one per row and
+// half tile, 16-byte aligned, a multiple of 16 bytes) into padded 144-byte
+// row slots of a ring (the padding puts the rows read by a quarter warp in
+// distinct banks).  W tiles and the MMA are as in the propose kernel.
+// Outputs, as the CUDA-core residual pass: atomicMax of the residual key and
+// of the fallback key per request, atomicAdd of the two sums.
+constexpr int kRRows = 64;                       // list rows per CTA
+constexpr int kRStride = 144;                    // bytes per row slot (128 + 16 of padding)
+constexpr int kRArr = kRRows * kRStride;         // one array (U or P) of one slot
+constexpr int kRSlot = 2 * kRArr;                // U rows, then P rows
+constexpr int kRNU = 2;                          // slots per column half
+constexpr int kROffA = 0;
+constexpr int kROffB = kROffA + kMaxKC * kBox;               // 64 KB of A
+constexpr int kROffU = kROffB + kNB * kCPS * kBox;           // + 64 KB of W
+constexpr int kROffBar = kROffU + 2 * kRNU * kRSlot;         // + 72 KB of U and P rows
+constexpr int kRNumBars = 2 * kNB + 4 * kRNU + 2 * kNAcc + 2;
+constexpr int kRSmemBytes = kROffBar + kRNumBars * 8 + 64 + 1024;
+static_assert(kRSmemBytes <= 232448, "shared memory budget of one CTA");
+static_assert(kROffB % 1024 == 0 && kROffU % 1024 == 0 && kRStride % 16 == 0, "alignment");
+
+struct ResParams {
+  const __nv_bfloat16* E;
+  const __nv_bfloat16* U;
+  const __nv_bfloat16* P;
+  const int32_t* prev_tok;
+  const int32_t* tokens;
+  const uint32_t* req_id;
+  const float* lse_q;
+  const int* rej_list;
+  const int* rej_k;
+  const float* rej_lseP;
+  const unsigned int* n_rej;
+  unsigned long long* res_keys;   // [2][R_max]: residual key, fallback key
+  float* res_sums;                // [2][R_max]: sum (p - q)+, sum p
+  int* status;
+  int R, R_max, V, rank, gamma, bias_at_first, n_vr, ntiles;
+  float inv_T;
+  uint32_t k0, k1;
+};
+
+struct ResState {
+  unsigned long long best, best2;   // residual key, fallback key
+  float fsum, fsum2;
+};
+
+// WC consecutive columns of one row (a multiple of 4): x = acc + U, the
+// residual terms and the two Gumbel-max keys (one Philox block per four
+// columns).  uw / pw: the row's U and P values, two bf16 per word.
+template <int WC>
+__device__ __forceinline__ void fold_res(ResState& st, const uint32_t (&acc)[WC],
+                                         const uint32_t* uw, const uint32_t* pw, int v0,
+                                         const ResParams& p, uint32_t rid, uint32_t pos, float lq,
+                                         float lp) {
+#pragma unroll
+  for (int g = 0; g < WC / 4; ++g) {
+    const uint32_t v = (uint32_t)(v0 + 4 * g);
+    if (v >= (uint32_t)p.V) break;   // V % 8 == 0: groups of four are all in or all out
+    float xs[4], ps[4];
+    add_bf16x2(uw[2 * g], acc[4 * g], acc[4 * g + 1], xs[0], xs[1]);
+    add_bf16x2(uw[2 * g + 1], acc[4 * g + 2], acc[4 * g + 3], xs[2], xs[3]);
+    ps[0] = bf16lo(pw[2 * g]);
+    ps[1] = bf16hi(pw[2 * g]);
+    ps[2] = bf16lo(pw[2 * g + 1]);
+    ps[3] = bf16hi(pw[2 * g + 1]);
+    const Philox4 ph = philox4x32_10(v >> 2, pos, rid, 2u, p.k0, p.k1);
+    const uint32_t words[4] = {ph.x, ph.y, ph.z, ph.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float ql = xs[e] * p.inv_T - lq;
+      const float pl = ps[e] * p.inv_T - lp;
+      const float gg = gumbel_from_word(words[e]);
+      if (pl > ql) {
+        // log(p - q) = pl + log(1 - exp(ql - pl)), kept accurate when p ~ q
+        const float lr = pl + log1pf(-__expf(ql - pl));
+        const unsigned long long key = make_key(lr + gg, v + e);
+        st.best = key > st.best ? key : st.best;
+        st.fsum += __expf(pl) - __expf(ql);
+      }
+      const unsigned long long key2 = make_key(pl + gg, v + e);
+      st.best2 = key2 > st.best2 ? key2 : st.best2;
+      st.fsum2 += __expf(pl);
+    }
+  }
+}
+
+// One tile of one thread of the residual epilogue: its WC columns starting at
+// column `col` of the tile (TMEM lane = its row of A).
+template <int WC>
+__device__ __forceinline__ void res_tile(ResState& st, uint32_t tmem_addr,
+                                         const unsigned char* urow, const unsigned char* prow,
+                                         bool active, int v0, const ResParams& p, uint32_t rid,
+                                         uint32_t pos, float lq, float lp) {
+  uint32_t uw[WC / 2], pw[WC / 2];
+  if (active) {
+    static_assert(WC == 16 || WC == 32, "a copy folds 16 or 32 columns of a half");
+    {
+#pragma unroll
+      for (int c = 0; c < WC / 8; ++c) {
+        const uint4 a = *reinterpret_cast<const uint4*>(urow + 16 * c);
+        const uint4 b = *reinterpret_cast<const uint4*>(prow + 16 * c);
+        uw[4 * c] = a.x; uw[4 * c + 1] = a.y; uw[4 * c + 2] = a.z; uw[4 * c + 3] = a.w;
+        pw[4 * c] = b.x; pw[4 * c + 1] = b.y; pw[4 * c + 2] = b.z; pw[4 * c + 3] = b.w;
+      }
+    }
+  }
+  // `active` differs between lanes: the warp reconverges before the
+  // warp-wide (.sync.aligned) tensor-memory load
+  __syncwarp();
+  uint32_t acc[WC];
+  tc::tmem_ld_wait<WC>(tmem_addr, acc);
+  if (active) fold_res<WC>(st, acc, uw, pw, v0, p, rid, pos, lq, lp);
+}
+
+__global__ void __launch_bounds__(kTcThreads, 1)
+    residual_tc_kernel(const __grid_constant__ CUtensorMap tmW, const ResParams p) {
+  extern __shared__ unsigned char smem_raw[];
+  __shared__ int s_req[kRRows];
+  __shared__ int s_pos[kRRows];
+  __shared__ int s_tok[kRRows];     // x_{k-1}, or -1 without a bias
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int mt = blockIdx.x / p.n_vr;
+  const int vr = blockIdx.x - mt * p.n_vr;
+  const int n_rej = min((int)*p.n_rej, p.R);
+  const int li0 = mt * kRRows;
+  if (li0 >= n_rej) return;          // the whole CTA, before any barrier or TMEM
+  const int nvalid = min(kRRows, n_rej - li0);
+
+  const uint32_t raw = tc::smem_u32(smem_raw);
+  unsigned char* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
+  unsigned char* sA = smem + kROffA;
+  unsigned char* sB = smem + kROffB;
+  unsigned char* sU = smem + kROffU;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kROffBar);
+  Bars b;
+  b.bfull = bars;
+  b.bempty = b.bfull + kNB;
+  b.ufull = b.bempty + kNB;
+  b.uempty = b.ufull + 2 * kRNU;
+  b.accfull = b.uempty + 2 * kRNU;
+  b.accempty = b.accfull + kNAcc;
+  b.aready = b.accempty + kNAcc;
+  b.mmadone = b.aready + 1;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + kRNumBars);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + kRNumBars) + 1;
+
+  const int KC = p.rank / kKChunk;
+  const int t0 = (int)(((long long)vr * p.ntiles) / p.n_vr);
+  const int t1 = (int)(((long long)(vr + 1) * p.ntiles) / p.n_vr);
+  const int nt = t1 - t0;
+
+  if (tid < kRRows) {
+    int req = 0, pos = 0, tok = -1;
+    if (tid < nvalid) {
+      req = p.rej_list[li0 + tid];
+      if (req < 0 || req >= p.R) {
+        set_status(p.status, kErrArg);
+        req = 0;
+      }
+      pos = p.rej_k[req];
+      if (pos < 0 || pos >= p.gamma) {
+        set_status(p.status, kErrArg);
+        pos = 0;
+      }
+      if (pos > 0 || p.bias_at_first) {
+        tok = pos == 0 ? p.prev_tok[req] : p.tokens[(size_t)req * p.gamma + pos - 1];
+        if (tok < 0 || tok >= p.V) {
+          set_status(p.status, kErrArg);
+          tok = 0;
+        }
+      }
+    }
+    s_req[tid] = req;
+    s_pos[tid] = pos;
+    s_tok[tid] = tok;
+  }
+  if (tid == 0) {
+    for (int i = 0; i < kNB; ++i) {
+      tc::mbar_init(&b.bfull[i], 1);
+      tc::mbar_init(&b.bempty[i], 1);
+    }
+    for (int i = 0; i < 2 * kRNU; ++i) {
+      tc::mbar_init(&b.ufull[i], 1);
+      tc::mbar_init(&b.uempty[i], 4);
+    }
+    for (int i = 0; i < kNAcc; ++i) {
+      tc::mbar_init(&b.accfull[i], 1);
+      tc::mbar_init(&b.accempty[i], 8);
+    }
+    tc::mbar_init(b.aready, 8);
+    tc::mbar_init(b.mmadone, 1);
+    *abort_flag = 0;
+    tc::mbar_fence_init();
+    tc::fence_proxy_async_smem();
+    tc::prefetch_tensormap(&tmW);
+  }
+  if (warp == 1) {
+    __syncwarp();
+    tc::tmem_alloc(tmem_holder, kTmemCols);
+    tc::tmem_relinquish();
+    tc::tc_fence_before();
+  }
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tmem_base = *tmem_holder;
+
+  if (warp == 0) {
+    // ------------------------------------------------------ W producer
+    if (lane == 0) {
+      const uint64_t pol = policy_evict_last();
+      uint32_t it = 0;
+      for (int t = t0; t < t1 && !*abort_flag; ++t)
+        for (int k0 = 0; k0 < KC; k0 += kCPS, ++it) {
+          const int s = it % kNB;
+          const int nch = KC - k0 < kCPS ? KC - k0 : kCPS;
+          if (!wait_bar(&b.bempty[s], ((it / kNB) & 1) ^ 1, abort_flag, p.status)) break;
+          tc::mbar_arrive_expect_tx(&b.bfull[s], (uint32_t)(nch * kBox));
+          for (int c = 0; c < nch; ++c)
+            tc::tma_load_2d(sB + (s * kCPS + c) * kBox, &tmW, &b.bfull[s], (k0 + c) * kKChunk,
+                            t * kTileN, pol);
+        }
+      for (uint32_t k = (it > kNB ? it - kNB : 0); k < it; ++k)
+        drain_bar(&b.bfull[k % kNB], (k / kNB) & 1);
+      for (uint32_t k = (it > kNB ? it - kNB : 0); k < it; ++k)
+        drain_bar(&b.bempty[k % kNB], (k / kNB) & 1);
+    }
+  } else if (warp == 2 || warp == 3) {
+    // ---------------------- U and P rows of column half hs: bulk copies per row
+    const int hs = warp - 2;
+    const uint64_t pol = policy_evict_first();
+    uint64_t* full = b.ufull + hs * kRNU;
+    uint64_t* empty = b.uempty + hs * kRNU;
+    unsigned char* ring = sU + hs * kRNU * kRSlot;
+    // this lane's rows i = lane and lane + 32: the start of their U and P rows
+    const __nv_bfloat16* usrc[2];
+    const __nv_bfloat16* psrc[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int i = lane + 32 * h;
+      const int req = s_req[i], pos = s_pos[i];
+      usrc[h] = p.U + ((size_t)req * p.gamma + pos) * p.V;
+      psrc[h] = p.P + ((size_t)req * (p.gamma + 1) + pos) * p.V;
+    }
+    uint32_t it = 0;
+    for (int t = t0; t < t1; ++t) {
+      if (warp_aborted(abort_flag)) break;
+      const int vx = t * kTileN + hs * kHalf;
+      if (vx >= p.V) break;
+      const uint32_t bytes = (uint32_t)(min(kHalf, p.V - vx) * 2);   // a multiple of 16 (V % 8 == 0)
+      const int s = it % kRNU;
+      if (!warp_wait(&empty[s], ((it / kRNU) & 1) ^ 1, abort_flag, p.status)) break;
+      if (lane == 0) tc::mbar_arrive_expect_tx(&full[s], (uint32_t)nvalid * 2u * bytes);
+      __syncwarp();
+      unsigned char* slot = ring + s * kRSlot;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int i = lane + 32 * h;
+        if (i < nvalid && TC_CHECK(kRArr + i * kRStride + (int)bytes <= kRSlot, 6)) {
+          tc::bulk_load(slot + i * kRStride, usrc[h] + vx, bytes, &full[s], pol);
+          tc::bulk_load(slot + kRArr + i * kRStride, psrc[h] + vx, bytes, &full[s], pol);
+        }
+      }
+      ++it;
+    }
+    if (lane == 0) {
+      for (uint32_t k = (it > kRNU ? it - kRNU : 0); k < it; ++k)
+        drain_bar(&full[k % kRNU], (k / kRNU) & 1);
+      for (uint32_t k = (it > kRNU ? it - kRNU : 0); k < it; ++k)
+        drain_bar(&empty[k % kRNU], (k / kRNU) & 1);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      uint32_t bit = 0;
+      bool ok = wait_bar(b.aready, 0, abort_flag, p.status);
+      tc::tc_fence_after();
+      const uint64_t da0 = tc::sdesc_kmajor_sw128(tc::smem_u32(sA));
+      const uint64_t db0 = tc::sdesc_kmajor_sw128(tc::smem_u32(sB));
+      for (int tt = 0; tt < nt && ok; ++tt) {
+        const int buf = tt % kNAcc;
+        ok = wait_bar(&b.accempty[buf], ((tt / kNAcc) & 1) ^ 1, abort_flag, p.status);
+        if (!ok) break;
+        tc::tc_fence_after();
+        const uint32_t d_tmem = tmem_base + (uint32_t)(buf * kTileN);
+        for (int k0 = 0; k0 < KC; k0 += kCPS, ++bit) {
+          const int s = bit % kNB;
+          const int nch = KC - k0 < kCPS ? KC - k0 : kCPS;
+          ok = wait_bar(&b.bfull[s], (bit / kNB) & 1, abort_flag, p.status);
+          if (!ok) break;
+          for (int c = 0; c < nch; ++c) {
+            const int kc = k0 + c;
+            const uint64_t da = da0 + (uint64_t)((kc * kBox) >> 4);
+            const uint64_t db = db0 + (uint64_t)(((s * kCPS + c) * kBox) >> 4);
+#pragma unroll
+            for (int ks = 0; ks < kKChunk / 16; ++ks)
+              tc::umma_bf16(d_tmem, da + 2 * ks, db + 2 * ks, kIdesc, (kc | ks) != 0 ? 1u : 0u);
+          }
+          tc::umma_commit(&b.bempty[s]);
+        }
+        if (ok) tc::umma_commit(&b.accfull[buf]);
+      }
+      tc::umma_commit(b.mmadone);
+      drain_bar(b.mmadone, 0);
+    }
+  } else {
+    // ------------------------------------------------------ epilogue
+    // A holds the list rows 128 / nrep times (nrep = 32 or 64): row i of A is
+    // list row i % nrep, and its copy i / nrep folds nrep / 2 columns of each
+    // 64-column half.  A copy spans whole lane quarters, so the copy index is
+    // the same for every lane of a warp: a tensor-memory load addresses the
+    // same columns for all 32 lanes of the warp.
+    const int e = warp - 4;          // 0..7
+    const int hs = e >> 2;           // column half of each tile
+    const int q = warp & 3;          // TMEM lane quarter
+    const int row = q * 32 + lane;   // row of A / TMEM lane
+    const int nrep = nvalid <= 32 ? 32 : 64;
+    const int lrow = row & (nrep - 1);     // the list row it holds
+    const int copy = row / nrep;
+    const int wc = nrep / 2;               // columns per copy and half
+    const bool valid = lrow < nvalid;
+    const int req = s_req[lrow];
+    const uint32_t pos = (uint32_t)s_pos[lrow];
+    const uint32_t rid = valid ? (p.req_id ? p.req_id[req] : (uint32_t)req) : 0u;
+    const float lq = valid ? p.lse_q[(size_t)req * p.gamma + pos] : 0.f;
+    const float lp = valid ? p.rej_lseP[req] : 0.f;
+    if (valid && (!isfinite(lq) || !isfinite(lp))) set_status(p.status, kErrNonfinite);
+
+    // ---- A operand: rows of E for x_{k-1} of each listed request ----
+    {
+      int my_tok = -1;
+      if (lane < 16) my_tok = s_tok[(e + 8 * lane) & (nrep - 1)];
+      const int cpr = p.rank / 8;
+      uint4 v[16];
+#pragma unroll
+      for (int kk = 0; kk < 16; ++kk) {
+        const int tok = __shfl_sync(0xffffffffu, my_tok, kk);
+        v[kk] = make_uint4(0u, 0u, 0u, 0u);
+        if (tok >= 0 && lane < cpr &&
+            TC_CHECK((size_t)tok * p.rank + lane * 8 + 8 <= (size_t)p.V * p.rank, 2))
+          v[kk] = __ldcg(reinterpret_cast<const uint4*>(p.E + (size_t)tok * p.rank + lane * 8));
+      }
+      if (lane < cpr) {
+        const int kc = lane >> 3, c8 = lane & 7;
+#pragma unroll
+        for (int kk = 0; kk < 16; ++kk) {
+          const int ir = e + 8 * kk;
+          const size_t off = (size_t)kc * kBox + ir * 128 + ((c8 ^ (ir & 7)) << 4);
+          if (TC_CHECK(off + 16 <= (size_t)kMaxKC * kBox, 1))
+            *reinterpret_cast<uint4*>(sA + off) = v[kk];
+        }
+      }
+      tc::fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(b.aready);
+    }
+
+    ResState st{0ull, 0ull, 0.f, 0.f};
+    uint64_t* full = b.ufull + hs * kRNU;
+    uint64_t* empty = b.uempty + hs * kRNU;
+    const unsigned char* ring = sU + hs * kRNU * kRSlot;
+    uint32_t uit = 0;
+    for (int tt = 0; tt < nt; ++tt) {
+      if (warp_aborted(abort_flag)) break;
+      const int t = t0 + tt;
+      const int buf = tt % kNAcc;
+      if (!warp_wait(&b.accfull[buf], (tt / kNAcc) & 1, abort_flag, p.status)) break;
+      tc::tc_fence_after();
+      const int vx = t * kTileN + hs * kHalf;
+      if (vx < p.V) {
+        const int s = uit % kRNU;
+        if (!warp_wait(&full[s], (uit / kRNU) & 1, abort_flag, p.status)) break;
+        ++uit;
+        const int v0 = vx + copy * wc;
+        const bool active = valid && v0 < p.V;
+        const unsigned char* urow = ring + s * kRSlot + lrow * kRStride + copy * wc * 2;
+        const uint32_t taddr = tmem_base + ((uint32_t)(q * 32) << 16) +
+                               (uint32_t)(buf * kTileN + hs * kHalf + copy * wc);
+        // the tensor-memory load is warp-wide (every lane takes part); the
+        // width is the same for the whole CTA
+        if (wc == 16)
+          res_tile<16>(st, taddr, urow, urow + kRArr, active, v0, p, rid, pos, lq, lp);
+        else
+          res_tile<32>(st, taddr, urow, urow + kRArr, active, v0, p, rid, pos, lq, lp);
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(&empty[s]);   // this warp's reads of the slot are done
+      }
+      tc::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(&b.accempty[buf]);
+    }
+
+    // ---- merge the 2 x 128 / nrep partial states of each list row ----
+    // The A region is free: the last accumulator wait followed every MMA.
+    ResState* xch = reinterpret_cast<ResState*>(sA);   // [2][kTileM]
+    xch[hs * kTileM + row] = st;
+    asm volatile("bar.sync 1, 256;" ::: "memory");
+    if (hs == 0 && row < nvalid && TC_CHECK(req < p.R_max, 5)) {
+      ResState m{0ull, 0ull, 0.f, 0.f};
+      for (int h = 0; h < 2; ++h)
+        for (int c = 0; c < kTileM / nrep; ++c) {
+          const ResState o = xch[h * kTileM + c * nrep + row];
+          m.best = o.best > m.best ? o.best : m.best;
+          m.best2 = o.best2 > m.best2 ? o.best2 : m.best2;
+          m.fsum += o.fsum;
+          m.fsum2 += o.fsum2;
+        }
+      if (m.best) atomicMax(&p.res_keys[req], m.best);
+      if (m.best2) atomicMax(&p.res_keys[p.R_max + req], m.best2);
+      atomicAdd(&p.res_sums[req], m.fsum);
+      atomicAdd(&p.res_sums[p.R_max + req], m.fsum2);
+    }
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc::tc_fence_after();
+    tc::tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
 }  // namespace
 
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
@@ -1094,6 +1530,64 @@ cudaError_t launch_propose_tc(const Ctx& ctx, const ProposeArgs& a, cudaStream_t
     count_launch(ctx);
   }
   return cudaSuccess;
+}
+
+// The residual pass of sampled verification on the tensor cores (same
+// configurations as the propose engine: bf16 tables, no activation, rank a
+// multiple of 64 <= 256).  The grid covers every list row the batch could
+// need (ceil(R / 64) row blocks x vocabulary ranges); blocks past the
+// device-side list length return at once.
+cudaError_t launch_residual_tc(const Ctx& ctx, const VerifyArgs& a, cudaStream_t s) {
+  if (a.R <= 0) return cudaSuccess;
+  PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
+  if (!encode) return cudaErrorNotSupported;
+  CUtensorMap tmW;
+  {
+    const cuuint64_t dims[2] = {(cuuint64_t)a.rank, (cuuint64_t)a.V};
+    const cuuint64_t strides[1] = {(cuuint64_t)a.rank * 2};
+    const cuuint32_t box[2] = {kKChunk, (cuuint32_t)kTileN};
+    const cuuint32_t estr[2] = {1, 1};
+    if (encode(&tmW, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(a.W), dims, strides,
+               box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return cudaErrorInvalidValue;
+  }
+  cudaError_t e = cudaFuncSetAttribute(residual_tc_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kRSmemBytes);
+  if (e != cudaSuccess) return e;
+  ResParams p{};
+  p.E = static_cast<const __nv_bfloat16*>(a.E);
+  p.U = static_cast<const __nv_bfloat16*>(a.U);
+  p.P = static_cast<const __nv_bfloat16*>(a.P);
+  p.prev_tok = a.prev_tok;
+  p.tokens = a.tokens;
+  p.req_id = a.req_id;
+  p.lse_q = a.lse_q;
+  p.rej_list = ctx.ws.rej_list;
+  p.rej_k = ctx.ws.rej_k;
+  p.rej_lseP = ctx.ws.rej_lseP;
+  p.n_rej = ctx.ws.counters + 1;
+  p.res_keys = ctx.ws.res_keys;
+  p.res_sums = ctx.ws.res_sums;
+  p.status = ctx.ws.status;
+  p.R = a.R;
+  p.R_max = ctx.cfg.R_max;
+  p.V = a.V;
+  p.rank = a.rank;
+  p.gamma = a.gamma;
+  p.bias_at_first = a.bias_at_first;
+  p.ntiles = (a.V + kTileN - 1) / kTileN;
+  p.inv_T = 1.f / a.temperature;
+  p.k0 = (uint32_t)(a.seed & 0xFFFFFFFFull);
+  p.k1 = (uint32_t)(a.seed >> 32);
+  const int MT = (a.R + kRRows - 1) / kRRows;
+  int n_vr = ctx.num_sms / MT;
+  if (n_vr < 1) n_vr = 1;
+  if (n_vr > p.ntiles) n_vr = p.ntiles;
+  p.n_vr = n_vr;
+  residual_tc_kernel<<<MT * n_vr, kTcThreads, kRSmemBytes, s>>>(tmW, p);
+  count_launch(ctx);
+  return cudaGetLastError();
 }
 
 }  // namespace dsd

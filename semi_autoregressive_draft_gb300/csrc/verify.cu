@@ -16,14 +16,29 @@
 //                      and stops at the first rejection; writes accept_len
 //                      and (unless a residual draw is needed) next_token.
 //   residual pass      sampled only, requests with a rejection: recompute
-//                      q_k from U, E, W (the CUDA-core bias path) and draw
-//                      from norm(max(0, p_k - q_k)) by Gumbel-max (stream 2).
+//                      q_k from U, E, W (residual_tc_kernel on the tensor
+//                      cores where the propose engine could run, else the
+//                      CUDA-core bias path) and draw from
+//                      norm(max(0, p_k - q_k)) by Gumbel-max (stream 2).
 //   verify_finish      next_token of the rejected requests.
 #include "dsd_common.cuh"
 
 namespace dsd {
 
 cudaError_t launch_residual_simt(const Ctx& ctx, const VerifyArgs& a, cudaStream_t s);
+cudaError_t launch_residual_tc(const Ctx& ctx, const VerifyArgs& a, cudaStream_t s);
+int tc_supported(const Ctx& ctx, char* why, size_t why_len);
+
+// The residual pass runs on the tensor cores (residual_tc_kernel) wherever
+// the propose engine could: bf16 tables, no activation, a rank that is a
+// multiple of 64 (<= 256), the AUTO or TCGEN05 engine and the plain Markov
+// head.  Otherwise the CUDA-core residual pass.
+static bool residual_on_tc(const Ctx& ctx, const VerifyArgs& a) {
+  if (a.gated_rep != nullptr) return false;
+  if (ctx.cfg.engine != 0 && ctx.cfg.engine != 2) return false;   // AUTO, TCGEN05
+  char why[256];
+  return tc_supported(ctx, why, sizeof(why)) != 0;
+}
 
 constexpr int kRowThreads = 256;
 __device__ __forceinline__ float max_nan(float a, float b) {
@@ -519,7 +534,7 @@ cudaError_t launch_verify(const Ctx& ctx, const VerifyArgs& a, cudaStream_t s) {
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
   if (sampled) {
-    e = launch_residual_simt(ctx, a, s);
+    e = residual_on_tc(ctx, a) ? launch_residual_tc(ctx, a, s) : launch_residual_simt(ctx, a, s);
     if (e != cudaSuccess) return e;
     verify_finish<<<(a.R + 255) / 256, 256, 0, s>>>(ws.rej_list, ws.counters + 1, ws.res_keys,
                                                     ws.res_sums, ctx.cfg.R_max, a.next_token,

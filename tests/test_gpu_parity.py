@@ -149,6 +149,23 @@ def test_cycle_tc_shapes(dsd, R, V, rank, temperature):
     check_cycle(spec, x, k)
 
 
+@pytest.mark.parametrize("R,V,rank", [
+    (19, 2568, 256),     # one 64-row block of the rejection list, ragged vocabulary tail
+    (100, 1544, 128),    # two blocks, rank 128
+    (200, 4104, 256),    # four blocks, the last partial
+    (7, 1032, 64),       # a handful of rows, rank 64
+])
+def test_residual_pass_on_tensor_cores(dsd, R, V, rank):
+    # every drafted position is verified (keep_len = gamma) at T = 1, so most
+    # requests reject somewhere and take the residual draw of the tensor-core
+    # residual pass; accept lengths and next tokens against the oracle
+    spec = synth.scaled(synth.CYCLE_SPECS["sampled"], R=R, V=V, r=rank, ew_std=0.3,
+                        seed=300 + R, n_sps=None)
+    x, k = run_cycle(dsd, spec, engine="tcgen05", keep_all=True)
+    check_cycle(spec, x, k, keep_all=True)
+    assert (k["accept_len"] < spec.G).sum() >= max(1, R // 4)
+
+
 def test_tc_mma_simt_engines_agree(dsd):
     """Tokens identical and lse within tolerance across the three engines at
     two full M-tiles, on rows whose top-2 margin is not a near tie."""
