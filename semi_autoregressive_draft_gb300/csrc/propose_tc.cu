@@ -140,17 +140,21 @@ __device__ __forceinline__ void add_bf16x2(uint32_t w, uint32_t a_lo, uint32_t a
 // rescaling: terms of the running sum stay below 2^kLagBits.
 constexpr float kLagBits = 8.f;
 
-// Process 32 consecutive columns of one request row: x = acc + u (fp32),
-// masked beyond V; fold into the base-2 log-sum-exp and the argmax key.
-// The log-sum-exp state (m2, s) means sum = s * 2^m2.  Its reference m2 is
-// only raised when the chunk maximum exceeds it by more than kLagBits, so
-// the exponentials of a chunk do not wait for the chunk's maximum; pairs of
-// columns go through the packed fp32x2 pipe and the sum is a tree.
-__device__ __forceinline__ void fold32(RowState& st, const uint32_t (&acc)[32], const uint4* u,
-                                       int v0, const TcParams& p, uint32_t rid) {
-  float xs[32];
+// Process N (16 or 32) consecutive columns of one request row: x = acc + u
+// (fp32), masked beyond V; fold into the base-2 log-sum-exp and the argmax
+// key.  The log-sum-exp state (m2, s) means sum = s * 2^m2.  Its reference
+// m2 is only raised when the chunk maximum exceeds it by more than
+// kLagBits, so the exponentials of a chunk do not wait for the chunk's
+// maximum; pairs of columns go through the packed fp32x2 pipe and the sum is
+// a tree.
+template <int N>
+__device__ __forceinline__ void foldN(RowState& st, const uint32_t (&acc)[N], const uint4* u,
+                                      int v0, const TcParams& p, uint32_t rid) {
+  static_assert(N == 16 || N == 32, "16 or 32 columns");
+  constexpr int NG = N / 4;          // groups of four columns
+  float xs[N];
 #pragma unroll
-  for (int c = 0; c < 4; ++c) {
+  for (int c = 0; c < N / 8; ++c) {
     const uint32_t w[4] = {u[c].x, u[c].y, u[c].z, u[c].w};
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
@@ -158,26 +162,27 @@ __device__ __forceinline__ void fold32(RowState& st, const uint32_t (&acc)[32], 
       add_bf16x2(w[e], acc[i], acc[i + 1], xs[i], xs[i + 1]);
     }
   }
-  if (v0 + 32 > p.V) {
+  if (v0 + N > p.V) {
 #pragma unroll
-    for (int i = 0; i < 32; ++i)
+    for (int i = 0; i < N; ++i)
       if (v0 + i >= p.V) xs[i] = -INFINITY;
   }
   if (p.sampled) {
     const uint64_t t2 = tc::pack2(p.inv_T, p.inv_T);
 #pragma unroll
-    for (int i = 0; i < 32; i += 2) {
+    for (int i = 0; i < N; i += 2) {
       const uint64_t x2 = tc::mul2(tc::pack2(xs[i], xs[i + 1]), t2);
       tc::unpack2(x2, xs[i], xs[i + 1]);
     }
   }
-  // maxima of the eight groups of four, then of the chunk
-  float gm[8];
+  // maxima of the groups of four, then of the chunk
+  float gm[NG];
 #pragma unroll
-  for (int g = 0; g < 8; ++g)
+  for (int g = 0; g < NG; ++g)
     gm[g] = fmaxf(tc::max3(xs[4 * g], xs[4 * g + 1], xs[4 * g + 2]), xs[4 * g + 3]);
-  const float cm = fmaxf(tc::max3(gm[0], gm[1], gm[2]),
-                         fmaxf(tc::max3(gm[3], gm[4], gm[5]), fmaxf(gm[6], gm[7])));
+  float cm = fmaxf(gm[0], gm[1]);
+#pragma unroll
+  for (int g = 2; g < NG; g += 2) cm = tc::max3(cm, gm[g], gm[g + 1]);
   const float cm2 = cm * kLog2e;
   if (cm2 > st.m2 + kLagBits) {       // rare after the first chunks
     st.s *= tc::ex2(st.m2 - cm2);     // 0 while the state is empty
@@ -186,15 +191,15 @@ __device__ __forceinline__ void fold32(RowState& st, const uint32_t (&acc)[32], 
   if (st.m2 != -INFINITY) {
     const uint64_t l2 = tc::pack2(kLog2e, kLog2e);
     const uint64_t nm = tc::pack2(-st.m2, -st.m2);
-    uint64_t e2[16];
+    uint64_t e2[N / 2];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
+    for (int i = 0; i < N / 2; ++i) {
       float a, b;
       tc::unpack2(tc::fma2(tc::pack2(xs[2 * i], xs[2 * i + 1]), l2, nm), a, b);
       e2[i] = tc::pack2(tc::ex2(a), tc::ex2(b));
     }
 #pragma unroll
-    for (int w = 8; w >= 1; w >>= 1)
+    for (int w = N / 4; w >= 1; w >>= 1)
 #pragma unroll
       for (int i = 0; i < w; ++i) e2[i] = tc::add2(e2[i], e2[i + w]);
     float slo, shi;
@@ -204,13 +209,13 @@ __device__ __forceinline__ void fold32(RowState& st, const uint32_t (&acc)[32], 
   if (!p.sampled) {
     if (cm > st.best_z) {
       // lowest index attaining the maximum: first group, then within it
-      int g = 7;
+      int g = NG - 1;
 #pragma unroll
-      for (int k = 6; k >= 0; --k)
+      for (int k = NG - 2; k >= 0; --k)
         if (gm[k] == cm) g = k;
       float a0 = xs[0], a1 = xs[1], a2 = xs[2];
 #pragma unroll
-      for (int k = 1; k < 8; ++k)
+      for (int k = 1; k < NG; ++k)
         if (g == k) {
           a0 = xs[4 * k];
           a1 = xs[4 * k + 1];
@@ -224,7 +229,7 @@ __device__ __forceinline__ void fold32(RowState& st, const uint32_t (&acc)[32], 
     float zb = st.best_z;
     uint32_t vb = st.best_v;
 #pragma unroll
-    for (int g = 0; g < 8; ++g) {
+    for (int g = 0; g < NG; ++g) {
       const uint32_t v = (uint32_t)(v0 + 4 * g);
       const Philox4 ph = philox4x32_10(v >> 2, (uint32_t)p.j, rid, 0u, p.k0, p.k1);
       const float z0 = xs[4 * g + 0] + gumbel_from_word(ph.x);
@@ -241,10 +246,21 @@ __device__ __forceinline__ void fold32(RowState& st, const uint32_t (&acc)[32], 
   }
 }
 
-template <bool DUP>   // p.dup as a compile-time constant: the R > 64 path carries none of it
-__global__ void __launch_bounds__(kTcThreads, 1)
+// EW epilogue warps (8, or 16 with setmaxnreg 56 / 104 as in the pair
+// kernel): warp 4 + e folds column group e / 4 (EW / 4 groups of 128 / (EW/4)
+// columns per tile) of TMEM lane quarter warp % 4.  DUP (at most 64
+// requests): rows 64..127 of A repeat rows 0..63 and the two copies of a row
+// fold the two halves of each group's columns.
+template <int EW, bool DUP>
+__global__ void __launch_bounds__(128 + 32 * EW, 1)
     propose_tc_kernel(const __grid_constant__ CUtensorMap tmW,
                       const __grid_constant__ CUtensorMap tmU, const TcParams p) {
+  constexpr int kGroups = EW / 4;               // column groups per tile
+  constexpr int kGCols = kTileN / kGroups;      // columns of a group (64 or 32)
+  constexpr int kFW = DUP ? kGCols / 2 : kGCols;   // columns one thread folds per tile
+  constexpr int kChunk = kFW < 32 ? kFW : 32;   // columns per TMEM load and fold
+  constexpr int kRowsPerWarp = kTileM / EW;     // A rows each epilogue warp gathers
+  static_assert(EW == 8 || EW == 16, "8 or 16 epilogue warps");
   extern __shared__ unsigned char smem_raw[];
   const uint32_t raw = tc::smem_u32(smem_raw);
   unsigned char* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
@@ -285,13 +301,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
     for (int i = 0; i < 2 * kNU; ++i) {
       tc::mbar_init(&b.ufull[i], 1);
-      tc::mbar_init(&b.uempty[i], 4);
+      tc::mbar_init(&b.uempty[i], EW / 2);   // the warps that read a half
     }
     for (int i = 0; i < kNAcc; ++i) {
       tc::mbar_init(&b.accfull[i], 1);
-      tc::mbar_init(&b.accempty[i], 8);
+      tc::mbar_init(&b.accempty[i], EW);
     }
-    tc::mbar_init(b.aready, 8);
+    tc::mbar_init(b.aready, EW);
     tc::mbar_init(b.mmadone, 1);
     *abort_flag = 0;
     tc::mbar_fence_init();
@@ -309,6 +325,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   tc::tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
 
+  if (warp < 4) {
+  if constexpr (EW == 16) asm volatile("setmaxnreg.dec.sync.aligned.u32 56;" ::: "memory");
   if (warp == 0) {
     // ------------------------------------------------------ W producer
     if (lane == 0) {
@@ -397,15 +415,20 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       tc::umma_commit(b.mmadone);
       drain_bar(b.mmadone, 0);
     }
-  } else if (warp >= 4) {
+  }
+  } else {
     // ------------------------------------------------------ epilogue
-    const int e = warp - 4;          // 0..7
-    const int hs = e >> 2;           // column half of each tile
+    if constexpr (EW == 16) asm volatile("setmaxnreg.inc.sync.aligned.u32 104;" ::: "memory");
+    const int e = warp - 4;          // 0 .. EW - 1
+    const int cg = e >> 2;           // column group of each tile
     const int q = warp & 3;          // TMEM lane quarter this warp may access
     const int row = q * 32 + lane;   // row within the M-tile
-    // With dup, rows 64..127 hold the requests of rows 0..63 again, and the
-    // two copies of a request fold different 32-column chunks of each tile.
+    // With dup, rows 64..127 hold the requests of rows 0..63 again (lane
+    // quarters 2 and 3), and each copy folds its half of the group.
     const int rrow = DUP ? (row & 63) : row;   // the request's row (its U row)
+    const int copy = DUP ? (q >> 1) : 0;       // the same for the whole warp
+    const int cbase = cg * kGCols + copy * kFW;   // first column of this thread, in the tile
+    const int hs = cbase / kHalf;    // the U box (column half) it reads
     const int r = r0 + rrow;
     const bool valid = r < p.R;
     const bool warp_rows = r0 + (DUP ? (q & 1) : q) * 32 < p.R;   // any request in this warp?
@@ -417,14 +440,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     asm volatile("griddepcontrol.wait;" ::: "memory");
 
     // ---- A operand: rows of E for the tokens of step j-1 ----
-    // This warp fills rows e, e+8, ..., e+120: lane k < 16 fetches the token
-    // of row e+8k, then the 16 rows are copied (16 loads in flight per lane)
-    // into the 128-byte-swizzled K-major layout of the UMMA descriptors.
+    // This warp fills rows e, e + EW, ...: lane k < kRowsPerWarp fetches the
+    // token of row e + EW k, then the rows are copied into the 128-byte-
+    // swizzled K-major layout of the UMMA descriptors.
     {
       const bool biased = (j > 0) || p.bias_at_first;
       int my_tok = -1;
-      if (lane < 16) {
-        const int rr = r0 + (DUP ? ((e + 8 * lane) & 63) : (e + 8 * lane));
+      if (lane < kRowsPerWarp) {
+        const int rr = r0 + (DUP ? ((e + EW * lane) & 63) : (e + EW * lane));
         if (biased && rr < p.R) {
           int tk = (j == 0) ? p.prev_tok[rr]
                             : (int)key_index(__ldcg(&p.keys[(size_t)(j - 1) * p.R_max + rr]));
@@ -436,9 +459,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
       }
       const int cpr = p.rank / 8;    // 16-byte chunks per row
-      uint4 v[16];
+      uint4 v[kRowsPerWarp];
 #pragma unroll
-      for (int kk = 0; kk < 16; ++kk) {
+      for (int kk = 0; kk < kRowsPerWarp; ++kk) {
         const int tok = __shfl_sync(0xffffffffu, my_tok, kk);
         v[kk] = make_uint4(0u, 0u, 0u, 0u);
         if (tok >= 0 && lane < cpr &&
@@ -446,11 +469,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           v[kk] = __ldcg(reinterpret_cast<const uint4*>(p.E + (size_t)tok * p.rank + lane * 8));
       }
       if (lane < cpr) {
-        const int kc = lane >> 3, cc = lane & 7;
+        const int kc = lane >> 3, c8 = lane & 7;
 #pragma unroll
-        for (int kk = 0; kk < 16; ++kk) {
-          const int ir = e + 8 * kk;
-          const size_t off = (size_t)kc * kBox + ir * 128 + ((cc ^ (ir & 7)) << 4);
+        for (int kk = 0; kk < kRowsPerWarp; ++kk) {
+          const int ir = e + EW * kk;
+          const size_t off = (size_t)kc * kBox + ir * 128 + ((c8 ^ (ir & 7)) << 4);
           if (TC_CHECK(off + 16 <= (size_t)kMaxKC * kBox, 1))
             *reinterpret_cast<uint4*>(sA + off) = v[kk];
         }
@@ -465,6 +488,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     uint64_t* full = b.ufull + hs * kNU;
     uint64_t* empty = b.uempty + hs * kNU;
     const unsigned char* ring = sU + hs * kNU * kBox;
+    const int c0 = (cbase - hs * kHalf) / 8;   // this thread's first 16-byte chunk of its U row
     uint32_t uit = 0;
     for (int tt = 0; tt < nt; ++tt) {
       if (warp_aborted(abort_flag)) break;
@@ -477,46 +501,28 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const int s = uit % kNU;
         if (!warp_wait(&full[s], (uit / kNU) & 1, abort_flag, p.status)) break;
         ++uit;
-        // 128-byte swizzle: 16-byte chunk c of row `row` sits at chunk
-        // c ^ (row & 7) of that row.
-        uint4 u[8];
+        // 128-byte swizzle: 16-byte chunk c of row `rrow` sits at chunk
+        // c ^ (rrow & 7) of that row.
+        uint4 u[kFW / 8];
         const unsigned char* urow = ring + s * kBox + rrow * 128;
-        const int cc = q >> 1;   // DUP: this copy's 32-column chunk of the half
         if (warp_rows) {
-          if constexpr (DUP) {
 #pragma unroll
-            for (int c = 0; c < 4; ++c)
-              u[c] = *reinterpret_cast<const uint4*>(urow + (((cc * 4 + c) ^ (rrow & 7)) << 4));
-          } else {
-#pragma unroll
-            for (int c = 0; c < 8; ++c)
-              u[c] = *reinterpret_cast<const uint4*>(urow + ((c ^ (rrow & 7)) << 4));
-          }
+          for (int c = 0; c < kFW / 8; ++c)
+            u[c] = *reinterpret_cast<const uint4*>(urow + (((c0 + c) ^ (rrow & 7)) << 4));
         }
         __syncwarp();
         if (lane == 0) tc::mbar_arrive(&empty[s]);   // the slot's data is in registers
         __syncwarp();
         if (warp_rows) {
-          if constexpr (DUP) {   // one chunk: the other copy folds the other
-            const int v0 = vx + cc * 32;
-            if (v0 < p.V) {
-              uint32_t acc[32];
-              tc::tmem_ld_32x32b_x32_wait(tmem_base + ((uint32_t)(q * 32) << 16) +
-                                              (uint32_t)(buf * kTileN + hs * kHalf + cc * 32),
-                                          acc);
-              fold32(st, acc, u, v0, p, rid);
-            }
-          } else {
 #pragma unroll
-            for (int c = 0; c < 2; ++c) {
-              const int v0 = vx + c * 32;
-              if (v0 >= p.V) break;
-              uint32_t acc[32];
-              tc::tmem_ld_32x32b_x32_wait(tmem_base + ((uint32_t)(q * 32) << 16) +
-                                              (uint32_t)(buf * kTileN + hs * kHalf + c * 32),
-                                          acc);
-              fold32(st, acc, u + 4 * c, v0, p, rid);
-            }
+          for (int c = 0; c < kFW / kChunk; ++c) {
+            const int v0 = t * kTileN + cbase + c * kChunk;
+            if (v0 >= p.V) break;
+            uint32_t acc[kChunk];
+            tc::tmem_ld_wait<kChunk>(tmem_base + ((uint32_t)(q * 32) << 16) +
+                                         (uint32_t)(buf * kTileN + cbase + c * kChunk),
+                                     acc);
+            foldN<kChunk>(st, acc, u + (kChunk / 8) * c, v0, p, rid);
           }
         }
       }
@@ -525,27 +531,31 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       if (lane == 0) tc::mbar_arrive(&b.accempty[buf]);
     }
 
-    // ---- merge the two column halves of each row, publish step j's partial ----
+    // ---- merge the column groups (and with dup, the two copies) of each
+    // row, publish step j's partial ----
     // The A region is free: the last accumulator barrier this warp waited on
     // was committed after every MMA that reads A, so they have all completed.
-    RowState* xch = reinterpret_cast<RowState*>(sA);
-    RowState* xch2 = xch + kTileM;   // dup: the second copy's merged state
-    if (hs == 1) xch[row] = st;
-    asm volatile("bar.sync 1, 256;" ::: "memory");   // the eight epilogue warps
-    if (hs == 0) {
-      const RowState o = xch[row];
-      const Lse2 l = lse2_merge(Lse2{st.m2, st.s}, Lse2{o.m2, o.s});
-      st.m2 = l.m;
-      st.s = l.s;
-      if (o.best_z > st.best_z || (o.best_z == st.best_z && o.best_v < st.best_v)) {
-        st.best_z = o.best_z;
-        st.best_v = o.best_v;
+    RowState* xch = reinterpret_cast<RowState*>(sA);   // [kGroups][kTileM]
+    RowState* xch2 = xch + kGroups * kTileM;           // dup: the second copy's merged state
+    if (cg > 0) xch[(cg - 1) * kTileM + row] = st;
+    asm volatile("bar.sync 1, %0;" ::"n"(32 * EW) : "memory");   // the epilogue warps
+    if (cg == 0) {
+#pragma unroll
+      for (int k = 0; k < kGroups - 1; ++k) {
+        const RowState o = xch[k * kTileM + row];
+        const Lse2 l = lse2_merge(Lse2{st.m2, st.s}, Lse2{o.m2, o.s});
+        st.m2 = l.m;
+        st.s = l.s;
+        if (o.best_z > st.best_z || (o.best_z == st.best_z && o.best_v < st.best_v)) {
+          st.best_z = o.best_z;
+          st.best_v = o.best_v;
+        }
       }
       if (DUP && row >= 64) xch2[row - 64] = st;
     }
     if (DUP) {
-      asm volatile("bar.sync 1, 256;" ::: "memory");
-      if (hs == 0 && row < 64) {
+      asm volatile("bar.sync 1, %0;" ::"n"(32 * EW) : "memory");
+      if (cg == 0 && row < 64) {
         const RowState o = xch2[row];
         const Lse2 l = lse2_merge(Lse2{st.m2, st.s}, Lse2{o.m2, o.s});
         st.m2 = l.m;
@@ -556,7 +566,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
       }
     }
-    if (hs == 0 && (!DUP || row < 64) && valid && TC_CHECK(vr < p.n_part && r < p.R_max, 5)) {
+    if (cg == 0 && (!DUP || row < 64) && valid && TC_CHECK(vr < p.n_part && r < p.R_max, 5)) {
       atomicMax(&p.keys[(size_t)j * p.R_max + r], make_key(st.best_z, st.best_v));
       p.parts[((size_t)j * p.n_part + vr) * p.R_max + r] = make_float2(st.m2, st.s);
     }
@@ -892,7 +902,7 @@ __global__ void __launch_bounds__(128 + 32 * EW, 1)
             tc::tmem_ld_32x32b_x32_wait(tmem_base + ((uint32_t)(q * 32) << 16) +
                                             (uint32_t)(buf * kTileN + (v0 - t * kTileN)),
                                         acc);
-            fold32(st, acc, u + 4 * c, v0, p, rid);
+            foldN<32>(st, acc, u + 4 * c, v0, p, rid);
           }
         }
       }
@@ -1433,6 +1443,7 @@ int tc_vranges(const Ctx& ctx, int R) {
 
 // An even number of M-tiles runs on CTA pairs (propose_tc_pair_kernel).
 constexpr int kPairEpiWarps = 16;
+constexpr int kSingleEpiWarps = 16;
 static bool use_pair(int R) {
   const int MT = (R + kTileM - 1) / kTileM;
   return MT >= 2 && MT % 2 == 0;
@@ -1467,11 +1478,11 @@ cudaError_t launch_propose_tc(const Ctx& ctx, const ProposeArgs& a, cudaStream_t
   cudaError_t e = cudaMemsetAsync(ctx.ws.keys, 0,
                                   sizeof(unsigned long long) * (size_t)a.gamma * ctx.cfg.R_max, s);
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(propose_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           kSmemBytes);
+  e = cudaFuncSetAttribute(propose_tc_kernel<kSingleEpiWarps, false>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(propose_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kSmemBytes);
+    e = cudaFuncSetAttribute(propose_tc_kernel<kSingleEpiWarps, true>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(propose_tc_pair_kernel<kPairEpiWarps>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, kPSmemBytes);
@@ -1515,7 +1526,7 @@ cudaError_t launch_propose_tc(const Ctx& ctx, const ProposeArgs& a, cudaStream_t
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(pair ? 128 + 32 * kPairEpiWarps : kTcThreads);
+  cfg.blockDim = dim3(128 + 32 * (pair ? kPairEpiWarps : kSingleEpiWarps));
   cfg.dynamicSmemBytes = pair ? kPSmemBytes : kSmemBytes;
   cfg.stream = s;
   cfg.attrs = pair ? attr : attr + 1;
@@ -1523,8 +1534,8 @@ cudaError_t launch_propose_tc(const Ctx& ctx, const ProposeArgs& a, cudaStream_t
     p.j = j;
     cfg.numAttrs = (pair ? 1 : 0) + (j > 0 ? 1 : 0);
     e = pair    ? cudaLaunchKernelEx(&cfg, propose_tc_pair_kernel<kPairEpiWarps>, tmW, tmU, p)
-        : p.dup ? cudaLaunchKernelEx(&cfg, propose_tc_kernel<true>, tmW, tmU, p)
-                : cudaLaunchKernelEx(&cfg, propose_tc_kernel<false>, tmW, tmU, p);
+        : p.dup ? cudaLaunchKernelEx(&cfg, propose_tc_kernel<kSingleEpiWarps, true>, tmW, tmU, p)
+                : cudaLaunchKernelEx(&cfg, propose_tc_kernel<kSingleEpiWarps, false>, tmW, tmU, p);
     if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     count_launch(ctx);
