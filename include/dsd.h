@@ -80,8 +80,9 @@ enum dsd_dtype { DSD_F32 = 0, DSD_BF16 = 1 };
 enum dsd_act { DSD_ACT_NONE = 0, DSD_ACT_SILU = 1 };
 /* Propose engine.  AUTO picks the 5th-generation tensor-core engine
  * (TCGEN05: TMA-staged operands, tcgen05.mma into TMEM accumulators) for bf16
- * tables, no activation, a rank that is a multiple of 64 (<= 256) and batches
- * of at least 16 requests, and the CUDA-core engine (SIMT) otherwise.  MMA
+ * tables, no activation and a rank that is a multiple of 64 (<= 256), at any
+ * batch size, and the CUDA-core engine (SIMT) otherwise.  The same rule picks
+ * the engine of dsd_verify's residual pass (sampled verification).  MMA
  * (warp-level mma.sync tensor cores, same requirements) is only used when
  * asked for.  TCGEN05 or MMA asked for with a configuration they do not
  * support makes dsd_propose return DSD_ERR_UNSUPPORTED before any launch. */

@@ -474,7 +474,8 @@ def test_full_size_overlap_sampled_blocks(dsd):
 
 @pytest.mark.parametrize("R,dtype,act,expect", [
     (16, "bf16", "none", "tcgen05"),
-    (15, "bf16", "none", "simt"),
+    (15, "bf16", "none", "tcgen05"),
+    (1, "bf16", "none", "tcgen05"),
     (64, "f32", "none", "simt"),
     (64, "bf16", "silu", "simt"),
 ])
