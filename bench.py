@@ -38,6 +38,8 @@ TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
 KERNEL_SOURCES = {
     "simt_bias_kernel": ["propose_simt.cu", "dsd_common.cuh"],
     "propose_tc_kernel": ["propose_tc.cu", "tc_common.cuh", "tc_ptx.cuh", "dsd_common.cuh"],
+    "propose_tc_pair_kernel": ["propose_tc.cu", "tc_common.cuh", "tc_ptx.cuh", "dsd_common.cuh"],
+    "residual_tc_kernel": ["propose_tc.cu", "tc_common.cuh", "tc_ptx.cuh", "dsd_common.cuh"],
     "propose_mma_kernel": ["propose_mma.cu", "dsd_common.cuh"],
     "verify_rows": ["verify.cu", "dsd_common.cuh"],
     "overlap_split": ["overlap.cu", "tc_common.cuh", "tc_ptx.cuh", "dsd_common.cuh"],
@@ -259,88 +261,241 @@ def verify_alg_bytes(spec, B):
 
 
 # --------------------------------------------------------------- CPU oracle
+# The fp64 oracle is timed in worker processes started with "spawn" (never
+# forked: the parent may already hold a CUDA context), each with
+# single-threaded BLAS, so that "cores" is the number of workers that really
+# ran.  The inputs reach the workers as memory-mapped .npy files in a
+# temporary directory (shared page cache, no per-worker copy): the bf16 logit
+# rows as their raw 16-bit patterns, widened exactly to fp32 in the worker,
+# and E, W widened once to fp64 (the oracle's precision).
 
-def oracle_sample_cycle(spec, h, n_req, seed, idx=None):
-    """Time the fp64 oracle on a bounded sample: the schedule of the whole
-    batch plus propose and verify of n_req requests; returns estimated
-    seconds per full-batch cycle and the sample description."""
+_POOL_ARRAYS = {}
+_BLAS_ENV = ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS")
+
+
+def _pool_init(dirpath):
+    import numpy as np
+
+    for k in ("U", "P", "E", "W", "conf", "prev_tok", "req_id"):
+        _POOL_ARRAYS[k] = np.load(os.path.join(dirpath, k + ".npy"), mmap_mode="r")
+
+
+def _pool_rows(a, idx):
+    import numpy as np
+
+    rows = np.asarray(a[idx])
+    if rows.dtype == np.uint16:          # bf16 bit patterns -> fp32, exactly
+        rows = (rows.astype(np.uint32) << 16).view(np.float32)
+    return rows
+
+
+def _pool_requests(job):
+    """Propose + verify of some requests of the batch (one worker)."""
     import numpy as np
 
     from oracle import dsd_oracle as O
 
-    R = spec.R
-    if idx is None:
-        idx = np.arange(n_req)
-    rid = h["req_id"].astype(np.int64)
+    idx, keep, temperature, seed = job
+    h = _POOL_ARRAYS
+    idx = np.asarray(idx)
     t0 = time.perf_counter()
-    surv_all = O.survival(h["conf"]).astype(np.float32)
-    sch = O.schedule(surv_all, h["sps"])
-    t1 = time.perf_counter()
-    prop = O.propose(h["U"][idx], h["E"], h["W"], h["conf"][idx], h["prev_tok"][idx], rid[idx],
-                     spec.temperature, seed)
-    O.verify(h["P"][idx], h["U"][idx], h["E"], h["W"], h["prev_tok"][idx], prop["tokens"],
-             sch["keep_len"][idx], rid[idx], spec.temperature, seed)
-    t2 = time.perf_counter()
-    per_req = (t2 - t1) / len(idx)
-    est = (t1 - t0) + per_req * R
-    desc = (f"schedule of all {R} requests + propose/verify of {len(idx)} of {R} requests "
-            f"(all {spec.G} positions, full V={spec.V}; E, W widened to fp64 once); cycle time "
-            f"extrapolated linearly in requests ({t2 - t0:.1f} s measured)")
-    return est, desc, t2 - t0
+    rid = np.asarray(h["req_id"][idx]).astype(np.int64)
+    U = _pool_rows(h["U"], idx)
+    P = _pool_rows(h["P"], idx)
+    prev = np.asarray(h["prev_tok"][idx])
+    prop = O.propose(U, h["E"], h["W"], np.asarray(h["conf"][idx]), prev, rid, temperature, seed)
+    ver = O.verify(P, U, h["E"], h["W"], prev, prop["tokens"], np.asarray(keep), rid,
+                   temperature, seed)
+    return time.perf_counter() - t0, ver["accept_len"].tolist()
 
 
-def host_arrays(x, rows=None):
-    """Host copies for the oracle: the per-request logit rows only for the
-    first `rows` requests (the sample), everything else in full."""
-    from semi_autoregressive_draft_gb300 import synth
+class OraclePool:
+    """Times full draft-verify cycles of the fp64 oracle on the host cores."""
 
-    out = {}
-    for k in ("U", "E", "W", "P", "conf", "prev_tok", "req_id", "sps"):
-        t = x[k]
-        if rows is not None and k in ("U", "P"):
-            t = t[:rows]
-        out[k] = synth.to_numpy(t)
-    return out
+    def __init__(self, spec, x, workers=None):
+        import tempfile
+
+        import numpy as np
+
+        from oracle import dsd_oracle as O
+        from semi_autoregressive_draft_gb300 import synth
+
+        self.spec = spec
+        self.workers = max(1, workers or os.cpu_count() or 1)
+        self.seed = x["seed"]
+        self.dir = tempfile.mkdtemp(prefix="dsd_oracle_")
+        for k in ("U", "P"):
+            t = x[k].detach()
+            a = (t.view(dtype=__import__("torch").int16).cpu().numpy().view(np.uint16)
+                 if spec.dtype == "bf16" else t.float().cpu().numpy())
+            np.save(os.path.join(self.dir, k + ".npy"), a)
+        for k in ("E", "W"):
+            np.save(os.path.join(self.dir, k + ".npy"), synth.to_numpy(x[k]).astype(np.float64))
+        for k in ("conf", "prev_tok", "req_id"):
+            np.save(os.path.join(self.dir, k + ".npy"), synth.to_numpy(x[k]))
+        self.conf = synth.to_numpy(x["conf"])
+        self.sps = synth.to_numpy(x["sps"])
+        self._O = O
+        self._pools = {}
+
+    def _pool(self, n):
+        import multiprocessing as mp
+
+        if n not in self._pools:
+            saved = {k: os.environ.get(k) for k in _BLAS_ENV}
+            for k in _BLAS_ENV:
+                os.environ[k] = "1"
+            try:
+                pool = mp.get_context("spawn").Pool(n, initializer=_pool_init,
+                                                    initargs=(self.dir,))
+                pool.map(abs, range(n))           # every worker has started
+            finally:
+                for k, v in saved.items():
+                    if v is None:
+                        os.environ.pop(k, None)
+                    else:
+                        os.environ[k] = v
+            self._pools[n] = pool
+        return self._pools[n]
+
+    def schedule(self):
+        O = self._O
+        surv = O.survival(self.conf).astype("float32")
+        return O.schedule(surv, self.sps)["keep_len"]
+
+    def cycle(self, reqs=None, workers=None):
+        """One cycle (schedule of the whole batch, then propose + verify of
+        `reqs`, default all requests) on `workers` processes; returns (wall
+        seconds, committed tokens of those requests, CPU seconds in workers)."""
+        R = self.spec.R
+        reqs = list(range(R)) if reqs is None else list(reqs)
+        n = workers or self.workers
+        pool = self._pool(n)
+        chunk = max(1, len(reqs) // (4 * n))
+        t0 = time.perf_counter()
+        keep = self.schedule()
+        jobs = [(reqs[i:i + chunk], keep[reqs[i:i + chunk]], self.spec.temperature, self.seed)
+                for i in range(0, len(reqs), chunk)]
+        res = pool.map(_pool_requests, jobs, chunksize=1)
+        wall = time.perf_counter() - t0
+        tokens = sum(a + 1 for _, acc in res for a in acc)
+        return wall, tokens, sum(t for t, _ in res)
+
+    def single_thread(self, n_req):
+        """Per-request time of one single-threaded worker over n_req requests,
+        extrapolated to the whole batch (plus the measured schedule)."""
+        self.cycle(reqs=[0], workers=1)            # warm the worker
+        t0 = time.perf_counter()
+        self.schedule()
+        t_sched = time.perf_counter() - t0
+        wall, _, _ = self.cycle(reqs=range(n_req), workers=1)
+        per_req = (wall - t_sched) / n_req
+        return t_sched + per_req * self.spec.R, wall
+
+    def close(self):
+        import shutil
+
+        for pool in self._pools.values():
+            pool.close()
+            pool.join()
+        self._pools = {}
+        shutil.rmtree(self.dir, ignore_errors=True)
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+
+def oracle_baseline(spec, x, n_cycles=2, n_single=8):
+    """The in-run CPU baseline: n_cycles full-batch cycles on every host core
+    (after one untimed cycle), measured, plus a single-thread figure."""
+    with OraclePool(spec, x) as pool:
+        pool.cycle()
+        runs = [pool.cycle() for _ in range(n_cycles)]
+        st_est, st_wall = pool.single_thread(min(n_single, spec.R))
+        wall = statistics.mean(w for w, _, _ in runs)
+        busy = sum(c for _, _, c in runs)
+        return {
+            "value": 1.0 / wall, "unit": "cycles/s", "cores": pool.workers, "kind": "oracle",
+            "sample": (f"{n_cycles} full cycles of the whole batch (schedule of all {spec.R} "
+                       f"requests, then propose + verify of every request, all {spec.G} "
+                       f"positions, full V={spec.V}) on {pool.workers} single-threaded worker "
+                       f"processes, after one untimed cycle; measured, not extrapolated"),
+            "ms_per_cycle": wall * 1e3,
+            "cpu_seconds": busy,
+            "single_thread": {
+                "value": 1.0 / st_est, "unit": "cycles/s", "cores": 1,
+                "sample": (f"propose + verify of {min(n_single, spec.R)} requests on one "
+                           f"single-threaded process ({st_wall:.1f} s measured) plus the "
+                           f"measured schedule, extrapolated linearly to {spec.R} requests"),
+            },
+        }
+
+
+def cycle_config(spec, world):
+    """The config dict both arms print for a draft-verify workload."""
+    return {"workload": workload_label(spec), "R": spec.R, "gamma": spec.G, "V": spec.V,
+            "rank": spec.r, "temperature": spec.temperature, "parallelism": f"replicas x{world}",
+            "l2": f"inputs {cycle_input_bytes(spec) / 1e9:.2f} GB; the GPU arm flushes L2 "
+                  f"(512 MB write outside the events) between steps"}
+
+
+def cycle_input_bytes(spec):
+    esz = 2 if spec.dtype == "bf16" else 4
+    return (spec.R * spec.G + spec.R * (spec.G + 1)) * spec.V * esz + 2 * spec.V * spec.r * esz
 
 
 # --------------------------------------------------------------------- arms
 
 def run_reference(args):
+    """The oracle arm: each step is one full draft-verify cycle of the whole
+    batch (schedule, then propose + verify of every request) on the host
+    cores, timed on the wall clock; nothing is extrapolated."""
     rank, local_rank, world = dist_info()
     if rank != 0:
         return 0
-    import numpy as np
-    import torch
-
     from semi_autoregressive_draft_gb300 import synth
 
     spec = cycle_spec(args.workload)
     x = synth.cycle_inputs(spec, device="cpu")
-    h = host_arrays(x)
-    for k in ("E", "W"):
-        h[k] = h[k].astype(np.float64)
-    n_req = 1
-    for _ in range(args.warmup):
-        oracle_sample_cycle(spec, h, n_req, x["seed"])
-    times = []
-    desc = ""
-    for s in range(args.steps):
-        idx = np.array([(s * 37) % spec.R])
-        est, desc, _ = oracle_sample_cycle(spec, h, n_req, x["seed"], idx)
-        times.append(est)
-    desc = desc.replace("propose/verify of 1 of", "propose/verify of 1 (a different one each step) of")
+    n_req = spec.R if args.ref_requests <= 0 else min(args.ref_requests, spec.R)
+    with OraclePool(spec, x) as pool:
+        for s in range(args.warmup):
+            pool.cycle(reqs=[(s * 37 + i) % spec.R for i in range(n_req)])
+        times, toks = [], []
+        for s in range(args.steps):
+            wall, tok, _ = pool.cycle(reqs=[(s * 37 + i) % spec.R for i in range(n_req)])
+            times.append(wall)
+            toks.append(tok)
+        st_est, st_wall = pool.single_thread(min(8, spec.R))
+        workers = pool.workers
     sec = statistics.mean(times)
-    value = 1.0 / sec
-    cores = os.cpu_count()
+    frac = n_req / spec.R
+    value = frac / sec                     # whole-batch cycles per second
+    if n_req == spec.R:
+        sample = (f"each step: one full cycle of the whole batch (schedule of all {spec.R} "
+                  f"requests, then propose + verify of every request, all {spec.G} positions, "
+                  f"full V={spec.V}) on {workers} single-threaded worker processes; measured")
+    else:
+        sample = (f"each step: schedule of all {spec.R} requests, then propose + verify of "
+                  f"{n_req} of them on {workers} single-threaded worker processes; value = "
+                  f"{n_req}/{spec.R} of a cycle per measured step time")
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "cycles/s",
-        "tokens_per_s": None, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "tokens_per_s": statistics.mean(toks) / frac * value if toks else None,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": sec * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": workload_label(spec), "R": spec.R, "gamma": spec.G, "V": spec.V,
-                   "rank": spec.r},
-        "cpu_baseline": {"value": value, "unit": "cycles/s", "cores": cores, "kind": "oracle",
-                         "sample": "each step: " + desc},
+        "config": cycle_config(spec, world),
+        "cpu_baseline": {"value": value, "unit": "cycles/s", "cores": workers, "kind": "oracle",
+                         "sample": sample,
+                         "single_thread": {"value": 1.0 / st_est, "unit": "cycles/s",
+                                           "cores": 1,
+                                           "sample": f"propose + verify of {min(8, spec.R)} "
+                                                     f"requests on one process ({st_wall:.1f} s "
+                                                     f"measured), extrapolated to {spec.R}"}},
         "e2e": {"value": value, "unit": "cycles/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
         "notes": "fp64 numpy oracle on the host cores; no GPU involved",
@@ -932,7 +1087,9 @@ def run_ours(args):
     achieved = pbytes / prop_mean_s / 1e9
     w_once = propose_w_once_bytes(spec) / prop_mean_s / 1e9
     engine_used = ctx.last_engine()
-    engine_kernel = {"tcgen05": "propose_tc_kernel", "mma": "propose_mma_kernel"}.get(
+    m_tiles = (spec.R + 127) // 128
+    tc_kernel = "propose_tc_pair_kernel" if m_tiles >= 2 and m_tiles % 2 == 0 else "propose_tc_kernel"
+    engine_kernel = {"tcgen05": tc_kernel, "mma": "propose_mma_kernel"}.get(
         engine_used, "simt_bias_kernel")
     roofline = {"bound": "hbm", "kernel": f"propose phase ({engine_kernel})",
                 "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
@@ -952,13 +1109,7 @@ def run_ours(args):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
-        n_cpu = min(args.cpu_requests, spec.R)
-        h = host_arrays(x, rows=n_cpu)
-        for k in ("E", "W"):
-            h[k] = h[k].astype(np.float64)
-        est, desc, spent = oracle_sample_cycle(spec, h, n_cpu, seed)
-        cpu = {"value": 1.0 / est, "unit": "cycles/s", "cores": os.cpu_count(), "kind": "oracle",
-               "sample": desc, "cpu_seconds": spent}
+        cpu = oracle_baseline(spec, x, n_cycles=args.cpu_cycles)
 
     line = {
         "metric": METRIC, "value": value, "unit": "cycles/s",
@@ -968,11 +1119,8 @@ def run_ours(args):
         "wall_ms_per_step_incl_flush": wall * 1e3 / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": spec.dtype, "accumulate": "fp32", "data": "synthetic",
-        "config": {"workload": workload_label(spec), "R": spec.R, "gamma": spec.G, "V": spec.V,
-                   "rank": spec.r, "temperature": spec.temperature,
-                   "engine": f"{args.engine} -> {engine_used}",
-                   "verify_batch_B": B, "parallelism": f"replicas x{world}",
-                   "l2": "flushed between steps (512 MB write outside the events); inputs 1.2 GB"},
+        "config": cycle_config(spec, world),
+        "engine": f"{args.engine} -> {engine_used}", "verify_batch_B": B,
         "phases_ms": {"propose": statistics.mean(prop_ms), "schedule": statistics.mean(sch_ms),
                       "verify": statistics.mean(ver_ms),
                       "note": "separate pass through dsd_propose, dsd_schedule and dsd_verify, "
@@ -1006,10 +1154,11 @@ def main(argv=None):
                     choices=["highconc", "greedy", "sampled", "tiny", "overlap", "loss",
                              "confidence", "gated", "rnn", "candidates"])
     ap.add_argument("--engine", default="auto", choices=["auto", "simt", "mma", "tcgen05"])
-    ap.add_argument("--cpu-requests", type=int, default=128,
-                    help="requests in the CPU-baseline sample")
-    ap.add_argument("--ref-requests", type=int, default=16,
-                    help="requests per step of the reference (oracle) arm")
+    ap.add_argument("--cpu-cycles", type=int, default=2,
+                    help="timed full-batch oracle cycles of the in-run CPU baseline")
+    ap.add_argument("--ref-requests", type=int, default=0,
+                    help="reference arm: requests proposed and verified per step (default 0: "
+                         "the whole batch)")
     ap.add_argument("--blocks", type=int, default=0,
                     help="overlap workload: blocks N instead of 4096 (small profiling cases)")
     ap.add_argument("--no-e2e", action="store_true")

@@ -82,3 +82,29 @@ def test_tensor_report_of_the_high_concurrency_workload():
     assert rep["flops_per_phase"] == 2.0 * 256 * 256 * 151936 * 7
     assert abs(rep["achieved_tflops"] - rep["flops_per_phase"] / 1e-3 / 1e12) < 1e-9
     assert rep["frac"] == rep["achieved_tflops"] / rep["peak_tflops"]
+
+
+def test_oracle_pool_times_whole_cycles_and_matches_the_oracle():
+    # the CPU baseline's worker pool (spawned processes, single-threaded BLAS)
+    # runs the same oracle cycle as a direct call: same committed tokens
+    import numpy as np
+
+    from oracle import dsd_oracle as O
+    from semi_autoregressive_draft_gb300 import synth
+
+    spec = synth.scaled(synth.CYCLE_SPECS["greedy"], R=5, V=1032, ew_std=0.3, seed=3)
+    x = synth.cycle_inputs(spec, device="cpu")
+    h = {k: synth.to_numpy(v) for k, v in x.items() if isinstance(v, torch.Tensor)}
+    ref = O.cycle(h["U"], h["E"], h["W"], h["conf"], h["prev_tok"], h["P"], h["sps"],
+                  req_id=h["req_id"].astype(np.int64), temperature=0.0, seed=x["seed"])
+    want = int((ref["verify"]["accept_len"] + 1).sum())
+    with bench.OraclePool(spec, x, workers=2) as pool:
+        wall, tokens, busy = pool.cycle()
+        assert tokens == want
+        assert wall > 0 and busy > 0
+        est, st_wall = pool.single_thread(2)
+        assert est > 0 and st_wall > 0
+    line = bench.oracle_baseline(spec, x, n_cycles=1, n_single=2)
+    assert line["kind"] == "oracle" and line["cores"] >= 1 and line["value"] > 0
+    assert line["single_thread"]["cores"] == 1
+    assert "measured, not extrapolated" in line["sample"]
