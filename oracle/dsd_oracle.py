@@ -771,3 +771,40 @@ def calibration(conf, accept_len, n_bins=10):
                 n_tested=n_tested,
                 pos_pred=pos_pred / M if M else pos_pred,
                 pos_real=pos_real / M if M else pos_real)
+
+
+def auroc(conf, accept_len):
+    """Ranking quality of predicted survival ([READ] 5: the raw confidence
+    head's AUROC beside its reliability diagram).  Reading: over all (r, j)
+    positions, the score is the predicted prefix survival a[r, j] (fp64
+    product of the clamped confidences, as in calibration) and the label the
+    realised survival y[r, j] = (j < accept_len[r]).  AUROC is the
+    probability that a random positive outscores a random negative, a tie
+    counting one half (the Mann-Whitney statistic over all pairs).  With no
+    positive or no negative it is 0.5.  Written with a stable sort: within a
+    run of equal scores each positive meets the run's negatives as ties."""
+    c = np.clip(_f64(conf), 0.0, 1.0)
+    M, G = c.shape
+    L = np.asarray(accept_len).astype(np.int64)
+    a = survival(c).reshape(-1)
+    y = (np.arange(G)[None, :] < L[:, None]).reshape(-1)
+    n_pos = int(y.sum())
+    n_neg = y.size - n_pos
+    if n_pos == 0 or n_neg == 0:
+        return 0.5
+    order = np.argsort(a, kind="stable")
+    a_s, y_s = a[order], y[order]
+    u = 0.0
+    neg_below = 0            # negatives with a strictly smaller score
+    i = 0
+    while i < a_s.size:
+        k = i
+        while k < a_s.size and a_s[k] == a_s[i]:
+            k += 1
+        pos_run = int(y_s[i:k].sum())
+        neg_run = (k - i) - pos_run
+        u += pos_run * (neg_below + 0.5 * neg_run)
+        neg_below += neg_run
+        i = k
+    return u / (n_pos * n_neg)
+

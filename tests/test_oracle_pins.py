@@ -959,3 +959,54 @@ def test_candidates_follow_the_drafted_chain():
         assert np.allclose(out["cand_logit"][0, j], ell[ref], atol=1e-12)
         prev = int(out["tokens"][0, j])
         assert prev == ref[0]
+
+
+# ---------------------------------------------------------------------- AUROC
+
+def _auroc_brute(score, label):
+    pos = score[label]
+    neg = score[~label]
+    if pos.size == 0 or neg.size == 0:
+        return 0.5
+    gt = (pos[:, None] > neg[None, :]).sum()
+    eq = (pos[:, None] == neg[None, :]).sum()
+    return (gt + 0.5 * eq) / (pos.size * neg.size)
+
+
+def test_auroc_against_brute_force_pairs():
+    # every positive/negative pair counted by brute force (ties one half)
+    rng = np.random.default_rng(21)
+    for trial in range(20):
+        M, G = int(rng.integers(1, 12)), int(rng.integers(1, 8))
+        # few distinct confidence values so that ties occur
+        conf = rng.choice([0.5, 0.8, 0.9, 1.0], size=(M, G)) if trial % 2 else rng.uniform(0, 1, (M, G))
+        L = rng.integers(0, G + 1, size=M)
+        a = np.cumprod(np.clip(conf, 0, 1), axis=1).reshape(-1)
+        y = (np.arange(G)[None, :] < L[:, None]).reshape(-1)
+        assert abs(O.auroc(conf, L) - _auroc_brute(a, y)) <= 1e-12
+
+
+def test_auroc_closed_cases():
+    G = 4
+    conf = np.tile(np.array([0.9, 0.9, 0.9, 0.9]), (6, 1))
+    # perfect ranking: survival falls along the block, acceptance ends at 2 for all
+    assert O.auroc(conf, np.full(6, 2)) == 1.0
+    # every score tied: one half
+    assert O.auroc(np.ones((5, G)), np.array([0, 1, 2, 3, 4])) == 0.5
+    # only positives or only negatives: one half by convention
+    assert O.auroc(conf, np.full(6, G)) == 0.5
+    assert O.auroc(conf, np.zeros(6, dtype=int)) == 0.5
+    # reversed ranking is 0: the high-survival position is the negative one
+    conf2 = np.array([[1.0, 1.0], [0.2, 1.0]])
+    # scores a = [1, 1, .2, .2]; labels: request 0 accepts nothing, request 1 all
+    assert O.auroc(conf2, np.array([0, 2])) == 0.0
+
+
+def test_auroc_matches_a_library_implementation():
+    metrics = pytest.importorskip("sklearn.metrics")
+    rng = np.random.default_rng(22)
+    conf = rng.beta(6, 2, size=(300, 7))
+    L = rng.integers(0, 8, size=300)
+    a = np.cumprod(conf, axis=1).reshape(-1)
+    y = (np.arange(7)[None, :] < L[:, None]).reshape(-1)
+    assert abs(O.auroc(conf, L) - metrics.roc_auc_score(y, a)) <= 1e-12
