@@ -485,6 +485,29 @@ int dsd_threshold_keep(dsd_ctx* ctx, int R, const float* conf, float threshold, 
                        void* stream);
 
 /*
+ * dsd_auroc -- ranking quality of predicted survival ([READ] 5: the raw
+ * confidence head's AUROC, quoted beside its reliability diagram).
+ *
+ * conf [M, gamma] f32 and accept_len [M] i32 as for dsd_calibration.  Over
+ * all M * gamma positions the score is a = prod_{i <= j} clamp(conf[r, i])
+ * (fp64, the same product as dsd_calibration) and the label
+ * y = (j < accept_len[r]).  *auroc (one device double) receives the
+ * probability that a random positive outscores a random negative, a tie
+ * counting one half (the Mann-Whitney statistic; 0.5 when a class is empty),
+ * computed exactly: the positions are sorted twice (a bitonic network on
+ * keys bits(a) << 1 | label) and the negatives before each positive counted.
+ * scratch: caller-owned device memory of at least
+ * dsd_auroc_scratch_bytes(M, gamma) bytes, 256-byte aligned (the library
+ * allocates nothing); its contents are overwritten.  M * gamma <= 2^30.
+ * Errors: DSD_ERR_ARG (NULL or negative M), DSD_ERR_ALIGN, DSD_ERR_SHAPE
+ * (scratch too small, M * gamma too large) before any launch; accept_len
+ * outside 0..gamma or a non-finite confidence set the device status.
+ */
+size_t dsd_auroc_scratch_bytes(int M, int gamma);
+int dsd_auroc(dsd_ctx* ctx, int M, const float* conf, const int32_t* accept_len, void* scratch,
+              size_t scratch_bytes, double* auroc, void* stream);
+
+/*
  * dsd_calibration -- calibration of predicted survival against realised
  * acceptance ([READ] 3.1: per-step error and cumulative-product bias of the
  * confidence head; [READ] 5: reliability diagram, ECE).

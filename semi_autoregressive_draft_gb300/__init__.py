@@ -38,6 +38,7 @@ EXPORTED = [
     "dsd_propose_noalloc", "dsd_loss_forward", "dsd_confidence_head", "dsd_threshold_keep",
     "dsd_calibration", "dsd_propose_gated", "dsd_verify_gated", "dsd_propose_candidates",
     "dsd_propose_rnn", "dsd_verify_rnn", "dsd_gumbel_noise", "dsd_wait_selftest",
+    "dsd_auroc", "dsd_auroc_scratch_bytes",
 ]
 
 
@@ -98,6 +99,8 @@ def load_library(path: str | None = None):
                                   _P, _P, _P]),
         "dsd_gumbel_noise": (_I, [_P, _P, _I, _P]),
         "dsd_wait_selftest": (_I, [_P, ctypes.c_uint32, _P, _P]),
+        "dsd_auroc_scratch_bytes": (ctypes.c_size_t, [_I, _I]),
+        "dsd_auroc": (_I, [_P, _I, _P, _P, _P, ctypes.c_size_t, _P, _P]),
         "dsd_propose_rnn": (_I, [_P, _I, _P, _P, _P, _P, _I, _P, _P, _P, _P, _F, _U64, _P, _P,
                                  _P, _P, _P, _P]),
         "dsd_verify_rnn": (_I, [_P, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _F, _U64,
@@ -289,6 +292,19 @@ def dsd_calibration(ctx, M, conf, accept_len, n_bins, bins, pos, metrics, stream
     _check(ctx, load_library().dsd_calibration(ctx, M, _ptr(conf), _ptr(accept_len), n_bins,
                                                _ptr(bins), _ptr(pos), _ptr(metrics),
                                                _stream(stream, device)))
+
+
+def dsd_auroc_scratch_bytes(M, gamma):
+    return int(load_library().dsd_auroc_scratch_bytes(int(M), int(gamma)))
+
+
+def dsd_auroc(ctx, M, conf, accept_len, scratch, auroc, stream=None, device=0):
+    """AUROC of predicted survival against realised survival, into the device
+    double `auroc`; `scratch` is a caller-owned uint8 device tensor of at least
+    dsd_auroc_scratch_bytes(M, gamma) bytes."""
+    nbytes = scratch.numel() * scratch.element_size() if isinstance(scratch, torch.Tensor) else 0
+    _check(ctx, load_library().dsd_auroc(ctx, int(M), _ptr(conf), _ptr(accept_len), _ptr(scratch),
+                                         nbytes, _ptr(auroc), _stream(stream, device)))
 
 
 def dsd_wait_selftest(ctx, poll_limit, roles_out=None, stream=None, device=0):
@@ -592,6 +608,20 @@ class Context:
         dsd_calibration(self.handle, conf.shape[0], conf, accept_len, n_bins, o["bins"], o["pos"],
                         o["metrics"], stream, self.device)
         return o
+
+    def auroc(self, conf, accept_len, scratch=None, stream=None):
+        """AUROC of predicted survival against realised survival (one device
+        double).  `scratch` (uint8 device tensor) may be passed to reuse it;
+        otherwise it is allocated here, by torch, outside the library."""
+        self._check_in("conf", conf, torch.float32)
+        self._check_in("accept_len", accept_len, torch.int32)
+        M = conf.shape[0]
+        need = dsd_auroc_scratch_bytes(M, self.gamma)
+        if scratch is None or scratch.numel() < need:
+            scratch = torch.empty(need, dtype=torch.uint8, device=self._dev)
+        out = self._empty((1,), torch.float64)
+        dsd_auroc(self.handle, M, conf, accept_len, scratch, out, stream, self.device)
+        return out
 
     def loss_forward(self, U, E, W, prev_tok, P, target, conf_logit, ce_alpha=0.1, l1_alpha=0.9,
                      conf_alpha=1.0, decay=4.0, rows=True, out=None, stream=None):

@@ -335,4 +335,239 @@ cudaError_t launch_calibration(const Ctx& ctx, const CalArgs& a, cudaStream_t s)
   return cudaGetLastError();
 }
 
+
+// ---------------------------------------------------------------------------
+// AUROC of predicted survival against realised survival ("DSpark 论文精读"
+// 5: the raw head's ranking quality beside its reliability diagram).  Over
+// all (r, j) positions the score is a[r, j] = prod_{i <= j} clamp(conf[r, i])
+// (fp64, the same sequential product as dsd_calibration) and the label
+// y = (j < accept_len[r]).  AUROC = (#pairs positive > negative + 1/2 #ties)
+// / (P N), 0.5 when a class is empty.
+//
+// Sorting instead of binning keeps it exact: each position becomes the key
+// bits(a) << 1 | label bit (a >= 0, so its bits order like its value), the
+// caller's scratch holds the keys padded to a power of two with all-ones
+// keys, and a bitonic network sorts them in place.  With the label bit 0 for
+// positives, a positive is preceded within its run of equal scores only by
+// positives, so the negatives before it are those with a smaller score
+// (U_low); with the bit reversed, those with a smaller or equal score
+// (U_high).  U_low + U_high = 2 (#greater + 1/2 #ties) over all pairs.  The
+// counts are exact integers; the division is fp64.
+// ---------------------------------------------------------------------------
+namespace {
+
+constexpr int kAucTile = 1024;       // keys per shared-memory bitonic tile
+constexpr int kAucThreads = 512;     // threads of the tile kernels (two keys each)
+
+struct AucScratch {
+  unsigned long long* keys;    // [n_pad]
+  unsigned int* bneg;          // [n_pad / kAucTile] negatives per tile, then their exclusive scan
+  unsigned long long* acc;     // [4]: U (this ordering), P, N, U_low
+};
+
+__global__ void auc_keys_kernel(const float* conf, const int32_t* accept_len, int M, int gamma,
+                                int n_pad, int pos_bit, unsigned long long* keys,
+                                unsigned long long* acc, int* status) {
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n_pad; i += gridDim.x * blockDim.x) {
+    if (i >= M * gamma) {
+      keys[i] = ~0ull;
+      continue;
+    }
+    const int r = i / gamma, j = i - r * gamma;
+    int L = accept_len[r];
+    if (L < 0 || L > gamma) {
+      set_status(status, kErrArg);
+      L = L < 0 ? 0 : gamma;
+    }
+    double a = 1.0;
+    for (int t = 0; t <= j; ++t) {
+      float cf = conf[(size_t)r * gamma + t];
+      if (!isfinite(cf)) {
+        set_status(status, kErrNonfinite);
+        cf = 0.f;
+      }
+      a *= (double)fminf(fmaxf(cf, 0.f), 1.f);
+    }
+    const int y = j < L ? 1 : 0;
+    const unsigned long long lbit = (unsigned long long)(y ? pos_bit : 1 - pos_bit);
+    keys[i] = ((unsigned long long)__double_as_longlong(a) << 1) | lbit;
+    if (pos_bit == 0) atomicAdd(&acc[y ? 1 : 2], 1ull);   // P, N: counted once
+  }
+}
+
+// One comparator of the bitonic network at stage k, distance j: element i1
+// and i1 + j, ascending where bit k of i1 is clear.
+__device__ __forceinline__ void auc_cmp(unsigned long long& x, unsigned long long& y, bool asc) {
+  if ((x > y) == asc) {
+    const unsigned long long t = x;
+    x = y;
+    y = t;
+  }
+}
+
+// Stage k, every distance j < kAucTile down to 1 (all of stages k <= kAucTile
+// when sort_tile is set), within tiles of kAucTile keys in shared memory.
+__global__ void __launch_bounds__(kAucThreads) auc_tile_kernel(unsigned long long* keys, int k,
+                                                               int sort_tile) {
+  __shared__ unsigned long long sk[kAucTile];
+  const int base = blockIdx.x * kAucTile, t = threadIdx.x;
+  sk[t] = keys[base + t];
+  sk[t + kAucThreads] = keys[base + t + kAucThreads];
+  __syncthreads();
+  const int k_first = sort_tile ? 2 : k, k_last = sort_tile ? kAucTile : k;
+  for (int kk = k_first; kk <= k_last; kk <<= 1) {
+    for (int j = (kk >> 1) < (kAucTile >> 1) ? (kk >> 1) : (kAucTile >> 1); j >= 1; j >>= 1) {
+      const int i1 = 2 * j * (t / j) + (t % j);
+      auc_cmp(sk[i1], sk[i1 + j], ((base + i1) & kk) == 0);
+      __syncthreads();
+    }
+  }
+  keys[base + t] = sk[t];
+  keys[base + t + kAucThreads] = sk[t + kAucThreads];
+}
+
+// Stage k, one distance j >= kAucTile over the whole array.
+__global__ void auc_global_kernel(unsigned long long* keys, int n_pad, int k, int j) {
+  for (int t = blockIdx.x * blockDim.x + threadIdx.x; t < n_pad / 2; t += gridDim.x * blockDim.x) {
+    const int i1 = 2 * j * (t / j) + (t % j);
+    unsigned long long x = keys[i1], y = keys[i1 + j];
+    auc_cmp(x, y, (i1 & k) == 0);
+    keys[i1] = x;
+    keys[i1 + j] = y;
+  }
+}
+
+__device__ __forceinline__ bool auc_is_neg(unsigned long long key, int pos_bit) {
+  return key != ~0ull && (int)(key & 1ull) != pos_bit;
+}
+
+// Negatives per tile of the sorted keys.
+__global__ void __launch_bounds__(kAucThreads) auc_count_kernel(const unsigned long long* keys,
+                                                                int pos_bit, unsigned int* bneg) {
+  const int base = blockIdx.x * kAucTile, t = threadIdx.x;
+  const int n = (auc_is_neg(keys[base + t], pos_bit) ? 1 : 0) +
+                (auc_is_neg(keys[base + t + kAucThreads], pos_bit) ? 1 : 0);
+  const int tot = __syncthreads_count(n & 1) + 2 * __syncthreads_count(n >> 1);
+  if (t == 0) bneg[blockIdx.x] = (unsigned int)tot;
+}
+
+// Exclusive scan of the tiles' negative counts (one CTA).
+__global__ void __launch_bounds__(1024) auc_scan_kernel(unsigned int* bneg, int n_tiles) {
+  __shared__ unsigned long long part[1024];
+  const int t = threadIdx.x;
+  const int per = (n_tiles + 1023) / 1024;
+  unsigned long long s = 0ull;
+  for (int q = 0; q < per; ++q) {
+    const int i = t * per + q;
+    if (i < n_tiles) s += bneg[i];
+  }
+  part[t] = s;
+  __syncthreads();
+  for (int o = 1; o < 1024; o <<= 1) {
+    const unsigned long long v = t >= o ? part[t - o] : 0ull;
+    __syncthreads();
+    part[t] += v;
+    __syncthreads();
+  }
+  unsigned long long off = t > 0 ? part[t - 1] : 0ull;
+  for (int q = 0; q < per; ++q) {
+    const int i = t * per + q;
+    if (i < n_tiles) {
+      const unsigned int c = bneg[i];
+      bneg[i] = (unsigned int)off;
+      off += c;
+    }
+  }
+}
+
+// Sum over positives of the negatives before them in the sorted order.
+__global__ void __launch_bounds__(kAucThreads) auc_sum_kernel(const unsigned long long* keys,
+                                                              int pos_bit,
+                                                              const unsigned int* bneg_off,
+                                                              unsigned long long* acc) {
+  __shared__ unsigned int wsum[kAucThreads / 32];
+  const int base = blockIdx.x * kAucTile, t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  // thread t holds keys base + 2t and base + 2t + 1 (consecutive)
+  const unsigned long long k0 = keys[base + 2 * t], k1 = keys[base + 2 * t + 1];
+  const unsigned int n0 = auc_is_neg(k0, pos_bit) ? 1u : 0u, n1 = auc_is_neg(k1, pos_bit) ? 1u : 0u;
+  unsigned int incl = n0 + n1;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const unsigned int v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  if (lane == 31) wsum[warp] = incl;
+  __syncthreads();
+  unsigned int woff = 0;
+  for (int w = 0; w < warp; ++w) woff += wsum[w];
+  const unsigned long long before = (unsigned long long)bneg_off[blockIdx.x] + woff + incl - n0 - n1;
+  unsigned long long u = 0ull;
+  if (k0 != ~0ull && !n0) u += before;            // a positive: the negatives before it
+  if (k1 != ~0ull && !n1) u += before + n0;
+  for (int o = 16; o >= 1; o >>= 1) u += __shfl_xor_sync(0xffffffffu, u, o);
+  if (lane == 0 && u) atomicAdd(&acc[0], u);
+}
+
+__global__ void auc_finish_kernel(unsigned long long* acc, int phase, double* auroc) {
+  if (threadIdx.x != 0 || blockIdx.x != 0) return;
+  if (phase == 0) {            // U_low done: keep it, clear the running sum
+    acc[3] = acc[0];
+    acc[0] = 0ull;
+    return;
+  }
+  const double P = (double)acc[1], N = (double)acc[2];
+  *auroc = (P == 0.0 || N == 0.0) ? 0.5 : (0.5 * ((double)acc[3] + (double)acc[0])) / (P * N);
+}
+
+}  // namespace
+
+size_t auroc_npad(int M, int gamma) {
+  const long long n = (long long)M * gamma;
+  long long p = kAucTile;
+  while (p < n) p <<= 1;
+  return (size_t)p;
+}
+
+size_t auroc_scratch_bytes(int M, int gamma) {
+  const size_t n_pad = auroc_npad(M, gamma);
+  return n_pad * 8 + ((n_pad / kAucTile * 4 + 255) / 256) * 256 + 64;
+}
+
+cudaError_t launch_auroc(const Ctx& ctx, int M, const float* conf, const int32_t* accept_len,
+                         void* scratch, double* auroc, cudaStream_t s) {
+  const int gamma = ctx.cfg.gamma;
+  const int n_pad = (int)auroc_npad(M, gamma);
+  const int n_tiles = n_pad / kAucTile;
+  unsigned char* base = static_cast<unsigned char*>(scratch);
+  AucScratch w;
+  w.keys = reinterpret_cast<unsigned long long*>(base);
+  w.bneg = reinterpret_cast<unsigned int*>(base + (size_t)n_pad * 8);
+  w.acc = reinterpret_cast<unsigned long long*>(base + (size_t)n_pad * 8 +
+                                                ((size_t)n_tiles * 4 + 255) / 256 * 256);
+  cudaError_t e = cudaMemsetAsync(w.acc, 0, 4 * sizeof(unsigned long long), s);
+  if (e != cudaSuccess) return e;
+  const int grid_e = ctx.num_sms * 8;
+  for (int pos_bit = 0; pos_bit < 2; ++pos_bit) {
+    auc_keys_kernel<<<grid_e, 256, 0, s>>>(conf, accept_len, M, gamma, n_pad, pos_bit, w.keys,
+                                           w.acc, ctx.ws.status);
+    auc_tile_kernel<<<n_tiles, kAucThreads, 0, s>>>(w.keys, kAucTile, 1);
+    count_launch(ctx, 2);
+    for (int k = 2 * kAucTile; k <= n_pad; k <<= 1) {
+      for (int j = k >> 1; j >= kAucTile; j >>= 1) {
+        auc_global_kernel<<<grid_e, 256, 0, s>>>(w.keys, n_pad, k, j);
+        count_launch(ctx);
+      }
+      auc_tile_kernel<<<n_tiles, kAucThreads, 0, s>>>(w.keys, k, 0);
+      count_launch(ctx);
+    }
+    auc_count_kernel<<<n_tiles, kAucThreads, 0, s>>>(w.keys, pos_bit, w.bneg);
+    auc_scan_kernel<<<1, 1024, 0, s>>>(w.bneg, n_tiles);
+    auc_sum_kernel<<<n_tiles, kAucThreads, 0, s>>>(w.keys, pos_bit, w.bneg, w.acc);
+    auc_finish_kernel<<<1, 32, 0, s>>>(w.acc, pos_bit, auroc);
+    count_launch(ctx, 4);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
 }  // namespace dsd

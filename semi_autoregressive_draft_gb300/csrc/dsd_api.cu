@@ -8,6 +8,8 @@
 #include <cmath>
 #include <new>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "../../include/dsd.h"
 #include "dsd_common.cuh"
 #include "dsd_internal.h"
@@ -17,6 +19,16 @@ using namespace dsd;
 struct dsd_ctx : public dsd::Ctx {};
 
 namespace {
+
+// One NVTX range per public call (named after the call), so a profiler's
+// timeline shows which API call launched which kernels.  Without a tool
+// attached a push or pop is a call through an empty hook.
+struct Trace {
+  explicit Trace(const char* name) { nvtxRangePushA(name); }
+  ~Trace() { nvtxRangePop(); }
+  Trace(const Trace&) = delete;
+  Trace& operator=(const Trace&) = delete;
+};
 
 int fail(dsd_ctx* ctx, int code, const char* fmt, ...) {
   if (ctx) {
@@ -207,6 +219,7 @@ static __global__ void gumbel_noise_kernel(const uint32_t* words, float* out, in
 }
 
 int dsd_gumbel_noise(const uint32_t* words, float* out, int n, void* stream) {
+  Trace trace_("dsd_gumbel_noise");
   if (n < 0 || (n > 0 && (!words || !out))) return DSD_ERR_ARG;
   if (n == 0) return DSD_OK;
   const int grid = (n + 255) / 256 < 4096 ? (n + 255) / 256 : 4096;
@@ -215,6 +228,7 @@ int dsd_gumbel_noise(const uint32_t* words, float* out, int n, void* stream) {
 }
 
 int dsd_wait_selftest(dsd_ctx* ctx, uint32_t poll_limit, int32_t* roles_out, void* stream) {
+  Trace trace_("dsd_wait_selftest");
   int rc = check_ctx(ctx);
   if (rc) return rc;
   if (poll_limit == 0 || poll_limit > (1u << 20))
@@ -226,6 +240,7 @@ int dsd_wait_selftest(dsd_ctx* ctx, uint32_t poll_limit, int32_t* roles_out, voi
 }
 
 int dsd_sync_status(dsd_ctx* ctx, void* stream) {
+  Trace trace_("dsd_sync_status");
   int rc = check_ctx(ctx);
   if (rc) return rc;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -316,12 +331,14 @@ int dsd_propose(dsd_ctx* ctx, int R, const void* U, const void* E, const void* W
                 const float* conf, const int32_t* prev_tok, const uint32_t* req_id,
                 float temperature, uint64_t seed, int32_t* tokens, float* lse_q,
                 float* logit_at_tok, float* survival, void* stream) {
+  Trace trace_("dsd_propose");
   return propose_impl(ctx, R, U, E, W, conf, prev_tok, req_id, temperature, seed, tokens, lse_q,
                       logit_at_tok, survival, nullptr, 0, nullptr, nullptr, stream);
 }
 
 int dsd_schedule(dsd_ctx* ctx, int R, const float* survival, const float* sps, int n_sps,
                  int32_t* keep_len, float* theta_B, void* stream) {
+  Trace trace_("dsd_schedule");
   int rc = check_ctx(ctx);
   if (rc) return rc;
   if ((rc = check_R(ctx, R))) return rc;
@@ -389,6 +406,7 @@ int dsd_verify(dsd_ctx* ctx, int R, const void* P, const void* U, const void* E,
                const float* logit_at_tok, const int32_t* keep_len, const uint32_t* req_id,
                float temperature, uint64_t seed, int32_t* accept_len, int32_t* next_token,
                void* stream) {
+  Trace trace_("dsd_verify");
   return verify_impl(ctx, R, P, U, E, W, prev_tok, tokens, lse_q, logit_at_tok, keep_len, req_id,
                      temperature, seed, accept_len, next_token, nullptr, stream);
 }
@@ -398,6 +416,7 @@ int dsd_verify_rnn(dsd_ctx* ctx, int R, const void* P, const void* U, const void
                    const int32_t* tokens, const float* lse_q, const float* logit_at_tok,
                    const int32_t* keep_len, const uint32_t* req_id, float temperature,
                    uint64_t seed, int32_t* accept_len, int32_t* next_token, void* stream) {
+  Trace trace_("dsd_verify_rnn");
   int rc = check_ctx(ctx);
   if (rc) return rc;
   if (R > 0 && temperature > 0.f && !rnn_rep)
@@ -411,6 +430,7 @@ int dsd_verify_gated(dsd_ctx* ctx, int R, const void* P, const void* U, const vo
                      const int32_t* tokens, const float* lse_q, const float* logit_at_tok,
                      const int32_t* keep_len, const uint32_t* req_id, float temperature,
                      uint64_t seed, int32_t* accept_len, int32_t* next_token, void* stream) {
+  Trace trace_("dsd_verify_gated");
   int rc = check_ctx(ctx);
   if (rc) return rc;
   if (R > 0 && temperature > 0.f && !gated_rep)
@@ -478,6 +498,7 @@ int dsd_propose_gated(dsd_ctx* ctx, int R, const void* U, const void* E, const v
                       const int32_t* prev_tok, const uint32_t* req_id, float temperature,
                       uint64_t seed, int32_t* tokens, float* lse_q, float* logit_at_tok,
                       float* survival, float* gated_rep, void* stream) {
+  Trace trace_("dsd_propose_gated");
   if (ctx && !W_g) return fail(ctx, DSD_ERR_ARG, "dsd_propose_gated: W_g is NULL");
   return propose_hidden_head(ctx, "dsd_propose_gated", R, U, E, W, h, H, W_g, nullptr, conf,
                              prev_tok, req_id, temperature, seed, tokens, lse_q, logit_at_tok,
@@ -489,6 +510,7 @@ int dsd_propose_rnn(dsd_ctx* ctx, int R, const void* U, const void* E, const voi
                     const int32_t* prev_tok, const uint32_t* req_id, float temperature,
                     uint64_t seed, int32_t* tokens, float* lse_q, float* logit_at_tok,
                     float* survival, float* rnn_rep, void* stream) {
+  Trace trace_("dsd_propose_rnn");
   if (ctx && !W_rnn) return fail(ctx, DSD_ERR_ARG, "dsd_propose_rnn: W_rnn is NULL");
   return propose_hidden_head(ctx, "dsd_propose_rnn", R, U, E, W, h, H, nullptr, W_rnn, conf,
                              prev_tok, req_id, temperature, seed, tokens, lse_q, logit_at_tok,
@@ -500,6 +522,7 @@ int dsd_cycle(dsd_ctx* ctx, int R, const void* U, const void* E, const void* W, 
               int n_sps, float temperature, uint64_t seed, int32_t* tokens, float* lse_q,
               float* logit_at_tok, float* survival, int32_t* keep_len, float* theta_B,
               int32_t* accept_len, int32_t* next_token, void* stream) {
+  Trace trace_("dsd_cycle");
   // the schedule depends on the confidences only: it runs in extra CTAs of
   // the proposal's finalize launch
   int rc = check_ctx(ctx);
@@ -525,6 +548,7 @@ int dsd_cycle_host(dsd_ctx* ctx, int R, const void* U_host, const void* E, const
                    const uint32_t* req_id_host, const void* P_host, const float* sps, int n_sps,
                    float temperature, uint64_t seed, int32_t* tokens_host, int32_t* keep_len_host,
                    int32_t* accept_len_host, int32_t* next_token_host, void* stream) {
+  Trace trace_("dsd_cycle_host");
   int rc = check_ctx(ctx);
   if (rc) return rc;
   if ((rc = check_R(ctx, R))) return rc;
@@ -610,6 +634,7 @@ int dsd_cycle_host(dsd_ctx* ctx, int R, const void* U_host, const void* E, const
 int dsd_overlap(dsd_ctx* ctx, int N, const void* P_logits, const void* Q_logits,
                 const int32_t* valid_len, float* a, float* l1, float* tau, float* accept_rate,
                 float* mean_tau, void* stream) {
+  Trace trace_("dsd_overlap");
   int rc = check_ctx(ctx);
   if (rc) return rc;
   if (N < 0) return fail(ctx, DSD_ERR_ARG, "N = %d < 0", N);
@@ -642,6 +667,7 @@ int dsd_loss_forward(dsd_ctx* ctx, int B, const void* U, const void* E, const vo
                      const int32_t* prev_tok, const void* P, const int32_t* target,
                      const float* conf_logit, float ce_alpha, float l1_alpha, float conf_alpha,
                      float decay, float* row_out, float* losses, void* stream) {
+  Trace trace_("dsd_loss_forward");
   int rc = check_ctx(ctx);
   if (rc) return rc;
   if ((rc = check_R(ctx, B))) return rc;
@@ -693,6 +719,7 @@ int dsd_loss_forward(dsd_ctx* ctx, int B, const void* U, const void* E, const vo
 int dsd_confidence_head(dsd_ctx* ctx, int R, int H, const void* h, const void* E, const void* w_c,
                         float b_c, const int32_t* prev_tok, const int32_t* tokens, float* conf,
                         float* survival, void* stream) {
+  Trace trace_("dsd_confidence_head");
   int rc = check_ctx(ctx);
   if (rc) return rc;
   if (R < 0) return fail(ctx, DSD_ERR_ARG, "R = %d < 0", R);
@@ -727,6 +754,7 @@ int dsd_confidence_head(dsd_ctx* ctx, int R, int H, const void* h, const void* E
 
 int dsd_threshold_keep(dsd_ctx* ctx, int R, const float* conf, float threshold, int32_t* keep_len,
                        void* stream) {
+  Trace trace_("dsd_threshold_keep");
   int rc = check_ctx(ctx);
   if (rc) return rc;
   if (R < 0) return fail(ctx, DSD_ERR_ARG, "R = %d < 0", R);
@@ -741,6 +769,7 @@ int dsd_threshold_keep(dsd_ctx* ctx, int R, const float* conf, float threshold, 
 
 int dsd_calibration(dsd_ctx* ctx, int M, const float* conf, const int32_t* accept_len, int n_bins,
                     float* bins, float* pos, float* metrics, void* stream) {
+  Trace trace_("dsd_calibration");
   int rc = check_ctx(ctx);
   if (rc) return rc;
   if (M < 0) return fail(ctx, DSD_ERR_ARG, "M = %d < 0", M);
@@ -763,11 +792,36 @@ int dsd_calibration(dsd_ctx* ctx, int M, const float* conf, const int32_t* accep
   return DSD_OK;
 }
 
+size_t dsd_auroc_scratch_bytes(int M, int gamma) {
+  if (M < 0 || gamma < 1 || (long long)M * gamma > (1LL << 30)) return 0;
+  return dsd::auroc_scratch_bytes(M, gamma);
+}
+
+int dsd_auroc(dsd_ctx* ctx, int M, const float* conf, const int32_t* accept_len, void* scratch,
+              size_t scratch_bytes, double* auroc, void* stream) {
+  Trace trace_("dsd_auroc");
+  int rc = check_ctx(ctx);
+  if (rc) return rc;
+  if (M < 0) return fail(ctx, DSD_ERR_ARG, "M = %d < 0", M);
+  if ((long long)M * ctx->cfg.gamma > (1LL << 30)) return fail(ctx, DSD_ERR_SHAPE, "M * gamma > 2^30");
+  if (!auroc || !scratch || (M > 0 && (!conf || !accept_len)))
+    return fail(ctx, DSD_ERR_ARG, "dsd_auroc: NULL argument");
+  if (((uintptr_t)scratch & 255u) != 0) return fail(ctx, DSD_ERR_ALIGN, "scratch not 256-byte aligned");
+  const size_t need = dsd::auroc_scratch_bytes(M, ctx->cfg.gamma);
+  if (scratch_bytes < need)
+    return fail(ctx, DSD_ERR_SHAPE, "scratch of %zu bytes, %zu needed", scratch_bytes, need);
+  cudaError_t e = dsd::launch_auroc(*ctx, M, conf, accept_len, scratch, auroc,
+                                    static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "auroc launch");
+  return DSD_OK;
+}
+
 int dsd_propose_candidates(dsd_ctx* ctx, int R, const void* U, const void* E, const void* W,
                            const float* conf, const int32_t* prev_tok, const uint32_t* req_id,
                            float temperature, uint64_t seed, int32_t* tokens, float* lse_q,
                            float* logit_at_tok, float* survival, int32_t* cand_tok,
                            float* cand_logit, void* stream) {
+  Trace trace_("dsd_propose_candidates");
   int rc = check_ctx(ctx);
   if (rc) return rc;
   if ((rc = check_R(ctx, R))) return rc;

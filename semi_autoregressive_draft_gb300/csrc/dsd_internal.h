@@ -187,6 +187,9 @@ struct CalArgs {
   float* metrics;
 };
 cudaError_t launch_calibration(const Ctx& ctx, const CalArgs& a, cudaStream_t s);
+size_t auroc_scratch_bytes(int M, int gamma);
+cudaError_t launch_auroc(const Ctx& ctx, int M, const float* conf, const int32_t* accept_len,
+                         void* scratch, double* auroc, cudaStream_t s);
 
 struct LossArgs {
   int B, V, rank, gamma, bias_at_first;

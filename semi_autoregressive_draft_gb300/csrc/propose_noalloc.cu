@@ -25,6 +25,8 @@
 #include <mutex>
 #include <string.h>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "../../include/dsd.h"
 #include "dsd_internal.h"
 
@@ -88,12 +90,33 @@ bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 
 }  // namespace
 
+static int propose_noalloc_impl(int V, int rank, int gamma, int dtype, int act, int bias_at_first,
+                                int R, const void* U, const void* E, const void* W,
+                                const float* conf, const int32_t* prev_tok, const uint32_t* req_id,
+                                float temperature, uint64_t seed, int32_t* tokens, float* lse_q,
+                                float* logit_at_tok, float* survival, int32_t* status,
+                                void* stream);
+
 extern "C" int dsd_propose_noalloc(int V, int rank, int gamma, int dtype, int act,
                                    int bias_at_first, int R, const void* U, const void* E,
                                    const void* W, const float* conf, const int32_t* prev_tok,
                                    const uint32_t* req_id, float temperature, uint64_t seed,
                                    int32_t* tokens, float* lse_q, float* logit_at_tok,
                                    float* survival, int32_t* status, void* stream) {
+  nvtxRangePushA("dsd_propose_noalloc");
+  const int rc = propose_noalloc_impl(V, rank, gamma, dtype, act, bias_at_first, R, U, E, W, conf,
+                                      prev_tok, req_id, temperature, seed, tokens, lse_q,
+                                      logit_at_tok, survival, status, stream);
+  nvtxRangePop();
+  return rc;
+}
+
+static int propose_noalloc_impl(int V, int rank, int gamma, int dtype, int act, int bias_at_first,
+                                int R, const void* U, const void* E, const void* W,
+                                const float* conf, const int32_t* prev_tok, const uint32_t* req_id,
+                                float temperature, uint64_t seed, int32_t* tokens, float* lse_q,
+                                float* logit_at_tok, float* survival, int32_t* status,
+                                void* stream) {
   if (V < 8 || V % 8 != 0) return DSD_ERR_ALIGN;
   const bool rank_ok = (rank % 64 == 0 && rank <= 256) || (rank > 0 && rank <= 64 && rank % 8 == 0);
   if (!rank_ok || gamma < 1 || gamma > dsd::kMaxGamma || R < 0) return DSD_ERR_SHAPE;

@@ -165,3 +165,50 @@ def test_calibration_page_example_and_edges(dsd):
     ctx.calibration(conf, bad, 10)
     assert ctx.sync_status() == -1
     ctx.close()
+
+
+# ---------------------------------------------------------------------- AUROC
+# Both sides form the survivals as the same fp64 products of the same fp32
+# confidences and count pairs exactly (integers); only the final division is
+# floating point, so the results agree to fp64 rounding.
+AUC_TOL = 1e-12
+
+
+@pytest.mark.parametrize("M,G,seed", [(1, 7, 60), (200, 7, 61), (5000, 7, 62), (40000, 7, 63),
+                                      (37, 1, 64), (1500, 16, 65)])
+def test_auroc_matches_the_oracle(dsd, M, G, seed):
+    # n = M G from 7 (one tile) through 280,000 (a 2^19-key bitonic network)
+    x = synth.calibration_inputs(M, G, seed=seed, device=DEV)
+    ctx = dsd.Context(1024, 64, G, 4, dtype="f32")
+    got = float(ctx.auroc(x["conf"], x["accept_len"]).cpu()[0])
+    assert ctx.sync_status() == 0
+    ref = O.auroc(x["conf"].cpu().numpy(), x["accept_len"].cpu().numpy())
+    assert abs(got - ref) <= AUC_TOL, (got, ref)
+    ctx.close()
+
+
+def test_auroc_ties_edges_and_scratch(dsd):
+    rng = np.random.default_rng(66)
+    G = 5
+    ctx = dsd.Context(1024, 64, G, 4, dtype="f32")
+    # confidences from a few values: many equal survivals across requests
+    conf = torch.as_tensor(rng.choice([0.5, 0.8, 1.0], size=(3000, G)).astype(np.float32),
+                           device=DEV)
+    L = torch.as_tensor(rng.integers(0, G + 1, size=3000).astype(np.int32), device=DEV)
+    got = float(ctx.auroc(conf, L).cpu()[0])
+    assert abs(got - O.auroc(conf.cpu().numpy(), L.cpu().numpy())) <= AUC_TOL
+    # one class only: one half
+    full = torch.full((50,), G, dtype=torch.int32, device=DEV)
+    assert float(ctx.auroc(conf[:50], full).cpu()[0]) == 0.5
+    # a caller-owned scratch reused across calls, then one that is too small
+    need = dsd.dsd_auroc_scratch_bytes(3000, G)
+    scratch = torch.empty(need, dtype=torch.uint8, device=DEV)
+    out = torch.empty(1, dtype=torch.float64, device=DEV)
+    for _ in range(2):
+        dsd.dsd_auroc(ctx.handle, 3000, conf, L, scratch, out)
+        assert float(out.cpu()[0]) == got
+    with pytest.raises(dsd.DsdError) as ei:
+        dsd.dsd_auroc(ctx.handle, 3000, conf, L, scratch[: need - 256], out)
+    assert ei.value.code == -4
+    assert ctx.sync_status() == 0
+    ctx.close()
