@@ -711,16 +711,16 @@ def run_hidden_head(args, dsd, synth, dev, world, head):
     """A head that reads the backbone's hidden state -- the gated Markov head
     (head = "gated") or the RNN head ("rnn") -- proposing on the greedy
     workload (R=16 requests, gamma=7, V=151936, rank 256) with backbone
-    hidden size 2560, on the CUDA-core engine; L2 flushed between steps
-    outside the events.  Beside it, the plain head's proposal on the same
-    engine."""
+    hidden size 2560, on the --engine chosen (AUTO: the tensor-core engine's
+    split mode; simt: the CUDA cores); L2 flushed between steps outside the
+    events.  Beside it, the plain head's proposal on the same engine."""
     import torch
 
     spec = synth.CYCLE_SPECS["greedy"]
     H = 2560
     R, G, V, r = spec.R, spec.G, spec.V, spec.r
     x = synth.cycle_inputs(spec, device=dev)
-    ctx = dsd.Context(spec.V, spec.r, spec.G, spec.R, dtype="bf16", engine="simt",
+    ctx = dsd.Context(spec.V, spec.r, spec.G, spec.R, dtype="bf16", engine=args.engine,
                       device=dev.index)
     if head == "gated":
         hx = synth.gate_inputs(R, G, H, r, spec.ew_std, seed=66, device=dev)
@@ -776,8 +776,7 @@ def run_hidden_head(args, dsd, synth, dev, world, head):
     peak, peak_kind = hbm_peak()
     achieved = alg / (ms / 1e3) / 1e9
     line = {
-        "metric": f"{name} draft tokens/s (CUDA-core engine) at R=16, gamma=7, "
-                  "V=151936, rank 256, H=2560",
+        "metric": f"{name} draft tokens/s at R=16, gamma=7, V=151936, rank 256, H=2560",
         "value": world * R * G / (ms / 1e3), "unit": "draft tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
@@ -786,7 +785,11 @@ def run_hidden_head(args, dsd, synth, dev, world, head):
                    "l2": "flushed between steps (512 MB write outside the events); "
                          "inputs 0.6 GB per call"},
         "plain_head_ms": plain_ms,
-        "roofline": {"bound": "hbm", "kernel": "simt_bias_kernel", "achieved": achieved,
+        "engine": f"{args.engine} -> {ctx.last_engine()}",
+        "roofline": {"bound": "hbm",
+                     "kernel": ("propose_tc_kernel (split mode)" if ctx.last_engine() == "tcgen05"
+                                else "simt_bias_kernel"),
+                     "achieved": achieved,
                      "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)",
                      "traffic": None, "alg_bytes": alg, "per": f"one {head} propose call",

@@ -80,9 +80,13 @@ enum dsd_dtype { DSD_F32 = 0, DSD_BF16 = 1 };
 enum dsd_act { DSD_ACT_NONE = 0, DSD_ACT_SILU = 1 };
 /* Propose engine.  AUTO picks the 5th-generation tensor-core engine
  * (TCGEN05: TMA-staged operands, tcgen05.mma into TMEM accumulators) for bf16
- * tables, no activation and a rank that is a multiple of 64 (<= 256), at any
- * batch size, and the CUDA-core engine (SIMT) otherwise.  The same rule picks
- * the engine of dsd_verify's residual pass (sampled verification).  MMA
+ * tables and a rank that is a multiple of 64 (<= 256), at any batch size, and
+ * the CUDA-core engine (SIMT) otherwise.  With an activation, and for the
+ * gated and RNN heads, whose Markov representations are fp32, the tensor-core
+ * engine splits each representation into hi + lo bf16 parts (|residual| <=
+ * 2^-18 of the value) that two MMAs add into one fp32 accumulator.  The
+ * residual pass of sampled verification runs on the tensor cores for the
+ * plain head without an activation, on the CUDA cores otherwise.  MMA
  * (warp-level mma.sync tensor cores, same requirements) is only used when
  * asked for.  TCGEN05 or MMA asked for with a configuration they do not
  * support makes dsd_propose return DSD_ERR_UNSUPPORTED before any launch. */
@@ -362,11 +366,12 @@ int dsd_loss_forward(dsd_ctx* ctx, int B, const void* U, const void* E, const vo
  * [rank, H + rank] (hidden-state columns first) in the context's dtype,
  * device, 16-byte aligned; H a positive multiple of 8.  gated_rep
  * [R, gamma, rank] f32 out: g_j * m_j per position (0 at position 0 when the
- * context has bias_at_first = 0); dsd_verify_gated reads it.  Runs on the
- * CUDA-core engine whatever the context's engine: one launch for the
- * hidden-state part of every gate, then per draft position a gate launch and
- * a bias launch, then the finalize.  Errors as dsd_propose; a non-finite gate
- * argument sets DSD_ERR_NONFINITE.
+ * context has bias_at_first = 0); dsd_verify_gated reads it.  One launch for
+ * the hidden-state part of every gate, then per draft position a gate launch
+ * and a bias launch, then the finalize.  The bias launch runs on the
+ * tensor-core engine's split mode (AUTO, TCGEN05; bf16 tables, rank a
+ * multiple of 64), on the CUDA cores otherwise (SIMT, f32).  Errors as
+ * dsd_propose; a non-finite gate argument sets DSD_ERR_NONFINITE.
  */
 int dsd_propose_gated(dsd_ctx* ctx, int R, const void* U, const void* E, const void* W,
                       const void* h, int H, const void* W_g, const float* conf,
@@ -401,10 +406,11 @@ int dsd_verify_gated(dsd_ctx* ctx, int R, const void* P, const void* U, const vo
  * state) in the context's dtype, device, 16-byte aligned; H a positive
  * multiple of 8.  rnn_rep [R, gamma, rank] f32 out: o_j per position (0 at
  * position 0 when the context has bias_at_first = 0; the recursion then
- * starts at position 1); dsd_verify_rnn reads it.  Runs on the CUDA-core
- * engine whatever the context's engine: one launch for the hidden-state
- * parts of all three matrices, then per draft position a state launch, an
- * output launch and a bias launch, then the finalize.  Errors as
+ * starts at position 1); dsd_verify_rnn reads it.  One launch for the
+ * hidden-state parts of all three matrices, then per draft position a state
+ * launch, an output launch and a bias launch (the tensor-core engine's split
+ * mode, or the CUDA cores as for dsd_propose_gated), then the finalize.
+ * Errors as
  * dsd_propose; a non-finite gate, candidate or output argument sets
  * DSD_ERR_NONFINITE.
  */

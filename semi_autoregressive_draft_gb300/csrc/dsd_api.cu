@@ -131,13 +131,15 @@ cudaError_t launch_propose_finalize_n(const Ctx& ctx, const ProposeArgs& a, int 
                                       cudaStream_t s);
 int tc_supported(const Ctx& ctx, char* why, size_t why_len);
 int tc_vranges(const Ctx& ctx, int R);
+int tc_parts_used(const Ctx& ctx, const ProposeArgs& a);
 }  // namespace dsd
 
 namespace {
 // AUTO sends every batch to the tcgen05 engine when the configuration
-// allows it (bf16 tables, no activation, rank a multiple of 64 <= 256): even
-// one request drafts about 3x faster there than on the CUDA-core engine,
-// whose per-tile shared-memory traffic does not shrink with R.
+// allows it (bf16 tables, rank a multiple of 64 <= 256; an activation runs in
+// its split mode): even one request drafts about 3x faster there than on the
+// CUDA-core engine, whose per-tile shared-memory traffic does not shrink
+// with R.
 bool auto_uses_tc(const dsd_ctx* ctx, int R) {
   if (ctx->cfg.engine != DSD_ENGINE_AUTO || R < 1) return false;
   char why[256];
@@ -307,7 +309,7 @@ static int propose_impl(dsd_ctx* ctx, int R, const void* U, const void* E, const
     char why[256];
     if (!tc_supported(*ctx, why, sizeof(why))) return fail(ctx, DSD_ERR_UNSUPPORTED, "%s", why);
     e = launch_propose_tc(*ctx, a, s);
-    n_used = tc_vranges(*ctx, R);
+    n_used = tc_parts_used(*ctx, a);
     ctx->last_engine = DSD_ENGINE_TCGEN05;
   } else if (ctx->cfg.engine == DSD_ENGINE_MMA && !mma_ok(ctx)) {
     return fail(ctx, DSD_ERR_UNSUPPORTED,
@@ -440,7 +442,9 @@ int dsd_verify_gated(dsd_ctx* ctx, int R, const void* P, const void* U, const vo
 }
 
 // The heads that read the backbone's hidden state: the gated Markov head
-// (W_g) or the RNN head (W_rnn), on the CUDA-core engine.
+// (W_g) or the RNN head (W_rnn).  Their per-step representation is fp32, so
+// the tensor-core engine runs them in its split mode (hi and lo bf16 parts);
+// the SIMT engine, or a configuration it cannot take, uses the CUDA cores.
 static int propose_hidden_head(dsd_ctx* ctx, const char* name, int R, const void* U,
                                const void* E, const void* W, const void* h, int H,
                                const void* W_g, const void* W_rnn, const float* conf,
@@ -485,10 +489,15 @@ static int propose_hidden_head(dsd_ctx* ctx, const char* name, int R, const void
   a.rnn_W = W_rnn;
   a.H = H;
   a.gated_rep = rep;
-  cudaError_t e = launch_propose_simt(*ctx, a, s);
+  char why[256];
+  const bool tc = (ctx->cfg.engine == DSD_ENGINE_AUTO || ctx->cfg.engine == DSD_ENGINE_TCGEN05) &&
+                  tc_supported(*ctx, why, sizeof(why));
+  if (ctx->cfg.engine == DSD_ENGINE_TCGEN05 && !tc)
+    return fail(ctx, DSD_ERR_UNSUPPORTED, "%s", why);
+  cudaError_t e = tc ? launch_propose_tc(*ctx, a, s) : launch_propose_simt(*ctx, a, s);
   if (e != cudaSuccess) return cuda_fail(ctx, e, name);
-  ctx->last_engine = DSD_ENGINE_SIMT;
-  e = launch_propose_finalize_n(*ctx, a, simt_grid(*ctx, a.V), s);
+  ctx->last_engine = tc ? DSD_ENGINE_TCGEN05 : DSD_ENGINE_SIMT;
+  e = launch_propose_finalize_n(*ctx, a, tc ? tc_parts_used(*ctx, a) : simt_grid(*ctx, a.V), s);
   if (e != cudaSuccess) return cuda_fail(ctx, e, "propose finalize launch");
   return DSD_OK;
 }
@@ -681,6 +690,8 @@ int dsd_loss_forward(dsd_ctx* ctx, int B, const void* U, const void* E, const vo
   char why[256];
   if (!dsd::tc_supported(*ctx, why, sizeof(why)))
     return fail(ctx, DSD_ERR_UNSUPPORTED, "dsd_loss_forward: %s", why);
+  if (ctx->cfg.act != DSD_ACT_NONE)   // its A operand is the stored bf16 rows of E
+    return fail(ctx, DSD_ERR_UNSUPPORTED, "dsd_loss_forward runs without an activation");
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (B == 0) {
     cudaError_t e = cudaMemsetAsync(losses, 0, 4 * sizeof(float), s);

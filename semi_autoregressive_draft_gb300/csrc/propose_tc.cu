@@ -106,6 +106,9 @@ struct TcParams {
   int R, R_max, V, rank, gamma, bias_at_first, n_part, n_vr, ntiles, sampled;
   int dup;                   // R <= 64: rows 64..127 repeat rows 0..63 and take the second
                              // 32-column chunk of every 64-column half
+  const float* A;            // split mode: the head's representations [R, gamma, rank] f32
+                             // (gated / RNN heads), or nullptr: act(E[x_{j-1}])
+  int act;                   // split mode without A: the activation of the E rows
   float inv_T;
   uint32_t k0, k1;
 };
@@ -251,10 +254,13 @@ __device__ __forceinline__ void foldN(RowState& st, const uint32_t (&acc)[N], co
 // columns per tile) of TMEM lane quarter warp % 4.  DUP (at most 64
 // requests): rows 64..127 of A repeat rows 0..63 and the two copies of a row
 // fold the two halves of each group's columns.
-template <int EW, bool DUP>
+template <int EW, bool DUP, bool SPLIT>
 __global__ void __launch_bounds__(128 + 32 * EW, 1)
     propose_tc_kernel(const __grid_constant__ CUtensorMap tmW,
                       const __grid_constant__ CUtensorMap tmU, const TcParams p) {
+  static_assert(!(DUP && SPLIT), "the split mode uses rows 64..127 of A for the low parts");
+  constexpr int kRowsM = SPLIT ? 64 : kTileM;   // requests per M-tile
+  constexpr int kUBytes = SPLIT ? kBox / 2 : kBox;   // one U box ([kRowsM x 64] bf16)
   constexpr int kGroups = EW / 4;               // column groups per tile
   constexpr int kGCols = kTileN / kGroups;      // columns of a group (64 or 32)
   constexpr int kFW = DUP ? kGCols / 2 : kGCols;   // columns one thread folds per tile
@@ -285,7 +291,7 @@ __global__ void __launch_bounds__(128 + 32 * EW, 1)
   const int j = p.j;
   const int mt = blockIdx.x / p.n_vr;
   const int vr = blockIdx.x - mt * p.n_vr;
-  const int r0 = mt * kTileM;        // first request of this CTA's M-tile
+  const int r0 = mt * kRowsM;        // first request of this CTA's M-tile
   const int t0 = (int)(((long long)vr * p.ntiles) / p.n_vr);
   const int t1 = (int)(((long long)(vr + 1) * p.ntiles) / p.n_vr);
   const int nt = t1 - t0;
@@ -366,7 +372,7 @@ __global__ void __launch_bounds__(128 + 32 * EW, 1)
         if (vx >= p.V) break;
         const int s = it % kNU;
         if (!wait_bar(&empty[s], ((it / kNU) & 1) ^ 1, abort_flag, p.status)) break;
-        tc::mbar_arrive_expect_tx(&full[s], kBox);
+        tc::mbar_arrive_expect_tx(&full[s], kUBytes);
         tc::tma_load_3d(ring + s * kBox, &tmU, &full[s], vx, j, r0, pol);
         ++it;
       }
@@ -404,8 +410,14 @@ __global__ void __launch_bounds__(128 + 32 * EW, 1)
             const uint64_t da = da0 + (uint64_t)((kc * kBox) >> 4);
             const uint64_t db = db0 + (uint64_t)(((s * kCPS + c) * kBox) >> 4);
 #pragma unroll
-            for (int ks = 0; ks < kKChunk / 16; ++ks)   // K = 16 is 32 bytes = 2 units
+            for (int ks = 0; ks < kKChunk / 16; ++ks) {   // K = 16 is 32 bytes = 2 units
               tc::umma_bf16(d_tmem, da + 2 * ks, db + 2 * ks, kIdesc, (kc | ks) != 0 ? 1u : 0u);
+              // split: A's rows 64..127 (the low parts) start 8 KB into the
+              // box; as rows 0..63 of a second MMA they add W lo to the same
+              // accumulator rows (its rows 64..127 read past the box: unused)
+              if constexpr (SPLIT)
+                tc::umma_bf16(d_tmem, da + 512 + 2 * ks, db + 2 * ks, kIdesc, 1u);
+            }
           }
           tc::umma_commit(&b.bempty[s]);
         }
@@ -430,8 +442,9 @@ __global__ void __launch_bounds__(128 + 32 * EW, 1)
     const int cbase = cg * kGCols + copy * kFW;   // first column of this thread, in the tile
     const int hs = cbase / kHalf;    // the U box (column half) it reads
     const int r = r0 + rrow;
-    const bool valid = r < p.R;
-    const bool warp_rows = r0 + (DUP ? (q & 1) : q) * 32 < p.R;   // any request in this warp?
+    // split: only rows 0..63 of the accumulator are requests
+    const bool valid = r < p.R && (!SPLIT || row < kRowsM);
+    const bool warp_rows = (!SPLIT || q < 2) && r0 + (DUP ? (q & 1) : q) * 32 < p.R;
     const uint32_t rid = valid ? (p.req_id ? p.req_id[r] : (uint32_t)r) : 0u;
 
     // The keys of step j-1 come from the previous grid: wait until it has
@@ -439,6 +452,79 @@ __global__ void __launch_bounds__(128 + 32 * EW, 1)
     // dependency).
     asm volatile("griddepcontrol.wait;" ::: "memory");
 
+    if constexpr (SPLIT) {
+      // ---- A operand, split: the fp32 representation a of each request
+      // (the head's buffer, or act(E[x_{j-1}])) as hi = bf16(a) in row i and
+      // lo = bf16(a - hi) in row 64 + i; |a - hi - lo| <= 2^-18 |a|.  This
+      // warp fills rows e, e + EW, ... of the 64.
+      constexpr int kSR = kRowsM / EW;
+      const bool biased = (j > 0) || p.bias_at_first;
+      int my_tok = -1;
+      if (lane < kSR && !p.A) {
+        const int rr = r0 + e + EW * lane;
+        if (biased && rr < p.R) {
+          int tk = (j == 0) ? p.prev_tok[rr]
+                            : (int)key_index(__ldcg(&p.keys[(size_t)(j - 1) * p.R_max + rr]));
+          if (tk < 0 || tk >= p.V) {
+            set_status(p.status, kErrArg);
+            tk = 0;
+          }
+          my_tok = tk;
+        }
+      }
+      const int cpr = p.rank / 8;    // 8 elements per lane
+      float a[kSR][8];
+#pragma unroll
+      for (int kk = 0; kk < kSR; ++kk) {
+        const int rr = r0 + e + EW * kk;
+        const int tok = __shfl_sync(0xffffffffu, my_tok, kk);
+#pragma unroll
+        for (int q8 = 0; q8 < 8; ++q8) a[kk][q8] = 0.f;
+        if (lane < cpr && biased && rr < p.R) {
+          if (p.A) {
+            const float4* src = reinterpret_cast<const float4*>(
+                p.A + ((size_t)rr * p.gamma + j) * p.rank + lane * 8);
+            const float4 x0 = __ldcg(src), x1 = __ldcg(src + 1);
+            a[kk][0] = x0.x; a[kk][1] = x0.y; a[kk][2] = x0.z; a[kk][3] = x0.w;
+            a[kk][4] = x1.x; a[kk][5] = x1.y; a[kk][6] = x1.z; a[kk][7] = x1.w;
+          } else if (tok >= 0 &&
+                     TC_CHECK((size_t)tok * p.rank + lane * 8 + 8 <= (size_t)p.V * p.rank, 2)) {
+            const uint4 w = __ldcg(reinterpret_cast<const uint4*>(p.E + (size_t)tok * p.rank + lane * 8));
+            const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+            for (int q8 = 0; q8 < 4; ++q8) {
+              a[kk][2 * q8] = act_apply(bf16lo(ws[q8]), p.act);
+              a[kk][2 * q8 + 1] = act_apply(bf16hi(ws[q8]), p.act);
+            }
+          }
+        }
+      }
+      if (lane < cpr) {
+        const int kc = lane >> 3, c8 = lane & 7;
+#pragma unroll
+        for (int kk = 0; kk < kSR; ++kk) {
+          const int ir = e + EW * kk;    // row 0..63; its low part goes to row 64 + ir
+          uint32_t hw[4], lw[4];
+#pragma unroll
+          for (int q8 = 0; q8 < 4; ++q8) {
+            const __nv_bfloat16 h0 = __float2bfloat16_rn(a[kk][2 * q8]);
+            const __nv_bfloat16 h1 = __float2bfloat16_rn(a[kk][2 * q8 + 1]);
+            const __nv_bfloat16 l0 = __float2bfloat16_rn(a[kk][2 * q8] - __bfloat162float(h0));
+            const __nv_bfloat16 l1 = __float2bfloat16_rn(a[kk][2 * q8 + 1] - __bfloat162float(h1));
+            hw[q8] = (uint32_t)__bfloat16_as_ushort(h0) | ((uint32_t)__bfloat16_as_ushort(h1) << 16);
+            lw[q8] = (uint32_t)__bfloat16_as_ushort(l0) | ((uint32_t)__bfloat16_as_ushort(l1) << 16);
+          }
+          const size_t off = (size_t)kc * kBox + ir * 128 + ((c8 ^ (ir & 7)) << 4);
+          if (TC_CHECK(off + 64 * 128 + 16 <= (size_t)kMaxKC * kBox, 1)) {
+            *reinterpret_cast<uint4*>(sA + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+            *reinterpret_cast<uint4*>(sA + off + 64 * 128) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+          }
+        }
+      }
+      tc::fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(b.aready);
+    } else
     // ---- A operand: rows of E for the tokens of step j-1 ----
     // This warp fills rows e, e + EW, ...: lane k < kRowsPerWarp fetches the
     // token of row e + EW k, then the rows are copied into the 128-byte-
@@ -1412,8 +1498,8 @@ int tc_supported(const Ctx& ctx, char* why, size_t why_len) {
     snprintf(why, why_len, "tcgen05 engine needs a Markov rank that is a multiple of 64, <= 256");
     return 0;
   }
-  if (ctx.cfg.act != kActNone) {
-    snprintf(why, why_len, "tcgen05 engine runs without an activation (bf16 operands)");
+  if (ctx.cfg.act != kActNone && ctx.cfg.act != kActSilu) {
+    snprintf(why, why_len, "tcgen05 engine: unknown activation");
     return 0;
   }
   if (!tensor_map_encoder()) {
@@ -1430,15 +1516,28 @@ int tc_supported(const Ctx& ctx, char* why, size_t why_len) {
   return 1;
 }
 
+// The split mode (the Markov representation is not a bf16 row of E: an
+// activation, or the gated / RNN head's fp32 representation) runs M-tiles of
+// 64 requests with A's rows 64..127 holding the low parts.
+static bool use_split(const Ctx& ctx, const ProposeArgs& a) {
+  return a.act != kActNone || a.gate_h != nullptr;
+}
+
 // Vocabulary ranges per M-tile: the grid is M-tiles x ranges, one CTA per SM.
-int tc_vranges(const Ctx& ctx, int R) {
-  const int MT = (R + kTileM - 1) / kTileM;
+int tc_vranges_rows(const Ctx& ctx, int R, int rows_per_tile) {
+  const int MT = (R + rows_per_tile - 1) / rows_per_tile;
   const int ntiles = (ctx.cfg.V + kTileN - 1) / kTileN;
   int n = ctx.num_sms / (MT > 0 ? MT : 1);
   if (n < 1) n = 1;
   if (n > ntiles) n = ntiles;
   if (n > ctx.n_part) n = ctx.n_part;
   return n;
+}
+int tc_vranges(const Ctx& ctx, int R) { return tc_vranges_rows(ctx, R, kTileM); }
+int tc_vranges_split(const Ctx& ctx, int R) { return tc_vranges_rows(ctx, R, 64); }
+// The partial slots a propose call on this engine fills (the finalize's n_used).
+int tc_parts_used(const Ctx& ctx, const ProposeArgs& a) {
+  return use_split(ctx, a) ? tc_vranges_split(ctx, a.R) : tc_vranges(ctx, a.R);
 }
 
 // An even number of M-tiles runs on CTA pairs (propose_tc_pair_kernel).
@@ -1452,7 +1551,9 @@ static bool use_pair(int R) {
 cudaError_t launch_propose_tc(const Ctx& ctx, const ProposeArgs& a, cudaStream_t s) {
   PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
   if (!encode) return cudaErrorNotSupported;
-  const bool pair = use_pair(a.R);
+  const bool split = use_split(ctx, a);
+  const bool pair = !split && use_pair(a.R);
+  const int rows_m = split ? 64 : kTileM;   // requests per M-tile
   CUtensorMap tmW, tmU;
   {
     const cuuint64_t dims[2] = {(cuuint64_t)a.rank, (cuuint64_t)a.V};
@@ -1468,7 +1569,7 @@ cudaError_t launch_propose_tc(const Ctx& ctx, const ProposeArgs& a, cudaStream_t
   {
     const cuuint64_t dims[3] = {(cuuint64_t)a.V, (cuuint64_t)a.gamma, (cuuint64_t)a.R};
     const cuuint64_t strides[2] = {(cuuint64_t)a.V * 2, (cuuint64_t)a.V * 2 * a.gamma};
-    const cuuint32_t box[3] = {kHalf, 1, kTileM};
+    const cuuint32_t box[3] = {kHalf, 1, (cuuint32_t)rows_m};
     const cuuint32_t estr[3] = {1, 1, 1};
     if (encode(&tmU, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(a.U), dims, strides,
                box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -1478,10 +1579,13 @@ cudaError_t launch_propose_tc(const Ctx& ctx, const ProposeArgs& a, cudaStream_t
   cudaError_t e = cudaMemsetAsync(ctx.ws.keys, 0,
                                   sizeof(unsigned long long) * (size_t)a.gamma * ctx.cfg.R_max, s);
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(propose_tc_kernel<kSingleEpiWarps, false>,
+  e = cudaFuncSetAttribute(propose_tc_kernel<kSingleEpiWarps, false, false>,
                            cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(propose_tc_kernel<kSingleEpiWarps, true>,
+    e = cudaFuncSetAttribute(propose_tc_kernel<kSingleEpiWarps, true, false>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(propose_tc_kernel<kSingleEpiWarps, false, true>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(propose_tc_pair_kernel<kPairEpiWarps>,
@@ -1507,9 +1611,15 @@ cudaError_t launch_propose_tc(const Ctx& ctx, const ProposeArgs& a, cudaStream_t
   p.inv_T = a.temperature > 0.f ? 1.f / a.temperature : 1.f;
   p.k0 = (uint32_t)(a.seed & 0xFFFFFFFFull);
   p.k1 = (uint32_t)(a.seed >> 32);
-  p.n_vr = tc_vranges(ctx, a.R);
-  p.dup = a.R <= kTileM / 2 ? 1 : 0;
-  const int grid = ((a.R + kTileM - 1) / kTileM) * p.n_vr;
+  p.n_vr = split ? tc_vranges_split(ctx, a.R) : tc_vranges(ctx, a.R);
+  p.dup = !split && a.R <= kTileM / 2 ? 1 : 0;
+  p.A = a.gate_h ? a.gated_rep : nullptr;
+  p.act = a.act;
+  const int grid = ((a.R + rows_m - 1) / rows_m) * p.n_vr;
+  if (a.gate_h) {   // gated or RNN head: the hidden-state parts of every position, once
+    e = a.rnn_W ? launch_rnn_h(ctx, a, s) : launch_gate_h(ctx, a, s);
+    if (e != cudaSuccess) return e;
+  }
 
   // One launch per step: the next step's A operand needs every CTA's argmax.
   // Steps after the first are launched with a programmatic dependency on the
@@ -1532,10 +1642,16 @@ cudaError_t launch_propose_tc(const Ctx& ctx, const ProposeArgs& a, cudaStream_t
   cfg.attrs = pair ? attr : attr + 1;
   for (int j = 0; j < a.gamma; ++j) {
     p.j = j;
-    cfg.numAttrs = (pair ? 1 : 0) + (j > 0 ? 1 : 0);
+    if (a.gate_h) {   // this step's representation from the tokens of the last
+      e = a.rnn_W ? launch_rnn_step(ctx, a, j, s) : launch_gate_step(ctx, a, j, s);
+      if (e != cudaSuccess) return e;
+    }
+    // a head kernel in between: plain stream order
+    cfg.numAttrs = (pair ? 1 : 0) + (j > 0 && !a.gate_h ? 1 : 0);
     e = pair    ? cudaLaunchKernelEx(&cfg, propose_tc_pair_kernel<kPairEpiWarps>, tmW, tmU, p)
-        : p.dup ? cudaLaunchKernelEx(&cfg, propose_tc_kernel<kSingleEpiWarps, true>, tmW, tmU, p)
-                : cudaLaunchKernelEx(&cfg, propose_tc_kernel<kSingleEpiWarps, false>, tmW, tmU, p);
+        : split ? cudaLaunchKernelEx(&cfg, propose_tc_kernel<kSingleEpiWarps, false, true>, tmW, tmU, p)
+        : p.dup ? cudaLaunchKernelEx(&cfg, propose_tc_kernel<kSingleEpiWarps, true, false>, tmW, tmU, p)
+                : cudaLaunchKernelEx(&cfg, propose_tc_kernel<kSingleEpiWarps, false, false>, tmW, tmU, p);
     if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     count_launch(ctx);

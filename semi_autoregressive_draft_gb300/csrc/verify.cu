@@ -34,7 +34,7 @@ int tc_supported(const Ctx& ctx, char* why, size_t why_len);
 // multiple of 64 (<= 256), the AUTO or TCGEN05 engine and the plain Markov
 // head.  Otherwise the CUDA-core residual pass.
 static bool residual_on_tc(const Ctx& ctx, const VerifyArgs& a) {
-  if (a.gated_rep != nullptr) return false;
+  if (a.gated_rep != nullptr || ctx.cfg.act != kActNone) return false;   // E rows as stored
   if (ctx.cfg.engine != 0 && ctx.cfg.engine != 2) return false;   // AUTO, TCGEN05
   char why[256];
   return tc_supported(ctx, why, sizeof(why)) != 0;

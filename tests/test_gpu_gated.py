@@ -35,10 +35,11 @@ def host(x):
     return {k: synth.to_numpy(v) for k, v in x.items() if isinstance(v, torch.Tensor)}
 
 
-def run_gated(dsd, spec, gx, bias_at_first=True, keep_all=False, act="none"):
+def run_gated(dsd, spec, gx, bias_at_first=True, keep_all=False, act="none",
+              engine="auto"):
     x = synth.cycle_inputs(spec, device=DEV)
     ctx = dsd.Context(spec.V, spec.r, spec.G, spec.R, dtype=spec.dtype, act=act,
-                      bias_at_first=bias_at_first)
+                      bias_at_first=bias_at_first, engine=engine)
     T = spec.temperature
     prop = ctx.propose_gated(x["U"], x["E"], x["W"], gx["h"], gx["W_g"], x["conf"], x["prev_tok"],
                              req_id=x["req_id"], temperature=T, seed=x["seed"])
@@ -153,3 +154,17 @@ def test_gated_errors(dsd):
     ctx.propose_gated(x["U"], x["E"], x["W"], h, gx["W_g"], x["conf"], x["prev_tok"])
     assert ctx.sync_status() == -6
     ctx.close()
+
+
+@pytest.mark.parametrize("engine,R,temperature", [("simt", 19, 1.0), ("simt", 19, 0.0),
+                                                  ("tcgen05", 100, 1.0), ("tcgen05", 64, 0.0)])
+def test_gated_on_each_engine(dsd, engine, R, temperature):
+    # the CUDA-core engine, and the tensor-core engine's split mode (hi and
+    # lo bf16 parts of the fp32 representation, 64-request M-tiles: R = 100
+    # takes two, one of them partial)
+    spec = synth.scaled(synth.CYCLE_SPECS["greedy"], temperature=temperature, seed=69 + R,
+                        p_noise=1.0, r=128, R=R, V=2568, ew_std=0.3)
+    gx = synth.gate_inputs(spec.R, spec.G, 64, spec.r, spec.ew_std, seed=70, device=DEV)
+    x, k = run_gated(dsd, spec, gx, engine=engine)
+    check_gated(spec, x, gx, k)
+

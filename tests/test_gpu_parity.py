@@ -189,9 +189,10 @@ def test_tc_mma_simt_engines_agree(dsd):
 
 
 def test_tc_engine_rejects_unsupported_config_before_any_launch(dsd):
-    spec = synth.scaled(synth.CYCLE_SPECS["greedy"], R=16, V=1032, seed=34)
+    # rank 32: a valid context, but the tensor-core engine needs a multiple of 64
+    spec = synth.scaled(synth.CYCLE_SPECS["greedy"], R=16, V=1032, r=32, seed=34)
     x = synth.cycle_inputs(spec, device=DEV)
-    ctx = dsd.Context(spec.V, spec.r, spec.G, spec.R, dtype="bf16", act="silu", engine="tcgen05")
+    ctx = dsd.Context(spec.V, spec.r, spec.G, spec.R, dtype="bf16", engine="tcgen05")
     n0 = ctx.launch_count()
     with pytest.raises(dsd.DsdError) as ei:
         ctx.propose(x["U"], x["E"], x["W"], x["conf"], x["prev_tok"], x["req_id"], 0.0, 1)
@@ -229,6 +230,16 @@ def test_cycle_variants(dsd, act, baf):
     spec = synth.scaled(synth.CYCLE_SPECS["greedy"], seed=24, temperature=1.0, **SMALL)
     x, k = run_cycle(dsd, spec, act=act, bias_at_first=baf)
     check_cycle(spec, x, k, act=act, bias_at_first=baf)
+
+
+@pytest.mark.parametrize("R,temperature,rank", [(19, 1.0, 256), (100, 0.0, 128), (130, 1.0, 64)])
+def test_silu_on_the_tensor_core_split_mode(dsd, R, temperature, rank):
+    # SiLU rows are not bf16: the tensor-core engine feeds their hi and lo
+    # bf16 parts (64-request M-tiles: R = 130 takes three)
+    spec = synth.scaled(synth.CYCLE_SPECS["greedy"], seed=26 + R, temperature=temperature, R=R,
+                        V=2568, ew_std=0.3, r=rank)
+    x, k = run_cycle(dsd, spec, engine="tcgen05", act="silu")
+    check_cycle(spec, x, k, act="silu")
 
 
 def test_single_position_and_single_request(dsd):
@@ -477,7 +488,7 @@ def test_full_size_overlap_sampled_blocks(dsd):
     (15, "bf16", "none", "tcgen05"),
     (1, "bf16", "none", "tcgen05"),
     (64, "f32", "none", "simt"),
-    (64, "bf16", "silu", "simt"),
+    (64, "bf16", "silu", "tcgen05"),
 ])
 def test_auto_engine_choice(dsd, R, dtype, act, expect):
     spec = synth.scaled(synth.CYCLE_SPECS["greedy"], R=R, V=1032, seed=36, dtype=dtype)

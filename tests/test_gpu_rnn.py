@@ -38,10 +38,11 @@ def host(x):
     return {k: synth.to_numpy(v) for k, v in x.items() if isinstance(v, torch.Tensor)}
 
 
-def run_rnn(dsd, spec, rx, bias_at_first=True, keep_all=False, act="none"):
+def run_rnn(dsd, spec, rx, bias_at_first=True, keep_all=False, act="none",
+            engine="auto"):
     x = synth.cycle_inputs(spec, device=DEV)
     ctx = dsd.Context(spec.V, spec.r, spec.G, spec.R, dtype=spec.dtype, act=act,
-                      bias_at_first=bias_at_first)
+                      bias_at_first=bias_at_first, engine=engine)
     T = spec.temperature
     prop = ctx.propose_rnn(x["U"], x["E"], x["W"], rx["h"], rx["W_rnn"], x["conf"], x["prev_tok"],
                            req_id=x["req_id"], temperature=T, seed=x["seed"])
@@ -158,3 +159,15 @@ def test_rnn_errors(dsd):
     ctx.propose_rnn(x["U"], x["E"], x["W"], h, rx["W_rnn"], x["conf"], x["prev_tok"])
     assert ctx.sync_status() == -6
     ctx.close()
+
+
+@pytest.mark.parametrize("engine,R,temperature", [("simt", 19, 1.0), ("tcgen05", 70, 1.0),
+                                                  ("tcgen05", 19, 0.0)])
+def test_rnn_on_each_engine(dsd, engine, R, temperature):
+    # the CUDA-core engine, and the tensor-core engine's split mode
+    spec = synth.scaled(synth.CYCLE_SPECS["greedy"], temperature=temperature, seed=80 + R,
+                        p_noise=1.0, r=64, R=R, V=2568, ew_std=0.3)
+    rx = synth.rnn_inputs(spec.R, spec.G, 64, spec.r, spec.ew_std, seed=81, device=DEV)
+    x, k = run_rnn(dsd, spec, rx, engine=engine)
+    check_rnn(spec, x, rx, k)
+
