@@ -60,7 +60,9 @@ size_t carve(dsd_ctx* c, unsigned char* base) {
   Workspace w{};
   w.status = reinterpret_cast<int*>(take(sizeof(int) * 4));
   w.counters = reinterpret_cast<unsigned int*>(take(sizeof(unsigned int) * 16));
-  w.keys = reinterpret_cast<unsigned long long*>(take(sizeof(unsigned long long) * (size_t)G * Rm));
+  w.keys = reinterpret_cast<unsigned long long*>(
+      take(sizeof(unsigned long long) * (size_t)G * Rm + sizeof(unsigned int) * kStepSyncWords));
+  w.step_sync = w.keys ? reinterpret_cast<unsigned int*>(w.keys + (size_t)G * Rm) : nullptr;
   w.lse_parts = reinterpret_cast<float2*>(take(sizeof(float2) * (size_t)G * c->n_part * Rm));
   w.vparts = reinterpret_cast<RowPart*>(take(sizeof(RowPart) * (size_t)Rm * (G + 1) * kVerifySplits));
   w.rej_list = reinterpret_cast<int*>(take(sizeof(int) * (size_t)Rm));

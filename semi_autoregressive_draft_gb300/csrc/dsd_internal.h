@@ -18,6 +18,7 @@ constexpr int kCandMaxR = 32;        // requests per call of dsd_propose_candida
 constexpr int kGateZhFactor = 12;    // gated / RNN heads: split-K partials, 12 x R_max gamma x rank floats
 constexpr int kMaxSchedItems = 4096;  // R_max * gamma
 constexpr int kVerifySplits = 8;      // V chunks per verified row
+constexpr int kStepSyncWords = 32;    // kMaxGamma counters + an abort word, padded
 
 // Status codes (mirror enum dsd_status in include/dsd.h).
 constexpr int kOk = 0;
@@ -37,6 +38,8 @@ struct Workspace {
   int* status;                  // first device-side error of the calls so far
   unsigned int* counters;       // [16] tickets / barrier counters (zeroed per call)
   unsigned long long* keys;     // [gamma][R_max] argmax keys of the propose steps
+  unsigned int* step_sync;      // [kStepSyncWords], right after keys (one memset clears both):
+                                // per-position counters of a several-position propose launch
   float2* lse_parts;            // [gamma][n_part][R_max] (m, s) partials
   RowPart* vparts;              // [R_max*(gamma+1)][kVerifySplits]
   int* rej_list;                // [R_max] requests with a rejection (sampled verify)

@@ -56,6 +56,8 @@
 // its own copies in flight, frees its TMEM and returns.
 #include <stdio.h>
 
+#include <atomic>
+
 #include "tc_common.cuh"
 
 namespace dsd {
@@ -102,7 +104,11 @@ struct TcParams {
   unsigned long long* keys;  // [gamma][R_max]
   float2* parts;             // [gamma][n_part][R_max]
   int* status;
-  int j;                     // draft position of this launch
+  int j;                     // draft position of this launch (the first, if several)
+  int j_end;                 // one past the last draft position of this launch
+  unsigned int* step_sync;   // several positions per launch: [kMaxGamma] CTAs done with
+                             // position j (zero before the launch); the last entry is the
+                             // launch's abort word
   int R, R_max, V, rank, gamma, bias_at_first, n_part, n_vr, ntiles, sampled;
   int dup;                   // R <= 64: rows 64..127 repeat rows 0..63 and take the second
                              // 32-column chunk of every 64-column half
@@ -152,7 +158,7 @@ constexpr float kLagBits = 8.f;
 // a tree.
 template <int N>
 __device__ __forceinline__ void foldN(RowState& st, const uint32_t (&acc)[N], const uint4* u,
-                                      int v0, const TcParams& p, uint32_t rid) {
+                                      int v0, const TcParams& p, uint32_t rid, int j) {
   static_assert(N == 16 || N == 32, "16 or 32 columns");
   constexpr int NG = N / 4;          // groups of four columns
   float xs[N];
@@ -234,7 +240,7 @@ __device__ __forceinline__ void foldN(RowState& st, const uint32_t (&acc)[N], co
 #pragma unroll
     for (int g = 0; g < NG; ++g) {
       const uint32_t v = (uint32_t)(v0 + 4 * g);
-      const Philox4 ph = philox4x32_10(v >> 2, (uint32_t)p.j, rid, 0u, p.k0, p.k1);
+      const Philox4 ph = philox4x32_10(v >> 2, (uint32_t)j, rid, 0u, p.k0, p.k1);
       const float z0 = xs[4 * g + 0] + gumbel_from_word(ph.x);
       const float z1 = xs[4 * g + 1] + gumbel_from_word(ph.y);
       const float z2 = xs[4 * g + 2] + gumbel_from_word(ph.z);
@@ -608,7 +614,7 @@ __global__ void __launch_bounds__(128 + 32 * EW, 1)
             tc::tmem_ld_wait<kChunk>(tmem_base + ((uint32_t)(q * 32) << 16) +
                                          (uint32_t)(buf * kTileN + cbase + c * kChunk),
                                      acc);
-            foldN<kChunk>(st, acc, u + (kChunk / 8) * c, v0, p, rid);
+            foldN<kChunk>(st, acc, u + (kChunk / 8) * c, v0, p, rid, j);
           }
         }
       }
@@ -693,6 +699,7 @@ __global__ void __launch_bounds__(128 + 32 * EW, 1)
 // Every barrier still has one consumer role that waits on each of its phases
 // in order.  Waits that see the peer's arrivals acquire at cluster scope.
 constexpr int kPCPS = 4;                 // W half-boxes (K-chunks) per ring stage: a whole tile
+constexpr int kStepAbort = kMaxGamma;    // abort word of a several-position launch
 constexpr int kPNB = 3;                  // W ring stages
 constexpr int kPNU = 2;                  // U ring slots per column half
 constexpr int kHalfBox = kBox / 2;       // [64 vocab x 64 K] bf16
@@ -743,7 +750,6 @@ __global__ void __launch_bounds__(128 + 32 * EW, 1)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int KC = p.rank / kKChunk;
-  const int j = p.j;
   const uint32_t crank = tc::cluster_ctarank();      // 0: issues the MMAs
   const int cid = (int)(blockIdx.x >> 1);
   const int mt = 2 * (cid / p.n_vr) + (int)crank;
@@ -800,6 +806,7 @@ __global__ void __launch_bounds__(128 + 32 * EW, 1)
     if (lane == 0) {
       const uint64_t pol = policy_evict_last();
       uint32_t it = 0;
+      for (int jj = p.j; jj < p.j_end; ++jj)     // the same W tiles at every position
       for (int t = t0; t < t1 && !*abort_flag; ++t)
         for (int k0 = 0; k0 < KC; k0 += kPCPS, ++it) {
           const int s = it % kPNB;
@@ -829,13 +836,14 @@ __global__ void __launch_bounds__(128 + 32 * EW, 1)
       uint64_t* empty = b.uempty + hs * kPNU;
       unsigned char* ring = sU + hs * kPNU * kBox;
       uint32_t it = 0;
+      for (int jj = p.j; jj < p.j_end; ++jj)
       for (int t = t0; t < t1 && !*abort_flag; ++t) {
         const int vx = t * kTileN + hs * kHalf;
         if (vx >= p.V) break;
         const int s = it % kPNU;
         if (!wait_bar(&empty[s], ((it / kPNU) & 1) ^ 1, abort_flag, p.status)) break;
         tc::mbar_arrive_expect_tx(&full[s], kBox);
-        tc::tma_load_3d(ring + s * kBox, &tmU, &full[s], vx, j, r0, pol);
+        tc::tma_load_3d(ring + s * kBox, &tmU, &full[s], vx, jj, r0, pol);
         ++it;
       }
       for (uint32_t k = (it > kPNU ? it - kPNU : 0); k < it; ++k)
@@ -851,13 +859,17 @@ __global__ void __launch_bounds__(128 + 32 * EW, 1)
       const uint32_t bempty_peer = tc::mapa(bempty_own, 1);
       const uint32_t accfull_own = tc::smem_u32(b.accfull);
       const uint32_t accfull_peer = tc::mapa(accfull_own, 1);
-      bool ok = wait_bar_cl(b.aready, 0, abort_flag, p.status);
-      tc::tc_fence_after();
       const uint64_t da0 = tc::sdesc_kmajor_sw128(tc::smem_u32(sA));
       const uint64_t db0 = tc::sdesc_kmajor_sw128(tc::smem_u32(sB));
-      for (int tt = 0; tt < nt && ok; ++tt) {
-        const int buf = tt % kNAcc;
-        ok = wait_bar_cl(&b.accempty[buf], ((tt / kNAcc) & 1) ^ 1, abort_flag, p.status);
+      bool ok = true;
+      uint32_t gt = 0;   // tiles of the launch so far (accumulator ring position)
+      for (int jj = p.j; jj < p.j_end && ok; ++jj) {
+      // A of position jj gathered in both CTAs (one phase of aready per position)
+      ok = wait_bar_cl(b.aready, (uint32_t)(jj - p.j) & 1u, abort_flag, p.status);
+      tc::tc_fence_after();
+      for (int tt = 0; tt < nt && ok; ++tt, ++gt) {
+        const int buf = gt % kNAcc;
+        ok = wait_bar_cl(&b.accempty[buf], ((gt / kNAcc) & 1) ^ 1, abort_flag, p.status);
         if (!ok) break;
         tc::tc_fence_after();    // both CTAs' TMEM reads of this buffer are done
         const uint32_t d_tmem = tmem_base + (uint32_t)(buf * kTileN);
@@ -883,6 +895,7 @@ __global__ void __launch_bounds__(128 + 32 * EW, 1)
           tc::umma_commit_pair(accfull_peer + 8u * buf);
         }
       }
+      }
       // all issued MMAs (which read both CTAs' shared memory and write both
       // TMEMs) complete before the pair passes the final cluster barrier
       tc::umma_commit_pair(tc::smem_u32(b.mmadone));
@@ -902,7 +915,22 @@ __global__ void __launch_bounds__(128 + 32 * EW, 1)
     const bool warp_rows = r0 + q * 32 < p.R;
     const uint32_t rid = valid ? (p.req_id ? p.req_id[r] : (uint32_t)r) : 0u;
 
-    asm volatile("griddepcontrol.wait;" ::: "memory");
+    uint32_t gt = 0;    // tiles of the launch so far (accumulator ring position)
+    uint32_t uit = 0;   // U boxes of the launch so far (U ring position)
+    // After a failure (the CTA's abort flag) every warp still runs every
+    // position's named barriers, with its waits failing at once, so that no
+    // warp is left at a bar.sync.
+    for (int j = p.j; j < p.j_end; ++j) {
+    if (j == p.j) {
+      asm volatile("griddepcontrol.wait;" ::: "memory");
+    } else {
+      // every CTA of the launch has published position j - 1
+      if (e == 0 && lane == 0 && !*abort_flag &&
+          !wait_count_gpu(&p.step_sync[j - 1], gridDim.x, &p.step_sync[kStepAbort], abort_flag,
+                          p.status))
+        *abort_flag = 1;
+      asm volatile("bar.sync 1, %0;" ::"n"(32 * EW) : "memory");
+    }
 
     // ---- A operand: rows of E for the tokens of step j-1 (this M-tile) ----
     // This warp fills rows e, e + EW, ...: lane k < kRowsPerWarp fetches the
@@ -953,12 +981,11 @@ __global__ void __launch_bounds__(128 + 32 * EW, 1)
     uint64_t* full = b.ufull + hs * kPNU;
     uint64_t* empty = b.uempty + hs * kPNU;
     const unsigned char* ring = sU + hs * kPNU * kBox;
-    uint32_t uit = 0;
-    for (int tt = 0; tt < nt; ++tt) {
+    for (int tt = 0; tt < nt; ++tt, ++gt) {
       if (warp_aborted(abort_flag)) break;
       const int t = t0 + tt;
-      const int buf = tt % kNAcc;
-      if (!warp_wait_cl(&b.accfull[buf], (tt / kNAcc) & 1, abort_flag, p.status)) break;
+      const int buf = gt % kNAcc;
+      if (!warp_wait_cl(&b.accfull[buf], (gt / kNAcc) & 1, abort_flag, p.status)) break;
       tc::tc_fence_after();
       const int vx = t * kTileN + hs * kHalf;        // first column of this warp's U box
       if (vx < p.V) {
@@ -988,7 +1015,7 @@ __global__ void __launch_bounds__(128 + 32 * EW, 1)
             tc::tmem_ld_32x32b_x32_wait(tmem_base + ((uint32_t)(q * 32) << 16) +
                                             (uint32_t)(buf * kTileN + (v0 - t * kTileN)),
                                         acc);
-            foldN<32>(st, acc, u + 4 * c, v0, p, rid);
+            foldN<32>(st, acc, u + 4 * c, v0, p, rid, j);
           }
         }
       }
@@ -1022,6 +1049,17 @@ __global__ void __launch_bounds__(128 + 32 * EW, 1)
         atomicMax(&p.keys[(size_t)j * p.R_max + r], make_key(st.best_z, st.best_v));
         p.parts[((size_t)j * p.n_part + vr) * p.R_max + r] = make_float2(st.m2, st.s);
       }
+    }
+    if (j + 1 < p.j_end) {
+      // position j published by this CTA: one release arrival on the
+      // launch's counter (an aborted CTA raises the launch's abort word)
+      asm volatile("bar.sync 1, %0;" ::"n"(32 * EW) : "memory");
+      if (e == 0 && lane == 0) {
+        __threadfence();
+        atomicAdd(&p.step_sync[j], 1u);
+        if (*abort_flag) atomicExch(&p.step_sync[kStepAbort], 1u);
+      }
+    }
     }
   }
   tc::tc_fence_before();
@@ -1548,6 +1586,30 @@ static bool use_pair(int R) {
   return MT >= 2 && MT % 2 == 0;
 }
 
+// Whether every cluster of a pair launch can be resident at once (one CTA
+// per SM): the condition for running all draft steps in one launch, whose
+// CTAs wait for one another between steps.  Asked once per device and grid.
+static bool pair_grid_resident(const Ctx& ctx, const cudaLaunchConfig_t& cfg,
+                               const cudaLaunchAttribute& cluster) {
+  // cache word: 1 (valid) | ok << 1 | grid << 2 | device << 34
+  static std::atomic<unsigned long long> cache{0ull};
+  const unsigned long long key =
+      ((unsigned long long)(unsigned)ctx.cfg.device << 34) | ((unsigned long long)cfg.gridDim.x << 2);
+  const unsigned long long c = cache.load(std::memory_order_relaxed);
+  if ((c & 1ull) && (c & ~3ull) == key) return (c & 2ull) != 0;
+  cudaLaunchConfig_t q = cfg;
+  cudaLaunchAttribute at = cluster;
+  q.attrs = &at;
+  q.numAttrs = 1;
+  int n = 0;
+  const cudaError_t e =
+      cudaOccupancyMaxActiveClusters(&n, propose_tc_pair_kernel<kPairEpiWarps>, &q);
+  if (e != cudaSuccess) cudaGetLastError();   // unknown: one launch per step
+  const bool ok = e == cudaSuccess && 2ull * (unsigned)n >= cfg.gridDim.x;
+  cache.store(key | 1ull | (ok ? 2ull : 0ull), std::memory_order_relaxed);
+  return ok;
+}
+
 cudaError_t launch_propose_tc(const Ctx& ctx, const ProposeArgs& a, cudaStream_t s) {
   PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
   if (!encode) return cudaErrorNotSupported;
@@ -1576,8 +1638,12 @@ cudaError_t launch_propose_tc(const Ctx& ctx, const ProposeArgs& a, cudaStream_t
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return cudaErrorInvalidValue;
   }
+  // the keys and, right after them, the position counters of a
+  // several-position launch
   cudaError_t e = cudaMemsetAsync(ctx.ws.keys, 0,
-                                  sizeof(unsigned long long) * (size_t)a.gamma * ctx.cfg.R_max, s);
+                                  sizeof(unsigned long long) * (size_t)ctx.cfg.gamma * ctx.cfg.R_max +
+                                      sizeof(unsigned int) * kStepSyncWords,
+                                  s);
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(propose_tc_kernel<kSingleEpiWarps, false, false>,
                            cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
@@ -1611,6 +1677,7 @@ cudaError_t launch_propose_tc(const Ctx& ctx, const ProposeArgs& a, cudaStream_t
   p.inv_T = a.temperature > 0.f ? 1.f / a.temperature : 1.f;
   p.k0 = (uint32_t)(a.seed & 0xFFFFFFFFull);
   p.k1 = (uint32_t)(a.seed >> 32);
+  p.step_sync = ctx.ws.step_sync;
   p.n_vr = split ? tc_vranges_split(ctx, a.R) : tc_vranges(ctx, a.R);
   p.dup = !split && a.R <= kTileM / 2 ? 1 : 0;
   p.A = a.gate_h ? a.gated_rep : nullptr;
@@ -1621,10 +1688,12 @@ cudaError_t launch_propose_tc(const Ctx& ctx, const ProposeArgs& a, cudaStream_t
     if (e != cudaSuccess) return e;
   }
 
-  // One launch per step: the next step's A operand needs every CTA's argmax.
-  // Steps after the first are launched with a programmatic dependency on the
-  // previous step (see griddepcontrol in the kernel); the first follows the
-  // memset of the keys in plain stream order.
+  // The next step's A operand needs every CTA's argmax.  Pairs whose whole
+  // grid fits on the device at once run all draft steps in one launch, the
+  // CTAs meeting at a counter per position (p.step_sync); otherwise one
+  // launch per step, steps after the first launched with a programmatic
+  // dependency on the previous step (see griddepcontrol in the kernel).
+  // The first launch follows the memset of the keys in plain stream order.
   // Pairs: clusters of two CTAs, block 2 c + m = M-tile 2 (c / n_vr) + m of
   // vocabulary range c % n_vr.
   cudaLaunchAttribute attr[2];
@@ -1640,8 +1709,10 @@ cudaError_t launch_propose_tc(const Ctx& ctx, const ProposeArgs& a, cudaStream_t
   cfg.dynamicSmemBytes = pair ? kPSmemBytes : kSmemBytes;
   cfg.stream = s;
   cfg.attrs = pair ? attr : attr + 1;
-  for (int j = 0; j < a.gamma; ++j) {
+  const bool whole = pair && a.gamma > 1 && pair_grid_resident(ctx, cfg, attr[0]);
+  for (int j = 0; j < a.gamma; j = p.j_end) {
     p.j = j;
+    p.j_end = whole ? a.gamma : j + 1;
     if (a.gate_h) {   // this step's representation from the tokens of the last
       e = a.rnn_W ? launch_rnn_step(ctx, a, j, s) : launch_gate_step(ctx, a, j, s);
       if (e != cudaSuccess) return e;

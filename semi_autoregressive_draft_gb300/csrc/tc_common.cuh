@@ -53,6 +53,26 @@ __device__ __forceinline__ void drain_bar_cl(uint64_t* bar, uint32_t parity) {
     if (tc::mbar_try_wait_cluster(bar, parity)) return;
 }
 
+// Bounded wait for a counter in global memory that the CTAs of one launch
+// (all resident at once) raise: acquire at gpu scope once it reaches target.
+// Gives up when the launch's abort word is raised (another CTA failed), or
+// after kSpinLimit polls (records DSD_ERR_TIMEOUT and raises the abort word).
+__device__ __forceinline__ bool wait_count_gpu(const unsigned int* c, unsigned int target,
+                                               unsigned int* abort_word, volatile int* abort_flag,
+                                               int* status) {
+  for (uint32_t i = 0; i < kSpinLimit; ++i) {
+    unsigned int v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(c) : "memory");
+    if (v >= target) return true;
+    if ((i & 31u) == 31u && (*abort_flag || *(volatile unsigned int*)abort_word)) return false;
+    __nanosleep(32);
+  }
+  set_status(status, kErrTimeout);
+  atomicExch(abort_word, 1u);
+  *abort_flag = 1;
+  return false;
+}
+
 // Bounded wait that ignores the abort flag: used to drain copies in flight
 // before the CTA exits.
 __device__ __forceinline__ void drain_bar(uint64_t* bar, uint32_t parity) {
