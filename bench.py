@@ -246,6 +246,28 @@ def tensor_report(spec, phase_s, engine):
             "frac": achieved / peak}
 
 
+def fma_report(flops, phase_s, engine):
+    """The CUDA-core engine's inner products (2 R r V flops per draft step) on
+    the fp32 FMA pipes, against their peak derived from unit counts and the
+    clock: SMs x 128 fp32 lanes x 2 flops x the maximum SM clock
+    (MEASURED_PEAKS.json sm_max_mhz, else 2070 MHz).  At R = 16 this work,
+    not the table bytes, bounds the engine: 1.24 GFLOP per step is 15 us at
+    the peak against 12 us for its 82.7 MB at the measured copy rate."""
+    import torch
+
+    try:
+        with open(PEAKS_FILE) as f:
+            mhz, kind = float(json.load(f)["sm_max_mhz"]), "MEASURED_PEAKS.json sm_max_mhz"
+    except (OSError, ValueError, KeyError):
+        mhz, kind = 2070.0, "nominal maximum SM clock"
+    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    peak = sms * 128 * 2 * mhz * 1e6 / 1e12
+    achieved = flops / phase_s / 1e12
+    return {"engine": engine, "bound": "alu", "flops": flops, "achieved_tflops": achieved,
+            "peak_tflops": peak, "frac": achieved / peak,
+            "peak_kind": f"derived: {sms} SMs x 128 fp32 lanes x 2 x {mhz:.0f} MHz ({kind})"}
+
+
 def propose_w_once_bytes(spec):
     """The phase's compulsory bytes: every U row once and W once for the
     whole phase (the lower bound if W stayed in L2 across the steps)."""
@@ -797,6 +819,8 @@ def run_hidden_head(args, dsd, synth, dev, world, head):
         "cpu_baseline": None, "e2e": None,
         "gpu_launches": launches, "clocks": clk,
     }
+    if ctx.last_engine() == "simt":
+        line["roofline"]["fma"] = fma_report(2.0 * R * r * V * G, ms / 1e3, "simt")
     ctx.close()
     return line
 
@@ -874,6 +898,7 @@ def run_candidates(args, dsd, synth, dev, world):
         "cpu_baseline": None, "e2e": None,
         "gpu_launches": launches, "clocks": clk,
     }
+    line["roofline"]["fma"] = fma_report(2.0 * R * r * V * G, ms / 1e3, "simt")
     ctx.close()
     return line
 
@@ -1021,6 +1046,33 @@ def run_ours(args):
     tokens_per_cycle = int((acc + 1).sum())
     B = int((keep + 1).sum())
 
+    # the verify phase's read floor: where every request keeps the same
+    # number of draft tokens, verification reads one row per request at the
+    # same position; a library reduction over exactly those rows, captured
+    # in a graph and timed like the verify phase, shows what a plain read of
+    # those bytes costs on this GPU
+    read_floor = None
+    if (keep == keep[0]).all():
+        rows = x["P"].view(spec.R, spec.G + 1, spec.V)[:, int(keep[0]), :]
+        g_rf = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_rf, stream=stream):
+            torch.amax(rows, dim=1)
+        rf_evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)]
+                  for _ in range(args.steps)]
+        with torch.cuda.stream(stream):
+            for ev in rf_evs:
+                flush.zero_()
+                ev[0].record(stream)
+                g_rf.replay()
+                ev[1].record(stream)
+        stream.synchronize()
+        rf_ms = statistics.mean(ev[0].elapsed_time(ev[1]) for ev in rf_evs)
+        rf_bytes = spec.R * spec.V * (2 if spec.dtype == "bf16" else 4)
+        read_floor = {"kernel": "torch.amax over the rows verification reads (library kernel), "
+                                "one graph per replay, L2 flushed before each",
+                      "ms": rf_ms, "bytes": rf_bytes, "GBps": rf_bytes / (rf_ms / 1e3) / 1e9,
+                      "verify_phase_ms": statistics.mean(ver_ms)}
+
     # acceptance of the scheduled cycle, and of one untimed pass that keeps
     # every draft position (l = gamma for all requests), so the histogram and
     # the per-position conditional accept rate cover every position
@@ -1099,15 +1151,19 @@ def run_ours(args):
                 "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)",
                 "traffic": traffic_for(engine_kernel, spec.name),
                 "alg_bytes": propose_step_bytes(spec),
-                "per": "one draft-step launch; achieved = gamma launches' bytes + the phase's "
-                       "small I/O over the propose phase's mean time (gamma launches and the "
-                       "finalize)",
-                "alg_bytes_note": "per launch: the U rows of one position + all of W + the "
+                "per": "one draft step (the pair engine runs all gamma steps in one launch, the "
+                       "single-CTA engine one launch per step); achieved = gamma steps' bytes + "
+                       "the phase's small I/O over the propose phase's mean time (the launches "
+                       "and the finalize); traffic = DRAM bytes per draft step",
+                "alg_bytes_note": "per step: the U rows of one position + all of W + the "
                                   "gathered E rows + the argmax keys",
                 "w_once": {"achieved": w_once, "frac": w_once / peak,
                            "alg_bytes": propose_w_once_bytes(spec),
                            "note": "the same time against U rows once + W once per phase"},
                 "tensor": tensor_report(spec, prop_mean_s, engine_used)}
+    if engine_used == "simt":
+        roofline["fma"] = fma_report(2.0 * spec.R * spec.r * spec.V * spec.G, prop_mean_s,
+                                     engine_used)
     vbytes = verify_alg_bytes(spec, B)
 
     cpu = None
@@ -1130,6 +1186,7 @@ def run_ours(args):
                               "one graph each (adds a graph launch each); the timed cycle "
                               "(dsd_cycle) runs the schedule inside the proposal's last launch"},
         "verify_alg_GBps": vbytes / (statistics.mean(ver_ms) / 1e3) / 1e9,
+        "verify_read_floor": read_floor,
         "acceptance": acceptance,
         "roofline": roofline,
         "cpu_baseline": cpu,
