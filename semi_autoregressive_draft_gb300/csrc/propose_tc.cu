@@ -97,6 +97,8 @@ static_assert(kTmemCols == 512, "TMEM allocation is a power of two <= 512 column
 #define TC_CHECK(cond, site) true
 #endif
 
+constexpr int kStepAbort = kMaxGamma;    // abort word of a several-position launch
+
 struct TcParams {
   const __nv_bfloat16* E;
   const int32_t* prev_tok;
@@ -294,7 +296,6 @@ __global__ void __launch_bounds__(128 + 32 * EW, 1)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int KC = p.rank / kKChunk;
-  const int j = p.j;
   const int mt = blockIdx.x / p.n_vr;
   const int vr = blockIdx.x - mt * p.n_vr;
   const int r0 = mt * kRowsM;        // first request of this CTA's M-tile
@@ -344,6 +345,7 @@ __global__ void __launch_bounds__(128 + 32 * EW, 1)
     if (lane == 0) {
       const uint64_t pol = policy_evict_last();
       uint32_t it = 0;
+      for (int jj = p.j; jj < p.j_end; ++jj)     // the same W tiles at every position
       for (int t = t0; t < t1 && !*abort_flag; ++t)
         for (int k0 = 0; k0 < KC; k0 += kCPS, ++it) {
           const int s = it % kNB;
@@ -373,13 +375,14 @@ __global__ void __launch_bounds__(128 + 32 * EW, 1)
       uint64_t* empty = b.uempty + hs * kNU;
       unsigned char* ring = sU + hs * kNU * kBox;
       uint32_t it = 0;
+      for (int jj = p.j; jj < p.j_end; ++jj)
       for (int t = t0; t < t1 && !*abort_flag; ++t) {
         const int vx = t * kTileN + hs * kHalf;
         if (vx >= p.V) break;
         const int s = it % kNU;
         if (!wait_bar(&empty[s], ((it / kNU) & 1) ^ 1, abort_flag, p.status)) break;
         tc::mbar_arrive_expect_tx(&full[s], kUBytes);
-        tc::tma_load_3d(ring + s * kBox, &tmU, &full[s], vx, j, r0, pol);
+        tc::tma_load_3d(ring + s * kBox, &tmU, &full[s], vx, jj, r0, pol);
         ++it;
       }
       for (uint32_t k = (it > kNU ? it - kNU : 0); k < it; ++k)
@@ -391,17 +394,21 @@ __global__ void __launch_bounds__(128 + 32 * EW, 1)
     // ------------------------------------------------------ MMA issuer
     if (lane == 0) {
       uint32_t bit = 0;
-      bool ok = wait_bar(b.aready, 0, abort_flag, p.status);
-      tc::tc_fence_after();
+      bool ok = true;
       // Descriptors of the first A box and the first W stage; the others
       // differ only in the start-address field, which counts 16-byte units.
       // Every operand lies inside this CTA's shared memory (< 2^18 bytes), so
       // adding an offset in those units never carries out of the field.
       const uint64_t da0 = tc::sdesc_kmajor_sw128(tc::smem_u32(sA));
       const uint64_t db0 = tc::sdesc_kmajor_sw128(tc::smem_u32(sB));
-      for (int tt = 0; tt < nt && ok; ++tt) {
-        const int buf = tt % kNAcc;
-        ok = wait_bar(&b.accempty[buf], ((tt / kNAcc) & 1) ^ 1, abort_flag, p.status);
+      uint32_t gt = 0;   // tiles of the launch so far (accumulator ring position)
+      for (int jj = p.j; jj < p.j_end && ok; ++jj) {
+      // A of position jj gathered (one phase of aready per position)
+      ok = wait_bar(b.aready, (uint32_t)(jj - p.j) & 1u, abort_flag, p.status);
+      tc::tc_fence_after();
+      for (int tt = 0; tt < nt && ok; ++tt, ++gt) {
+        const int buf = gt % kNAcc;
+        ok = wait_bar(&b.accempty[buf], ((gt / kNAcc) & 1) ^ 1, abort_flag, p.status);
         if (!ok) break;
         tc::tc_fence_after();    // the epilogue's TMEM reads of this buffer are done
         const uint32_t d_tmem = tmem_base + (uint32_t)(buf * kTileN);
@@ -429,6 +436,7 @@ __global__ void __launch_bounds__(128 + 32 * EW, 1)
         }
         if (ok) tc::umma_commit(&b.accfull[buf]);
       }
+      }
       // all issued MMAs complete before TMEM is released
       tc::umma_commit(b.mmadone);
       drain_bar(b.mmadone, 0);
@@ -453,10 +461,25 @@ __global__ void __launch_bounds__(128 + 32 * EW, 1)
     const bool warp_rows = (!SPLIT || q < 2) && r0 + (DUP ? (q & 1) : q) * 32 < p.R;
     const uint32_t rid = valid ? (p.req_id ? p.req_id[r] : (uint32_t)r) : 0u;
 
-    // The keys of step j-1 come from the previous grid: wait until it has
-    // completed and its writes are visible (a no-op without a programmatic
-    // dependency).
-    asm volatile("griddepcontrol.wait;" ::: "memory");
+    uint32_t gt = 0;    // tiles of the launch so far (accumulator ring position)
+    uint32_t uit = 0;   // U boxes of the launch so far (U ring position)
+    // After a failure (the CTA's abort flag) every warp still runs every
+    // position's named barriers, with its waits failing at once, so that no
+    // warp is left at a bar.sync.
+    for (int j = p.j; j < p.j_end; ++j) {
+    if (j == p.j) {
+      // The keys of step j-1 come from the previous grid: wait until it has
+      // completed and its writes are visible (a no-op without a programmatic
+      // dependency).
+      asm volatile("griddepcontrol.wait;" ::: "memory");
+    } else {
+      // every CTA of the launch has published position j - 1
+      if (e == 0 && lane == 0 && !*abort_flag &&
+          !wait_count_gpu(&p.step_sync[j - 1], gridDim.x, &p.step_sync[kStepAbort], abort_flag,
+                          p.status))
+        *abort_flag = 1;
+      asm volatile("bar.sync 1, %0;" ::"n"(32 * EW) : "memory");
+    }
 
     if constexpr (SPLIT) {
       // ---- A operand, split: the fp32 representation a of each request
@@ -581,12 +604,11 @@ __global__ void __launch_bounds__(128 + 32 * EW, 1)
     uint64_t* empty = b.uempty + hs * kNU;
     const unsigned char* ring = sU + hs * kNU * kBox;
     const int c0 = (cbase - hs * kHalf) / 8;   // this thread's first 16-byte chunk of its U row
-    uint32_t uit = 0;
-    for (int tt = 0; tt < nt; ++tt) {
+    for (int tt = 0; tt < nt; ++tt, ++gt) {
       if (warp_aborted(abort_flag)) break;
       const int t = t0 + tt;
-      const int buf = tt % kNAcc;
-      if (!warp_wait(&b.accfull[buf], (tt / kNAcc) & 1, abort_flag, p.status)) break;
+      const int buf = gt % kNAcc;
+      if (!warp_wait(&b.accfull[buf], (gt / kNAcc) & 1, abort_flag, p.status)) break;
       tc::tc_fence_after();
       const int vx = t * kTileN + hs * kHalf;
       if (vx < p.V) {
@@ -662,6 +684,18 @@ __global__ void __launch_bounds__(128 + 32 * EW, 1)
       atomicMax(&p.keys[(size_t)j * p.R_max + r], make_key(st.best_z, st.best_v));
       p.parts[((size_t)j * p.n_part + vr) * p.R_max + r] = make_float2(st.m2, st.s);
     }
+    if (j + 1 < p.j_end) {
+      // position j published by this CTA (the merge's reads of the A region
+      // done before the next gather writes it): one release arrival on the
+      // launch's counter; an aborted CTA raises the launch's abort word
+      asm volatile("bar.sync 1, %0;" ::"n"(32 * EW) : "memory");
+      if (e == 0 && lane == 0) {
+        __threadfence();
+        atomicAdd(&p.step_sync[j], 1u);
+        if (*abort_flag) atomicExch(&p.step_sync[kStepAbort], 1u);
+      }
+    }
+    }
   }
   tc::tc_fence_before();
   __syncthreads();
@@ -695,11 +729,11 @@ __global__ void __launch_bounds__(128 + 32 * EW, 1)
 //   accfull[b]  1 arrival: commit to both CTAs after a tile's MMAs;
 //   accempty[b] 16 arrivals (8 epilogue warps of each CTA) on the first CTA's;
 //   aready      16 arrivals (A gathered in both CTAs) on the first CTA's;
-//   ufull/uempty per CTA, as in the single-CTA kernel.
+//   ufull/uempty per CTA, as in the single-CTA kernel;
+//   ugo         16 arrivals (this CTA's epilogue warps, first gather only).
 // Every barrier still has one consumer role that waits on each of its phases
 // in order.  Waits that see the peer's arrivals acquire at cluster scope.
 constexpr int kPCPS = 4;                 // W half-boxes (K-chunks) per ring stage: a whole tile
-constexpr int kStepAbort = kMaxGamma;    // abort word of a several-position launch
 constexpr int kPNB = 3;                  // W ring stages
 constexpr int kPNU = 2;                  // U ring slots per column half
 constexpr int kHalfBox = kBox / 2;       // [64 vocab x 64 K] bf16
@@ -708,7 +742,7 @@ constexpr int kPOffA = 0;
 constexpr int kPOffB = kPOffA + kMaxKC * kBox;                // 64 KB of A
 constexpr int kPOffU = kPOffB + kPNB * kPCPS * kHalfBox;      // + 96 KB of W halves
 constexpr int kPOffBar = kPOffU + 2 * kPNU * kBox;            // + 64 KB of U
-constexpr int kPNumBars = 2 * kPNB + 4 * kPNU + 2 * kNAcc + 2;
+constexpr int kPNumBars = 2 * kPNB + 4 * kPNU + 2 * kNAcc + 3;
 constexpr int kPSmemBytes = kPOffBar + kPNumBars * 8 + 64 + 1024;
 static_assert(kPSmemBytes <= 232448, "shared memory budget of one CTA");
 static_assert(kPOffB % 1024 == 0 && kPOffU % 1024 == 0 && kHalfBox % 1024 == 0,
@@ -745,6 +779,7 @@ __global__ void __launch_bounds__(128 + 32 * EW, 1)
   b.accempty = b.accfull + kNAcc;
   b.aready = b.accempty + kNAcc;
   b.mmadone = b.aready + 1;
+  uint64_t* ugo = b.mmadone + 1;   // this CTA's first A operand is gathered
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + kPNumBars);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + kPNumBars) + 1;
 
@@ -775,6 +810,7 @@ __global__ void __launch_bounds__(128 + 32 * EW, 1)
     }
     tc::mbar_init(b.aready, 2 * EW);
     tc::mbar_init(b.mmadone, 1);
+    tc::mbar_init(ugo, EW);
     *abort_flag = 0;
     tc::mbar_fence_init();
     tc::fence_proxy_async_smem();
@@ -836,6 +872,10 @@ __global__ void __launch_bounds__(128 + 32 * EW, 1)
       uint64_t* empty = b.uempty + hs * kPNU;
       unsigned char* ring = sU + hs * kPNU * kBox;
       uint32_t it = 0;
+      // the first U boxes wait for this CTA's first E-row gather, which would
+      // otherwise queue behind them in DRAM (U is needed only after the first
+      // MMA; W starts at once)
+      wait_bar(ugo, 0, abort_flag, p.status);
       for (int jj = p.j; jj < p.j_end; ++jj)
       for (int t = t0; t < t1 && !*abort_flag; ++t) {
         const int vx = t * kTileN + hs * kHalf;
@@ -974,6 +1014,7 @@ __global__ void __launch_bounds__(128 + 32 * EW, 1)
       tc::fence_proxy_async_smem();      // visible to the tensor cores of either SM
       __syncwarp();
       if (lane == 0) tc::mbar_arrive_cluster(aready0);
+      if (lane == 0 && j == p.j) tc::mbar_arrive(ugo);
     }
 
     // ---- tiles ----
@@ -1586,26 +1627,39 @@ static bool use_pair(int R) {
   return MT >= 2 && MT % 2 == 0;
 }
 
-// Whether every cluster of a pair launch can be resident at once (one CTA
-// per SM): the condition for running all draft steps in one launch, whose
-// CTAs wait for one another between steps.  Asked once per device and grid.
-static bool pair_grid_resident(const Ctx& ctx, const cudaLaunchConfig_t& cfg,
-                               const cudaLaunchAttribute& cluster) {
+// Whether every CTA (or cluster) of a launch can be resident at once, one
+// CTA per SM: the condition for running all draft steps in one launch,
+// whose CTAs wait for one another between steps.  Asked once per kernel,
+// device and grid.
+template <auto Kernel>
+static bool grid_resident(const Ctx& ctx, const cudaLaunchConfig_t& cfg, bool cluster) {
   // cache word: 1 (valid) | ok << 1 | grid << 2 | device << 34
   static std::atomic<unsigned long long> cache{0ull};
   const unsigned long long key =
       ((unsigned long long)(unsigned)ctx.cfg.device << 34) | ((unsigned long long)cfg.gridDim.x << 2);
   const unsigned long long c = cache.load(std::memory_order_relaxed);
   if ((c & 1ull) && (c & ~3ull) == key) return (c & 2ull) != 0;
-  cudaLaunchConfig_t q = cfg;
-  cudaLaunchAttribute at = cluster;
-  q.attrs = &at;
-  q.numAttrs = 1;
   int n = 0;
-  const cudaError_t e =
-      cudaOccupancyMaxActiveClusters(&n, propose_tc_pair_kernel<kPairEpiWarps>, &q);
+  cudaError_t e;
+  unsigned long long fits = 0;
+  if (cluster) {
+    cudaLaunchConfig_t q = cfg;
+    cudaLaunchAttribute at;
+    at.id = cudaLaunchAttributeClusterDimension;
+    at.val.clusterDim.x = 2;
+    at.val.clusterDim.y = 1;
+    at.val.clusterDim.z = 1;
+    q.attrs = &at;
+    q.numAttrs = 1;
+    e = cudaOccupancyMaxActiveClusters(&n, Kernel, &q);
+    fits = 2ull * (unsigned)n;
+  } else {
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, Kernel, (int)cfg.blockDim.x,
+                                                      cfg.dynamicSmemBytes);
+    fits = (unsigned long long)(unsigned)n * (unsigned)ctx.num_sms;
+  }
   if (e != cudaSuccess) cudaGetLastError();   // unknown: one launch per step
-  const bool ok = e == cudaSuccess && 2ull * (unsigned)n >= cfg.gridDim.x;
+  const bool ok = e == cudaSuccess && fits >= cfg.gridDim.x;
   cache.store(key | 1ull | (ok ? 2ull : 0ull), std::memory_order_relaxed);
   return ok;
 }
@@ -1688,11 +1742,12 @@ cudaError_t launch_propose_tc(const Ctx& ctx, const ProposeArgs& a, cudaStream_t
     if (e != cudaSuccess) return e;
   }
 
-  // The next step's A operand needs every CTA's argmax.  Pairs whose whole
-  // grid fits on the device at once run all draft steps in one launch, the
-  // CTAs meeting at a counter per position (p.step_sync); otherwise one
-  // launch per step, steps after the first launched with a programmatic
-  // dependency on the previous step (see griddepcontrol in the kernel).
+  // The next step's A operand needs every CTA's argmax.  A grid that fits on
+  // the device at once runs all draft steps in one launch, the CTAs meeting
+  // at a counter per position (p.step_sync); otherwise (or with a head
+  // kernel between the steps) one launch per step, steps after the first
+  // launched with a programmatic dependency on the previous step (see
+  // griddepcontrol in the kernel).
   // The first launch follows the memset of the keys in plain stream order.
   // Pairs: clusters of two CTAs, block 2 c + m = M-tile 2 (c / n_vr) + m of
   // vocabulary range c % n_vr.
@@ -1709,7 +1764,13 @@ cudaError_t launch_propose_tc(const Ctx& ctx, const ProposeArgs& a, cudaStream_t
   cfg.dynamicSmemBytes = pair ? kPSmemBytes : kSmemBytes;
   cfg.stream = s;
   cfg.attrs = pair ? attr : attr + 1;
-  const bool whole = pair && a.gamma > 1 && pair_grid_resident(ctx, cfg, attr[0]);
+  // all steps in one launch unless a head kernel runs between the steps
+  bool whole = false;
+  if (a.gamma > 1 && !a.gate_h)
+    whole = pair    ? grid_resident<propose_tc_pair_kernel<kPairEpiWarps>>(ctx, cfg, true)
+            : split ? grid_resident<propose_tc_kernel<kSingleEpiWarps, false, true>>(ctx, cfg, false)
+            : p.dup ? grid_resident<propose_tc_kernel<kSingleEpiWarps, true, false>>(ctx, cfg, false)
+                    : grid_resident<propose_tc_kernel<kSingleEpiWarps, false, false>>(ctx, cfg, false);
   for (int j = 0; j < a.gamma; j = p.j_end) {
     p.j = j;
     p.j_end = whole ? a.gamma : j + 1;
