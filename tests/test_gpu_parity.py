@@ -149,6 +149,23 @@ def test_cycle_tc_shapes(dsd, R, V, rank, temperature):
     check_cycle(spec, x, k)
 
 
+@pytest.mark.parametrize("R,G,temperature", [
+    (256, 16, 0.0),    # CTA pairs, the largest gamma: every position counter of one launch
+    (256, 2, 1.0),     # CTA pairs, one counter, sampled
+    (256, 1, 0.0),     # one position: a single launch without counters
+    (64, 16, 1.0),     # single CTAs with repeated rows, sampled
+    (100, 16, 0.0),    # single CTAs, no repeated rows
+    (1, 16, 0.0),      # one request
+])
+def test_cycle_tc_gamma_range(dsd, R, G, temperature):
+    # all draft positions in one launch, the CTAs meeting at a counter per
+    # position, from one position up to the largest gamma
+    spec = synth.scaled(synth.CYCLE_SPECS["greedy"], R=R, G=G, V=1544, ew_std=0.3,
+                        temperature=temperature, seed=400 + R + G, n_sps=None)
+    x, k = run_cycle(dsd, spec, engine="tcgen05")
+    check_cycle(spec, x, k)
+
+
 @pytest.mark.parametrize("R,V,rank", [
     (19, 2568, 256),     # one 64-row block of the rejection list, ragged vocabulary tail
     (100, 1544, 128),    # two blocks, rank 128
