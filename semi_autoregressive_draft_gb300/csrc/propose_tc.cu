@@ -1178,11 +1178,19 @@ struct ResState {
 // WC consecutive columns of one row (a multiple of 4): x = acc + U, the
 // residual terms and the two Gumbel-max keys (one Philox block per four
 // columns).  uw / pw: the row's U and P values, two bf16 per word.
+// Base 2 throughout on the special-function unit: with pl2 = log2 p and
+// ql2 = log2 q, where p > q the residual's logarithm is
+// ln(p - q) = (pl2 + log2(1 - 2^d)) ln 2, d = ql2 - pl2 < 0.  For d > -1/2
+// (p within a factor of sqrt 2 of q) 1 - 2^d = -(e^u - 1), u = d ln 2 in
+// (-0.35, 0], from the Taylor series of e^u - 1 to u^7 / 5040 (the rest is
+// below u^8 / 40320, 5e-9), which keeps the relative accuracy when p ~ q;
+// below it 1 - 2^d >= 0.29 comes straight from 2^d.
 template <int WC>
 __device__ __forceinline__ void fold_res(ResState& st, const uint32_t (&acc)[WC],
                                          const uint32_t* uw, const uint32_t* pw, int v0,
                                          const ResParams& p, uint32_t rid, uint32_t pos, float lq,
                                          float lp) {
+  const float sT = p.inv_T * kLog2e, lq2 = lq * kLog2e, lp2 = lp * kLog2e;
 #pragma unroll
   for (int g = 0; g < WC / 4; ++g) {
     const uint32_t v = (uint32_t)(v0 + 4 * g);
@@ -1198,19 +1206,25 @@ __device__ __forceinline__ void fold_res(ResState& st, const uint32_t (&acc)[WC]
     const uint32_t words[4] = {ph.x, ph.y, ph.z, ph.w};
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-      const float ql = xs[e] * p.inv_T - lq;
-      const float pl = ps[e] * p.inv_T - lp;
+      const float ql2 = fmaf(xs[e], sT, -lq2);   // log2 q
+      const float pl2 = fmaf(ps[e], sT, -lp2);   // log2 p
       const float gg = gumbel_from_word(words[e]);
-      if (pl > ql) {
-        // log(p - q) = pl + log(1 - exp(ql - pl)), kept accurate when p ~ q
-        const float lr = pl + log1pf(-__expf(ql - pl));
+      const float pv = tc::ex2(pl2), qv = tc::ex2(ql2);
+      const float d = ql2 - pl2;
+      const float u = d * kLn2;
+      const float em1 =
+          u * (1.f + u * (0.5f + u * (1.f / 6.f + u * (1.f / 24.f +
+                                      u * (1.f / 120.f + u * (1.f / 720.f + u * (1.f / 5040.f)))))));
+      const float om = d > -0.5f ? -em1 : 1.f - tc::ex2(d);   // 1 - 2^d
+      if (pl2 > ql2) {
+        const float lr = (pl2 + lg2_approx(om)) * kLn2;
         const unsigned long long key = make_key(lr + gg, v + e);
         st.best = key > st.best ? key : st.best;
-        st.fsum += __expf(pl) - __expf(ql);
+        st.fsum += pv - qv;
       }
-      const unsigned long long key2 = make_key(pl + gg, v + e);
+      const unsigned long long key2 = make_key(pl2 * kLn2 + gg, v + e);
       st.best2 = key2 > st.best2 ? key2 : st.best2;
-      st.fsum2 += __expf(pl);
+      st.fsum2 += pv;
     }
   }
 }
