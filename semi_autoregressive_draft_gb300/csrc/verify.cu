@@ -234,19 +234,20 @@ __device__ __forceinline__ void fold_vec(RowFold& f, uint4 q, int v0, bool bonus
       }
     }
   } else {
-    float cmax = -INFINITY;
 #pragma unroll
-    for (int e = 0; e < epc; ++e) {
-      x[e] *= p.inv_T;
-      cmax = fmaxf(cmax, x[e] * kLog2e);
-    }
-    const float M = fmaxf(f.st.m, cmax);
-    float s = f.st.s * exp2f(f.st.m - M);
+    for (int e = 0; e < epc; ++e) x[e] *= p.inv_T;
+    if (!bonus) {
+      // a tested row: the normaliser of P/T (a bonus row needs only its key)
+      float cmax = -INFINITY;
 #pragma unroll
-    for (int e = 0; e < epc; ++e) s += exp2f(fmaf(x[e], kLog2e, -M));
-    f.st.m = M;
-    f.st.s = s;
-    if (bonus) {
+      for (int e = 0; e < epc; ++e) cmax = fmaxf(cmax, x[e] * kLog2e);
+      const float M = fmaxf(f.st.m, cmax);
+      float s = f.st.s * exp2f(f.st.m - M);
+#pragma unroll
+      for (int e = 0; e < epc; ++e) s += exp2f(fmaf(x[e], kLog2e, -M));
+      f.st.m = M;
+      f.st.s = s;
+    } else {
 #pragma unroll
       for (int e = 0; e < epc; e += 4) {
         const uint32_t v = (uint32_t)(v0 + e);
