@@ -100,6 +100,22 @@ __device__ __forceinline__ float lg2_approx(float x) {
   return y;
 }
 
+// log2(1 - 2^d) for d < 0: the log of the residual p - q = p (1 - 2^d) with
+// d = log2 q - log2 p.  For d > -1/2 (p within a factor of sqrt 2 of q),
+// 1 - 2^d = -(e^u - 1) with u = d ln 2 in (-0.35, 0), from the Taylor series
+// of e^u - 1 to u^7 / 5040 (the rest is below u^8 / 40320, 5e-9), which keeps
+// the relative accuracy as p approaches q; below it 1 - 2^d >= 0.29 comes
+// from the hardware 2^x.  Then the hardware base-2 logarithm.
+__device__ __forceinline__ float log2_one_minus_exp2(float d) {
+  const float u = d * 0.6931471805599453f;
+  const float em1 =
+      u * (1.f + u * (0.5f + u * (1.f / 6.f + u * (1.f / 24.f +
+                                  u * (1.f / 120.f + u * (1.f / 720.f + u * (1.f / 5040.f)))))));
+  float e2;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e2) : "f"(d));
+  return lg2_approx(d > -0.5f ? -em1 : 1.f - e2);
+}
+
 // Gumbel noise g = -ln(-ln u) of a Philox word, u = ((w >> 9) + 0.5) 2^-23.
 // t = -ln u: for u <= 15/16 from the hardware logarithm, whose absolute
 // error there is at most 2^-22 against |log2 u| >= 0.093, so t is within a

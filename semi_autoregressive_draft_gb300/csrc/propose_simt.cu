@@ -397,7 +397,7 @@ __global__ void __launch_bounds__(kSimtThreads) simt_bias_kernel(SimtParams p) {
           const float g = gumbel_from_word(nword[rho][i]);
           if (pl > ql) {
             // log(p - q) = pl + log(1 - exp(ql - pl)), kept accurate when p ~ q
-            const float lr = pl + log1pf(-__expf(ql - pl));
+            const float lr = pl + log2_one_minus_exp2((ql - pl) * kLog2e) * kLn2;
             const unsigned long long key = make_key(lr + g, (uint32_t)v);
             best[i] = key > best[i] ? key : best[i];
             fsum[i] += pv - qv;

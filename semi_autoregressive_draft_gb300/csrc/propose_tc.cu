@@ -1180,11 +1180,8 @@ struct ResState {
 // columns).  uw / pw: the row's U and P values, two bf16 per word.
 // Base 2 throughout on the special-function unit: with pl2 = log2 p and
 // ql2 = log2 q, where p > q the residual's logarithm is
-// ln(p - q) = (pl2 + log2(1 - 2^d)) ln 2, d = ql2 - pl2 < 0.  For d > -1/2
-// (p within a factor of sqrt 2 of q) 1 - 2^d = -(e^u - 1), u = d ln 2 in
-// (-0.35, 0], from the Taylor series of e^u - 1 to u^7 / 5040 (the rest is
-// below u^8 / 40320, 5e-9), which keeps the relative accuracy when p ~ q;
-// below it 1 - 2^d >= 0.29 comes straight from 2^d.
+// ln(p - q) = (pl2 + log2(1 - 2^d)) ln 2, d = ql2 - pl2 < 0
+// (log2_one_minus_exp2).
 template <int WC>
 __device__ __forceinline__ void fold_res(ResState& st, const uint32_t (&acc)[WC],
                                          const uint32_t* uw, const uint32_t* pw, int v0,
@@ -1210,14 +1207,9 @@ __device__ __forceinline__ void fold_res(ResState& st, const uint32_t (&acc)[WC]
       const float pl2 = fmaf(ps[e], sT, -lp2);   // log2 p
       const float gg = gumbel_from_word(words[e]);
       const float pv = tc::ex2(pl2), qv = tc::ex2(ql2);
-      const float d = ql2 - pl2;
-      const float u = d * kLn2;
-      const float em1 =
-          u * (1.f + u * (0.5f + u * (1.f / 6.f + u * (1.f / 24.f +
-                                      u * (1.f / 120.f + u * (1.f / 720.f + u * (1.f / 5040.f)))))));
-      const float om = d > -0.5f ? -em1 : 1.f - tc::ex2(d);   // 1 - 2^d
+      // computed by every lane (the lanes of a warp are different rows), used where p > q
+      const float lr = (pl2 + log2_one_minus_exp2(ql2 - pl2)) * kLn2;
       if (pl2 > ql2) {
-        const float lr = (pl2 + lg2_approx(om)) * kLn2;
         const unsigned long long key = make_key(lr + gg, v + e);
         st.best = key > st.best ? key : st.best;
         st.fsum += pv - qv;
