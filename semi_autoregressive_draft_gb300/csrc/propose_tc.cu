@@ -1634,9 +1634,9 @@ static bool use_pair(int R) {
 }
 
 // Whether every CTA (or cluster) of a launch can be resident at once, one
-// CTA per SM: the condition for running all draft steps in one launch,
-// whose CTAs wait for one another between steps.  Asked once per kernel,
-// device and grid.
+// CTA per SM: the condition for running all draft steps in one cooperative
+// launch, whose CTAs wait for one another between steps.  Asked once per
+// kernel, device and grid.
 template <auto Kernel>
 static bool grid_resident(const Ctx& ctx, const cudaLaunchConfig_t& cfg, bool cluster) {
   // cache word: 1 (valid) | ok << 1 | grid << 2 | device << 34
@@ -1757,19 +1757,24 @@ cudaError_t launch_propose_tc(const Ctx& ctx, const ProposeArgs& a, cudaStream_t
   // The first launch follows the memset of the keys in plain stream order.
   // Pairs: clusters of two CTAs, block 2 c + m = M-tile 2 (c / n_vr) + m of
   // vocabulary range c % n_vr.
-  cudaLaunchAttribute attr[2];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = pair ? 2 : 1;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchAttribute cluster_attr, coop_attr, pdl_attr;
+  cluster_attr.id = cudaLaunchAttributeClusterDimension;
+  cluster_attr.val.clusterDim.x = pair ? 2 : 1;
+  cluster_attr.val.clusterDim.y = 1;
+  cluster_attr.val.clusterDim.z = 1;
+  // a launch whose CTAs wait for one another is cooperative: it starts only
+  // when every CTA can be resident, also beside other work on the device
+  coop_attr.id = cudaLaunchAttributeCooperative;
+  coop_attr.val.cooperative = 1;
+  pdl_attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  pdl_attr.val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchAttribute attr[3];
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(128 + 32 * (pair ? kPairEpiWarps : kSingleEpiWarps));
   cfg.dynamicSmemBytes = pair ? kPSmemBytes : kSmemBytes;
   cfg.stream = s;
-  cfg.attrs = pair ? attr : attr + 1;
+  cfg.attrs = attr;
   // all steps in one launch unless a head kernel runs between the steps
   bool whole = false;
   if (a.gamma > 1 && !a.gate_h)
@@ -1785,7 +1790,13 @@ cudaError_t launch_propose_tc(const Ctx& ctx, const ProposeArgs& a, cudaStream_t
       if (e != cudaSuccess) return e;
     }
     // a head kernel in between: plain stream order
-    cfg.numAttrs = (pair ? 1 : 0) + (j > 0 && !a.gate_h ? 1 : 0);
+    int na = 0;
+    if (pair) attr[na++] = cluster_attr;
+    if (whole)
+      attr[na++] = coop_attr;
+    else if (j > 0 && !a.gate_h)
+      attr[na++] = pdl_attr;
+    cfg.numAttrs = (unsigned)na;
     e = pair    ? cudaLaunchKernelEx(&cfg, propose_tc_pair_kernel<kPairEpiWarps>, tmW, tmU, p)
         : split ? cudaLaunchKernelEx(&cfg, propose_tc_kernel<kSingleEpiWarps, false, true>, tmW, tmU, p)
         : p.dup ? cudaLaunchKernelEx(&cfg, propose_tc_kernel<kSingleEpiWarps, true, false>, tmW, tmU, p)
