@@ -89,7 +89,16 @@ enum dsd_act { DSD_ACT_NONE = 0, DSD_ACT_SILU = 1 };
  * plain head without an activation, on the CUDA cores otherwise.  MMA
  * (warp-level mma.sync tensor cores, same requirements) is only used when
  * asked for.  TCGEN05 or MMA asked for with a configuration they do not
- * support makes dsd_propose return DSD_ERR_UNSUPPORTED before any launch. */
+ * support makes dsd_propose return DSD_ERR_UNSUPPORTED before any launch.
+ * The tensor-core engine runs all draft steps of a call in one launch whose
+ * CTAs wait for one another between steps, when the whole grid fits on the
+ * device (else one launch per step, and always one per step for the gated
+ * and RNN heads).  That launch is cooperative: it starts only when every CTA
+ * can be resident, so calls on different streams may overlap.  The
+ * environment variable DSD_PROPOSE_COOPERATIVE=0 drops the cooperative
+ * attribute (for profilers that cannot replay cooperative launches); then
+ * two such launches overlapping on the device can each hold SMs the other
+ * needs, and their bounded waits end the calls with DSD_ERR_TIMEOUT. */
 enum dsd_engine {
   DSD_ENGINE_AUTO = 0,
   DSD_ENGINE_SIMT = 1,

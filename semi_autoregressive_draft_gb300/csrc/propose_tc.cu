@@ -55,6 +55,7 @@
 // the kernel records DSD_ERR_TIMEOUT, stops issuing work, waits (bounded) for
 // its own copies in flight, frees its TMEM and returns.
 #include <stdio.h>
+#include <stdlib.h>
 
 #include <atomic>
 
@@ -1633,6 +1634,18 @@ static bool use_pair(int R) {
   return MT >= 2 && MT % 2 == 0;
 }
 
+// The single launch is cooperative unless DSD_PROPOSE_COOPERATIVE=0: ncu
+// cannot replay a cooperative launch (the driver reports LaunchFailed), so
+// profiling runs set it to 0 and time the same kernel launched without the
+// attribute.  Read once.
+static bool cooperative_launches() {
+  static const bool on = [] {
+    const char* v = getenv("DSD_PROPOSE_COOPERATIVE");
+    return !(v && v[0] == '0');
+  }();
+  return on;
+}
+
 // Whether every CTA (or cluster) of a launch can be resident at once, one
 // CTA per SM: the condition for running all draft steps in one cooperative
 // launch, whose CTAs wait for one another between steps.  Asked once per
@@ -1792,10 +1805,11 @@ cudaError_t launch_propose_tc(const Ctx& ctx, const ProposeArgs& a, cudaStream_t
     // a head kernel in between: plain stream order
     int na = 0;
     if (pair) attr[na++] = cluster_attr;
-    if (whole)
-      attr[na++] = coop_attr;
-    else if (j > 0 && !a.gate_h)
+    if (whole) {
+      if (cooperative_launches()) attr[na++] = coop_attr;
+    } else if (j > 0 && !a.gate_h) {
       attr[na++] = pdl_attr;
+    }
     cfg.numAttrs = (unsigned)na;
     e = pair    ? cudaLaunchKernelEx(&cfg, propose_tc_pair_kernel<kPairEpiWarps>, tmW, tmU, p)
         : split ? cudaLaunchKernelEx(&cfg, propose_tc_kernel<kSingleEpiWarps, false, true>, tmW, tmU, p)
