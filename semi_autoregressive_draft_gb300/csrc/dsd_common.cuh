@@ -88,8 +88,12 @@ __device__ __forceinline__ uint32_t philox_pick(const Philox4& p, int i) {
 }
 
 // u = ((w >> 9) + 0.5) * 2^-23: exact in fp32, strictly inside (0, 1).
+// No integer-to-float conversion (a slow-pipe instruction): the 23 bits k
+// become the mantissa of 1 + k 2^-23, and subtracting 1 - 2^-24 (exact in
+// fp32) leaves (2k + 1) 2^-24, which has at most 24 significant bits, so
+// the subtraction is exact.
 __device__ __forceinline__ float uniform_from_word(uint32_t w) {
-  return (float(w >> 9) + 0.5f) * 1.1920928955078125e-07f;
+  return __uint_as_float((w >> 9) | 0x3F800000u) - 0.999999940395355224609375f;
 }
 
 // Hardware base-2 logarithm (MUFU): absolute error about 2^-22 for
@@ -116,25 +120,27 @@ __device__ __forceinline__ float log2_one_minus_exp2(float d) {
   return lg2_approx(d > -0.5f ? -em1 : 1.f - e2);
 }
 
-// Gumbel noise g = -ln(-ln u) of a Philox word, u = ((w >> 9) + 0.5) 2^-23.
-// t = -ln u: for u <= 15/16 from the hardware logarithm, whose absolute
-// error there is at most 2^-22 against |log2 u| >= 0.093, so t is within a
-// relative 3e-6; above 15/16 from the Taylor series of -ln(1 - d) in
-// d = 1 - u (exact in fp32), six terms, truncated below d^7/7 < 2^-26 of
-// t.  Then g = -ln t from the hardware logarithm, within about 3e-6.  The
-// winning draws (t small, g large) come from the series, accurate to fp32
-// rounding.
-__device__ __forceinline__ float gumbel_from_word(uint32_t w) {
-  const uint32_t k = w >> 9;
+// t = -ln u of a Philox word, u = ((w >> 9) + 0.5) 2^-23 (an Exp(1) draw).
+// For u <= 15/16 from the hardware logarithm, whose absolute error there is
+// at most 2^-22 against |log2 u| >= 0.093, so t is within a relative 3e-6;
+// above 15/16 (w >= 15 2^28) from the Taylor series of -ln(1 - d) in
+// d = 1 - u (exact in fp32 by Sterbenz' lemma), six terms, truncated below
+// d^7/7 < 2^-26 of t.  The smallest t (the draws that win a race) come from
+// the series, accurate to fp32 rounding.
+__device__ __forceinline__ float neg_ln_uniform(uint32_t w) {
   constexpr float kLn2f = 0.6931471805599453f;
-  float t;
-  if (k >= (15u << 19)) {   // u > 15/16
-    const float d = (float((1u << 23) - k) - 0.5f) * 1.1920928955078125e-07f;   // 1 - u
-    t = d * (1.f + d * (0.5f + d * (1.f / 3.f + d * (0.25f + d * (0.2f + d * (1.f / 6.f))))));
-  } else {
-    t = -kLn2f * lg2_approx(uniform_from_word(w));
+  const float u = uniform_from_word(w);
+  if (w >= (15u << 28)) {   // u > 15/16
+    const float d = 1.f - u;
+    return d * (1.f + d * (0.5f + d * (1.f / 3.f + d * (0.25f + d * (0.2f + d * (1.f / 6.f))))));
   }
-  return -kLn2f * lg2_approx(t);
+  return -kLn2f * lg2_approx(u);
+}
+
+// Gumbel noise g = -ln(-ln u) of a Philox word: t = -ln u as above, then
+// g = -ln t from the hardware logarithm, within about 3e-6.
+__device__ __forceinline__ float gumbel_from_word(uint32_t w) {
+  return -0.6931471805599453f * lg2_approx(neg_ln_uniform(w));
 }
 
 // ---------------------------------------------------------------------------
