@@ -18,7 +18,8 @@ constexpr int kCandMaxR = 32;        // requests per call of dsd_propose_candida
 constexpr int kGateZhFactor = 12;    // gated / RNN heads: split-K partials, 12 x R_max gamma x rank floats
 constexpr int kMaxSchedItems = 4096;  // R_max * gamma
 constexpr int kVerifySplits = 8;      // V chunks per verified row
-constexpr int kStepSyncWords = 32;    // kMaxGamma counters + an abort word, padded
+constexpr int kStepSyncWords = 64;    // kMaxGamma counters + an abort word, padded to 32,
+                                       // then 2 per position for a head's step phases
 
 // Status codes (mirror enum dsd_status in include/dsd.h).
 constexpr int kOk = 0;
@@ -121,6 +122,9 @@ cudaError_t launch_cand_finalize(const Ctx& ctx, const ProposeArgs& a, int n_use
 
 cudaError_t launch_propose_simt(const Ctx& ctx, const ProposeArgs& a, cudaStream_t s);
 cudaError_t launch_gate_h(const Ctx& ctx, const ProposeArgs& a, cudaStream_t s);
+struct HeadStepParams;
+// The per-step head arguments of a gated or RNN proposal (head_step.cuh).
+HeadStepParams head_step_params(const Ctx& ctx, const ProposeArgs& a);
 cudaError_t launch_gate_step(const Ctx& ctx, const ProposeArgs& a, int j, cudaStream_t s);
 cudaError_t launch_rnn_h(const Ctx& ctx, const ProposeArgs& a, cudaStream_t s);
 cudaError_t launch_rnn_step(const Ctx& ctx, const ProposeArgs& a, int j, cudaStream_t s);

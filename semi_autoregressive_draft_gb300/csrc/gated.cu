@@ -28,7 +28,7 @@
 // candidate and state update: the state and Markov columns of W_g and W_c)
 // and rnn_out_kernel (o_j from the new state), which writes the
 // representation the bias kernel and the verifier's residual pass read.
-#include "dsd_common.cuh"
+#include "head_step.cuh"
 
 namespace dsd {
 
@@ -36,21 +36,6 @@ namespace {
 
 constexpr int kGhBM = 64, kGhBN = 64, kGhBK = 32, kGhThreads = 256;
 constexpr int kGsOut = 8;          // outputs per CTA of the per-step kernels: one per warp
-
-template <typename T>
-__device__ __forceinline__ void load8(const T* p, float* x) {
-  const uint4 q = __ldg(reinterpret_cast<const uint4*>(p));
-  if constexpr (sizeof(T) == 2) {
-    x[0] = bf16lo(q.x); x[1] = bf16hi(q.x); x[2] = bf16lo(q.y); x[3] = bf16hi(q.y);
-    x[4] = bf16lo(q.z); x[5] = bf16hi(q.z); x[6] = bf16lo(q.w); x[7] = bf16hi(q.w);
-  } else {
-    const uint4 q2 = __ldg(reinterpret_cast<const uint4*>(p) + 1);
-    x[0] = __uint_as_float(q.x); x[1] = __uint_as_float(q.y);
-    x[2] = __uint_as_float(q.z); x[3] = __uint_as_float(q.w);
-    x[4] = __uint_as_float(q2.x); x[5] = __uint_as_float(q2.y);
-    x[6] = __uint_as_float(q2.z); x[7] = __uint_as_float(q2.w);
-  }
-}
 
 // Zh[s, n, k] = sum over c in split s (columns s width .. + width, below H)
 // of h[n, c] Wh[k, c], for n < rows, k < n_out (width a multiple of 32),
@@ -112,176 +97,30 @@ __global__ void __launch_bounds__(kGhThreads) gate_h_kernel(const T* __restrict_
   }
 }
 
-struct GateStepParams {
-  const void* E;
-  const void* W_g;
-  const float* Zh;                 // [n_split][R gamma][rank] split-K partials
-  int n_split, rows;
-  const int32_t* prev_tok;
-  const unsigned long long* keys;  // [gamma][R_max] argmax keys of the draft steps
-  float* A;                        // [R, gamma, rank] gated representation out
-  int* status;
-  int R_max, V, H, rank, gamma, j, act, bias_at_first;
-};
-
+// One CTA per request and 8 outputs, one warp per output.
 template <typename T>
-__global__ void __launch_bounds__(256) gate_step_kernel(GateStepParams p) {
-  extern __shared__ float ms[];   // [rank]
-  const int r = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int k0 = blockIdx.y * kGsOut, k1 = min(p.rank, k0 + kGsOut);   // this CTA's outputs
-  const size_t row = (size_t)r * p.gamma + p.j;
-  float* out = p.A + row * p.rank;
-  if (p.j == 0 && !p.bias_at_first) {   // position 0 carries no bias
-    for (int k = k0 + tid; k < k1; k += blockDim.x) out[k] = 0.f;
-    return;
-  }
-  int prev = p.j == 0 ? p.prev_tok[r] : (int)key_index(p.keys[(size_t)(p.j - 1) * p.R_max + r]);
-  if (prev < 0 || prev >= p.V) {
-    if (tid == 0) set_status(p.status, kErrArg);
-    prev = 0;
-  }
-  const T* E = static_cast<const T*>(p.E);
-  const T* Wg = static_cast<const T*>(p.W_g);
-  for (int k = tid; k < p.rank; k += blockDim.x)
-    ms[k] = act_apply(ld_elem(E, (size_t)prev * p.rank + k), p.act);
-  __syncthreads();
-  for (int k = k0 + warp; k < k1; k += blockDim.x / 32) {
-    const T* wrow = Wg + (size_t)k * (p.H + p.rank) + p.H;
-    float dot = 0.f;
-    for (int c = lane * 8; c < p.rank; c += 32 * 8) {
-      float w[8];
-      load8<T>(wrow + c, w);
-#pragma unroll
-      for (int e = 0; e < 8; ++e) dot = fmaf(w[e], ms[c + e], dot);
-    }
-    dot = warp_sum(dot);
-    if (lane == 0) {
-      float z = dot;
-      for (int sp = 0; sp < p.n_split; ++sp) z += p.Zh[((size_t)sp * p.rows + row) * p.rank + k];
-      const float g = z >= 0.f ? 1.f / (1.f + expf(-z)) : expf(z) / (1.f + expf(z));
-      if (!isfinite(z)) set_status(p.status, kErrNonfinite);
-      out[k] = g * ms[k];
-    }
-  }
-}
-
-struct RnnStepParams {
-  const void* E;
-  const void* W_rnn;               // [3][rank][2 rank + H]
-  const float* Zh;                 // [n_split][R gamma][3 rank] hidden-state parts
-  int n_split, rows;
-  const int32_t* prev_tok;
-  const unsigned long long* keys;  // [gamma][R_max] argmax keys of the draft steps
-  const float* s_prev;             // [R_max][rank] state after the previous position
-  float* s_new;                    // [R_max][rank] state after this position
-  float* A;                        // [R, gamma, rank] o_j out
-  int* status;
-  int R_max, V, H, rank, gamma, j, act, bias_at_first;
-  int first;                       // this is the first biased position: s_prev is zero
-};
-
-// The previous token of request r at step p.j (the anchor at j = 0).
-__device__ __forceinline__ int rnn_prev_token(const RnnStepParams& p, int r) {
-  int prev = p.j == 0 ? p.prev_tok[r] : (int)key_index(p.keys[(size_t)(p.j - 1) * p.R_max + r]);
-  if (prev < 0 || prev >= p.V) {
-    if (threadIdx.x == 0) set_status(p.status, kErrArg);
-    prev = 0;
-  }
-  return prev;
-}
-
-__device__ __forceinline__ float sigmoid_f(float z) {
-  return z >= 0.f ? 1.f / (1.f + expf(-z)) : expf(z) / (1.f + expf(z));
-}
-
-// Dot of a weight row's first 2 rank columns with [a; b] (a, b in shared
-// memory), one warp.
-template <typename T>
-__device__ __forceinline__ float rnn_dot2(const T* wrow, const float* a, const float* b, int rank) {
-  const int lane = threadIdx.x & 31;
-  float dot = 0.f;
-  for (int c = lane * 8; c < 2 * rank; c += 32 * 8) {
-    float w[8];
-    load8<T>(wrow + c, w);
-    const float* x = c < rank ? a + c : b + (c - rank);   // rank % 8 == 0: no group straddles
-#pragma unroll
-    for (int e = 0; e < 8; ++e) dot = fmaf(w[e], x[e], dot);
-  }
-  return warp_sum(dot);
+__global__ void __launch_bounds__(256) gate_step_kernel(HeadStepParams p, int j) {
+  const int r = blockIdx.x, warp = threadIdx.x >> 5;
+  const int k0 = blockIdx.y * kGsOut, k1 = min(p.rank, k0 + kGsOut);
+  for (int k = k0 + warp; k < k1; k += blockDim.x / 32) gate_outputs_warp<T, 1>(p, j, r, k);
 }
 
 // Gate, candidate and state update of one step: CTA = one request and 8
 // state units, one warp per unit.
 template <typename T>
-__global__ void __launch_bounds__(256) rnn_state_kernel(RnnStepParams p) {
-  extern __shared__ float sm[];   // [rank] previous state, [rank] Markov row
-  float* sp = sm;
-  float* ms = sm + p.rank;
-  const int r = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+__global__ void __launch_bounds__(256) rnn_state_kernel(HeadStepParams p, int j) {
+  const int r = blockIdx.x, warp = threadIdx.x >> 5;
   const int k0 = blockIdx.y * kGsOut, k1 = min(p.rank, k0 + kGsOut);
-  if (p.j == 0 && !p.bias_at_first) return;   // no bias, the state stays zero
-  const int prev = rnn_prev_token(p, r);
-  const T* E = static_cast<const T*>(p.E);
-  const T* Wr = static_cast<const T*>(p.W_rnn);
-  for (int k = tid; k < p.rank; k += blockDim.x) {
-    ms[k] = act_apply(ld_elem(E, (size_t)prev * p.rank + k), p.act);
-    sp[k] = p.first ? 0.f : p.s_prev[(size_t)r * p.rank + k];
-  }
-  __syncthreads();
-  const size_t row = (size_t)r * p.gamma + p.j;
-  const int ld = 2 * p.rank + p.H;
-  for (int k = k0 + warp; k < k1; k += blockDim.x / 32) {
-    const float dg = rnn_dot2<T>(Wr + (size_t)k * ld, sp, ms, p.rank);
-    const float dc = rnn_dot2<T>(Wr + (size_t)(p.rank + k) * ld, sp, ms, p.rank);
-    if (lane == 0) {
-      float zg = dg, zc = dc;
-      for (int q = 0; q < p.n_split; ++q) {
-        const float* z = p.Zh + ((size_t)q * p.rows + row) * 3 * p.rank;
-        zg += z[k];
-        zc += z[p.rank + k];
-      }
-      if (!isfinite(zg) || !isfinite(zc)) set_status(p.status, kErrNonfinite);
-      const float g = sigmoid_f(zg);
-      const float c = tanhf(zc);
-      p.s_new[(size_t)r * p.rank + k] = g * sp[k] + (1.f - g) * c;
-    }
-  }
+  for (int k = k0 + warp; k < k1; k += blockDim.x / 32) rnn_state_warp<T, 1>(p, j, r, k);
 }
 
 // Output of one step: o_j = tanh(W_o [s_j; m_j; h_j]), the representation
 // the bias projection multiplies.
 template <typename T>
-__global__ void __launch_bounds__(256) rnn_out_kernel(RnnStepParams p) {
-  extern __shared__ float sm[];   // [rank] new state, [rank] Markov row
-  float* sn = sm;
-  float* ms = sm + p.rank;
-  const int r = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+__global__ void __launch_bounds__(256) rnn_out_kernel(HeadStepParams p, int j) {
+  const int r = blockIdx.x, warp = threadIdx.x >> 5;
   const int k0 = blockIdx.y * kGsOut, k1 = min(p.rank, k0 + kGsOut);
-  const size_t row = (size_t)r * p.gamma + p.j;
-  float* out = p.A + row * p.rank;
-  if (p.j == 0 && !p.bias_at_first) {   // position 0 carries no bias
-    for (int k = k0 + tid; k < k1; k += blockDim.x) out[k] = 0.f;
-    return;
-  }
-  const int prev = rnn_prev_token(p, r);
-  const T* E = static_cast<const T*>(p.E);
-  const T* Wr = static_cast<const T*>(p.W_rnn);
-  for (int k = tid; k < p.rank; k += blockDim.x) {
-    ms[k] = act_apply(ld_elem(E, (size_t)prev * p.rank + k), p.act);
-    sn[k] = p.s_new[(size_t)r * p.rank + k];
-  }
-  __syncthreads();
-  const int ld = 2 * p.rank + p.H;
-  for (int k = k0 + warp; k < k1; k += blockDim.x / 32) {
-    const float d = rnn_dot2<T>(Wr + (size_t)(2 * p.rank + k) * ld, sn, ms, p.rank);
-    if (lane == 0) {
-      float z = d;
-      for (int q = 0; q < p.n_split; ++q)
-        z += p.Zh[((size_t)q * p.rows + row) * 3 * p.rank + 2 * p.rank + k];
-      if (!isfinite(z)) set_status(p.status, kErrNonfinite);
-      out[k] = tanhf(z);
-    }
-  }
+  for (int k = k0 + warp; k < k1; k += blockDim.x / 32) rnn_out_warp<T, 1>(p, j, r, k);
 }
 
 }  // namespace
@@ -329,16 +168,17 @@ cudaError_t launch_gate_h(const Ctx& ctx, const ProposeArgs& a, cudaStream_t s) 
   return launch_hidden(ctx, a, a.W_g, a.rank, a.H + a.rank, 0, s);
 }
 
-cudaError_t launch_gate_step(const Ctx& ctx, const ProposeArgs& a, int j, cudaStream_t s) {
-  GateStepParams p{};
+HeadStepParams head_step_params(const Ctx& ctx, const ProposeArgs& a) {
+  HeadStepParams p{};
   p.E = a.E;
-  p.W_g = a.W_g;
+  p.W = a.rnn_W ? a.rnn_W : a.W_g;
   p.Zh = ctx.ws.gate_zh;
   p.rows = a.R * a.gamma;
   int width;
-  gate_split(ctx, p.rows, a.H, a.rank, &p.n_split, &width);
+  gate_split(ctx, p.rows, a.H, a.rnn_W ? 3 * a.rank : a.rank, &p.n_split, &width);
   p.prev_tok = a.prev_tok;
   p.keys = ctx.ws.keys;
+  p.state = ctx.ws.rnn_state;
   p.A = a.gated_rep;
   p.status = ctx.ws.status;
   p.R_max = ctx.cfg.R_max;
@@ -346,15 +186,18 @@ cudaError_t launch_gate_step(const Ctx& ctx, const ProposeArgs& a, int j, cudaSt
   p.H = a.H;
   p.rank = a.rank;
   p.gamma = a.gamma;
-  p.j = j;
   p.act = a.act;
   p.bias_at_first = a.bias_at_first;
-  const size_t smem = sizeof(float) * a.rank;
+  return p;
+}
+
+cudaError_t launch_gate_step(const Ctx& ctx, const ProposeArgs& a, int j, cudaStream_t s) {
+  const HeadStepParams p = head_step_params(ctx, a);
   const dim3 grid(a.R, (a.rank + kGsOut - 1) / kGsOut);
   if (a.dtype == 1)
-    gate_step_kernel<__nv_bfloat16><<<grid, 256, smem, s>>>(p);
+    gate_step_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(p, j);
   else
-    gate_step_kernel<float><<<grid, 256, smem, s>>>(p);
+    gate_step_kernel<float><<<grid, 256, 0, s>>>(p, j);
   count_launch(ctx);
   return cudaGetLastError();
 }
@@ -364,37 +207,14 @@ cudaError_t launch_rnn_h(const Ctx& ctx, const ProposeArgs& a, cudaStream_t s) {
 }
 
 cudaError_t launch_rnn_step(const Ctx& ctx, const ProposeArgs& a, int j, cudaStream_t s) {
-  RnnStepParams p{};
-  p.E = a.E;
-  p.W_rnn = a.rnn_W;
-  p.Zh = ctx.ws.gate_zh;
-  p.rows = a.R * a.gamma;
-  int width;
-  gate_split(ctx, p.rows, a.H, 3 * a.rank, &p.n_split, &width);
-  p.prev_tok = a.prev_tok;
-  p.keys = ctx.ws.keys;
-  // the state ping-pongs between two buffers: position j writes buffer j % 2
-  p.s_prev = ctx.ws.rnn_state + (size_t)((j + 1) % 2) * ctx.cfg.R_max * a.rank;
-  p.s_new = ctx.ws.rnn_state + (size_t)(j % 2) * ctx.cfg.R_max * a.rank;
-  p.A = a.gated_rep;
-  p.status = ctx.ws.status;
-  p.R_max = ctx.cfg.R_max;
-  p.V = a.V;
-  p.H = a.H;
-  p.rank = a.rank;
-  p.gamma = a.gamma;
-  p.j = j;
-  p.act = a.act;
-  p.bias_at_first = a.bias_at_first;
-  p.first = (j == 0 || (j == 1 && !a.bias_at_first)) ? 1 : 0;
-  const size_t smem = sizeof(float) * 2 * a.rank;
+  const HeadStepParams p = head_step_params(ctx, a);
   const dim3 grid(a.R, (a.rank + kGsOut - 1) / kGsOut);
   if (a.dtype == 1) {
-    rnn_state_kernel<__nv_bfloat16><<<grid, 256, smem, s>>>(p);
-    rnn_out_kernel<__nv_bfloat16><<<grid, 256, smem, s>>>(p);
+    rnn_state_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(p, j);
+    rnn_out_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(p, j);
   } else {
-    rnn_state_kernel<float><<<grid, 256, smem, s>>>(p);
-    rnn_out_kernel<float><<<grid, 256, smem, s>>>(p);
+    rnn_state_kernel<float><<<grid, 256, 0, s>>>(p, j);
+    rnn_out_kernel<float><<<grid, 256, 0, s>>>(p, j);
   }
   count_launch(ctx, 2);
   return cudaGetLastError();

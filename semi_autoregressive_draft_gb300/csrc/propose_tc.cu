@@ -59,6 +59,7 @@
 
 #include <atomic>
 
+#include "head_step.cuh"
 #include "tc_common.cuh"
 
 namespace dsd {
@@ -99,6 +100,9 @@ static_assert(kTmemCols == 512, "TMEM allocation is a power of two <= 512 column
 #endif
 
 constexpr int kStepAbort = kMaxGamma;    // abort word of a several-position launch
+constexpr int kHeadSync = 32;            // + 2 j + phase: the head's step phases of position j
+static_assert(kStepAbort < kHeadSync && kHeadSync + 2 * kMaxGamma <= kStepSyncWords,
+              "step counters fit the workspace words");
 
 struct TcParams {
   const __nv_bfloat16* E;
@@ -120,6 +124,9 @@ struct TcParams {
   int act;                   // split mode without A: the activation of the E rows
   float inv_T;
   uint32_t k0, k1;
+  int head;                  // split mode in one launch: 1 gated head, 2 RNN head (their
+                             // per-step work runs inside the launch), else 0
+  HeadStepParams hs;         // the head's step arguments (head != 0)
 };
 
 struct Bars {
@@ -255,6 +262,48 @@ __device__ __forceinline__ void foldN(RowState& st, const uint32_t (&acc)[N], co
     }
     st.best_z = zb;
     st.best_v = vb;
+  }
+}
+
+// The sequential head's work for position j inside a one-launch proposal
+// (split mode): every epilogue warp of the grid takes outputs (request r,
+// two units k) in turn, with the routines of the standalone step kernels;
+// then the CTAs meet at a counter so that every output is written before any
+// CTA gathers it.  The RNN head has two such phases (the new state, then the
+// output from it).  After a failure the warps still pass both named barriers
+// of every phase.
+template <int EW>
+__device__ __forceinline__ void head_step_phases(const TcParams& p, int j, int e,
+                                                 volatile int* abort_flag) {
+  const int lane = threadIdx.x & 31;
+  const int nw = (int)gridDim.x * EW, gw = (int)blockIdx.x * EW + e;
+  constexpr int NK = 2;                       // outputs per warp task (rank % 8 == 0)
+  const int per_r = p.rank / NK;
+  const int n_task = p.R * per_r;
+  const int nph = p.head == 2 ? 2 : 1;
+  for (int ph = 0; ph < nph; ++ph) {
+    if (!warp_aborted(abort_flag)) {
+      for (int task = gw; task < n_task; task += nw) {
+        const int r = task / per_r, k0 = (task - r * per_r) * NK;
+        if (p.head == 1)
+          gate_outputs_warp<__nv_bfloat16, NK>(p.hs, j, r, k0);
+        else if (ph == 0)
+          rnn_state_warp<__nv_bfloat16, NK>(p.hs, j, r, k0);
+        else
+          rnn_out_warp<__nv_bfloat16, NK>(p.hs, j, r, k0);
+      }
+    }
+    unsigned int* ctr = &p.step_sync[kHeadSync + 2 * j + ph];
+    asm volatile("bar.sync 1, %0;" ::"n"(32 * EW) : "memory");   // this CTA's outputs written
+    if (e == 0 && lane == 0) {
+      __threadfence();
+      atomicAdd(ctr, 1u);
+      if (!*abort_flag &&
+          !wait_count_gpu(ctr, gridDim.x, &p.step_sync[kStepAbort], abort_flag, p.status))
+        *abort_flag = 1;
+      if (*abort_flag) atomicExch(&p.step_sync[kStepAbort], 1u);
+    }
+    asm volatile("bar.sync 1, %0;" ::"n"(32 * EW) : "memory");
   }
 }
 
@@ -482,6 +531,9 @@ __global__ void __launch_bounds__(128 + 32 * EW, 1)
       asm volatile("bar.sync 1, %0;" ::"n"(32 * EW) : "memory");
     }
 
+    if constexpr (SPLIT) {
+      if (p.head) head_step_phases<EW>(p, j, e, abort_flag);
+    }
     if constexpr (SPLIT) {
       // ---- A operand, split: the fp32 representation a of each request
       // (the head's buffer, or act(E[x_{j-1}])) as hi = bf16(a) in row i and
@@ -1788,17 +1840,22 @@ cudaError_t launch_propose_tc(const Ctx& ctx, const ProposeArgs& a, cudaStream_t
   cfg.dynamicSmemBytes = pair ? kPSmemBytes : kSmemBytes;
   cfg.stream = s;
   cfg.attrs = attr;
-  // all steps in one launch unless a head kernel runs between the steps
+  // all steps in one launch (with a gated or RNN head, the split kernel runs
+  // the head's step work itself)
   bool whole = false;
-  if (a.gamma > 1 && !a.gate_h)
+  if (a.gamma > 1 && (!a.gate_h || split))
     whole = pair    ? grid_resident<propose_tc_pair_kernel<kPairEpiWarps>>(ctx, cfg, true)
             : split ? grid_resident<propose_tc_kernel<kSingleEpiWarps, false, true>>(ctx, cfg, false)
             : p.dup ? grid_resident<propose_tc_kernel<kSingleEpiWarps, true, false>>(ctx, cfg, false)
                     : grid_resident<propose_tc_kernel<kSingleEpiWarps, false, false>>(ctx, cfg, false);
+  if (whole && a.gate_h) {
+    p.head = a.rnn_W ? 2 : 1;
+    p.hs = head_step_params(ctx, a);
+  }
   for (int j = 0; j < a.gamma; j = p.j_end) {
     p.j = j;
     p.j_end = whole ? a.gamma : j + 1;
-    if (a.gate_h) {   // this step's representation from the tokens of the last
+    if (a.gate_h && !whole) {   // this step's representation from the tokens of the last
       e = a.rnn_W ? launch_rnn_step(ctx, a, j, s) : launch_gate_step(ctx, a, j, s);
       if (e != cudaSuccess) return e;
     }

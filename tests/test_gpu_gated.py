@@ -168,3 +168,23 @@ def test_gated_on_each_engine(dsd, engine, R, temperature):
     x, k = run_gated(dsd, spec, gx, engine=engine)
     check_gated(spec, x, gx, k)
 
+
+
+def test_gated_in_launch_step_matches_the_step_kernels(dsd):
+    # the tensor-core engine runs the gate inside its one-launch proposal;
+    # the CUDA-core engine runs the standalone step kernel.  Both compute each
+    # output with the same warp routine, so wherever the drafted prefix is the
+    # same the representation is the same bit for bit.
+    spec = synth.scaled(synth.CYCLE_SPECS["greedy"], temperature=1.0, seed=75, p_noise=1.0,
+                        r=128, R=40, V=2568, ew_std=0.3)
+    gx = synth.gate_inputs(spec.R, spec.G, 96, spec.r, spec.ew_std, seed=76, device=DEV)
+    _, kt = run_gated(dsd, spec, gx, engine="tcgen05")
+    _, ks = run_gated(dsd, spec, gx, engine="simt")
+    same = 0
+    for q in range(spec.R):
+        for j in range(spec.G):
+            if np.array_equal(kt["tokens"][q, :j], ks["tokens"][q, :j]):
+                same += 1
+                assert np.array_equal(kt["gated_rep"][q, j].view(np.uint32),
+                                      ks["gated_rep"][q, j].view(np.uint32)), (q, j)
+    assert same >= 0.9 * spec.R * spec.G, same

@@ -171,3 +171,22 @@ def test_rnn_on_each_engine(dsd, engine, R, temperature):
     x, k = run_rnn(dsd, spec, rx, engine=engine)
     check_rnn(spec, x, rx, k)
 
+
+
+def test_rnn_in_launch_step_matches_the_step_kernels(dsd):
+    # the tensor-core engine runs the state and output phases inside its
+    # one-launch proposal, the CUDA-core engine the standalone step kernels;
+    # the same warp routines, so equal drafted prefixes give equal bits
+    spec = synth.scaled(synth.CYCLE_SPECS["greedy"], temperature=1.0, seed=85, p_noise=1.0,
+                        r=64, R=40, V=2568, ew_std=0.3)
+    rx = synth.rnn_inputs(spec.R, spec.G, 64, spec.r, spec.ew_std, seed=86, device=DEV)
+    _, kt = run_rnn(dsd, spec, rx, engine="tcgen05")
+    _, ks = run_rnn(dsd, spec, rx, engine="simt")
+    same = 0
+    for q in range(spec.R):
+        for j in range(spec.G):
+            if np.array_equal(kt["tokens"][q, :j], ks["tokens"][q, :j]):
+                same += 1
+                assert np.array_equal(kt["rnn_rep"][q, j].view(np.uint32),
+                                      ks["rnn_rep"][q, j].view(np.uint32)), (q, j)
+    assert same >= 0.9 * spec.R * spec.G, same
