@@ -1228,15 +1228,27 @@ struct ResState {
   float fsum, fsum2;
 };
 
-// WC consecutive columns of one row (a multiple of 4): x = acc + U, the
-// residual terms and the two Gumbel-max keys (one Philox block per four
-// columns).  uw / pw: the row's U and P values, two bf16 per word.
-// Base 2 throughout on the special-function unit: with pl2 = log2 p and
-// ql2 = log2 q, where p > q the residual's logarithm is
-// ln(p - q) = (pl2 + log2(1 - 2^d)) ln 2, d = ql2 - pl2 < 0
-// (log2_one_minus_exp2).
+// A thread's running state of the two draws inside the tile loop, each an
+// exponential race: the Gumbel-max draw argmax_v ln w_v - ln(-ln u_v) is
+// argmax_v w_v / t_v with t_v = -ln u_v, so the residual draw compares
+// (p - q) / t and the fallback draw p / t, by cross products, without
+// logarithms of the weights; the winner (w, t) becomes the key
+// ln w - ln t = ln w + g after the tile loop (race_keys).
+struct ResRace {
+  float rb, tb;     // residual: best p - q and its t (rb = 0: none yet)
+  float fb, tfb;    // fallback: best p and its t
+  uint32_t vb, vfb;
+  float fsum, fsum2;
+};
+
+// WC consecutive columns of one row (a multiple of 4): x = acc + U, then
+// p and q from their base-2 logits on the special-function unit (2^x), the
+// residual p - q, one Philox block per four columns for the races' t, and
+// the sums of (p - q)+ and of p.  uw / pw: the row's U and P values, two
+// bf16 per word.  p - q carries the error of the logits it comes from
+// (about 1e-6 of p), as the logarithm of the difference did.
 template <int WC>
-__device__ __forceinline__ void fold_res(ResState& st, const uint32_t (&acc)[WC],
+__device__ __forceinline__ void fold_res(ResRace& st, const uint32_t (&acc)[WC],
                                          const uint32_t* uw, const uint32_t* pw, int v0,
                                          const ResParams& p, uint32_t rid, uint32_t pos, float lq,
                                          float lp) {
@@ -1256,28 +1268,42 @@ __device__ __forceinline__ void fold_res(ResState& st, const uint32_t (&acc)[WC]
     const uint32_t words[4] = {ph.x, ph.y, ph.z, ph.w};
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-      const float ql2 = fmaf(xs[e], sT, -lq2);   // log2 q
-      const float pl2 = fmaf(ps[e], sT, -lp2);   // log2 p
-      const float gg = gumbel_from_word(words[e]);
-      const float pv = tc::ex2(pl2), qv = tc::ex2(ql2);
-      // computed by every lane (the lanes of a warp are different rows), used where p > q
-      const float lr = (pl2 + log2_one_minus_exp2(ql2 - pl2)) * kLn2;
-      if (pl2 > ql2) {
-        const unsigned long long key = make_key(lr + gg, v + e);
-        st.best = key > st.best ? key : st.best;
-        st.fsum += pv - qv;
+      const float pv = tc::ex2(fmaf(ps[e], sT, -lp2));   // p
+      const float qv = tc::ex2(fmaf(xs[e], sT, -lq2));   // q
+      const float t = neg_ln_uniform(words[e]);
+      const float r = pv - qv;
+      if (r > 0.f) {
+        st.fsum += r;
+        if (r * st.tb > st.rb * t) {
+          st.rb = r;
+          st.tb = t;
+          st.vb = v + e;
+        }
       }
-      const unsigned long long key2 = make_key(pl2 * kLn2 + gg, v + e);
-      st.best2 = key2 > st.best2 ? key2 : st.best2;
+      if (pv * st.tfb > st.fb * t) {
+        st.fb = pv;
+        st.tfb = t;
+        st.vfb = v + e;
+      }
       st.fsum2 += pv;
     }
   }
 }
 
+// The races' winners as packed keys (0: no entry with a positive weight).
+__device__ __forceinline__ ResState race_keys(const ResRace& st) {
+  ResState o;
+  o.best = st.rb > 0.f ? make_key((lg2_approx(st.rb) - lg2_approx(st.tb)) * kLn2, st.vb) : 0ull;
+  o.best2 = st.fb > 0.f ? make_key((lg2_approx(st.fb) - lg2_approx(st.tfb)) * kLn2, st.vfb) : 0ull;
+  o.fsum = st.fsum;
+  o.fsum2 = st.fsum2;
+  return o;
+}
+
 // One tile of one thread of the residual epilogue: its WC columns starting at
 // column `col` of the tile (TMEM lane = its row of A).
 template <int WC>
-__device__ __forceinline__ void res_tile(ResState& st, uint32_t tmem_addr,
+__device__ __forceinline__ void res_tile(ResRace& st, uint32_t tmem_addr,
                                          const unsigned char* urow, const unsigned char* prow,
                                          bool active, int v0, const ResParams& p, uint32_t rid,
                                          uint32_t pos, float lq, float lp) {
@@ -1545,7 +1571,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       if (lane == 0) tc::mbar_arrive(b.aready);
     }
 
-    ResState st{0ull, 0ull, 0.f, 0.f};
+    ResRace st{0.f, 1.f, 0.f, 1.f, 0u, 0u, 0.f, 0.f};
     uint64_t* full = b.ufull + hs * kRNU;
     uint64_t* empty = b.uempty + hs * kRNU;
     const unsigned char* ring = sU + hs * kRNU * kRSlot;
@@ -1583,7 +1609,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // ---- merge the 2 x 128 / nrep partial states of each list row ----
     // The A region is free: the last accumulator wait followed every MMA.
     ResState* xch = reinterpret_cast<ResState*>(sA);   // [2][kTileM]
-    xch[hs * kTileM + row] = st;
+    xch[hs * kTileM + row] = race_keys(st);
     asm volatile("bar.sync 1, 256;" ::: "memory");
     if (hs == 0 && row < nvalid && TC_CHECK(req < p.R_max, 5)) {
       ResState m{0ull, 0ull, 0.f, 0.f};
