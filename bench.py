@@ -835,13 +835,14 @@ def run_rnn(args, dsd, synth, dev, world):
 
 def run_candidates(args, dsd, synth, dev, world):
     """The proposal with the Markov top-16 candidate sets on the greedy
-    workload (R=16, gamma=7, V=151936, rank 256), CUDA-core engine; beside it
-    the plain proposal on the same engine; L2 flushed between steps."""
+    workload (R=16, gamma=7, V=151936, rank 256) on the --engine chosen
+    (AUTO: the tensor-core engine's repeated-rows kernel); beside it the
+    plain proposal on the same engine; L2 flushed between steps."""
     import torch
 
     spec = synth.CYCLE_SPECS["greedy"]
     x = synth.cycle_inputs(spec, device=dev)
-    ctx = dsd.Context(spec.V, spec.r, spec.G, spec.R, dtype="bf16", engine="simt",
+    ctx = dsd.Context(spec.V, spec.r, spec.G, spec.R, dtype="bf16", engine=args.engine,
                       device=dev.index)
     stream = torch.cuda.Stream(device=dev)
     flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
@@ -880,8 +881,9 @@ def run_candidates(args, dsd, synth, dev, world):
     alg = G * V * r * 2 + R * G * V * 2 + R * G * r * 2 + R * G * 16 * 8
     peak, peak_kind = hbm_peak()
     achieved = alg / (ms / 1e3) / 1e9
+    eng = ctx.last_engine()
     line = {
-        "metric": "draft tokens/s with Markov top-16 candidate sets (CUDA-core engine) at R=16, "
+        "metric": "draft tokens/s with Markov top-16 candidate sets at R=16, "
                   "gamma=7, V=151936, rank 256",
         "value": world * R * G / (ms / 1e3), "unit": "draft tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
@@ -890,7 +892,11 @@ def run_candidates(args, dsd, synth, dev, world):
         "config": {"workload": f"candidates: R={R} gamma={G} V={V} rank={r} bf16 greedy",
                    "l2": "flushed between steps (512 MB write outside the events)"},
         "plain_propose_ms": plain_ms,
-        "roofline": {"bound": "hbm", "kernel": "simt_bias_kernel", "achieved": achieved,
+        "engine": f"{args.engine} -> {eng}",
+        "roofline": {"bound": "hbm",
+                     "kernel": ("propose_tc_kernel (candidate mode)" if eng == "tcgen05"
+                                else "simt_bias_kernel"),
+                     "achieved": achieved,
                      "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "peak_kind": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)",
                      "traffic": None, "alg_bytes": alg, "per": "one call",
@@ -898,7 +904,8 @@ def run_candidates(args, dsd, synth, dev, world):
         "cpu_baseline": None, "e2e": None,
         "gpu_launches": launches, "clocks": clk,
     }
-    line["roofline"]["fma"] = fma_report(2.0 * R * r * V * G, ms / 1e3, "simt")
+    if eng == "simt":
+        line["roofline"]["fma"] = fma_report(2.0 * R * r * V * G, ms / 1e3, "simt")
     ctx.close()
     return line
 

@@ -871,10 +871,25 @@ int dsd_propose_candidates(dsd_ctx* ctx, int R, const void* U, const void* E, co
   a.survival = survival;
   a.cand_tok = cand_tok;
   a.cand_logit = cand_logit;
-  cudaError_t e = launch_propose_simt(*ctx, a, s);
+  // the tensor-core engine keeps the candidate lists in its repeated-rows
+  // kernel (no activation); otherwise the CUDA-core engine
+  cudaError_t e;
+  int n_used;
+  char why[256];
+  if ((ctx->cfg.engine == DSD_ENGINE_TCGEN05 || auto_uses_tc(ctx, R)) &&
+      ctx->cfg.act == DSD_ACT_NONE && tc_supported(*ctx, why, sizeof(why))) {
+    e = launch_propose_tc(*ctx, a, s);
+    n_used = tc_parts_used(*ctx, a);
+    ctx->last_engine = DSD_ENGINE_TCGEN05;
+  } else if (ctx->cfg.engine == DSD_ENGINE_TCGEN05) {
+    return fail(ctx, DSD_ERR_UNSUPPORTED,
+                "candidate sets on the tensor-core engine need no activation and its tables");
+  } else {
+    e = launch_propose_simt(*ctx, a, s);
+    n_used = simt_grid(*ctx, a.V);
+    ctx->last_engine = DSD_ENGINE_SIMT;
+  }
   if (e != cudaSuccess) return cuda_fail(ctx, e, "candidate propose launch");
-  ctx->last_engine = DSD_ENGINE_SIMT;
-  const int n_used = simt_grid(*ctx, a.V);
   e = launch_propose_finalize_n(*ctx, a, n_used, s);
   if (e == cudaSuccess) e = launch_cand_finalize(*ctx, a, n_used, s);
   if (e != cudaSuccess) return cuda_fail(ctx, e, "propose finalize launch");

@@ -127,6 +127,8 @@ struct TcParams {
   int head;                  // split mode in one launch: 1 gated head, 2 RNN head (their
                              // per-step work runs inside the launch), else 0
   HeadStepParams hs;         // the head's step arguments (head != 0)
+  unsigned long long* cand_parts;   // candidate mode: [gamma][n_part][cand_R][kCandK] keys
+  int cand_R;
 };
 
 struct Bars {
@@ -307,18 +309,99 @@ __device__ __forceinline__ void head_step_phases(const TcParams& p, int j, int e
   }
 }
 
+// ---------------------------------------------------------------------------
+// Candidate mode (the Markov top-16 candidate sets, at most 32 requests, the
+// repeated-rows kernel): the U boxes hold 64 rows, and the rest of the U
+// region holds per request row a sorted top-16 of packed (logit, token) keys
+// of this CTA's columns (largest first, 0 = empty), the key of its 16th
+// entry (the admission threshold) and one 16-key buffer per folding thread
+// (4 column groups x 2 copies).  Each thread appends the keys of its tile's
+// columns that beat the threshold; after the tile one warp per row inserts
+// them into the list (warp-parallel insertion: a ballot of the entries above
+// the key gives its place, the rest shift down one lane) and the threshold
+// rises.  The lists go to the global parts at the end of each position.
+constexpr int kCandRows = 32;                              // request rows (R <= 32)
+constexpr int kCandSlots = 8;                              // folding threads per row
+constexpr int kCandUBox = kBox / 2;                        // a U box of 64 rows
+constexpr int kCandOffBuf = 2 * kNU * kCandUBox;           // within the U region
+constexpr int kCandOffCnt = kCandOffBuf + kCandRows * kCandSlots * kCandK * 8;
+constexpr int kCandOffList = kCandOffCnt + kCandRows * kCandSlots * 4;
+constexpr int kCandOffTau = kCandOffList + kCandRows * kCandK * 8;
+static_assert(kCandOffTau + kCandRows * 8 <= 2 * kNU * kBox, "candidate state fits the U region");
+
+// Append this thread's keys of N consecutive columns (x = acc + U, the
+// biased logits before any temperature) that beat the row's threshold.
+template <int N>
+__device__ __forceinline__ void cand_filter(const uint32_t (&acc)[N], const uint4* u, int v0,
+                                            int V, unsigned long long tau,
+                                            unsigned long long* buf, int& cnt) {
+  const float tv = tau ? key_value(tau) : -INFINITY;   // an empty list admits every key
+#pragma unroll
+  for (int c = 0; c < N / 8; ++c) {
+    const uint32_t w[4] = {u[c].x, u[c].y, u[c].z, u[c].w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int i = c * 8 + 2 * e;
+      float x0, x1;
+      add_bf16x2(w[e], acc[i], acc[i + 1], x0, x1);
+      // a key equal in value to the threshold may still beat it by index
+      if (x0 >= tv && v0 + i < V) {
+        const unsigned long long k = make_key(x0, (uint32_t)(v0 + i));
+        if (k > tau) buf[cnt++] = k;
+      }
+      if (x1 >= tv && v0 + i + 1 < V) {
+        const unsigned long long k = make_key(x1, (uint32_t)(v0 + i + 1));
+        if (k > tau) buf[cnt++] = k;
+      }
+    }
+  }
+}
+
+// One warp: insert the row's appended keys (kCandSlots buffers with counts
+// cnt[]) into its sorted list (lanes 0..15 hold it), then store the list and
+// its threshold.  Every key is distinct (token index in its low bits).
+__device__ __forceinline__ void cand_insert_row(unsigned long long* list, unsigned long long* tau,
+                                                const unsigned long long* bufs, int* cnt) {
+  const int lane = threadIdx.x & 31;
+  int total = 0;
+  int n[kCandSlots];
+#pragma unroll
+  for (int sl = 0; sl < kCandSlots; ++sl) {
+    n[sl] = cnt[sl];
+    total += n[sl];
+  }
+  if (total == 0) return;
+  unsigned long long L = lane < kCandK ? list[lane] : 0ull;
+#pragma unroll
+  for (int sl = 0; sl < kCandSlots; ++sl)
+    for (int i = 0; i < n[sl]; ++i) {
+      const unsigned long long k = bufs[sl * kCandK + i];
+      const unsigned int above = __ballot_sync(0xffffffffu, L > k) & 0xFFFFu;
+      const int pos = __popc(above);
+      const unsigned long long prev = __shfl_up_sync(0xffffffffu, L, 1);
+      if (pos < kCandK) L = lane < pos ? L : (lane == pos ? k : prev);
+    }
+  if (lane < kCandK) list[lane] = L;
+  const unsigned long long t16 = __shfl_sync(0xffffffffu, L, kCandK - 1);
+  if (lane == 0) *tau = t16;
+  __syncwarp();
+  if (lane < kCandSlots) cnt[lane] = 0;
+}
+
 // EW epilogue warps (8, or 16 with setmaxnreg 56 / 104 as in the pair
 // kernel): warp 4 + e folds column group e / 4 (EW / 4 groups of 128 / (EW/4)
 // columns per tile) of TMEM lane quarter warp % 4.  DUP (at most 64
 // requests): rows 64..127 of A repeat rows 0..63 and the two copies of a row
 // fold the two halves of each group's columns.
-template <int EW, bool DUP, bool SPLIT>
+template <int EW, bool DUP, bool SPLIT, bool CAND = false>
 __global__ void __launch_bounds__(128 + 32 * EW, 1)
     propose_tc_kernel(const __grid_constant__ CUtensorMap tmW,
                       const __grid_constant__ CUtensorMap tmU, const TcParams p) {
+  static_assert(!CAND || (DUP && !SPLIT && EW == 16), "candidates: the repeated-rows kernel");
   static_assert(!(DUP && SPLIT), "the split mode uses rows 64..127 of A for the low parts");
   constexpr int kRowsM = SPLIT ? 64 : kTileM;   // requests per M-tile
-  constexpr int kUBytes = SPLIT ? kBox / 2 : kBox;   // one U box ([kRowsM x 64] bf16)
+  constexpr int kUBytes = (SPLIT || CAND) ? kBox / 2 : kBox;   // one U box ([kRowsM x 64] bf16)
+  constexpr int kUSlot = CAND ? kCandUBox : kBox;   // U ring slot stride
   constexpr int kGroups = EW / 4;               // column groups per tile
   constexpr int kGCols = kTileN / kGroups;      // columns of a group (64 or 32)
   constexpr int kFW = DUP ? kGCols / 2 : kGCols;   // columns one thread folds per tile
@@ -423,7 +506,7 @@ __global__ void __launch_bounds__(128 + 32 * EW, 1)
       const uint64_t pol = policy_evict_first();
       uint64_t* full = b.ufull + hs * kNU;
       uint64_t* empty = b.uempty + hs * kNU;
-      unsigned char* ring = sU + hs * kNU * kBox;
+      unsigned char* ring = sU + hs * kNU * kUSlot;
       uint32_t it = 0;
       for (int jj = p.j; jj < p.j_end; ++jj)
       for (int t = t0; t < t1 && !*abort_flag; ++t) {
@@ -432,7 +515,7 @@ __global__ void __launch_bounds__(128 + 32 * EW, 1)
         const int s = it % kNU;
         if (!wait_bar(&empty[s], ((it / kNU) & 1) ^ 1, abort_flag, p.status)) break;
         tc::mbar_arrive_expect_tx(&full[s], kUBytes);
-        tc::tma_load_3d(ring + s * kBox, &tmU, &full[s], vx, jj, r0, pol);
+        tc::tma_load_3d(ring + s * kUSlot, &tmU, &full[s], vx, jj, r0, pol);
         ++it;
       }
       for (uint32_t k = (it > kNU ? it - kNU : 0); k < it; ++k)
@@ -655,47 +738,102 @@ __global__ void __launch_bounds__(128 + 32 * EW, 1)
     RowState st{-INFINITY, 0.f, -INFINITY, 0u};
     uint64_t* full = b.ufull + hs * kNU;
     uint64_t* empty = b.uempty + hs * kNU;
-    const unsigned char* ring = sU + hs * kNU * kBox;
+    const unsigned char* ring = sU + hs * kNU * kUSlot;
     const int c0 = (cbase - hs * kHalf) / 8;   // this thread's first 16-byte chunk of its U row
+    // candidate mode: this thread's buffer, its row's list and threshold
+    unsigned long long* c_list = reinterpret_cast<unsigned long long*>(sU + kCandOffList);
+    unsigned long long* c_tau = reinterpret_cast<unsigned long long*>(sU + kCandOffTau);
+    int* c_cnt = reinterpret_cast<int*>(sU + kCandOffCnt);
+    unsigned long long* c_buf = reinterpret_cast<unsigned long long*>(sU + kCandOffBuf);
+    const int c_slot = cg * 2 + copy;
+    const bool c_row = CAND && valid && rrow < kCandRows;
+    unsigned long long c_thr = 0ull;
+    int c_n = 0;
+    if constexpr (CAND) {
+      // empty lists for position j: warp e clears rows e and e + 16
+      for (int rr = e; rr < kCandRows; rr += EW) {
+        if (lane < kCandK) c_list[rr * kCandK + lane] = 0ull;
+        if (lane < kCandSlots) c_cnt[rr * kCandSlots + lane] = 0;
+        if (lane == 0) c_tau[rr] = 0ull;
+      }
+      asm volatile("bar.sync 2, %0;" ::"n"(32 * EW) : "memory");
+    }
     for (int tt = 0; tt < nt; ++tt, ++gt) {
-      if (warp_aborted(abort_flag)) break;
+      // A failed wait ends this warp's work; in candidate mode the warp still
+      // passes every tile's named barriers.
+      bool ok = !warp_aborted(abort_flag);
       const int t = t0 + tt;
       const int buf = gt % kNAcc;
-      if (!warp_wait(&b.accfull[buf], (gt / kNAcc) & 1, abort_flag, p.status)) break;
-      tc::tc_fence_after();
-      const int vx = t * kTileN + hs * kHalf;
-      if (vx < p.V) {
-        const int s = uit % kNU;
-        if (!warp_wait(&full[s], (uit / kNU) & 1, abort_flag, p.status)) break;
-        ++uit;
-        // 128-byte swizzle: 16-byte chunk c of row `rrow` sits at chunk
-        // c ^ (rrow & 7) of that row.
-        uint4 u[kFW / 8];
-        const unsigned char* urow = ring + s * kBox + rrow * 128;
-        if (warp_rows) {
+      if (ok) ok = warp_wait(&b.accfull[buf], (gt / kNAcc) & 1, abort_flag, p.status);
+      if (ok) {
+        tc::tc_fence_after();
+        const int vx = t * kTileN + hs * kHalf;
+        if (vx < p.V) {
+          const int s = uit % kNU;
+          ok = warp_wait(&full[s], (uit / kNU) & 1, abort_flag, p.status);
+          if (ok) {
+            ++uit;
+            // 128-byte swizzle: 16-byte chunk c of row `rrow` sits at chunk
+            // c ^ (rrow & 7) of that row.
+            uint4 u[kFW / 8];
+            const unsigned char* urow = ring + s * kUSlot + rrow * 128;
+            if (warp_rows) {
 #pragma unroll
-          for (int c = 0; c < kFW / 8; ++c)
-            u[c] = *reinterpret_cast<const uint4*>(urow + (((c0 + c) ^ (rrow & 7)) << 4));
-        }
-        __syncwarp();
-        if (lane == 0) tc::mbar_arrive(&empty[s]);   // the slot's data is in registers
-        __syncwarp();
-        if (warp_rows) {
+              for (int c = 0; c < kFW / 8; ++c)
+                u[c] = *reinterpret_cast<const uint4*>(urow + (((c0 + c) ^ (rrow & 7)) << 4));
+            }
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(&empty[s]);   // the slot's data is in registers
+            __syncwarp();
+            if (warp_rows) {
 #pragma unroll
-          for (int c = 0; c < kFW / kChunk; ++c) {
-            const int v0 = t * kTileN + cbase + c * kChunk;
-            if (v0 >= p.V) break;
-            uint32_t acc[kChunk];
-            tc::tmem_ld_wait<kChunk>(tmem_base + ((uint32_t)(q * 32) << 16) +
-                                         (uint32_t)(buf * kTileN + cbase + c * kChunk),
-                                     acc);
-            foldN<kChunk>(st, acc, u + (kChunk / 8) * c, v0, p, rid, j);
+              for (int c = 0; c < kFW / kChunk; ++c) {
+                const int v0 = t * kTileN + cbase + c * kChunk;
+                if (v0 >= p.V) break;
+                uint32_t acc[kChunk];
+                tc::tmem_ld_wait<kChunk>(tmem_base + ((uint32_t)(q * 32) << 16) +
+                                             (uint32_t)(buf * kTileN + cbase + c * kChunk),
+                                         acc);
+                foldN<kChunk>(st, acc, u + (kChunk / 8) * c, v0, p, rid, j);
+                if constexpr (CAND) {
+                  if (c_row)
+                    cand_filter<kChunk>(acc, u + (kChunk / 8) * c, v0, p.V, c_thr,
+                                        c_buf + (rrow * kCandSlots + c_slot) * kCandK, c_n);
+                }
+              }
+            }
           }
         }
+        if (ok) {
+          tc::tc_fence_before();
+          __syncwarp();
+          if (lane == 0) tc::mbar_arrive(&b.accempty[buf]);
+        }
       }
-      tc::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) tc::mbar_arrive(&b.accempty[buf]);
+      if constexpr (CAND) {
+        // the tile's appends, then one warp per row inserts them
+        if (c_row) c_cnt[rrow * kCandSlots + c_slot] = c_n;
+        asm volatile("bar.sync 2, %0;" ::"n"(32 * EW) : "memory");
+        for (int rr = e; rr < kCandRows; rr += EW)
+          if (r0 + rr < p.R)
+            cand_insert_row(c_list + rr * kCandK, c_tau + rr, c_buf + rr * kCandSlots * kCandK,
+                            c_cnt + rr * kCandSlots);
+        asm volatile("bar.sync 2, %0;" ::"n"(32 * EW) : "memory");
+        c_n = 0;
+        if (c_row) c_thr = c_tau[rrow];
+      } else {
+        if (!ok) break;
+      }
+    }
+    if constexpr (CAND) {
+      // this CTA's top-16 of every row for position j (the last tile's
+      // insertions are complete: the loop ended on a named barrier)
+      for (int rr = e; rr < kCandRows; rr += EW) {
+        const int r_out = r0 + rr;
+        if (r_out < p.R && r_out < p.cand_R && lane < kCandK && vr < p.n_part)
+          p.cand_parts[(((size_t)j * p.n_part + vr) * p.cand_R + r_out) * kCandK + lane] =
+              c_list[rr * kCandK + lane];
+      }
     }
 
     // ---- merge the column groups (and with dup, the two copies) of each
@@ -1767,6 +1905,11 @@ cudaError_t launch_propose_tc(const Ctx& ctx, const ProposeArgs& a, cudaStream_t
   const bool split = use_split(ctx, a);
   const bool pair = !split && use_pair(a.R);
   const int rows_m = split ? 64 : kTileM;   // requests per M-tile
+  // candidate sets (at most 32 requests, no activation): the repeated-rows
+  // kernel with 64-row U boxes
+  const bool cand = a.cand_tok != nullptr;
+  if (cand && (split || a.R > kCandRows)) return cudaErrorInvalidValue;
+  const int u_rows = cand ? 64 : rows_m;   // rows of a U box
   CUtensorMap tmW, tmU;
   {
     const cuuint64_t dims[2] = {(cuuint64_t)a.rank, (cuuint64_t)a.V};
@@ -1782,7 +1925,7 @@ cudaError_t launch_propose_tc(const Ctx& ctx, const ProposeArgs& a, cudaStream_t
   {
     const cuuint64_t dims[3] = {(cuuint64_t)a.V, (cuuint64_t)a.gamma, (cuuint64_t)a.R};
     const cuuint64_t strides[2] = {(cuuint64_t)a.V * 2, (cuuint64_t)a.V * 2 * a.gamma};
-    const cuuint32_t box[3] = {kHalf, 1, (cuuint32_t)rows_m};
+    const cuuint32_t box[3] = {kHalf, 1, (cuuint32_t)u_rows};
     const cuuint32_t estr[3] = {1, 1, 1};
     if (encode(&tmU, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(a.U), dims, strides,
                box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -1800,6 +1943,9 @@ cudaError_t launch_propose_tc(const Ctx& ctx, const ProposeArgs& a, cudaStream_t
                            cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(propose_tc_kernel<kSingleEpiWarps, true, false>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(propose_tc_kernel<kSingleEpiWarps, true, false, true>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(propose_tc_kernel<kSingleEpiWarps, false, true>,
@@ -1831,6 +1977,8 @@ cudaError_t launch_propose_tc(const Ctx& ctx, const ProposeArgs& a, cudaStream_t
   p.step_sync = ctx.ws.step_sync;
   p.n_vr = split ? tc_vranges_split(ctx, a.R) : tc_vranges(ctx, a.R);
   p.dup = !split && a.R <= kTileM / 2 ? 1 : 0;
+  p.cand_parts = cand ? ctx.ws.cand_parts : nullptr;
+  p.cand_R = ctx.cfg.R_max < kCandMaxR ? ctx.cfg.R_max : kCandMaxR;
   p.A = a.gate_h ? a.gated_rep : nullptr;
   p.act = a.act;
   const int grid = ((a.R + rows_m - 1) / rows_m) * p.n_vr;
@@ -1871,6 +2019,7 @@ cudaError_t launch_propose_tc(const Ctx& ctx, const ProposeArgs& a, cudaStream_t
   bool whole = false;
   if (a.gamma > 1 && (!a.gate_h || split))
     whole = pair    ? grid_resident<propose_tc_pair_kernel<kPairEpiWarps>>(ctx, cfg, true)
+            : cand  ? grid_resident<propose_tc_kernel<kSingleEpiWarps, true, false, true>>(ctx, cfg, false)
             : split ? grid_resident<propose_tc_kernel<kSingleEpiWarps, false, true>>(ctx, cfg, false)
             : p.dup ? grid_resident<propose_tc_kernel<kSingleEpiWarps, true, false>>(ctx, cfg, false)
                     : grid_resident<propose_tc_kernel<kSingleEpiWarps, false, false>>(ctx, cfg, false);
@@ -1895,6 +2044,7 @@ cudaError_t launch_propose_tc(const Ctx& ctx, const ProposeArgs& a, cudaStream_t
     }
     cfg.numAttrs = (unsigned)na;
     e = pair    ? cudaLaunchKernelEx(&cfg, propose_tc_pair_kernel<kPairEpiWarps>, tmW, tmU, p)
+        : cand  ? cudaLaunchKernelEx(&cfg, propose_tc_kernel<kSingleEpiWarps, true, false, true>, tmW, tmU, p)
         : split ? cudaLaunchKernelEx(&cfg, propose_tc_kernel<kSingleEpiWarps, false, true>, tmW, tmU, p)
         : p.dup ? cudaLaunchKernelEx(&cfg, propose_tc_kernel<kSingleEpiWarps, true, false>, tmW, tmU, p)
                 : cudaLaunchKernelEx(&cfg, propose_tc_kernel<kSingleEpiWarps, false, false>, tmW, tmU, p);

@@ -64,9 +64,9 @@ def compare_candidates(k, o, rows_exempt):
     return checked
 
 
-def run(dsd, spec, n_sample=None, seed_idx=0):
+def run(dsd, spec, n_sample=None, seed_idx=0, engine="simt"):
     x = synth.cycle_inputs(spec, device=DEV)
-    ctx = dsd.Context(spec.V, spec.r, spec.G, spec.R, dtype=spec.dtype, engine="simt")
+    ctx = dsd.Context(spec.V, spec.r, spec.G, spec.R, dtype=spec.dtype, engine=engine)
     T = spec.temperature
     out = ctx.propose_candidates(x["U"], x["E"], x["W"], x["conf"], x["prev_tok"],
                                  req_id=x["req_id"], temperature=T, seed=x["seed"])
@@ -119,3 +119,22 @@ def test_candidates_tiny_vocabulary_and_capacity(dsd):
 def test_candidates_full_size_sampled_requests(dsd):
     # the greedy workload: R = 16, V = 151936, rank 256
     run(dsd, synth.CYCLE_SPECS["greedy"], n_sample=4)
+
+
+@pytest.mark.parametrize("R,rank,temperature", [(19, 64, 0.0), (19, 256, 1.0), (32, 128, 0.0),
+                                                (1, 64, 0.6)])
+def test_candidates_on_the_tensor_cores(dsd, R, rank, temperature):
+    # the tensor-core engine's repeated-rows kernel keeps the lists (21 tiles
+    # of 128 with an 8-row tail; one request; the 32-request maximum)
+    spec = synth.scaled(synth.CYCLE_SPECS["greedy"], temperature=temperature, seed=74 + R,
+                        r=rank, V=2568, R=R, ew_std=0.3)
+    k, plain = run(dsd, spec, engine="tcgen05")
+    assert torch.equal(plain["tokens"].cpu(), torch.as_tensor(k["tokens"]))
+    if temperature == 0.0:
+        assert np.array_equal(k["cand_tok"][:, :, 0], k["tokens"])
+
+
+def test_candidates_on_the_tensor_cores_full_size_sampled_requests(dsd):
+    # the greedy workload (R = 16, V = 151936, rank 256) on AUTO, which takes
+    # the tensor-core engine
+    run(dsd, synth.CYCLE_SPECS["greedy"], n_sample=4, engine="auto")
