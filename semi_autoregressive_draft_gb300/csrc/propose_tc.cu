@@ -357,34 +357,58 @@ __device__ __forceinline__ void cand_filter(const uint32_t (&acc)[N], const uint
   }
 }
 
-// One warp: insert the row's appended keys (kCandSlots buffers with counts
-// cnt[]) into its sorted list (lanes 0..15 hold it), then store the list and
-// its threshold.  Every key is distinct (token index in its low bits).
+// One warp: merge the row's appended keys (kCandSlots buffers with counts
+// cnt[]) into its sorted list, 32 keys at a time.  Every key is distinct (the
+// token index is in its low bits) and 0 marks an empty entry, so a key's
+// place in the merged list is the number of keys above it in the list and in
+// the batch: lane l ranks the batch's key l, lanes 0..15 rank the list's
+// entries, and every key with a place below 16 is written there.  Then the
+// threshold (the 16th key, 0 while the list is not full).
 __device__ __forceinline__ void cand_insert_row(unsigned long long* list, unsigned long long* tau,
                                                 const unsigned long long* bufs, int* cnt) {
   const int lane = threadIdx.x & 31;
+  int n[kCandSlots], pre[kCandSlots];
   int total = 0;
-  int n[kCandSlots];
 #pragma unroll
   for (int sl = 0; sl < kCandSlots; ++sl) {
     n[sl] = cnt[sl];
+    pre[sl] = total;
     total += n[sl];
   }
   if (total == 0) return;
-  unsigned long long L = lane < kCandK ? list[lane] : 0ull;
+  for (int b0 = 0; b0 < total; b0 += 32) {
+    const unsigned long long L = lane < kCandK ? list[lane] : 0ull;
+    unsigned long long K = 0ull;
+    const int f = b0 + lane;
+    if (f < total) {
+      // key f of the flattened buffers: slot q with pre[q] <= f, at f - pre[q]
+      int adj = 0;
 #pragma unroll
-  for (int sl = 0; sl < kCandSlots; ++sl)
-    for (int i = 0; i < n[sl]; ++i) {
-      const unsigned long long k = bufs[sl * kCandK + i];
-      const unsigned int above = __ballot_sync(0xffffffffu, L > k) & 0xFFFFu;
-      const int pos = __popc(above);
-      const unsigned long long prev = __shfl_up_sync(0xffffffffu, L, 1);
-      if (pos < kCandK) L = lane < pos ? L : (lane == pos ? k : prev);
+      for (int q = 1; q < kCandSlots; ++q)
+        if (f >= pre[q]) adj = q * kCandK - pre[q];
+      K = bufs[f + adj];
     }
-  if (lane < kCandK) list[lane] = L;
-  const unsigned long long t16 = __shfl_sync(0xffffffffu, L, kCandK - 1);
-  if (lane == 0) *tau = t16;
-  __syncwarp();
+    // the batch's keys sit in lanes 0 .. n_b - 1 (the shuffles bound the
+    // merge, so only those lanes are visited)
+    const int n_b = total - b0 < 32 ? total - b0 : 32;
+    int rk = 0, rl = lane;   // list entries above list entry `lane`: lane
+#pragma unroll
+    for (int i = 0; i < kCandK; ++i) rk += __shfl_sync(0xffffffffu, L, i) > K ? 1 : 0;
+    for (int i = 0; i < n_b; ++i) {
+      const unsigned long long ki = __shfl_sync(0xffffffffu, K, i);
+      rk += ki > K ? 1 : 0;
+      rl += ki > L ? 1 : 0;
+    }
+    const int n_l = __popc(__ballot_sync(0xffffffffu, L != 0ull));
+    const int n_k = n_b;
+    const int n_u = n_l + n_k < kCandK ? n_l + n_k : kCandK;
+    __syncwarp();
+    if (L != 0ull && rl < kCandK) list[rl] = L;
+    if (K != 0ull && rk < kCandK) list[rk] = K;
+    if (lane >= n_u && lane < kCandK) list[lane] = 0ull;
+    __syncwarp();
+  }
+  if (lane == 0) *tau = list[kCandK - 1];
   if (lane < kCandSlots) cnt[lane] = 0;
 }
 
