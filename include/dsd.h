@@ -376,10 +376,12 @@ int dsd_loss_forward(dsd_ctx* ctx, int B, const void* U, const void* E, const vo
  * device, 16-byte aligned; H a positive multiple of 8.  gated_rep
  * [R, gamma, rank] f32 out: g_j * m_j per position (0 at position 0 when the
  * context has bias_at_first = 0); dsd_verify_gated reads it.  One launch for
- * the hidden-state part of every gate, then per draft position a gate launch
- * and a bias launch, then the finalize.  The bias launch runs on the
- * tensor-core engine's split mode (AUTO, TCGEN05; bf16 tables, rank a
- * multiple of 64), on the CUDA cores otherwise (SIMT, f32).  Errors as
+ * the hidden-state part of every gate, then the bias steps, then the
+ * finalize.  On the tensor-core engine's split mode (AUTO, TCGEN05; bf16
+ * tables, rank a multiple of 64) one launch runs every draft position, its
+ * CTAs computing each position's gates before its bias step; on the CUDA
+ * cores (SIMT, f32) each position has a gate launch and a bias launch.
+ * Errors as
  * dsd_propose; a non-finite gate argument sets DSD_ERR_NONFINITE.
  */
 int dsd_propose_gated(dsd_ctx* ctx, int R, const void* U, const void* E, const void* W,
@@ -416,9 +418,11 @@ int dsd_verify_gated(dsd_ctx* ctx, int R, const void* P, const void* U, const vo
  * multiple of 8.  rnn_rep [R, gamma, rank] f32 out: o_j per position (0 at
  * position 0 when the context has bias_at_first = 0; the recursion then
  * starts at position 1); dsd_verify_rnn reads it.  One launch for the
- * hidden-state parts of all three matrices, then per draft position a state
- * launch, an output launch and a bias launch (the tensor-core engine's split
- * mode, or the CUDA cores as for dsd_propose_gated), then the finalize.
+ * hidden-state parts of all three matrices, then on the tensor-core engine
+ * (split mode) one launch for all draft positions, whose CTAs compute each
+ * position's state and output between the bias steps; on the CUDA cores per
+ * draft position a state launch, an output launch and a bias launch; then
+ * the finalize.
  * Errors as
  * dsd_propose; a non-finite gate, candidate or output argument sets
  * DSD_ERR_NONFINITE.
@@ -452,10 +456,12 @@ int dsd_verify_rnn(dsd_ctx* ctx, int R, const void* P, const void* U, const void
  *     largest first, equal logits in token order (-1 past V when V < 16)
  *   cand_logit [R, gamma, 16] f32 out: those biased logits (not divided by
  *     the temperature)
- * Runs on the CUDA-core engine whatever the context's engine; the biased
- * logits stay in registers: each CTA keeps per request a sorted top-16 of
- * its vocabulary tiles in shared memory, and one more launch merges the
- * CTAs' lists.  R <= 32 (DSD_ERR_CAPACITY otherwise); other errors as
+ * Runs on the tensor-core engine where dsd_propose would (AUTO, TCGEN05)
+ * and the context has no activation, on the CUDA-core engine otherwise
+ * (TCGEN05 with an activation is DSD_ERR_UNSUPPORTED); the biased logits
+ * never reach memory: each CTA keeps per request a sorted top-16 of its
+ * vocabulary tiles in shared memory, and one more launch merges the CTAs'
+ * lists.  R <= 32 (DSD_ERR_CAPACITY otherwise); other errors as
  * dsd_propose.
  */
 int dsd_propose_candidates(dsd_ctx* ctx, int R, const void* U, const void* E, const void* W,
