@@ -9,11 +9,12 @@
 // "DSpark 论文精读", 3.1 (prefix survival a = prod c, why the
 // cumulative-product bias is monitored) and 5 (reliability diagram, ECE).
 //
-// confidence_head_kernel: one CTA per request, two warps per position: the
-//   dot products of the row's hidden state (H values, split over the two
-//   warps, four 16-byte loads in flight per lane) and of the Markov row of
-//   the previous token (rank values) with w_c, fp32 sums; then thread 0
-//   forms c = sigmoid(s) and the survival prefix products in fp64.
+// confidence_head_kernel: one CTA per request, wpp = 2 warps per position:
+//   the previous token first, then the 16-byte
+//   loads of the row's hidden state (H values split over the position's
+//   warps) and of the Markov row of the token (rank values, the last warp's
+//   lanes) in flight together, fp32 products with w_c; then thread 0 forms
+//   c = sigmoid(s) and the survival prefix products in fp64.
 // threshold_keep_kernel: one thread per request.
 // calibration_kernel: a grid-stride pass, one thread per request: survival
 //   in fp64, reliability bin floor(a n_bins) taken in fp64 (the oracle's
@@ -40,21 +41,26 @@ __device__ __forceinline__ int chunk_to_f32(uint4 q, float* x) {
   }
 }
 
-// sum over one warp's lanes of a[i] * b[i], i < n (n a multiple of the
-// elements per 16 bytes; both arrays 16-byte aligned)
-// The warp covers 16-byte chunks first, first + nw, first + 2 nw, ... of the
-// 32-chunk groups (nw warps share one dot product).
+__device__ __forceinline__ float sigmoid_f(float z) {
+  if (z >= 0.f) return 1.f / (1.f + expf(-z));
+  const float e = expf(z);
+  return e / (1.f + e);
+}
+
+constexpr int kHeadMaxWarps = 32;   // warps per CTA (1024 threads)
+constexpr int kHeadDepth = 4;       // 16-byte loads of each operand in flight per lane
+
+// Sum over one warp of a[v] b[v] for v in this lane's 16-byte chunks
+// (first * 32 + lane) * epc + k * step, k = 0, 1, ...: the loads of up to
+// kHeadDepth chunks are issued before any product.
 template <typename T>
-__device__ __forceinline__ float warp_dot(const T* a, const T* b, int n, int lane, int first,
-                                          int nw) {
+__device__ __forceinline__ float lane_dot(const T* a, const T* b, int n, int v_first, int step) {
   constexpr int epc = 16 / (int)sizeof(T);
-  constexpr int kDepth = 4;   // 16-byte loads of each operand in flight per lane
-  const int step = nw * 32 * epc;
   float acc = 0.f;
-  for (int v0 = (first * 32 + lane) * epc; v0 < n; v0 += kDepth * step) {
-    uint4 qa[kDepth], qb[kDepth];
+  for (int v0 = v_first; v0 < n; v0 += kHeadDepth * step) {
+    uint4 qa[kHeadDepth], qb[kHeadDepth];
 #pragma unroll
-    for (int d = 0; d < kDepth; ++d) {
+    for (int d = 0; d < kHeadDepth; ++d) {
       const int v = v0 + d * step;
       if (v < n) {
         qa[d] = ld_stream16(a + v);
@@ -62,7 +68,7 @@ __device__ __forceinline__ float warp_dot(const T* a, const T* b, int n, int lan
       }
     }
 #pragma unroll
-    for (int d = 0; d < kDepth; ++d) {
+    for (int d = 0; d < kHeadDepth; ++d) {
       if (v0 + d * step < n) {
         float x[8], y[8];
         const int k = chunk_to_f32<T>(qa[d], x);
@@ -73,43 +79,66 @@ __device__ __forceinline__ float warp_dot(const T* a, const T* b, int n, int lan
       }
     }
   }
-  return warp_sum(acc);
+  return acc;
 }
-
-__device__ __forceinline__ float sigmoid_f(float z) {
-  if (z >= 0.f) return 1.f / (1.f + expf(-z));
-  const float e = expf(z);
-  return e / (1.f + e);
-}
-
-constexpr int kHeadWarps = 2;   // warps per position
 
 template <typename T>
-__global__ void __launch_bounds__(32 * kHeadWarps * kMaxGamma) confidence_head_kernel(
+__global__ void __launch_bounds__(32 * kHeadMaxWarps) confidence_head_kernel(
     const T* __restrict__ h, const T* __restrict__ E, const T* __restrict__ w_c, float b_c,
     const int32_t* __restrict__ prev_tok, const int32_t* __restrict__ tokens, int H, int rank,
-    int V, int gamma, float* conf, float* survival, int* status) {
-  __shared__ float s_part[kMaxGamma][kHeadWarps];
+    int V, int gamma, int wpp, float* conf, float* survival, int* status) {
+  constexpr int epc = 16 / (int)sizeof(T);
+  __shared__ float s_part[kMaxGamma][kHeadMaxWarps / 2];
   const int r = blockIdx.x, w = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int j = w / kHeadWarps, half = w % kHeadWarps;
+  const int j = w / wpp, part = w - j * wpp;
   if (j < gamma) {
-    float v = warp_dot<T>(h + ((size_t)r * gamma + j) * H, w_c, H, lane, half, kHeadWarps);
-    if (half == 0) {
-      int t = j == 0 ? prev_tok[r] : tokens[(size_t)r * gamma + j - 1];
+    // the Markov row's token, loaded before anything that waits on memory
+    const bool markov = part == wpp - 1;
+    int t = 0;
+    if (markov) {
+      t = j == 0 ? prev_tok[r] : tokens[(size_t)r * gamma + j - 1];
       if (t < 0 || t >= V) {
         if (lane == 0) set_status(status, kErrArg);
         t = 0;
       }
-      v += warp_dot<T>(E + (size_t)t * rank, w_c + H, rank, lane, 0, 1);
     }
-    if (lane == 0) s_part[j][half] = v;
+    // the Markov row's loads (rank <= 256: at most two 16-byte chunks per
+    // lane) go out with the hidden state's first loads
+    uint4 qe[2], qw[2];
+#pragma unroll
+    for (int d = 0; d < 2; ++d) {
+      const int c = (lane + 32 * d) * epc;
+      if (markov && c < rank) {
+        qe[d] = __ldg(reinterpret_cast<const uint4*>(E + (size_t)t * rank + c));
+        qw[d] = __ldg(reinterpret_cast<const uint4*>(w_c + H + c));
+      }
+    }
+    const int step = wpp * 32 * epc;
+    float v = lane_dot<T>(h + ((size_t)r * gamma + j) * H, w_c, H, (part * 32 + lane) * epc, step);
+    if (markov) {
+      float acc = 0.f;
+#pragma unroll
+      for (int d = 0; d < 2; ++d) {
+        if ((lane + 32 * d) * epc < rank) {
+          float x[8], y[8];
+          const int k = chunk_to_f32<T>(qe[d], x);
+          chunk_to_f32<T>(qw[d], y);
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+            if (e < k) acc = fmaf(x[e], y[e], acc);
+        }
+      }
+      v += acc;
+    }
+    v = warp_sum(v);
+    if (lane == 0) s_part[j][part] = v;
   }
   __syncthreads();
   if (threadIdx.x == 0) {
     double acc = 1.0;
     for (int i = 0; i < gamma; ++i) {
       float sl = b_c;
-      for (int k = 0; k < kHeadWarps; ++k) sl += s_part[i][k];
+      for (int k = 0; k < wpp; ++k) sl += s_part[i][k];
       float c = sigmoid_f(sl);
       if (!isfinite(c)) {
         set_status(status, kErrNonfinite);
@@ -288,17 +317,20 @@ __global__ void __launch_bounds__(kCalThreads) calibration_kernel(CalParams p) {
 
 cudaError_t launch_confidence_head(const Ctx& ctx, const ConfHeadArgs& a, cudaStream_t s) {
   if (a.R == 0) return cudaSuccess;
-  const dim3 grid(a.R), block(32 * kHeadWarps * a.gamma);
+  // two warps per position: two CTAs of 448 threads share an SM at gamma = 7,
+  // so 256 requests run in one wave (four warps per position took two)
+  const int wpp = 2;
+  const dim3 grid(a.R), block(32 * wpp * a.gamma);
   if (a.dtype == 1)
     confidence_head_kernel<__nv_bfloat16><<<grid, block, 0, s>>>(
         static_cast<const __nv_bfloat16*>(a.h), static_cast<const __nv_bfloat16*>(a.E),
         static_cast<const __nv_bfloat16*>(a.w_c), a.b_c, a.prev_tok, a.tokens, a.H, a.rank, a.V,
-        a.gamma, a.conf, a.survival, ctx.ws.status);
+        a.gamma, wpp, a.conf, a.survival, ctx.ws.status);
   else
     confidence_head_kernel<float><<<grid, block, 0, s>>>(
         static_cast<const float*>(a.h), static_cast<const float*>(a.E),
         static_cast<const float*>(a.w_c), a.b_c, a.prev_tok, a.tokens, a.H, a.rank, a.V, a.gamma,
-        a.conf, a.survival, ctx.ws.status);
+        wpp, a.conf, a.survival, ctx.ws.status);
   count_launch(ctx);
   return cudaGetLastError();
 }
