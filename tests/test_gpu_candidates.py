@@ -138,3 +138,11 @@ def test_candidates_on_the_tensor_cores_full_size_sampled_requests(dsd):
     # the greedy workload (R = 16, V = 151936, rank 256) on AUTO, which takes
     # the tensor-core engine
     run(dsd, synth.CYCLE_SPECS["greedy"], n_sample=4, engine="auto")
+
+
+def test_candidates_on_the_tensor_cores_one_position(dsd):
+    # gamma = 1: one launch for the one step (no per-position counter)
+    spec = synth.scaled(synth.CYCLE_SPECS["greedy"], temperature=0.0, seed=79, r=64, V=2568,
+                        R=7, G=1, ew_std=0.3)
+    k, plain = run(dsd, spec, engine="tcgen05")
+    assert np.array_equal(k["cand_tok"][:, :, 0], k["tokens"])

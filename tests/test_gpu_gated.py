@@ -188,3 +188,14 @@ def test_gated_in_launch_step_matches_the_step_kernels(dsd):
                 assert np.array_equal(kt["gated_rep"][q, j].view(np.uint32),
                                       ks["gated_rep"][q, j].view(np.uint32)), (q, j)
     assert same >= 0.9 * spec.R * spec.G, same
+
+
+@pytest.mark.parametrize("G", [1, 2])
+def test_gated_short_blocks_on_the_tensor_cores(dsd, G):
+    # gamma = 1: one launch per draft step with the standalone gate kernel
+    # before it; gamma = 2: the one-launch proposal with its in-launch gate
+    spec = synth.scaled(synth.CYCLE_SPECS["greedy"], temperature=1.0, seed=77 + G, p_noise=1.0,
+                        r=128, R=19, G=G, V=2568, ew_std=0.3)
+    gx = synth.gate_inputs(spec.R, spec.G, 64, spec.r, spec.ew_std, seed=78, device=DEV)
+    x, k = run_gated(dsd, spec, gx, engine="tcgen05")
+    check_gated(spec, x, gx, k)

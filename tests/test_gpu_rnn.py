@@ -190,3 +190,14 @@ def test_rnn_in_launch_step_matches_the_step_kernels(dsd):
                 assert np.array_equal(kt["rnn_rep"][q, j].view(np.uint32),
                                       ks["rnn_rep"][q, j].view(np.uint32)), (q, j)
     assert same >= 0.9 * spec.R * spec.G, same
+
+
+@pytest.mark.parametrize("G", [1, 2])
+def test_rnn_short_blocks_on_the_tensor_cores(dsd, G):
+    # gamma = 1: the standalone state and output kernels before one step
+    # launch; gamma = 2: both phases inside the one-launch proposal
+    spec = synth.scaled(synth.CYCLE_SPECS["greedy"], temperature=1.0, seed=87 + G, p_noise=1.0,
+                        r=64, R=19, G=G, V=2568, ew_std=0.3)
+    rx = synth.rnn_inputs(spec.R, spec.G, 64, spec.r, spec.ew_std, seed=88, device=DEV)
+    x, k = run_rnn(dsd, spec, rx, engine="tcgen05")
+    check_rnn(spec, x, rx, k)
