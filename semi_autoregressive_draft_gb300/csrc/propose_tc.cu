@@ -932,7 +932,7 @@ __global__ void __launch_bounds__(128 + 32 * EW, 1)
 // CTA's shared memory, A's rows 128..255 and B's last 64 rows from the
 // second's, and write each CTA's 128 accumulator rows into its own TMEM.  So
 // each SM takes in 32 KB of W per tile instead of 64 KB, and every W byte
-// crosses L2 once per pair.  No load is multicast.
+// crosses L2 once per pair.  Each CTA's copies land in its own shared memory only.
 //
 // Barriers (per CTA; the first CTA's copies of aready, accempty and bfull
 // collect both CTAs' arrivals):

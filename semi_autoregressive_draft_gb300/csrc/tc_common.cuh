@@ -80,7 +80,7 @@ __device__ __forceinline__ void drain_bar(uint64_t* bar, uint32_t parity) {
     if (tc::mbar_try_wait(bar, parity)) return;
 }
 
-// Warp-uniform bounded wait: lane 0 polls, the verdict is broadcast, so the
+// Warp-uniform bounded wait: lane 0 polls, the outcome is broadcast, so the
 // warp stays converged for the .sync.aligned tcgen05 instructions after it.
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
                                           int* status, uint32_t limit = kSpinLimit) {

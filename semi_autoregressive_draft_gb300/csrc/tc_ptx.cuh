@@ -139,7 +139,7 @@ __device__ __forceinline__ uint32_t cluster_ctarank() {
   return r;
 }
 
-// ------------------------------------------- CTA pairs (cta_group::2, no multicast)
+// ------------------------------------------- CTA pairs (cta_group::2)
 // Shared-memory address of the same variable in CTA `rank` of the cluster.
 __device__ __forceinline__ uint32_t mapa(uint32_t saddr, uint32_t rank) {
   uint32_t r;
