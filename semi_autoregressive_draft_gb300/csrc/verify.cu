@@ -248,6 +248,9 @@ __device__ __forceinline__ void fold_vec(RowFold& f, uint4 q, int v0, bool bonus
       f.st.m = M;
       f.st.s = s;
     } else {
+      // a bonus row: the Gumbel-max draw as a running (value, index) pair,
+      // the first maximum kept (a later entry must be strictly larger; a
+      // NaN logit never wins)
 #pragma unroll
       for (int e = 0; e < epc; e += 4) {
         const uint32_t v = (uint32_t)(v0 + e);
@@ -257,11 +260,10 @@ __device__ __forceinline__ void fold_vec(RowFold& f, uint4 q, int v0, bool bonus
         const float z1 = x[e + 1] + gumbel_from_word(ph.y);
         const float z2 = x[e + 2] + gumbel_from_word(ph.z);
         const float z3 = x[e + 3] + gumbel_from_word(ph.w);
-        unsigned long long k;
-        k = make_key(z0, v + 0); f.best = k > f.best ? k : f.best;
-        k = make_key(z1, v + 1); f.best = k > f.best ? k : f.best;
-        k = make_key(z2, v + 2); f.best = k > f.best ? k : f.best;
-        k = make_key(z3, v + 3); f.best = k > f.best ? k : f.best;
+        if (z0 > f.bz) { f.bz = z0; f.bv = v + 0; }
+        if (z1 > f.bz) { f.bz = z1; f.bv = v + 1; }
+        if (z2 > f.bz) { f.bz = z2; f.bv = v + 2; }
+        if (z3 > f.bz) { f.bz = z3; f.bv = v + 3; }
       }
     }
   }
@@ -335,9 +337,11 @@ __device__ __forceinline__ int row_request(const int* s_off, int R, int b) {
 // Block reduction of one item's folds; thread 0 writes the item's part.
 template <bool SAMPLED>
 __device__ __forceinline__ void finish_item(const RowsParams& p, RowFold& f, int part, int v_first,
-                                            int v_end, RowsShared& sh) {
+                                            int v_end, bool bonus, RowsShared& sh) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  if (!SAMPLED && v_first < v_end) {
+  // greedy rows and sampled bonus rows: the thread's (value, index) pair
+  // as a packed key (tested rows of the sampled path keep no key)
+  if ((!SAMPLED || bonus) && v_first < v_end) {
     if (f.nan_seen) set_status(p.status, kErrNonfinite);
     // every element was -inf: the first one holds the maximum
     f.best = make_key(f.bz, f.bv == 0xFFFFFFFFu ? (uint32_t)v_first : f.bv);
@@ -462,7 +466,7 @@ __global__ void __launch_bounds__(kRowThreads, 4) verify_rows(RowsParams p) {
         fold_vec<T, SAMPLED>(f, q[u], v0, bonus, (uint32_t)t, rid, p);
       }
     }
-    finish_item<SAMPLED>(p, f, b * kVerifySplits + sp, v_first, v_end, sh);
+    finish_item<SAMPLED>(p, f, b * kVerifySplits + sp, v_first, v_end, bonus, sh);
   }
   decide_all<T>(p, s_off, splits, splits_bonus, sh);
 }
