@@ -257,7 +257,10 @@ int dsd_schedule(dsd_ctx* ctx, int R, const float* survival, const float* sps, i
  * of request r are tokens[r, :k] followed by next_token[r].
  * keep_len must come from dsd_schedule (or any values in 0..gamma; others
  * are clamped to it and set DSD_ERR_ARG in the status word); U, E, W,
- * prev_tok, lse_q, logit_at_tok may be NULL when T == 0.
+ * prev_tok, lse_q, logit_at_tok may be NULL when T == 0.  Non-finite
+ * values: with T == 0 a NaN in a read row sets DSD_ERR_NONFINITE; with
+ * T > 0 a non-finite normaliser of a tested row does, and a NaN logit never
+ * wins a Gumbel-max draw.
  */
 int dsd_verify(dsd_ctx* ctx, int R, const void* P, const void* U, const void* E,
                const void* W, const int32_t* prev_tok, const int32_t* tokens,
